@@ -1,0 +1,122 @@
+"""Seeded synthetic inputs for the gated delta rule workloads.
+
+This module is shared by the tests, the benchmark and the oracle checks.  It
+holds the input *recipe* only -- distributions, shapes and seeds -- and none
+of the method's arithmetic (no decay, no recurrence).
+
+Recipe (one per workload, all drawn with torch's generator on the requested
+device, one generator per tensor seeded from (seed, tensor id)):
+
+* q, k ~ N(0, 1) in fp32, L2-normalised per token and head in fp32, then cast
+  to the compute dtype (bf16 values are what both the kernels and the oracle
+  receive; their norms are ~1, not exactly 1).
+* v ~ N(0, 1), cast to the compute dtype.
+* beta = sigmoid(N(0, 1)) in fp32 -- the write strength in (0, 1).
+* g ~ N(g_mean, 1) in fp32 -- the raw decay logit (g_mean = 2 for the long
+  prefill so that alpha stays close to 1).
+* init_state ~ N(0, init_std) fp32 [B,H,dk,dv] (standard deviation 0.02) where
+  the workload says so, else None (zero state).
+
+Decode draws fresh q, k, v, g, beta every step from a seed derived from
+(seed, step); its starting state is N(0, 0.02).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import torch
+
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "init": 6}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    T: int
+    dk: int
+    dv: int
+    chunk: int
+    dtype: str            # "f32" or "bf16": dtype of q, k, v and out
+    a_min: float
+    g_mean: float = 0.0
+    init_std: float | None = None   # None -> zero initial state
+    final_state: bool = True
+    seed: int = 0
+    steps: int = 0        # decode workloads only: number of single-token steps
+
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads of the gated-delta-rule hot path (prefill shapes are
+# [B, H, T, d]; decode is N sequences x H heads, one token per step).
+CORRECTNESS = Workload("correctness_b1h2t256_d64_f32", 1, 2, 256, 64, 64, 64, "f32", 0.9)
+PREFILL = Workload("prefill_b4h16t4096_d128_bf16", 4, 16, 4096, 128, 128, 64, "bf16", 0.95,
+                   init_std=0.02)
+LONG_PREFILL = Workload("long_prefill_b1h32t65536_d128_bf16", 1, 32, 65536, 128, 128, 64,
+                        "bf16", 0.98, g_mean=2.0)
+MILLION_PREFILL = Workload("million_prefill_b1h16t1048576_d128_bf16", 1, 16, 1048576, 128,
+                           128, 64, "bf16", 0.99)
+DECODE = Workload("decode_n256h32_d128_bf16_64steps", 256, 32, 1, 128, 128, 64, "bf16", 0.95,
+                  init_std=0.02, steps=64)
+
+WORKLOADS = {w.name: w for w in (CORRECTNESS, PREFILL, LONG_PREFILL, MILLION_PREFILL, DECODE)}
+
+
+def _gen(device, seed: int, tensor: str, extra: int = 0) -> torch.Generator:
+    gen = torch.Generator(device=device)
+    gen.manual_seed((seed * 1_000_003 + _TENSOR_IDS[tensor] * 7919 + extra * 104729)
+                    & 0x7FFF_FFFF_FFFF_FFFF)
+    return gen
+
+
+def _unit_rows(shape, device, gen, dtype):
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    x = x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    return x.to(dtype)
+
+
+def prefill_inputs(w: Workload, device="cpu"):
+    """Returns dict(q, k, v, g, beta, init_state) for a prefill workload."""
+    dt = w.torch_dtype()
+    B, H, T = w.B, w.H, w.T
+    q = _unit_rows((B, H, T, w.dk), device, _gen(device, w.seed, "q"), dt)
+    k = _unit_rows((B, H, T, w.dk), device, _gen(device, w.seed, "k"), dt)
+    v = torch.randn((B, H, T, w.dv), generator=_gen(device, w.seed, "v"), device=device,
+                    dtype=torch.float32).to(dt)
+    g = torch.randn((B, H, T), generator=_gen(device, w.seed, "g"), device=device,
+                    dtype=torch.float32) + w.g_mean
+    beta = torch.sigmoid(torch.randn((B, H, T), generator=_gen(device, w.seed, "beta"),
+                                     device=device, dtype=torch.float32))
+    init = None
+    if w.init_std is not None:
+        init = torch.randn((B, H, w.dk, w.dv), generator=_gen(device, w.seed, "init"),
+                           device=device, dtype=torch.float32) * w.init_std
+    return dict(q=q, k=k, v=v, g=g, beta=beta, init_state=init)
+
+
+def decode_state(w: Workload, device="cpu"):
+    """Starting fp32 state [N,H,dk,dv] of a decode workload."""
+    std = 0.02 if w.init_std is None else w.init_std
+    return torch.randn((w.B, w.H, w.dk, w.dv), generator=_gen(device, w.seed, "init"),
+                       device=device, dtype=torch.float32) * std
+
+
+def decode_step_inputs(w: Workload, step: int, device="cpu"):
+    """Fresh q, k, v [N,H,d], g, beta [N,H] for decode step ``step``."""
+    dt = w.torch_dtype()
+    N, H = w.B, w.H
+    q = _unit_rows((N, H, w.dk), device, _gen(device, w.seed, "q", step + 1), dt)
+    k = _unit_rows((N, H, w.dk), device, _gen(device, w.seed, "k", step + 1), dt)
+    v = torch.randn((N, H, w.dv), generator=_gen(device, w.seed, "v", step + 1),
+                    device=device, dtype=torch.float32).to(dt)
+    g = torch.randn((N, H), generator=_gen(device, w.seed, "g", step + 1), device=device,
+                    dtype=torch.float32) + w.g_mean
+    beta = torch.sigmoid(torch.randn((N, H), generator=_gen(device, w.seed, "beta", step + 1),
+                                     device=device, dtype=torch.float32))
+    return dict(q=q, k=k, v=v, g=g, beta=beta)

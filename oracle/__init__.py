@@ -1,0 +1,172 @@
+"""fp64 CPU oracle for the gated delta rule with a lower-bounded decay.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  It never imports the CUDA library package and shares no code with
+it; the two meet only in the seeded input generator, which holds none of the
+method's arithmetic.
+
+Contents
+--------
+* ``fwd``      -- the token-by-token recurrence (C, fp64, ``gdr_oracle.c``):
+                  alpha_t = a_min + (1 - a_min) sigmoid(g_t),
+                  S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+                  o_t = S_t q_t.
+* ``decode``   -- one step of the same recurrence, in place on the state.
+* ``alpha``    -- the lower-bounded decay itself.
+* ``chunkwise`` (module) -- the chunked reformulation in numpy fp64, used to
+                  check the token loop and to export per-stage intermediates.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` (see the module
+docstrings there for which mathematical fact pins which part).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdr_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libgdr_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gdr_oracle.c`` with the host C compiler (fp64, no fast-math)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            f32p = ctypes.POINTER(ctypes.c_float)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            lib.gdr_oracle_alpha.restype = ctypes.c_double
+            lib.gdr_oracle_alpha.argtypes = [ctypes.c_double, ctypes.c_double]
+            lib.gdr_oracle_fwd.restype = ctypes.c_int
+            lib.gdr_oracle_fwd.argtypes = [f32p, f32p, f32p, f32p, f32p, ctypes.c_double,
+                                           f32p, f64p, f64p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int]
+            lib.gdr_oracle_decode.restype = ctypes.c_int
+            lib.gdr_oracle_decode.argtypes = [f32p, f32p, f32p, f32p, f32p, ctypes.c_double,
+                                              f64p, f64p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _f32(x) -> np.ndarray:
+    """Widen to a contiguous float32 numpy array.
+
+    Accepts numpy arrays or CPU torch tensors of bf16/fp32 (bf16 -> fp32 is
+    exact).  Values are never rounded: fp64 input is refused.
+    """
+    if hasattr(x, "detach"):          # a torch tensor
+        import torch
+        t = x.detach()
+        if t.dtype not in (torch.float32, torch.bfloat16, torch.float16):
+            raise TypeError(f"oracle input dtype {t.dtype} is not a 16/32-bit float")
+        x = t.to("cpu", torch.float32).contiguous().numpy()
+    a = np.asarray(x)
+    if a.dtype == np.float64:
+        raise TypeError("oracle inputs are the kernel's fp32/bf16 values; got float64")
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def alpha(g, a_min: float):
+    """alpha = a_min + (1 - a_min) * sigmoid(g), elementwise, fp64."""
+    lib = _load()
+    g = np.asarray(g, dtype=np.float64)
+    return np.vectorize(lambda x: lib.gdr_oracle_alpha(float(x), float(a_min)),
+                        otypes=[np.float64])(g)
+
+
+def fwd(q, k, v, g, beta, a_min: float, init_state=None, *, want_out: bool = True,
+        want_final: bool = True, nthreads: int | None = None):
+    """Token-by-token forward.  Shapes: q,k [B,H,T,dk], v [B,H,T,dv], g,beta [B,H,T],
+    init_state [B,H,dk,dv] or None (zeros).  Returns (out [B,H,T,dv] fp64 or None,
+    final_state [B,H,dk,dv] fp64 or None).
+    """
+    q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != (B, H, T, dk) or v.shape != (B, H, T, dv):
+        raise ValueError("q/k/v shape mismatch")
+    if g.shape != (B, H, T) or beta.shape != (B, H, T):
+        raise ValueError("g/beta shape mismatch")
+    init = None if init_state is None else _f32(init_state)
+    if init is not None and init.shape != (B, H, dk, dv):
+        raise ValueError("init_state shape mismatch")
+    out = np.empty((B, H, T, dv), np.float64) if want_out else None
+    fin = np.empty((B, H, dk, dv), np.float64) if want_final else None
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    lib = _load()
+    f32, f64 = ctypes.c_float, ctypes.c_double
+    rc = lib.gdr_oracle_fwd(_ptr(q, f32), _ptr(k, f32), _ptr(v, f32), _ptr(g, f32),
+                            _ptr(beta, f32), float(a_min),
+                            None if init is None else _ptr(init, f32),
+                            None if out is None else _ptr(out, f64),
+                            None if fin is None else _ptr(fin, f64),
+                            B, H, T, dk, dv, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"gdr_oracle_fwd failed with code {rc}")
+    return out, fin
+
+
+def decode(q, k, v, g, beta, a_min: float, state: np.ndarray):
+    """One decode step in place on ``state`` ([N,H,dk,dv] float64).  q,k [N,H,dk],
+    v [N,H,dv], g,beta [N,H].  Returns out [N,H,dv] fp64."""
+    q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if state.dtype != np.float64 or not state.flags["C_CONTIGUOUS"] \
+            or state.shape != (N, H, dk, dv):
+        raise ValueError("state must be a contiguous float64 [N,H,dk,dv] array")
+    out = np.empty((N, H, dv), np.float64)
+    lib = _load()
+    f32, f64 = ctypes.c_float, ctypes.c_double
+    rc = lib.gdr_oracle_decode(_ptr(q, f32), _ptr(k, f32), _ptr(v, f32), _ptr(g, f32),
+                               _ptr(beta, f32), float(a_min), _ptr(state, f64),
+                               _ptr(out, f64), N, H, dk, dv)
+    if rc != 0:
+        raise RuntimeError(f"gdr_oracle_decode failed with code {rc}")
+    return out
+
+
+def rel_l2(x, ref) -> float:
+    """||x - ref||_2 / ||ref||_2 over the whole tensor, in fp64."""
+    x = np.asarray(_f64(x), np.float64)
+    ref = np.asarray(_f64(ref), np.float64)
+    den = np.linalg.norm(ref.ravel())
+    num = np.linalg.norm((x - ref).ravel())
+    if den == 0.0:
+        return float(num)
+    return float(num / den)
+
+
+def _f64(x):
+    if hasattr(x, "detach"):
+        import torch
+        return x.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x, np.float64)

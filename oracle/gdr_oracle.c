@@ -1,0 +1,229 @@
+/*
+ * gdr_oracle.c -- the fp64 CPU oracle for the gated delta rule with a
+ * lower-bounded decay.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library.  It shares no
+ * code, header, table or helper with the CUDA library, and never calls it.
+ *
+ * What it computes (per head, one token at a time, all arithmetic in fp64):
+ *
+ *   alpha_t = a_min + (1 - a_min) * sigmoid(g_t)
+ *   S_t     = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   o_t     = S_t q_t
+ *
+ * S is the dv x dk associative-memory state.  The pages describe the
+ * incremental ("delta") rule only in words: a write that corrects what the
+ * state already returns for k_t, combined with a position-dependent decay
+ * gate ("How to Think About Trillion-Parameter Sparse Multimodal LLMs",
+ * section 2.2, Incremental Linear Attention).  The equations above are the
+ * plain reading of that rule with a scalar decay per token and head; the
+ * lower-bounded decay is the scaled-sigmoid bound of "Trillion-Parameter MoE
+ * Multimodal LLMs: How to Evaluate the New Generation", section 3.1, taken in
+ * the linear domain with floor a_min.
+ *
+ * Memory layouts are those of the library's public boundary: q, k [B,H,T,dk],
+ * v [B,H,T,dv], g and beta [B,H,T], state [B,H,dk,dv] holding M = S^T
+ * (M[i][j] = S[j][i]).  Inputs arrive as float32 arrays; bf16 inputs are
+ * widened exactly by the caller, so the oracle sees the very values a GPU
+ * kernel would see.  Nothing here is blocked, fused or reordered: the loop
+ * below is the recurrence as written.
+ *
+ * Parity status: every function here is pinned by the CPU tests (explicit
+ * unrolled matrix products, the orthonormal-key write/read invariant, closed
+ * forms for beta = 0 and a_min = 1, a hand-worked T = 1 case, and agreement
+ * with an independent chunkwise reformulation).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* alpha = a_min + (1 - a_min) * sigmoid(g), sigmoid(g) = 1 / (1 + e^{-g}). */
+double gdr_oracle_alpha(double g, double a_min)
+{
+    return a_min + (1.0 - a_min) / (1.0 + exp(-g));
+}
+
+/*
+ * One head.  q, k: [T][dk]; v: [T][dv]; g, beta: [T]; init: [dk][dv] (M
+ * layout) or NULL for a zero state; out: [T][dv] or NULL; final_state:
+ * [dk][dv] (M layout) or NULL.  S is held as S[j][i], j < dv, i < dk.
+ */
+static void oracle_head(const float *q, const float *k, const float *v,
+                        const float *g, const float *beta, double a_min,
+                        const float *init, double *out, double *final_state,
+                        int64_t T, int dk, int dv, double *S, double *u)
+{
+    for (int j = 0; j < dv; ++j)
+        for (int i = 0; i < dk; ++i)
+            S[(int64_t)j * dk + i] = init ? (double)init[(int64_t)i * dv + j] : 0.0;
+
+    for (int64_t t = 0; t < T; ++t) {
+        const float *kt = k + t * dk;
+        const float *qt = q + t * dk;
+        const float *vt = v + t * dv;
+        const double a = gdr_oracle_alpha((double)g[t], a_min);
+        const double b = (double)beta[t];
+
+        /* u = S k_t */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i)
+                acc += S[(int64_t)j * dk + i] * (double)kt[i];
+            u[j] = acc;
+        }
+        /* S <- a * (S - b * u k_t^T) + b * v_t k_t^T
+         *    = a * S (I - b k_t k_t^T) + b v_t k_t^T                  */
+        for (int j = 0; j < dv; ++j) {
+            const double uj = u[j];
+            const double vj = (double)vt[j];
+            for (int i = 0; i < dk; ++i) {
+                const double ki = (double)kt[i];
+                double *s = &S[(int64_t)j * dk + i];
+                *s = a * (*s - b * uj * ki) + b * vj * ki;
+            }
+        }
+        /* o_t = S q_t */
+        if (out) {
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i)
+                    acc += S[(int64_t)j * dk + i] * (double)qt[i];
+                out[t * dv + j] = acc;
+            }
+        }
+    }
+
+    if (final_state)
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j)
+                final_state[(int64_t)i * dv + j] = S[(int64_t)j * dk + i];
+}
+
+typedef struct {
+    const float *q, *k, *v, *g, *beta, *init;
+    double a_min;
+    double *out, *final_state;
+    int B, H, dk, dv;
+    int64_t T;
+    int64_t next;            /* next (b, h) work item, taken atomically */
+} job_t;
+
+static void *worker(void *arg)
+{
+    job_t *jb = (job_t *)arg;
+    const int64_t nbh = (int64_t)jb->B * jb->H;
+    double *S = (double *)malloc(sizeof(double) * (size_t)jb->dk * (size_t)jb->dv);
+    double *u = (double *)malloc(sizeof(double) * (size_t)jb->dv);
+    if (!S || !u) {
+        free(S);
+        free(u);
+        return (void *)1;
+    }
+    for (;;) {
+        const int64_t bh = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (bh >= nbh)
+            break;
+        const int64_t T = jb->T;
+        oracle_head(jb->q + bh * T * jb->dk, jb->k + bh * T * jb->dk,
+                    jb->v + bh * T * jb->dv, jb->g + bh * T, jb->beta + bh * T,
+                    jb->a_min,
+                    jb->init ? jb->init + bh * jb->dk * jb->dv : NULL,
+                    jb->out ? jb->out + bh * T * jb->dv : NULL,
+                    jb->final_state ? jb->final_state + bh * jb->dk * jb->dv : NULL,
+                    T, jb->dk, jb->dv, S, u);
+    }
+    free(S);
+    free(u);
+    return NULL;
+}
+
+/*
+ * Full forward over [B,H,T]: the token loop above for every (b, h), spread
+ * over nthreads host threads (one whole head per thread at a time, so the
+ * arithmetic of each head is the same whatever the thread count).
+ * Returns 0 on success, -1 on bad arguments, -2 if memory ran out.
+ */
+int gdr_oracle_fwd(const float *q, const float *k, const float *v,
+                   const float *g, const float *beta, double a_min,
+                   const float *init_state, double *out, double *final_state,
+                   int B, int H, int64_t T, int dk, int dv, int nthreads)
+{
+    if (!q || !k || !v || !g || !beta || B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    if (nthreads < 1)
+        nthreads = 1;
+    job_t jb = {q, k, v, g, beta, init_state, a_min, out, final_state,
+                B, H, dk, dv, T, 0};
+    const int64_t nbh = (int64_t)B * H;
+    if (nthreads > nbh)
+        nthreads = nbh > 0 ? (int)nbh : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th)
+        return -2;
+    int rc = 0;
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, worker, &jb) != 0)
+            break;
+        started = i;
+    }
+    if (worker(&jb) != NULL)
+        rc = -2;
+    for (int i = 1; i <= started; ++i) {
+        void *r = NULL;
+        pthread_join(th[i], &r);
+        if (r != NULL)
+            rc = -2;
+    }
+    free(th);
+    return rc;
+}
+
+/*
+ * One decode step for N independent sequences: the same recurrence with
+ * T = 1, applied in place to state [N,H,dk,dv] (fp64, M layout).
+ * q, k [N,H,dk]; v [N,H,dv]; g, beta [N,H]; out [N,H,dv].
+ */
+int gdr_oracle_decode(const float *q, const float *k, const float *v,
+                      const float *g, const float *beta, double a_min,
+                      double *state, double *out, int N, int H, int dk, int dv)
+{
+    if (!q || !k || !v || !g || !beta || !state || !out || N < 0 || H < 0 ||
+        dk <= 0 || dv <= 0)
+        return -1;
+    double *S = (double *)malloc(sizeof(double) * (size_t)dk * (size_t)dv);
+    if (!S)
+        return -2;
+    for (int64_t nh = 0; nh < (int64_t)N * H; ++nh) {
+        const float *kt = k + nh * dk, *qt = q + nh * dk, *vt = v + nh * dv;
+        double *M = state + nh * dk * dv;
+        const double a = gdr_oracle_alpha((double)g[nh], a_min);
+        const double b = (double)beta[nh];
+        for (int j = 0; j < dv; ++j)
+            for (int i = 0; i < dk; ++i)
+                S[(int64_t)j * dk + i] = M[(int64_t)i * dv + j];
+        for (int j = 0; j < dv; ++j) {
+            double uj = 0.0;
+            for (int i = 0; i < dk; ++i)
+                uj += S[(int64_t)j * dk + i] * (double)kt[i];
+            const double vj = (double)vt[j];
+            for (int i = 0; i < dk; ++i) {
+                const double ki = (double)kt[i];
+                double *s = &S[(int64_t)j * dk + i];
+                *s = a * (*s - b * uj * ki) + b * vj * ki;
+            }
+            double oj = 0.0;
+            for (int i = 0; i < dk; ++i)
+                oj += S[(int64_t)j * dk + i] * (double)qt[i];
+            out[nh * dv + j] = oj;
+        }
+        for (int j = 0; j < dv; ++j)
+            for (int i = 0; i < dk; ++i)
+                M[(int64_t)i * dv + j] = S[(int64_t)j * dk + i];
+    }
+    free(S);
+    return 0;
+}
