@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta rule hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload prefill|long|million|decode] [--no-cpu-baseline]
+
+One JSON line on rank 0.  A "step" of the default workload is one chunked
+prefill over B=4, H=16, T=4096, d=128, bf16 (cumulative decay, WY/UT
+transform, state pass and output); ``value`` is prefill tokens/s (B*T per
+step).  The same line carries a ``decode`` object for the single-token decode
+workload (N=256 sequences x H=32 heads, one token per step), because the
+metric asks for both.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on
+the launching stream with an L2 flush (a 256 MB write) between steps, outside
+the events.  Ranks are independent replicas (weak scaling): a barrier and a
+device synchronise bracket the timed region, and the slowest rank's time
+counts.  ``e2e`` repeats the measurement with the inputs in pinned host memory
+copied in, and the result copied out, inside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+project has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_gdr_gb300 import inputs as I  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def prefill_algorithmic(w: I.Workload):
+    """Algorithmic bytes and chunked FLOPs of one prefill call.
+
+    Bytes: q, k, v and out once each, g and beta once, the fp32 state read once
+    (if given) and written once.  FLOPs: per token-head, 6 dk dv for the three
+    state products plus 2 C (3 dk + 2 dv) for the five C x C tile products,
+    counted as full dense tiles as the chunked method computes them."""
+    es = 2 if w.dtype == "bf16" else 4
+    n_th = w.B * w.H * w.T
+    by = n_th * ((2 * w.dk + 2 * w.dv) * es + 8)
+    by += w.B * w.H * w.dk * w.dv * 4 * ((1 if w.init_std is not None else 0) + 1)
+    fl = n_th * (6 * w.dk * w.dv + 2 * w.chunk * (3 * w.dk + 2 * w.dv))
+    return by, fl
+
+
+def decode_algorithmic(w: I.Workload):
+    """Bytes of one decode step: state read + written (fp32), q, k, v, out, g, beta."""
+    es = 2 if w.dtype == "bf16" else 4
+    per = 2 * w.dk * w.dv * 4 + (2 * w.dk + 2 * w.dv) * es + 8
+    return w.B * w.H * per
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def committed_traffic(kernel: str, source_files):
+    """ncu DRAM bytes per launch committed under profiles/, valid only while the
+    kernel's source is unchanged (sha256 of its files)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    for fn in source_files:
+        with open(os.path.join(ROOT, fn), "rb") as f:
+            h.update(f.read())
+    if ent.get("source_sha256") != h.hexdigest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- our arm
+def time_steps(fn, K, W, flush, stream):
+    """Run W warm-ups then K timed steps; per-step CUDA-event times in ms."""
+    for _ in range(W):
+        fn(-1)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn(i)
+        e.record(stream)
+        times.append((s, e))
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in times]
+
+
+def bench_prefill(gdr, w, K, W, dev, flush, stream):
+    x = I.prefill_inputs(w, device=dev)
+    out = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype(), device=dev)
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+
+    def step(_):
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                      chunk=w.chunk, out=out, final_state=fin)
+
+    ms = time_steps(step, K, W, flush, stream)
+
+    # end to end: pinned host inputs in, output and final state out, every step
+    host = {n: (None if t is None else t.cpu().pin_memory()) for n, t in x.items()}
+    dx = {n: (None if t is None else torch.empty_like(t)) for n, t in x.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hfin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+
+    def e2e_step(_):
+        for n, t in host.items():
+            if t is not None:
+                dx[n].copy_(t, non_blocking=True)
+        gdr.chunk_fwd(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], w.a_min,
+                      dx["init_state"], chunk=w.chunk, out=out, final_state=fin)
+        hout.copy_(out, non_blocking=True)
+        hfin.copy_(fin, non_blocking=True)
+
+    ms_e2e = time_steps(e2e_step, max(3, K // 2), 2, flush, stream)
+    return ms, ms_e2e, h2d, d2h
+
+
+def bench_decode(gdr, w, K, W, dev, flush, stream):
+    state = I.decode_state(w, device=dev)
+    nsteps = max(K, 1)
+    xs = [I.decode_step_inputs(w, s % w.steps, device=dev) for s in range(min(nsteps, w.steps))]
+    out = torch.empty((w.B, w.H, w.dv), dtype=w.torch_dtype(), device=dev)
+
+    def step(i):
+        x = xs[i % len(xs)]
+        gdr.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, state, out=out)
+
+    # the state (537 MB) is larger than L2: no flush needed between decode steps
+    ms = time_steps(step, K, W, None, stream)
+
+    hx = [{n: t.cpu().pin_memory() for n, t in x.items()} for x in xs[:4]]
+    dx = {n: torch.empty_like(t) for n, t in xs[0].items()}
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in hx[0].values())
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step(i):
+        for n, t in hx[i % len(hx)].items():
+            dx[n].copy_(t, non_blocking=True)
+        gdr.decode_step(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], w.a_min, state, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    ms_e2e = time_steps(e2e_step, K, 2, None, stream)
+    return ms, ms_e2e, h2d, d2h
+
+
+def cpu_baseline_prefill(w, budget_s=12.0):
+    """fp64 oracle on a bounded sample of the prefill workload: all heads of
+    sequence 0 over the first T_s tokens, T_s grown until ~budget_s of work."""
+    import oracle
+    x = I.prefill_inputs(w.with_(B=1), device="cpu")
+    cores = os.cpu_count() or 1
+    Ts = 128
+    while True:
+        sub = {n: x[n][:, :, :Ts] for n in ("q", "k", "v", "g", "beta")}
+        init = x["init_state"]
+        t0 = time.perf_counter()
+        oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], w.a_min, init,
+                   nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or Ts >= w.T:
+            break
+        Ts = min(w.T, Ts * 4)
+    head_tok_s = w.H * Ts / dt
+    return {"value": head_tok_s / w.H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"B=1 of {w.B}, all {w.H} heads, first {Ts} of {w.T} tokens "
+                      f"({w.H * Ts} head-tokens in {dt:.2f} s); value = head-tokens/s / H",
+            "head_tokens_per_s": head_tok_s}
+
+
+def cpu_baseline_decode(w, budget_s=8.0):
+    import numpy as np
+    import oracle
+    cores = os.cpu_count() or 1
+    state = I.decode_state(w, device="cpu").double().numpy().copy()
+    steps, t_tot = 0, 0.0
+    while t_tot < budget_s and steps < w.steps:
+        x = I.decode_step_inputs(w, steps, device="cpu")
+        t0 = time.perf_counter()
+        oracle.decode(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, state, nthreads=cores)
+        t_tot += time.perf_counter() - t0
+        steps += 1
+    return {"value": w.B * steps / t_tot, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} of {w.steps} decode steps over all {w.B}x{w.H} (n,h)",
+            "ms_per_step": 1e3 * t_tot / steps}
+
+
+def run_ours(args):
+    import gated_delta_rule_gdr_gb300 as gdr
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gdr.load(build_if_missing=True)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    pk, pk_kind = peaks()
+
+    main_w = {"prefill": I.PREFILL, "long": I.LONG_PREFILL, "million": I.MILLION_PREFILL,
+              "decode": I.DECODE}[args.workload]
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    result = {}
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        t_wall0 = time.perf_counter()
+        if main_w.steps == 0:
+            ms, ms_e2e, h2d, d2h = bench_prefill(gdr, main_w, args.steps, args.warmup, dev, flush,
+                                                 stream)
+        else:
+            ms, ms_e2e, h2d, d2h = bench_decode(gdr, main_w, args.steps, args.warmup, dev, flush,
+                                                stream)
+        barrier()
+        wall = time.perf_counter() - t_wall0
+        dec = None
+        if main_w.steps == 0 and not args.no_decode:
+            dec = bench_decode(gdr, I.DECODE, args.decode_steps, args.warmup, dev, flush, stream)
+            barrier()
+    assert gdr.last_device_error(dev) == 0, "device error word set"
+
+    ms_step = max_over_ranks(statistics.mean(ms))
+    ms_e2e_step = max_over_ranks(statistics.mean(ms_e2e))
+    if main_w.steps == 0:
+        tokens = main_w.B * main_w.T
+        by, fl = prefill_algorithmic(main_w)
+        nk = gdr.chunk_fwd_kernels(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
+                                   main_w.chunk, main_w.a_min, main_w.torch_dtype())
+        kname = "gdr_fused_prefill" if nk == 1 else "gdr_chunk_fwd staged (4 kernels)"
+        srcs = ["gated_delta_rule_gdr_gb300/csrc/gdr_fused.cu"] if nk == 1 else \
+            ["gated_delta_rule_gdr_gb300/csrc/gdr_staged.cu"]
+        metric = "prefill tokens/s"
+    else:
+        tokens = main_w.B
+        by, fl = decode_algorithmic(main_w), 0
+        nk = 1
+        kname = "decode128_kernel"
+        srcs = ["gated_delta_rule_gdr_gb300/csrc/gdr_decode.cu"]
+        metric = "decode tokens/s"
+    value = world * tokens / (ms_step * 1e-3)
+    achieved_gbs = by / (statistics.mean(ms) * 1e-3) / 1e9
+    achieved_tf = fl / (statistics.mean(ms) * 1e-3) / 1e12
+    t_roof = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+    bound = "hbm" if by / (pk["hbm_gbs"] * 1e9) >= fl / (pk["bf16_tflops"] * 1e12) else "tensor"
+    roof = {
+        "bound": bound, "kernel": kname,
+        "achieved": round(achieved_gbs if bound == "hbm" else achieved_tf, 2),
+        "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
+        "peak_kind": pk_kind,
+        "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+        "frac": None, "traffic": committed_traffic(kname, srcs),
+        "algorithmic_bytes": by, "algorithmic_flops": fl,
+        "frac_of_roofline_time": round(t_roof / (statistics.mean(ms) * 1e-3), 4),
+        "achieved_tflops": round(achieved_tf, 2),
+        "nominal_hbm_frac": round(achieved_gbs / 7900.0, 4),
+    }
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    line = {
+        "metric": metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": main_w.dtype, "data": "synthetic (seeded; recipe in gated_delta_rule_gdr_gb300/inputs.py)",
+        "config": {"workload": main_w.name, "B": main_w.B, "H": main_w.H, "T": main_w.T,
+                   "dk": main_w.dk, "dv": main_w.dv, "chunk": main_w.chunk,
+                   "a_min": main_w.a_min, "parallelism": f"replicas x{world}",
+                   "l2": "256 MB L2 flush between timed steps" if main_w.steps == 0
+                   else "state (537 MB) larger than L2, no flush"},
+        "roofline": roof,
+        "e2e": {"value": round(world * tokens / (ms_e2e_step * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e_step, 4)},
+        "gpu_launches": nk * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(wall, 3),
+        "ms_per_step_all": [round(t, 4) for t in ms],
+    }
+    if dec is not None:
+        dms, dms_e2e, dh2d, dd2h = dec
+        w4 = I.DECODE
+        dby = decode_algorithmic(w4)
+        dmean = statistics.mean(dms)
+        dgbs = dby / (dmean * 1e-3) / 1e9
+        line["decode"] = {
+            "metric": "decode tokens/s", "workload": w4.name,
+            "value": round(world * w4.B / (max_over_ranks(dmean) * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(dmean, 4), "steps": args.decode_steps,
+            "roofline": {"bound": "hbm", "kernel": "decode128_kernel", "achieved": round(dgbs, 1),
+                         "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
+                         "frac": round(dgbs / pk["hbm_gbs"], 4),
+                         "traffic": committed_traffic(
+                             "decode128_kernel", ["gated_delta_rule_gdr_gb300/csrc/gdr_decode.cu"]),
+                         "algorithmic_bytes": dby, "nominal_hbm_frac": round(dgbs / 7900.0, 4)},
+            "e2e": {"value": round(world * w4.B / (max_over_ranks(statistics.mean(dms_e2e)) * 1e-3), 1),
+                    "unit": "tokens/s", "h2d_bytes_per_step": dh2d, "d2h_bytes_per_step": dd2h},
+            "gpu_launches": args.decode_steps,
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = (cpu_baseline_prefill(main_w) if main_w.steps == 0
+                                else cpu_baseline_decode(main_w))
+        if dec is not None:
+            line["decode"]["cpu_baseline"] = cpu_baseline_decode(I.DECODE)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 CPU oracle, as it stands, on bounded samples of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    w = {"prefill": I.PREFILL, "long": I.LONG_PREFILL, "million": I.MILLION_PREFILL,
+         "decode": I.DECODE}[args.workload]
+    cores = os.cpu_count() or 1
+    times = []
+    if w.steps == 0:
+        x = I.prefill_inputs(w.with_(B=1), device="cpu")
+        Ts = min(w.T, 512)
+        sub = {n: x[n][:, :, :Ts] for n in ("q", "k", "v", "g", "beta")}
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], w.a_min,
+                       x["init_state"], nthreads=cores)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        tok = Ts                     # B*T-tokens of the workload processed per step
+        sample = f"per step: B=1, all {w.H} heads, first {Ts} of {w.T} tokens"
+        metric = "prefill tokens/s"
+    else:
+        state = I.decode_state(w, device="cpu").double().numpy().copy()
+        for i in range(args.warmup + args.steps):
+            x = I.decode_step_inputs(w, i % w.steps, device="cpu")
+            t0 = time.perf_counter()
+            oracle.decode(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, state,
+                          nthreads=cores)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        tok = w.B
+        sample = f"per step: one decode step over all {w.B}x{w.H} (n,h)"
+        metric = "decode tokens/s"
+    mean = statistics.mean(times)
+    value = tok / mean
+    line = {"impl": "reference", "metric": metric, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "a_min": w.a_min},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["prefill", "long", "million", "decode"],
+                    default="prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+"""GB300 gated delta rule: thin Python binding over libgdr.so (include/gdr.h).
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+kernels behind the C ABI.  Tensors are torch CUDA tensors, contiguous, in the
+layouts of the header; the current torch stream is passed as the stream.  If
+the library is missing or fails to load, every call raises: there is no CPU
+or PyTorch fallback.
+
+    out, final = chunk_fwd(q, k, v, g, beta, a_min, init_state=None, chunk=64)
+    out        = decode_step(q, k, v, g, beta, a_min, state)   # state in place
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk_wy",
+           "chunk_state", "chunk_output", "chunk_fwd_kernels", "last_device_error", "status_string", "version",
+           "library_path", "STATUS"]
+
+STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
+          4: "GDR_ERR_CUDA", 5: "GDR_ERR_TIMEOUT"}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+
+_lib = None
+
+
+class GdrError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        msg = status_string(code) if _lib is not None else self.name
+        super().__init__(f"{where}: {self.name} ({msg})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libgdr.so (optionally building it first).  Raises if unavailable."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"libgdr.so not built ({path}); run __graft_entry__.build() or "
+                               "python -m gated_delta_rule_gdr_gb300.build")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sig = {
+        "gdr_chunk_fwd": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp],
+        "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
+        "gdr_chunk_decay": [vp, f, vp, i, i, i, vp],
+        "gdr_chunk_wy": [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
+        "gdr_chunk_state": [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
+        "gdr_chunk_output": [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
+        "gdr_last_device_error": [vp],
+        "gdr_chunk_fwd_kernels": [i, i, i, i, i, i, f, i],
+        "gdr_status_string": [i],
+        "gdr_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.gdr_status_string.restype = ctypes.c_char_p
+    lib.gdr_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().gdr_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return load().gdr_version().decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libgdr takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libgdr takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise GdrError(code, where)
+
+
+def _f32(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return t
+
+
+def chunk_fwd(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 64,
+              out=None, final_state=None, want_final: bool = True):
+    """Chunked prefill.  q,k [B,H,T,dk], v [B,H,T,dv] (fp32 or bf16), g,beta [B,H,T]
+    fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(init_state, "init_state")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and want_final:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check(lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
+                             _ptr(init_state), _ptr(out), _ptr(final_state), B, H, T, dk, dv,
+                             int(chunk), DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd")
+    return out, final_state
+
+
+def decode_step(q, k, v, g, beta, a_min: float, state, *, out=None):
+    """One token for N sequences.  q,k [N,H,dk], v [N,H,dv], g,beta [N,H] fp32,
+    state [N,H,dk,dv] fp32 updated in place.  Returns out [N,H,dv]."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype, float32 or bfloat16")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(state, "state")
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    _check(lib.gdr_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
+                               _ptr(state), _ptr(out), N, H, dk, dv, DTYPE[q.dtype],
+                               _stream(q.device)), "gdr_decode_step")
+    return out
+
+
+def chunk_decay(g, a_min: float, chunk: int = 64, *, gamma=None):
+    """gamma [BH,T] = chunk-local cumulative product of alpha.  g [..., T] fp32."""
+    lib = load()
+    T = g.shape[-1]
+    BH = g.numel() // max(T, 1) if T else 0
+    _f32(g, "g")
+    if gamma is None:
+        gamma = torch.empty_like(g)
+    _check(lib.gdr_chunk_decay(_ptr(g), float(a_min), _ptr(gamma), BH, T, int(chunk),
+                               _stream(g.device)), "gdr_chunk_decay")
+    return gamma
+
+
+def chunk_wy(k, v, beta, gamma, chunk: int = 64):
+    """U [BH,T,dv], Wk [BH,T,dk] (fp32) of the intra-chunk WY/UT transform."""
+    lib = load()
+    *lead, T, dk = k.shape
+    dv = v.shape[-1]
+    BH = k.numel() // max(T * dk, 1)
+    U = torch.empty((*lead, T, dv), dtype=torch.float32, device=k.device)
+    Wk = torch.empty((*lead, T, dk), dtype=torch.float32, device=k.device)
+    _check(lib.gdr_chunk_wy(_ptr(k), _ptr(v), _ptr(beta), _ptr(gamma), _ptr(U), _ptr(Wk), BH, T,
+                            dk, dv, int(chunk), DTYPE[k.dtype], _stream(k.device)),
+           "gdr_chunk_wy")
+    return U, Wk
+
+
+def chunk_state(k, gamma, U, Wk, init_state=None, chunk: int = 64, want_mn: bool = True):
+    """W [BH,T,dv], Mn [BH,NC,dk,dv] (or None), final [BH,dk,dv] of the state pass."""
+    lib = load()
+    *lead, T, dk = k.shape
+    dv = U.shape[-1]
+    BH = k.numel() // max(T * dk, 1)
+    NC = (T + chunk - 1) // chunk
+    W = torch.empty_like(U)
+    Mn = (torch.empty((*lead, NC, dk, dv), dtype=torch.float32, device=k.device)
+          if want_mn else None)
+    fin = torch.empty((*lead, dk, dv), dtype=torch.float32, device=k.device)
+    _check(lib.gdr_chunk_state(_ptr(k), _ptr(gamma), _ptr(U), _ptr(Wk), _ptr(init_state),
+                               _ptr(W), _ptr(Mn), _ptr(fin), BH, T, dk, dv, int(chunk),
+                               DTYPE[k.dtype], _stream(k.device)), "gdr_chunk_state")
+    return W, Mn, fin
+
+
+def chunk_output(q, k, gamma, Mn, W, chunk: int = 64):
+    """out [BH,T,dv] in q's dtype from the per-chunk states and W."""
+    lib = load()
+    *lead, T, dk = q.shape
+    dv = W.shape[-1]
+    BH = q.numel() // max(T * dk, 1)
+    out = torch.empty((*lead, T, dv), dtype=q.dtype, device=q.device)
+    _check(lib.gdr_chunk_output(_ptr(q), _ptr(k), _ptr(gamma), _ptr(Mn), _ptr(W), _ptr(out), BH,
+                                T, dk, dv, int(chunk), DTYPE[q.dtype], _stream(q.device)),
+           "gdr_chunk_output")
+    return out
+
+
+def chunk_fwd_kernels(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16) -> int:
+    """How many kernels one chunk_fwd call with these arguments launches."""
+    return int(load().gdr_chunk_fwd_kernels(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
+
+
+def last_device_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error word
+    as a status code (0 = ok, 5 = a bounded wait timed out)."""
+    lib = load()
+    return int(lib.gdr_last_device_error(_stream(device)))

@@ -1,0 +1,195 @@
+// gdr_api.cu -- the extern "C" boundary of libgdr.so (declared in
+// include/gdr.h): argument validation, dispatch to the kernels, status codes.
+// No C++ exception crosses this file's functions.
+
+#include "gdr.h"
+#include "gdr_internal.h"
+
+#include <cmath>
+#include <cstdint>
+
+namespace {
+
+using gdr::Elem;
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool chunk_ok(int c) { return c == 16 || c == 32 || c == 64; }
+
+// a_min in (0, 1]; NaN fails every comparison.
+bool a_min_ok(float a_min) { return a_min > 0.0f && a_min <= 1.0f; }
+
+// The pages' range argument allows a worst in-tile cumulative log-decay of
+// -80 (e^-80 ~ 1.8e-35 stays a normal fp32 number, its reciprocal ~5.5e34
+// stays finite).  With alpha >= a_min the worst is chunk * ln(a_min).
+bool range_ok(float a_min, int chunk) {
+    return (double)chunk * -std::log((double)a_min) <= 80.0;
+}
+
+gdr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
+
+Elem elem_of(gdr_dtype_t d) { return d == GDR_DTYPE_F32 ? Elem::F32 : Elem::BF16; }
+
+bool dtype_ok(gdr_dtype_t d) { return d == GDR_DTYPE_F32 || d == GDR_DTYPE_BF16; }
+
+// Common checks of the staged-step entry points.
+gdr_status_t check_staged(int BH, int T, int dk, int dv, int chunk) {
+    if (BH < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
+    return GDR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float a_min, const float *init_state, void *out,
+                           float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                           gdr_dtype_t dtype, void *stream) {
+    if (B < 0 || H < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
+    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    const int64_t BH = (int64_t)B * H;
+    if (BH > 0x7fffffff || (int64_t)T * BH > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (BH == 0) return GDR_OK;
+    if (T == 0) {
+        if (final_state == nullptr) return GDR_OK;
+        return from_cuda(gdr::launch_copy_state(init_state, final_state, BH * dk * dv, s));
+    }
+    if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
+    const Elem e = elem_of(dtype);
+
+    if (gdr::fused_supported(dk, dv, chunk, e))
+        return from_cuda(gdr::launch_fused(q, k, v, g, beta, a_min, init_state, out,
+                                           final_state, B, H, T, dk, dv, chunk, s));
+
+    // Staged path on stream-ordered scratch.
+    const int NC = (T + chunk - 1) / chunk;
+    const size_t n_tok = (size_t)BH * (size_t)T;
+    const size_t bytes = sizeof(float) * (n_tok                       // gamma
+                                          + n_tok * (size_t)dv        // U
+                                          + n_tok * (size_t)dk        // Wk
+                                          + n_tok * (size_t)dv        // W
+                                          + (size_t)BH * NC * (size_t)dk * dv);  // Mn
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return GDR_ERR_CUDA;
+    float *gamma = static_cast<float *>(scratch);
+    float *U = gamma + n_tok;
+    float *Wk = U + n_tok * dv;
+    float *W = Wk + n_tok * dk;
+    float *Mn = W + n_tok * dv;
+    const int bh = (int)BH;
+    cudaError_t err = gdr::launch_decay(g, a_min, gamma, bh, T, chunk, s);
+    if (err == cudaSuccess)
+        err = gdr::launch_wy(k, v, beta, gamma, U, Wk, bh, T, dk, dv, chunk, e, s);
+    if (err == cudaSuccess)
+        err = gdr::launch_state(k, gamma, U, Wk, init_state, W, Mn, final_state, bh, T, dk, dv,
+                                chunk, e, s);
+    if (err == cudaSuccess)
+        err = gdr::launch_output(q, k, gamma, Mn, W, out, bh, T, dk, dv, chunk, e, s);
+    const cudaError_t ferr = cudaFreeAsync(scratch, s);
+    if (err == cudaSuccess) err = ferr;
+    return from_cuda(err);
+}
+
+gdr_status_t gdr_decode_step(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, float a_min, float *state, void *out, int N,
+                             int H, int dk, int dv, gdr_dtype_t dtype, void *stream) {
+    if (N < 0 || H < 0) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return GDR_ERR_UNSUPPORTED;
+    if ((int64_t)N * H == 0) return GDR_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out) return GDR_ERR_INVALID_ARG;
+    if ((int64_t)N * H > 0x7fffffff) return GDR_ERR_UNSUPPORTED;
+    return from_cuda(gdr::launch_decode(q, k, v, g, beta, a_min, state, out, N, H, dk, dv,
+                                        elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
+gdr_status_t gdr_chunk_decay(const float *g, float a_min, float *gamma, int BH, int T,
+                             int chunk, void *stream) {
+    if (BH < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
+    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    if ((int64_t)BH * T == 0) return GDR_OK;
+    if (!g || !gamma) return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_decay(g, a_min, gamma, BH, T, chunk,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+gdr_status_t gdr_chunk_wy(const void *k, const void *v, const float *beta, const float *gamma,
+                          float *U, float *Wk, int BH, int T, int dk, int dv, int chunk,
+                          gdr_dtype_t dtype, void *stream) {
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    gdr_status_t st = check_staged(BH, T, dk, dv, chunk);
+    if (st != GDR_OK) return st;
+    if ((int64_t)BH * T == 0) return GDR_OK;
+    if (!k || !v || !beta || !gamma || !U || !Wk) return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_wy(k, v, beta, gamma, U, Wk, BH, T, dk, dv, chunk,
+                                    elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
+gdr_status_t gdr_chunk_state(const void *k, const float *gamma, const float *U,
+                             const float *Wk, const float *init_state, float *W, float *Mn,
+                             float *final_state, int BH, int T, int dk, int dv, int chunk,
+                             gdr_dtype_t dtype, void *stream) {
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    gdr_status_t st = check_staged(BH, T, dk, dv, chunk);
+    if (st != GDR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (BH == 0) return GDR_OK;
+    if (T == 0) return from_cuda(gdr::launch_copy_state(init_state, final_state,
+                                                        (int64_t)BH * dk * dv, s));
+    if (!k || !gamma || !U || !Wk || !W) return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_state(k, gamma, U, Wk, init_state, W, Mn, final_state, BH, T,
+                                       dk, dv, chunk, elem_of(dtype), s));
+}
+
+gdr_status_t gdr_chunk_output(const void *q, const void *k, const float *gamma, const float *Mn,
+                              const float *W, void *out, int BH, int T, int dk, int dv,
+                              int chunk, gdr_dtype_t dtype, void *stream) {
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    gdr_status_t st = check_staged(BH, T, dk, dv, chunk);
+    if (st != GDR_OK) return st;
+    if ((int64_t)BH * T == 0) return GDR_OK;
+    if (!q || !k || !gamma || !Mn || !W || !out) return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_output(q, k, gamma, Mn, W, out, BH, T, dk, dv, chunk,
+                                        elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
+int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float a_min,
+                          gdr_dtype_t dtype) {
+    if (B < 0 || H < 0 || T < 0 || !dtype_ok(dtype) || !a_min_ok(a_min)) return -1;
+    if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk) || !range_ok(a_min, chunk)) return -1;
+    if ((int64_t)B * H == 0) return 0;
+    if (T == 0) return 0;  // a copy or memset, no kernel
+    return gdr::fused_supported(dk, dv, chunk, elem_of(dtype)) ? 1 : 4;
+}
+
+gdr_status_t gdr_last_device_error(void *stream) {
+    unsigned word = 0;
+    cudaError_t e = gdr::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &word);
+    if (e != cudaSuccess) return GDR_ERR_CUDA;
+    if (word & gdr::kDevErrTimeout) return GDR_ERR_TIMEOUT;
+    return GDR_OK;
+}
+
+const char *gdr_status_string(gdr_status_t status) {
+    switch (status) {
+        case GDR_OK: return "ok";
+        case GDR_ERR_INVALID_ARG: return "invalid argument";
+        case GDR_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case GDR_ERR_RANGE: return "chunk * -ln(a_min) exceeds the in-chunk decay range (80)";
+        case GDR_ERR_CUDA: return "CUDA runtime error";
+        case GDR_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *gdr_version(void) { return "gdr 0.1.0 sm_103a"; }
+
+}  // extern "C"

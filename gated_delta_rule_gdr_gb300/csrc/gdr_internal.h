@@ -1,0 +1,48 @@
+// gdr_internal.h -- launchers shared between the C-ABI layer and the kernel
+// translation units of libgdr.so.  Not installed; the public surface is
+// include/gdr.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace gdr {
+
+// Element type of q, k, v and out.
+enum class Elem { F32 = 0, BF16 = 1 };
+
+// ---- staged chunked form (gdr_staged.cu) ----
+cudaError_t launch_decay(const float *g, float a_min, float *gamma, int BH, int T, int C,
+                         cudaStream_t s);
+cudaError_t launch_wy(const void *k, const void *v, const float *beta, const float *gamma,
+                      float *U, float *Wk, int BH, int T, int dk, int dv, int C, Elem e,
+                      cudaStream_t s);
+cudaError_t launch_state(const void *k, const float *gamma, const float *U, const float *Wk,
+                         const float *init, float *W, float *Mn, float *final_state, int BH,
+                         int T, int dk, int dv, int C, Elem e, cudaStream_t s);
+cudaError_t launch_output(const void *q, const void *k, const float *gamma, const float *Mn,
+                          const float *W, void *out, int BH, int T, int dk, int dv, int C,
+                          Elem e, cudaStream_t s);
+// final_state <- init (or zeros) for T == 0.
+cudaError_t launch_copy_state(const float *init, float *final_state, int64_t n, cudaStream_t s);
+
+// ---- single-token decode (gdr_decode.cu) ----
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float a_min, float *state, void *out, int N,
+                          int H, int dk, int dv, Elem e, cudaStream_t s);
+
+// ---- fused tensor-core prefill (gdr_fused.cu) ----
+bool fused_supported(int dk, int dv, int C, Elem e);
+cudaError_t launch_fused(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, float a_min, const float *init, void *out,
+                         float *final_state, int B, int H, int T, int dk, int dv, int C,
+                         cudaStream_t s);
+
+// Device error word shared by every kernel with a bounded wait.
+// Returns the word's value and clears it (synchronous on `s`).
+cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value);
+
+// Codes stored in the device error word.
+constexpr unsigned kDevErrTimeout = 1u;
+
+}  // namespace gdr

@@ -1,0 +1,187 @@
+/*
+ * gdr.h -- C ABI of the GB300 gated delta rule library (libgdr.so).
+ *
+ * The layer: incremental (delta-rule) linear attention with a lower-bounded
+ * decay gate.  For every sequence b and head h the library carries a fixed
+ * size state S (dv x dk) through the tokens t = 0..T-1:
+ *
+ *     alpha_t = a_min + (1 - a_min) * sigmoid(g_t)                 (decay)
+ *     S_t     = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t     = S_t q_t
+ *
+ * Sources.  The update is the "correct-on-write" incremental rule with a
+ * position-dependent decay gate of "How to Think About Trillion-Parameter
+ * Sparse Multimodal LLMs", section 2.2 (Incremental Linear Attention), whose
+ * state is fixed-size so that inference cost does not grow with the context
+ * ("Trillion-Parameter MoE Multimodal LLMs: How to Evaluate the New
+ * Generation", section 2.1).  The decay floor is the lower-bounded decay of
+ * the same page, section 3.1 (and "What a Trillion-Parameter MoE Model Reveals
+ * About the Next Stage of LLM Scaling", section 3.2), read in the linear
+ * domain: alpha in (a_min, 1], so inside a chunk of C tokens the cumulative
+ * decay gamma stays >= a_min^C and its reciprocal <= a_min^-C.  That bound is
+ * what lets every causal tile of the chunked form -- the diagonal (intra-
+ * chunk) one included -- run as one dense tensor-core product ("Architecture
+ * Evolution and Training Engineering for Trillion-Scale Sparse Multimodal
+ * Models", section 3.2).
+ *
+ * Conventions for every entry point below
+ *   - All array pointers are caller-owned DEVICE memory, contiguous,
+ *     row-major, in the layouts given.  The library keeps no pointer after a
+ *     call returns.
+ *   - The state is fp32 [.., dk, dv] and holds M = S^T (M[i][j] = S[j][i]),
+ *     the same layout for prefill and decode, so a prefill's final state
+ *     feeds decode directly.
+ *   - g, beta are fp32.  q, k, v and out are all of `dtype`.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously on it; no call synchronises except
+ *     gdr_last_device_error.
+ *   - Argument errors are reported synchronously, before anything is
+ *     enqueued.  A failed launch returns GDR_ERR_CUDA.  Kernels never trap:
+ *     a bounded wait that runs out records GDR_ERR_TIMEOUT in a device error
+ *     word, read by gdr_last_device_error.  No C++ exception crosses this ABI.
+ *   - Supported shapes: dk, dv in {16, 32, 64, 128}; chunk in {16, 32, 64};
+ *     any T >= 0 (a ragged last chunk is masked).  Others: GDR_ERR_UNSUPPORTED.
+ *   - Range rule: chunk * (-ln a_min) must not exceed 80, the worst in-tile
+ *     cumulative log-decay the pages' range argument allows (section 3.1 of
+ *     the first page above); otherwise GDR_ERR_RANGE.  a_min must lie in
+ *     (0, 1]: GDR_ERR_INVALID_ARG otherwise.
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDR_OK = 0,
+    GDR_ERR_INVALID_ARG = 1,  /* null pointer, negative size, a_min out of (0,1] */
+    GDR_ERR_UNSUPPORTED = 2,  /* shape or dtype this build does not implement   */
+    GDR_ERR_RANGE = 3,        /* chunk * (-ln a_min) > 80                        */
+    GDR_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed            */
+    GDR_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up              */
+} gdr_status_t;
+
+typedef enum {
+    GDR_DTYPE_F32 = 0,        /* q, k, v, out are float                          */
+    GDR_DTYPE_BF16 = 1        /* q, k, v, out are bfloat16 (round-to-nearest-even
+                                 on the output store)                            */
+} gdr_dtype_t;
+
+/*
+ * Chunked prefill over B sequences x H heads x T tokens.
+ *   q, k        [B,H,T,dk]  dtype
+ *   v           [B,H,T,dv]  dtype
+ *   g, beta     [B,H,T]     fp32: raw decay logit, write strength
+ *   a_min       decay floor, 0 < a_min <= 1
+ *   init_state  [B,H,dk,dv] fp32, or NULL for a zero state
+ *   out         [B,H,T,dv]  dtype
+ *   final_state [B,H,dk,dv] fp32, or NULL to skip; may alias init_state
+ *   chunk       tile length C of the chunked form
+ * Work: the chunked form of the recurrence (per chunk: cumulative decay, the
+ * intra-chunk WY/UT transform, the inter-chunk state step and the output),
+ * which equals the token recurrence in exact arithmetic.
+ * bf16 with dk = dv = 128 and chunk = 64 runs one fused tensor-core kernel
+ * and allocates nothing.  Other shapes and fp32 run the staged kernels (the
+ * four gdr_chunk_* steps below) on stream-ordered scratch from the device's
+ * default memory pool (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * T == 0 copies init_state (or zeros) to final_state.
+ */
+gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, float a_min,
+                           const float *init_state, void *out, float *final_state,
+                           int B, int H, int T, int dk, int dv, int chunk,
+                           gdr_dtype_t dtype, void *stream);
+
+/*
+ * One token per sequence: N sequences x H heads, state updated in place.
+ *   q, k [N,H,dk] dtype; v [N,H,dv] dtype; g, beta [N,H] fp32;
+ *   state [N,H,dk,dv] fp32 (in/out); out [N,H,dv] dtype.
+ * Work: p = S k and r = S q in one pass over the state, u = v - alpha p,
+ * o = alpha r + beta (q.k) u, S <- alpha S + beta u k^T (the same recurrence
+ * with T = 1).  state must not alias q, k, v or out.
+ */
+gdr_status_t gdr_decode_step(const void *q, const void *k, const void *v,
+                             const float *g, const float *beta, float a_min,
+                             float *state, void *out, int N, int H, int dk, int dv,
+                             gdr_dtype_t dtype, void *stream);
+
+/* ---- the staged steps of the chunked form (what gdr_chunk_fwd runs for fp32
+ *      and for shapes the fused kernel does not cover), exposed so each step
+ *      can be checked on its own.  BH = B * H; NC = ceil(T / chunk). ---- */
+
+/*
+ * Step 1, cumulative decay inside each chunk (the Gamma = exp(cumsum(log
+ * decay)) of "Architecture Evolution and Training Engineering for
+ * Trillion-Scale Sparse Multimodal Models", section 3.2):
+ *   gamma[bh][t] = prod_{s = chunk start .. t} alpha_s,   fp32 [BH,T].
+ * a_min^(r) <= gamma <= 1 for the r-th row of a chunk, so 1/gamma is finite.
+ */
+gdr_status_t gdr_chunk_decay(const float *g, float a_min, float *gamma,
+                             int BH, int T, int chunk, void *stream);
+
+/*
+ * Step 2, intra-chunk WY/UT transform, per chunk (rows r, s of the chunk):
+ *   A  = strict_lower(diag(beta*gamma) K (diag(1/gamma) K)^T),  T = (I + A)^-1
+ *   U  = T diag(beta) V           -> U  fp32 [BH,T,dv]
+ *   Wk = T diag(beta*gamma) K     -> Wk fp32 [BH,T,dk]
+ * k [BH,T,dk], v [BH,T,dv] in dtype; beta, gamma fp32 [BH,T].
+ */
+gdr_status_t gdr_chunk_wy(const void *k, const void *v, const float *beta,
+                          const float *gamma, float *U, float *Wk,
+                          int BH, int T, int dk, int dv, int chunk,
+                          gdr_dtype_t dtype, void *stream);
+
+/*
+ * Step 3, inter-chunk state pass, sequential over chunks n:
+ *   W_n = U_n - Wk_n M_n;   M_{n+1} = gamma_C M_n + (diag(gamma_C/gamma) K_n)^T W_n
+ * Writes W fp32 [BH,T,dv], the state at every chunk start Mn fp32
+ * [BH,NC,dk,dv] (may be NULL) and final_state (may be NULL).
+ * init_state may be NULL (zeros).
+ */
+gdr_status_t gdr_chunk_state(const void *k, const float *gamma, const float *U,
+                             const float *Wk, const float *init_state, float *W,
+                             float *Mn, float *final_state,
+                             int BH, int T, int dk, int dv, int chunk,
+                             gdr_dtype_t dtype, void *stream);
+
+/*
+ * Step 4, output of every chunk (intra-chunk causal tile plus state term):
+ *   O_n = diag(gamma) Q M_n + lower_incl(diag(gamma) Q (diag(1/gamma) K)^T) W_n
+ * q, k in dtype; gamma fp32 [BH,T]; Mn fp32 [BH,NC,dk,dv]; W fp32 [BH,T,dv];
+ * out [BH,T,dv] in dtype.
+ */
+gdr_status_t gdr_chunk_output(const void *q, const void *k, const float *gamma,
+                              const float *Mn, const float *W, void *out,
+                              int BH, int T, int dk, int dv, int chunk,
+                              gdr_dtype_t dtype, void *stream);
+
+/*
+ * Number of kernel launches one gdr_chunk_fwd call with these arguments
+ * enqueues (1 on the fused path, 4 on the staged path, 0 for empty work), or
+ * -1 if the call would be rejected.  Host-only; touches no device.
+ */
+int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float a_min,
+                          gdr_dtype_t dtype);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word:
+ * GDR_ERR_TIMEOUT if a kernel's bounded wait gave up since the last call,
+ * GDR_ERR_CUDA if the stream reports an error, else GDR_OK.
+ */
+gdr_status_t gdr_last_device_error(void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *gdr_status_string(gdr_status_t status);
+
+/* Library version string, e.g. "gdr 0.1.0 sm_103a". */
+const char *gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */

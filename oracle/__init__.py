@@ -66,7 +66,7 @@ def _load():
             lib.gdr_oracle_decode.restype = ctypes.c_int
             lib.gdr_oracle_decode.argtypes = [f32p, f32p, f32p, f32p, f32p, ctypes.c_double,
                                               f64p, f64p, ctypes.c_int, ctypes.c_int,
-                                              ctypes.c_int, ctypes.c_int]
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -134,7 +134,7 @@ def fwd(q, k, v, g, beta, a_min: float, init_state=None, *, want_out: bool = Tru
     return out, fin
 
 
-def decode(q, k, v, g, beta, a_min: float, state: np.ndarray):
+def decode(q, k, v, g, beta, a_min: float, state: np.ndarray, *, nthreads: int | None = None):
     """One decode step in place on ``state`` ([N,H,dk,dv] float64).  q,k [N,H,dk],
     v [N,H,dv], g,beta [N,H].  Returns out [N,H,dv] fp64."""
     q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
@@ -148,7 +148,8 @@ def decode(q, k, v, g, beta, a_min: float, state: np.ndarray):
     f32, f64 = ctypes.c_float, ctypes.c_double
     rc = lib.gdr_oracle_decode(_ptr(q, f32), _ptr(k, f32), _ptr(v, f32), _ptr(g, f32),
                                _ptr(beta, f32), float(a_min), _ptr(state, f64),
-                               _ptr(out, f64), N, H, dk, dv)
+                               _ptr(out, f64), N, H, dk, dv,
+                               int(nthreads or os.cpu_count() or 1))
     if rc != 0:
         raise RuntimeError(f"gdr_oracle_decode failed with code {rc}")
     return out

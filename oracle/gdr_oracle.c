@@ -182,48 +182,100 @@ int gdr_oracle_fwd(const float *q, const float *k, const float *v,
     return rc;
 }
 
+/* One (sequence, head) of a decode step: the recurrence with T = 1 applied in
+ * place to M [dk][dv] (fp64, M layout); S is dv x dk scratch. */
+static void oracle_decode_one(const float *qt, const float *kt, const float *vt,
+                              double a, double b, double *M, double *out, int dk, int dv,
+                              double *S)
+{
+    for (int j = 0; j < dv; ++j)
+        for (int i = 0; i < dk; ++i)
+            S[(int64_t)j * dk + i] = M[(int64_t)i * dv + j];
+    for (int j = 0; j < dv; ++j) {
+        double uj = 0.0;
+        for (int i = 0; i < dk; ++i)
+            uj += S[(int64_t)j * dk + i] * (double)kt[i];
+        const double vj = (double)vt[j];
+        for (int i = 0; i < dk; ++i) {
+            const double ki = (double)kt[i];
+            double *s = &S[(int64_t)j * dk + i];
+            *s = a * (*s - b * uj * ki) + b * vj * ki;
+        }
+        double oj = 0.0;
+        for (int i = 0; i < dk; ++i)
+            oj += S[(int64_t)j * dk + i] * (double)qt[i];
+        out[j] = oj;
+    }
+    for (int j = 0; j < dv; ++j)
+        for (int i = 0; i < dk; ++i)
+            M[(int64_t)i * dv + j] = S[(int64_t)j * dk + i];
+}
+
+typedef struct {
+    const float *q, *k, *v, *g, *beta;
+    double a_min;
+    double *state, *out;
+    int64_t NH;
+    int dk, dv;
+    int64_t next;
+} decode_job_t;
+
+static void *decode_worker(void *arg)
+{
+    decode_job_t *jb = (decode_job_t *)arg;
+    double *S = (double *)malloc(sizeof(double) * (size_t)jb->dk * (size_t)jb->dv);
+    if (!S)
+        return (void *)1;
+    for (;;) {
+        const int64_t nh = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (nh >= jb->NH)
+            break;
+        const double a = gdr_oracle_alpha((double)jb->g[nh], jb->a_min);
+        oracle_decode_one(jb->q + nh * jb->dk, jb->k + nh * jb->dk, jb->v + nh * jb->dv, a,
+                          (double)jb->beta[nh], jb->state + nh * jb->dk * jb->dv,
+                          jb->out + nh * jb->dv, jb->dk, jb->dv, S);
+    }
+    free(S);
+    return NULL;
+}
+
 /*
  * One decode step for N independent sequences: the same recurrence with
  * T = 1, applied in place to state [N,H,dk,dv] (fp64, M layout).
- * q, k [N,H,dk]; v [N,H,dv]; g, beta [N,H]; out [N,H,dv].
+ * q, k [N,H,dk]; v [N,H,dv]; g, beta [N,H]; out [N,H,dv].  The (n, h) pairs
+ * are spread over nthreads host threads; each pair's arithmetic is the same
+ * whatever the thread count.
  */
 int gdr_oracle_decode(const float *q, const float *k, const float *v,
                       const float *g, const float *beta, double a_min,
-                      double *state, double *out, int N, int H, int dk, int dv)
+                      double *state, double *out, int N, int H, int dk, int dv,
+                      int nthreads)
 {
     if (!q || !k || !v || !g || !beta || !state || !out || N < 0 || H < 0 ||
         dk <= 0 || dv <= 0)
         return -1;
-    double *S = (double *)malloc(sizeof(double) * (size_t)dk * (size_t)dv);
-    if (!S)
+    decode_job_t jb = {q, k, v, g, beta, a_min, state, out, (int64_t)N * H, dk, dv, 0};
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > jb.NH)
+        nthreads = jb.NH > 0 ? (int)jb.NH : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th)
         return -2;
-    for (int64_t nh = 0; nh < (int64_t)N * H; ++nh) {
-        const float *kt = k + nh * dk, *qt = q + nh * dk, *vt = v + nh * dv;
-        double *M = state + nh * dk * dv;
-        const double a = gdr_oracle_alpha((double)g[nh], a_min);
-        const double b = (double)beta[nh];
-        for (int j = 0; j < dv; ++j)
-            for (int i = 0; i < dk; ++i)
-                S[(int64_t)j * dk + i] = M[(int64_t)i * dv + j];
-        for (int j = 0; j < dv; ++j) {
-            double uj = 0.0;
-            for (int i = 0; i < dk; ++i)
-                uj += S[(int64_t)j * dk + i] * (double)kt[i];
-            const double vj = (double)vt[j];
-            for (int i = 0; i < dk; ++i) {
-                const double ki = (double)kt[i];
-                double *s = &S[(int64_t)j * dk + i];
-                *s = a * (*s - b * uj * ki) + b * vj * ki;
-            }
-            double oj = 0.0;
-            for (int i = 0; i < dk; ++i)
-                oj += S[(int64_t)j * dk + i] * (double)qt[i];
-            out[nh * dv + j] = oj;
-        }
-        for (int j = 0; j < dv; ++j)
-            for (int i = 0; i < dk; ++i)
-                M[(int64_t)i * dv + j] = S[(int64_t)j * dk + i];
+    int rc = 0, started = 0;
+    for (int i = 1; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, decode_worker, &jb) != 0)
+            break;
+        started = i;
     }
-    free(S);
-    return 0;
+    if (decode_worker(&jb) != NULL)
+        rc = -2;
+    for (int i = 1; i <= started; ++i) {
+        void *r = NULL;
+        pthread_join(th[i], &r);
+        if (r != NULL)
+            rc = -2;
+    }
+    free(th);
+    return rc;
 }

@@ -1,0 +1,116 @@
+"""The C ABI loads, exports every symbol include/gdr.h declares, and rejects bad
+arguments synchronously -- host-only checks, no GPU and no kernel launch."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_gdr_gb300 as gdr
+from gated_delta_rule_gdr_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdr.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("gdr_chunk_fwd", "gdr_decode_step", "gdr_chunk_decay", "gdr_chunk_wy",
+                 "gdr_chunk_state", "gdr_chunk_output", "gdr_last_device_error",
+                 "gdr_status_string", "gdr_version"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert gdr.version().startswith("gdr ")
+    assert "sm_103a" in gdr.version()
+    for code in range(6):
+        s = gdr.status_string(code)
+        assert s and s != "unknown status"
+    assert gdr.status_string(99) == "unknown status"
+
+
+P = ctypes.c_void_p(0x1000)   # never dereferenced: every case fails validation first
+
+
+def fwd(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, a_min=0.95, init=None, out=P, fin=None, B=1, H=1,
+             T=64, dk=128, dv=128, chunk=64, dtype=1, stream=None)
+    a.update(kw)
+    return lib.gdr_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["a_min"], a["init"],
+                             a["out"], a["fin"], a["B"], a["H"], a["T"], a["dk"], a["dv"],
+                             a["chunk"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), 1), (dict(H=-2), 1), (dict(T=-1), 1),
+    (dict(a_min=0.0), 1), (dict(a_min=-0.5), 1), (dict(a_min=1.5), 1),
+    (dict(a_min=float("nan")), 1),
+    (dict(dk=96), 2), (dict(dv=256), 2), (dict(chunk=128), 2), (dict(chunk=8), 2),
+    (dict(dtype=7), 2),
+    (dict(a_min=0.2), 3),                 # 64 * -ln 0.2 = 103 > 80
+    (dict(a_min=0.28), 3),                # 64 * -ln 0.28 = 81.5 > 80
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(g=None), 1),
+    (dict(beta=None), 1), (dict(out=None), 1),
+])
+def test_chunk_fwd_rejects(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+def test_range_rule_boundary(lib):
+    # chunk = 16 allows a_min down to e^-5 (the pages' own per-step floor)
+    assert fwd(lib, chunk=16, a_min=0.00674, q=None) == 1     # e^-5 = 0.006738: in range
+    assert fwd(lib, chunk=16, a_min=0.0067, q=None) == 3
+
+
+def test_empty_inputs_are_a_no_op(lib):
+    assert fwd(lib, B=0, q=None, k=None) == 0
+    assert fwd(lib, H=0, q=None) == 0
+
+
+def test_decode_rejects(lib):
+    d = lib.gdr_decode_step
+    assert d(P, P, P, P, P, 0.95, P, P, -1, 1, 128, 128, 1, None) == 1
+    assert d(P, P, P, P, P, 0.0, P, P, 1, 1, 128, 128, 1, None) == 1
+    assert d(P, P, P, P, P, 0.95, P, P, 1, 1, 100, 128, 1, None) == 2
+    assert d(P, P, P, P, P, 0.95, None, P, 1, 1, 128, 128, 1, None) == 1
+    assert d(P, P, P, P, P, 0.95, P, P, 0, 4, 128, 128, 1, None) == 0   # empty
+
+
+def test_staged_steps_reject(lib):
+    assert lib.gdr_chunk_decay(P, 0.0, P, 1, 64, 64, None) == 1
+    assert lib.gdr_chunk_decay(P, 0.9, P, 1, 64, 48, None) == 2
+    assert lib.gdr_chunk_decay(P, 0.1, P, 1, 64, 64, None) == 3
+    assert lib.gdr_chunk_decay(None, 0.9, P, 1, 64, 64, None) == 1
+    assert lib.gdr_chunk_wy(P, P, P, P, P, P, 1, 64, 48, 64, 64, 1, None) == 2
+    assert lib.gdr_chunk_wy(P, P, None, P, P, P, 1, 64, 64, 64, 64, 1, None) == 1
+    assert lib.gdr_chunk_state(P, P, P, P, None, None, None, None, 1, 64, 64, 64, 64, 0,
+                               None) == 1
+    assert lib.gdr_chunk_output(P, P, P, P, P, P, -1, 64, 64, 64, 64, 0, None) == 1
+
+
+def test_binding_fails_loudly_without_cuda_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(ValueError):
+        gdr.chunk_fwd(q, q, q, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4), 0.9, chunk=16)

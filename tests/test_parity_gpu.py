@@ -1,0 +1,241 @@
+"""GPU parity: libgdr.so (through its C ABI) against the fp64 oracle on the same
+seeded inputs.  Tolerances are relative L2 over the whole tensor: 1e-5 for the
+fp32 path, 5e-3 for the bf16 paths, for outputs and final states alike."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunkwise
+import gated_delta_rule_gdr_gb300 as gdr
+from gated_delta_rule_gdr_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 5e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdr.load(build_if_missing=True)
+    yield
+    assert gdr.last_device_error() == 0
+
+
+def rel(x, ref):
+    return oracle.rel_l2(x, ref)
+
+
+def run_gpu(x, w, init=None, chunk=None):
+    out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                             x["init_state"] if init is None else init,
+                             chunk=chunk or w.chunk)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def to(x, device):
+    return {k_: (None if t is None else t.to(device)) for k_, t in x.items()}
+
+
+# ------------------------------------------------------------------ the correctness workload
+def test_correctness_workload_fp32():
+    w = I.CORRECTNESS
+    x = to(I.prefill_inputs(w), "cuda")
+    out, fin = run_gpu(x, w)
+    ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min, None)
+    assert rel(out, ro) <= TOL["f32"], rel(out, ro)
+    assert rel(fin, rf) <= TOL["f32"], rel(fin, rf)
+
+
+# ------------------------------------------------------------------ per-step parity
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,C,d", [(256, 64, 64), (100, 32, 32), (65, 16, 128)])
+def test_staged_steps_match_chunked_algebra(dtype, T, C, d):
+    w = I.CORRECTNESS.with_(B=1, H=2, T=T, dk=d, dv=d, chunk=C, dtype=dtype, init_std=0.5)
+    x = to(I.prefill_inputs(w), "cuda")
+    BH = w.B * w.H
+    gamma = gdr.chunk_decay(x["g"], w.a_min, C)
+    U, Wk = gdr.chunk_wy(x["k"], x["v"], x["beta"], gamma, C)
+    W, Mn, fin = gdr.chunk_state(x["k"], gamma, U, Wk, x["init_state"], C)
+    out = gdr.chunk_output(x["q"], x["k"], gamma, Mn, W, C)
+    torch.cuda.synchronize()
+    tol = 2e-6 if dtype == "f32" else 2e-6   # steps compute in fp32 on exact inputs
+    for h in range(BH):
+        b_, h_ = divmod(h, w.H)
+        args = [x[n][b_, h_].float().cpu().numpy() for n in ("q", "k", "v")]
+        ref_o, ref_M, inter = chunkwise.head(*args, x["g"][b_, h_].cpu().numpy(),
+                                             x["beta"][b_, h_].cpu().numpy(), w.a_min,
+                                             x["init_state"][b_, h_].cpu().numpy(), C, keep=True)
+        assert rel(gamma[b_, h_], np.concatenate(inter["gamma"])) <= tol
+        assert rel(U[b_, h_], np.concatenate(inter["U"])) <= 1e-5
+        assert rel(Wk[b_, h_], np.concatenate(inter["Wk"])) <= 1e-5
+        assert rel(W[b_, h_], np.concatenate(inter["W"])) <= 1e-5
+        assert rel(Mn[b_, h_], np.stack(inter["M"])) <= 1e-5
+        assert rel(fin[b_, h_], ref_M) <= 1e-5
+        assert rel(out[b_, h_], ref_o) <= (1e-5 if dtype == "f32" else TOL["bf16"])
+
+
+def test_decay_bounds_on_device():
+    g = torch.cat([torch.full((1, 1, 70), -80.0), torch.full((1, 1, 58), 60.0),
+                   torch.randn(1, 1, 128) * 4], dim=-1).cuda()
+    for a_min in (0.3, 0.9, 0.99):
+        gam = gdr.chunk_decay(g, a_min, 64).cpu().double().numpy().ravel()
+        r = (np.arange(gam.size) % 64) + 1
+        assert np.all(gam <= 1.0 + 1e-7)
+        assert np.all(gam >= a_min ** r * (1 - 1e-5))
+        assert np.all(np.isfinite(1.0 / gam.astype(np.float32)))
+
+
+# ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 100, 200])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_and_tiny(dtype, T, d):
+    w = I.CORRECTNESS.with_(B=1, H=1, T=T, dk=d, dv=d, dtype=dtype, init_std=0.02)
+    x = to(I.prefill_inputs(w), "cuda")
+    out, fin = run_gpu(x, w)
+    ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min,
+                        x["init_state"].cpu())
+    assert rel(out, ro) <= TOL[dtype]
+    assert rel(fin, rf) <= TOL[dtype]
+    assert torch.isfinite(out.float()).all()
+
+
+def test_zero_length_copies_state():
+    w = I.PREFILL.with_(B=2, H=3, T=0)
+    init = torch.randn(2, 3, 128, 128, device="cuda")
+    e = torch.empty(2, 3, 0, 128, device="cuda", dtype=torch.bfloat16)
+    z = torch.empty(2, 3, 0, device="cuda")
+    out, fin = gdr.chunk_fwd(e, e, e, z, z, 0.95, init)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, init)
+    out, fin = gdr.chunk_fwd(e, e, e, z, z, 0.95, None)
+    torch.cuda.synchronize()
+    assert not fin.any()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_init_may_alias_final(dtype):
+    w = I.CORRECTNESS.with_(B=2, H=2, T=130, dk=128, dv=128, dtype=dtype, init_std=0.02)
+    x = to(I.prefill_inputs(w), "cuda")
+    ref_out, ref_fin = run_gpu(x, w)
+    st = x["init_state"].clone()
+    gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, st, final_state=st)
+    torch.cuda.synchronize()
+    assert torch.equal(st, ref_fin)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T1", [64, 100, 1])
+def test_split_resume_and_prefill_to_decode(dtype, T1):
+    """One call over [0,T) equals two calls [0,T1), [T1,T) carrying the state;
+    a decode step after a prefill equals a prefill one token longer."""
+    T = 257
+    w = I.CORRECTNESS.with_(B=1, H=2, T=T, dk=128, dv=128, dtype=dtype, init_std=0.02)
+    x = to(I.prefill_inputs(w), "cuda")
+    tol = TOL[dtype]
+    full_o, full_f = run_gpu(x, w)
+    a = {n: (x[n][:, :, :T1] if n != "init_state" else x[n]) for n in x}
+    b = {n: (x[n][:, :, T1:].contiguous() if n != "init_state" else None) for n in x}
+    o1, f1 = run_gpu(a, w)
+    o2, f2 = run_gpu(b, w, init=f1)
+    assert rel(torch.cat([o1, o2], 2), full_o) <= tol
+    assert rel(f2, full_f) <= tol
+    # prefill T-1 tokens, then decode the last one
+    p = {n: (x[n][:, :, :T - 1].contiguous() if n != "init_state" else x[n]) for n in x}
+    po, pf = run_gpu(p, w)
+    o_last = gdr.decode_step(x["q"][:, :, -1].contiguous(), x["k"][:, :, -1].contiguous(),
+                             x["v"][:, :, -1].contiguous(), x["g"][:, :, -1].contiguous(),
+                             x["beta"][:, :, -1].contiguous(), w.a_min, pf)
+    torch.cuda.synchronize()
+    assert rel(o_last, full_o[:, :, -1]) <= tol
+    assert rel(pf, full_f) <= tol
+
+
+# ------------------------------------------------------------------ the prefill workloads
+def _prefill_full(w):
+    x = I.prefill_inputs(w, device="cuda")
+    out, fin = run_gpu(x, w)
+    cpu = {n: (None if t is None else t.cpu()) for n, t in x.items()}
+    return x, cpu, out, fin
+
+
+def test_prefill_b4h16t4096():
+    w = I.PREFILL
+    x, cpu, out, fin = _prefill_full(w)
+    ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,
+                        cpu["init_state"])
+    e_o, e_f = rel(out, ro), rel(fin, rf)
+    print(f"prefill rel-L2 out {e_o:.3e} final {e_f:.3e}")
+    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
+
+
+@pytest.mark.slow
+def test_long_prefill_b1h32t65536():
+    w = I.LONG_PREFILL
+    x, cpu, out, fin = _prefill_full(w)
+    ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min, None)
+    e_o, e_f = rel(out, ro), rel(fin, rf)
+    print(f"long prefill rel-L2 out {e_o:.3e} final {e_f:.3e}")
+    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
+
+
+@pytest.mark.slow
+def test_million_prefill_b1h16t1048576():
+    """The oracle checks heads 0-1 over the first 32768 tokens and head 0's final
+    state over the full million tokens; every output is finite."""
+    w = I.MILLION_PREFILL
+    x = I.prefill_inputs(w, device="cuda")
+    out, fin = run_gpu(x, w)
+    assert torch.isfinite(out).all() and torch.isfinite(fin).all()
+    P = 32768
+    sub = {n: x[n][:, :2, :P].cpu() for n in ("q", "k", "v", "g", "beta")}
+    ro, _ = oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], w.a_min, None,
+                       want_final=False)
+    e_o = rel(out[:, :2, :P], ro)
+    h0 = {n: x[n][:, :1].cpu() for n in ("q", "k", "v", "g", "beta")}
+    _, rf = oracle.fwd(h0["q"], h0["k"], h0["v"], h0["g"], h0["beta"], w.a_min, None,
+                       want_out=False)
+    e_f = rel(fin[:, :1], rf)
+    print(f"million prefill rel-L2 out[h0-1,:32768] {e_o:.3e} final[h0] {e_f:.3e}")
+    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ the decode workload
+def test_decode_n256h32_64steps():
+    w = I.DECODE
+    state = I.decode_state(w, device="cuda")
+    ref_state = state.cpu().double().numpy().copy()
+    worst_o = 0.0
+    for s in range(w.steps):
+        x = I.decode_step_inputs(w, s, device="cuda")
+        out = gdr.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, state)
+        ro = oracle.decode(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min,
+                           ref_state)
+        e = rel(out, ro)
+        worst_o = max(worst_o, e)
+        assert e <= TOL["bf16"], (s, e)
+    e_f = rel(state, ref_state)
+    print(f"decode worst step rel-L2 out {worst_o:.3e}; final state {e_f:.3e}")
+    assert e_f <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [(64, 64), (128, 64), (32, 128), (128, 128)])
+def test_decode_shapes(dtype, d):
+    dk, dv = d
+    w = I.DECODE.with_(B=5, H=3, dk=dk, dv=dv, dtype=dtype)
+    state = I.decode_state(w, device="cuda")
+    ref_state = state.cpu().double().numpy().copy()
+    for s in range(4):
+        x = I.decode_step_inputs(w, s, device="cuda")
+        out = gdr.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, state)
+        ro = oracle.decode(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min,
+                           ref_state)
+        assert rel(out, ro) <= (1e-5 if dtype == "f32" else TOL["bf16"])
+    assert rel(state, ref_state) <= 1e-5
