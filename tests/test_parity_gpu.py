@@ -140,7 +140,7 @@ def test_split_resume_and_prefill_to_decode(dtype, T1):
     x = to(I.prefill_inputs(w), "cuda")
     tol = TOL[dtype]
     full_o, full_f = run_gpu(x, w)
-    a = {n: (x[n][:, :, :T1] if n != "init_state" else x[n]) for n in x}
+    a = {n: (x[n][:, :, :T1].contiguous() if n != "init_state" else x[n]) for n in x}
     b = {n: (x[n][:, :, T1:].contiguous() if n != "init_state" else None) for n in x}
     o1, f1 = run_gpu(a, w)
     o2, f2 = run_gpu(b, w, init=f1)
