@@ -15,6 +15,7 @@
 // (Gamma = exp(cumsum(log-decay)); every causal tile scaled by 1/Gamma).
 
 #include "gdr_internal.h"
+#include "gdr_math.cuh"
 
 #include <cuda_bf16.h>
 
@@ -28,13 +29,6 @@ __device__ __forceinline__ float ld_elem(const __nv_bfloat16 *p, int64_t i) {
 __device__ __forceinline__ void st_elem(float *p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16 *p, int64_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
-}
-
-// log(alpha) for alpha = a_min + (1 - a_min) sigmoid(g).  Written through
-// 1 - alpha = (1 - a_min) / (1 + e^g) so that alpha close to 1 keeps its
-// relative accuracy.
-__device__ __forceinline__ float log_alpha(float g, float a_min) {
-    return log1pf(-(1.0f - a_min) / (1.0f + expf(g)));
 }
 
 // ---------------------------------------------------------------- step 1
