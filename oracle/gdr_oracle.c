@@ -31,7 +31,7 @@
  *
  * Parity status: every function here is pinned by the CPU tests (explicit
  * unrolled matrix products, the orthonormal-key write/read invariant, closed
- * forms for beta = 0 and a_min = 1, a hand-worked T = 1 case, and agreement
+ * forms for beta = 0 and a_min = 1, a hand-worked two-step case, and agreement
  * with an independent chunkwise reformulation).
  */
 #include <math.h>
