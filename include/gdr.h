@@ -160,6 +160,34 @@ gdr_status_t gdr_chunk_output(const void *q, const void *k, const float *gamma,
                               gdr_dtype_t dtype, void *stream);
 
 /*
+ * Chunked prefill that allocates no device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that must not
+ * allocate while they run -- for example a plugin inside a framework that owns
+ * all device memory through its own pool, or a deployment that forbids
+ * allocation after start-up because it can stall or fail mid-stream.
+ *
+ * Same arguments, layouts and results as gdr_chunk_fwd, computed by the
+ * staged kernels (steps 1-4 below) for every dtype and shape.  Their
+ * intermediates live in a fixed 32 MiB device array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   - Size limit: 4 * (B*H*T*(1 + dk + 2*dv) + B*H*ceil(T/chunk)*dk*dv) bytes
+ *     must not exceed 32 MiB (33554432); larger work returns
+ *     GDR_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device, with that device current on the calling
+ *     thread, looks up the array's device address (cudaGetSymbolAddress) and
+ *     caches it; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (every value is rewritten before it is read, so nothing needs
+ *     clearing).  Calls whose work overlaps on the GPU -- on different
+ *     streams, or from different threads -- race on it: order them.
+ */
+gdr_status_t gdr_chunk_fwd_static(const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta, float a_min,
+                                  const float *init_state, void *out, float *final_state,
+                                  int B, int H, int T, int dk, int dv, int chunk,
+                                  gdr_dtype_t dtype, void *stream);
+
+/*
  * Number of kernel launches one gdr_chunk_fwd call with these arguments
  * enqueues (1 on the fused path, 4 on the staged path, 0 for empty work), or
  * -1 if the call would be rejected.  Host-only; touches no device.
