@@ -30,14 +30,24 @@
 // (dv or dk):  U^T = V^T Lb^T,  Wk^T = K^T Lbg^T,  W^T = U^T - M^T Wk^T,
 // O^T = M^T Q^T + Wt^T P^T,  M^T_{n+1} = gamma_C M^T + Wt^T K.
 //
-// Shared-memory operands (all 128-byte swizzled, 1024-byte aligned):
+// Warp roles (288 threads):
+//   prep  (warps 0-3)  chunk k: decay, A and P from [K;Q]K^T, the triangular
+//                      solve, Lb / Lbg, then Wk^T          -- state-independent
+//   chain (warps 4-7)  chunk n: W^T epilogue, state update, output
+//   copy  (warp 8)     one lane issues the TMA loads of the inputs and the TMA
+//                      stores of the output
+// Each warpgroup issues its own tcgen05.mma from one elected thread, so the
+// preparation of chunk n+1 overlaps the state chain of chunk n.
+//
+// Shared-memory operands (128-byte swizzled, 1024-byte aligned):
 //   KQ[stage]  32 KB  [slab i/64][K rows 0..63 | Q rows 0..63][128 B]  (TMA)
 //   V[stage]   16 KB  [slab j/64][V rows 0..63][128 B]                   (TMA)
 //   MT         32 KB  M^T bf16, K-major ([j][i], two i slabs)
 //   WkT        16 KB  Wk^T bf16, MN-major ([i][r])
 //   WtT        16 KB  Wt^T bf16, K-major ([j][s])
-//   P, Lb, Lbg  8 KB each, K-major ([r][s])
-// TMEM (fp32, 128 lanes): KQK^T 64 cols, W^T 64, Wk^T 64, O^T 64, M^T 128.
+//   P[2]        8 KB each, K-major ([r][s]), one per stage
+//   Lb, Lbg     8 KB each, K-major ([r][s]), sharing space with the fp32 A
+// TMEM (fp32, 128 lanes): KQK^T 64 cols, W^T 2 x 64, Wk^T 64, O^T 64, M^T 128.
 
 #include "gdr_internal.h"
 #include "gdr_math.cuh"
@@ -58,9 +68,10 @@ namespace {
 
 using namespace sm100;
 
-constexpr int C = 64;     // chunk
-constexpr int D = 128;    // dk = dv
-constexpr int NT = 128;   // threads: one per TMEM lane
+constexpr int C = 64;      // chunk
+constexpr int D = 128;     // dk = dv
+constexpr int NT = 288;    // prep (128) + chain (128) + issue (32)
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;   // named barriers (0 is __syncthreads)
 
 // shared-memory map (bytes from the 1024-aligned base)
 constexpr uint32_t OFF_KQ = 0;             // 2 x 32 KB
@@ -70,20 +81,23 @@ constexpr uint32_t V_BYTES = 16384;
 constexpr uint32_t OFF_MT = 98304;         // 32 KB
 constexpr uint32_t OFF_WKT = 131072;       // 16 KB
 constexpr uint32_t OFF_WTT = 147456;       // 16 KB
-constexpr uint32_t OFF_P = 163840;         // 8 KB
-constexpr uint32_t OFF_LB = 172032;        // 8 KB
-constexpr uint32_t OFF_LBG = 180224;       // 8 KB
+constexpr uint32_t OFF_P = 163840;         // 2 x 8 KB
 constexpr int LDA = 68;                    // fp32 row stride of the solve matrices
-constexpr uint32_t OFF_AS = 188416;        // 64 x 68 fp32
+constexpr uint32_t OFF_AS = 180224;        // 64 x 68 fp32; Lb, Lbg reuse its first 16 KB
+constexpr uint32_t OFF_LB = OFF_AS;
+constexpr uint32_t OFF_LBG = OFF_AS + 8192;
 constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;   // 64 x 68 fp32
-constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;   // 32 x 32 fp32
-constexpr uint32_t OFF_SC = OFF_YS + 32 * 32 * 4;    // scalars: 2 stages x 4 x 64 fp32
+constexpr int LDY = 40;                    // row stride of the merge scratch
+constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;   // 32 x 40 fp32
+constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;   // scalars: 2 stages x 4 x 64 fp32
 constexpr uint32_t SMEM_USED = OFF_SC + 2 * 4 * 64 * 4;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
+static_assert(OFF_AS % 1024 == 0 && 64 * LDA * 4 >= 16384, "Lb/Lbg must fit in A's space");
 
 // TMEM columns
-constexpr uint32_t TM_KQK = 0, TM_W = 64, TM_WK = 128, TM_O = 192, TM_M = 256;
+constexpr uint32_t TM_KQK = 0, TM_W = 64 /* two buffers */, TM_WK = 192, TM_O = 256,
+                   TM_M = 320;
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
@@ -115,18 +129,50 @@ __device__ __forceinline__ void st_row_bf16(uint8_t *tile, uint32_t row, const f
     }
 }
 
+// Write 32 fp32 values as half a 128-byte bf16 row (chunks 4h..4h+3).
+__device__ __forceinline__ void st_halfrow_bf16(uint8_t *tile, uint32_t row, uint32_t h,
+                                                const float *v) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t ch = h * 4 + q4;
+        uint4 u;
+        u.x = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
+        u.y = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
+        u.z = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
+        u.w = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
+        *reinterpret_cast<uint4 *>(tile + row * 128u + ((ch ^ (row & 7u)) << 4)) = u;
+    }
+}
+
 __device__ __forceinline__ float ld_bf16_sw(const uint8_t *tile, uint32_t row, uint32_t col) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_offset(row, col)));
 }
 
-// Cumulative decay of one chunk (threads 0..63 hold row t's g and beta; all
-// 128 threads must call: it contains two block barriers).
-__device__ __forceinline__ void chunk_decay(int tid, float gv, float bv, int c, float a_min,
+// Bounded wait used by the warpgroups: gives up when the CTA-wide abort flag
+// is raised or the time limit passes (then raises the flag and the error word).
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            atomicOr(&g_device_error_word, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Cumulative decay of one chunk by the prep warpgroup (threads w < 64 hold row
+// w's g and beta).  Contains two prep-group barriers.
+__device__ __forceinline__ void chunk_decay(int w, float gv, float bv, int c, float a_min,
                                             Scal s, float *s_part, float *s_gC) {
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = w & 31, warp = w >> 5;
     float incl = 0.f;
-    if (tid < 64) {
-        incl = (tid < c) ? log_alpha(gv, a_min) : 0.f;
+    if (w < 64) {
+        incl = (w < c) ? log_alpha(gv, a_min) : 0.f;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, incl, off);
@@ -134,462 +180,551 @@ __device__ __forceinline__ void chunk_decay(int tid, float gv, float bv, int c, 
         }
         if (lane == 31) s_part[warp] = incl;
     }
-    __syncthreads();
-    if (tid < 64) {
+    named_sync(BAR_PREP, 128);
+    if (w < 64) {
         if (warp == 1) incl += s_part[0];
-        const bool valid = tid < c;
+        const bool valid = w < c;
         const float gam = valid ? expf(incl) : 1.f;
         const float b = valid ? bv : 0.f;
-        s.gam[tid] = gam;
-        s.ig[tid] = 1.f / gam;
-        s.bs[tid] = b;
-        s.bg[tid] = b * gam;
-        if (tid == c - 1) *s_gC = gam;
+        s.gam[w] = gam;
+        s.ig[w] = 1.f / gam;
+        s.bs[w] = b;
+        s.bg[w] = b * gam;
+        if (w == c - 1) *s_gC = gam;
     }
-    __syncthreads();
+    named_sync(BAR_PREP, 128);
 }
 
-// T = (I + A)^-1 for the strictly lower 64 x 64 A in As (fp32), into Ts
-// (lower part only is defined).  Blocked: four 16 x 16 diagonal inverses by
-// forward substitution, then two merge levels T_ij = -T_ii A_ij T_jj.
-__device__ __forceinline__ void solve_unit_lower(int tid, const float *As, float *Ts, float *Ys) {
-    if (tid < 64) {
-        const int b = tid >> 4, l = tid & 15, o = 16 * b;
-        float x[16];
+// tf32 warp-level MMA (m16n8k8) for the small merge products of the solve.
+// Fragment layouts (g = lane / 4, t = lane % 4): A (16 x 8) a0 (g, t), a1
+// (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8) b0 (t, g), b1 (t+4, g);
+// C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *M, int ld, int r0, int c0,
+                                       int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    a[0] = to_tf32(M[(r0 + g) * ld + c0 + t]);
+    a[1] = to_tf32(M[(r0 + g + 8) * ld + c0 + t]);
+    a[2] = to_tf32(M[(r0 + g) * ld + c0 + t + 4]);
+    a[3] = to_tf32(M[(r0 + g + 8) * ld + c0 + t + 4]);
+}
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *M, int ld, int k0, int n0,
+                                       int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    b[0] = to_tf32(M[(k0 + t) * ld + n0 + g]);
+    b[1] = to_tf32(M[(k0 + t + 4) * ld + n0 + g]);
+}
+__device__ __forceinline__ void frag_store(float *M, int ld, int r0, int n0, const float (&d)[4],
+                                           float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2 *>(&M[(r0 + g) * ld + n0 + 2 * t]) = make_float2(sign * d[0], sign * d[1]);
+    *reinterpret_cast<float2 *>(&M[(r0 + g + 8) * ld + n0 + 2 * t]) =
+        make_float2(sign * d[2], sign * d[3]);
+}
+
+// T = (I + A)^-1 for the strictly lower 64 x 64 A in As (fp32), into Ts, by
+// the prep warpgroup (w = thread index 0..127).  Blocked: four 16 x 16
+// diagonal inverses by right-looking forward substitution in fp32 (one column
+// per thread), then two merge levels T_ij = -T_ii (A_ij T_jj) on tf32 warp
+// MMAs.  On return the lower triangle of Ts holds T; the 16 x 16 blocks right
+// of the even diagonal blocks hold zeros (the merges read them).  T feeds
+// bf16 tensor-core operands, so the tf32 merges cost no accuracy that matters.
+__device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *Ts, float *Ys) {
+    const int lane = w & 31, wp = w >> 5;
+    if (w < 64) {
+        const int b = w >> 4, l = w & 15, o = 16 * b;
+        float x[16], acc[16];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) x[m] = (m == l) ? 1.f : 0.f;
-#pragma unroll
-        for (int r = 1; r < 16; ++r) {
-            float acc = 0.f;
-#pragma unroll
-            for (int m = 0; m < r; ++m) acc = fmaf(As[(o + r) * LDA + o + m], x[m], acc);
-            if (r > l) x[r] = -acc;
+        for (int m = 0; m < 16; ++m) {
+            x[m] = (m == l) ? 1.f : 0.f;
+            acc[m] = 0.f;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Ts[(o + r) * LDA + o + l] = x[r];
-    }
-    __syncthreads();
-    // level 1: blocks (1,0) and (3,2), 16 x 16 each
+        for (int m = 0; m < 16; ++m) {
+            if (m > l) x[m] = -acc[m];          // x[m] is final from here on
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int idx = u * NT + tid, p = idx >> 8, r = (idx >> 4) & 15, l = idx & 15;
+            for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(As[(o + r) * LDA + o + m], x[m], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            Ts[(o + r) * LDA + o + l] = x[r];
+            if ((b & 1) == 0) Ts[(o + r) * LDA + o + 16 + l] = 0.f;
+        }
+    }
+    named_sync(BAR_PREP, 128);
+    {   // level 1: T(1,0) and T(3,2); warp -> (pair, 8-column tile)
+        const int p = wp >> 1, nt = wp & 1;
         const int R = 16 * (2 * p + 1), Cb = 16 * (2 * p);
-        float acc = 0.f;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc = fmaf(As[(R + r) * LDA + Cb + m], Ts[(Cb + m) * LDA + Cb + l], acc);
-        Ys[p * 256 + r * 16 + l] = acc;
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t fa[4], fb[2];
+            frag_a(fa, As, LDA, R, Cb + 8 * ks, lane);
+            frag_b(fb, Ts, LDA, Cb + 8 * ks, Cb + 8 * nt, lane);
+            mma_tf32(d, fa, fb);
+        }
+        frag_store(Ys + p * 16 * LDY, LDY, 0, 8 * nt, d, 1.f, lane);
+        named_sync(BAR_PREP, 128);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t fa[4], fb[2];
+            frag_a(fa, Ts, LDA, R, R + 8 * ks, lane);          // zero above the diagonal
+            frag_b(fb, Ys + p * 16 * LDY, LDY, 8 * ks, 8 * nt, lane);
+            mma_tf32(e, fa, fb);
+        }
+        frag_store(Ts, LDA, R, Cb + 8 * nt, e, -1.f, lane);
     }
-    __syncthreads();
+    named_sync(BAR_PREP, 128);
+    {   // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
+        // warp -> 8-column tile, both 16-row tiles
+        const int n0 = 8 * wp;
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int idx = u * NT + tid, p = idx >> 8, r = (idx >> 4) & 15, l = idx & 15;
-        const int R = 16 * (2 * p + 1), Cb = 16 * (2 * p);
-        float acc = 0.f;
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t fb[2], fa0[4], fa1[4];
+            frag_b(fb, Ts, LDA, 8 * ks, n0, lane);
+            frag_a(fa0, As, LDA, 32, 8 * ks, lane);
+            frag_a(fa1, As, LDA, 48, 8 * ks, lane);
+            mma_tf32(d0, fa0, fb);
+            mma_tf32(d1, fa1, fb);
+        }
+        frag_store(Ys, LDY, 0, n0, d0, 1.f, lane);
+        frag_store(Ys, LDY, 16, n0, d1, 1.f, lane);
+        named_sync(BAR_PREP, 128);
+        float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-            if (m <= r) acc = fmaf(Ts[(R + r) * LDA + R + m], Ys[p * 256 + m * 16 + l], acc);
-        Ts[(R + r) * LDA + Cb + l] = -acc;
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t fb[2], fa0[4], fa1[4];
+            frag_b(fb, Ys, LDY, 8 * ks, n0, lane);
+            frag_a(fa0, Ts, LDA, 32, 32 + 8 * ks, lane);
+            frag_a(fa1, Ts, LDA, 48, 32 + 8 * ks, lane);
+            mma_tf32(e0, fa0, fb);
+            mma_tf32(e1, fa1, fb);
+        }
+        frag_store(Ts, LDA, 32, n0, e0, -1.f, lane);
+        frag_store(Ts, LDA, 48, n0, e1, -1.f, lane);
     }
-    __syncthreads();
-    // level 2: block rows 32..63, cols 0..31
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int idx = u * NT + tid, r = idx >> 5, l = idx & 31;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < 32; ++m)
-            if (m >= l) acc = fmaf(As[(32 + r) * LDA + m], Ts[m * LDA + l], acc);
-        Ys[r * 32 + l] = acc;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int idx = u * NT + tid, r = idx >> 5, l = idx & 31;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < 32; ++m)
-            if (m <= r) acc = fmaf(Ts[(32 + r) * LDA + 32 + m], Ys[m * 32 + l], acc);
-        Ts[(32 + r) * LDA + l] = -acc;
-    }
-    __syncthreads();
+    named_sync(BAR_PREP, 128);
 }
 
 struct FusedArgs {
     const float *g, *beta, *init;
-    __nv_bfloat16 *out;
     float *final_state;
     float a_min;
     int T;
     uint64_t limit_ns;
 };
 
+// mbarriers of the pipeline (index into s_bar)
+enum : int {
+    B_FULL0 = 0, B_FULL1,      // copy: TMA inputs of a stage landed
+    B_KQK,                     // prep commit: [K;Q]K^T done
+    B_UWK,                     // prep commit: U^T', Wk^T' done
+    B_W,                       // chain commit: W^T done
+    B_D,                       // chain commit: M^T update, O^T done
+    B_SCAL,                    // prep: decay scalars of chunk k written
+    B_WKT,                     // prep: Wk^T written (and U^T' in TMEM)
+    B_RWFREE0, B_RWFREE1,      // chain: W^T buffer read out, per buffer
+    B_OSTAGE0, B_OSTAGE1,      // chain: output tile staged, input stage done with
+    B_DRAINP, B_DRAINC,        // commits of the error path (prep, chain)
+    NUM_BARS
+};
+
 __global__ void __launch_bounds__(NT, 1)
 fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const FusedArgs a) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    __shared__ __align__(8) uint64_t bar_tma[2];
-    __shared__ __align__(8) uint64_t bar_mma;
+    __shared__ __align__(8) uint64_t s_bar[NUM_BARS];
     __shared__ uint32_t s_tmem;
     __shared__ float s_part[2];
     __shared__ float s_gC[2];
+    __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int bh = blockIdx.x;
     const int T = a.T;
     const int NC = (T + C - 1) / C;
     const int64_t row_base = (int64_t)bh * T;
-    const uint32_t btma0 = smem_u32(&bar_tma[0]), btma1 = smem_u32(&bar_tma[1]);
-    const uint32_t bmma = smem_u32(&bar_mma);
+    auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
 
     if (tid == 0) {
-        mbar_init(btma0, 1);
-        mbar_init(btma1, 1);
-        mbar_init(bmma, 1);
+        for (int i = 0; i < NUM_BARS; ++i) mbar_init(bar(i), 1);
+        s_abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
     }
-    if (warp == 0) {
+    if (warp == 8) {
         tmem_alloc(smem_u32(&s_tmem), TM_COLS);
         tmem_relinquish();
+        if (tid == 256) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's lane quadrant
-
-    bool tma_pending[2] = {false, false};   // meaningful in thread 0
-    uint32_t tma_parity[2] = {0u, 0u};      // parity of the outstanding load per stage
-    bool mma_pending = false;               // meaningful in thread 0
-    uint32_t mma_phase = 0;
-    bool ok = true;
-
-    auto issue_tma = [&](int n) {
-        const int st = n & 1;
-        const uint32_t bar = st ? btma1 : btma0;
-        const uint32_t kq = sbase + OFF_KQ + st * KQ_BYTES;
-        const uint32_t vv = sbase + OFF_V + st * V_BYTES;
-        mbar_arrive_expect_tx(bar, KQ_BYTES + V_BYTES);
-        tma_load_3d(kq + 0, &tm_k, bar, 0, n * C, bh);
-        tma_load_3d(kq + 8192, &tm_q, bar, 0, n * C, bh);
-        tma_load_3d(kq + 16384, &tm_k, bar, 64, n * C, bh);
-        tma_load_3d(kq + 24576, &tm_q, bar, 64, n * C, bh);
-        tma_load_3d(vv + 0, &tm_v, bar, 0, n * C, bh);
-        tma_load_3d(vv + 8192, &tm_v, bar, 64, n * C, bh);
-        tma_pending[st] = true;
-        tma_parity[st] = (uint32_t)(n >> 1) & 1u;
-    };
-    auto mma_wait = [&]() -> bool {
-        const bool w = mbar_wait(bmma, mma_phase, a.limit_ns);
-        if (w) {
-            mma_phase ^= 1u;
-            mma_pending = false;
-        }
-        return w;
-    };
-
-    if (tid == 0) {
-        issue_tma(0);
-        if (NC > 1) issue_tma(1);
-    }
-
-    // decay of chunk 0, prefetch of chunk 1's g / beta
-    float g_next = 0.f, b_next = 0.f;
-    {
-        const int c0 = min(C, T);
-        float gv = 0.f, bv = 0.f;
-        if (tid < c0) {
-            gv = a.g[row_base + tid];
-            bv = a.beta[row_base + tid];
-        }
-        chunk_decay(tid, gv, bv, c0, a.a_min, scal(sm, 0), s_part, &s_gC[0]);
-        if (NC > 1 && tid < min(C, T - C)) {
-            g_next = a.g[row_base + C + tid];
-            b_next = a.beta[row_base + C + tid];
-        }
-    }
-
-    // initial state: TMEM M^T <- gamma_C(0) * M0^T, MT <- bf16(M0^T)
-    {
-        const float gC = s_gC[0];
-        const int j = tid;
-#pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-            float v[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int i = cb * 32 + e;
-                v[e] = a.init ? a.init[((int64_t)bh * D + i) * D + j] : 0.f;
-            }
-            uint8_t *slab = sm + OFF_MT + (cb >> 1) * 16384;
-            // 32 values = 4 swizzle chunks of the row
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const uint32_t ch = (cb & 1) * 4 + q4;
-                uint4 u;
-                u.x = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
-                u.y = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
-                u.z = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
-                u.w = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(slab + j * 128u + ((ch ^ (j & 7u)) << 4)) = u;
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] *= gC;
-            tmem_st32(tl + TM_M + cb * 32, v);
-        }
-        tmem_wait_st();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-    }
-
-    const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
-    const uint32_t idesc_u = idesc_bf16(128, 64, true, false);
-    const uint32_t idesc_w = idesc_bf16(128, 64, false, true, true);
-    const uint32_t idesc_o1 = idesc_bf16(128, 64, false, false);
-    const uint32_t idesc_d = idesc_bf16(128, 128, false, true);
-
     float *As = reinterpret_cast<float *>(sm + OFF_AS);
     float *Ts = reinterpret_cast<float *>(sm + OFF_TS);
     float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
 
-#pragma unroll 1
-    for (int n = 0; n < NC; ++n) {
-        const int st = n & 1;
-        const int t0 = n * C;
-        const int c = min(C, T - t0);
-        const Scal S = scal(sm, st);
-        const float gC = s_gC[st];
-        const float igC = 1.f / gC;
-        uint8_t *kq = sm + OFF_KQ + st * KQ_BYTES;
-        uint8_t *vt = sm + OFF_V + st * V_BYTES;
-        const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
-        const uint32_t v_a = sbase + OFF_V + st * V_BYTES;
+    const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
+    const uint32_t idesc_u = idesc_bf16(128, 64, true, false);
+    const uint32_t idesc_w = idesc_bf16(128, 64, false, true, true);
+    const uint32_t idesc_o = idesc_bf16(128, 64, false, false);
+    const uint32_t idesc_d = idesc_bf16(128, 128, false, true);
 
-        // ---- inputs of chunk n
-        ok = mbar_wait(st ? btma1 : btma0, (uint32_t)(n >> 1) & 1u, a.limit_ns);
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        if (tid == 0) tma_pending[st] = false;
+    if (warp < 4) {
+        // ================================================================ prep
+        const int w = tid;
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        bool issued = false;
+        float g_next = 0.f, b_next = 0.f;
+        if (w < min(C, T)) {
+            g_next = a.g[row_base + w];
+            b_next = a.beta[row_base + w];
+        }
+        for (int k = 0; k < NC; ++k) {
+            const int st = k & 1;
+            const int c = min(C, T - k * C);
+            const Scal S = scal(sm, st);
+            uint8_t *kq = sm + OFF_KQ + st * KQ_BYTES;
+            const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
+            const uint32_t v_a = sbase + OFF_V + st * V_BYTES;
 
-        // ---- [K;Q] K^T
-        if (tid == 0) {
+            bool ok = role_wait(bar(B_FULL0 + st), (uint32_t)(k >> 1) & 1u, a.limit_ns, &s_abort);
+            if (!named_and(BAR_PREP, 128, ok)) break;
+            if (w == 0) {   // [K;Q] K^T  (the accumulator was read out last chunk)
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ad = kq_a + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + TM_KQK, sdesc_sw128(ad, 16, 1024), sdesc_sw128(ad, 16, 1024),
+                             idesc_kqk, kk > 0);
+                }
+                mma_commit(bar(B_KQK));
+                issued = true;
+            }
+            chunk_decay(w, g_next, b_next, c, a.a_min, S, s_part, &s_gC[st]);
+            if (w == 0) mbar_arrive(bar(B_SCAL));
+            if (k + 1 < NC && w < min(C, T - (k + 1) * C)) {
+                g_next = a.g[row_base + (int64_t)(k + 1) * C + w];
+                b_next = a.beta[row_base + (int64_t)(k + 1) * C + w];
+            }
+            const float igC = 1.f / s_gC[st];
+
+            // A = strict_lower(diag(beta gamma) K K^T diag(1/gamma)), P = lower(Q K^T) / gamma_C
+            ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
+            if (!named_and(BAR_PREP, 128, ok)) break;
             tc_fence_after();
+            {
+                float v[64];
+                tmem_ld32(tl + TM_KQK, *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(tl + TM_KQK + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                if (w < 64) {
+                    const int r = w;
+                    const float br = (r < c) ? S.bg[r] : 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ad = kq_a + (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + TM_KQK, sdesc_sw128(ad, 16, 1024), sdesc_sw128(ad, 16, 1024),
-                         idesc_kqk, kk > 0);
+                    for (int s4 = 0; s4 < 64; s4 += 4) {
+                        const float4 ig4 = *reinterpret_cast<const float4 *>(&S.ig[s4]);
+                        float4 o;
+                        o.x = (s4 + 0 < r) ? br * v[s4 + 0] * ig4.x : 0.f;
+                        o.y = (s4 + 1 < r) ? br * v[s4 + 1] * ig4.y : 0.f;
+                        o.z = (s4 + 2 < r) ? br * v[s4 + 2] * ig4.z : 0.f;
+                        o.w = (s4 + 3 < r) ? br * v[s4 + 3] * ig4.w : 0.f;
+                        *reinterpret_cast<float4 *>(&As[r * LDA + s4]) = o;
+                    }
+                } else {
+                    const int r = w - 64;
+#pragma unroll
+                    for (int s = 0; s < 64; ++s) v[s] = (s <= r && r < c) ? v[s] * igC : 0.f;
+                    st_row_bf16(sm + OFF_P + st * 8192, r, v);
+                }
             }
-            mma_commit(bmma);
-            mma_pending = true;
-        }
-        ok = __syncthreads_and(mma_wait());
-        if (!ok) break;
-        tc_fence_after();
-        {
-            float v[64];
-            tmem_ld32(tl + TM_KQK, *reinterpret_cast<float(*)[32]>(&v[0]));
-            tmem_ld32(tl + TM_KQK + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-            tmem_wait_ld();
-            if (tid < 64) {
-                const int r = tid;
-                const float br = S.bg[r];
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(BAR_PREP, 128);
+
+            solve_unit_lower(w, As, Ts, Ys);
+            {   // Lb = (T - I) diag(beta), Lbg = (T - I) diag(beta gamma), bf16 rows
+                const int r = w & 63;
+                const float *sc = (w < 64) ? S.bs : S.bg;
+                float v[64];
 #pragma unroll
-                for (int s = 0; s < 64; ++s)
-                    As[r * LDA + s] = (s < r && r < c) ? br * v[s] * S.ig[s] : 0.f;
-            } else {
-                const int r = tid - 64;
-#pragma unroll
-                for (int s = 0; s < 64; ++s) v[s] = (s <= r && r < c) ? v[s] * igC : 0.f;
-                st_row_bf16(sm + OFF_P, r, v);
+                for (int s4 = 0; s4 < 64; s4 += 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s4]);
+                    const float4 f = *reinterpret_cast<const float4 *>(&sc[s4]);
+                    v[s4 + 0] = (s4 + 0 < r) ? t.x * f.x : 0.f;
+                    v[s4 + 1] = (s4 + 1 < r) ? t.y * f.y : 0.f;
+                    v[s4 + 2] = (s4 + 2 < r) ? t.z * f.z : 0.f;
+                    v[s4 + 3] = (s4 + 3 < r) ? t.w * f.w : 0.f;
+                }
+                st_row_bf16(sm + ((w < 64) ? OFF_LB : OFF_LBG), r, v);
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- T = (I + A)^-1, then Lb, Lbg
-        solve_unit_lower(tid, As, Ts, Ys);
-        {
-            const int r = tid & 63;
-            const float *sc = (tid < 64) ? S.bs : S.bg;
-            float v[64];
+            fence_proxy_async_smem();
+            // U^T' = V^T Lb^T into W^T buffer st (free once the chain read chunk k-2's W^T)
+            ok = (k < 2) || role_wait(bar(B_RWFREE0 + st), (uint32_t)((k - 2) >> 1) & 1u,
+                                      a.limit_ns, &s_abort);
+            if (!named_and(BAR_PREP, 128, ok)) break;
+            if (w == 0) {
+                tc_fence_after();
 #pragma unroll
-            for (int s = 0; s < 64; ++s) v[s] = (s < r) ? Ts[r * LDA + s] * sc[s] : 0.f;
-            st_row_bf16(sm + ((tid < 64) ? OFF_LB : OFF_LBG), r, v);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_W + st * 64, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
+                             sdesc_sw128(sbase + OFF_LB + kk * 32, 16, 1024), idesc_u, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_WK, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
+                             sdesc_sw128(sbase + OFF_LBG + kk * 32, 16, 1024), idesc_u, kk > 0);
+                mma_commit(bar(B_UWK));
+            }
 
-        // ---- U^T' = V^T Lb^T, Wk^T' = K^T Lbg^T
-        if (tid == 0) {
+            // Wk^T[i][r] = Wk^T'[i][r] + beta_r gamma_r K[r][i]  ->  WkT (MN-major, row i)
+            ok = role_wait(bar(B_UWK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
+            if (ok && k > 0) ok = role_wait(bar(B_W), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
+            if (!named_and(BAR_PREP, 128, ok)) break;
             tc_fence_after();
+            {
+                const int i = w;
+                float v[64];
+                tmem_ld32(tl + TM_WK, *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(tl + TM_WK + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                const uint8_t *kslab = kq + (i >> 6) * 16384;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem + TM_W, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
-                         sdesc_sw128(sbase + OFF_LB + kk * 32, 16, 1024), idesc_u, kk > 0);
+                for (int r = 0; r < 64; ++r) v[r] = fmaf(S.bg[r], ld_bf16_sw(kslab, r, i & 63), v[r]);
+                st_row_bf16(sm + OFF_WKT, i, v);
             }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem + TM_WK, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
-                         sdesc_sw128(sbase + OFF_LBG + kk * 32, 16, 1024), idesc_u, kk > 0);
-            }
-            mma_commit(bmma);
-            mma_pending = true;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(BAR_PREP, 128);
+            if (w == 0) mbar_arrive(bar(B_WKT));
         }
-        ok = __syncthreads_and(mma_wait());
-        if (!ok) break;
-        tc_fence_after();
-        {   // Wk^T[i][r] = Wk^T'[i][r] + beta_r gamma_r K[r][i]  ->  WkT (MN-major, row i)
-            const int i = tid;
-            float v[64];
-            tmem_ld32(tl + TM_WK, *reinterpret_cast<float(*)[32]>(&v[0]));
-            tmem_ld32(tl + TM_WK + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-            tmem_wait_ld();
-            const uint8_t *kslab = kq + (i >> 6) * 16384;
-#pragma unroll
-            for (int r = 0; r < 64; ++r) v[r] = fmaf(S.bg[r], ld_bf16_sw(kslab, r, i & 63), v[r]);
-            st_row_bf16(sm + OFF_WKT, i, v);
+        if (s_abort && w == 0 && issued) {   // let this thread's MMAs land before TMEM goes away
+            mma_commit(bar(B_DRAINP));
+            mbar_wait(bar(B_DRAINP), 0u, kCleanupLimitNs);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- W^T = U^T' - M^T Wk^T ;  O^T = M^T Q^T
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ad = sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + TM_W, sdesc_sw128(ad, 16, 1024),
-                         sdesc_sw128(sbase + OFF_WKT + kk * 2048, 16384, 1024), idesc_w, 1);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ad = sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint32_t bd = kq_a + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + TM_O, sdesc_sw128(ad, 16, 1024), sdesc_sw128(bd, 16, 1024),
-                         idesc_o1, kk > 0);
-            }
-            mma_commit(bmma);
-            mma_pending = true;
-        }
-        ok = __syncthreads_and(mma_wait());
-        if (!ok) break;
-        tc_fence_after();
-        {   // Wt^T[j][s] = (W^T'[j][s] + beta_s V[s][j]) * gamma_C / gamma_s  -> WtT (row j)
-            const int j = tid;
-            float v[64];
-            tmem_ld32(tl + TM_W, *reinterpret_cast<float(*)[32]>(&v[0]));
-            tmem_ld32(tl + TM_W + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-            tmem_wait_ld();
-            const uint8_t *vslab = vt + (j >> 6) * 8192;
-#pragma unroll
-            for (int s = 0; s < 64; ++s) {
-                const float w = fmaf(S.bs[s], ld_bf16_sw(vslab, s, j & 63), v[s]);
-                v[s] = (s < c) ? w * (gC * S.ig[s]) : 0.f;
-            }
-            st_row_bf16(sm + OFF_WTT, j, v);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- M^T += Wt^T K ;  O^T += Wt^T P^T
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem + TM_M, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
-                         sdesc_sw128(kq_a + kk * 2048, 16384, 1024), idesc_d, 1);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
-                         sdesc_sw128(sbase + OFF_P + kk * 32, 16, 1024), idesc_o1, 1);
-            }
-            mma_commit(bmma);
-            mma_pending = true;
-        }
-        // decay of the next chunk while the tensor core works
-        if (n + 1 < NC) {
-            const int c1 = min(C, T - (n + 1) * C);
-            chunk_decay(tid, g_next, b_next, c1, a.a_min, scal(sm, st ^ 1), s_part, &s_gC[st ^ 1]);
-            if (n + 2 < NC && tid < min(C, T - (n + 2) * C)) {
-                g_next = a.g[row_base + (int64_t)(n + 2) * C + tid];
-                b_next = a.beta[row_base + (int64_t)(n + 2) * C + tid];
-            }
-        }
-        ok = __syncthreads_and(mma_wait());
-        if (!ok) break;
-        tc_fence_after();
-        {   // output: out[t0 + r][j] = gamma_r * O^T[j][r]
-            const int j = tid;
-            float v[64];
-            tmem_ld32(tl + TM_O, *reinterpret_cast<float(*)[32]>(&v[0]));
-            tmem_ld32(tl + TM_O + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-            tmem_wait_ld();
-            __nv_bfloat16 *o = a.out + (row_base + t0) * D + j;
-#pragma unroll
-            for (int r = 0; r < 64; ++r)
-                if (r < c) o[(int64_t)r * D] = __float2bfloat16_rn(v[r] * S.gam[r]);
-        }
-        {   // state: MT <- bf16(M^T_{n+1}); TMEM M^T <- gamma_C(n+1) M^T_{n+1}
-            const int j = tid;
-            const bool last = (n + 1 == NC);
-            const float gn = last ? 1.f : s_gC[st ^ 1];
+    } else if (warp < 8) {
+        // ================================================================ chain
+        const int w = tid - 128;    // = TMEM lane (row j of the transposed products)
+        const int j = w;
+        const int lane = w & 31;
+        const uint32_t tl = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        bool issued = false;
+        bool ok = role_wait(bar(B_SCAL), 0u, a.limit_ns, &s_abort);
+        ok = named_and(BAR_CHAIN, 128, ok);
+        uint32_t scal_seen = 1;    // phases of B_SCAL observed
+        if (ok) {
+            // initial state: TMEM M^T <- gamma_C(0) M0^T, MT <- bf16(M0^T)
+            const float gC = s_gC[0];
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float v[32];
-                tmem_ld32(tl + TM_M + cb * 32, v);
-                tmem_wait_ld();
-                if (last) {
-                    if (a.final_state) {
-                        float *f = a.final_state + (int64_t)bh * D * D + j;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) f[(int64_t)(cb * 32 + e) * D] = v[e];
-                    }
-                } else {
-                    uint8_t *slab = sm + OFF_MT + (cb >> 1) * 16384;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint32_t ch = (cb & 1) * 4 + q4;
-                        uint4 u;
-                        u.x = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
-                        u.y = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
-                        u.z = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
-                        u.w = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
-                        *reinterpret_cast<uint4 *>(slab + j * 128u + ((ch ^ (j & 7u)) << 4)) = u;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] *= gn;
-                    tmem_st32(tl + TM_M + cb * 32, v);
+                for (int e = 0; e < 32; ++e) {
+                    const int i = cb * 32 + e;
+                    v[e] = a.init ? a.init[((int64_t)bh * D + i) * D + j] : 0.f;
                 }
+                st_halfrow_bf16(sm + OFF_MT + (cb >> 1) * 16384, j, cb & 1, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] *= gC;
+                tmem_st32(tl + TM_M + cb * 32, v);
             }
             tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(BAR_CHAIN, 128);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && n + 2 < NC) issue_tma(n + 2);
-    }
+        for (int n = 0; ok && n < NC; ++n) {
+            const int st = n & 1;
+            const int t0 = n * C;
+            const int c = min(C, T - t0);
+            const Scal S = scal(sm, st);
+            const float gC = s_gC[st];
+            uint8_t *kq = sm + OFF_KQ + st * KQ_BYTES;
+            uint8_t *vt = sm + OFF_V + st * V_BYTES;
+            const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
+            const bool last = (n + 1 == NC);
 
-    if (!ok && tid == 0) {
-        // A bounded wait gave up: record it, let this CTA's copies and MMAs in
-        // flight land (each wait bounded again), then release TMEM below.
-        atomicOr(&g_device_error_word, kDevErrTimeout);
-        if (tma_pending[0]) mbar_wait(btma0, tma_parity[0], kCleanupLimitNs);
-        if (tma_pending[1]) mbar_wait(btma1, tma_parity[1], kCleanupLimitNs);
-        if (mma_pending) mbar_wait(bmma, mma_phase, kCleanupLimitNs);
+            // W^T = U^T' - M^T Wk^T ;  O^T = M^T Q^T
+            ok = role_wait(bar(B_FULL0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
+            if (ok) ok = role_wait(bar(B_WKT), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + TM_W + st * 64,
+                             sdesc_sw128(sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             sdesc_sw128(sbase + OFF_WKT + kk * 2048, 16384, 1024), idesc_w, 1);
+                mma_commit(bar(B_W));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + TM_O,
+                             sdesc_sw128(sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             sdesc_sw128(kq_a + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             idesc_o, kk > 0);
+                issued = true;
+            }
+            ok = role_wait(bar(B_W), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            tc_fence_after();
+            {   // Wt^T[j][s] = (W^T'[j][s] + beta_s V[s][j]) * gamma_C / gamma_s  -> WtT (row j)
+                float v[64];
+                tmem_ld32(tl + TM_W + st * 64, *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(tl + TM_W + st * 64 + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                const uint8_t *vslab = vt + (j >> 6) * 8192;
+#pragma unroll
+                for (int s = 0; s < 64; ++s) {
+                    const float wv = fmaf(S.bs[s], ld_bf16_sw(vslab, s, j & 63), v[s]);
+                    v[s] = (s < c) ? wv * (gC * S.ig[s]) : 0.f;
+                }
+                st_row_bf16(sm + OFF_WTT, j, v);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(BAR_CHAIN, 128);
+            if (w == 0) {
+                mbar_arrive(bar(B_RWFREE0 + st));
+                tc_fence_after();
+                // M^T += Wt^T K ;  O^T += Wt^T P^T
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_M, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
+                             sdesc_sw128(kq_a + kk * 2048, 16384, 1024), idesc_d, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
+                             sdesc_sw128(sbase + OFF_P + st * 8192 + kk * 32, 16, 1024), idesc_o,
+                             1);
+                mma_commit(bar(B_D));
+            }
+
+            ok = role_wait(bar(B_D), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            if (ok && !last) {
+                ok = role_wait(bar(B_SCAL), scal_seen & 1u, a.limit_ns, &s_abort);
+                ++scal_seen;
+            }
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            tc_fence_after();
+            {   // state: MT <- bf16(M^T_{n+1}); TMEM M^T <- gamma_C(n+1) M^T_{n+1}
+                const float gn = last ? 1.f : s_gC[st ^ 1];
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float v[32];
+                    tmem_ld32(tl + TM_M + cb * 32, v);
+                    tmem_wait_ld();
+                    if (last) {
+                        if (a.final_state) {
+                            float *f = a.final_state + (int64_t)bh * D * D + j;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) f[(int64_t)(cb * 32 + e) * D] = v[e];
+                        }
+                    } else {
+                        st_halfrow_bf16(sm + OFF_MT + (cb >> 1) * 16384, j, cb & 1, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] *= gn;
+                        tmem_st32(tl + TM_M + cb * 32, v);
+                    }
+                }
+                tmem_wait_st();
+            }
+            {   // output: out[t0 + r][j] = gamma_r O^T[j][r], staged as a swizzled
+                // 64 x 128 bf16 tile in the consumed Q half of this input stage.
+                // Lanes pair up (j, j^1) so that each store writes two columns.
+                float v[64];
+                tmem_ld32(tl + TM_O, *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(tl + TM_O + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                uint8_t *ost = kq + 8192 + (j >> 6) * 16384;
+                const bool odd = lane & 1;
+                const uint32_t jc = (uint32_t)(j & 63) & ~1u;   // even column of the pair
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr) {
+                    const float x0 = v[2 * rr] * S.gam[2 * rr];
+                    const float x1 = v[2 * rr + 1] * S.gam[2 * rr + 1];
+                    const float other = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+                    const uint32_t row = 2 * rr + (odd ? 1 : 0);
+                    const uint32_t pk = odd ? pack_bf16x2(other, x1) : pack_bf16x2(x0, other);
+                    *reinterpret_cast<uint32_t *>(ost + sw128_offset(row, jc)) = pk;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(BAR_CHAIN, 128);
+            if (w == 0) mbar_arrive(bar(B_OSTAGE0 + st));
+        }
+        if (s_abort && w == 0 && issued) {
+            mma_commit(bar(B_DRAINC));
+            mbar_wait(bar(B_DRAINC), 0u, kCleanupLimitNs);
+        }
+    } else if (tid == 256) {
+        // ================================================================ copy
+        uint32_t issued[2] = {0, 0};
+        auto issue_tma = [&](int n) {
+            const int st = n & 1;
+            const uint32_t b = bar(B_FULL0 + st);
+            const uint32_t kq = sbase + OFF_KQ + st * KQ_BYTES;
+            const uint32_t vv = sbase + OFF_V + st * V_BYTES;
+            mbar_arrive_expect_tx(b, KQ_BYTES + V_BYTES);
+            tma_load_3d(kq + 0, &tm_k, b, 0, n * C, bh);
+            tma_load_3d(kq + 8192, &tm_q, b, 0, n * C, bh);
+            tma_load_3d(kq + 16384, &tm_k, b, 64, n * C, bh);
+            tma_load_3d(kq + 24576, &tm_q, b, 64, n * C, bh);
+            tma_load_3d(vv + 0, &tm_v, b, 0, n * C, bh);
+            tma_load_3d(vv + 8192, &tm_v, b, 64, n * C, bh);
+            ++issued[st];
+        };
+        issue_tma(0);
+        if (NC > 1) issue_tma(1);
+        for (int n = 0; n < NC; ++n) {
+            const int st = n & 1;
+            if (!role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort))
+                break;
+            const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
+            tma_store_3d(&tm_o, kq_a + 8192, 0, n * C, bh);
+            tma_store_3d(&tm_o, kq_a + 24576, 64, n * C, bh);
+            bulk_commit();
+            if (n + 2 < NC) {
+                bulk_wait_read_all();      // refill the stage once the store has read it
+                issue_tma(n + 2);
+            }
+        }
+        bulk_wait_all();
+        if (s_abort) {
+            // at most the latest load of each stage can still be in flight
+            for (int st = 0; st < 2; ++st)
+                if (issued[st] > 0)
+                    mbar_wait(bar(B_FULL0 + st), (issued[st] - 1) & 1u, kCleanupLimitNs);
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+    if (warp == 8) {
+        __syncwarp();
+        tmem_dealloc(tmem, TM_COLS);
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -606,7 +741,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [BH][T][128] bf16 viewed as a 3-D tensor; 64 x 64 boxes, 128-byte swizzle,
-// zero fill beyond T.
+// zero fill beyond T on loads, clipping beyond T on stores.
 bool make_map(CUtensorMap *m, const void *ptr, int BH, int T) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -642,18 +777,18 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
     if (BH == 0 || T == 0) return cudaSuccess;
     // TMA needs 16-byte aligned bases
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-         reinterpret_cast<uintptr_t>(v)) & 15)
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
         return cudaErrorMisalignedAddress;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T))
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
+        !make_map(&mo, out, BH, T))
         return cudaErrorInvalidValue;
-    FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, T,
-                wait_limit_ns()};
+    FusedArgs a{g, beta, init, final_state, a_min, T, wait_limit_ns()};
     cudaError_t e = cudaFuncSetAttribute(fused_prefill_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    fused_prefill_kernel<<<BH, NT, SMEM_ALLOC, s>>>(mq, mk, mv, a);
+    fused_prefill_kernel<<<BH, NT, SMEM_ALLOC, s>>>(mq, mk, mv, mo, a);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,40 @@
+"""Failure detection without a GPU fault: GDR_FAULT_INJECT=timeout makes every
+bounded wait of the fused kernel give up at once.  The kernel must unwind (let
+its own copies land, free TMEM, return), gdr_last_device_error must report
+GDR_ERR_TIMEOUT, and the context must stay usable for the next call."""
+from __future__ import annotations
+
+import os
+
+import pytest
+import torch
+
+import oracle
+import gated_delta_rule_gdr_gb300 as gdr
+from gated_delta_rule_gdr_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+def test_injected_timeout_is_reported_and_recovers():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdr.load(build_if_missing=True)
+    w = I.PREFILL.with_(B=1, H=2, T=300)
+    x = I.prefill_inputs(w, device="cuda")
+    assert gdr.last_device_error() == 0
+    os.environ["GDR_FAULT_INJECT"] = "timeout"
+    try:
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"])
+        assert gdr.last_device_error() == 5          # GDR_ERR_TIMEOUT
+    finally:
+        del os.environ["GDR_FAULT_INJECT"]
+    assert gdr.last_device_error() == 0              # the word was cleared
+    out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                             x["init_state"])
+    torch.cuda.synchronize()
+    cpu = {n: t.cpu() for n, t in x.items()}
+    ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,
+                        cpu["init_state"])
+    assert oracle.rel_l2(out, ro) <= 5e-3 and oracle.rel_l2(fin, rf) <= 5e-3
+    assert gdr.last_device_error() == 0
