@@ -26,16 +26,17 @@
 //   P   = lower_incl(Q K^T) / gamma_C
 //   O   = diag(gamma) (Q M_n + P Wt)
 //   M_{n+1} = gamma_C M_n + K^T Wt
-// Every product is computed transposed so that its M dimension is 128
+// The products are computed transposed so that their M dimension is 128
 // (dv or dk):  U^T = V^T Lb^T,  Wk^T = K^T Lbg^T,  W^T = U^T - M^T Wk^T,
-// O^T = M^T Q^T + Wt^T P^T,  M^T_{n+1} = gamma_C M^T + Wt^T K.
+// M^T_{n+1} = gamma_C M^T + Wt^T K -- except the output, O = Q M + P Wt, an
+// M = 64 product whose TMEM rows are whole output rows, so each row leaves the
+// SM as contiguous 16-byte stores without a transpose.
 //
 // Warp roles (288 threads):
 //   prep  (warps 0-3)  chunk k: decay, A and P from [K;Q]K^T, the triangular
 //                      solve, Lb / Lbg, then Wk^T          -- state-independent
 //   chain (warps 4-7)  chunk n: W^T epilogue, state update, output
-//   copy  (warp 8)     one lane issues the TMA loads of the inputs and the TMA
-//                      stores of the output
+//   copy  (warp 8)     one lane issues the TMA loads of the inputs
 // Each warpgroup issues its own tcgen05.mma from one elected thread, so the
 // preparation of chunk n+1 overlaps the state chain of chunk n.
 //
@@ -47,7 +48,8 @@
 //   WtT        16 KB  Wt^T bf16, K-major ([j][s])
 //   P[2]        8 KB each, K-major ([r][s]), one per stage
 //   Lb, Lbg     8 KB each, K-major ([r][s]), sharing space with the fp32 A
-// TMEM (fp32, 128 lanes): KQK^T 64 cols, W^T 2 x 64, Wk^T 64, O^T 64, M^T 128.
+// TMEM (fp32, 128 lanes): KQK^T 64 cols, W^T 2 x 64, Wk^T 64, M^T 128, and O
+// 128 cols in the M = 64 layout (row r in lane r % 16 + 32 (r / 16)).
 
 #include "gdr_internal.h"
 #include "gdr_math.cuh"
@@ -96,8 +98,8 @@ static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
 static_assert(OFF_AS % 1024 == 0 && 64 * LDA * 4 >= 16384, "Lb/Lbg must fit in A's space");
 
 // TMEM columns
-constexpr uint32_t TM_KQK = 0, TM_W = 64 /* two buffers */, TM_WK = 192, TM_O = 256,
-                   TM_M = 320;
+constexpr uint32_t TM_KQK = 0, TM_W = 64 /* two buffers */, TM_WK = 192, TM_O = 256 /* 128 */,
+                   TM_M = 384;
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
@@ -322,6 +324,7 @@ __device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *
 
 struct FusedArgs {
     const float *g, *beta, *init;
+    __nv_bfloat16 *out;
     float *final_state;
     float a_min;
     int T;
@@ -338,15 +341,14 @@ enum : int {
     B_SCAL,                    // prep: decay scalars of chunk k written
     B_WKT,                     // prep: Wk^T written (and U^T' in TMEM)
     B_RWFREE0, B_RWFREE1,      // chain: W^T buffer read out, per buffer
-    B_OSTAGE0, B_OSTAGE1,      // chain: output tile staged, input stage done with
+    B_OSTAGE0, B_OSTAGE1,      // chain: input stage (and its scalars) done with
     B_DRAINP, B_DRAINC,        // commits of the error path (prep, chain)
     NUM_BARS
 };
 
 __global__ void __launch_bounds__(NT, 1)
 fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                     const FusedArgs a) {
+                     const __grid_constant__ CUtensorMap tm_v, const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -376,7 +378,6 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_o);
         }
     }
     tc_fence_before();
@@ -390,7 +391,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
     const uint32_t idesc_u = idesc_bf16(128, 64, true, false);
     const uint32_t idesc_w = idesc_bf16(128, 64, false, true, true);
-    const uint32_t idesc_o = idesc_bf16(128, 64, false, false);
+    const uint32_t idesc_o = idesc_bf16(64, 128, false, false);
     const uint32_t idesc_d = idesc_bf16(128, 128, false, true);
 
     if (warp < 4) {
@@ -436,29 +437,30 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_PREP, 128, ok)) break;
             tc_fence_after();
-            {
-                float v[64];
-                tmem_ld32(tl + TM_KQK, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(tl + TM_KQK + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {     // 32 columns at a time
+                float v[32];
+                tmem_ld32(tl + TM_KQK + h * 32, v);
                 tmem_wait_ld();
                 if (w < 64) {
                     const int r = w;
                     const float br = (r < c) ? S.bg[r] : 0.f;
 #pragma unroll
-                    for (int s4 = 0; s4 < 64; s4 += 4) {
-                        const float4 ig4 = *reinterpret_cast<const float4 *>(&S.ig[s4]);
+                    for (int s4 = 0; s4 < 32; s4 += 4) {
+                        const int s0 = h * 32 + s4;
+                        const float4 ig4 = *reinterpret_cast<const float4 *>(&S.ig[s0]);
                         float4 o;
-                        o.x = (s4 + 0 < r) ? br * v[s4 + 0] * ig4.x : 0.f;
-                        o.y = (s4 + 1 < r) ? br * v[s4 + 1] * ig4.y : 0.f;
-                        o.z = (s4 + 2 < r) ? br * v[s4 + 2] * ig4.z : 0.f;
-                        o.w = (s4 + 3 < r) ? br * v[s4 + 3] * ig4.w : 0.f;
-                        *reinterpret_cast<float4 *>(&As[r * LDA + s4]) = o;
+                        o.x = (s0 + 0 < r) ? br * v[s4 + 0] * ig4.x : 0.f;
+                        o.y = (s0 + 1 < r) ? br * v[s4 + 1] * ig4.y : 0.f;
+                        o.z = (s0 + 2 < r) ? br * v[s4 + 2] * ig4.z : 0.f;
+                        o.w = (s0 + 3 < r) ? br * v[s4 + 3] * ig4.w : 0.f;
+                        *reinterpret_cast<float4 *>(&As[r * LDA + s0]) = o;
                     }
                 } else {
                     const int r = w - 64;
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) v[s] = (s <= r && r < c) ? v[s] * igC : 0.f;
-                    st_row_bf16(sm + OFF_P + st * 8192, r, v);
+                    for (int e = 0; e < 32; ++e) v[e] = (h * 32 + e <= r && r < c) ? v[e] * igC : 0.f;
+                    st_halfrow_bf16(sm + OFF_P + st * 8192, r, h, v);
                 }
             }
             fence_proxy_async_smem();
@@ -469,17 +471,22 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             {   // Lb = (T - I) diag(beta), Lbg = (T - I) diag(beta gamma), bf16 rows
                 const int r = w & 63;
                 const float *sc = (w < 64) ? S.bs : S.bg;
-                float v[64];
+                uint8_t *dst = sm + ((w < 64) ? OFF_LB : OFF_LBG);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[32];
 #pragma unroll
-                for (int s4 = 0; s4 < 64; s4 += 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s4]);
-                    const float4 f = *reinterpret_cast<const float4 *>(&sc[s4]);
-                    v[s4 + 0] = (s4 + 0 < r) ? t.x * f.x : 0.f;
-                    v[s4 + 1] = (s4 + 1 < r) ? t.y * f.y : 0.f;
-                    v[s4 + 2] = (s4 + 2 < r) ? t.z * f.z : 0.f;
-                    v[s4 + 3] = (s4 + 3 < r) ? t.w * f.w : 0.f;
+                    for (int s4 = 0; s4 < 32; s4 += 4) {
+                        const int s0 = h * 32 + s4;
+                        const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s0]);
+                        const float4 f = *reinterpret_cast<const float4 *>(&sc[s0]);
+                        v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : 0.f;
+                        v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
+                        v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
+                        v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
+                    }
+                    st_halfrow_bf16(dst, r, h, v);
                 }
-                st_row_bf16(sm + ((w < 64) ? OFF_LB : OFF_LBG), r, v);
             }
             fence_proxy_async_smem();
             // U^T' = V^T Lb^T into W^T buffer st (free once the chain read chunk k-2's W^T)
@@ -506,14 +513,17 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after();
             {
                 const int i = w;
-                float v[64];
-                tmem_ld32(tl + TM_WK, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(tl + TM_WK + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-                tmem_wait_ld();
                 const uint8_t *kslab = kq + (i >> 6) * 16384;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[32];
+                    tmem_ld32(tl + TM_WK + h * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int r = 0; r < 64; ++r) v[r] = fmaf(S.bg[r], ld_bf16_sw(kslab, r, i & 63), v[r]);
-                st_row_bf16(sm + OFF_WKT, i, v);
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = fmaf(S.bg[h * 32 + e], ld_bf16_sw(kslab, h * 32 + e, i & 63), v[e]);
+                    st_halfrow_bf16(sm + OFF_WKT, i, h, v);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -566,7 +576,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
             const bool last = (n + 1 == NC);
 
-            // W^T = U^T' - M^T Wk^T ;  O^T = M^T Q^T
+            // W^T = U^T' - M^T Wk^T ;  O = Q M
             ok = role_wait(bar(B_FULL0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
             if (ok) ok = role_wait(bar(B_WKT), (uint32_t)n & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
@@ -581,8 +591,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tmem + TM_O,
-                             sdesc_sw128(sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                              sdesc_sw128(kq_a + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             sdesc_sw128(sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                              idesc_o, kk > 0);
                 issued = true;
             }
@@ -590,17 +600,20 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
             {   // Wt^T[j][s] = (W^T'[j][s] + beta_s V[s][j]) * gamma_C / gamma_s  -> WtT (row j)
-                float v[64];
-                tmem_ld32(tl + TM_W + st * 64, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(tl + TM_W + st * 64 + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-                tmem_wait_ld();
                 const uint8_t *vslab = vt + (j >> 6) * 8192;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[32];
+                    tmem_ld32(tl + TM_W + st * 64 + h * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int s = 0; s < 64; ++s) {
-                    const float wv = fmaf(S.bs[s], ld_bf16_sw(vslab, s, j & 63), v[s]);
-                    v[s] = (s < c) ? wv * (gC * S.ig[s]) : 0.f;
+                    for (int e = 0; e < 32; ++e) {
+                        const int s = h * 32 + e;
+                        const float wv = fmaf(S.bs[s], ld_bf16_sw(vslab, s, j & 63), v[e]);
+                        v[e] = (s < c) ? wv * (gC * S.ig[s]) : 0.f;
+                    }
+                    st_halfrow_bf16(sm + OFF_WTT, j, h, v);
                 }
-                st_row_bf16(sm + OFF_WTT, j, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -608,16 +621,15 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (w == 0) {
                 mbar_arrive(bar(B_RWFREE0 + st));
                 tc_fence_after();
-                // M^T += Wt^T K ;  O^T += Wt^T P^T
+                // M^T += Wt^T K ;  O += P Wt
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM_M, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
                              sdesc_sw128(kq_a + kk * 2048, 16384, 1024), idesc_d, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
-                             sdesc_sw128(sbase + OFF_P + st * 8192 + kk * 32, 16, 1024), idesc_o,
-                             1);
+                    mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_P + st * 8192 + kk * 32, 16, 1024),
+                             sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024), idesc_o, 1);
                 mma_commit(bar(B_D));
             }
 
@@ -650,27 +662,30 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 }
                 tmem_wait_st();
             }
-            {   // output: out[t0 + r][j] = gamma_r O^T[j][r], staged as a swizzled
-                // 64 x 128 bf16 tile in the consumed Q half of this input stage.
-                // Lanes pair up (j, j^1) so that each store writes two columns.
-                float v[64];
-                tmem_ld32(tl + TM_O, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(tl + TM_O + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-                tmem_wait_ld();
-                uint8_t *ost = kq + 8192 + (j >> 6) * 16384;
-                const bool odd = lane & 1;
-                const uint32_t jc = (uint32_t)(j & 63) & ~1u;   // even column of the pair
+            {   // output row r = gamma_r O[r][:]: lanes 0..15 of each quadrant hold
+                // rows 16 q .. 16 q + 15 (the M = 64 TMEM layout), 128 columns each
+                const int r = 16 * (warp - 4) + (lane & 15);
+                const bool has_row = (lane < 16) && (r < c);
+                const float gr = S.gam[r];
+                uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + t0 + r) * D);
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float v[32];
+                    tmem_ld32(tl + TM_O + cb * 32, v);    // warp-wide; lanes 16..31 unused
+                    tmem_wait_ld();
+                    if (has_row) {
 #pragma unroll
-                for (int rr = 0; rr < 32; ++rr) {
-                    const float x0 = v[2 * rr] * S.gam[2 * rr];
-                    const float x1 = v[2 * rr + 1] * S.gam[2 * rr + 1];
-                    const float other = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
-                    const uint32_t row = 2 * rr + (odd ? 1 : 0);
-                    const uint32_t pk = odd ? pack_bf16x2(other, x1) : pack_bf16x2(x0, other);
-                    *reinterpret_cast<uint32_t *>(ost + sw128_offset(row, jc)) = pk;
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 u;
+                            u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
+                            u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
+                            u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
+                            u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+                            __stcs(orow + cb * 4 + q4, u);
+                        }
+                    }
                 }
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             named_sync(BAR_CHAIN, 128);
             if (w == 0) mbar_arrive(bar(B_OSTAGE0 + st));
@@ -698,20 +713,12 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         };
         issue_tma(0);
         if (NC > 1) issue_tma(1);
-        for (int n = 0; n < NC; ++n) {
+        for (int n = 0; n + 2 < NC; ++n) {   // refill a stage once chunk n is done with it
             const int st = n & 1;
             if (!role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort))
                 break;
-            const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
-            tma_store_3d(&tm_o, kq_a + 8192, 0, n * C, bh);
-            tma_store_3d(&tm_o, kq_a + 24576, 64, n * C, bh);
-            bulk_commit();
-            if (n + 2 < NC) {
-                bulk_wait_read_all();      // refill the stage once the store has read it
-                issue_tma(n + 2);
-            }
+            issue_tma(n + 2);
         }
-        bulk_wait_all();
         if (s_abort) {
             // at most the latest load of each stage can still be in flight
             for (int st = 0; st < 2; ++st)
@@ -741,7 +748,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [BH][T][128] bf16 viewed as a 3-D tensor; 64 x 64 boxes, 128-byte swizzle,
-// zero fill beyond T on loads, clipping beyond T on stores.
+// zero fill beyond T.
 bool make_map(CUtensorMap *m, const void *ptr, int BH, int T) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -775,20 +782,20 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
     if (!fused_supported(dk, dv, C_, Elem::BF16)) return cudaErrorInvalidValue;
     const int BH = B * H;
     if (BH == 0 || T == 0) return cudaSuccess;
-    // TMA needs 16-byte aligned bases
+    // TMA needs 16-byte aligned bases; the output rows are written as 16-byte vectors
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
         return cudaErrorMisalignedAddress;
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
-        !make_map(&mo, out, BH, T))
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T))
         return cudaErrorInvalidValue;
-    FusedArgs a{g, beta, init, final_state, a_min, T, wait_limit_ns()};
+    FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, T,
+                wait_limit_ns()};
     cudaError_t e = cudaFuncSetAttribute(fused_prefill_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    fused_prefill_kernel<<<BH, NT, SMEM_ALLOC, s>>>(mq, mk, mv, mo, a);
+    fused_prefill_kernel<<<BH, NT, SMEM_ALLOC, s>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 
