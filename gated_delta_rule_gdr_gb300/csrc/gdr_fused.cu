@@ -19,8 +19,9 @@
 // Algebra per chunk (rows r, s; gamma, 1/gamma, gamma_C as usual; M = S^T):
 //   A   = strict_lower(diag(beta gamma) K K^T diag(1/gamma)),  T = (I + A)^-1
 //   L   = T - I (strictly lower);  Lb = L diag(beta),  Lbg = L diag(beta gamma)
-//   U   = diag(beta) V + Lb V                        (identity part kept exact)
-//   Wk  = diag(beta gamma) K + Lbg K
+//   U   = (Lb + diag(beta)) V,  Wk = (Lbg + diag(beta gamma)) K, where each
+//         diagonal is split into its bf16 value plus a bf16 residual applied
+//         by a second product, so the identity part stays exact to ~2^-17
 //   W   = U - Wk M_n
 //   Wt  = diag(gamma_C / gamma) W
 //   P   = lower_incl(Q K^T) / gamma_C
@@ -33,10 +34,10 @@
 // SM as contiguous 16-byte stores without a transpose.
 //
 // Warp roles (288 threads):
-//   prep  (warps 0-3)  chunk k: decay, A and P from [K;Q]K^T, the triangular
-//                      solve, Lb / Lbg, then Wk^T          -- state-independent
-//   chain (warps 4-7)  chunk n: W^T epilogue, state update, output
-//   copy  (warp 8)     one lane issues the TMA loads of the inputs
+//   prep  (warps 0-3)  chunk k: A and P from [K;Q]K^T, the triangular solve,
+//                      Lb / Lbg and the U^T, Wk^T products -- state-independent
+//   chain (warps 4-7)  chunk n: Wk^T to bf16, W^T epilogue, state update, output
+//   copy  (warp 8)     the TMA loads of the inputs and the cumulative decay
 // Each warpgroup issues its own tcgen05.mma from one elected thread, so the
 // preparation of chunk n+1 overlaps the state chain of chunk n.
 //
@@ -48,6 +49,7 @@
 //   WtT        16 KB  Wt^T bf16, K-major ([j][s])
 //   P[2]        8 KB each, K-major ([r][s]), one per stage
 //   Lb, Lbg     8 KB each, K-major ([r][s]), sharing space with the fp32 A
+//   Db, Dbg     8 KB each, the diagonal residuals, sharing space with the fp32 T
 // TMEM (fp32, 128 lanes): KQK^T 64 cols, W^T 2 x 64, Wk^T 64, M^T 128, and O
 // 128 cols in the M = 64 layout (row r in lane r % 16 + 32 (r / 16)).
 
@@ -88,14 +90,18 @@ constexpr int LDA = 68;                    // fp32 row stride of the solve matri
 constexpr uint32_t OFF_AS = 180224;        // 64 x 68 fp32; Lb, Lbg reuse its first 16 KB
 constexpr uint32_t OFF_LB = OFF_AS;
 constexpr uint32_t OFF_LBG = OFF_AS + 8192;
-constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;   // 64 x 68 fp32
+constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;   // 64 x 68 fp32; Db, Dbg reuse it
+constexpr uint32_t OFF_DB = OFF_TS;
+constexpr uint32_t OFF_DBG = OFF_TS + 8192;
 constexpr int LDY = 40;                    // row stride of the merge scratch
 constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;   // 32 x 40 fp32
-constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;   // scalars: 2 stages x 4 x 64 fp32
-constexpr uint32_t SMEM_USED = OFF_SC + 2 * 4 * 64 * 4;
+constexpr int NSCAL = 3;                   // scalar slots (chunk m uses slot m % 3)
+constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;   // scalars: 3 slots x 5 x 64 fp32
+constexpr uint32_t SMEM_USED = OFF_SC + NSCAL * 5 * 64 * 4;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
 static_assert(OFF_AS % 1024 == 0 && 64 * LDA * 4 >= 16384, "Lb/Lbg must fit in A's space");
+static_assert(OFF_TS % 1024 == 0, "Db/Dbg must be 1024-byte aligned");
 
 // TMEM columns
 constexpr uint32_t TM_KQK = 0, TM_W = 64 /* two buffers */, TM_WK = 192, TM_O = 256 /* 128 */,
@@ -105,30 +111,17 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
 
 struct Scal {   // per-stage per-row scalars of one chunk
-    float *gam, *ig, *bs, *bg;
+    float *gam, *ig, *bs, *bg, *sc;   // gamma, 1/gamma, beta, beta gamma, gamma_C / gamma
 };
 
-__device__ __forceinline__ Scal scal(uint8_t *sm, int stage) {
-    float *b = reinterpret_cast<float *>(sm + OFF_SC) + stage * 4 * 64;
-    return {b, b + 64, b + 128, b + 192};
+__device__ __forceinline__ Scal scal(uint8_t *sm, int slot) {
+    float *b = reinterpret_cast<float *>(sm + OFF_SC) + slot * 5 * 64;
+    return {b, b + 64, b + 128, b + 192, b + 256};
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Write 64 fp32 values as one 128-byte bf16 row of a 128B-swizzled tile.
-__device__ __forceinline__ void st_row_bf16(uint8_t *tile, uint32_t row, const float *v) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint4 u;
-        u.x = pack_bf16x2(v[ch * 8 + 0], v[ch * 8 + 1]);
-        u.y = pack_bf16x2(v[ch * 8 + 2], v[ch * 8 + 3]);
-        u.z = pack_bf16x2(v[ch * 8 + 4], v[ch * 8 + 5]);
-        u.w = pack_bf16x2(v[ch * 8 + 6], v[ch * 8 + 7]);
-        *reinterpret_cast<uint4 *>(tile + row * 128u + ((ch ^ (row & 7u)) << 4)) = u;
-    }
 }
 
 // Write 32 fp32 values as half a 128-byte bf16 row (chunks 4h..4h+3).
@@ -146,15 +139,16 @@ __device__ __forceinline__ void st_halfrow_bf16(uint8_t *tile, uint32_t row, uin
     }
 }
 
-__device__ __forceinline__ float ld_bf16_sw(const uint8_t *tile, uint32_t row, uint32_t col) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_offset(row, col)));
-}
-
 // Bounded wait used by the warpgroups: gives up when the CTA-wide abort flag
 // is raised or the time limit passes (then raises the flag and the error word).
 __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;      // non-blocking first look
+    if (limit_ns == 0) {                                // injected timeout: give up at once
+        *abort = 1;
+        atomicOr(&g_device_error_word, kDevErrTimeout);
+        return false;
+    }
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -167,34 +161,41 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
-// Cumulative decay of one chunk by the prep warpgroup (threads w < 64 hold row
-// w's g and beta).  Contains two prep-group barriers.
-__device__ __forceinline__ void chunk_decay(int w, float gv, float bv, int c, float a_min,
-                                            Scal s, float *s_part, float *s_gC) {
-    const int lane = w & 31, warp = w >> 5;
-    float incl = 0.f;
-    if (w < 64) {
-        incl = (w < c) ? log_alpha(gv, a_min) : 0.f;
+// Cumulative decay of one chunk by one warp (lane l owns rows 2l, 2l+1, whose
+// g and beta it already holds): alpha = a_min + (1 - a_min) sigmoid(g), the
+// inclusive scan of log alpha, gamma = exp(scan), 1/gamma, beta, beta gamma,
+// gamma_C (the last valid row) and gamma_C / gamma.  Rows past the chunk's end
+// get gamma = 1, beta = 0 and gamma_C / gamma = 0 so that they drop out of
+// every product.
+__device__ __forceinline__ void warp_decay(int lane, const float (&gv)[2], const float (&bv)[2],
+                                           int c, float a_min, Scal s, float *s_gC) {
+    const int r0 = 2 * lane;
+    const float l0 = (r0 < c) ? log_alpha(gv[0], a_min) : 0.f;
+    const float l1 = (r0 + 1 < c) ? log_alpha(gv[1], a_min) : 0.f;
+    float incl = l0 + l1;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        if (lane == 31) s_part[warp] = incl;
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
     }
-    named_sync(BAR_PREP, 128);
-    if (w < 64) {
-        if (warp == 1) incl += s_part[0];
-        const bool valid = w < c;
-        const float gam = valid ? expf(incl) : 1.f;
-        const float b = valid ? bv : 0.f;
-        s.gam[w] = gam;
-        s.ig[w] = 1.f / gam;
-        s.bs[w] = b;
-        s.bg[w] = b * gam;
-        if (w == c - 1) *s_gC = gam;
+    const float b1 = incl, b0 = incl - l1;
+    // gamma_C: the scan value of row c - 1, held by lane (c - 1) / 2
+    const float bC = __shfl_sync(0xffffffffu, ((c - 1) & 1) ? b1 : b0, (c - 1) >> 1);
+    const float gC = expf(bC);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = r0 + e;
+        const bool valid = r < c;
+        const float gam = valid ? expf(e ? b1 : b0) : 1.f;
+        const float b = valid ? bv[e] : 0.f;
+        s.gam[r] = gam;
+        s.ig[r] = 1.f / gam;
+        s.bs[r] = b;
+        s.bg[r] = b * gam;
+        s.sc[r] = valid ? gC / gam : 0.f;
     }
-    named_sync(BAR_PREP, 128);
+    if (lane == 0) *s_gC = gC;
+    __syncwarp();
 }
 
 // tf32 warp-level MMA (m16n8k8) for the small merge products of the solve.
@@ -338,10 +339,10 @@ enum : int {
     B_UWK,                     // prep commit: U^T', Wk^T' done
     B_W,                       // chain commit: W^T done
     B_D,                       // chain commit: M^T update, O^T done
-    B_SCAL,                    // prep: decay scalars of chunk k written
-    B_WKT,                     // prep: Wk^T written (and U^T' in TMEM)
+    B_SCAL0, B_SCAL1, B_SCAL2, // copy: decay scalars of a chunk written, per slot
+    B_WKFREE,                  // chain: Wk^T of a chunk read out of TMEM
     B_RWFREE0, B_RWFREE1,      // chain: W^T buffer read out, per buffer
-    B_OSTAGE0, B_OSTAGE1,      // chain: input stage (and its scalars) done with
+    B_OSTAGE0, B_OSTAGE1,      // chain: input stage done with (its MMAs complete)
     B_DRAINP, B_DRAINC,        // commits of the error path (prep, chain)
     NUM_BARS
 };
@@ -355,8 +356,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t sbase = smem_u32(sm);
     __shared__ __align__(8) uint64_t s_bar[NUM_BARS];
     __shared__ uint32_t s_tmem;
-    __shared__ float s_part[2];
-    __shared__ float s_gC[2];
+    __shared__ float s_gC[NSCAL];
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -399,16 +399,10 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int w = tid;
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
         bool issued = false;
-        float g_next = 0.f, b_next = 0.f;
-        if (w < min(C, T)) {
-            g_next = a.g[row_base + w];
-            b_next = a.beta[row_base + w];
-        }
         for (int k = 0; k < NC; ++k) {
-            const int st = k & 1;
+            const int st = k & 1, sl = k % NSCAL;
             const int c = min(C, T - k * C);
-            const Scal S = scal(sm, st);
-            uint8_t *kq = sm + OFF_KQ + st * KQ_BYTES;
+            const Scal S = scal(sm, sl);
             const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
             const uint32_t v_a = sbase + OFF_V + st * V_BYTES;
 
@@ -425,17 +419,14 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mma_commit(bar(B_KQK));
                 issued = true;
             }
-            chunk_decay(w, g_next, b_next, c, a.a_min, S, s_part, &s_gC[st]);
-            if (w == 0) mbar_arrive(bar(B_SCAL));
-            if (k + 1 < NC && w < min(C, T - (k + 1) * C)) {
-                g_next = a.g[row_base + (int64_t)(k + 1) * C + w];
-                b_next = a.beta[row_base + (int64_t)(k + 1) * C + w];
-            }
-            const float igC = 1.f / s_gC[st];
 
             // A = strict_lower(diag(beta gamma) K K^T diag(1/gamma)), P = lower(Q K^T) / gamma_C
-            ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
+            ok = role_wait(bar(B_SCAL0 + sl), (uint32_t)(k / NSCAL) & 1u, a.limit_ns, &s_abort);
+            if (ok) ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
+            // A's space holds Lb / Lbg of chunk k-1 until its U / Wk products are done
+            if (ok && k > 0) ok = role_wait(bar(B_UWK), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_PREP, 128, ok)) break;
+            const float igC = 1.f / s_gC[sl];
             tc_fence_after();
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {     // 32 columns at a time
@@ -480,18 +471,38 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                         const int s0 = h * 32 + s4;
                         const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s0]);
                         const float4 f = *reinterpret_cast<const float4 *>(&sc[s0]);
-                        v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : 0.f;
-                        v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
-                        v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
-                        v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
+                        v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : (s0 + 0 == r ? f.x : 0.f);
+                        v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : (s0 + 1 == r ? f.y : 0.f);
+                        v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : (s0 + 2 == r ? f.z : 0.f);
+                        v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : (s0 + 3 == r ? f.w : 0.f);
                     }
                     st_halfrow_bf16(dst, r, h, v);
                 }
             }
+            named_sync(BAR_PREP, 128);     // T is read out; its space takes the residuals
+            {   // Db = diag(beta - bf16(beta)), Dbg = diag(beta gamma - bf16(beta gamma))
+                const int r = w & 63;
+                const float x = (w < 64) ? S.bs[r] : S.bg[r];
+                const float lo = x - __bfloat162float(__float2bfloat16_rn(x));
+                uint8_t *dst = sm + ((w < 64) ? OFF_DB : OFF_DBG);
+                const __nv_bfloat16 lo16 = __float2bfloat16_rn(lo);
+                const uint32_t lo_bits = (uint32_t)*reinterpret_cast<const unsigned short *>(&lo16);
+                const uint32_t word = lo_bits << (16 * (r & 1));
+                const int wi = (r & 7) >> 1;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const bool here = (r >> 3) == ch;
+                    *reinterpret_cast<uint4 *>(dst + r * 128u + ((ch ^ (r & 7u)) << 4)) =
+                        make_uint4(here && wi == 0 ? word : 0u, here && wi == 1 ? word : 0u,
+                                   here && wi == 2 ? word : 0u, here && wi == 3 ? word : 0u);
+                }
+            }
             fence_proxy_async_smem();
-            // U^T' = V^T Lb^T into W^T buffer st (free once the chain read chunk k-2's W^T)
+            // U^T = V^T (Lb + Db)^T into W^T buffer st (free once the chain read chunk k-2's
+            // W^T);  Wk^T = K^T (Lbg + Dbg)^T
             ok = (k < 2) || role_wait(bar(B_RWFREE0 + st), (uint32_t)((k - 2) >> 1) & 1u,
                                       a.limit_ns, &s_abort);
+            if (ok && k > 0) ok = role_wait(bar(B_WKFREE), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_PREP, 128, ok)) break;
             if (w == 0) {
                 tc_fence_after();
@@ -501,34 +512,19 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                              sdesc_sw128(sbase + OFF_LB + kk * 32, 16, 1024), idesc_u, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_W + st * 64, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
+                             sdesc_sw128(sbase + OFF_DB + kk * 32, 16, 1024), idesc_u, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM_WK, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
                              sdesc_sw128(sbase + OFF_LBG + kk * 32, 16, 1024), idesc_u, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_WK, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
+                             sdesc_sw128(sbase + OFF_DBG + kk * 32, 16, 1024), idesc_u, 1);
                 mma_commit(bar(B_UWK));
             }
 
-            // Wk^T[i][r] = Wk^T'[i][r] + beta_r gamma_r K[r][i]  ->  WkT (MN-major, row i)
-            ok = role_wait(bar(B_UWK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
-            if (ok && k > 0) ok = role_wait(bar(B_W), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_PREP, 128, ok)) break;
-            tc_fence_after();
-            {
-                const int i = w;
-                const uint8_t *kslab = kq + (i >> 6) * 16384;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[32];
-                    tmem_ld32(tl + TM_WK + h * 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = fmaf(S.bg[h * 32 + e], ld_bf16_sw(kslab, h * 32 + e, i & 63), v[e]);
-                    st_halfrow_bf16(sm + OFF_WKT, i, h, v);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(BAR_PREP, 128);
-            if (w == 0) mbar_arrive(bar(B_WKT));
         }
         if (s_abort && w == 0 && issued) {   // let this thread's MMAs land before TMEM goes away
             mma_commit(bar(B_DRAINP));
@@ -541,9 +537,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int lane = w & 31;
         const uint32_t tl = tmem + ((uint32_t)((warp - 4) * 32) << 16);
         bool issued = false;
-        bool ok = role_wait(bar(B_SCAL), 0u, a.limit_ns, &s_abort);
+        bool ok = role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
         ok = named_and(BAR_CHAIN, 128, ok);
-        uint32_t scal_seen = 1;    // phases of B_SCAL observed
         if (ok) {
             // initial state: TMEM M^T <- gamma_C(0) M0^T, MT <- bf16(M0^T)
             const float gC = s_gC[0];
@@ -566,21 +561,31 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             named_sync(BAR_CHAIN, 128);
         }
         for (int n = 0; ok && n < NC; ++n) {
-            const int st = n & 1;
+            const int st = n & 1, sl = n % NSCAL, sl1 = (n + 1) % NSCAL;
             const int t0 = n * C;
             const int c = min(C, T - t0);
-            const Scal S = scal(sm, st);
-            const float gC = s_gC[st];
-            uint8_t *kq = sm + OFF_KQ + st * KQ_BYTES;
-            uint8_t *vt = sm + OFF_V + st * V_BYTES;
+            const Scal S = scal(sm, sl);
             const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
             const bool last = (n + 1 == NC);
 
-            // W^T = U^T' - M^T Wk^T ;  O = Q M
+            // ---- Wk^T -> WkT (bf16, MN-major, row i = this lane)
             ok = role_wait(bar(B_FULL0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
-            if (ok) ok = role_wait(bar(B_WKT), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            if (ok) ok = role_wait(bar(B_UWK), (uint32_t)n & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                tmem_ld32(tl + TM_WK + h * 32, v);
+                tmem_wait_ld();
+                st_halfrow_bf16(sm + OFF_WKT, w, h, v);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(BAR_CHAIN, 128);
+            // ---- W^T = U^T - M^T Wk^T ;  O = Q M
             if (w == 0) {
+                mbar_arrive(bar(B_WKFREE));
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
@@ -596,24 +601,25 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                              idesc_o, kk > 0);
                 issued = true;
             }
+
+            // ---- Wt^T[j][s] = W^T[j][s] * gamma_C / gamma_s -> WtT (row j); then D(n)
             ok = role_wait(bar(B_W), (uint32_t)n & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
-            {   // Wt^T[j][s] = (W^T'[j][s] + beta_s V[s][j]) * gamma_C / gamma_s  -> WtT (row j)
-                const uint8_t *vslab = vt + (j >> 6) * 8192;
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[32];
-                    tmem_ld32(tl + TM_W + st * 64 + h * 32, v);
-                    tmem_wait_ld();
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                tmem_ld32(tl + TM_W + st * 64 + h * 32, v);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int s = h * 32 + e;
-                        const float wv = fmaf(S.bs[s], ld_bf16_sw(vslab, s, j & 63), v[e]);
-                        v[e] = (s < c) ? wv * (gC * S.ig[s]) : 0.f;
-                    }
-                    st_halfrow_bf16(sm + OFF_WTT, j, h, v);
+                for (int e4 = 0; e4 < 32; e4 += 4) {
+                    const float4 f = *reinterpret_cast<const float4 *>(&S.sc[h * 32 + e4]);
+                    v[e4 + 0] *= f.x;
+                    v[e4 + 1] *= f.y;
+                    v[e4 + 2] *= f.z;
+                    v[e4 + 3] *= f.w;
                 }
+                st_halfrow_bf16(sm + OFF_WTT, j, h, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -633,15 +639,17 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mma_commit(bar(B_D));
             }
 
+            // ---- state: MT <- bf16(M^T_{n+1}); TMEM M^T <- gamma_C(n+1) M^T_{n+1}
             ok = role_wait(bar(B_D), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-            if (ok && !last) {
-                ok = role_wait(bar(B_SCAL), scal_seen & 1u, a.limit_ns, &s_abort);
-                ++scal_seen;
-            }
+            // every MMA that reads this input stage is complete: let the copy warp refill it
+            if (w == 0 && ok) mbar_arrive(bar(B_OSTAGE0 + st));
+            if (ok && !last)
+                ok = role_wait(bar(B_SCAL0 + sl1), (uint32_t)((n + 1) / NSCAL) & 1u, a.limit_ns,
+                               &s_abort);
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
-            {   // state: MT <- bf16(M^T_{n+1}); TMEM M^T <- gamma_C(n+1) M^T_{n+1}
-                const float gn = last ? 1.f : s_gC[st ^ 1];
+            {
+                const float gn = last ? 1.f : s_gC[sl1];
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     float v[32];
@@ -662,8 +670,9 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 }
                 tmem_wait_st();
             }
-            {   // output row r = gamma_r O[r][:]: lanes 0..15 of each quadrant hold
-                // rows 16 q .. 16 q + 15 (the M = 64 TMEM layout), 128 columns each
+            // ---- output row r = gamma_r O[r][:]: lanes 0..15 of each quadrant hold
+            // rows 16 q .. 16 q + 15 (the M = 64 TMEM layout), 128 columns each
+            {
                 const int r = 16 * (warp - 4) + (lane & 15);
                 const bool has_row = (lane < 16) && (r < c);
                 const float gr = S.gam[r];
@@ -686,18 +695,19 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     }
                 }
             }
+            fence_proxy_async_smem();
             tc_fence_before();
             named_sync(BAR_CHAIN, 128);
-            if (w == 0) mbar_arrive(bar(B_OSTAGE0 + st));
         }
         if (s_abort && w == 0 && issued) {
             mma_commit(bar(B_DRAINC));
             mbar_wait(bar(B_DRAINC), 0u, kCleanupLimitNs);
         }
-    } else if (tid == 256) {
+    } else {
         // ================================================================ copy
+        const int lane = tid & 31;
         uint32_t issued[2] = {0, 0};
-        auto issue_tma = [&](int n) {
+        auto issue_tma = [&](int n) {     // lane 0 only
             const int st = n & 1;
             const uint32_t b = bar(B_FULL0 + st);
             const uint32_t kq = sbase + OFF_KQ + st * KQ_BYTES;
@@ -711,15 +721,35 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_load_3d(vv + 8192, &tm_v, b, 64, n * C, bh);
             ++issued[st];
         };
-        issue_tma(0);
-        if (NC > 1) issue_tma(1);
+        auto load_gb = [&](int n, float (&gv)[2], float (&bv)[2]) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = n * C + 2 * lane + e;
+                gv[e] = (t < T) ? a.g[row_base + t] : 0.f;
+                bv[e] = (t < T) ? a.beta[row_base + t] : 0.f;
+            }
+        };
+        auto decay = [&](int n, const float (&gv)[2], const float (&bv)[2]) {
+            const int sl = n % NSCAL;
+            warp_decay(lane, gv, bv, min(C, T - n * C), a.a_min, scal(sm, sl), &s_gC[sl]);
+            if (lane == 0) mbar_arrive(bar(B_SCAL0 + sl));
+        };
+        float gv[2], bv[2];
+        for (int n = 0; n < 2 && n < NC; ++n) {
+            load_gb(n, gv, bv);
+            if (lane == 0) issue_tma(n);
+            decay(n, gv, bv);
+        }
+        if (NC > 2) load_gb(2, gv, bv);
         for (int n = 0; n + 2 < NC; ++n) {   // refill a stage once chunk n is done with it
             const int st = n & 1;
-            if (!role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort))
-                break;
-            issue_tma(n + 2);
+            bool ok = role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) issue_tma(n + 2);
+            decay(n + 2, gv, bv);
+            if (n + 3 < NC) load_gb(n + 3, gv, bv);
         }
-        if (s_abort) {
+        if (s_abort && lane == 0) {
             // at most the latest load of each stage can still be in flight
             for (int st = 0; st < 2; ++st)
                 if (issued[st] > 0)
