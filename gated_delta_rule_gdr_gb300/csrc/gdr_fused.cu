@@ -33,11 +33,11 @@
 // M = 64 product whose TMEM rows are whole output rows, so each row leaves the
 // SM as contiguous 16-byte stores without a transpose.
 //
-// Warp roles (288 threads):
-//   prep  (warps 0-3)  chunk k: A and P from [K;Q]K^T, the triangular solve,
+// Warp roles (416 threads):
+//   prep  (warps 0-7)  chunk k: A and P from [K;Q]K^T, the triangular solve,
 //                      Lb / Lbg and the U^T, Wk^T products -- state-independent
-//   chain (warps 4-7)  chunk n: Wk^T to bf16, W^T epilogue, state update, output
-//   copy  (warp 8)     the TMA loads of the inputs and the cumulative decay
+//   chain (warps 8-11) chunk n: Wk^T to bf16, W^T epilogue, state update, output
+//   copy  (warp 12)    the TMA loads of the inputs and the cumulative decay
 // Each warpgroup issues its own tcgen05.mma from one elected thread, so the
 // preparation of chunk n+1 overlaps the state chain of chunk n.
 //
@@ -74,7 +74,8 @@ using namespace sm100;
 
 constexpr int C = 64;      // chunk
 constexpr int D = 128;     // dk = dv
-constexpr int NT = 288;    // prep (128) + chain (128) + issue (32)
+constexpr int NT = 416;    // prep (256) + chain (128) + copy (32)
+constexpr int NPREP = 256;
 constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;   // named barriers (0 is __syncthreads)
 
 // shared-memory map (bytes from the 1024-aligned base)
@@ -109,6 +110,7 @@ constexpr uint32_t TM_KQK = 0, TM_W = 64 /* two buffers */, TM_WK = 192, TM_O = 
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
+constexpr int kL2Ahead = 3;   // chunks prefetched into L2 beyond the two staged in SMEM
 
 struct Scal {   // per-stage per-row scalars of one chunk
     float *gam, *ig, *bs, *bg, *sc;   // gamma, 1/gamma, beta, beta gamma, gamma_C / gamma
@@ -238,7 +240,7 @@ __device__ __forceinline__ void frag_store(float *M, int ld, int r0, int n0, con
 }
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A in As (fp32), into Ts, by
-// the prep warpgroup (w = thread index 0..127).  Blocked: four 16 x 16
+// the prep warps (w = thread index 0..255).  Blocked: four 16 x 16
 // diagonal inverses by right-looking forward substitution in fp32 (one column
 // per thread), then two merge levels T_ij = -T_ii (A_ij T_jj) on tf32 warp
 // MMAs.  On return the lower triangle of Ts holds T; the 16 x 16 blocks right
@@ -266,61 +268,59 @@ __device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *
             if ((b & 1) == 0) Ts[(o + r) * LDA + o + 16 + l] = 0.f;
         }
     }
-    named_sync(BAR_PREP, 128);
-    {   // level 1: T(1,0) and T(3,2); warp -> (pair, 8-column tile)
-        const int p = wp >> 1, nt = wp & 1;
+    named_sync(BAR_PREP, NPREP);
+    {   // level 1: T(1,0) and T(3,2); warps 0-3 -> (pair, 8-column tile)
+        const int p = (wp >> 1) & 1, nt = wp & 1;
         const int R = 16 * (2 * p + 1), Cb = 16 * (2 * p);
+        if (wp < 4) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t fa[4], fb[2];
+                frag_a(fa, As, LDA, R, Cb + 8 * ks, lane);
+                frag_b(fb, Ts, LDA, Cb + 8 * ks, Cb + 8 * nt, lane);
+                mma_tf32(d, fa, fb);
+            }
+            frag_store(Ys + p * 16 * LDY, LDY, 0, 8 * nt, d, 1.f, lane);
+        }
+        named_sync(BAR_PREP, NPREP);
+        if (wp < 4) {
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t fa[4], fb[2];
+                frag_a(fa, Ts, LDA, R, R + 8 * ks, lane);          // zero above the diagonal
+                frag_b(fb, Ys + p * 16 * LDY, LDY, 8 * ks, 8 * nt, lane);
+                mma_tf32(e, fa, fb);
+            }
+            frag_store(Ts, LDA, R, Cb + 8 * nt, e, -1.f, lane);
+        }
+    }
+    named_sync(BAR_PREP, NPREP);
+    {   // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
+        // warp -> (16-row tile, 8-column tile)
+        const int m0 = 16 * (wp & 1), n0 = 8 * (wp >> 1);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t fa[4], fb[2];
-            frag_a(fa, As, LDA, R, Cb + 8 * ks, lane);
-            frag_b(fb, Ts, LDA, Cb + 8 * ks, Cb + 8 * nt, lane);
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t fb[2], fa[4];
+            frag_b(fb, Ts, LDA, 8 * ks, n0, lane);
+            frag_a(fa, As, LDA, 32 + m0, 8 * ks, lane);
             mma_tf32(d, fa, fb);
         }
-        frag_store(Ys + p * 16 * LDY, LDY, 0, 8 * nt, d, 1.f, lane);
-        named_sync(BAR_PREP, 128);
+        frag_store(Ys, LDY, m0, n0, d, 1.f, lane);
+        named_sync(BAR_PREP, NPREP);
         float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t fa[4], fb[2];
-            frag_a(fa, Ts, LDA, R, R + 8 * ks, lane);          // zero above the diagonal
-            frag_b(fb, Ys + p * 16 * LDY, LDY, 8 * ks, 8 * nt, lane);
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t fb[2], fa[4];
+            frag_b(fb, Ys, LDY, 8 * ks, n0, lane);
+            frag_a(fa, Ts, LDA, 32 + m0, 32 + 8 * ks, lane);
             mma_tf32(e, fa, fb);
         }
-        frag_store(Ts, LDA, R, Cb + 8 * nt, e, -1.f, lane);
+        frag_store(Ts, LDA, 32 + m0, n0, e, -1.f, lane);
     }
-    named_sync(BAR_PREP, 128);
-    {   // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
-        // warp -> 8-column tile, both 16-row tiles
-        const int n0 = 8 * wp;
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t fb[2], fa0[4], fa1[4];
-            frag_b(fb, Ts, LDA, 8 * ks, n0, lane);
-            frag_a(fa0, As, LDA, 32, 8 * ks, lane);
-            frag_a(fa1, As, LDA, 48, 8 * ks, lane);
-            mma_tf32(d0, fa0, fb);
-            mma_tf32(d1, fa1, fb);
-        }
-        frag_store(Ys, LDY, 0, n0, d0, 1.f, lane);
-        frag_store(Ys, LDY, 16, n0, d1, 1.f, lane);
-        named_sync(BAR_PREP, 128);
-        float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t fb[2], fa0[4], fa1[4];
-            frag_b(fb, Ys, LDY, 8 * ks, n0, lane);
-            frag_a(fa0, Ts, LDA, 32, 32 + 8 * ks, lane);
-            frag_a(fa1, Ts, LDA, 48, 32 + 8 * ks, lane);
-            mma_tf32(e0, fa0, fb);
-            mma_tf32(e1, fa1, fb);
-        }
-        frag_store(Ts, LDA, 32, n0, e0, -1.f, lane);
-        frag_store(Ts, LDA, 48, n0, e1, -1.f, lane);
-    }
-    named_sync(BAR_PREP, 128);
+    named_sync(BAR_PREP, NPREP);
 }
 
 struct FusedArgs {
@@ -371,10 +371,10 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == 12) {
         tmem_alloc(smem_u32(&s_tmem), TM_COLS);
         tmem_relinquish();
-        if (tid == 256) {
+        if (tid == 384) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
@@ -394,10 +394,12 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t idesc_o = idesc_bf16(64, 128, false, false);
     const uint32_t idesc_d = idesc_bf16(128, 128, false, true);
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ================================================================ prep
         const int w = tid;
-        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        const int qd = warp & 3, half = warp >> 2;   // TMEM lane quadrant, column half
+        const int lrow = qd * 32 + (tid & 31);       // TMEM lane = accumulator row
+        const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
         bool issued = false;
         for (int k = 0; k < NC; ++k) {
             const int st = k & 1, sl = k % NSCAL;
@@ -407,7 +409,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const uint32_t v_a = sbase + OFF_V + st * V_BYTES;
 
             bool ok = role_wait(bar(B_FULL0 + st), (uint32_t)(k >> 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_PREP, 128, ok)) break;
+            if (!named_and(BAR_PREP, NPREP, ok)) break;
             if (w == 0) {   // [K;Q] K^T  (the accumulator was read out last chunk)
                 tc_fence_after();
 #pragma unroll
@@ -425,16 +427,16 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (ok) ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
             // A's space holds Lb / Lbg of chunk k-1 until its U / Wk products are done
             if (ok && k > 0) ok = role_wait(bar(B_UWK), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_PREP, 128, ok)) break;
+            if (!named_and(BAR_PREP, NPREP, ok)) break;
             const float igC = 1.f / s_gC[sl];
             tc_fence_after();
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {     // 32 columns at a time
+            {   // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
+                const int h = half;
                 float v[32];
                 tmem_ld32(tl + TM_KQK + h * 32, v);
                 tmem_wait_ld();
-                if (w < 64) {
-                    const int r = w;
+                if (lrow < 64) {
+                    const int r = lrow;
                     const float br = (r < c) ? S.bg[r] : 0.f;
 #pragma unroll
                     for (int s4 = 0; s4 < 32; s4 += 4) {
@@ -448,7 +450,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                         *reinterpret_cast<float4 *>(&As[r * LDA + s0]) = o;
                     }
                 } else {
-                    const int r = w - 64;
+                    const int r = lrow - 64;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = (h * 32 + e <= r && r < c) ? v[e] * igC : 0.f;
                     st_halfrow_bf16(sm + OFF_P + st * 8192, r, h, v);
@@ -456,15 +458,16 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(BAR_PREP, 128);
+            named_sync(BAR_PREP, NPREP);
 
             solve_unit_lower(w, As, Ts, Ys);
-            {   // Lb = (T - I) diag(beta), Lbg = (T - I) diag(beta gamma), bf16 rows
-                const int r = w & 63;
-                const float *sc = (w < 64) ? S.bs : S.bg;
-                uint8_t *dst = sm + ((w < 64) ? OFF_LB : OFF_LBG);
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
+            {   // Lb = (T - I) diag(beta) + diag(bf16(beta)), Lbg likewise with beta gamma;
+                // thread -> (matrix w / 128, row w % 64, column half (w / 64) % 2)
+                const int r = w & 63, mat = w >> 7;
+                const float *sc = mat ? S.bg : S.bs;
+                uint8_t *dst = sm + (mat ? OFF_LBG : OFF_LB);
+                {
+                    const int h = (w >> 6) & 1;
                     float v[32];
 #pragma unroll
                     for (int s4 = 0; s4 < 32; s4 += 4) {
@@ -479,8 +482,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     st_halfrow_bf16(dst, r, h, v);
                 }
             }
-            named_sync(BAR_PREP, 128);     // T is read out; its space takes the residuals
-            {   // Db = diag(beta - bf16(beta)), Dbg = diag(beta gamma - bf16(beta gamma))
+            named_sync(BAR_PREP, NPREP);     // T is read out; its space takes the residuals
+            if (w < 128) {   // Db = diag(beta - bf16(beta)), Dbg = diag(beta gamma - bf16(beta gamma))
                 const int r = w & 63;
                 const float x = (w < 64) ? S.bs[r] : S.bg[r];
                 const float lo = x - __bfloat162float(__float2bfloat16_rn(x));
@@ -503,7 +506,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             ok = (k < 2) || role_wait(bar(B_RWFREE0 + st), (uint32_t)((k - 2) >> 1) & 1u,
                                       a.limit_ns, &s_abort);
             if (ok && k > 0) ok = role_wait(bar(B_WKFREE), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_PREP, 128, ok)) break;
+            if (!named_and(BAR_PREP, NPREP, ok)) break;
             if (w == 0) {
                 tc_fence_after();
 #pragma unroll
@@ -530,12 +533,12 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             mma_commit(bar(B_DRAINP));
             mbar_wait(bar(B_DRAINP), 0u, kCleanupLimitNs);
         }
-    } else if (warp < 8) {
+    } else if (warp < 12) {
         // ================================================================ chain
-        const int w = tid - 128;    // = TMEM lane (row j of the transposed products)
+        const int w = tid - 256;    // = TMEM lane (row j of the transposed products)
         const int j = w;
         const int lane = w & 31;
-        const uint32_t tl = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        const uint32_t tl = tmem + ((uint32_t)((warp - 8) * 32) << 16);
         bool issued = false;
         bool ok = role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
         ok = named_and(BAR_CHAIN, 128, ok);
@@ -673,7 +676,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             // ---- output row r = gamma_r O[r][:]: lanes 0..15 of each quadrant hold
             // rows 16 q .. 16 q + 15 (the M = 64 TMEM layout), 128 columns each
             {
-                const int r = 16 * (warp - 4) + (lane & 15);
+                const int r = 16 * (warp - 8) + (lane & 15);
                 const bool has_row = (lane < 16) && (r < c);
                 const float gr = S.gam[r];
                 uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + t0 + r) * D);
@@ -721,6 +724,17 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_load_3d(vv + 8192, &tm_v, b, 64, n * C, bh);
             ++issued[st];
         };
+        // Pull the inputs of chunk n into L2 ahead of its shared-memory load, so
+        // that the load (issued when a stage frees up) hits L2 rather than HBM.
+        auto prefetch_l2 = [&](int n) {   // lane 0 only
+            if (n >= NC) return;
+            tma_prefetch_3d(&tm_k, 0, n * C, bh);
+            tma_prefetch_3d(&tm_k, 64, n * C, bh);
+            tma_prefetch_3d(&tm_q, 0, n * C, bh);
+            tma_prefetch_3d(&tm_q, 64, n * C, bh);
+            tma_prefetch_3d(&tm_v, 0, n * C, bh);
+            tma_prefetch_3d(&tm_v, 64, n * C, bh);
+        };
         auto load_gb = [&](int n, float (&gv)[2], float (&bv)[2]) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -740,12 +754,17 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (lane == 0) issue_tma(n);
             decay(n, gv, bv);
         }
+        if (lane == 0)
+            for (int n = 2; n < 2 + kL2Ahead; ++n) prefetch_l2(n);
         if (NC > 2) load_gb(2, gv, bv);
         for (int n = 0; n + 2 < NC; ++n) {   // refill a stage once chunk n is done with it
             const int st = n & 1;
             bool ok = role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
             if (!__all_sync(0xffffffffu, ok)) break;
-            if (lane == 0) issue_tma(n + 2);
+            if (lane == 0) {
+                issue_tma(n + 2);
+                prefetch_l2(n + 2 + kL2Ahead);
+            }
             decay(n + 2, gv, bv);
             if (n + 3 < NC) load_gb(n + 3, gv, bv);
         }
@@ -758,7 +777,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == 12) {
         __syncwarp();
         tmem_dealloc(tmem, TM_COLS);
     }
