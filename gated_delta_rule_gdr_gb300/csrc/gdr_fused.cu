@@ -338,11 +338,13 @@ enum : int {
     B_KQK,                     // prep commit: [K;Q]K^T done
     B_UWK,                     // prep commit: U^T', Wk^T' done
     B_W,                       // chain commit: W^T done
-    B_D,                       // chain commit: M^T update, O^T done
+    B_D,                       // chain commit: M^T update done
+    B_O2,                      // chain commit: output accumulation done
     B_SCAL0, B_SCAL1, B_SCAL2, // copy: decay scalars of a chunk written, per slot
     B_WKFREE,                  // chain: Wk^T of a chunk read out of TMEM
     B_RWFREE0, B_RWFREE1,      // chain: W^T buffer read out, per buffer
     B_OSTAGE0, B_OSTAGE1,      // chain: input stage done with (its MMAs complete)
+    B_PFREE0, B_PFREE1,        // chain: P buffer read by the output product, per buffer
     B_DRAINP, B_DRAINC,        // commits of the error path (prep, chain)
     NUM_BARS
 };
@@ -427,6 +429,9 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (ok) ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
             // A's space holds Lb / Lbg of chunk k-1 until its U / Wk products are done
             if (ok && k > 0) ok = role_wait(bar(B_UWK), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
+            // P's buffer holds P of chunk k-2 until that chunk's output product is done
+            if (ok && k > 1)
+                ok = role_wait(bar(B_PFREE0 + st), (uint32_t)((k - 2) >> 1) & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_PREP, NPREP, ok)) break;
             const float igC = 1.f / s_gC[sl];
             tc_fence_after();
@@ -635,11 +640,12 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM_M, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
                              sdesc_sw128(kq_a + kk * 2048, 16384, 1024), idesc_d, 1);
+                mma_commit(bar(B_D));       // the state update needs only this
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_P + st * 8192 + kk * 32, 16, 1024),
                              sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024), idesc_o, 1);
-                mma_commit(bar(B_D));
+                mma_commit(bar(B_O2));
             }
 
             // ---- state: MT <- bf16(M^T_{n+1}); TMEM M^T <- gamma_C(n+1) M^T_{n+1}
@@ -653,11 +659,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after();
             {
                 const float gn = last ? 1.f : s_gC[sl1];
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    float v[32];
-                    tmem_ld32(tl + TM_M + cb * 32, v);
-                    tmem_wait_ld();
+                float va[32];
+                auto consume = [&](int cb, float (&v)[32]) {
                     if (last) {
                         if (a.final_state) {
                             float *f = a.final_state + (int64_t)bh * D * D + j;
@@ -670,21 +673,28 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                         for (int e = 0; e < 32; ++e) v[e] *= gn;
                         tmem_st32(tl + TM_M + cb * 32, v);
                     }
+                };
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    tmem_ld32(tl + TM_M + cb * 32, va);
+                    tmem_wait_ld();
+                    consume(cb, va);
                 }
                 tmem_wait_st();
             }
             // ---- output row r = gamma_r O[r][:]: lanes 0..15 of each quadrant hold
             // rows 16 q .. 16 q + 15 (the M = 64 TMEM layout), 128 columns each
+            ok = role_wait(bar(B_O2), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            if (w == 0 && ok) mbar_arrive(bar(B_PFREE0 + st));
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            tc_fence_after();
             {
                 const int r = 16 * (warp - 8) + (lane & 15);
                 const bool has_row = (lane < 16) && (r < c);
                 const float gr = S.gam[r];
                 uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + t0 + r) * D);
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    float v[32];
-                    tmem_ld32(tl + TM_O + cb * 32, v);    // warp-wide; lanes 16..31 unused
-                    tmem_wait_ld();
+                float va[32], vb[32];
+                auto emit = [&](int cb, const float (&v)[32]) {
                     if (has_row) {
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
@@ -696,7 +706,21 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                             __stcs(orow + cb * 4 + q4, u);
                         }
                     }
-                }
+                };
+                // warp-wide loads (lanes 16..31 unused); the next block loads while
+                // the current one is converted and stored
+                tmem_ld32(tl + TM_O + 0, va);
+                tmem_wait_ld();
+                tmem_ld32(tl + TM_O + 32, vb);
+                emit(0, va);
+                tmem_wait_ld();
+                tmem_ld32(tl + TM_O + 64, va);
+                emit(1, vb);
+                tmem_wait_ld();
+                tmem_ld32(tl + TM_O + 96, vb);
+                emit(2, va);
+                tmem_wait_ld();
+                emit(3, vb);
             }
             fence_proxy_async_smem();
             tc_fence_before();
