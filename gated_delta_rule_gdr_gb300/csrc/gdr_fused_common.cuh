@@ -1,0 +1,305 @@
+// gdr_fused_common.cuh -- pieces shared by the fused tensor-core prefill
+// kernels (one CTA per head, and the value-split pair per head): the chunk
+// geometry, bf16 tile writes, bounded role waits, the per-chunk decay of one
+// warp, the 64 x 64 unit-lower triangular solve and the TMA map of a
+// [BH][T][128] bf16 tensor.  Everything here has internal linkage: each
+// kernel translation unit gets its own copy, including its own device error
+// word, which its host code reads and clears.
+#pragma once
+
+#include "gdr_internal.h"
+#include "gdr_math.cuh"
+#include "gdr_sm100.cuh"
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+namespace gdr {
+namespace {
+
+using namespace sm100;
+
+constexpr int C = 64;      // chunk
+constexpr int D = 128;     // dk (and dv of the input tensors)
+constexpr int NPREP = 256; // threads of the preparation warps
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;   // named barriers (0 is __syncthreads)
+constexpr int LDA = 68;    // fp32 row stride of the solve matrices
+constexpr int LDY = 40;    // row stride of the merge scratch
+constexpr uint64_t kCleanupLimitNs = 2000000000ull;
+
+// Sticky device error word of this translation unit's kernels.
+__device__ unsigned g_device_error_word = 0;
+
+struct Scal {   // per-stage per-row scalars of one chunk
+    float *gam, *ig, *bs, *bg, *sc;   // gamma, 1/gamma, beta, beta gamma, gamma_C / gamma
+};
+
+__device__ __forceinline__ Scal scal_at(float *b) {   // 5 x 64 floats
+    return {b, b + 64, b + 128, b + 192, b + 256};
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Write 32 fp32 values as half a 128-byte bf16 row (chunks 4h..4h+3).
+__device__ __forceinline__ void st_halfrow_bf16(uint8_t *tile, uint32_t row, uint32_t h,
+                                                const float *v) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t ch = h * 4 + q4;
+        uint4 u;
+        u.x = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
+        u.y = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
+        u.z = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
+        u.w = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
+        *reinterpret_cast<uint4 *>(tile + row * 128u + ((ch ^ (row & 7u)) << 4)) = u;
+    }
+}
+
+// Bounded wait used by the warpgroups: gives up when the CTA-wide abort flag
+// is raised or the time limit passes (then raises the flag and the error word).
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          volatile int *abort) {
+    if (mbar_test_wait(bar, parity)) return true;      // non-blocking first look
+    if (limit_ns == 0) {                                // injected timeout: give up at once
+        *abort = 1;
+        atomicOr(&g_device_error_word, kDevErrTimeout);
+        return false;
+    }
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            atomicOr(&g_device_error_word, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Cumulative decay of one chunk by one warp (lane l owns rows 2l, 2l+1, whose
+// g and beta it already holds): alpha = a_min + (1 - a_min) sigmoid(g), the
+// inclusive scan of log alpha, gamma = exp(scan), 1/gamma, beta, beta gamma,
+// gamma_C (the last valid row) and gamma_C / gamma.  Rows past the chunk's end
+// get gamma = 1, beta = 0 and gamma_C / gamma = 0 so that they drop out of
+// every product.
+__device__ __forceinline__ void warp_decay(int lane, const float (&gv)[2], const float (&bv)[2],
+                                           int c, float a_min, Scal s, float *s_gC) {
+    const int r0 = 2 * lane;
+    const float l0 = (r0 < c) ? log_alpha(gv[0], a_min) : 0.f;
+    const float l1 = (r0 + 1 < c) ? log_alpha(gv[1], a_min) : 0.f;
+    float incl = l0 + l1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const float b1 = incl, b0 = incl - l1;
+    // gamma_C: the scan value of row c - 1, held by lane (c - 1) / 2
+    const float bC = __shfl_sync(0xffffffffu, ((c - 1) & 1) ? b1 : b0, (c - 1) >> 1);
+    const float gC = expf(bC);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = r0 + e;
+        const bool valid = r < c;
+        const float gam = valid ? expf(e ? b1 : b0) : 1.f;
+        const float b = valid ? bv[e] : 0.f;
+        s.gam[r] = gam;
+        s.ig[r] = 1.f / gam;
+        s.bs[r] = b;
+        s.bg[r] = b * gam;
+        s.sc[r] = valid ? gC / gam : 0.f;
+    }
+    if (lane == 0) *s_gC = gC;
+    __syncwarp();
+}
+
+// tf32 warp-level MMA (m16n8k8) for the small merge products of the solve.
+// Fragment layouts (g = lane / 4, t = lane % 4): A (16 x 8) a0 (g, t), a1
+// (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8) b0 (t, g), b1 (t+4, g);
+// C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *M, int ld, int r0, int c0,
+                                       int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    a[0] = to_tf32(M[(r0 + g) * ld + c0 + t]);
+    a[1] = to_tf32(M[(r0 + g + 8) * ld + c0 + t]);
+    a[2] = to_tf32(M[(r0 + g) * ld + c0 + t + 4]);
+    a[3] = to_tf32(M[(r0 + g + 8) * ld + c0 + t + 4]);
+}
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *M, int ld, int k0, int n0,
+                                       int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    b[0] = to_tf32(M[(k0 + t) * ld + n0 + g]);
+    b[1] = to_tf32(M[(k0 + t + 4) * ld + n0 + g]);
+}
+__device__ __forceinline__ void frag_store(float *M, int ld, int r0, int n0, const float (&d)[4],
+                                           float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2 *>(&M[(r0 + g) * ld + n0 + 2 * t]) = make_float2(sign * d[0], sign * d[1]);
+    *reinterpret_cast<float2 *>(&M[(r0 + g + 8) * ld + n0 + 2 * t]) =
+        make_float2(sign * d[2], sign * d[3]);
+}
+
+// T = (I + A)^-1 for the strictly lower 64 x 64 A in As (fp32), into Ts, by
+// the prep warps (w = thread index 0..255).  Blocked: four 16 x 16
+// diagonal inverses by right-looking forward substitution in fp32 (one column
+// per thread), then two merge levels T_ij = -T_ii (A_ij T_jj) on tf32 warp
+// MMAs.  On return the lower triangle of Ts holds T; the 16 x 16 blocks right
+// of the even diagonal blocks hold zeros (the merges read them).  T feeds
+// bf16 tensor-core operands, so the tf32 merges cost no accuracy that matters.
+__device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *Ts, float *Ys) {
+    const int lane = w & 31, wp = w >> 5;
+    if (w < 64) {
+        const int b = w >> 4, l = w & 15, o = 16 * b;
+        float x[16], acc[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            x[m] = (m == l) ? 1.f : 0.f;
+            acc[m] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            if (m > l) x[m] = -acc[m];          // x[m] is final from here on
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(As[(o + r) * LDA + o + m], x[m], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            Ts[(o + r) * LDA + o + l] = x[r];
+            if ((b & 1) == 0) Ts[(o + r) * LDA + o + 16 + l] = 0.f;
+        }
+    }
+    named_sync(BAR_PREP, NPREP);
+    {   // level 1: T(1,0) and T(3,2); warps 0-3 -> (pair, 8-column tile)
+        const int p = (wp >> 1) & 1, nt = wp & 1;
+        const int R = 16 * (2 * p + 1), Cb = 16 * (2 * p);
+        if (wp < 4) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t fa[4], fb[2];
+                frag_a(fa, As, LDA, R, Cb + 8 * ks, lane);
+                frag_b(fb, Ts, LDA, Cb + 8 * ks, Cb + 8 * nt, lane);
+                mma_tf32(d, fa, fb);
+            }
+            frag_store(Ys + p * 16 * LDY, LDY, 0, 8 * nt, d, 1.f, lane);
+        }
+        named_sync(BAR_PREP, NPREP);
+        if (wp < 4) {
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t fa[4], fb[2];
+                frag_a(fa, Ts, LDA, R, R + 8 * ks, lane);          // zero above the diagonal
+                frag_b(fb, Ys + p * 16 * LDY, LDY, 8 * ks, 8 * nt, lane);
+                mma_tf32(e, fa, fb);
+            }
+            frag_store(Ts, LDA, R, Cb + 8 * nt, e, -1.f, lane);
+        }
+    }
+    named_sync(BAR_PREP, NPREP);
+    {   // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
+        // warp -> (16-row tile, 8-column tile)
+        const int m0 = 16 * (wp & 1), n0 = 8 * (wp >> 1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t fb[2], fa[4];
+            frag_b(fb, Ts, LDA, 8 * ks, n0, lane);
+            frag_a(fa, As, LDA, 32 + m0, 8 * ks, lane);
+            mma_tf32(d, fa, fb);
+        }
+        frag_store(Ys, LDY, m0, n0, d, 1.f, lane);
+        named_sync(BAR_PREP, NPREP);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t fb[2], fa[4];
+            frag_b(fb, Ys, LDY, 8 * ks, n0, lane);
+            frag_a(fa, Ts, LDA, 32 + m0, 32 + 8 * ks, lane);
+            mma_tf32(e, fa, fb);
+        }
+        frag_store(Ts, LDA, 32 + m0, n0, e, -1.f, lane);
+    }
+    named_sync(BAR_PREP, NPREP);
+}
+
+struct FusedArgs {
+    const float *g, *beta, *init;
+    __nv_bfloat16 *out;
+    float *final_state;
+    float a_min;
+    int T;
+    uint64_t limit_ns;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [BH][T][128] bf16 viewed as a 3-D tensor; 64 x 64 boxes, 128-byte swizzle,
+// zero fill beyond T.
+bool make_map(CUtensorMap *m, const void *ptr, int BH, int T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t wait_limit_ns() {
+    // Test hook: GDR_FAULT_INJECT=timeout makes every bounded wait give up at
+    // once, exercising the error path without any GPU fault.
+    const char *e = std::getenv("GDR_FAULT_INJECT");
+    if (e && std::strcmp(e, "timeout") == 0) return 0;
+    return 2000000000ull;   // 2 s
+}
+
+// Reads and clears this translation unit's device error word (synchronous).
+cudaError_t take_error_word(unsigned *value) {
+    unsigned word = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&word, g_device_error_word, sizeof(word));
+    if (e != cudaSuccess) return e;
+    *value = word;
+    if (word != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace
+}  // namespace gdr

@@ -16,7 +16,9 @@ from gated_delta_rule_gdr_gb300 import inputs as I
 pytestmark = pytest.mark.gpu
 
 
-def test_injected_timeout_is_reported_and_recovers():
+@pytest.mark.parametrize("variant", ["single", "pair"])
+def test_injected_timeout_is_reported_and_recovers(variant, monkeypatch):
+    monkeypatch.setenv("GDR_FUSED_VARIANT", variant)
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     gdr.load(build_if_missing=True)

@@ -3,6 +3,9 @@ seeded inputs.  Tolerances are relative L2 over the whole tensor: 1e-5 for the
 fp32 path, 5e-3 for the bf16 paths, for outputs and final states alike."""
 from __future__ import annotations
 
+import contextlib
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -40,6 +43,21 @@ def run_gpu(x, w, init=None, chunk=None):
 
 def to(x, device):
     return {k_: (None if t is None else t.to(device)) for k_, t in x.items()}
+
+
+@contextlib.contextmanager
+def fused_variant(name):
+    """Force the one-CTA-per-head ("single") or the value-split ("pair") fused
+    kernel; by default the launcher picks by the number of heads."""
+    old = os.environ.get("GDR_FUSED_VARIANT")
+    os.environ["GDR_FUSED_VARIANT"] = name
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["GDR_FUSED_VARIANT"]
+        else:
+            os.environ["GDR_FUSED_VARIANT"] = old
 
 
 # ------------------------------------------------------------------ the correctness workload
@@ -104,6 +122,22 @@ def test_ragged_and_tiny(dtype, T, d):
     assert rel(out, ro) <= TOL[dtype]
     assert rel(fin, rf) <= TOL[dtype]
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("variant", ["single", "pair"])
+@pytest.mark.parametrize("B,H,T", [(1, 1, 1), (1, 2, 63), (2, 1, 64), (1, 3, 65), (2, 2, 200),
+                                   (1, 2, 700)])
+def test_fused_variants(variant, B, H, T):
+    """Both fused kernels (bf16, dk = dv = 128, chunk 64) against the oracle:
+    ragged tails, one to three input-stage rounds, several heads."""
+    w = I.PREFILL.with_(B=B, H=H, T=T)
+    x = to(I.prefill_inputs(w), "cuda")
+    with fused_variant(variant):
+        out, fin = run_gpu(x, w)
+    ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min,
+                        x["init_state"].cpu())
+    assert rel(out, ro) <= TOL["bf16"], rel(out, ro)
+    assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
 
 
 def test_zero_length_copies_state():
@@ -172,6 +206,12 @@ def test_prefill_b4h16t4096():
                         cpu["init_state"])
     e_o, e_f = rel(out, ro), rel(fin, rf)
     print(f"prefill rel-L2 out {e_o:.3e} final {e_f:.3e}")
+    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
+    # the other fused kernel on the same inputs
+    with fused_variant("single"):
+        out1, fin1 = run_gpu(x, w)
+    e_o, e_f = rel(out1, ro), rel(fin1, rf)
+    print(f"prefill (one CTA per head) rel-L2 out {e_o:.3e} final {e_f:.3e}")
     assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
 
 
