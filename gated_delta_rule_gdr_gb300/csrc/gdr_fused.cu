@@ -3,90 +3,93 @@
 //
 // One CTA owns one (sequence, head) and walks its chunks of C = 64 tokens in
 // order.  Per chunk it does the whole chunked form -- cumulative decay, the
-// intra-chunk WY/UT transform, the state step and the output -- with every
-// contraction on the tensor core, and the fp32 state never leaves the SM.
-// HBM sees q, k, v, g, beta once, out once, and the state twice (in, out).
+// intra-chunk triangular transform, the state step and the output -- with
+// every contraction on the tensor core, and the fp32 state never leaves the
+// SM.  HBM sees q, k, v, g, beta once, out once, and the state twice.
 //
 // The method: with the lower-bounded decay, gamma_r >= a_min^r inside a chunk,
 // so 1/gamma and 1/gamma_C are finite and every causal tile -- the diagonal
 // (intra-chunk) tile included -- is one dense product with diagonal scalings
 // ("What a Trillion-Parameter MoE Model Reveals About the Next Stage of LLM
 // Scaling", sections 3.1-3.3; "Architecture Evolution and Training Engineering
-// for Trillion-Scale Sparse Multimodal Models", section 3.2).  Here those
-// scalings are applied in fp32 on the TMEM accumulators, not folded into the
+// for Trillion-Scale Sparse Multimodal Models", section 3.2).  The scalings are
+// applied in fp32 on TMEM accumulators and in registers, not folded into the
 // bf16 operands, so q, k and v enter the tensor core exactly as given.
 //
 // Algebra per chunk (rows r, s; gamma, 1/gamma, gamma_C as usual; M = S^T):
 //   A   = strict_lower(diag(beta gamma) K K^T diag(1/gamma)),  T = (I + A)^-1
-//   L   = T - I (strictly lower);  Lb = L diag(beta),  Lbg = L diag(beta gamma)
-//   U   = (Lb + diag(beta)) V,  Wk = (Lbg + diag(beta gamma)) K, where each
-//         diagonal is split into its bf16 value plus a bf16 residual applied
-//         by a second product, so the identity part stays exact to ~2^-17
-//   W   = U - Wk M_n
+//   E   = V - diag(gamma) K M_n                 (what the state mispredicts)
+//   W   = T diag(beta) E = diag(beta) E + Lb E,  Lb = strict_lower(T) diag(beta)
 //   Wt  = diag(gamma_C / gamma) W
 //   P   = lower_incl(Q K^T) / gamma_C
 //   O   = diag(gamma) (Q M_n + P Wt)
 //   M_{n+1} = gamma_C M_n + K^T Wt
-// The products are computed transposed so that their M dimension is 128
-// (dv or dk):  U^T = V^T Lb^T,  Wk^T = K^T Lbg^T,  W^T = U^T - M^T Wk^T,
-// M^T_{n+1} = gamma_C M^T + Wt^T K -- except the output, O = Q M + P Wt, an
-// M = 64 product whose TMEM rows are whole output rows, so each row leaves the
-// SM as contiguous 16-byte stores without a transpose.
+// W is the chunked WY/UT form U - Wk M_n (U = T diag(beta) V, Wk = T
+// diag(beta gamma) K) regrouped as T diag(beta) (V - diag(gamma) K M_n): the
+// same values with two products fewer, and the identity part of T (the
+// dominant diag(beta) E) is added in fp32 rather than taken through bf16.
 //
-// Warp roles (416 threads):
+// Products (tcgen05.mma, bf16 operands, fp32 accumulators in TMEM):
+//   prep   [K;Q] K^T              M = 128, N = 64,  K = 128
+//   chain  K M_n                  M = 64,  N = 128, K = 128  -> X
+//          X += Lb E              M = 64,  N = 128, K = 64   (X = W afterwards)
+//          Q M_n                  M = 64,  N = 128, K = 128  -> O
+//          M  += K^T Wt           M = 128, N = 128, K = 64   (M prescaled by gamma_C)
+//          O  += P Wt             M = 64,  N = 128, K = 64
+// X and O use the M = 64 layout (row r in lane r % 16 + 32 (r / 16)), read and
+// written by all four chain warps with the 16x32bx2 TMEM shape.
+//
+// Warp roles (448 threads):
 //   prep  (warps 0-7)  chunk k: A and P from [K;Q]K^T, the triangular solve,
-//                      Lb / Lbg and the U^T, Wk^T products -- state-independent
-//   chain (warps 8-11) chunk n: Wk^T to bf16, W^T epilogue, state update, output
-//   copy  (warp 12)    the TMA loads of the inputs and the cumulative decay
-// Each warpgroup issues its own tcgen05.mma from one elected thread, so the
-// preparation of chunk n+1 overlaps the state chain of chunk n.
+//                      Lb -- state-independent, runs ahead of the chain
+//   chain (warps 8-11) chunk n: E, W, Wt, the state update and the output
+//   copy  (warp 12)    TMA loads of the inputs, the cumulative decay, L2
+//                      prefetch of later chunks
+//   MMA   (warp 13)    issues [K;Q]K^T of chunk k+1 as soon as the preparation
+//                      has read chunk k's accumulator
+// The chain issues its own products; the output epilogue of chunk n runs
+// while K M_{n+1} is on the tensor core.
 //
-// Shared-memory operands (128-byte swizzled, 1024-byte aligned):
-//   KQ[stage]  32 KB  [slab i/64][K rows 0..63 | Q rows 0..63][128 B]  (TMA)
-//   V[stage]   16 KB  [slab j/64][V rows 0..63][128 B]                   (TMA)
-//   MT         32 KB  M^T bf16, K-major ([j][i], two i slabs)
-//   WkT        16 KB  Wk^T bf16, MN-major ([i][r])
-//   WtT        16 KB  Wt^T bf16, K-major ([j][s])
-//   P[2]        8 KB each, K-major ([r][s]), one per stage
-//   Lb, Lbg     8 KB each, K-major ([r][s]), sharing space with the fp32 A
-//   Db, Dbg     8 KB each, the diagonal residuals, sharing space with the fp32 T
-// TMEM (fp32, 128 lanes): KQK^T 64 cols, W^T 2 x 64, Wk^T 64, M^T 128, and O
-// 128 cols in the M = 64 layout (row r in lane r % 16 + 32 (r / 16)).
+// Shared memory (128-byte swizzled operands, 1024-byte aligned):
+//   KQ[2]   32 KB  [slab i/64][K rows 0..63 | Q rows 0..63][128 B]   (TMA)
+//   V[2]    16 KB  [slab j/64][rows 0..63][128 B]                    (TMA)
+//   MS      32 KB  bf16 M_n, [slab j/64][i][128 B]   (MN-major operand)
+//   EW      16 KB  bf16 E, then bf16 Wt, [slab j/64][s][128 B]  (MN-major)
+//   LP[2]   16 KB  bf16 Lb [r][s] and P [r][s] of one chunk  (K-major)
+//   A, T    fp32 64 x 68 each, merge scratch, 4 slots of per-chunk scalars
+// TMEM: [K;Q]K^T 64 cols, X 128, O 128, M 128.
 
 #include "gdr_fused_common.cuh"
 
 namespace gdr {
 namespace {
 
-constexpr int NT = 416;    // prep (256) + chain (128) + copy (32)
+constexpr int NT = 448;    // prep (256) + chain (128) + copy (32) + MMA issue (32)
+constexpr int NSTAGE = 2;  // input stages
+constexpr int NSCAL = 4;   // scalar slots (chunk m uses slot m % 4)
 
 // shared-memory map (bytes from the 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;             // 2 x 32 KB
+constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t KQ_BYTES = 32768;
-constexpr uint32_t OFF_V = 65536;          // 2 x 16 KB
+constexpr uint32_t OFF_V = OFF_KQ + NSTAGE * KQ_BYTES;
 constexpr uint32_t V_BYTES = 16384;
-constexpr uint32_t OFF_MT = 98304;         // 32 KB
-constexpr uint32_t OFF_WKT = 131072;       // 16 KB
-constexpr uint32_t OFF_WTT = 147456;       // 16 KB
-constexpr uint32_t OFF_P = 163840;         // 2 x 8 KB
-constexpr uint32_t OFF_AS = 180224;        // 64 x 68 fp32; Lb, Lbg reuse its first 16 KB
-constexpr uint32_t OFF_LB = OFF_AS;
-constexpr uint32_t OFF_LBG = OFF_AS + 8192;
-constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;   // 64 x 68 fp32; Db, Dbg reuse it
-constexpr uint32_t OFF_DB = OFF_TS;
-constexpr uint32_t OFF_DBG = OFF_TS + 8192;
-constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;   // 32 x 40 fp32
-constexpr int NSCAL = 3;                   // scalar slots (chunk m uses slot m % 3)
-constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;   // scalars: 3 slots x 5 x 64 fp32
+constexpr uint32_t OFF_MS = OFF_V + NSTAGE * V_BYTES;     // 32 KB
+constexpr uint32_t OFF_EW = OFF_MS + 32768;               // 16 KB
+constexpr uint32_t OFF_LP = OFF_EW + 16384;               // 2 x (Lb 8 KB, P 8 KB)
+constexpr uint32_t LP_BYTES = 16384;
+constexpr uint32_t OFF_AS = OFF_LP + 2 * LP_BYTES;        // 64 x 68 fp32
+constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;        // 64 x 68 fp32
+constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;        // 32 x 40 fp32
+constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;        // 4 slots x 5 x 64 fp32
 constexpr uint32_t SMEM_USED = OFF_SC + NSCAL * 5 * 64 * 4;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;         // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
-static_assert(OFF_AS % 1024 == 0 && 64 * LDA * 4 >= 16384, "Lb/Lbg must fit in A's space");
-static_assert(OFF_TS % 1024 == 0, "Db/Dbg must be 1024-byte aligned");
+static_assert(OFF_V % 1024 == 0 && OFF_MS % 1024 == 0 && OFF_EW % 1024 == 0 &&
+                  OFF_LP % 1024 == 0,
+              "swizzled operands must be 1024-byte aligned");
 
 // TMEM columns
-constexpr uint32_t TM_KQK = 0, TM_W = 64 /* two buffers */, TM_WK = 192, TM_O = 256 /* 128 */,
-                   TM_M = 384;
+constexpr uint32_t TM_KQK = 0, TM_X = 64, TM_O = 192, TM_M = 320;
 constexpr uint32_t TM_COLS = 512;
 
 constexpr int kL2Ahead = 3;   // chunks prefetched into L2 beyond the two staged in SMEM
@@ -97,18 +100,18 @@ __device__ __forceinline__ Scal scal(uint8_t *sm, int slot) {
 
 // mbarriers of the pipeline (index into s_bar)
 enum : int {
-    B_FULL0 = 0, B_FULL1,      // copy: TMA inputs of a stage landed
-    B_KQK,                     // prep commit: [K;Q]K^T done
-    B_UWK,                     // prep commit: U^T', Wk^T' done
-    B_W,                       // chain commit: W^T done
-    B_D,                       // chain commit: M^T update done
-    B_O2,                      // chain commit: output accumulation done
-    B_SCAL0, B_SCAL1, B_SCAL2, // copy: decay scalars of a chunk written, per slot
-    B_WKFREE,                  // chain: Wk^T of a chunk read out of TMEM
-    B_RWFREE0, B_RWFREE1,      // chain: W^T buffer read out, per buffer
-    B_OSTAGE0, B_OSTAGE1,      // chain: input stage done with (its MMAs complete)
-    B_PFREE0, B_PFREE1,        // chain: P buffer read by the output product, per buffer
-    B_DRAINP, B_DRAINC,        // commits of the error path (prep, chain)
+    B_FULL0 = 0,                    // copy: TMA inputs of a stage landed (x2)
+    B_KQFREE0 = B_FULL0 + NSTAGE,   // chain: every reader of a stage is done (x2)
+    B_SCAL0 = B_KQFREE0 + NSTAGE,   // copy: decay scalars of a chunk written (x4)
+    B_KQK = B_SCAL0 + NSCAL,        // MMA-warp commit: [K;Q]K^T done
+    B_KQKFREE,                      // prep: [K;Q]K^T accumulator read out
+    B_LREADY0,                      // prep: Lb and P of buffer b written (x2)
+    B_LPFREE0 = B_LREADY0 + 2,      // chain: buffer b read by its last product (x2)
+    B_KM = B_LPFREE0 + 2,           // chain commit: X = K M_n done
+    B_C3,                           // chain commit: X = W done
+    B_D,                            // chain commit: state update (and Q M_n) done
+    B_O2,                           // chain commit: output accumulation done
+    B_DRAINM, B_DRAINC,             // commits of the error path (MMA warp, chain)
     NUM_BARS
 };
 
@@ -149,56 +152,37 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    float *As = reinterpret_cast<float *>(sm + OFF_AS);
-    float *Ts = reinterpret_cast<float *>(sm + OFF_TS);
-    float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
 
     const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
-    const uint32_t idesc_u = idesc_bf16(128, 64, true, false);
-    const uint32_t idesc_w = idesc_bf16(128, 64, false, true, true);
-    const uint32_t idesc_o = idesc_bf16(64, 128, false, false);
-    const uint32_t idesc_d = idesc_bf16(128, 128, false, true);
+    const uint32_t idesc_x = idesc_bf16(64, 128, false, true);   // K-major A, MN-major B
+    const uint32_t idesc_d = idesc_bf16(128, 128, true, true);
 
     if (warp < 8) {
         // ================================================================ prep
+        float *As = reinterpret_cast<float *>(sm + OFF_AS);
+        float *Ts = reinterpret_cast<float *>(sm + OFF_TS);
+        float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
         const int w = tid;
         const int qd = warp & 3, half = warp >> 2;   // TMEM lane quadrant, column half
         const int lrow = qd * 32 + (tid & 31);       // TMEM lane = accumulator row
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
-        bool issued = false;
         for (int k = 0; k < NC; ++k) {
-            const int st = k & 1, sl = k % NSCAL;
+            const int sl = k % NSCAL, b = k & 1;
             const int c = min(C, T - k * C);
             const Scal S = scal(sm, sl);
-            const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
-            const uint32_t v_a = sbase + OFF_V + st * V_BYTES;
+            uint8_t *lp = sm + OFF_LP + b * LP_BYTES;
 
-            bool ok = role_wait(bar(B_FULL0 + st), (uint32_t)(k >> 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_PREP, NPREP, ok)) break;
-            if (w == 0) {   // [K;Q] K^T  (the accumulator was read out last chunk)
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ad = kq_a + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_KQK, sdesc_sw128(ad, 16, 1024), sdesc_sw128(ad, 16, 1024),
-                             idesc_kqk, kk > 0);
-                }
-                mma_commit(bar(B_KQK));
-                issued = true;
-            }
-
-            // A = strict_lower(diag(beta gamma) K K^T diag(1/gamma)), P = lower(Q K^T) / gamma_C
-            ok = role_wait(bar(B_SCAL0 + sl), (uint32_t)(k / NSCAL) & 1u, a.limit_ns, &s_abort);
+            bool ok = role_wait(bar(B_SCAL0 + sl), (uint32_t)(k / NSCAL) & 1u, a.limit_ns, &s_abort);
             if (ok) ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
-            // A's space holds Lb / Lbg of chunk k-1 until its U / Wk products are done
-            if (ok && k > 0) ok = role_wait(bar(B_UWK), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
-            // P's buffer holds P of chunk k-2 until that chunk's output product is done
+            // buffer b holds Lb, P of chunk k-2 until the chain's last product reading them is done
             if (ok && k > 1)
-                ok = role_wait(bar(B_PFREE0 + st), (uint32_t)((k - 2) >> 1) & 1u, a.limit_ns, &s_abort);
+                ok = role_wait(bar(B_LPFREE0 + b), (uint32_t)((k - 2) >> 1) & 1u, a.limit_ns,
+                               &s_abort);
             if (!named_and(BAR_PREP, NPREP, ok)) break;
             const float igC = 1.f / s_gC[sl];
             tc_fence_after();
-            {   // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
+            {   // A = strict_lower(diag(beta gamma) K K^T diag(1/gamma)), P = lower(Q K^T) / gamma_C;
+                // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
                 const int h = half;
                 float v[32];
                 tmem_ld32(tl + TM_KQK + h * 32, v);
@@ -221,107 +205,134 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     const int r = lrow - 64;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = (h * 32 + e <= r && r < c) ? v[e] * igC : 0.f;
-                    st_halfrow_bf16(sm + OFF_P + st * 8192, r, h, v);
+                    st_halfrow_bf16(lp + 8192, r, h, v);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(BAR_PREP, NPREP);
+            if (w == 0) mbar_arrive(bar(B_KQKFREE));   // the next [K;Q]K^T may start
 
             solve_unit_lower(w, As, Ts, Ys);
-            {   // Lb = (T - I) diag(beta) + diag(bf16(beta)), Lbg likewise with beta gamma;
-                // thread -> (matrix w / 128, row w % 64, column half (w / 64) % 2)
-                const int r = w & 63, mat = w >> 7;
-                const float *sc = mat ? S.bg : S.bs;
-                uint8_t *dst = sm + (mat ? OFF_LBG : OFF_LB);
-                {
-                    const int h = (w >> 6) & 1;
-                    float v[32];
+            {   // Lb = strict_lower(T) diag(beta): thread -> row w % 64, columns 16 (w / 64) + 0..15
+                const int r = w & 63, q4 = w >> 6;
+                float v[16];
 #pragma unroll
-                    for (int s4 = 0; s4 < 32; s4 += 4) {
-                        const int s0 = h * 32 + s4;
-                        const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s0]);
-                        const float4 f = *reinterpret_cast<const float4 *>(&sc[s0]);
-                        v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : (s0 + 0 == r ? f.x : 0.f);
-                        v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : (s0 + 1 == r ? f.y : 0.f);
-                        v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : (s0 + 2 == r ? f.z : 0.f);
-                        v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : (s0 + 3 == r ? f.w : 0.f);
-                    }
-                    st_halfrow_bf16(dst, r, h, v);
+                for (int s4 = 0; s4 < 16; s4 += 4) {
+                    const int s0 = q4 * 16 + s4;
+                    const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s0]);
+                    const float4 f = *reinterpret_cast<const float4 *>(&S.bs[s0]);
+                    v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : 0.f;
+                    v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
+                    v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
+                    v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
                 }
-            }
-            named_sync(BAR_PREP, NPREP);     // T is read out; its space takes the residuals
-            if (w < 128) {   // Db = diag(beta - bf16(beta)), Dbg = diag(beta gamma - bf16(beta gamma))
-                const int r = w & 63;
-                const float x = (w < 64) ? S.bs[r] : S.bg[r];
-                const float lo = x - __bfloat162float(__float2bfloat16_rn(x));
-                uint8_t *dst = sm + ((w < 64) ? OFF_DB : OFF_DBG);
-                const __nv_bfloat16 lo16 = __float2bfloat16_rn(lo);
-                const uint32_t lo_bits = (uint32_t)*reinterpret_cast<const unsigned short *>(&lo16);
-                const uint32_t word = lo_bits << (16 * (r & 1));
-                const int wi = (r & 7) >> 1;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const bool here = (r >> 3) == ch;
-                    *reinterpret_cast<uint4 *>(dst + r * 128u + ((ch ^ (r & 7u)) << 4)) =
-                        make_uint4(here && wi == 0 ? word : 0u, here && wi == 1 ? word : 0u,
-                                   here && wi == 2 ? word : 0u, here && wi == 3 ? word : 0u);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t ch = (uint32_t)(q4 * 2 + h2);
+                    uint4 u;
+                    u.x = pack_bf16x2(v[h2 * 8 + 0], v[h2 * 8 + 1]);
+                    u.y = pack_bf16x2(v[h2 * 8 + 2], v[h2 * 8 + 3]);
+                    u.z = pack_bf16x2(v[h2 * 8 + 4], v[h2 * 8 + 5]);
+                    u.w = pack_bf16x2(v[h2 * 8 + 6], v[h2 * 8 + 7]);
+                    *reinterpret_cast<uint4 *>(lp + r * 128u + ((ch ^ (uint32_t)(r & 7)) << 4)) = u;
                 }
             }
             fence_proxy_async_smem();
-            // U^T = V^T (Lb + Db)^T into W^T buffer st (free once the chain read chunk k-2's
-            // W^T);  Wk^T = K^T (Lbg + Dbg)^T
-            ok = (k < 2) || role_wait(bar(B_RWFREE0 + st), (uint32_t)((k - 2) >> 1) & 1u,
-                                      a.limit_ns, &s_abort);
-            if (ok && k > 0) ok = role_wait(bar(B_WKFREE), (uint32_t)(k - 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_PREP, NPREP, ok)) break;
-            if (w == 0) {
+            named_sync(BAR_PREP, NPREP);
+            if (w == 0) mbar_arrive(bar(B_LREADY0 + b));
+        }
+    } else if (warp == 13) {
+        // ================================================================ MMA issue
+        // [K;Q]K^T of chunk k+1 once stage k+1 has landed and the preparation has read
+        // chunk k's accumulator.
+        if ((tid & 31) == 0) {
+            bool issued = false;
+            auto kqk = [&](int k) {
+                const uint32_t kq_a = sbase + OFF_KQ + (k & 1) * KQ_BYTES;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_W + st * 64, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
-                             sdesc_sw128(sbase + OFF_LB + kk * 32, 16, 1024), idesc_u, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_W + st * 64, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
-                             sdesc_sw128(sbase + OFF_DB + kk * 32, 16, 1024), idesc_u, 1);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_WK, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
-                             sdesc_sw128(sbase + OFF_LBG + kk * 32, 16, 1024), idesc_u, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_WK, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
-                             sdesc_sw128(sbase + OFF_DBG + kk * 32, 16, 1024), idesc_u, 1);
-                mma_commit(bar(B_UWK));
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ad = kq_a + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + TM_KQK, sdesc_sw128(ad, 16, 1024), sdesc_sw128(ad, 16, 1024),
+                             idesc_kqk, kk > 0);
+                }
+                mma_commit(bar(B_KQK));
+                issued = true;
+            };
+            bool ok = role_wait(bar(B_FULL0), 0u, a.limit_ns, &s_abort);
+            if (ok) kqk(0);
+            for (int k = 0; ok && k + 1 < NC; ++k) {
+                ok = role_wait(bar(B_KQKFREE), (uint32_t)k & 1u, a.limit_ns, &s_abort);
+                if (ok)
+                    ok = role_wait(bar(B_FULL0 + ((k + 1) & 1)), (uint32_t)((k + 1) >> 1) & 1u,
+                                   a.limit_ns, &s_abort);
+                if (ok) kqk(k + 1);
             }
-
+            if (s_abort && issued) {   // let this thread's MMAs land before TMEM goes away
+                mma_commit(bar(B_DRAINM));
+                mbar_wait(bar(B_DRAINM), 0u, kCleanupLimitNs);
+            }
         }
-        if (s_abort && w == 0 && issued) {   // let this thread's MMAs land before TMEM goes away
-            mma_commit(bar(B_DRAINP));
-            mbar_wait(bar(B_DRAINP), 0u, kCleanupLimitNs);
-        }
+        __syncwarp();
     } else if (warp < 12) {
         // ================================================================ chain
-        const int w = tid - 256;    // = TMEM lane (row j of the transposed products)
-        const int j = w;
-        const int lane = w & 31;
-        const uint32_t tl = tmem + ((uint32_t)((warp - 8) * 32) << 16);
+        const int w = tid - 256;                 // TMEM lane of the M = 128 state: row i
+        const int lane = w & 31, qd = warp - 8;
+        const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+        // M = 64 layout: this thread reads row 16 qd + lane % 16, columns 64 (lane / 16) + 0..63
+        const int r64 = 16 * qd + (lane & 15), h64 = lane >> 4;
         bool issued = false;
+
+        // out rows of chunk m: gamma_r O[r][:], this thread's row and column half
+        auto output_epilogue = [&](int m) {
+            const int cm = min(C, T - m * C);
+            const Scal Sm = scal(sm, m % NSCAL);
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                float v[32];
+                tmem_ld32_m64<64>(tl + TM_O + cb * 32, v);
+                tmem_wait_ld();
+                if (r64 < cm) {
+                    const float gr = Sm.gam[r64];
+                    uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + m * C + r64) * D +
+                                                            h64 * 64 + cb * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 u;
+                        u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
+                        u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
+                        u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
+                        u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+                        __stcs(orow + q4, u);
+                    }
+                }
+            }
+        };
+        // X = K M_n into TMEM (chunk n's stage)
+        auto issue_km = [&](int n) {
+            const uint32_t kq_a = sbase + OFF_KQ + (n & 1) * KQ_BYTES;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tmem + TM_X, sdesc_sw128(kq_a + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                         sdesc_sw128(sbase + OFF_MS + kk * 2048, 16384, 1024), idesc_x, kk > 0);
+            mma_commit(bar(B_KM));
+            issued = true;
+        };
+
         bool ok = role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
         ok = named_and(BAR_CHAIN, 128, ok);
         if (ok) {
-            // initial state: TMEM M^T <- gamma_C(0) M0^T, MT <- bf16(M0^T)
+            // initial state: TMEM M <- gamma_C(0) M_0, MS <- bf16(M_0); thread = row i
             const float gC = s_gC[0];
+            const float *src = a.init ? a.init + ((int64_t)bh * D + w) * D : nullptr;
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float v[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int i = cb * 32 + e;
-                    v[e] = a.init ? a.init[((int64_t)bh * D + i) * D + j] : 0.f;
-                }
-                st_halfrow_bf16(sm + OFF_MT + (cb >> 1) * 16384, j, cb & 1, v);
+                for (int e = 0; e < 32; ++e) v[e] = src ? src[cb * 32 + e] : 0.f;
+                st_halfrow_bf16(sm + OFF_MS + (cb >> 1) * 16384, w, cb & 1, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= gC;
                 tmem_st32(tl + TM_M + cb * 32, v);
@@ -329,92 +340,115 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(BAR_CHAIN, 128);
+            ok = role_wait(bar(B_FULL0), 0u, a.limit_ns, &s_abort);
+            ok = named_and(BAR_CHAIN, 128, ok);
+            if (ok && w == 0) issue_km(0);
         }
         for (int n = 0; ok && n < NC; ++n) {
-            const int st = n & 1, sl = n % NSCAL, sl1 = (n + 1) % NSCAL;
-            const int t0 = n * C;
-            const int c = min(C, T - t0);
+            const int st = n & 1, b = n & 1, sl = n % NSCAL, sl1 = (n + 1) % NSCAL;
             const Scal S = scal(sm, sl);
             const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
+            const uint32_t lp_a = sbase + OFF_LP + b * LP_BYTES;
             const bool last = (n + 1 == NC);
 
-            // ---- Wk^T -> WkT (bf16, MN-major, row i = this lane)
-            ok = role_wait(bar(B_FULL0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
-            if (ok) ok = role_wait(bar(B_UWK), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            // ---- output of chunk n-1 (its O is complete once O2(n-1) lands), overlapping
+            // K M_n on the tensor core
+            if (n > 0) {
+                ok = role_wait(bar(B_O2), (uint32_t)(n - 1) & 1u, a.limit_ns, &s_abort);
+                if (w == 0 && ok) mbar_arrive_relaxed(bar(B_LPFREE0 + (b ^ 1)));
+                if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+                tc_fence_after();
+                output_epilogue(n - 1);
+            }
+
+            // ---- E = V - gamma K M_n -> EW (bf16); X <- beta E (fp32, the identity part of W)
+            ok = role_wait(bar(B_KM), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            if (ok) ok = role_wait(bar(B_LREADY0 + b), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
+            {
+                const float gr = S.gam[r64], br = S.bs[r64];
+                const uint8_t *vrow = sm + OFF_V + st * V_BYTES + h64 * 8192 + r64 * 128;
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float v[32];
-                tmem_ld32(tl + TM_WK + h * 32, v);
-                tmem_wait_ld();
-                st_halfrow_bf16(sm + OFF_WKT, w, h, v);
+                for (int cb = 0; cb < 2; ++cb) {
+                    float x[32];
+                    tmem_ld32_m64<64>(tl + TM_X + cb * 32, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint32_t ch = (uint32_t)(cb * 4 + q4);
+                        const uint4 u = *reinterpret_cast<const uint4 *>(
+                            vrow + ((ch ^ (uint32_t)(r64 & 7)) << 4));
+                        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int p2 = 0; p2 < 4; ++p2) {
+                            const float2 f = __bfloat1622float2(
+                                *reinterpret_cast<const __nv_bfloat162 *>(&wv[p2]));
+                            x[q4 * 8 + 2 * p2 + 0] = fmaf(-gr, x[q4 * 8 + 2 * p2 + 0], f.x);
+                            x[q4 * 8 + 2 * p2 + 1] = fmaf(-gr, x[q4 * 8 + 2 * p2 + 1], f.y);
+                        }
+                    }
+                    st_halfrow_bf16(sm + OFF_EW + h64 * 8192, r64, cb, x);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] *= br;
+                    tmem_st32_m64<64>(tl + TM_X + cb * 32, x);
+                }
+                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(BAR_CHAIN, 128);
-            // ---- W^T = U^T - M^T Wk^T ;  O = Q M
-            if (w == 0) {
-                mbar_arrive(bar(B_WKFREE));
+            if (w == 0) {   // X += Lb E (so X = W) ;  O = Q M_n
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + TM_W + st * 64,
-                             sdesc_sw128(sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                             sdesc_sw128(sbase + OFF_WKT + kk * 2048, 16384, 1024), idesc_w, 1);
-                mma_commit(bar(B_W));
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_X, sdesc_sw128(lp_a + kk * 32, 16, 1024),
+                             sdesc_sw128(sbase + OFF_EW + kk * 2048, 8192, 1024), idesc_x, 1);
+                mma_commit(bar(B_C3));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tmem + TM_O,
                              sdesc_sw128(kq_a + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                             sdesc_sw128(sbase + OFF_MT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                             idesc_o, kk > 0);
-                issued = true;
+                             sdesc_sw128(sbase + OFF_MS + kk * 2048, 16384, 1024), idesc_x, kk > 0);
             }
 
-            // ---- Wt^T[j][s] = W^T[j][s] * gamma_C / gamma_s -> WtT (row j); then D(n)
-            ok = role_wait(bar(B_W), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+            // ---- Wt = diag(gamma_C / gamma) W -> EW (bf16)
+            ok = role_wait(bar(B_C3), (uint32_t)n & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
+            {
+                const float sr = S.sc[r64];
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float v[32];
-                tmem_ld32(tl + TM_W + st * 64 + h * 32, v);
-                tmem_wait_ld();
+                for (int cb = 0; cb < 2; ++cb) {
+                    float x[32];
+                    tmem_ld32_m64<64>(tl + TM_X + cb * 32, x);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int e4 = 0; e4 < 32; e4 += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(&S.sc[h * 32 + e4]);
-                    v[e4 + 0] *= f.x;
-                    v[e4 + 1] *= f.y;
-                    v[e4 + 2] *= f.z;
-                    v[e4 + 3] *= f.w;
+                    for (int e = 0; e < 32; ++e) x[e] *= sr;
+                    st_halfrow_bf16(sm + OFF_EW + h64 * 8192, r64, cb, x);
                 }
-                st_halfrow_bf16(sm + OFF_WTT, j, h, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(BAR_CHAIN, 128);
-            if (w == 0) {
-                mbar_arrive(bar(B_RWFREE0 + st));
+            if (w == 0) {   // M += K^T Wt ;  O += P Wt
                 tc_fence_after();
-                // M^T += Wt^T K ;  O += P Wt
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_M, sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024),
-                             sdesc_sw128(kq_a + kk * 2048, 16384, 1024), idesc_d, 1);
-                mma_commit(bar(B_D));       // the state update needs only this
+                    mma_bf16(tmem + TM_M, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
+                             sdesc_sw128(sbase + OFF_EW + kk * 2048, 8192, 1024), idesc_d, 1);
+                mma_commit(bar(B_D));
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_P + st * 8192 + kk * 32, 16, 1024),
-                             sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024), idesc_o, 1);
+                    mma_bf16(tmem + TM_O, sdesc_sw128(lp_a + 8192 + kk * 32, 16, 1024),
+                             sdesc_sw128(sbase + OFF_EW + kk * 2048, 8192, 1024), idesc_x, 1);
                 mma_commit(bar(B_O2));
             }
 
-            // ---- state: MT <- bf16(M^T_{n+1}); TMEM M^T <- gamma_C(n+1) M^T_{n+1}
+            // ---- state: MS <- bf16(M_{n+1}); TMEM M <- gamma_C(n+1) M_{n+1}; thread = row i
             ok = role_wait(bar(B_D), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-            // every MMA that reads this input stage is complete: let the copy warp refill it
-            if (w == 0 && ok) mbar_arrive(bar(B_OSTAGE0 + st));
+            // every product reading this input stage is complete: let the copy warp refill it
+            if (w == 0 && ok) mbar_arrive(bar(B_KQFREE0 + st));
             if (ok && !last)
                 ok = role_wait(bar(B_SCAL0 + sl1), (uint32_t)((n + 1) / NSCAL) & 1u, a.limit_ns,
                                &s_abort);
@@ -422,72 +456,44 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after();
             {
                 const float gn = last ? 1.f : s_gC[sl1];
-                float va[32];
-                auto consume = [&](int cb, float (&v)[32]) {
+                float *fin = (last && a.final_state) ? a.final_state + ((int64_t)bh * D + w) * D
+                                                     : nullptr;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float v[32];
+                    tmem_ld32(tl + TM_M + cb * 32, v);
+                    tmem_wait_ld();
                     if (last) {
-                        if (a.final_state) {
-                            float *f = a.final_state + (int64_t)bh * D * D + j;
+                        if (fin) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) f[(int64_t)(cb * 32 + e) * D] = v[e];
+                            for (int e = 0; e < 32; ++e) fin[cb * 32 + e] = v[e];
                         }
                     } else {
-                        st_halfrow_bf16(sm + OFF_MT + (cb >> 1) * 16384, j, cb & 1, v);
+                        st_halfrow_bf16(sm + OFF_MS + (cb >> 1) * 16384, w, cb & 1, v);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] *= gn;
                         tmem_st32(tl + TM_M + cb * 32, v);
                     }
-                };
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    tmem_ld32(tl + TM_M + cb * 32, va);
-                    tmem_wait_ld();
-                    consume(cb, va);
                 }
                 tmem_wait_st();
             }
-            // ---- output row r = gamma_r O[r][:]: lanes 0..15 of each quadrant hold
-            // rows 16 q .. 16 q + 15 (the M = 64 TMEM layout), 128 columns each
-            ok = role_wait(bar(B_O2), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-            if (w == 0 && ok) mbar_arrive(bar(B_PFREE0 + st));
-            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
-            tc_fence_after();
-            {
-                const int r = 16 * (warp - 8) + (lane & 15);
-                const bool has_row = (lane < 16) && (r < c);
-                const float gr = S.gam[r];
-                uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + t0 + r) * D);
-                float va[32], vb[32];
-                auto emit = [&](int cb, const float (&v)[32]) {
-                    if (has_row) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 u;
-                            u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
-                            u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
-                            u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
-                            u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
-                            __stcs(orow + cb * 4 + q4, u);
-                        }
-                    }
-                };
-                // warp-wide loads (lanes 16..31 unused); the next block loads while
-                // the current one is converted and stored
-                tmem_ld32(tl + TM_O + 0, va);
-                tmem_wait_ld();
-                tmem_ld32(tl + TM_O + 32, vb);
-                emit(0, va);
-                tmem_wait_ld();
-                tmem_ld32(tl + TM_O + 64, va);
-                emit(1, vb);
-                tmem_wait_ld();
-                tmem_ld32(tl + TM_O + 96, vb);
-                emit(2, va);
-                tmem_wait_ld();
-                emit(3, vb);
-            }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(BAR_CHAIN, 128);
+            if (!last) {   // K M_{n+1} as soon as its stage has landed
+                ok = role_wait(bar(B_FULL0 + (st ^ 1)), (uint32_t)((n + 1) >> 1) & 1u, a.limit_ns,
+                               &s_abort);
+                if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+                if (w == 0) issue_km(n + 1);
+            } else {
+                named_sync(BAR_CHAIN, 128);
+            }
+        }
+        if (ok) {   // output of the last chunk
+            ok = role_wait(bar(B_O2), (uint32_t)(NC - 1) & 1u, a.limit_ns, &s_abort);
+            if (named_and(BAR_CHAIN, 128, ok)) {
+                tc_fence_after();
+                output_epilogue(NC - 1);
+            }
         }
         if (s_abort && w == 0 && issued) {
             mma_commit(bar(B_DRAINC));
@@ -496,7 +502,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     } else {
         // ================================================================ copy
         const int lane = tid & 31;
-        uint32_t issued[2] = {0, 0};
+        uint32_t issued[NSTAGE] = {0, 0};
         auto issue_tma = [&](int n) {     // lane 0 only
             const int st = n & 1;
             const uint32_t b = bar(B_FULL0 + st);
@@ -536,28 +542,28 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (lane == 0) mbar_arrive(bar(B_SCAL0 + sl));
         };
         float gv[2], bv[2];
-        for (int n = 0; n < 2 && n < NC; ++n) {
+        for (int n = 0; n < NSTAGE && n < NC; ++n) {
             load_gb(n, gv, bv);
             if (lane == 0) issue_tma(n);
             decay(n, gv, bv);
         }
         if (lane == 0)
-            for (int n = 2; n < 2 + kL2Ahead; ++n) prefetch_l2(n);
-        if (NC > 2) load_gb(2, gv, bv);
-        for (int n = 0; n + 2 < NC; ++n) {   // refill a stage once chunk n is done with it
+            for (int n = NSTAGE; n < NSTAGE + kL2Ahead; ++n) prefetch_l2(n);
+        if (NC > NSTAGE) load_gb(NSTAGE, gv, bv);
+        for (int n = 0; n + NSTAGE < NC; ++n) {   // refill a stage once chunk n is done with it
             const int st = n & 1;
-            bool ok = role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
+            bool ok = role_wait(bar(B_KQFREE0 + st), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (lane == 0) {
-                issue_tma(n + 2);
-                prefetch_l2(n + 2 + kL2Ahead);
+                issue_tma(n + NSTAGE);
+                prefetch_l2(n + NSTAGE + kL2Ahead);
             }
-            decay(n + 2, gv, bv);
-            if (n + 3 < NC) load_gb(n + 3, gv, bv);
+            decay(n + NSTAGE, gv, bv);
+            if (n + NSTAGE + 1 < NC) load_gb(n + NSTAGE + 1, gv, bv);
         }
         if (s_abort && lane == 0) {
             // at most the latest load of each stage can still be in flight
-            for (int st = 0; st < 2; ++st)
+            for (int st = 0; st < NSTAGE; ++st)
                 if (issued[st] > 0)
                     mbar_wait(bar(B_FULL0 + st), (issued[st] - 1) & 1u, kCleanupLimitNs);
         }
@@ -570,19 +576,15 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
 }
 
-// Two CTAs per head (the value-split kernel) while they fit on the GPU in one
-// wave; one CTA per head beyond that, where every SM already has a head.
+// A cluster of two CTAs per head while every head's cluster is resident at
+// once; one CTA per head beyond that, where every SM already has a head.
 // GDR_FUSED_VARIANT=single|pair overrides the choice (used by the tests to
 // cover both kernels on small shapes).
 bool use_pair(int BH) {
     const char *env = std::getenv("GDR_FUSED_VARIANT");
     if (env && std::strcmp(env, "single") == 0) return false;
     if (env && std::strcmp(env, "pair") == 0) return true;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return false;
-    return 2 * (int64_t)BH <= sms;
+    return BH <= fused_pair_max_clusters();
 }
 
 }  // namespace

@@ -27,6 +27,7 @@ constexpr int C = 64;      // chunk
 constexpr int D = 128;     // dk (and dv of the input tensors)
 constexpr int NPREP = 256; // threads of the preparation warps
 constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;   // named barriers (0 is __syncthreads)
+constexpr uint32_t BAR_EROWS = 3, BAR_OROWS = 4;  // chain warps owning rows 0-63 / 64-127 of X
 constexpr int LDA = 68;    // fp32 row stride of the solve matrices
 constexpr int LDY = 40;    // row stride of the merge scratch
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
@@ -62,9 +63,13 @@ __device__ __forceinline__ void st_halfrow_bf16(uint8_t *tile, uint32_t row, uin
     }
 }
 
-// Bounded wait used by the warpgroups: gives up when the CTA-wide abort flag
-// is raised or the time limit passes (then raises the flag and the error word).
-__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+// Bounded wait used by the warp roles: gives up when the CTA-wide abort flag is
+// raised or the time limit passes (then raises the flag and the error word).
+// Each try suspends the thread until the phase completes or kWaitSliceNs pass,
+// so a waiting thread takes no issue slots from the working warps; one thread
+// per role waits and a named barrier passes the result on.
+constexpr uint32_t kWaitSliceNs = 20000;
+__device__ __noinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int *abort) {
     if (mbar_test_wait(bar, parity)) return true;      // non-blocking first look
     if (limit_ns == 0) {                                // injected timeout: give up at once
@@ -74,7 +79,29 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_
     }
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            atomicOr(&g_device_error_word, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// role_wait for barriers that another CTA of the cluster arrives on
+// (cluster-scope acquire).
+__device__ __noinline__ bool role_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile int *abort) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (limit_ns == 0) {
+        *abort = 1;
+        atomicOr(&g_device_error_word, kDevErrTimeout);
+        return false;
+    }
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster_hint(bar, parity, kWaitSliceNs)) return true;
         if (*abort) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort = 1;
@@ -89,12 +116,18 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_
 // inclusive scan of log alpha, gamma = exp(scan), 1/gamma, beta, beta gamma,
 // gamma_C (the last valid row) and gamma_C / gamma.  Rows past the chunk's end
 // get gamma = 1, beta = 0 and gamma_C / gamma = 0 so that they drop out of
-// every product.
-__device__ __forceinline__ void warp_decay(int lane, const float (&gv)[2], const float (&bv)[2],
-                                           int c, float a_min, Scal s, float *s_gC) {
+// every product.  log alpha = log1p(-(1 - a_min) / (1 + e^g)) keeps alpha
+// close to 1 accurate; the exponentials and reciprocals use the hardware
+// approximations (relative error below 1e-5 over the range the range rule
+// allows, far inside the bf16 tolerance of the fused path).  Not inlined: the
+// copy warp calls it at two places and its code would otherwise crowd the
+// instruction cache the other warps share.
+__device__ __noinline__ void warp_decay(int lane, const float (&gv)[2], const float (&bv)[2],
+                                        int c, float a_min, Scal s, float *s_gC) {
     const int r0 = 2 * lane;
-    const float l0 = (r0 < c) ? log_alpha(gv[0], a_min) : 0.f;
-    const float l1 = (r0 + 1 < c) ? log_alpha(gv[1], a_min) : 0.f;
+    const float om = 1.0f - a_min;
+    const float l0 = (r0 < c) ? log1pf(-__fdividef(om, 1.0f + __expf(gv[0]))) : 0.f;
+    const float l1 = (r0 + 1 < c) ? log1pf(-__fdividef(om, 1.0f + __expf(gv[1]))) : 0.f;
     float incl = l0 + l1;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -104,18 +137,19 @@ __device__ __forceinline__ void warp_decay(int lane, const float (&gv)[2], const
     const float b1 = incl, b0 = incl - l1;
     // gamma_C: the scan value of row c - 1, held by lane (c - 1) / 2
     const float bC = __shfl_sync(0xffffffffu, ((c - 1) & 1) ? b1 : b0, (c - 1) >> 1);
-    const float gC = expf(bC);
+    const float gC = __expf(bC);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int r = r0 + e;
         const bool valid = r < c;
-        const float gam = valid ? expf(e ? b1 : b0) : 1.f;
+        const float gam = valid ? __expf(e ? b1 : b0) : 1.f;
+        const float ig = __frcp_rn(gam);
         const float b = valid ? bv[e] : 0.f;
         s.gam[r] = gam;
-        s.ig[r] = 1.f / gam;
+        s.ig[r] = ig;
         s.bs[r] = b;
         s.bg[r] = b * gam;
-        s.sc[r] = valid ? gC / gam : 0.f;
+        s.sc[r] = valid ? gC * ig : 0.f;
     }
     if (lane == 0) *s_gC = gC;
     __syncwarp();
@@ -251,6 +285,7 @@ struct FusedArgs {
     float a_min;
     int T;
     uint64_t limit_ns;
+    const __nv_bfloat16 *v = nullptr;   // read directly by kernels that load v rows themselves
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

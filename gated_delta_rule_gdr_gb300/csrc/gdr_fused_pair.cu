@@ -1,46 +1,43 @@
-// gdr_fused_pair.cu -- fused chunked prefill with the value columns of each
-// head split over two CTAs.
+// gdr_fused_pair.cu -- fused chunked prefill with each head on a cluster of
+// two CTAs: the value columns split between them, and the state-independent
+// preparation of the chunks alternated between them and shared over DSMEM.
 //
-// Same method and the same chunk algebra as the one-CTA-per-head kernel in
-// gdr_fused.cu (the lower-bounded decay keeps 1/gamma finite, so every causal
-// tile is one dense product with diagonal scalings: "What a Trillion-Parameter
-// MoE Model Reveals About the Next Stage of LLM Scaling", sections 3.1-3.3).
-// What changes is the split of the work.  CTA rho of head bh owns the value
-// columns J = [64 rho, 64 rho + 64): its state block M_J = S^T[:, J] (dk x 64,
-// fp32, in TMEM), its U_J, W_J, Wt_J, and the output columns O[:, J].  Every
-// one of those products touches only J, so the two CTAs never exchange data.
-// The state-independent preparation of a chunk (A and P from [K;Q]K^T, the
-// triangular solve, Lb / Lbg, Wk) does not depend on J and is done by both
-// CTAs; an SM that would otherwise sit idle repeats it.  With half the value
-// columns the state chain per chunk halves, and the shared memory saved buys
-// a third input stage, so the preparation runs further ahead of the chain.
-// The launcher picks this kernel when two CTAs per head still fit on the GPU
-// in one wave.
+// Same method and chunk algebra as the one-CTA-per-head kernel (gdr_fused.cu:
+// the lower-bounded decay keeps 1/gamma finite, so every causal tile is one
+// dense product with diagonal scalings -- "What a Trillion-Parameter MoE Model
+// Reveals About the Next Stage of LLM Scaling", sections 3.1-3.3):
+//   E = V - diag(gamma) K M_n,   W = diag(beta) E + Lb E,   Wt = diag(gamma_C/gamma) W,
+//   O = diag(gamma) (Q M_n + P Wt),   M_{n+1} = gamma_C M_n + K^T Wt,
+// with Lb = strict_lower(T) diag(beta), T = (I + A)^-1, P = lower_incl(Q K^T)/gamma_C.
 //
-// Products per chunk (orientation chosen so that shared-memory copies are
-// written row by row from the TMEM rows that hold them):
-//   U_J^T  = V_J^T (Lb + Db)^T            M = 64,  N = 64, K = 64   (prep)
-//   Wk^T   = K^T (Lbg + Dbg)^T            M = 128, N = 64, K = 64   (prep)
-//   W_J^T  = U_J^T - M_J^T Wk^T           M = 64,  N = 64, K = 128  (chain)
-//   O_J    = Q M_J (+ P Wt_J)             M = 64,  N = 64, K = 128 (+64)
-//   M_J   += K^T Wt_J                     M = 128, N = 64, K = 64
-// with the state kept as gamma_C-prescaled fp32 M_J in TMEM and a bf16 copy
-// MS = bf16(M_J) ([i][j], the MN-major operand of both W_J^T and O_J).
-// Lb = (T - I) diag(beta) + diag(bf16(beta)) and Db = diag(beta - bf16(beta))
-// (Lbg, Dbg likewise with beta gamma): the identity part of T enters the
-// products as a bf16 value plus its bf16 residual, exact to ~2^-17.
+// Work split.  CTA rho (the cluster rank) owns the value columns J = [64 rho,
+// 64 rho + 64): the state block M_J = M[:, J] (fp32 in TMEM, bf16 copy MS), E_J,
+// W_J, Wt_J and O[:, J].  Those products touch only J.  The preparation of
+// chunk k -- [K;Q]K^T, A and P, the triangular solve, Lb -- does not depend on
+// J: CTA (k mod 2) does it and writes Lb and P into its own shared memory and
+// into its peer's (st.shared::cluster), then arrives on the peer's mbarrier.
+// Each CTA so prepares every other chunk and runs the state chain of all of
+// them on half the columns.
 //
-// Warp roles (448 threads): prep warps 0-7, chain warps 8-11, copy warp 12,
-// and warp 13, which issues the preparation's tensor-core products ([K;Q]K^T
-// of the next chunk as soon as its accumulator is read out, U_J^T and Wk^T
-// once Lb / Lbg are written), so that the preparation warps never stall on a
-// busy tensor-core queue.  The chain issues its own products.
-// Shared memory: KQ[3] 32 KB, V_J[3] 8 KB, MS 16 KB, WkT 16 KB, WtT 8 KB,
-// P[2] 8 KB, the fp32 solve space (A, T; Lb / Lbg take A's space and Db / Dbg
-// T's once the solve is done), the merge scratch and 4 slots of per-chunk
-// scalars.
-// TMEM: [K;Q]K^T 64 cols, W_J^T 2 x 64 (M = 64 layout), Wk^T 2 x 64, O_J 64
-// (M = 64 layout), M_J 64.
+// Products of the chain per chunk (M = 128 accumulators, X in TMEM):
+//   X  = [K;Q] MS                      N = 64, K = 128  (rows 0-63 K M_n, 64-127 Q M_n)
+//   X += [Lb;0] E                      N = 64, K = 64   (rows 0-63 become W)
+//   M += K^T Wt                        N = 64, K = 64
+//   X += [0;P] Wt                      N = 64, K = 64   (rows 64-127 become O / gamma)
+// where E's bf16 copy feeds the second product and the chain first stores
+// diag(beta) E in fp32 over X's rows 0-63, so the identity part of T is exact.
+// The zero halves come from an 8 KB zero tile between Lb and P.
+//
+// Warp roles (448 threads): prep 0-7, chain 8-11 (warps 8-9 own X rows 0-63,
+// warps 10-11 rows 64-127), copy 12 (TMA of K and Q, decay, L2 prefetch of
+// K, Q and V), MMA 13 ([K;Q]K^T of the chunks this CTA prepares).  v rows are
+// read by the chain straight from global memory (L2) into registers.
+//
+// Shared memory: KQ[3] 32 KB, MS 16 KB ([i][j] bf16, MN-major), EW 8 KB
+// ([s][j] bf16, MN-major; E, then Wt), LP[2] 24 KB ([Lb | 0 | P], K-major;
+// LP[rho] holds the chunks this CTA prepares, LP[1 - rho] its peer's), the fp32
+// solve space (A, T), merge scratch, 4 slots of per-chunk scalars.
+// TMEM: [K;Q]K^T 64 cols, X[2] 2 x 64, M_J 64.
 
 #include "gdr_fused_common.cuh"
 
@@ -53,34 +50,28 @@ constexpr int NSTAGE = 3;  // input stages
 constexpr int NSCAL = 4;   // scalar slots (chunk m uses slot m % 4)
 
 // shared-memory map (bytes from the 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;              // 3 x 32 KB: [slab i/64][K rows | Q rows][128 B]
+constexpr uint32_t OFF_KQ = 0;              // [slab i/64][K rows | Q rows][128 B]
 constexpr uint32_t KQ_BYTES = 32768;
-constexpr uint32_t OFF_V = OFF_KQ + NSTAGE * KQ_BYTES;   // 3 x 8 KB: V[:, J] rows
-constexpr uint32_t V_BYTES = 8192;
-constexpr uint32_t OFF_MS = OFF_V + NSTAGE * V_BYTES;    // 16 KB: bf16 M_J [i][j]
-constexpr uint32_t OFF_WKT = OFF_MS + 16384;             // 16 KB: bf16 Wk^T [i][s]
-constexpr uint32_t OFF_WTT = OFF_WKT + 16384;            // 8 KB: bf16 Wt_J^T [j][s]
-constexpr uint32_t OFF_P = OFF_WTT + 8192;               // 2 x 8 KB: bf16 P [r][s]
-constexpr uint32_t OFF_AS = OFF_P + 2 * 8192;            // 64 x 68 fp32; Lb, Lbg after the solve
-constexpr uint32_t OFF_LB = OFF_AS;
-constexpr uint32_t OFF_LBG = OFF_AS + 8192;
-constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;       // 64 x 68 fp32; Db, Dbg after the solve
-constexpr uint32_t OFF_DB = OFF_TS;
-constexpr uint32_t OFF_DBG = OFF_TS + 8192;
-constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;       // 32 x 40 fp32
-constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;       // 4 slots x 5 x 64 fp32
+constexpr uint32_t OFF_MS = OFF_KQ + NSTAGE * KQ_BYTES;   // 16 KB
+constexpr uint32_t OFF_EW = OFF_MS + 16384;               // 8 KB
+constexpr uint32_t OFF_VB = OFF_EW + 8192;                // 8 KB: v[chunk rows][J] (TMA)
+constexpr uint32_t OFF_LP = OFF_VB + 8192;                // 2 x [Lb 8 KB | zeros 8 KB | P 8 KB]
+constexpr uint32_t LP_BYTES = 24576;
+constexpr uint32_t LP_P = 16384;                          // offset of P in an LP buffer
+constexpr uint32_t OFF_AS = OFF_LP + 2 * LP_BYTES;        // 64 x 68 fp32
+constexpr uint32_t OFF_TS = OFF_AS + 64 * LDA * 4;        // 64 x 68 fp32
+constexpr uint32_t OFF_YS = OFF_TS + 64 * LDA * 4;        // 32 x 40 fp32
+constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;        // 4 slots x 5 x 64 fp32
 constexpr uint32_t SMEM_USED = OFF_SC + NSCAL * 5 * 64 * 4;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;        // alignment slack
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;         // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
-static_assert(OFF_V % 1024 == 0 && OFF_MS % 1024 == 0 && OFF_WKT % 1024 == 0 &&
-                  OFF_WTT % 1024 == 0 && OFF_P % 1024 == 0 && OFF_AS % 1024 == 0 &&
-                  OFF_TS % 1024 == 0,
+static_assert(OFF_MS % 1024 == 0 && OFF_EW % 1024 == 0 && OFF_VB % 1024 == 0 && OFF_LP % 1024 == 0 &&
+                  LP_BYTES % 1024 == 0,
               "swizzled operands must be 1024-byte aligned");
 
 // TMEM columns
-constexpr uint32_t TM_KQK = 0, TM_W = 64 /* 2 x 64 */, TM_WK = 192 /* 2 x 64 */, TM_O = 320,
-                   TM_M = 384;
-constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TM_KQK = 0, TM_X = 64 /* 2 x 64 */, TM_M = 192;
+constexpr uint32_t TM_COLS = 256;
 
 constexpr int kL2Ahead = 3;   // chunks prefetched into L2 beyond the three staged in SMEM
 
@@ -88,27 +79,52 @@ __device__ __forceinline__ Scal scal(uint8_t *sm, int slot) {
     return scal_at(reinterpret_cast<float *>(sm + OFF_SC) + slot * 5 * 64);
 }
 
+// Output row r (< 64) of a chunk with c valid rows, this CTA's 64 columns:
+// out[r][:] = gamma_r X[64 + r][:], X in TMEM at column x (this thread's lane
+// = 64 + r).  One copy for both call sites.
+__device__ __noinline__ void emit_output_rows(uint32_t x, int r, int c, const float *gam,
+                                              __nv_bfloat16 *out0) {
+#pragma unroll 1
+    for (int cb = 0; cb < 2; ++cb) {
+        float v[32];
+        tmem_ld32(x + cb * 32, v);
+        tmem_wait_ld();
+        if (r < c) {
+            const float gr = gam[r];
+            uint4 *orow = reinterpret_cast<uint4 *>(out0 + (int64_t)r * D + cb * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint4 u;
+                u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
+                u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
+                u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
+                u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+                __stcs(orow + q4, u);
+            }
+        }
+    }
+}
+
 // mbarriers of the pipeline (index into s_bar)
 enum : int {
     B_FULL0 = 0,                       // copy: TMA inputs of a stage landed (x3)
-    B_OSTAGE0 = B_FULL0 + NSTAGE,      // chain: every MMA reading a stage is done (x3)
-    B_SCAL0 = B_OSTAGE0 + NSTAGE,      // copy: decay scalars of a chunk written (x4)
+    B_KQFREE0 = B_FULL0 + NSTAGE,      // chain: every reader of a stage is done (x3)
+    B_SCAL0 = B_KQFREE0 + NSTAGE,      // copy: decay scalars of a chunk written (x4)
     B_KQK = B_SCAL0 + NSCAL,           // MMA-warp commit: [K;Q]K^T done
     B_KQKFREE,                         // prep: [K;Q]K^T accumulator read out
-    B_LREADY,                          // prep: Lb, Lbg, Db, Dbg of a chunk written
-    B_UWK0,                            // MMA-warp commit: U_J^T, Wk^T of buffer b done (x2)
-    B_W = B_UWK0 + 2,                  // chain commit: W_J^T done
-    B_D,                               // chain commit: state update (and O = Q M) done
-    B_O2,                              // chain commit: output accumulation done
-    B_WKFREE0,                         // chain: Wk^T buffer b read out (x2)
-    B_RWFREE0 = B_WKFREE0 + 2,         // chain: W_J^T buffer b read out (x2)
-    B_PFREE0 = B_RWFREE0 + 2,          // chain: P buffer b read by the output product (x2)
-    B_DRAINP = B_PFREE0 + 2,           // commits of the error path (MMA warp, chain)
-    B_DRAINC,
+    B_LREADY0,                         // Lb, P of LP buffer b written (x2; b = 1 - rho by the peer)
+    B_LPFREE = B_LREADY0 + 2,          // own chain: LP[rho] read by its last product
+    B_PEERFREE,                        // peer chain (remote arrive): its copy of LP[rho] read
+    B_KM,                              // chain commit: X = [K;Q] MS done
+    B_C3,                              // chain commit: X rows 0-63 = W done
+    B_D,                               // chain commit: state update done
+    B_O2,                              // chain commit (warp 10): X rows 64-127 = O / gamma done
+    B_VFULL,                           // chain-issued TMA: v rows of the next chunk landed
+    B_DRAINM, B_DRAINC, B_DRAINO,      // commits of the error path
     NUM_BARS
 };
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
 fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -121,7 +137,8 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int bh = blockIdx.x >> 1, rho = blockIdx.x & 1;
+    const int rho = (int)cluster_rank(), peer = rho ^ 1;
+    const int bh = blockIdx.x >> 1;
     const int j0 = rho * DVH;                 // first value column of this CTA
     const int T = a.T;
     const int NC = (T + C - 1) / C;
@@ -142,48 +159,55 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_prefetch_desc(&tm_v);
         }
     }
+    {   // the zero tiles between Lb and P of both LP buffers
+        uint4 *z0 = reinterpret_cast<uint4 *>(sm + OFF_LP + 8192);
+        uint4 *z1 = reinterpret_cast<uint4 *>(sm + OFF_LP + LP_BYTES + 8192);
+        for (int i = tid; i < 512; i += NT) z0[i] = z1[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
-    __syncthreads();
+    // both CTAs' barriers are initialised before either touches the other's shared memory
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    float *As = reinterpret_cast<float *>(sm + OFF_AS);
-    float *Ts = reinterpret_cast<float *>(sm + OFF_TS);
-    float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
 
     const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
-    const uint32_t idesc_u = idesc_bf16(64, 64, true, false);
-    const uint32_t idesc_wk = idesc_bf16(128, 64, true, false);
-    const uint32_t idesc_w = idesc_bf16(64, 64, true, true, true);
-    const uint32_t idesc_o1 = idesc_bf16(64, 64, false, true);
-    const uint32_t idesc_d = idesc_bf16(128, 64, true, false);
-    const uint32_t idesc_o2 = idesc_bf16(64, 64, false, false);
+    const uint32_t idesc_x = idesc_bf16(128, 64, false, true);   // K-major A, MN-major B
+    const uint32_t idesc_d = idesc_bf16(128, 64, true, true);
 
     if (warp < 8) {
         // ================================================================ prep
+        // the chunks k = rho, rho + 2, ...; results into LP[rho] here and at the peer
+        float *As = reinterpret_cast<float *>(sm + OFF_AS);
+        float *Ts = reinterpret_cast<float *>(sm + OFF_TS);
+        float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
         const int w = tid;
         const int qd = warp & 3, half = warp >> 2;   // TMEM lane quadrant, column half
         const int lrow = qd * 32 + (tid & 31);       // TMEM lane = accumulator row
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
-        for (int k = 0; k < NC; ++k) {
-            const int sl = k % NSCAL, b = k & 1;
+        uint8_t *lp = sm + OFF_LP + rho * LP_BYTES;
+        const uint32_t lp_peer = cluster_map(smem_u32(lp), (uint32_t)peer);
+        for (int k = rho, j = 0; k < NC; k += 2, ++j) {
+            const int sl = k % NSCAL;
             const int c = min(C, T - k * C);
             const Scal S = scal(sm, sl);
 
-            // A = strict_lower(diag(beta gamma) K K^T diag(1/gamma)), P = lower(Q K^T) / gamma_C
-            bool ok = role_wait(bar(B_SCAL0 + sl), (uint32_t)(k / NSCAL) & 1u, a.limit_ns, &s_abort);
-            if (ok) ok = role_wait(bar(B_KQK), (uint32_t)k & 1u, a.limit_ns, &s_abort);
-            // A's space holds Lb / Lbg of chunk k-1 until its U / Wk products are done
-            if (ok && k > 0)
-                ok = role_wait(bar(B_UWK0 + (b ^ 1)), (uint32_t)((k - 1) >> 1) & 1u, a.limit_ns,
-                               &s_abort);
-            // P's buffer holds P of chunk k-2 until that chunk's output product is done
-            if (ok && k > 1)
-                ok = role_wait(bar(B_PFREE0 + b), (uint32_t)((k - 2) >> 1) & 1u, a.limit_ns,
-                               &s_abort);
+            bool ok = true;
+            if (w == 0) {   // one thread waits; the named barrier passes the result on
+                ok = role_wait(bar(B_SCAL0 + sl), (uint32_t)(k / NSCAL) & 1u, a.limit_ns, &s_abort);
+                if (ok) ok = role_wait(bar(B_KQK), (uint32_t)j & 1u, a.limit_ns, &s_abort);
+                // LP[rho] here and at the peer hold chunk k-2 until both chains have read it
+                if (ok && j > 0)
+                    ok = role_wait(bar(B_LPFREE), (uint32_t)(j - 1) & 1u, a.limit_ns, &s_abort);
+                if (ok && j > 0)
+                    ok = role_wait_cluster(bar(B_PEERFREE), (uint32_t)(j - 1) & 1u, a.limit_ns,
+                                           &s_abort);
+            }
             if (!named_and(BAR_PREP, NPREP, ok)) break;
             const float igC = 1.f / s_gC[sl];
             tc_fence_after();
-            {   // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
+            {   // A = strict_lower(diag(beta gamma) K K^T diag(1/gamma)), P = lower(Q K^T) / gamma_C;
+                // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
                 const int h = half;
                 float v[32];
                 tmem_ld32(tl + TM_KQK + h * 32, v);
@@ -205,8 +229,23 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 } else {
                     const int r = lrow - 64;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = (h * 32 + e <= r && r < c) ? v[e] * igC : 0.f;
-                    st_halfrow_bf16(sm + OFF_P + b * 8192, r, h, v);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        float p8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int s = h * 32 + q4 * 8 + e;
+                            p8[e] = (s <= r && r < c) ? v[q4 * 8 + e] * igC : 0.f;
+                        }
+                        uint4 u;
+                        u.x = pack_bf16x2(p8[0], p8[1]);
+                        u.y = pack_bf16x2(p8[2], p8[3]);
+                        u.z = pack_bf16x2(p8[4], p8[5]);
+                        u.w = pack_bf16x2(p8[6], p8[7]);
+                        const uint32_t off =
+                            LP_P + (uint32_t)r * 128u + (((uint32_t)(h * 4 + q4) ^ (uint32_t)(r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(lp + off) = u;
+                        st_cluster_v4(lp_peer + off, u);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -215,126 +254,96 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (w == 0) mbar_arrive(bar(B_KQKFREE));   // the next [K;Q]K^T may start
 
             solve_unit_lower(w, As, Ts, Ys);
-            {   // Lb = (T - I) diag(beta) + diag(bf16(beta)), Lbg likewise with beta gamma;
-                // thread -> (matrix w / 128, row w % 64, column half (w / 64) % 2)
-                const int r = w & 63, mat = w >> 7;
-                const float *sc = mat ? S.bg : S.bs;
-                uint8_t *dst = sm + (mat ? OFF_LBG : OFF_LB);
-                const int h = (w >> 6) & 1;
-                float v[32];
+            {   // Lb = strict_lower(T) diag(beta): thread -> row w % 64, columns 16 (w / 64) + 0..15
+                const int r = w & 63, q4 = w >> 6;
+                float v[16];
 #pragma unroll
-                for (int s4 = 0; s4 < 32; s4 += 4) {
-                    const int s0 = h * 32 + s4;
+                for (int s4 = 0; s4 < 16; s4 += 4) {
+                    const int s0 = q4 * 16 + s4;
                     const float4 t = *reinterpret_cast<const float4 *>(&Ts[r * LDA + s0]);
-                    const float4 f = *reinterpret_cast<const float4 *>(&sc[s0]);
-                    v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : (s0 + 0 == r ? f.x : 0.f);
-                    v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : (s0 + 1 == r ? f.y : 0.f);
-                    v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : (s0 + 2 == r ? f.z : 0.f);
-                    v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : (s0 + 3 == r ? f.w : 0.f);
+                    const float4 f = *reinterpret_cast<const float4 *>(&S.bs[s0]);
+                    v[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : 0.f;
+                    v[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
+                    v[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
+                    v[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
                 }
-                st_halfrow_bf16(dst, r, h, v);
-            }
-            named_sync(BAR_PREP, NPREP);     // T is read out; its space takes the residuals
-            if (w < 128) {   // Db = diag(beta - bf16(beta)), Dbg = diag(beta gamma - bf16(beta gamma))
-                const int r = w & 63;
-                const float x = (w < 64) ? S.bs[r] : S.bg[r];
-                const float lo = x - __bfloat162float(__float2bfloat16_rn(x));
-                uint8_t *dst = sm + ((w < 64) ? OFF_DB : OFF_DBG);
-                const __nv_bfloat16 lo16 = __float2bfloat16_rn(lo);
-                const uint32_t lo_bits = (uint32_t)*reinterpret_cast<const unsigned short *>(&lo16);
-                const uint32_t word = lo_bits << (16 * (r & 1));
-                const int wi = (r & 7) >> 1;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const bool here = (r >> 3) == ch;
-                    *reinterpret_cast<uint4 *>(dst + r * 128u + ((ch ^ (r & 7u)) << 4)) =
-                        make_uint4(here && wi == 0 ? word : 0u, here && wi == 1 ? word : 0u,
-                                   here && wi == 2 ? word : 0u, here && wi == 3 ? word : 0u);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t ch = (uint32_t)(q4 * 2 + h2);
+                    uint4 u;
+                    u.x = pack_bf16x2(v[h2 * 8 + 0], v[h2 * 8 + 1]);
+                    u.y = pack_bf16x2(v[h2 * 8 + 2], v[h2 * 8 + 3]);
+                    u.z = pack_bf16x2(v[h2 * 8 + 4], v[h2 * 8 + 5]);
+                    u.w = pack_bf16x2(v[h2 * 8 + 6], v[h2 * 8 + 7]);
+                    const uint32_t off = (uint32_t)r * 128u + ((ch ^ (uint32_t)(r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(lp + off) = u;
+                    st_cluster_v4(lp_peer + off, u);
                 }
             }
             fence_proxy_async_smem();
+            fence_proxy_async_cluster();
             named_sync(BAR_PREP, NPREP);
-            if (w == 0) mbar_arrive(bar(B_LREADY));    // U_J^T and Wk^T may start
+            if (w == 0) {
+                mbar_arrive(bar(B_LREADY0 + rho));
+                mbar_arrive_remote(cluster_map(bar(B_LREADY0 + rho), (uint32_t)peer));
+            }
         }
     } else if (warp == 13) {
         // ================================================================ MMA issue
-        // [K;Q]K^T of chunk k+1 once chunk k's accumulator is read out; then U_J^T =
-        // V_J^T (Lb + Db)^T into W buffer b and Wk^T = K^T (Lbg + Dbg)^T into Wk buffer b,
-        // both free once the chain has read chunk k-2's.
+        // [K;Q]K^T of this CTA's chunks k = rho, rho + 2, ...: each once its stage has
+        // landed and the preparation has read the previous one's accumulator.
         if ((tid & 31) == 0) {
             bool issued = false;
-            auto kqk = [&](int k) {
-                const uint32_t kq_a = sbase + OFF_KQ + (k % NSTAGE) * KQ_BYTES;
+            for (int k = rho, j = 0; k < NC; k += 2, ++j) {
+                bool ok = (j == 0) ||
+                          role_wait(bar(B_KQKFREE), (uint32_t)(j - 1) & 1u, a.limit_ns, &s_abort);
+                if (ok)
+                    ok = role_wait(bar(B_FULL0 + k % NSTAGE), (uint32_t)(k / NSTAGE) & 1u, a.limit_ns,
+                                   &s_abort);
+                if (!ok) break;
+                const uint64_t dkq = sdesc_sw128(sbase + OFF_KQ + (k % NSTAGE) * KQ_BYTES, 16, 1024);
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ad = kq_a + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_KQK, sdesc_sw128(ad, 16, 1024), sdesc_sw128(ad, 16, 1024),
-                             idesc_kqk, kk > 0);
+                    const uint64_t d = sdesc_add(dkq, (kk >> 2) * 16384 + (kk & 3) * 32);
+                    mma_bf16(tmem + TM_KQK, d, d, idesc_kqk, kk > 0);
                 }
                 mma_commit(bar(B_KQK));
                 issued = true;
-            };
-            bool ok = role_wait(bar(B_FULL0), 0u, a.limit_ns, &s_abort);
-            if (ok) kqk(0);
-            for (int k = 0; ok && k < NC; ++k) {
-                const int st = k % NSTAGE, b = k & 1;
-                if (k + 1 < NC) {
-                    ok = role_wait(bar(B_KQKFREE), (uint32_t)k & 1u, a.limit_ns, &s_abort);
-                    if (ok)
-                        ok = role_wait(bar(B_FULL0 + (k + 1) % NSTAGE),
-                                       (uint32_t)((k + 1) / NSTAGE) & 1u, a.limit_ns, &s_abort);
-                    if (!ok) break;
-                    kqk(k + 1);
-                }
-                ok = role_wait(bar(B_LREADY), (uint32_t)k & 1u, a.limit_ns, &s_abort);
-                if (ok && k > 1)
-                    ok = role_wait(bar(B_RWFREE0 + b), (uint32_t)((k - 2) >> 1) & 1u, a.limit_ns,
-                                   &s_abort);
-                if (ok && k > 1)
-                    ok = role_wait(bar(B_WKFREE0 + b), (uint32_t)((k - 2) >> 1) & 1u, a.limit_ns,
-                                   &s_abort);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
-                const uint32_t v_a = sbase + OFF_V + st * V_BYTES;
-                const uint32_t tw = tmem + TM_W + b * 64, twk = tmem + TM_WK + b * 64;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tw, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
-                             sdesc_sw128(sbase + OFF_LB + kk * 32, 16, 1024), idesc_u, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tw, sdesc_sw128(v_a + kk * 2048, 8192, 1024),
-                             sdesc_sw128(sbase + OFF_DB + kk * 32, 16, 1024), idesc_u, 1);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(twk, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
-                             sdesc_sw128(sbase + OFF_LBG + kk * 32, 16, 1024), idesc_wk, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(twk, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
-                             sdesc_sw128(sbase + OFF_DBG + kk * 32, 16, 1024), idesc_wk, 1);
-                mma_commit(bar(B_UWK0 + b));
             }
             if (s_abort && issued) {   // let this thread's MMAs land before TMEM goes away
-                mma_commit(bar(B_DRAINP));
-                mbar_wait(bar(B_DRAINP), 0u, kCleanupLimitNs);
+                mma_commit(bar(B_DRAINM));
+                mbar_wait(bar(B_DRAINM), 0u, kCleanupLimitNs);
             }
         }
         __syncwarp();
     } else if (warp < 12) {
         // ================================================================ chain
-        const int w = tid - 256;    // TMEM lane: row i of M_J and of Wk^T
-        const int lane = w & 31, qd = warp - 8;
+        const int w = tid - 256;                 // TMEM lane = row of X and of M_J
+        const int qd = warp - 8;
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
-        // M = 64 layout rows: this thread reads row 16 qd + (lane % 16), column half lane / 16
-        const int r64 = 16 * qd + (lane & 15), h64 = lane >> 4;
-        bool issued = false;
-        bool ok = role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
+        bool issued = false, issued_o = false;
+        uint32_t issued_v = 0;   // TMA loads of v issued (threads 0 and 64)
+        const uint32_t peer_free = cluster_map(bar(B_PEERFREE), (uint32_t)peer);
+
+        // X(n) = [K;Q] MS  (chunk n's stage)
+        auto issue_km = [&](int n) {
+            const uint64_t da = sdesc_sw128(sbase + OFF_KQ + (n % NSTAGE) * KQ_BYTES, 16, 1024);
+            const uint64_t db = sdesc_sw128(sbase + OFF_MS, 8192, 1024);
+            const uint32_t dst = tmem + TM_X + (n & 1) * 64;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(dst, sdesc_add(da, (kk >> 2) * 16384 + (kk & 3) * 32),
+                         sdesc_add(db, kk * 2048), idesc_x, kk > 0);
+            mma_commit(bar(B_KM));
+            issued = true;
+        };
+
+        bool ok = (w != 0) || role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
         ok = named_and(BAR_CHAIN, 128, ok);
         if (ok) {
-            // initial state: TMEM M_J <- gamma_C(0) M0[:, J], MS <- bf16(M0[:, J])
+            // initial state: TMEM M_J <- gamma_C(0) M_0[:, J], MS <- bf16(M_0[:, J]); thread = row i
             const float gC = s_gC[0];
             const float *src = a.init ? a.init + ((int64_t)bh * D + w) * D + j0 : nullptr;
 #pragma unroll 1
@@ -350,93 +359,151 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(BAR_CHAIN, 128);
+            if (w == 64) {
+                mbar_arrive_expect_tx(bar(B_VFULL), 8192);
+                tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, 0, bh);
+                issued_v = 1;
+            }
         }
         for (int n = 0; ok && n < NC; ++n) {
+            // ---- X(n) = [K;Q] MS_n once chunk n's stage has landed (MS_n: the previous
+            // iteration's state step, or the initial state)
+            if (w == 0)
+                ok = role_wait(bar(B_FULL0 + n % NSTAGE), (uint32_t)(n / NSTAGE) & 1u, a.limit_ns,
+                               &s_abort);
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 0) issue_km(n);
             const int st = n % NSTAGE, b = n & 1, sl = n % NSCAL, sl1 = (n + 1) % NSCAL;
             const int t0 = n * C;
             const int c = min(C, T - t0);
             const Scal S = scal(sm, sl);
             const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
+            const uint32_t lp_a = sbase + OFF_LP + b * LP_BYTES;
+            const uint32_t xcol = TM_X + (n & 1) * 64;
             const bool last = (n + 1 == NC);
 
-            // ---- Wk^T -> WkT (bf16, MN-major operand; row i = this lane)
-            ok = role_wait(bar(B_FULL0 + st), (uint32_t)(n / NSTAGE) & 1u, a.limit_ns, &s_abort);
-            if (ok) ok = role_wait(bar(B_UWK0 + b), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
-            tc_fence_after();
+            if (w < 64) {
+                // ---- E = V - gamma K M_n -> EW (bf16); X rows 0-63 <- beta E (fp32)
+                if (w == 0) ok = role_wait(bar(B_VFULL), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_EROWS, 64, ok);
+                if (w == 0 && ok) ok = role_wait(bar(B_KM), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_EROWS, 64, ok);
+                tc_fence_after();
+                const float gr = S.gam[w], br = S.bs[w];
+                // v[t0 + w][J], row w of the v buffer (zero-filled past T by the copy); the
+                // buffer is refilled only after the chain barrier that follows this step
+                const uint8_t *vrow = sm + OFF_VB + w * 128;
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float v[32];
-                tmem_ld32(tl + TM_WK + b * 64 + h * 32, v);
-                tmem_wait_ld();
-                st_halfrow_bf16(sm + OFF_WKT, w, h, v);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(BAR_CHAIN, 128);
-            // ---- W_J^T = U_J^T - M_J^T Wk^T ;  O_J = Q M_J
-            if (w == 0) {
-                mbar_arrive(bar(B_WKFREE0 + b));
-                tc_fence_after();
+                for (int cb = 0; cb < (ok ? 2 : 0); ++cb) {
+                    float x[32];
+                    tmem_ld32(tl + xcol + cb * 32, x);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + TM_W + b * 64, sdesc_sw128(sbase + OFF_MS + kk * 2048, 16384, 1024),
-                             sdesc_sw128(sbase + OFF_WKT + kk * 2048, 16384, 1024), idesc_w, 1);
-                mma_commit(bar(B_W));
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(
+                            vrow + (((uint32_t)(cb * 4 + q4) ^ (uint32_t)(w & 7)) << 4));
+                        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + TM_O,
-                             sdesc_sw128(kq_a + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                             sdesc_sw128(sbase + OFF_MS + kk * 2048, 16384, 1024), idesc_o1, kk > 0);
-                issued = true;
-            }
-
-            // ---- Wt_J^T[j][s] = W_J^T[j][s] gamma_C / gamma_s -> WtT (row j); then the state
-            // update and the output accumulation
-            ok = role_wait(bar(B_W), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
-            tc_fence_after();
-            {
-                float v[32];
-                tmem_ld32_m64(tl + TM_W + b * 64, v);
-                tmem_wait_ld();
+                        for (int p2 = 0; p2 < 4; ++p2) {
+                            const float2 f = __bfloat1622float2(
+                                *reinterpret_cast<const __nv_bfloat162 *>(&wv[p2]));
+                            x[q4 * 8 + 2 * p2 + 0] = fmaf(-gr, x[q4 * 8 + 2 * p2 + 0], f.x);
+                            x[q4 * 8 + 2 * p2 + 1] = fmaf(-gr, x[q4 * 8 + 2 * p2 + 1], f.y);
+                        }
+                    }
+                    st_halfrow_bf16(sm + OFF_EW, w, cb, x);
 #pragma unroll
-                for (int e4 = 0; e4 < 32; e4 += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(&S.sc[h64 * 32 + e4]);
-                    v[e4 + 0] *= f.x;
-                    v[e4 + 1] *= f.y;
-                    v[e4 + 2] *= f.z;
-                    v[e4 + 3] *= f.w;
+                    for (int e = 0; e < 32; ++e) x[e] *= br;
+                    tmem_st32(tl + xcol + cb * 32, x);
                 }
-                st_halfrow_bf16(sm + OFF_WTT, r64, h64, v);
+                tmem_wait_st();
+                fence_proxy_async_smem();
+            } else if (n > 0) {
+                // ---- output of chunk n-1, once its last product has landed
+                if (w == 64) ok = role_wait(bar(B_O2), (uint32_t)(n - 1) & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_OROWS, 64, ok);
+                if (ok) {
+                    if (w == 64) {   // chunk n-1's LP buffer is read: free it for its producer
+                        if (((n - 1) & 1) == rho) mbar_arrive_relaxed(bar(B_LPFREE));
+                        else mbar_arrive_remote_relaxed(peer_free);
+                    }
+                    tc_fence_after();
+                    const int m = n - 1;
+                    emit_output_rows(tl + TM_X + (m & 1) * 64, w - 64, min(C, T - m * C),
+                                     scal(sm, m % NSCAL).gam, a.out + (row_base + m * C) * D + j0);
+                }
             }
-            fence_proxy_async_smem();
+            // Lb of chunk n is needed from here on
+            if (ok && w == 0)
+                ok = role_wait_cluster(bar(B_LREADY0 + b), (uint32_t)(n >> 1) & 1u, a.limit_ns,
+                                       &s_abort);
             tc_fence_before();
-            named_sync(BAR_CHAIN, 128);
-            if (w == 0) {
-                mbar_arrive(bar(B_RWFREE0 + b));
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 64 && !last) {   // the v buffer is read: refill it with the next chunk's rows
+                mbar_arrive_expect_tx(bar(B_VFULL), 8192);
+                tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, t0 + C, bh);
+                ++issued_v;
+            }
+            if (w == 0) {   // X += [Lb; 0] E  (rows 0-63 become W)
+                fence_proxy_async_smem();
                 tc_fence_after();
-                // M_J += K^T Wt_J ;  O_J += P Wt_J
+                const uint64_t da = sdesc_sw128(lp_a, 16, 1024);
+                const uint64_t db = sdesc_sw128(sbase + OFF_EW, 8192, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_M, sdesc_sw128(kq_a + kk * 2048, 16384, 1024),
-                             sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024), idesc_d, 1);
-                mma_commit(bar(B_D));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM_O, sdesc_sw128(sbase + OFF_P + b * 8192 + kk * 32, 16, 1024),
-                             sdesc_sw128(sbase + OFF_WTT + kk * 32, 16, 1024), idesc_o2, 1);
-                mma_commit(bar(B_O2));
+                    mma_bf16(tmem + xcol, sdesc_add(da, kk * 32), sdesc_add(db, kk * 2048), idesc_x, 1);
+                mma_commit(bar(B_C3));
             }
 
-            // ---- state: MS <- bf16(M_J,n+1); TMEM M_J <- gamma_C(n+1) M_J,n+1
-            ok = role_wait(bar(B_D), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-            // every MMA that reads this input stage is complete: let the copy warp refill it
-            if (w == 0 && ok) mbar_arrive(bar(B_OSTAGE0 + st));
-            if (ok && !last)
-                ok = role_wait(bar(B_SCAL0 + sl1), (uint32_t)((n + 1) / NSCAL) & 1u, a.limit_ns,
-                               &s_abort);
+            // ---- Wt = diag(gamma_C / gamma) W -> EW (bf16), warps 8-9
+            if (w < 64) {
+                if (w == 0) ok = role_wait(bar(B_C3), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_EROWS, 64, ok);
+                if (ok) {
+                    tc_fence_after();
+                    const float sr = S.sc[w];
+#pragma unroll 1
+                    for (int cb = 0; cb < 2; ++cb) {
+                        float x[32];
+                        tmem_ld32(tl + xcol + cb * 32, x);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) x[e] *= sr;
+                        st_halfrow_bf16(sm + OFF_EW, w, cb, x);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            tc_fence_before();
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 0) {   // M_J += K^T Wt
+                tc_fence_after();
+                const uint64_t da = sdesc_sw128(kq_a, 16384, 1024);
+                const uint64_t db = sdesc_sw128(sbase + OFF_EW, 8192, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM_M, sdesc_add(da, kk * 2048), sdesc_add(db, kk * 2048), idesc_d, 1);
+                mma_commit(bar(B_D));
+            } else if (w == 64) {   // X += [0; P] Wt  (rows 64-127 become O / gamma)
+                tc_fence_after();
+                const uint64_t da = sdesc_sw128(lp_a + 8192, 16, 1024);
+                const uint64_t db = sdesc_sw128(sbase + OFF_EW, 8192, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + xcol, sdesc_add(da, kk * 32), sdesc_add(db, kk * 2048), idesc_x, 1);
+                mma_commit(bar(B_O2));
+                issued_o = true;
+            }
+
+            // ---- state: MS <- bf16(M_{n+1}); TMEM M_J <- gamma_C(n+1) M_{n+1}; thread = row i
+            if (w == 0) {
+                ok = role_wait(bar(B_D), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                // every product reading this input stage is complete: let the copy warp refill it
+                if (ok) mbar_arrive(bar(B_KQFREE0 + st));
+                if (ok && !last)
+                    ok = role_wait(bar(B_SCAL0 + sl1), (uint32_t)((n + 1) / NSCAL) & 1u,
+                                   a.limit_ns, &s_abort);
+            }
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
             {
@@ -463,37 +530,28 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 tmem_wait_st();
             }
-            // ---- output row r = gamma_r O_J[r][:], the column half h64 of this thread
-            ok = role_wait(bar(B_O2), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-            if (w == 0 && ok) mbar_arrive(bar(B_PFREE0 + b));
-            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
-            tc_fence_after();
-            {
-                float v[32];
-                tmem_ld32_m64(tl + TM_O, v);
-                tmem_wait_ld();
-                if (r64 < c) {
-                    const float gr = S.gam[r64];
-                    uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + t0 + r64) * D + j0 +
-                                                            h64 * 32);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 u;
-                        u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
-                        u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
-                        u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
-                        u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
-                        __stcs(orow + q4, u);
-                    }
-                }
-            }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(BAR_CHAIN, 128);
+        }
+        if (ok && w >= 64) {   // output of the last chunk
+            if (w == 64) ok = role_wait(bar(B_O2), (uint32_t)(NC - 1) & 1u, a.limit_ns, &s_abort);
+            ok = named_and(BAR_OROWS, 64, ok);
+            if (ok) {
+                tc_fence_after();
+                const int m = NC - 1;
+                emit_output_rows(tl + TM_X + (m & 1) * 64, w - 64, min(C, T - m * C),
+                                 scal(sm, m % NSCAL).gam, a.out + (row_base + m * C) * D + j0);
+            }
         }
         if (s_abort && w == 0 && issued) {
             mma_commit(bar(B_DRAINC));
             mbar_wait(bar(B_DRAINC), 0u, kCleanupLimitNs);
+        }
+        if (s_abort && w == 64 && issued_v > 0)   // the latest v load may still be in flight
+            mbar_wait(bar(B_VFULL), (issued_v - 1) & 1u, kCleanupLimitNs);
+        if (s_abort && w == 64 && issued_o) {
+            mma_commit(bar(B_DRAINO));
+            mbar_wait(bar(B_DRAINO), 0u, kCleanupLimitNs);
         }
     } else {
         // ================================================================ copy
@@ -503,16 +561,14 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int st = n % NSTAGE;
             const uint32_t b = bar(B_FULL0 + st);
             const uint32_t kq = sbase + OFF_KQ + st * KQ_BYTES;
-            const uint32_t vv = sbase + OFF_V + st * V_BYTES;
-            mbar_arrive_expect_tx(b, KQ_BYTES + V_BYTES);
+            mbar_arrive_expect_tx(b, KQ_BYTES);
             tma_load_3d(kq + 0, &tm_k, b, 0, n * C, bh);
             tma_load_3d(kq + 8192, &tm_q, b, 0, n * C, bh);
             tma_load_3d(kq + 16384, &tm_k, b, 64, n * C, bh);
             tma_load_3d(kq + 24576, &tm_q, b, 64, n * C, bh);
-            tma_load_3d(vv, &tm_v, b, j0, n * C, bh);
             ++issued[st];
         };
-        // Pull the inputs of chunk n into L2 ahead of its shared-memory load.
+        // Pull the inputs of chunk n into L2 ahead of use (v is read from L2 by the chain).
         auto prefetch_l2 = [&](int n) {   // lane 0 only
             if (n >= NC) return;
             tma_prefetch_3d(&tm_k, 0, n * C, bh);
@@ -535,18 +591,18 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (lane == 0) mbar_arrive(bar(B_SCAL0 + sl));
         };
         float gv[2], bv[2];
+        if (lane == 0)
+            for (int n = 0; n < NSTAGE + kL2Ahead; ++n) prefetch_l2(n);
         for (int n = 0; n < NSTAGE && n < NC; ++n) {
             load_gb(n, gv, bv);
             if (lane == 0) issue_tma(n);
             decay(n, gv, bv);
         }
-        if (lane == 0)
-            for (int n = NSTAGE; n < NSTAGE + kL2Ahead; ++n) prefetch_l2(n);
         if (NC > NSTAGE) load_gb(NSTAGE, gv, bv);
         for (int n = 0; n + NSTAGE < NC; ++n) {   // refill a stage once chunk n is done with it
             const int st = n % NSTAGE;
-            bool ok = role_wait(bar(B_OSTAGE0 + st), (uint32_t)(n / NSTAGE) & 1u, a.limit_ns,
-                                &s_abort);
+            bool ok = (lane != 0) || role_wait(bar(B_KQFREE0 + st), (uint32_t)(n / NSTAGE) & 1u,
+                                               a.limit_ns, &s_abort);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (lane == 0) {
                 issue_tma(n + NSTAGE);
@@ -568,6 +624,8 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncwarp();
         tmem_dealloc(tmem, TM_COLS);
     }
+    // neither CTA leaves while the other may still write into its shared memory
+    cluster_sync();
 }
 
 }  // namespace
@@ -583,13 +641,33 @@ cudaError_t launch_fused_pair(const void *q, const void *k, const void *v, const
     if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T))
         return cudaErrorInvalidValue;
     FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, T,
-                wait_limit_ns()};
+                wait_limit_ns(), static_cast<const __nv_bfloat16 *>(v)};
     cudaError_t e = cudaFuncSetAttribute(fused_pair_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     fused_pair_kernel<<<2 * BH, NT, SMEM_ALLOC, s>>>(mq, mk, mv, a);
     return cudaGetLastError();
+}
+
+// Clusters of the pair kernel that can be resident at once on the current device.
+int fused_pair_max_clusters() {
+    static int cached = -1;
+    if (cached >= 0) return cached;
+    if (cudaFuncSetAttribute(fused_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_ALLOC) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fused_pair_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cached = n;
+    return n;
 }
 
 cudaError_t take_pair_error_word(unsigned *value) { return take_error_word(value); }

@@ -38,11 +38,14 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
                          float *final_state, int B, int H, int T, int dk, int dv, int C,
                          cudaStream_t s);
 
-// ---- fused tensor-core prefill, value columns split over two CTAs per head
-// (gdr_fused_pair.cu); chosen by launch_fused when the pair grid fits the GPU ----
+// ---- fused tensor-core prefill on a cluster of two CTAs per head (value columns
+// split, preparation alternated; gdr_fused_pair.cu); chosen by launch_fused when
+// every head's cluster is resident at once ----
 cudaError_t launch_fused_pair(const void *q, const void *k, const void *v, const float *g,
                               const float *beta, float a_min, const float *init, void *out,
                               float *final_state, int BH, int T, cudaStream_t s);
+// Clusters of the pair kernel resident at once on the current device (0 if unknown).
+int fused_pair_max_clusters();
 // Reads and clears the device error word of the pair kernel (synchronous).
 cudaError_t take_pair_error_word(unsigned *value);
 
