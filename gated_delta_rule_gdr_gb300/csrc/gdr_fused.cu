@@ -119,8 +119,9 @@ __global__ void __launch_bounds__(NT, 1)
 fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived from the __shared__ array by pointer
+    // arithmetic so that every access through it stays a shared-memory access
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     __shared__ __align__(8) uint64_t s_bar[NUM_BARS];
     __shared__ uint32_t s_tmem;

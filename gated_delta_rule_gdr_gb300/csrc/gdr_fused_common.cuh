@@ -159,10 +159,11 @@ __device__ __noinline__ void warp_decay(int lane, const float (&gv)[2], const fl
 // Fragment layouts (g = lane / 4, t = lane % 4): A (16 x 8) a0 (g, t), a1
 // (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8) b0 (t, g), b1 (t+4, g);
 // C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+// fp32 -> tf32 bit pattern, rounded to nearest with ties away from zero: add
+// half of the 13 dropped mantissa bits' weight, then clear them (finite inputs;
+// the solve's operands always are).  Two integer operations.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
                                          const uint32_t (&b)[2]) {
