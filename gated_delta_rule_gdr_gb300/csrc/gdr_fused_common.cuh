@@ -69,9 +69,8 @@ __device__ __forceinline__ void st_halfrow_bf16(uint8_t *tile, uint32_t row, uin
 // so a waiting thread takes no issue slots from the working warps; one thread
 // per role waits and a named barrier passes the result on.
 constexpr uint32_t kWaitSliceNs = 20000;
-__device__ __noinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                          volatile int *abort) {
-    if (mbar_test_wait(bar, parity)) return true;      // non-blocking first look
+__device__ __noinline__ bool role_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                            volatile int *abort, bool cluster_scope) {
     if (limit_ns == 0) {                                // injected timeout: give up at once
         *abort = 1;
         atomicOr(&g_device_error_word, kDevErrTimeout);
@@ -79,7 +78,9 @@ __device__ __noinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t l
     }
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return true;
+        if (cluster_scope ? mbar_try_wait_cluster_hint(bar, parity, kWaitSliceNs)
+                          : mbar_try_wait_hint(bar, parity, kWaitSliceNs))
+            return true;
         if (*abort) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort = 1;
@@ -88,27 +89,18 @@ __device__ __noinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t l
         }
     }
 }
-
+// The common case -- the phase has already completed -- stays inline.
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          volatile int *abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return role_wait_slow(bar, parity, limit_ns, abort, false);
+}
 // role_wait for barriers that another CTA of the cluster arrives on
 // (cluster-scope acquire).
-__device__ __noinline__ bool role_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+__device__ __forceinline__ bool role_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int *abort) {
     if (mbar_test_wait_cluster(bar, parity)) return true;
-    if (limit_ns == 0) {
-        *abort = 1;
-        atomicOr(&g_device_error_word, kDevErrTimeout);
-        return false;
-    }
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait_cluster_hint(bar, parity, kWaitSliceNs)) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > limit_ns) {
-            *abort = 1;
-            atomicOr(&g_device_error_word, kDevErrTimeout);
-            return false;
-        }
-    }
+    return role_wait_slow(bar, parity, limit_ns, abort, true);
 }
 
 // Cumulative decay of one chunk by one warp (lane l owns rows 2l, 2l+1, whose

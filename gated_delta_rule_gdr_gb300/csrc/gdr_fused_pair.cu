@@ -30,11 +30,14 @@
 //
 // Warp roles (448 threads): prep 0-7, chain 8-11 (warps 8-9 own X rows 0-63,
 // warps 10-11 rows 64-127), copy 12 (TMA of K and Q, decay, L2 prefetch of
-// K, Q and V), MMA 13 ([K;Q]K^T of the chunks this CTA prepares).  v rows are
-// read by the chain straight from global memory (L2) into registers.
+// K, Q and V), MMA 13 ([K;Q]K^T of the chunks this CTA prepares).  The v rows
+// of the next chunk are loaded by TMA (issued by a chain thread of warps 10-11)
+// into a single buffer as soon as the current chunk's E step has read it.
+// Every wait is done by one thread per role, suspended in mbarrier.try_wait,
+// and passed on by a named barrier.
 //
 // Shared memory: KQ[3] 32 KB, MS 16 KB ([i][j] bf16, MN-major), EW 8 KB
-// ([s][j] bf16, MN-major; E, then Wt), LP[2] 24 KB ([Lb | 0 | P], K-major;
+// ([s][j] bf16, MN-major; E, then Wt), V 8 KB, LP[2] 24 KB ([Lb | 0 | P], K-major;
 // LP[rho] holds the chunks this CTA prepares, LP[1 - rho] its peer's), the fp32
 // solve space (A, T), merge scratch, 4 slots of per-chunk scalars.
 // TMEM: [K;Q]K^T 64 cols, X[2] 2 x 64, M_J 64.
