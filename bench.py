@@ -329,9 +329,15 @@ def run_ours(args):
         by, fl = prefill_algorithmic(main_w)
         nk = gdr.chunk_fwd_kernels(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
                                    main_w.chunk, main_w.a_min, main_w.torch_dtype())
-        kname = "gdr_fused_prefill" if nk == 1 else "gdr_chunk_fwd staged (4 kernels)"
-        srcs = ["gated_delta_rule_gdr_gb300/csrc/gdr_fused.cu"] if nk == 1 else \
-            ["gated_delta_rule_gdr_gb300/csrc/gdr_staged.cu"]
+        path = gdr.chunk_fwd_path(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
+                                  main_w.chunk, main_w.a_min, main_w.torch_dtype())
+        csrc = "gated_delta_rule_gdr_gb300/csrc/"
+        common = [csrc + "gdr_fused_common.cuh", csrc + "gdr_sm100.cuh"]
+        kname, srcs = {
+            1: ("gdr_chunk_fwd staged (4 kernels)", [csrc + "gdr_staged.cu"]),
+            2: ("fused_prefill_kernel", [csrc + "gdr_fused.cu"] + common),
+            3: ("fused_pair_kernel", [csrc + "gdr_fused_pair.cu"] + common),
+        }[path]
         metric = "prefill tokens/s"
     else:
         tokens = main_w.B

@@ -19,7 +19,7 @@ import torch
 from . import build as _build
 
 __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk_wy",
-           "chunk_state", "chunk_output", "chunk_fwd_kernels", "last_device_error", "status_string", "version",
+           "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "last_device_error", "status_string", "version",
            "library_path", "STATUS"]
 
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
@@ -63,6 +63,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_output": [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
         "gdr_last_device_error": [vp],
         "gdr_chunk_fwd_kernels": [i, i, i, i, i, i, f, i],
+        "gdr_chunk_fwd_path": [i, i, i, i, i, i, f, i],
         "gdr_status_string": [i],
         "gdr_version": [],
     }
@@ -206,6 +207,15 @@ def chunk_output(q, k, gamma, Mn, W, chunk: int = 64):
 def chunk_fwd_kernels(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16) -> int:
     """How many kernels one chunk_fwd call with these arguments launches."""
     return int(load().gdr_chunk_fwd_kernels(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
+
+
+PATHS = {0: "none", 1: "staged", 2: "fused one CTA per head", 3: "fused two-CTA cluster per head"}
+
+
+def chunk_fwd_path(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16) -> int:
+    """Which path one chunk_fwd call with these arguments takes on the current
+    device (see PATHS; -1 = rejected)."""
+    return int(load().gdr_chunk_fwd_path(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
 
 
 def last_device_error(device=None) -> int:

@@ -170,6 +170,16 @@ int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float 
     return gdr::fused_supported(dk, dv, chunk, elem_of(dtype)) ? 1 : 4;
 }
 
+int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
+                       gdr_dtype_t dtype) {
+    const int n = gdr_chunk_fwd_kernels(B, H, T, dk, dv, chunk, a_min, dtype);
+    if (n <= 0) return n;
+    if (n == 4) return 1;
+    const int64_t BH = (int64_t)B * H;
+    if (BH > 0x7fffffff) return -1;
+    return gdr::fused_uses_pair((int)BH) ? 3 : 2;
+}
+
 gdr_status_t gdr_last_device_error(void *stream) {
     unsigned word = 0;
     cudaError_t e = gdr::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &word);

@@ -590,6 +590,8 @@ bool use_pair(int BH) {
 
 }  // namespace
 
+bool fused_uses_pair(int BH) { return use_pair(BH); }
+
 bool fused_supported(int dk, int dv, int C_, Elem e) {
     return e == Elem::BF16 && dk == D && dv == D && C_ == C;
 }

@@ -46,6 +46,8 @@ cudaError_t launch_fused_pair(const void *q, const void *k, const void *v, const
                               float *final_state, int BH, int T, cudaStream_t s);
 // Clusters of the pair kernel resident at once on the current device (0 if unknown).
 int fused_pair_max_clusters();
+// Whether launch_fused runs the cluster-pair kernel for BH heads on the current device.
+bool fused_uses_pair(int BH);
 // Reads and clears the device error word of the pair kernel (synchronous).
 cudaError_t take_pair_error_word(unsigned *value);
 

@@ -196,6 +196,19 @@ int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float 
                           gdr_dtype_t dtype);
 
 /*
+ * Which code path one gdr_chunk_fwd call with these arguments takes on the
+ * calling thread's current device: 0 no kernel (empty work), 1 the staged
+ * kernels, 2 the fused kernel with one CTA per head, 3 the fused kernel with a
+ * cluster of two CTAs per head (value columns split, chunk preparation
+ * alternated between the two), or -1 if the call would be rejected.  The
+ * choice between 2 and 3 depends on how many two-CTA clusters the device holds
+ * at once (queried once per process) and on the GDR_FUSED_VARIANT environment
+ * variable ("single" or "pair" forces one).  Launches nothing.
+ */
+int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
+                       gdr_dtype_t dtype);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word:
  * GDR_ERR_TIMEOUT if a kernel's bounded wait gave up since the last call,
  * GDR_ERR_CUDA if the stream reports an error, else GDR_OK.

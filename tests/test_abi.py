@@ -114,3 +114,14 @@ def test_binding_fails_loudly_without_cuda_tensors(lib):
     q = torch.zeros(1, 1, 4, 16)
     with pytest.raises(ValueError):
         gdr.chunk_fwd(q, q, q, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4), 0.9, chunk=16)
+
+
+def test_path_query(lib, monkeypatch):
+    q = lib.gdr_chunk_fwd_path
+    assert q(1, 2, 256, 64, 64, 64, 0.9, 0) == 1          # fp32: staged kernels
+    assert q(1, 2, 0, 128, 128, 64, 0.95, 1) == 0         # empty: no kernel
+    assert q(1, 2, 256, 48, 128, 64, 0.95, 1) == -1       # rejected
+    monkeypatch.setenv("GDR_FUSED_VARIANT", "single")
+    assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 2
+    monkeypatch.setenv("GDR_FUSED_VARIANT", "pair")
+    assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 3
