@@ -28,11 +28,10 @@
 // diag(beta) E in fp32 over X's rows 0-63, so the identity part of T is exact.
 // The zero halves come from an 8 KB zero tile between Lb and P.
 //
-// Warp roles (512 threads, 128 registers each): prep 0-7; chain 8-13 (warps 8,
-// 9, 12, 13 own X rows 0-63, two warps per TMEM lane quadrant splitting the 64
-// columns; warps 10-11 own rows 64-127); copy 14 (TMA of K and Q, decay, L2
-// prefetch of K, Q and V); MMA 15 ([K;Q]K^T of the chunks this CTA prepares).
-// The v rows of the next chunk are loaded by TMA (issued by a chain thread of warps 10-11)
+// Warp roles (448 threads): prep 0-7, chain 8-11 (warps 8-9 own X rows 0-63,
+// warps 10-11 rows 64-127), copy 12 (TMA of K and Q, decay, L2 prefetch of
+// K, Q and V), MMA 13 ([K;Q]K^T of the chunks this CTA prepares).  The v rows
+// of the next chunk are loaded by TMA (issued by a chain thread of warps 10-11)
 // into a single buffer as soon as the current chunk's E step has read it.
 // Every wait is done by one thread per role, suspended in mbarrier.try_wait,
 // and passed on by a named barrier.
@@ -48,8 +47,7 @@
 namespace gdr {
 namespace {
 
-constexpr int NT = 512;    // prep (256) + chain (192) + copy (32) + MMA issue (32)
-constexpr int NCHAIN = 192, NEROWS = 128, NOROWS = 64;   // chain, its E group, its O group
+constexpr int NT = 448;    // prep (256) + chain (128) + copy (32) + MMA issue (32)
 constexpr int DVH = 64;    // value columns per CTA
 constexpr int NSTAGE = 3;  // input stages
 constexpr int NSCAL = 4;   // scalar slots (chunk m uses slot m % 4)
@@ -156,10 +154,10 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 14) {
+    if (warp == 12) {
         tmem_alloc(smem_u32(&s_tmem), TM_COLS);
         tmem_relinquish();
-        if (tid == 448) {
+        if (tid == 384) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
@@ -294,7 +292,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mbar_arrive_remote(cluster_map(bar(B_LREADY0 + rho), (uint32_t)peer));
             }
         }
-    } else if (warp == 15) {
+    } else if (warp == 13) {
         // ================================================================ MMA issue
         // [K;Q]K^T of this CTA's chunks k = rho, rho + 2, ...: each once its stage has
         // landed and the preparation has read the previous one's accumulator.
@@ -323,20 +321,13 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
         }
         __syncwarp();
-    } else if (warp < 14) {
+    } else if (warp < 12) {
         // ================================================================ chain
-        // warps 8-13.  TMEM lane quadrant qd = warp % 4; lane = row of X and of M_J.
-        // E group (X rows 0-63): warps 8, 9 (columns 0-31) and 12, 13 (columns 32-63).
-        // O group (X rows 64-127): warps 10, 11, all 64 columns.
-        const int lane = tid & 31, qd = warp & 3;
-        const int row = qd * 32 + lane;
-        const bool eg = qd < 2;
-        const int hc = (warp >= 12) ? 1 : 0;            // E group: this warp's column half
-        const int h_lo = eg ? hc : 0, h_hi = eg ? hc + 1 : 2;   // column halves of M_J rows
-        const bool elead = (warp == 8 && lane == 0), olead = (warp == 10 && lane == 0);
+        const int w = tid - 256;                 // TMEM lane = row of X and of M_J
+        const int qd = warp - 8;
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
         bool issued = false, issued_o = false;
-        uint32_t issued_v = 0;   // TMA loads of v issued (O-group leader)
+        uint32_t issued_v = 0;   // TMA loads of v issued (threads 0 and 64)
         const uint32_t peer_free = cluster_map(bar(B_PEERFREE), (uint32_t)peer);
 
         // X(n) = [K;Q] MS  (chunk n's stage)
@@ -353,18 +344,18 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             issued = true;
         };
 
-        bool ok = !elead || role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
-        ok = named_and(BAR_CHAIN, NCHAIN, ok);
+        bool ok = (w != 0) || role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
+        ok = named_and(BAR_CHAIN, 128, ok);
         if (ok) {
-            // initial state: TMEM M_J <- gamma_C(0) M_0[:, J], MS <- bf16(M_0[:, J]); lane = row i
+            // initial state: TMEM M_J <- gamma_C(0) M_0[:, J], MS <- bf16(M_0[:, J]); thread = row i
             const float gC = s_gC[0];
-            const float *src = a.init ? a.init + ((int64_t)bh * D + row) * D + j0 : nullptr;
+            const float *src = a.init ? a.init + ((int64_t)bh * D + w) * D + j0 : nullptr;
 #pragma unroll 1
-            for (int h = h_lo; h < h_hi; ++h) {
+            for (int h = 0; h < 2; ++h) {
                 float v[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = src ? src[h * 32 + e] : 0.f;
-                st_halfrow_bf16(sm + OFF_MS, row, h, v);
+                st_halfrow_bf16(sm + OFF_MS, w, h, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= gC;
                 tmem_st32(tl + TM_M + h * 32, v);
@@ -372,7 +363,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            if (olead) {
+            if (w == 64) {
                 mbar_arrive_expect_tx(bar(B_VFULL), 8192);
                 tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, 0, bh);
                 issued_v = 1;
@@ -381,38 +372,40 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int n = 0; ok && n < NC; ++n) {
             // ---- X(n) = [K;Q] MS_n once chunk n's stage has landed (MS_n: the previous
             // iteration's state step, or the initial state)
-            if (elead)
+            if (w == 0)
                 ok = role_wait(bar(B_FULL0 + n % NSTAGE), (uint32_t)(n / NSTAGE) & 1u, a.limit_ns,
                                &s_abort);
-            if (!named_and(BAR_CHAIN, NCHAIN, ok)) { ok = false; break; }
-            if (elead) issue_km(n);
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 0) issue_km(n);
             const int st = n % NSTAGE, b = n & 1, sl = n % NSCAL, sl1 = (n + 1) % NSCAL;
             const int t0 = n * C;
+            const int c = min(C, T - t0);
             const Scal S = scal(sm, sl);
             const uint32_t kq_a = sbase + OFF_KQ + st * KQ_BYTES;
             const uint32_t lp_a = sbase + OFF_LP + b * LP_BYTES;
             const uint32_t xcol = TM_X + (n & 1) * 64;
             const bool last = (n + 1 == NC);
 
-            if (eg) {
-                // ---- E = V - gamma K M_n -> EW (bf16); X rows 0-63 <- beta E (fp32);
-                // this thread: row `row`, columns 32 hc .. 32 hc + 31
-                if (elead) ok = role_wait(bar(B_VFULL), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-                if (ok && elead) ok = role_wait(bar(B_KM), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-                ok = named_and(BAR_EROWS, NEROWS, ok);
+            if (w < 64) {
+                // ---- E = V - gamma K M_n -> EW (bf16); X rows 0-63 <- beta E (fp32)
+                if (w == 0) ok = role_wait(bar(B_VFULL), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_EROWS, 64, ok);
+                if (w == 0 && ok) ok = role_wait(bar(B_KM), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_EROWS, 64, ok);
                 tc_fence_after();
-                if (ok) {
-                    const float gr = S.gam[row], br = S.bs[row];
-                    // v[t0 + row][J] in the v buffer (zero-filled past T by the copy); the
-                    // buffer is refilled only after the chain barrier that follows this step
-                    const uint8_t *vrow = sm + OFF_VB + row * 128;
+                const float gr = S.gam[w], br = S.bs[w];
+                // v[t0 + w][J], row w of the v buffer (zero-filled past T by the copy); the
+                // buffer is refilled only after the chain barrier that follows this step
+                const uint8_t *vrow = sm + OFF_VB + w * 128;
+#pragma unroll 1
+                for (int cb = 0; cb < (ok ? 2 : 0); ++cb) {
                     float x[32];
-                    tmem_ld32(tl + xcol + hc * 32, x);
+                    tmem_ld32(tl + xcol + cb * 32, x);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         const uint4 u = *reinterpret_cast<const uint4 *>(
-                            vrow + (((uint32_t)(hc * 4 + q4) ^ (uint32_t)(row & 7)) << 4));
+                            vrow + (((uint32_t)(cb * 4 + q4) ^ (uint32_t)(w & 7)) << 4));
                         const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int p2 = 0; p2 < 4; ++p2) {
@@ -422,40 +415,41 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             x[q4 * 8 + 2 * p2 + 1] = fmaf(-gr, x[q4 * 8 + 2 * p2 + 1], f.y);
                         }
                     }
-                    st_halfrow_bf16(sm + OFF_EW, row, hc, x);
+                    st_halfrow_bf16(sm + OFF_EW, w, cb, x);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[e] *= br;
-                    tmem_st32(tl + xcol + hc * 32, x);
-                    tmem_wait_st();
-                    fence_proxy_async_smem();
+                    tmem_st32(tl + xcol + cb * 32, x);
                 }
+                tmem_wait_st();
+                fence_proxy_async_smem();
             } else if (n > 0) {
                 // ---- output of chunk n-1, once its last product has landed
-                if (olead) ok = role_wait(bar(B_O2), (uint32_t)(n - 1) & 1u, a.limit_ns, &s_abort);
-                ok = named_and(BAR_OROWS, NOROWS, ok);
+                if (w == 64) ok = role_wait(bar(B_O2), (uint32_t)(n - 1) & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_OROWS, 64, ok);
                 if (ok) {
-                    if (olead) {   // chunk n-1's LP buffer is read: free it for its producer
+                    if (w == 64) {   // chunk n-1's LP buffer is read: free it for its producer
                         if (((n - 1) & 1) == rho) mbar_arrive_relaxed(bar(B_LPFREE));
                         else mbar_arrive_remote_relaxed(peer_free);
                     }
                     tc_fence_after();
                     const int m = n - 1;
-                    emit_output_rows(tl + TM_X + (m & 1) * 64, row - 64, min(C, T - m * C),
+                    emit_output_rows(tl + TM_X + (m & 1) * 64, w - 64, min(C, T - m * C),
                                      scal(sm, m % NSCAL).gam, a.out + (row_base + m * C) * D + j0);
                 }
             }
             // Lb of chunk n is needed from here on
-            if (ok && elead)
+            if (ok && w == 0)
                 ok = role_wait_cluster(bar(B_LREADY0 + b), (uint32_t)(n >> 1) & 1u, a.limit_ns,
                                        &s_abort);
             tc_fence_before();
-            if (!named_and(BAR_CHAIN, NCHAIN, ok)) { ok = false; break; }
-            if (olead && !last) {   // the v buffer is read: refill it with the next chunk's rows
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 64 && !last) {   // the v buffer is read: refill it with the next chunk's rows
                 mbar_arrive_expect_tx(bar(B_VFULL), 8192);
                 tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, t0 + C, bh);
                 ++issued_v;
             }
-            if (elead) {   // X += [Lb; 0] E  (rows 0-63 become W)
+            if (w == 0) {   // X += [Lb; 0] E  (rows 0-63 become W)
+                fence_proxy_async_smem();
                 tc_fence_after();
                 const uint64_t da = sdesc_sw128(lp_a, 16, 1024);
                 const uint64_t db = sdesc_sw128(sbase + OFF_EW, 8192, 1024);
@@ -465,25 +459,28 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mma_commit(bar(B_C3));
             }
 
-            // ---- Wt = diag(gamma_C / gamma) W -> EW (bf16), E group
-            if (eg) {
-                if (elead) ok = role_wait(bar(B_C3), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-                ok = named_and(BAR_EROWS, NEROWS, ok);
+            // ---- Wt = diag(gamma_C / gamma) W -> EW (bf16), warps 8-9
+            if (w < 64) {
+                if (w == 0) ok = role_wait(bar(B_C3), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                ok = named_and(BAR_EROWS, 64, ok);
                 if (ok) {
                     tc_fence_after();
-                    const float sr = S.sc[row];
-                    float x[32];
-                    tmem_ld32(tl + xcol + hc * 32, x);
-                    tmem_wait_ld();
+                    const float sr = S.sc[w];
+#pragma unroll 1
+                    for (int cb = 0; cb < 2; ++cb) {
+                        float x[32];
+                        tmem_ld32(tl + xcol + cb * 32, x);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] *= sr;
-                    st_halfrow_bf16(sm + OFF_EW, row, hc, x);
+                        for (int e = 0; e < 32; ++e) x[e] *= sr;
+                        st_halfrow_bf16(sm + OFF_EW, w, cb, x);
+                    }
                     fence_proxy_async_smem();
                 }
             }
             tc_fence_before();
-            if (!named_and(BAR_CHAIN, NCHAIN, ok)) { ok = false; break; }
-            if (elead) {   // M_J += K^T Wt
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
+            if (w == 0) {   // M_J += K^T Wt
                 tc_fence_after();
                 const uint64_t da = sdesc_sw128(kq_a, 16384, 1024);
                 const uint64_t db = sdesc_sw128(sbase + OFF_EW, 8192, 1024);
@@ -491,7 +488,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM_M, sdesc_add(da, kk * 2048), sdesc_add(db, kk * 2048), idesc_d, 1);
                 mma_commit(bar(B_D));
-            } else if (olead) {   // X += [0; P] Wt  (rows 64-127 become O / gamma)
+            } else if (w == 64) {   // X += [0; P] Wt  (rows 64-127 become O / gamma)
                 tc_fence_after();
                 const uint64_t da = sdesc_sw128(lp_a + 8192, 16, 1024);
                 const uint64_t db = sdesc_sw128(sbase + OFF_EW, 8192, 1024);
@@ -502,8 +499,8 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 issued_o = true;
             }
 
-            // ---- state: MS <- bf16(M_{n+1}); TMEM M_J <- gamma_C(n+1) M_{n+1}; lane = row i
-            if (elead) {
+            // ---- state: MS <- bf16(M_{n+1}); TMEM M_J <- gamma_C(n+1) M_{n+1}; thread = row i
+            if (w == 0) {
                 ok = role_wait(bar(B_D), (uint32_t)n & 1u, a.limit_ns, &s_abort);
                 // every product reading this input stage is complete: let the copy warp refill it
                 if (ok) mbar_arrive(bar(B_KQFREE0 + st));
@@ -511,15 +508,15 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ok = role_wait(bar(B_SCAL0 + sl1), (uint32_t)((n + 1) / NSCAL) & 1u,
                                    a.limit_ns, &s_abort);
             }
-            if (!named_and(BAR_CHAIN, NCHAIN, ok)) { ok = false; break; }
+            if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             tc_fence_after();
             {
                 const float gn = last ? 1.f : s_gC[sl1];
                 float *fin = (last && a.final_state)
-                                 ? a.final_state + ((int64_t)bh * D + row) * D + j0
+                                 ? a.final_state + ((int64_t)bh * D + w) * D + j0
                                  : nullptr;
 #pragma unroll 1
-                for (int h = h_lo; h < h_hi; ++h) {
+                for (int h = 0; h < 2; ++h) {
                     float v[32];
                     tmem_ld32(tl + TM_M + h * 32, v);
                     tmem_wait_ld();
@@ -529,7 +526,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             for (int e = 0; e < 32; ++e) fin[h * 32 + e] = v[e];
                         }
                     } else {
-                        st_halfrow_bf16(sm + OFF_MS, row, h, v);
+                        st_halfrow_bf16(sm + OFF_MS, w, h, v);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] *= gn;
                         tmem_st32(tl + TM_M + h * 32, v);
@@ -540,23 +537,23 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             fence_proxy_async_smem();
             tc_fence_before();
         }
-        if (ok && !eg) {   // output of the last chunk
-            if (olead) ok = role_wait(bar(B_O2), (uint32_t)(NC - 1) & 1u, a.limit_ns, &s_abort);
-            ok = named_and(BAR_OROWS, NOROWS, ok);
+        if (ok && w >= 64) {   // output of the last chunk
+            if (w == 64) ok = role_wait(bar(B_O2), (uint32_t)(NC - 1) & 1u, a.limit_ns, &s_abort);
+            ok = named_and(BAR_OROWS, 64, ok);
             if (ok) {
                 tc_fence_after();
                 const int m = NC - 1;
-                emit_output_rows(tl + TM_X + (m & 1) * 64, row - 64, min(C, T - m * C),
+                emit_output_rows(tl + TM_X + (m & 1) * 64, w - 64, min(C, T - m * C),
                                  scal(sm, m % NSCAL).gam, a.out + (row_base + m * C) * D + j0);
             }
         }
-        if (s_abort && elead && issued) {
+        if (s_abort && w == 0 && issued) {
             mma_commit(bar(B_DRAINC));
             mbar_wait(bar(B_DRAINC), 0u, kCleanupLimitNs);
         }
-        if (s_abort && olead && issued_v > 0)   // the latest v load may still be in flight
+        if (s_abort && w == 64 && issued_v > 0)   // the latest v load may still be in flight
             mbar_wait(bar(B_VFULL), (issued_v - 1) & 1u, kCleanupLimitNs);
-        if (s_abort && olead && issued_o) {
+        if (s_abort && w == 64 && issued_o) {
             mma_commit(bar(B_DRAINO));
             mbar_wait(bar(B_DRAINO), 0u, kCleanupLimitNs);
         }
@@ -627,7 +624,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 14) {
+    if (warp == 12) {
         __syncwarp();
         tmem_dealloc(tmem, TM_COLS);
     }
