@@ -19,7 +19,7 @@ import torch
 from . import build as _build
 
 __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk_wy",
-           "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "last_device_error", "status_string", "version",
+           "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "chunk_fwd_varlen", "last_device_error", "status_string", "version",
            "library_path", "STATUS"]
 
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
@@ -56,6 +56,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     sig = {
         "gdr_chunk_fwd": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp],
+        "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
         "gdr_chunk_decay": [vp, f, vp, i, i, i, vp],
         "gdr_chunk_wy": [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
@@ -127,6 +128,31 @@ def chunk_fwd(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 6
     _check(lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
                              _ptr(init_state), _ptr(out), _ptr(final_state), B, H, T, dk, dv,
                              int(chunk), DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd")
+    return out, final_state
+
+
+def chunk_fwd_varlen(q, k, v, g, beta, a_min: float, cu_seqlens, init_state=None, *,
+                     chunk: int = 64, out=None, final_state=None, want_final: bool = True):
+    """Chunked prefill over packed sequences.  q,k [total_T,H,dk], v [total_T,H,dv] bf16,
+    g,beta [total_T,H] fp32, cu_seqlens int32 [S+1] on the device, init_state [S,H,dk,dv]
+    fp32 or None.  Returns (out [total_T,H,dv], final_state [S,H,dk,dv])."""
+    lib = load()
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    S = cu_seqlens.numel() - 1
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_contiguous():
+        raise TypeError("cu_seqlens must be a contiguous int32 tensor")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(init_state, "init_state")
+    if out is None:
+        out = torch.empty((total_T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and want_final:
+        final_state = torch.empty((S, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check(lib.gdr_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
+                                    _ptr(init_state), _ptr(out), _ptr(final_state),
+                                    _ptr(cu_seqlens), S, H, total_T, dk, dv, int(chunk),
+                                    DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd_varlen")
     return out, final_state
 
 

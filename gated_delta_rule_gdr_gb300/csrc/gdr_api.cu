@@ -161,6 +161,31 @@ gdr_status_t gdr_chunk_output(const void *q, const void *k, const float *gamma, 
                                         elem_of(dtype), static_cast<cudaStream_t>(stream)));
 }
 
+gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, float a_min, const float *init_state,
+                                  void *out, float *final_state, const int *cu_seqlens, int S,
+                                  int H, int total_T, int dk, int dv, int chunk,
+                                  gdr_dtype_t dtype, void *stream) {
+    if (S < 0 || H < 0 || total_T < 0) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
+    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return GDR_ERR_UNSUPPORTED;
+    const int64_t SH = (int64_t)S * H;
+    if (SH > 0x7fffffff || (int64_t)total_T * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (SH == 0) return GDR_OK;
+    if (!cu_seqlens) return GDR_ERR_INVALID_ARG;
+    if (total_T == 0) {   // every sequence is empty
+        if (final_state == nullptr) return GDR_OK;
+        return from_cuda(gdr::launch_copy_state(init_state, final_state, SH * dk * dv, s));
+    }
+    if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_fused_varlen(q, k, v, g, beta, a_min, init_state, out,
+                                              final_state, cu_seqlens, S, H, total_T, s));
+}
+
 int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float a_min,
                           gdr_dtype_t dtype) {
     if (B < 0 || H < 0 || T < 0 || !dtype_ok(dtype) || !a_min_ok(a_min)) return -1;

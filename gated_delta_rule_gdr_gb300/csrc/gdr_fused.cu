@@ -130,9 +130,9 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int bh = blockIdx.x;
-    const int T = a.T;
+    const SeqView sv = seq_view(a, bh);        // dense [B][H][T] or packed sequences
+    const int T = sv.T;
     const int NC = (T + C - 1) / C;
-    const int64_t row_base = (int64_t)bh * T;
     auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
 
     if (tid == 0) {
@@ -261,7 +261,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mma_commit(bar(B_KQK));
                 issued = true;
             };
-            bool ok = role_wait(bar(B_FULL0), 0u, a.limit_ns, &s_abort);
+            bool ok = NC > 0 && role_wait(bar(B_FULL0), 0u, a.limit_ns, &s_abort);
             if (ok) kqk(0);
             for (int k = 0; ok && k + 1 < NC; ++k) {
                 ok = role_wait(bar(B_KQKFREE), (uint32_t)k & 1u, a.limit_ns, &s_abort);
@@ -296,8 +296,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tmem_wait_ld();
                 if (r64 < cm) {
                     const float gr = Sm.gam[r64];
-                    uint4 *orow = reinterpret_cast<uint4 *>(a.out + (row_base + m * C + r64) * D +
-                                                            h64 * 64 + cb * 32);
+                    uint4 *orow = reinterpret_cast<uint4 *>(
+                        a.out + (sv.gbase + (int64_t)(m * C + r64) * sv.stride) * D + h64 * 64 + cb * 32);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 u;
@@ -322,7 +322,12 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             issued = true;
         };
 
-        bool ok = role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
+        if (NC == 0 && a.final_state) {   // an empty sequence: final state = initial state
+            float *fin = a.final_state + ((int64_t)bh * D + w) * D;
+            const float *src = a.init ? a.init + ((int64_t)bh * D + w) * D : nullptr;
+            for (int e = 0; e < D; ++e) fin[e] = src ? src[e] : 0.f;
+        }
+        bool ok = NC > 0 && role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
         ok = named_and(BAR_CHAIN, 128, ok);
         if (ok) {
             // initial state: TMEM M <- gamma_C(0) M_0, MS <- bf16(M_0); thread = row i
@@ -510,31 +515,31 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const uint32_t kq = sbase + OFF_KQ + st * KQ_BYTES;
             const uint32_t vv = sbase + OFF_V + st * V_BYTES;
             mbar_arrive_expect_tx(b, KQ_BYTES + V_BYTES);
-            tma_load_3d(kq + 0, &tm_k, b, 0, n * C, bh);
-            tma_load_3d(kq + 8192, &tm_q, b, 0, n * C, bh);
-            tma_load_3d(kq + 16384, &tm_k, b, 64, n * C, bh);
-            tma_load_3d(kq + 24576, &tm_q, b, 64, n * C, bh);
-            tma_load_3d(vv + 0, &tm_v, b, 0, n * C, bh);
-            tma_load_3d(vv + 8192, &tm_v, b, 64, n * C, bh);
+            tma_load_3d(kq + 0, &tm_k, b, 0, sv.tz + n * C, sv.z);
+            tma_load_3d(kq + 8192, &tm_q, b, 0, sv.tz + n * C, sv.z);
+            tma_load_3d(kq + 16384, &tm_k, b, 64, sv.tz + n * C, sv.z);
+            tma_load_3d(kq + 24576, &tm_q, b, 64, sv.tz + n * C, sv.z);
+            tma_load_3d(vv + 0, &tm_v, b, 0, sv.tz + n * C, sv.z);
+            tma_load_3d(vv + 8192, &tm_v, b, 64, sv.tz + n * C, sv.z);
             ++issued[st];
         };
         // Pull the inputs of chunk n into L2 ahead of its shared-memory load, so
         // that the load (issued when a stage frees up) hits L2 rather than HBM.
         auto prefetch_l2 = [&](int n) {   // lane 0 only
             if (n >= NC) return;
-            tma_prefetch_3d(&tm_k, 0, n * C, bh);
-            tma_prefetch_3d(&tm_k, 64, n * C, bh);
-            tma_prefetch_3d(&tm_q, 0, n * C, bh);
-            tma_prefetch_3d(&tm_q, 64, n * C, bh);
-            tma_prefetch_3d(&tm_v, 0, n * C, bh);
-            tma_prefetch_3d(&tm_v, 64, n * C, bh);
+            tma_prefetch_3d(&tm_k, 0, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_k, 64, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_q, 0, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_q, 64, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_v, 0, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_v, 64, sv.tz + n * C, sv.z);
         };
         auto load_gb = [&](int n, float (&gv)[2], float (&bv)[2]) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int t = n * C + 2 * lane + e;
-                gv[e] = (t < T) ? a.g[row_base + t] : 0.f;
-                bv[e] = (t < T) ? a.beta[row_base + t] : 0.f;
+                gv[e] = (t < T) ? a.g[sv.gbase + (int64_t)t * sv.stride] : 0.f;
+                bv[e] = (t < T) ? a.beta[sv.gbase + (int64_t)t * sv.stride] : 0.f;
             }
         };
         auto decay = [&](int n, const float (&gv)[2], const float (&bv)[2]) {
@@ -604,7 +609,8 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
     const int BH = B * H;
     if (BH == 0 || T == 0) return cudaSuccess;
     if (use_pair(BH))
-        return launch_fused_pair(q, k, v, g, beta, a_min, init, out, final_state, BH, T, s);
+        return launch_fused_pair(q, k, v, g, beta, a_min, init, out, final_state, BH, T, nullptr,
+                                 H, 0, s);
     // TMA needs 16-byte aligned bases; the output rows are written as 16-byte vectors
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
@@ -630,6 +636,35 @@ cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value) {
     if (e == cudaSuccess) e = take_pair_error_word(&b);
     *value = a | b;
     return e;
+}
+
+cudaError_t launch_fused_varlen(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float a_min, const float *init, void *out,
+                                float *final_state, const int *cu_seqlens, int S, int H,
+                                int total_T, cudaStream_t s) {
+    const int64_t SH = (int64_t)S * H;
+    if (SH == 0) return cudaSuccess;
+    if (use_pair((int)SH))
+        return launch_fused_pair(q, k, v, g, beta, a_min, init, out, final_state, (int)SH, 0,
+                                 cu_seqlens, H, total_T, s);
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return cudaErrorMisalignedAddress;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_packed(&mq, q, H, total_T) || !make_map_packed(&mk, k, H, total_T) ||
+        !make_map_packed(&mv, v, H, total_T))
+        return cudaErrorInvalidValue;
+    FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, 0,
+                wait_limit_ns()};
+    a.cu_seqlens = cu_seqlens;
+    a.H = H;
+    a.total_T = total_T;
+    cudaError_t e = cudaFuncSetAttribute(fused_prefill_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    fused_prefill_kernel<<<(unsigned)SH, NT, SMEM_ALLOC, s>>>(mq, mk, mv, a);
+    return cudaGetLastError();
 }
 
 }  // namespace gdr

@@ -279,7 +279,42 @@ struct FusedArgs {
     int T;
     uint64_t limit_ns;
     const __nv_bfloat16 *v = nullptr;   // read directly by kernels that load v rows themselves
+    // Packed variable-length sequences: q, k, v, out [total_T][H][d], g, beta
+    // [total_T][H], sequence s = tokens cu_seqlens[s] .. cu_seqlens[s+1]; the
+    // state index is s H + h.  nullptr = the dense [B][H][T] layout.
+    const int *cu_seqlens = nullptr;
+    int H = 0, total_T = 0;
 };
+
+// Where the tokens of the (sequence, head) with state index bh live.  Token t
+// (0 <= t < T) of it: g / beta index gbase + t * stride, out row (d elements)
+// obase + t * stride, TMA coordinates (x, tz + t, z).
+struct SeqView {
+    int T, tz, z, stride;
+    int64_t gbase;
+};
+__device__ __forceinline__ SeqView seq_view(const FusedArgs &a, int bh) {
+    SeqView v;
+    if (!a.cu_seqlens) {
+        v.T = a.T;
+        v.tz = 0;
+        v.z = bh;
+        v.stride = 1;
+        v.gbase = (int64_t)bh * a.T;
+    } else {
+        // clamped into [0, total_T] so that a malformed offset array cannot take
+        // a CTA out of the tensors
+        const int s = bh / a.H, h = bh % a.H;
+        const int t0 = min(max(a.cu_seqlens[s], 0), a.total_T);
+        const int t1 = min(max(a.cu_seqlens[s + 1], t0), a.total_T);
+        v.T = t1 - t0;
+        v.tz = t0;
+        v.z = h;
+        v.stride = a.H;
+        v.gbase = (int64_t)t0 * a.H + h;
+    }
+    return v;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -301,6 +336,20 @@ bool make_map(CUtensorMap *m, const void *ptr, int BH, int T) {
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Packed [total_T][H][128] bf16 as a 3-D tensor (d, t, h): 64 x 64 boxes of
+// consecutive tokens of one head, 128-byte swizzle, zero fill beyond total_T.
+bool make_map_packed(CUtensorMap *m, const void *ptr, int H, int total_T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)total_T, (cuuint64_t)H};
+    cuuint64_t strides[2] = {(cuuint64_t)H * D * 2, (cuuint64_t)D * 2};
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,

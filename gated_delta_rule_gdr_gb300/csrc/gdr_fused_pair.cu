@@ -84,9 +84,10 @@ __device__ __forceinline__ Scal scal(uint8_t *sm, int slot) {
 
 // Output row r (< 64) of a chunk with c valid rows, this CTA's 64 columns:
 // out[r][:] = gamma_r X[64 + r][:], X in TMEM at column x (this thread's lane
-// = 64 + r).  One copy for both call sites.
+// = 64 + r); out0 = row 0 of the chunk, rows `orow` elements apart.  One copy
+// for both call sites.
 __device__ __noinline__ void emit_output_rows(uint32_t x, int r, int c, const float *gam,
-                                              __nv_bfloat16 *out0) {
+                                              __nv_bfloat16 *out0, int64_t orow) {
 #pragma unroll 1
     for (int cb = 0; cb < 2; ++cb) {
         float v[32];
@@ -94,7 +95,7 @@ __device__ __noinline__ void emit_output_rows(uint32_t x, int r, int c, const fl
         tmem_wait_ld();
         if (r < c) {
             const float gr = gam[r];
-            uint4 *orow = reinterpret_cast<uint4 *>(out0 + (int64_t)r * D + cb * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(out0 + (int64_t)r * orow + cb * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint4 u;
@@ -102,7 +103,7 @@ __device__ __noinline__ void emit_output_rows(uint32_t x, int r, int c, const fl
                 u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
                 u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
                 u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
-                __stcs(orow + q4, u);
+                __stcs(dst + q4, u);
             }
         }
     }
@@ -144,9 +145,11 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int rho = (int)cluster_rank(), peer = rho ^ 1;
     const int bh = blockIdx.x >> 1;
     const int j0 = rho * DVH;                 // first value column of this CTA
-    const int T = a.T;
+    const SeqView sv = seq_view(a, bh);        // dense [B][H][T] or packed sequences
+    const int T = sv.T;
     const int NC = (T + C - 1) / C;
-    const int64_t row_base = (int64_t)bh * T;
+    __nv_bfloat16 *const out0 = a.out + sv.gbase * D + j0;   // out row of token 0, columns J
+    const int64_t orow = (int64_t)sv.stride * D;             // elements between token rows
     auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
 
     if (tid == 0) {
@@ -344,7 +347,12 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             issued = true;
         };
 
-        bool ok = (w != 0) || role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort);
+        if (NC == 0 && a.final_state) {   // an empty sequence: final state = initial state
+            float *fin = a.final_state + ((int64_t)bh * D + w) * D + j0;
+            const float *src = a.init ? a.init + ((int64_t)bh * D + w) * D + j0 : nullptr;
+            for (int e = 0; e < DVH; ++e) fin[e] = src ? src[e] : 0.f;
+        }
+        bool ok = NC > 0 && ((w != 0) || role_wait(bar(B_SCAL0), 0u, a.limit_ns, &s_abort));
         ok = named_and(BAR_CHAIN, 128, ok);
         if (ok) {
             // initial state: TMEM M_J <- gamma_C(0) M_0[:, J], MS <- bf16(M_0[:, J]); thread = row i
@@ -365,7 +373,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             if (w == 64) {
                 mbar_arrive_expect_tx(bar(B_VFULL), 8192);
-                tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, 0, bh);
+                tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, sv.tz, sv.z);
                 issued_v = 1;
             }
         }
@@ -434,7 +442,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tc_fence_after();
                     const int m = n - 1;
                     emit_output_rows(tl + TM_X + (m & 1) * 64, w - 64, min(C, T - m * C),
-                                     scal(sm, m % NSCAL).gam, a.out + (row_base + m * C) * D + j0);
+                                     scal(sm, m % NSCAL).gam, out0 + (int64_t)m * C * orow, orow);
                 }
             }
             // Lb of chunk n is needed from here on
@@ -445,7 +453,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!named_and(BAR_CHAIN, 128, ok)) { ok = false; break; }
             if (w == 64 && !last) {   // the v buffer is read: refill it with the next chunk's rows
                 mbar_arrive_expect_tx(bar(B_VFULL), 8192);
-                tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, t0 + C, bh);
+                tma_load_3d(sbase + OFF_VB, &tm_v, bar(B_VFULL), j0, sv.tz + t0 + C, sv.z);
                 ++issued_v;
             }
             if (w == 0) {   // X += [Lb; 0] E  (rows 0-63 become W)
@@ -544,7 +552,7 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 const int m = NC - 1;
                 emit_output_rows(tl + TM_X + (m & 1) * 64, w - 64, min(C, T - m * C),
-                                 scal(sm, m % NSCAL).gam, a.out + (row_base + m * C) * D + j0);
+                                 scal(sm, m % NSCAL).gam, out0 + (int64_t)m * C * orow, orow);
             }
         }
         if (s_abort && w == 0 && issued) {
@@ -566,27 +574,27 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t b = bar(B_FULL0 + st);
             const uint32_t kq = sbase + OFF_KQ + st * KQ_BYTES;
             mbar_arrive_expect_tx(b, KQ_BYTES);
-            tma_load_3d(kq + 0, &tm_k, b, 0, n * C, bh);
-            tma_load_3d(kq + 8192, &tm_q, b, 0, n * C, bh);
-            tma_load_3d(kq + 16384, &tm_k, b, 64, n * C, bh);
-            tma_load_3d(kq + 24576, &tm_q, b, 64, n * C, bh);
+            tma_load_3d(kq + 0, &tm_k, b, 0, sv.tz + n * C, sv.z);
+            tma_load_3d(kq + 8192, &tm_q, b, 0, sv.tz + n * C, sv.z);
+            tma_load_3d(kq + 16384, &tm_k, b, 64, sv.tz + n * C, sv.z);
+            tma_load_3d(kq + 24576, &tm_q, b, 64, sv.tz + n * C, sv.z);
             ++issued[st];
         };
         // Pull the inputs of chunk n into L2 ahead of use (v is read from L2 by the chain).
         auto prefetch_l2 = [&](int n) {   // lane 0 only
             if (n >= NC) return;
-            tma_prefetch_3d(&tm_k, 0, n * C, bh);
-            tma_prefetch_3d(&tm_k, 64, n * C, bh);
-            tma_prefetch_3d(&tm_q, 0, n * C, bh);
-            tma_prefetch_3d(&tm_q, 64, n * C, bh);
-            tma_prefetch_3d(&tm_v, j0, n * C, bh);
+            tma_prefetch_3d(&tm_k, 0, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_k, 64, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_q, 0, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_q, 64, sv.tz + n * C, sv.z);
+            tma_prefetch_3d(&tm_v, j0, sv.tz + n * C, sv.z);
         };
         auto load_gb = [&](int n, float (&gv)[2], float (&bv)[2]) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int t = n * C + 2 * lane + e;
-                gv[e] = (t < T) ? a.g[row_base + t] : 0.f;
-                bv[e] = (t < T) ? a.beta[row_base + t] : 0.f;
+                gv[e] = (t < T) ? a.g[sv.gbase + (int64_t)t * sv.stride] : 0.f;
+                bv[e] = (t < T) ? a.beta[sv.gbase + (int64_t)t * sv.stride] : 0.f;
             }
         };
         auto decay = [&](int n, const float (&gv)[2], const float (&bv)[2]) {
@@ -636,16 +644,24 @@ fused_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
 cudaError_t launch_fused_pair(const void *q, const void *k, const void *v, const float *g,
                               const float *beta, float a_min, const float *init, void *out,
-                              float *final_state, int BH, int T, cudaStream_t s) {
-    if (BH == 0 || T == 0) return cudaSuccess;
+                              float *final_state, int BH, int T, const int *cu_seqlens, int H,
+                              int total_T, cudaStream_t s) {
+    if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;   // callers copy the state
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
         return cudaErrorMisalignedAddress;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T))
-        return cudaErrorInvalidValue;
+    const bool ok = cu_seqlens ? (make_map_packed(&mq, q, H, total_T) &&
+                                  make_map_packed(&mk, k, H, total_T) &&
+                                  make_map_packed(&mv, v, H, total_T))
+                               : (make_map(&mq, q, BH, T) && make_map(&mk, k, BH, T) &&
+                                  make_map(&mv, v, BH, T));
+    if (!ok) return cudaErrorInvalidValue;
     FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, T,
                 wait_limit_ns(), static_cast<const __nv_bfloat16 *>(v)};
+    a.cu_seqlens = cu_seqlens;
+    a.H = H;
+    a.total_T = total_T;
     cudaError_t e = cudaFuncSetAttribute(fused_pair_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);

@@ -37,13 +37,21 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
                          const float *beta, float a_min, const float *init, void *out,
                          float *final_state, int B, int H, int T, int dk, int dv, int C,
                          cudaStream_t s);
+// Packed variable-length sequences on the fused path (bf16, dk = dv = 128, C = 64).
+cudaError_t launch_fused_varlen(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float a_min, const float *init, void *out,
+                                float *final_state, const int *cu_seqlens, int S, int H,
+                                int total_T, cudaStream_t s);
 
 // ---- fused tensor-core prefill on a cluster of two CTAs per head (value columns
 // split, preparation alternated; gdr_fused_pair.cu); chosen by launch_fused when
 // every head's cluster is resident at once ----
+// cu_seqlens == nullptr: dense [BH][T] layout.  Otherwise packed sequences
+// (BH = S H states, tokens [total_T][H]), see gdr_chunk_fwd_varlen.
 cudaError_t launch_fused_pair(const void *q, const void *k, const void *v, const float *g,
                               const float *beta, float a_min, const float *init, void *out,
-                              float *final_state, int BH, int T, cudaStream_t s);
+                              float *final_state, int BH, int T, const int *cu_seqlens, int H,
+                              int total_T, cudaStream_t s);
 // Clusters of the pair kernel resident at once on the current device (0 if unknown).
 int fused_pair_max_clusters();
 // Whether launch_fused runs the cluster-pair kernel for BH heads on the current device.

@@ -120,3 +120,25 @@ def decode_step_inputs(w: Workload, step: int, device="cpu"):
     beta = torch.sigmoid(torch.randn((N, H), generator=_gen(device, w.seed, "beta", step + 1),
                                      device=device, dtype=torch.float32))
     return dict(q=q, k=k, v=v, g=g, beta=beta)
+
+
+def varlen_inputs(w: Workload, lengths, device="cpu"):
+    """Packed variable-length prefill inputs: sequence s has ``lengths[s]`` tokens,
+    drawn as ``prefill_inputs`` of ``w`` with B = 1, T = lengths[s] and its own seed.
+    Returns dict(q, k, v [total_T,H,d], g, beta [total_T,H], init_state [S,H,dk,dv] or
+    None, cu_seqlens int32 [S+1], seqs = the per-sequence dense dicts [1,H,T,...])."""
+    seqs = [prefill_inputs(w.with_(B=1, T=int(n), seed=w.seed * 1000 + s + 1), device)
+            for s, n in enumerate(lengths)]
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+
+    def pack(name):   # [1,H,T,...] per sequence -> [total_T,H,...]
+        return torch.cat([x[name][0].transpose(0, 1) for x in seqs], 0).contiguous()
+
+    init = None
+    if w.init_std is not None:
+        init = torch.cat([x["init_state"] for x in seqs], 0).contiguous()
+    return dict(q=pack("q"), k=pack("k"), v=pack("v"), g=pack("g"), beta=pack("beta"),
+                init_state=init, cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=device),
+                seqs=seqs)

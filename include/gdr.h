@@ -188,6 +188,32 @@ gdr_status_t gdr_chunk_fwd_static(const void *q, const void *k, const void *v,
                                   gdr_dtype_t dtype, void *stream);
 
 /*
+ * Chunked prefill over packed variable-length sequences (the serving shape:
+ * the prompts of several requests in one launch, no padding).  Same method,
+ * per sequence and head, as gdr_chunk_fwd.
+ *
+ * q, k, v  bf16 [total_T][H][dk | dv], row-major, token-major: the tokens of
+ *          sequence s are cu_seqlens[s] .. cu_seqlens[s+1] - 1.
+ * g, beta  fp32 [total_T][H].
+ * out      bf16 [total_T][H][dv].
+ * init_state, final_state  fp32 [S][H][dk][dv] (init may be NULL = zeros,
+ *          final may be NULL; they may alias).  The final states are directly
+ *          the decode states of gdr_decode_step with N = S.
+ * cu_seqlens  DEVICE int32 [S + 1], nondecreasing, cu_seqlens[0] = 0,
+ *          cu_seqlens[S] = total_T.  Read by the kernel; not checked on the host
+ *          (that would need a copy).  Offsets outside [0, total_T] are clamped, so
+ *          a malformed array gives wrong results but no out-of-bounds access.
+ *          An empty sequence gets final = init.
+ * Supported: bf16, dk = dv = 128, chunk = 64 (the fused kernels); anything
+ * else returns GDR_ERR_UNSUPPORTED.  Other errors as gdr_chunk_fwd.
+ */
+gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, float a_min, const float *init_state,
+                                  void *out, float *final_state, const int *cu_seqlens, int S,
+                                  int H, int total_T, int dk, int dv, int chunk,
+                                  gdr_dtype_t dtype, void *stream);
+
+/*
  * Number of kernel launches one gdr_chunk_fwd call with these arguments
  * enqueues (1 on the fused path, 4 on the staged path, 0 for empty work), or
  * -1 if the call would be rejected.  Host-only; touches no device.

@@ -125,3 +125,19 @@ def test_path_query(lib, monkeypatch):
     assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 2
     monkeypatch.setenv("GDR_FUSED_VARIANT", "pair")
     assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 3
+
+
+def test_varlen_rejects(lib):
+    f = lib.gdr_chunk_fwd_varlen
+    args = lambda **kw: [kw.get(n, d) for n, d in (
+        ("q", P), ("k", P), ("v", P), ("g", P), ("beta", P), ("a_min", 0.95), ("init", None),
+        ("out", P), ("fin", None), ("cu", P), ("S", 2), ("H", 2), ("tt", 100), ("dk", 128),
+        ("dv", 128), ("chunk", 64), ("dtype", 1), ("stream", None))]
+    assert f(*args(S=-1)) == 1                 # GDR_ERR_INVALID_ARG
+    assert f(*args(dtype=0)) == 2              # fp32: not on the fused path
+    assert f(*args(dk=64, dv=64)) == 2         # only dk = dv = 128
+    assert f(*args(chunk=32)) == 2             # only chunk 64
+    assert f(*args(a_min=0.2)) == 3            # range rule
+    assert f(*args(cu=None)) == 1              # offsets required
+    assert f(*args(q=None)) == 1
+    assert f(*args(S=0)) == 0                  # no sequences: nothing to do

@@ -140,6 +140,49 @@ def test_fused_variants(variant, B, H, T):
     assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
 
 
+@pytest.mark.parametrize("variant", ["single", "pair"])
+def test_varlen_packed_sequences(variant):
+    """Packed variable-length sequences (empty, 1-token, ragged and multi-chunk ones in
+    one launch) against the oracle run on each sequence on its own; the final states
+    then feed one decode step, which must equal the oracle's next token."""
+    w = I.PREFILL.with_(H=2)
+    lengths = [1, 63, 64, 0, 65, 200, 700, 130]
+    x = I.varlen_inputs(w, lengths, device="cuda")
+    with fused_variant(variant):
+        out, fin = gdr.chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                                        x["cu_seqlens"], x["init_state"])
+    torch.cuda.synchronize()
+    cu = x["cu_seqlens"].tolist()
+    ref_out, ref_fin = [], []
+    for s, xs in enumerate(x["seqs"]):
+        cpu = {n: (None if t is None else t.cpu()) for n, t in xs.items()}
+        if lengths[s] == 0:
+            ref_fin.append(cpu["init_state"][0].double())
+            continue
+        ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,
+                            cpu["init_state"])
+        ref_out.append(torch.as_tensor(ro)[0].transpose(0, 1))
+        ref_fin.append(torch.as_tensor(rf)[0])
+    e_o = rel(out.cpu(), torch.cat(ref_out, 0))
+    e_f = rel(fin.cpu(), torch.stack(ref_fin, 0))
+    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"], (e_o, e_f)
+    for s in range(len(lengths)):   # every sequence on its own, and the empty one exactly
+        if lengths[s]:
+            assert rel(out[cu[s]:cu[s + 1]].cpu(), ref_out[sum(1 for t in lengths[:s] if t)]) \
+                <= TOL["bf16"]
+    assert torch.equal(fin[3], x["init_state"][3])
+    # prefill -> decode handoff: one more token per sequence from the varlen final states
+    nxt = I.decode_step_inputs(w.with_(B=len(lengths)), 0, device="cuda")
+    st = fin.clone()
+    o1 = gdr.decode_step(nxt["q"], nxt["k"], nxt["v"], nxt["g"], nxt["beta"], w.a_min, st)
+    torch.cuda.synchronize()
+    ref_st = torch.stack(ref_fin, 0).numpy().copy()
+    r1 = oracle.decode(nxt["q"].cpu(), nxt["k"].cpu(), nxt["v"].cpu(), nxt["g"].cpu(),
+                       nxt["beta"].cpu(), w.a_min, ref_st)
+    assert rel(o1.cpu(), r1) <= TOL["bf16"]
+    assert gdr.last_device_error() == 0   # no bounded wait ran out (e.g. on the empty sequence)
+
+
 def test_zero_length_copies_state():
     w = I.PREFILL.with_(B=2, H=3, T=0)
     init = torch.randn(2, 3, 128, 128, device="cuda")
