@@ -2,14 +2,16 @@
 """Benchmark of the gated delta rule hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload prefill|long|million|decode] [--no-cpu-baseline]
+                    [--workload prefill|long|million|decode|varlen] [--no-cpu-baseline]
 
 One JSON line on rank 0.  A "step" of the default workload is one chunked
 prefill over B=4, H=16, T=4096, d=128, bf16 (cumulative decay, WY/UT
 transform, state pass and output); ``value`` is prefill tokens/s (B*T per
 step).  The same line carries a ``decode`` object for the single-token decode
 workload (N=256 sequences x H=32 heads, one token per step), because the
-metric asks for both.
+metric asks for both.  ``--workload varlen`` times the packed variable-length
+prefill instead: 32 sequences of seeded lengths in [16, 4096] (34,599 tokens),
+H=16, through ``chunk_fwd_varlen``; ``value`` is packed tokens/s.
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on
 the launching stream with an L2 flush (a 256 MB write) between steps, outside
@@ -65,6 +67,17 @@ def prefill_algorithmic(w: I.Workload):
     n_th = w.B * w.H * w.T
     by = n_th * ((2 * w.dk + 2 * w.dv) * es + 8)
     by += w.B * w.H * w.dk * w.dv * 4 * ((1 if w.init_std is not None else 0) + 1)
+    fl = n_th * (6 * w.dk * w.dv + 2 * w.chunk * (3 * w.dk + 2 * w.dv))
+    return by, fl
+
+
+def varlen_algorithmic(w: I.Workload, lengths):
+    """Bytes and FLOPs of one packed call: the prefill counts over total_T tokens,
+    with one fp32 state read and written per (sequence, head)."""
+    es = 2 if w.dtype == "bf16" else 4
+    n_th = sum(lengths) * w.H
+    by = n_th * ((2 * w.dk + 2 * w.dv) * es + 8)
+    by += len(lengths) * w.H * w.dk * w.dv * 4 * ((1 if w.init_std is not None else 0) + 1)
     fl = n_th * (6 * w.dk * w.dv + 2 * w.chunk * (3 * w.dk + 2 * w.dv))
     return by, fl
 
@@ -203,6 +216,43 @@ def bench_prefill(gdr, w, K, W, dev, flush, stream):
     return ms, ms_e2e, h2d, d2h
 
 
+def bench_varlen(gdr, w, K, W, dev, flush, stream):
+    lengths = I.varlen_lengths(w)
+    x = I.varlen_inputs(w, lengths, device=dev)
+    del x["seqs"]
+    total_T, S = sum(lengths), len(lengths)
+    out = torch.empty((total_T, w.H, w.dv), dtype=w.torch_dtype(), device=dev)
+    fin = torch.empty((S, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+
+    def step(_):
+        gdr.chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                             x["cu_seqlens"], x["init_state"], chunk=w.chunk, out=out,
+                             final_state=fin)
+
+    ms = time_steps(step, K, W, flush, stream)
+
+    # end to end: every packed input (cu_seqlens included) in, output and final states out
+    host = {n: (None if t is None else t.cpu().pin_memory()) for n, t in x.items()}
+    dx = {n: (None if t is None else torch.empty_like(t)) for n, t in x.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hfin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+
+    def e2e_step(_):
+        for n, t in host.items():
+            if t is not None:
+                dx[n].copy_(t, non_blocking=True)
+        gdr.chunk_fwd_varlen(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], w.a_min,
+                             dx["cu_seqlens"], dx["init_state"], chunk=w.chunk, out=out,
+                             final_state=fin)
+        hout.copy_(out, non_blocking=True)
+        hfin.copy_(fin, non_blocking=True)
+
+    ms_e2e = time_steps(e2e_step, max(3, K // 2), 2, flush, stream)
+    return ms, ms_e2e, h2d, d2h
+
+
 def bench_decode(gdr, w, K, W, dev, flush, stream):
     state = I.decode_state(w, device=dev)
     nsteps = max(K, 1)
@@ -256,6 +306,33 @@ def cpu_baseline_prefill(w, budget_s=12.0):
             "head_tokens_per_s": head_tok_s}
 
 
+def oracle_varlen_sample(w, lengths, budget_s, cores):
+    """The fp64 oracle over whole sequences of the packed workload, all heads, in
+    the workload's order, until about budget_s of work; (tokens, seconds, count)."""
+    import oracle
+    tok, dt, n = 0, 0.0, 0
+    for s, T in enumerate(lengths):
+        x = I.prefill_inputs(w.with_(B=1, T=int(T), seed=w.seed * 1000 + s + 1), device="cpu")
+        t0 = time.perf_counter()
+        oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                   nthreads=cores)
+        dt += time.perf_counter() - t0
+        tok += int(T)
+        n += 1
+        if dt >= budget_s:
+            break
+    return tok, dt, n
+
+
+def cpu_baseline_varlen(w, budget_s=12.0):
+    cores = os.cpu_count() or 1
+    lengths = I.varlen_lengths(w)
+    tok, dt, n = oracle_varlen_sample(w, lengths, budget_s, cores)
+    return {"value": tok / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"the first {n} of {len(lengths)} sequences, all {w.H} heads "
+                      f"({tok} of {sum(lengths)} tokens in {dt:.2f} s)"}
+
+
 def cpu_baseline_decode(w, budget_s=8.0):
     import numpy as np
     import oracle
@@ -289,8 +366,8 @@ def run_ours(args):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     pk, pk_kind = peaks()
 
-    main_w = {"prefill": I.PREFILL, "long": I.LONG_PREFILL, "million": I.MILLION_PREFILL,
-              "decode": I.DECODE}[args.workload]
+    main_w = WORKLOAD_ARG[args.workload]
+    varlen = main_w is I.VARLEN
 
     def barrier():
         torch.cuda.synchronize()
@@ -308,7 +385,10 @@ def run_ours(args):
     with ClockSampler(dev.index) as clocks:
         barrier()
         t_wall0 = time.perf_counter()
-        if main_w.steps == 0:
+        if varlen:
+            ms, ms_e2e, h2d, d2h = bench_varlen(gdr, main_w, args.steps, args.warmup, dev, flush,
+                                                stream)
+        elif main_w.steps == 0:
             ms, ms_e2e, h2d, d2h = bench_prefill(gdr, main_w, args.steps, args.warmup, dev, flush,
                                                  stream)
         else:
@@ -317,7 +397,7 @@ def run_ours(args):
         barrier()
         wall = time.perf_counter() - t_wall0
         dec = None
-        if main_w.steps == 0 and not args.no_decode:
+        if main_w.steps == 0 and not varlen and not args.no_decode:
             dec = bench_decode(gdr, I.DECODE, args.decode_steps, args.warmup, dev, flush, stream)
             barrier()
     assert gdr.last_device_error(dev) == 0, "device error word set"
@@ -325,12 +405,18 @@ def run_ours(args):
     ms_step = max_over_ranks(statistics.mean(ms))
     ms_e2e_step = max_over_ranks(statistics.mean(ms_e2e))
     if main_w.steps == 0:
-        tokens = main_w.B * main_w.T
-        by, fl = prefill_algorithmic(main_w)
+        if varlen:   # the packed call takes the fused path chunk_fwd takes for B = S
+            lengths = I.varlen_lengths(main_w)
+            tokens = sum(lengths)
+            by, fl = varlen_algorithmic(main_w, lengths)
+        else:
+            tokens = main_w.B * main_w.T
+            by, fl = prefill_algorithmic(main_w)
         nk = gdr.chunk_fwd_kernels(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
                                    main_w.chunk, main_w.a_min, main_w.torch_dtype())
         path = gdr.chunk_fwd_path(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
                                   main_w.chunk, main_w.a_min, main_w.torch_dtype())
+        assert not varlen or path in (2, 3), "the packed call runs the fused kernels only"
         csrc = "gated_delta_rule_gdr_gb300/csrc/"
         common = [csrc + "gdr_fused_common.cuh", csrc + "gdr_sm100.cuh"]
         kname, srcs = {
@@ -338,7 +424,7 @@ def run_ours(args):
             2: ("fused_prefill_kernel", [csrc + "gdr_fused.cu"] + common),
             3: ("fused_pair_kernel", [csrc + "gdr_fused_pair.cu"] + common),
         }[path]
-        metric = "prefill tokens/s"
+        metric = "packed prefill tokens/s" if varlen else "prefill tokens/s"
     else:
         tokens = main_w.B
         by, fl = decode_algorithmic(main_w), 0
@@ -371,6 +457,7 @@ def run_ours(args):
         "dtype": main_w.dtype, "data": "synthetic (seeded; recipe in gated_delta_rule_gdr_gb300/inputs.py)",
         "config": {"workload": main_w.name, "B": main_w.B, "H": main_w.H, "T": main_w.T,
                    "dk": main_w.dk, "dv": main_w.dv, "chunk": main_w.chunk,
+                   **({"total_T": tokens} if varlen else {}),
                    "a_min": main_w.a_min, "parallelism": f"replicas x{world}",
                    "l2": "256 MB L2 flush between timed steps" if main_w.steps == 0
                    else "state (537 MB) larger than L2, no flush"},
@@ -404,7 +491,8 @@ def run_ours(args):
             "gpu_launches": args.decode_steps,
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = (cpu_baseline_prefill(main_w) if main_w.steps == 0
+        line["cpu_baseline"] = (cpu_baseline_varlen(main_w) if varlen
+                                else cpu_baseline_prefill(main_w) if main_w.steps == 0
                                 else cpu_baseline_decode(main_w))
         if dec is not None:
             line["decode"]["cpu_baseline"] = cpu_baseline_decode(I.DECODE)
@@ -415,6 +503,10 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+WORKLOAD_ARG = {"prefill": I.PREFILL, "long": I.LONG_PREFILL, "million": I.MILLION_PREFILL,
+                "decode": I.DECODE, "varlen": I.VARLEN}
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, on bounded samples of the workload."""
@@ -422,11 +514,21 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    w = {"prefill": I.PREFILL, "long": I.LONG_PREFILL, "million": I.MILLION_PREFILL,
-         "decode": I.DECODE}[args.workload]
+    w = WORKLOAD_ARG[args.workload]
     cores = os.cpu_count() or 1
     times = []
-    if w.steps == 0:
+    if w is I.VARLEN:
+        lengths = I.varlen_lengths(w)
+        toks = []
+        for i in range(args.warmup + args.steps):
+            tok, dt, n = oracle_varlen_sample(w, lengths, 2.0, cores)
+            if i >= args.warmup:
+                times.append(dt)
+                toks.append(tok)
+        tok = statistics.mean(toks)
+        sample = f"per step: the first {n} of {len(lengths)} sequences, all {w.H} heads ({tok} tokens)"
+        metric = "packed prefill tokens/s"
+    elif w.steps == 0:
         x = I.prefill_inputs(w.with_(B=1), device="cpu")
         Ts = min(w.T, 512)
         sub = {n: x[n][:, :, :Ts] for n in ("q", "k", "v", "g", "beta")}
@@ -473,7 +575,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["prefill", "long", "million", "decode"],
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_ARG),
                     default="prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

@@ -24,9 +24,11 @@ from __future__ import annotations
 
 from dataclasses import dataclass, replace
 
+import math
+
 import torch
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "init": 6}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "init": 6, "lengths": 7}
 
 
 @dataclass(frozen=True)
@@ -65,7 +67,13 @@ MILLION_PREFILL = Workload("million_prefill_b1h16t1048576_d128_bf16", 1, 16, 104
 DECODE = Workload("decode_n256h32_d128_bf16_64steps", 256, 32, 1, 128, 128, 64, "bf16", 0.95,
                   init_std=0.02, steps=64)
 
-WORKLOADS = {w.name: w for w in (CORRECTNESS, PREFILL, LONG_PREFILL, MILLION_PREFILL, DECODE)}
+# Packed variable-length prefill (the serving shape): B = 32 sequences, H = 16, lengths
+# log-uniform in [16, T] (``varlen_lengths``), everything else as the prefill workload.
+VARLEN = Workload("varlen_s32h16_len16to4096_d128_bf16", 32, 16, 4096, 128, 128, 64, "bf16", 0.95,
+                  init_std=0.02)
+
+WORKLOADS = {w.name: w for w in (CORRECTNESS, PREFILL, LONG_PREFILL, MILLION_PREFILL, DECODE,
+                                 VARLEN)}
 
 
 def _gen(device, seed: int, tensor: str, extra: int = 0) -> torch.Generator:
@@ -142,3 +150,10 @@ def varlen_inputs(w: Workload, lengths, device="cpu"):
     return dict(q=pack("q"), k=pack("k"), v=pack("v"), g=pack("g"), beta=pack("beta"),
                 init_state=init, cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=device),
                 seqs=seqs)
+
+
+def varlen_lengths(w: Workload):
+    """Seeded sequence lengths of a packed workload: w.B values, log-uniform in [16, w.T]."""
+    u = torch.rand(w.B, generator=_gen("cpu", w.seed, "lengths"), dtype=torch.float64)
+    lo, hi = math.log(16.0), math.log(float(w.T))
+    return [int(round(math.exp(lo + (hi - lo) * float(x)))) for x in u]
