@@ -416,14 +416,21 @@ def run_ours(args):
                                    main_w.chunk, main_w.a_min, main_w.torch_dtype())
         path = gdr.chunk_fwd_path(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
                                   main_w.chunk, main_w.a_min, main_w.torch_dtype())
-        assert not varlen or path in (2, 3), "the packed call runs the fused kernels only"
+        assert not varlen or path in (2, 3, 4, 5), "the packed call runs the fused or two-kernel path"
         csrc = "gated_delta_rule_gdr_gb300/csrc/"
         common = [csrc + "gdr_fused_common.cuh", csrc + "gdr_sm100.cuh"]
         kname, srcs = {
             1: ("gdr_chunk_fwd staged (4 kernels)", [csrc + "gdr_staged.cu"]),
             2: ("fused_prefill_kernel", [csrc + "gdr_fused.cu"] + common),
             3: ("fused_pair_kernel", [csrc + "gdr_fused_pair.cu"] + common),
+            # the two-kernel step is timed as one unit (its two launches back to back)
+            4: ("chunk_prep_kernel + chain_kernel<64>",
+                [csrc + "gdr_prep.cu", csrc + "gdr_chain.cu"] + common),
+            5: ("chunk_prep_kernel + chain_kernel<128>",
+                [csrc + "gdr_prep.cu", csrc + "gdr_chain.cu"] + common),
         }[path]
+        if path in (4, 5):
+            nk = 2
         metric = "packed prefill tokens/s" if varlen else "prefill tokens/s"
     else:
         tokens = main_w.B

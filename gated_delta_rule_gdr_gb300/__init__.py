@@ -8,6 +8,11 @@ or PyTorch fallback.
 
     out, final = chunk_fwd(q, k, v, g, beta, a_min, init_state=None, chunk=64)
     out        = decode_step(q, k, v, g, beta, a_min, state)   # state in place
+
+chunk_fwd and chunk_fwd_varlen take the two-kernel path (a parallel chunk
+preparation into a workspace, then the state chain) when it applies, with the
+workspace from torch's caching allocator; workspace=None selects the
+single-launch path, a uint8 CUDA tensor supplies the workspace.
 """
 from __future__ import annotations
 
@@ -19,8 +24,9 @@ import torch
 from . import build as _build
 
 __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk_wy",
-           "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "chunk_fwd_varlen", "last_device_error", "status_string", "version",
-           "library_path", "STATUS"]
+           "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "chunk_fwd_varlen",
+           "chunk_fwd_workspace_size", "chunk_fwd_varlen_workspace_size", "last_device_error",
+           "status_string", "version", "library_path", "STATUS", "PATHS"]
 
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
           4: "GDR_ERR_CUDA", 5: "GDR_ERR_TIMEOUT"}
@@ -53,9 +59,13 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                "python -m gated_delta_rule_gdr_gb300.build")
         _build.build()
     lib = ctypes.CDLL(path)
-    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     sig = {
         "gdr_chunk_fwd": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp],
+        "gdr_chunk_fwd_ws": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp],
+        "gdr_chunk_fwd_varlen_ws": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp,
+                                    sz, vp],
+        "gdr_chunk_fwd_ws_path": [i, i, i, i, i, i, f, i],
         "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
         "gdr_chunk_decay": [vp, f, vp, i, i, i, vp],
@@ -72,6 +82,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    for name in ("gdr_chunk_fwd_workspace_size", "gdr_chunk_fwd_varlen_workspace_size"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i, i, i, i, i, i, i]
+        fn.restype = sz
     lib.gdr_status_string.restype = ctypes.c_char_p
     lib.gdr_version.restype = ctypes.c_char_p
     _lib = lib
@@ -111,8 +125,32 @@ def _f32(t, name):
     return t
 
 
+def _workspace(nbytes: int, workspace, device):
+    """The workspace to pass: None for the single-launch path, else a uint8 CUDA
+    tensor of at least nbytes ("auto": from torch's caching allocator)."""
+    if workspace is None or nbytes == 0:
+        return None
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.dtype != torch.uint8 or workspace.numel() < nbytes:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {nbytes} bytes")
+    return workspace
+
+
+def chunk_fwd_workspace_size(B, H, T, dk, dv, chunk=64, dtype=torch.bfloat16) -> int:
+    """Bytes of workspace the two-kernel path needs (0 where it does not apply)."""
+    return int(load().gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, DTYPE[dtype]))
+
+
+def chunk_fwd_varlen_workspace_size(S, H, total_T, dk, dv, chunk=64, dtype=torch.bfloat16) -> int:
+    """Bytes of workspace the packed two-kernel path needs (0 where it does not apply)."""
+    return int(load().gdr_chunk_fwd_varlen_workspace_size(S, H, total_T, dk, dv, chunk, DTYPE[dtype]))
+
+
 def chunk_fwd(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 64,
-              out=None, final_state=None, want_final: bool = True):
+              out=None, final_state=None, want_final: bool = True, workspace="auto"):
     """Chunked prefill.  q,k [B,H,T,dk], v [B,H,T,dv] (fp32 or bf16), g,beta [B,H,T]
     fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
     lib = load()
@@ -125,14 +163,22 @@ def chunk_fwd(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 6
         out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
     if final_state is None and want_final:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    _check(lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
-                             _ptr(init_state), _ptr(out), _ptr(final_state), B, H, T, dk, dv,
-                             int(chunk), DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd")
+    ws = _workspace(chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, q.dtype), workspace, q.device)
+    if ws is None:
+        _check(lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
+                                 _ptr(init_state), _ptr(out), _ptr(final_state), B, H, T, dk, dv,
+                                 int(chunk), DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd")
+    else:
+        _check(lib.gdr_chunk_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
+                                    _ptr(init_state), _ptr(out), _ptr(final_state), B, H, T, dk,
+                                    dv, int(chunk), DTYPE[q.dtype], _ptr(ws), ws.numel(),
+                                    _stream(q.device)), "gdr_chunk_fwd_ws")
     return out, final_state
 
 
 def chunk_fwd_varlen(q, k, v, g, beta, a_min: float, cu_seqlens, init_state=None, *,
-                     chunk: int = 64, out=None, final_state=None, want_final: bool = True):
+                     chunk: int = 64, out=None, final_state=None, want_final: bool = True,
+                     workspace="auto"):
     """Chunked prefill over packed sequences.  q,k [total_T,H,dk], v [total_T,H,dv] bf16,
     g,beta [total_T,H] fp32, cu_seqlens int32 [S+1] on the device, init_state [S,H,dk,dv]
     fp32 or None.  Returns (out [total_T,H,dv], final_state [S,H,dk,dv])."""
@@ -149,10 +195,20 @@ def chunk_fwd_varlen(q, k, v, g, beta, a_min: float, cu_seqlens, init_state=None
         out = torch.empty((total_T, H, dv), dtype=q.dtype, device=q.device)
     if final_state is None and want_final:
         final_state = torch.empty((S, H, dk, dv), dtype=torch.float32, device=q.device)
-    _check(lib.gdr_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
-                                    _ptr(init_state), _ptr(out), _ptr(final_state),
-                                    _ptr(cu_seqlens), S, H, total_T, dk, dv, int(chunk),
-                                    DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd_varlen")
+    ws = _workspace(chunk_fwd_varlen_workspace_size(S, H, total_T, dk, dv, chunk, q.dtype),
+                    workspace, q.device)
+    if ws is None:
+        _check(lib.gdr_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        float(a_min), _ptr(init_state), _ptr(out),
+                                        _ptr(final_state), _ptr(cu_seqlens), S, H, total_T, dk, dv,
+                                        int(chunk), DTYPE[q.dtype], _stream(q.device)),
+               "gdr_chunk_fwd_varlen")
+    else:
+        _check(lib.gdr_chunk_fwd_varlen_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                           float(a_min), _ptr(init_state), _ptr(out),
+                                           _ptr(final_state), _ptr(cu_seqlens), S, H, total_T, dk,
+                                           dv, int(chunk), DTYPE[q.dtype], _ptr(ws), ws.numel(),
+                                           _stream(q.device)), "gdr_chunk_fwd_varlen_ws")
     return out, final_state
 
 
@@ -235,13 +291,16 @@ def chunk_fwd_kernels(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat1
     return int(load().gdr_chunk_fwd_kernels(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
 
 
-PATHS = {0: "none", 1: "staged", 2: "fused one CTA per head", 3: "fused two-CTA cluster per head"}
+PATHS = {0: "none", 1: "staged", 2: "fused one CTA per head", 3: "fused two-CTA cluster per head",
+         4: "prep + chain, two CTAs per head", 5: "prep + chain, one CTA per head"}
 
 
-def chunk_fwd_path(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16) -> int:
+def chunk_fwd_path(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16,
+                   workspace: bool = True) -> int:
     """Which path one chunk_fwd call with these arguments takes on the current
-    device (see PATHS; -1 = rejected)."""
-    return int(load().gdr_chunk_fwd_path(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
+    device (see PATHS; -1 = rejected); workspace=False: the single-launch path."""
+    fn = load().gdr_chunk_fwd_ws_path if workspace else load().gdr_chunk_fwd_path
+    return int(fn(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
 
 
 def last_device_error(device=None) -> int:

@@ -6,6 +6,7 @@
 #include "gdr_internal.h"
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 
 namespace {
@@ -184,6 +185,81 @@ gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
     return from_cuda(gdr::launch_fused_varlen(q, k, v, g, beta, a_min, init_state, out,
                                               final_state, cu_seqlens, S, H, total_T, s));
+}
+
+// ---- two-kernel path with a caller-owned workspace ----
+
+size_t gdr_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                    gdr_dtype_t dtype) {
+    if (B < 0 || H < 0 || T < 0 || !dtype_ok(dtype)) return 0;
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return 0;
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0 || BH > 0x7fffffff || T == 0) return 0;
+    return gdr::prep_workspace_bytes((int)BH, T, nullptr, 0, 0);
+}
+
+size_t gdr_chunk_fwd_varlen_workspace_size(int S, int H, int total_T, int dk, int dv, int chunk,
+                                           gdr_dtype_t dtype) {
+    if (S < 0 || H < 0 || total_T < 0 || !dtype_ok(dtype)) return 0;
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return 0;
+    const int64_t SH = (int64_t)S * H;
+    if (SH == 0 || SH > 0x7fffffff || total_T == 0) return 0;
+    // only the sizes matter here; a non-null marker selects the packed layout
+    static const int marker = 0;
+    return gdr::prep_workspace_bytes((int)SH, 0, &marker, H, total_T);
+}
+
+gdr_status_t gdr_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, float a_min, const float *init_state, void *out,
+                              float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                              gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    const size_t need = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype);
+    if (need == 0 || workspace == nullptr || workspace_bytes < need)
+        return gdr_chunk_fwd(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk,
+                             dv, chunk, dtype, stream);
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    if ((int64_t)T * B * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    cudaError_t e = gdr::launch_prep(q, k, g, beta, a_min, workspace, BH, T, nullptr, 0, 0, s);
+    if (e == cudaSuccess)
+        e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace, BH,
+                              T, nullptr, 0, 0, s);
+    return from_cuda(e);
+}
+
+gdr_status_t gdr_chunk_fwd_varlen_ws(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, float a_min, const float *init_state,
+                                     void *out, float *final_state, const int *cu_seqlens, int S,
+                                     int H, int total_T, int dk, int dv, int chunk,
+                                     gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+    const size_t need = gdr_chunk_fwd_varlen_workspace_size(S, H, total_T, dk, dv, chunk, dtype);
+    if (need == 0 || workspace == nullptr || workspace_bytes < need)
+        return gdr_chunk_fwd_varlen(q, k, v, g, beta, a_min, init_state, out, final_state,
+                                    cu_seqlens, S, H, total_T, dk, dv, chunk, dtype, stream);
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    if ((int64_t)total_T * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (!cu_seqlens || !q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int SH = S * H;
+    cudaError_t e = gdr::launch_prep(q, k, g, beta, a_min, workspace, SH, 0, cu_seqlens, H,
+                                     total_T, s);
+    if (e == cudaSuccess)
+        e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace, SH,
+                              0, cu_seqlens, H, total_T, s);
+    return from_cuda(e);
+}
+
+int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
+                          gdr_dtype_t dtype) {
+    const int p = gdr_chunk_fwd_path(B, H, T, dk, dv, chunk, a_min, dtype);
+    if (p < 2 || gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) == 0) return p;
+    return gdr::chain_split(B * H) == 2 ? 4 : 5;
 }
 
 int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float a_min,

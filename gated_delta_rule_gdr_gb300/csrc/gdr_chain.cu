@@ -1,0 +1,605 @@
+// gdr_chain.cu -- the sequential half of the two-kernel prefill path: the
+// state chain of every (sequence, head) and the chunk outputs, reading the
+// [Lb | P] tiles that gdr_prep.cu wrote for every chunk.
+//
+// Chunk algebra (sections 3.1-3.3 of "What a Trillion-Parameter MoE Model
+// Reveals About the Next Stage of LLM Scaling"; the lower-bounded decay keeps
+// 1/gamma finite):
+//   E = V - diag(gamma) K M_n,   W = diag(beta) E + Lb E,   Wt = diag(gamma_C/gamma) W,
+//   O = diag(gamma) (Q M_n + P Wt),   M_{n+1} = gamma_C M_n + K^T Wt.
+//
+// Work split.  A CTA owns DVH value columns J of one head (DVH = 64: two CTAs
+// per head, independent of each other; DVH = 128: one).  The recurrence never
+// mixes value columns, so each chain warp c owns 16 columns j = 16 c .. 16 c +
+// 15 of J and runs their chain alone, with warp-level MMAs (mma.sync m16n8k16,
+// bf16 operands, fp32 accumulators) whose accumulator layout is the A-operand
+// layout of the next product: S_J = M_J^T (16 x 128 fp32, rows j) stays in
+// registers and feeds X^T = S_J K^T, E^T feeds E^T Lb^T and Wt^T feeds
+// S_J = gamma_C S_J + Wt^T K directly.  No chain step waits for another warp
+// or for a tensor-memory round trip.
+//
+// The output leaves the chain: [K;Q] MS_n and [Lb;P] Wt_n run on the 5th-
+// generation tensor cores (tcgen05, M = 128, N = DVH, accumulator in TMEM),
+// issued by an output thread once the chain warps have published MS_n =
+// bf16(S_J) and Wt_n; rows 64-127 of the accumulator are Q M_n + P Wt_n, which
+// the two output warps scale by gamma and store.
+//
+// Warps: chain 0 .. NCH-1 (NCH = DVH / 16), copy NCH (TMA of K, Q, v, the
+// [Lb | P] tile by a plain bulk copy, the decay of each stage, L2 prefetch),
+// NCH + 1 idle, output NCH + 2 and NCH + 3 (TMEM lane quadrants 2 and 3).
+// Every mbarrier wait is bounded in time; a timeout sets the device error
+// word and makes every role of the CTA leave its loop.
+//
+// Shared memory: NST stages of [K | Q (two 64-column slabs each) | v[s][J]
+// (64-column slabs) | Lb | P], MS ([slab i/64][j][64 i]), Wt[2] ([j][r]; a
+// chain warp's rows hold E^T first), the stage scalars.  Every bf16 tile has
+// 128-byte rows with the 16-byte chunks XOR-swizzled by row (the TMA and UMMA
+// 128-byte swizzle).
+
+#include "gdr_fused_common.cuh"
+
+namespace gdr {
+namespace {
+
+template <int DVH> struct ChainCfg {
+    static constexpr int NCH = DVH / 16;                   // chain warps
+    static constexpr int NT = 32 * (NCH + 4);
+    static constexpr int NST = DVH == 64 ? 3 : 2;          // input stages
+    static constexpr uint32_t ST_K = 0, ST_Q = 8192;       // + 16384 per 64-column slab
+    static constexpr uint32_t ST_V = 32768;                // DVH / 64 slabs of 8 KB
+    static constexpr uint32_t ST_LP = ST_V + DVH * 128;    // [Lb | P]
+    static constexpr uint32_t ST_BYTES = ST_LP + TILE_BYTES;
+    static constexpr int MSB = DVH == 64 ? 2 : 1;           // MS buffers (as shared memory allows)
+    static constexpr uint32_t OFF_MS = NST * ST_BYTES;     // MSB x 2 slabs of DVH x 128 B
+    static constexpr uint32_t MS_SLAB = DVH * 128;
+    static constexpr uint32_t OFF_WT = OFF_MS + MSB * 2 * MS_SLAB;
+    static constexpr uint32_t WT_BYTES = DVH * 128;
+    static constexpr uint32_t OFF_SC = OFF_WT + 2 * WT_BYTES;   // a 5 x 64 fp32 slot per stage
+    static constexpr uint32_t SMEM_USED = OFF_SC + NST * 5 * 64 * 4;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+    static constexpr uint32_t TM_COLS = DVH == 64 ? 128 : 256;  // output accumulator x 2
+    static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
+    static_assert(ST_BYTES % 1024 == 0 && OFF_MS % 1024 == 0 && OFF_WT % 1024 == 0 &&
+                      ST_LP % 1024 == 0 && MS_SLAB % 1024 == 0,
+                  "swizzled tiles must be 1024-byte aligned");
+};
+
+// mbarriers (index into s_bar)
+enum : int {
+    B_FULL0 = 0,          // stage landed (TMA, bulk copy) and its scalars written (x3, count 2)
+    B_FREE0 = 3,          // chain warps + output warps done with a stage (x3, count NCH + 1)
+    B_MSREADY = 6,        // chain warps: MS_n published (count NCH)
+    B_WTREADY0 = 7,       // chain warps: Wt_n published in buffer n % 2 (x2, count NCH)
+    B_QMS = 9,            // issue commit: [K;Q] MS_n done (single MS buffer: may be overwritten)
+    B_SAFE0 = 10,         // issue commit after [K;Q] MS_{n-1}: the output products that read
+                          //   Wt[n % 2] (chunk n-2) and MS[n % 2] (chunk n-1) are done (x2)
+    B_OFULL0 = 12,        // issue commit: accumulator buffer b complete (x2)
+    B_OFREE0 = 14,        // output warps: accumulator buffer b read out (x2)
+    B_DRAIN = 16,         // commit of the error path
+    NUM_BARS = 17
+};
+constexpr uint32_t BAR_OUT = 5;   // named barrier of the two output warps
+
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t c8) {
+    return row * 128u + ((c8 ^ (row & 7u)) << 4);
+}
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+
+// Output row r (< 64) of a chunk with c valid rows, NCOL columns from TMEM
+// column x (this thread's lane = 64 + r): out[r][:] = gamma_r X[64 + r][:].
+template <int NCOL>
+__device__ __noinline__ void emit_rows(uint32_t x, int r, int c, const float *gam, __nv_bfloat16 *out0,
+                                       int64_t orow) {
+#pragma unroll 1
+    for (int cb = 0; cb < NCOL / 32; ++cb) {
+        float v[32];
+        tmem_ld32(x + cb * 32, v);
+        tmem_wait_ld();
+        if (r < c) {
+            const float gr = gam[r];
+            uint4 *dst = reinterpret_cast<uint4 *>(out0 + (int64_t)r * orow + cb * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint4 u;
+                u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
+                u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
+                u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
+                u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+                __stcs(dst + q4, u);
+            }
+        }
+    }
+}
+
+template <int DVH>
+__global__ void __launch_bounds__(ChainCfg<DVH>::NT, 1)
+chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_v, const FusedArgs a, const uint8_t *ws,
+             int64_t nslot) {
+    using Cfg = ChainCfg<DVH>;
+    constexpr int NCH = Cfg::NCH, NST = Cfg::NST, SPLIT = 128 / DVH;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base, derived from the __shared__ array by pointer
+    // arithmetic so that every access through it stays a shared-memory access
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    __shared__ __align__(8) uint64_t s_bar[NUM_BARS];
+    __shared__ uint32_t s_tmem;
+    __shared__ float s_gC[NST];
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x / SPLIT, rho = blockIdx.x % SPLIT;
+    const int j0 = rho * DVH;                  // first value column of this CTA
+    const SeqView sv = seq_view(a, bh);        // dense [B][H][T] or packed sequences
+    const int T = sv.T;
+    const int NC = (T + C - 1) / C;
+    __nv_bfloat16 *const out0 = a.out + sv.gbase * D + j0;   // out row of token 0, columns J
+    const int64_t orow = (int64_t)sv.stride * D;             // elements between token rows
+    const uint8_t *tiles = ws + ((int64_t)sv.z * nslot + tile_slot0(a, bh, sv)) * TILE_BYTES;
+    auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
+    auto stage = [&](int n) { return sbase + (uint32_t)(n % NST) * Cfg::ST_BYTES; };
+    auto scal = [&](int n) { return scal_at(reinterpret_cast<float *>(sm + Cfg::OFF_SC) + (n % NST) * 5 * 64); };
+
+    if (tid == 0) {
+        for (int i = 0; i < NUM_BARS; ++i) {
+            uint32_t count = 1;
+            if (i >= B_FULL0 && i < B_FULL0 + 3) count = 2;
+            if (i >= B_FREE0 && i < B_FREE0 + 3) count = NCH + 1;
+            if (i == B_MSREADY || i == B_WTREADY0 || i == B_WTREADY0 + 1) count = NCH;
+            mbar_init(bar(i), count);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == NCH) {
+        tmem_alloc(smem_u32(&s_tmem), Cfg::TM_COLS);
+        tmem_relinquish();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp < NCH) {
+        // ================================================================ chain
+        // Warp c: value columns jw .. jw + 15 of J (S_J rows); lane 4g + t holds rows
+        // jw + g, jw + g + 8 and the column pairs 8 q + 2 t, +1 of each 8-column tile q.
+        const int cw = warp, g = lane >> 2, t4 = lane & 3;
+        const int jw = 16 * cw;
+        // ldmatrix lane roles for B fragments: from [n][k] rows (non-transposed) ...
+        const uint32_t bn_r = (uint32_t)((lane & 7) + (lane >> 4) * 8);
+        const uint32_t bn_c = (uint32_t)((lane >> 3) & 1);
+        // ... and from [k][n] rows (transposed), which is also the A-fragment
+        // pattern of a non-transposed [m][k] load
+        const uint32_t bt_r = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
+        const uint32_t bt_c = (uint32_t)(lane >> 4);
+        float s[16][4];   // S_J: rows jw + g (+ 8), columns i = 8 q + 2 t4 (+ 1)
+        {
+            const float *src = a.init ? a.init + (int64_t)bh * D * D + j0 + jw : nullptr;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int i = 8 * q + 2 * t4;
+                s[q][0] = src ? src[(int64_t)i * D + g] : 0.f;
+                s[q][1] = src ? src[(int64_t)(i + 1) * D + g] : 0.f;
+                s[q][2] = src ? src[(int64_t)i * D + g + 8] : 0.f;
+                s[q][3] = src ? src[(int64_t)(i + 1) * D + g + 8] : 0.f;
+            }
+        }
+        auto store_state = [&]() {   // S_J^T into the fp32 [dk][dv] final state
+            float *fin = a.final_state + (int64_t)bh * D * D + j0 + jw;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int i = 8 * q + 2 * t4;
+                fin[(int64_t)i * D + g] = s[q][0];
+                fin[(int64_t)(i + 1) * D + g] = s[q][1];
+                fin[(int64_t)i * D + g + 8] = s[q][2];
+                fin[(int64_t)(i + 1) * D + g + 8] = s[q][3];
+            }
+        };
+        // MS_m = bf16(S_J) into buffer m % MSB, rows j (K-major operand of the output product)
+        auto publish_ms = [&](int m) {
+            uint8_t *ms = sm + Cfg::OFF_MS + (m % Cfg::MSB) * 2 * Cfg::MS_SLAB;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const uint32_t off = (uint32_t)(q >> 3) * Cfg::MS_SLAB + 4u * t4;
+                *reinterpret_cast<uint32_t *>(ms + off + swz((uint32_t)(jw + g), (uint32_t)(q & 7))) =
+                    pack_bf16x2(s[q][0], s[q][1]);
+                *reinterpret_cast<uint32_t *>(ms + off + swz((uint32_t)(jw + g + 8), (uint32_t)(q & 7))) =
+                    pack_bf16x2(s[q][2], s[q][3]);
+            }
+            fence_proxy_async_smem();   // read by the output's tensor-core product
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_MSREADY));
+        };
+        // one lane waits; the warp learns the result
+        auto warp_wait = [&](int b, uint32_t parity) -> bool {
+            bool ok = true;
+            if (lane == 0) ok = role_wait(bar(b), parity, a.limit_ns, &s_abort);
+            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        };
+        // the start of chunk n: its stage, and (n > 0) the buffers it overwrites
+        auto chunk_wait = [&](int n) -> bool {
+            bool ok = true;
+            if (lane == 0) {
+                ok = role_wait(bar(B_FULL0 + n % NST), (uint32_t)(n / NST) & 1u, a.limit_ns, &s_abort);
+                if (ok && n > 0)
+                    ok = role_wait(bar(B_SAFE0 + (n & 1)), (uint32_t)((n - 1) >> 1) & 1u, a.limit_ns,
+                                   &s_abort);
+            }
+            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        };
+        if (NC == 0 && a.final_state) store_state();   // an empty sequence: final = initial
+        if (NC > 0) publish_ms(0);
+
+        for (int n = 0; n < NC; ++n) {
+            const int wb = n & 1;
+            const uint32_t st_a = stage(n);
+            // ---- K, Q, v, [Lb | P] and the scalars of chunk n are in place, and the
+            // Wt and MS buffers this chunk writes are free
+            if (!chunk_wait(n)) break;
+            const Scal S = scal(n);
+
+            // ---- X^T = S_J K^T (16 x 64, K = 128): A = bf16(S_J), B = K[s][i] rows
+            float x[8][4];
+#pragma unroll
+            for (int p = 0; p < 8; ++p) x[p][0] = x[p][1] = x[p][2] = x[p][3] = 0.f;
+            {
+                // B fragments of one k-step (16 i x 64 s), loaded a k-step ahead
+                auto load_k = [&](uint32_t (&bf)[4][4], int kt) {
+                    const uint32_t kb = st_a + Cfg::ST_K + (uint32_t)(kt >> 2) * 16384u;
+#pragma unroll
+                    for (int sp = 0; sp < 4; ++sp)
+                        ldsm_x4(bf[sp], kb + swz((uint32_t)(16 * sp) + bn_r, (uint32_t)((kt & 3) * 2) + bn_c));
+                };
+                uint32_t bq[2][4][4];
+                load_k(bq[0], 0);
+#pragma unroll
+                for (int kt = 0; kt < 8; ++kt) {   // i = 16 kt .. 16 kt + 15
+                    if (kt + 1 < 8) load_k(bq[(kt + 1) & 1], kt + 1);
+                    uint32_t af[4];
+                    af[0] = pack_bf16x2(s[2 * kt][0], s[2 * kt][1]);
+                    af[1] = pack_bf16x2(s[2 * kt][2], s[2 * kt][3]);
+                    af[2] = pack_bf16x2(s[2 * kt + 1][0], s[2 * kt + 1][1]);
+                    af[3] = pack_bf16x2(s[2 * kt + 1][2], s[2 * kt + 1][3]);
+#pragma unroll
+                    for (int sp = 0; sp < 4; ++sp) {   // s = 16 sp .. 16 sp + 15
+                        mma16816(x[2 * sp], af, bq[kt & 1][sp][0], bq[kt & 1][sp][1]);
+                        mma16816(x[2 * sp + 1], af, bq[kt & 1][sp][2], bq[kt & 1][sp][3]);
+                    }
+                }
+            }
+
+            // ---- E^T = V^T - X^T diag(gamma) -> bf16 into this warp's rows of the Wt
+            // tile of this chunk (buffer n % 2);  X^T <- E^T diag(beta) (fp32: the
+            // identity part of T)
+            uint8_t *wt = sm + Cfg::OFF_WT + wb * Cfg::WT_BYTES;
+            {
+                // v[s][J] (TMA, 64-column slabs; zero-filled past the end of a dense tensor)
+                const uint32_t vt = st_a + Cfg::ST_V + (uint32_t)(jw >> 6) * 8192u;
+                const uint32_t vc = (uint32_t)((jw >> 3) & 7);
+#pragma unroll
+                for (int sp = 0; sp < 4; ++sp) {
+                    // matrices (s 16sp+0..7 | 8..15) x (j jw+0..7 | jw+8..15), transposed:
+                    // vf[0] s 16sp+2t.., j g;  vf[1] s 16sp+2t.., j g+8;
+                    // vf[2] s 16sp+8+2t.., j g;  vf[3] s 16sp+8+2t.., j g+8
+                    uint32_t vf[4];
+                    ldsm_x4_t(vf, vt + swz((uint32_t)(16 * sp) + (uint32_t)(lane & 7) + (uint32_t)((lane >> 4) * 8),
+                                           vc + (uint32_t)((lane >> 3) & 1)));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int p = 2 * sp + h, sc0 = 8 * p + 2 * t4;
+                        const float2 ga = *reinterpret_cast<const float2 *>(&S.gam[sc0]);
+                        const float2 be = *reinterpret_cast<const float2 *>(&S.bs[sc0]);
+                        const float2 vlo = bf16x2_to_float2(vf[2 * h]);
+                        const float2 vhi = bf16x2_to_float2(vf[2 * h + 1]);
+                        const float e0 = fmaf(-ga.x, x[p][0], vlo.x), e1 = fmaf(-ga.y, x[p][1], vlo.y);
+                        const float e2 = fmaf(-ga.x, x[p][2], vhi.x), e3 = fmaf(-ga.y, x[p][3], vhi.y);
+                        *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g), (uint32_t)p) + 4 * t4) =
+                            pack_bf16x2(e0, e1);
+                        *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g + 8), (uint32_t)p) + 4 * t4) =
+                            pack_bf16x2(e2, e3);
+                        x[p][0] = be.x * e0;
+                        x[p][1] = be.y * e1;
+                        x[p][2] = be.x * e2;
+                        x[p][3] = be.y * e3;
+                    }
+                }
+            }
+            __syncwarp();
+
+            // ---- W^T = X^T + E^T Lb^T: A = E^T (this warp's rows), B = Lb[r][s] rows
+            {
+                const uint32_t lb_a = st_a + Cfg::ST_LP;
+                auto load_l = [&](uint32_t (&af)[4], uint32_t (&bf)[4][4], int ks) {
+                    ldsm_x4(af, smem_u32(wt) + swz((uint32_t)jw + bt_r, (uint32_t)(2 * ks) + bt_c));
+#pragma unroll
+                    for (int rp = 0; rp < 4; ++rp)
+                        ldsm_x4(bf[rp], lb_a + swz((uint32_t)(16 * rp) + bn_r, (uint32_t)(2 * ks) + bn_c));
+                };
+                uint32_t aq[2][4], bq[2][4][4];
+                load_l(aq[0], bq[0], 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {   // s = 16 ks .. 16 ks + 15
+                    if (ks + 1 < 4) load_l(aq[(ks + 1) & 1], bq[(ks + 1) & 1], ks + 1);
+#pragma unroll
+                    for (int rp = 0; rp < 4; ++rp) {   // r = 16 rp .. 16 rp + 15
+                        mma16816(x[2 * rp], aq[ks & 1], bq[ks & 1][rp][0], bq[ks & 1][rp][1]);
+                        mma16816(x[2 * rp + 1], aq[ks & 1], bq[ks & 1][rp][2], bq[ks & 1][rp][3]);
+                    }
+                }
+            }
+            __syncwarp();   // every lane has read E^T: Wt may overwrite it
+
+            // ---- Wt^T = W^T diag(gamma_C / gamma) -> bf16: A fragments, and the Wt tile
+            // ([j][r], K-major) that the output product reads
+            uint32_t ef[4][4];
+            {
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const int r0 = 8 * p + 2 * t4;
+                    const float2 sc = *reinterpret_cast<const float2 *>(&S.sc[r0]);
+                    const uint32_t lo = pack_bf16x2(sc.x * x[p][0], sc.y * x[p][1]);
+                    const uint32_t hi = pack_bf16x2(sc.x * x[p][2], sc.y * x[p][3]);
+                    ef[p >> 1][2 * (p & 1) + 0] = lo;
+                    ef[p >> 1][2 * (p & 1) + 1] = hi;
+                    *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g), (uint32_t)p) + 4 * t4) = lo;
+                    *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g + 8), (uint32_t)p) + 4 * t4) = hi;
+                }
+                fence_proxy_async_smem();   // read by the output's tensor-core product
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_WTREADY0 + wb));
+            }
+
+            // ---- S_J = gamma_C S_J + Wt^T K: B = K[r][i] rows (transposed)
+            {
+                const float gC = s_gC[n % NST];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[q][e] *= gC;
+                // B fragments of a quarter step (16 r x 64 i), loaded a quarter ahead
+                auto load_kt = [&](uint32_t (&bf)[4][4], int qq) {
+                    const int ks = qq >> 1, slab = qq & 1;
+#pragma unroll
+                    for (int ip = 0; ip < 4; ++ip)
+                        ldsm_x4_t(bf[ip], st_a + Cfg::ST_K + (uint32_t)slab * 16384u +
+                                              swz((uint32_t)(16 * ks) + bt_r, (uint32_t)(ip * 2) + bt_c));
+                };
+                uint32_t bq[2][4][4];
+                load_kt(bq[0], 0);
+#pragma unroll
+                for (int qq = 0; qq < 8; ++qq) {   // r = 16 (qq / 2) .., i = 64 (qq % 2) ..
+                    if (qq + 1 < 8) load_kt(bq[(qq + 1) & 1], qq + 1);
+                    const int ks = qq >> 1, slab = qq & 1;
+#pragma unroll
+                    for (int ip = 0; ip < 4; ++ip) {   // i = 64 slab + 16 ip ..
+                        mma16816(s[8 * slab + 2 * ip], ef[ks], bq[qq & 1][ip][0], bq[qq & 1][ip][1]);
+                        mma16816(s[8 * slab + 2 * ip + 1], ef[ks], bq[qq & 1][ip][2], bq[qq & 1][ip][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_FREE0 + n % NST));   // this warp is done with stage n
+            if (n + 1 < NC) {
+                // a single MS buffer is free once the output's [K;Q] MS_n has completed
+                if (Cfg::MSB == 1 && !warp_wait(B_QMS, (uint32_t)n & 1u)) break;
+                publish_ms(n + 1);
+            } else if (a.final_state) {
+                store_state();
+            }
+        }
+    } else if (warp == NCH + 1) {
+        // ================================================================ output products
+        if (lane == 0) {
+            const uint32_t idesc_o = idesc_bf16(128, DVH, false, false);   // K-major A and B
+            bool issued = false;
+            for (int n = 0; n < NC; ++n) {
+                const uint32_t st_a = stage(n);
+                const uint32_t acc = tmem + (uint32_t)(n & 1) * DVH;
+                // O(n) = [K;Q] MS_n (rows 64-127: Q M_n), once MS_n is out and the
+                // accumulator buffer has been read out (chunk n-2)
+                bool ok = role_wait(bar(B_MSREADY), (uint32_t)n & 1u, a.limit_ns, &s_abort);
+                if (ok) ok = role_wait(bar(B_FULL0 + n % NST), (uint32_t)(n / NST) & 1u, a.limit_ns, &s_abort);
+                if (ok && n > 1)
+                    ok = role_wait(bar(B_OFREE0 + (n & 1)), (uint32_t)((n - 2) >> 1) & 1u, a.limit_ns, &s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    const uint64_t da = sdesc_sw128(st_a + Cfg::ST_K, 16, 1024);
+                    const uint64_t db = sdesc_sw128(sbase + Cfg::OFF_MS + (uint32_t)(n % Cfg::MSB) * 2 * Cfg::MS_SLAB,
+                                                    16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(acc, sdesc_add(da, (kk >> 2) * 16384 + (kk & 3) * 32),
+                                 sdesc_add(db, (kk >> 2) * Cfg::MS_SLAB + (kk & 3) * 32), idesc_o, kk > 0);
+                }
+                mma_commit(bar(B_QMS));
+                // chunk n+1 may overwrite Wt[(n+1) % 2] and MS[(n+1) % 2] once every
+                // product issued so far (up to this one) is done
+                if (n + 1 < NC) mma_commit(bar(B_SAFE0 + ((n + 1) & 1)));
+                issued = true;
+                // O(n) += [Lb;P] Wt_n (rows 64-127: P Wt_n)
+                if (!role_wait(bar(B_WTREADY0 + (n & 1)), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort)) break;
+                tc_fence_after();
+                {
+                    const uint64_t dl = sdesc_sw128(st_a + Cfg::ST_LP, 16, 1024);
+                    const uint64_t dw = sdesc_sw128(sbase + Cfg::OFF_WT + (uint32_t)(n & 1) * Cfg::WT_BYTES, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(acc, sdesc_add(dl, kk * 32), sdesc_add(dw, kk * 32), idesc_o, 1);
+                }
+                mma_commit(bar(B_OFULL0 + (n & 1)));
+            }
+            if (s_abort && issued) {   // let this thread's MMAs land before TMEM goes away
+                mma_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0u, kCleanupLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= NCH + 2) {
+        // ================================================================ output rows
+        // thread r: accumulator row 64 + r (TMEM lane 64 + r) = output row r of a chunk
+        const int r = tid - 32 * (NCH + 2);
+        const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        for (int m = 0; m < NC; ++m) {
+            bool ok = (r != 0) ||
+                      role_wait(bar(B_OFULL0 + (m & 1)), (uint32_t)(m >> 1) & 1u, a.limit_ns, &s_abort);
+            if (!named_and(BAR_OUT, 64, ok)) break;
+            tc_fence_after();
+            emit_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, r, min(C, T - m * C), scal(m).gam,
+                           out0 + (int64_t)m * C * orow, orow);
+            tc_fence_before();
+            named_sync(BAR_OUT, 64);
+            if (r == 0) {
+                mbar_arrive(bar(B_OFREE0 + (m & 1)));   // the accumulator buffer is read out
+                mbar_arrive(bar(B_FREE0 + m % NST));    // the products of chunk m are done
+            }
+        }
+    } else {
+        // ================================================================ copy (warp NCH)
+        // Stage n % NST of chunk n: K and Q (two slabs each) and v[., J] by TMA, the
+        // [Lb | P] tile by a bulk copy, and the chunk's decay scalars; two arrivals
+        // (the expect_tx and the decay) and the bytes complete it.
+        uint32_t issued[3] = {0, 0, 0};
+        constexpr uint32_t STAGE_TX = 32768 + DVH * 128 + TILE_BYTES;
+        auto issue = [&](int n) {     // lane 0 only
+            const int st = n % NST;
+            const uint32_t b = bar(B_FULL0 + st);
+            const uint32_t kq = stage(n);
+            const int row = sv.tz + n * C;
+            mbar_arrive_expect_tx(b, STAGE_TX);
+            tma_load_3d(kq + Cfg::ST_K, &tm_k, b, 0, row, sv.z);
+            tma_load_3d(kq + Cfg::ST_Q, &tm_q, b, 0, row, sv.z);
+            tma_load_3d(kq + Cfg::ST_K + 16384, &tm_k, b, 64, row, sv.z);
+            tma_load_3d(kq + Cfg::ST_Q + 16384, &tm_q, b, 64, row, sv.z);
+#pragma unroll
+            for (int vs = 0; vs < DVH / 64; ++vs)
+                tma_load_3d(kq + Cfg::ST_V + vs * 8192, &tm_v, b, j0 + 64 * vs, row, sv.z);
+            bulk_load(kq + Cfg::ST_LP, tiles + (int64_t)n * TILE_BYTES, TILE_BYTES, b);
+            ++issued[st];
+        };
+        // Pull the inputs of chunk n into L2 ahead of their shared-memory loads.
+        auto prefetch_l2 = [&](int n) {   // lane 0 only
+            if (n >= NC) return;
+            const int row = sv.tz + n * C;
+            tma_prefetch_3d(&tm_k, 0, row, sv.z);
+            tma_prefetch_3d(&tm_k, 64, row, sv.z);
+            tma_prefetch_3d(&tm_q, 0, row, sv.z);
+            tma_prefetch_3d(&tm_q, 64, row, sv.z);
+#pragma unroll
+            for (int vs = 0; vs < DVH / 64; ++vs) tma_prefetch_3d(&tm_v, j0 + 64 * vs, row, sv.z);
+        };
+        auto load_gb = [&](int n, float (&gv)[2], float (&bv)[2]) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = n * C + 2 * lane + e;
+                gv[e] = (t < T) ? a.g[sv.gbase + (int64_t)t * sv.stride] : 0.f;
+                bv[e] = (t < T) ? a.beta[sv.gbase + (int64_t)t * sv.stride] : 0.f;
+            }
+        };
+        auto decay = [&](int n, const float (&gv)[2], const float (&bv)[2]) {
+            const int st = n % NST;
+            warp_decay(lane, gv, bv, min(C, T - n * C), a.a_min, scal(n), &s_gC[st]);
+            if (lane == 0) mbar_arrive(bar(B_FULL0 + st));
+        };
+        constexpr int kAhead = 3;   // chunks prefetched into L2 beyond the staged ones
+        float gv[2], bv[2];
+        if (lane == 0)
+            for (int n = 0; n < NST + kAhead; ++n) prefetch_l2(n);
+        for (int n = 0; n < NST && n < NC; ++n) {
+            load_gb(n, gv, bv);
+            if (lane == 0) issue(n);
+            decay(n, gv, bv);
+        }
+        if (NC > NST) load_gb(NST, gv, bv);
+        for (int n = 0; n + NST < NC; ++n) {   // refill a stage once chunk n is done with it
+            const int st = n % NST;
+            bool ok = (lane != 0) ||
+                      role_wait(bar(B_FREE0 + st), (uint32_t)(n / NST) & 1u, a.limit_ns, &s_abort);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) {
+                issue(n + NST);
+                prefetch_l2(n + NST + kAhead);
+            }
+            decay(n + NST, gv, bv);
+            if (n + NST + 1 < NC) load_gb(n + NST + 1, gv, bv);
+        }
+        if (s_abort && lane == 0) {
+            // at most the latest load of each stage can still be in flight (its decay
+            // arrival was made with it): wait for its bytes
+            for (int st = 0; st < NST; ++st)
+                if (issued[st] > 0)
+                    mbar_wait(bar(B_FULL0 + st), (issued[st] - 1) & 1u, kCleanupLimitNs);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == NCH) {
+        __syncwarp();
+        tmem_dealloc(tmem, Cfg::TM_COLS);
+    }
+}
+
+template <int DVH>
+cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const FusedArgs &a, const void *ws, int64_t nslot, int BH, cudaStream_t s) {
+    using Cfg = ChainCfg<DVH>;
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    chain_kernel<DVH><<<(unsigned)(BH * (128 / DVH)), Cfg::NT, Cfg::SMEM_ALLOC, s>>>(
+        mq, mk, mv, a, static_cast<const uint8_t *>(ws), nslot);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Value columns per CTA: two CTAs per head while every CTA has an SM of its
+// own, one CTA per head beyond that.  GDR_CHAIN_SPLIT=1|2 overrides it (the
+// tests cover both on small shapes).
+int chain_split(int BH) {
+    const char *env = std::getenv("GDR_CHAIN_SPLIT");
+    if (env && std::strcmp(env, "1") == 0) return 1;
+    if (env && std::strcmp(env, "2") == 0) return 2;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return 2 * BH <= sms ? 2 : 1;
+}
+
+cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         float a_min, const float *init, void *out, float *final_state, const void *ws,
+                         int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s) {
+    if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;   // callers copy the state
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(ws)) & 15)
+        return cudaErrorMisalignedAddress;
+    CUtensorMap mq, mk, mv;
+    const bool ok = cu_seqlens ? (make_map_packed(&mq, q, H, total_T) && make_map_packed(&mk, k, H, total_T) &&
+                                  make_map_packed(&mv, v, H, total_T))
+                               : (make_map(&mq, q, BH, T) && make_map(&mk, k, BH, T) && make_map(&mv, v, BH, T));
+    if (!ok) return cudaErrorInvalidValue;
+    FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, T, wait_limit_ns(),
+                static_cast<const __nv_bfloat16 *>(v)};
+    a.cu_seqlens = cu_seqlens;
+    a.H = H;
+    a.total_T = total_T;
+    const int64_t nslot = tile_slots(a, BH);
+    return chain_split(BH) == 2 ? launch_chain_t<64>(mq, mk, mv, a, ws, nslot, BH, s)
+                                : launch_chain_t<128>(mq, mk, mv, a, ws, nslot, BH, s);
+}
+
+cudaError_t take_chain_error_word(unsigned *value) { return take_error_word(value); }
+
+}  // namespace gdr

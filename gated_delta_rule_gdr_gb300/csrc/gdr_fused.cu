@@ -631,10 +631,12 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
 cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0;
     e = take_error_word(&a);
     if (e == cudaSuccess) e = take_pair_error_word(&b);
-    *value = a | b;
+    if (e == cudaSuccess) e = take_prep_error_word(&c);
+    if (e == cudaSuccess) e = take_chain_error_word(&d);
+    *value = a | b | c | d;
     return e;
 }
 

@@ -187,7 +187,8 @@ __device__ __forceinline__ void frag_store(float *M, int ld, int r0, int n0, con
         make_float2(sign * d[2], sign * d[3]);
 }
 
-// T = (I + A)^-1 for the strictly lower 64 x 64 A in As (fp32), into Ts, by
+// T = (I + A)^-1 for the strictly lower 64 x 64 A in As (fp32), into Ts (which
+// may be As itself: every block of A is read before T overwrites it), by
 // the prep warps (w = thread index 0..255).  Blocked: four 16 x 16
 // diagonal inverses by right-looking forward substitution in fp32 (one column
 // per thread), then two merge levels T_ij = -T_ii (A_ij T_jj) on tf32 warp
@@ -210,6 +211,7 @@ __device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *
 #pragma unroll
             for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(As[(o + r) * LDA + o + m], x[m], acc[r]);
         }
+        __syncwarp();   // the block's 16 lanes have read it: T may overwrite A (in place)
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             Ts[(o + r) * LDA + o + l] = x[r];
@@ -314,6 +316,23 @@ __device__ __forceinline__ SeqView seq_view(const FusedArgs &a, int bh) {
         v.gbase = (int64_t)t0 * a.H + h;
     }
     return v;
+}
+
+// Tiles of the two-kernel path: the preparation writes the [Lb | P] tile of
+// chunk n of a (sequence, head) view to tile index z * nslot + slot0 + n of
+// the workspace, and the chain kernel reads it there.
+//   dense [B][H][T]:  z = bh, nslot = ceil(T / C), slot0 = 0
+//   packed sequences: z = h,  nslot = total_T / C + S + 1, slot0 = t0 / C + s
+// (t0 the sequence's first token).  Packed slots never overlap: sequence s
+// ends below t1 / C + s + 1 <= slot0 of s + 1, and every slot of a malformed
+// offset array still falls inside [0, nslot).
+constexpr uint32_t TILE_BYTES = 16384;   // [Lb rows | P rows] bf16, 128-byte swizzled rows
+
+__host__ __device__ __forceinline__ int64_t tile_slots(const FusedArgs &a, int BH) {
+    return a.cu_seqlens ? (int64_t)(a.total_T / C + BH / a.H + 1) : (int64_t)((a.T + C - 1) / C);
+}
+__device__ __forceinline__ int tile_slot0(const FusedArgs &a, int bh, const SeqView &v) {
+    return a.cu_seqlens ? v.tz / C + bh / a.H : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cstddef>
 #include <cstdint>
 
 namespace gdr {
@@ -58,6 +59,23 @@ int fused_pair_max_clusters();
 bool fused_uses_pair(int BH);
 // Reads and clears the device error word of the pair kernel (synchronous).
 cudaError_t take_pair_error_word(unsigned *value);
+
+// ---- two-kernel prefill (bf16, dk = dv = 128, C = 64): the preparation of every
+// chunk in parallel (gdr_prep.cu) into a caller-owned workspace of [Lb | P] tiles,
+// then the state chain and outputs (gdr_chain.cu).  Same dense / packed layouts as
+// launch_fused_pair.
+size_t prep_workspace_bytes(int BH, int T, const int *cu_seqlens, int H, int total_T);
+cudaError_t launch_prep(const void *q, const void *k, const float *g, const float *beta, float a_min,
+                        void *ws, int BH, int T, const int *cu_seqlens, int H, int total_T,
+                        cudaStream_t s);
+cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         float a_min, const float *init, void *out, float *final_state, const void *ws,
+                         int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s);
+// CTAs per head of the chain kernel for BH heads on the current device (2 or 1).
+int chain_split(int BH);
+// Read and clear the device error words of the two kernels (synchronous).
+cudaError_t take_prep_error_word(unsigned *value);
+cudaError_t take_chain_error_word(unsigned *value);
 
 // Device error word shared by every kernel with a bounded wait.
 // Returns the word's value and clears it (synchronous on `s`).

@@ -1,0 +1,318 @@
+// gdr_prep.cu -- the state-independent preparation of every chunk of a
+// prefill, as one fully parallel kernel (the first half of the two-kernel
+// path; gdr_chain.cu is the second).
+//
+// Per chunk (sections 3.1-3.3 of "What a Trillion-Parameter MoE Model Reveals
+// About the Next Stage of LLM Scaling": with the lower-bounded decay, 1/gamma
+// stays finite and the causal tile is a dense product with diagonal scalings):
+//   [K;Q] K^T                                  (tcgen05, M = 128, N = 64, K = 128)
+//   A  = strict_lower(diag(beta gamma) K K^T diag(1/gamma)),  T = (I + A)^-1
+//   Lb = bf16(strict_lower(T) diag(beta)),  P = bf16(lower_incl(Q K^T) / gamma_C)
+// and the [Lb | P] tile (16 KB, the 128-byte-swizzled shared-memory image the
+// chain kernel loads verbatim) goes to the workspace.  Nothing here depends on
+// the state, so every (sequence, head, chunk) is an independent work item; a
+// persistent grid walks them with the next item's K and Q loading while the
+// current one is prepared.
+//
+// CTA: 256 threads.  Thread 0 issues the TMA loads, the tensor-core product
+// and the bulk store of each tile; warp 0 computes the decay; all eight warps
+// read the accumulator (TMEM lane quadrant warp % 4, column half warp / 4),
+// solve and convert.  Shared memory: 2 input buffers of 32 KB (K and Q in two
+// 64-column slabs; once the product is done, the first 16 KB of the buffer
+// receive the tile), the fp32 solve space, the chunk scalars.
+
+#include "gdr_fused_common.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int NT = 256;
+constexpr uint32_t IN_BYTES = 32768;                    // [slab i/64][K rows | Q rows][128 B]
+constexpr uint32_t OFF_IN = 0;                          // 2 input buffers
+constexpr uint32_t OFF_AS = OFF_IN + 2 * IN_BYTES;      // 64 x 68 fp32: A, then T in place
+constexpr uint32_t OFF_YS = OFF_AS + 64 * LDA * 4;      // 32 x 40 fp32 merge scratch
+constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;      // 5 x 64 fp32 chunk scalars
+constexpr uint32_t SMEM_USED = OFF_SC + 5 * 64 * 4;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // alignment slack
+static_assert(IN_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+static_assert(2 * SMEM_ALLOC <= 232448, "two CTAs per SM");
+constexpr uint32_t TM_COLS = 64;
+
+enum : int { B_FULL0 = 0, B_KQK = 2, B_DRAIN, NUM_BARS };
+
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t c8) {
+    return row * 128u + ((c8 ^ (row & 7u)) << 4);
+}
+
+// Work item -> (bh, n) of a chunk, false for a padding slot of the packed layout.
+__device__ bool item_chunk(const FusedArgs &a, int BH, int64_t nslot, int64_t item, int &bh, int &n,
+                           SeqView &v) {
+    const int z = (int)(item / nslot), u = (int)(item % nslot);
+    if (!a.cu_seqlens) {
+        bh = z;
+        n = u;
+        v = seq_view(a, bh);
+        return true;
+    }
+    // the last sequence s whose first slot t0(s) / C + s is at most u
+    const int S = BH / a.H;
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const int t0 = min(max(a.cu_seqlens[mid], 0), a.total_T);
+        if (t0 / C + mid <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    bh = lo * a.H + z;
+    v = seq_view(a, bh);
+    n = u - tile_slot0(a, bh, v);
+    return n >= 0 && n * C < v.T;
+}
+
+__global__ void __launch_bounds__(NT, 2)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const FusedArgs a, uint8_t *ws, int BH, int64_t nslot, int64_t items) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    __shared__ __align__(8) uint64_t s_bar[NUM_BARS];
+    __shared__ uint32_t s_tmem;
+    __shared__ float s_gC;
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
+    if (tid == 0) {
+        for (int i = 0; i < NUM_BARS; ++i) mbar_init(bar(i), 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&s_tmem), TM_COLS);
+        tmem_relinquish();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
+    float *As = reinterpret_cast<float *>(sm + OFF_AS);
+    float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
+    const Scal S = scal_at(reinterpret_cast<float *>(sm + OFF_SC));
+    const int qd = warp & 3, half = warp >> 2;   // TMEM lane quadrant, column half
+    const int lrow = qd * 32 + lane;             // TMEM lane = accumulator row
+    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+
+    // the CTA's valid items, in order
+    auto next_valid = [&](int64_t it, int &bh, int &n, SeqView &v) -> int64_t {
+        for (; it < items; it += gridDim.x)
+            if (item_chunk(a, BH, nslot, it, bh, n, v)) return it;
+        return items;
+    };
+    auto issue = [&](int b, int n, const SeqView &v) {   // thread 0
+        const uint32_t buf = sbase + OFF_IN + (uint32_t)b * IN_BYTES;
+        const uint32_t fb = bar(B_FULL0 + b);
+        mbar_arrive_expect_tx(fb, IN_BYTES);
+        tma_load_3d(buf + 0, &tm_k, fb, 0, v.tz + n * C, v.z);
+        tma_load_3d(buf + 8192, &tm_q, fb, 0, v.tz + n * C, v.z);
+        tma_load_3d(buf + 16384, &tm_k, fb, 64, v.tz + n * C, v.z);
+        tma_load_3d(buf + 24576, &tm_q, fb, 64, v.tz + n * C, v.z);
+    };
+
+    int bh, n;
+    SeqView v;
+    int64_t it = next_valid(blockIdx.x, bh, n, v);
+    uint32_t loads = 0, products = 0;   // thread 0: TMA loads issued, products issued
+    if (tid == 0 && it < items) {
+        issue(0, n, v);
+        ++loads;
+    }
+    for (int cnt = 0; it < items; ++cnt) {
+        const int b = cnt & 1;
+        uint8_t *buf = sm + OFF_IN + b * IN_BYTES;
+        int bh2, n2;
+        SeqView v2;
+        const int64_t nx = next_valid(it + gridDim.x, bh2, n2, v2);
+        bool ok = true;
+        if (tid == 0) {
+            if (nx < items) {   // the other buffer: its tile store has been read out
+                bulk_wait_read_all();
+                issue(b ^ 1, n2, v2);
+                ++loads;
+            }
+            ok = role_wait(bar(B_FULL0 + b), (uint32_t)(cnt >> 1) & 1u, a.limit_ns, &s_abort);
+            if (ok) {   // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
+                tc_fence_after();
+                const uint64_t dkq = sdesc_sw128(smem_u32(buf), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t d = sdesc_add(dkq, (kk >> 2) * 16384 + (kk & 3) * 32);
+                    mma_bf16(tmem, d, d, idesc_kqk, kk > 0);
+                }
+                mma_commit(bar(B_KQK));
+                ++products;
+            }
+        }
+        if (warp == 0) {   // the chunk's decay, while the product runs
+            float gv[2], bv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = n * C + 2 * lane + e;
+                gv[e] = (t < v.T) ? a.g[v.gbase + (int64_t)t * v.stride] : 0.f;
+                bv[e] = (t < v.T) ? a.beta[v.gbase + (int64_t)t * v.stride] : 0.f;
+            }
+            warp_decay(lane, gv, bv, min(C, v.T - n * C), a.a_min, S, &s_gC);
+        }
+        if (tid == 0 && ok) ok = role_wait(bar(B_KQK), (uint32_t)cnt & 1u, a.limit_ns, &s_abort);
+        if (!__syncthreads_and(ok)) break;
+        tc_fence_after();
+        const int c = min(C, v.T - n * C);
+        const float igC = 1.f / s_gC;
+        {   // A (rows 0-63) into the solve space, P (rows 64-127) into the tile's second half;
+            // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
+            float x[32];
+            tmem_ld32(tl + half * 32, x);
+            tmem_wait_ld();
+            if (lrow < 64) {
+                const int r = lrow;
+                const float br = (r < c) ? S.bg[r] : 0.f;
+#pragma unroll
+                for (int s4 = 0; s4 < 32; s4 += 4) {
+                    const int s0 = half * 32 + s4;
+                    const float4 ig4 = *reinterpret_cast<const float4 *>(&S.ig[s0]);
+                    float4 o;
+                    o.x = (s0 + 0 < r) ? br * x[s4 + 0] * ig4.x : 0.f;
+                    o.y = (s0 + 1 < r) ? br * x[s4 + 1] * ig4.y : 0.f;
+                    o.z = (s0 + 2 < r) ? br * x[s4 + 2] * ig4.z : 0.f;
+                    o.w = (s0 + 3 < r) ? br * x[s4 + 3] * ig4.w : 0.f;
+                    *reinterpret_cast<float4 *>(&As[r * LDA + s0]) = o;
+                }
+            } else {
+                const int r = lrow - 64;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float p8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = half * 32 + q4 * 8 + e;
+                        p8[e] = (s <= r && r < c) ? x[q4 * 8 + e] * igC : 0.f;
+                    }
+                    uint4 u;
+                    u.x = pack_bf16x2(p8[0], p8[1]);
+                    u.y = pack_bf16x2(p8[2], p8[3]);
+                    u.z = pack_bf16x2(p8[4], p8[5]);
+                    u.w = pack_bf16x2(p8[6], p8[7]);
+                    *reinterpret_cast<uint4 *>(buf + 8192 + swz((uint32_t)r, (uint32_t)(half * 4 + q4))) = u;
+                }
+            }
+        }
+        tc_fence_before();
+        named_sync(BAR_PREP, NPREP);
+        solve_unit_lower(tid, As, As, Ys);   // T = (I + A)^-1, in place
+        {   // Lb = strict_lower(T) diag(beta): thread -> row tid % 64, columns 16 (tid / 64) + 0..15
+            const int r = tid & 63, q4 = tid >> 6;
+            float x[16];
+#pragma unroll
+            for (int s4 = 0; s4 < 16; s4 += 4) {
+                const int s0 = q4 * 16 + s4;
+                const float4 t = *reinterpret_cast<const float4 *>(&As[r * LDA + s0]);
+                const float4 f = *reinterpret_cast<const float4 *>(&S.bs[s0]);
+                x[s4 + 0] = (s0 + 0 < r) ? t.x * f.x : 0.f;
+                x[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
+                x[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
+                x[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint4 u;
+                u.x = pack_bf16x2(x[h2 * 8 + 0], x[h2 * 8 + 1]);
+                u.y = pack_bf16x2(x[h2 * 8 + 2], x[h2 * 8 + 3]);
+                u.z = pack_bf16x2(x[h2 * 8 + 4], x[h2 * 8 + 5]);
+                u.w = pack_bf16x2(x[h2 * 8 + 6], x[h2 * 8 + 7]);
+                *reinterpret_cast<uint4 *>(buf + swz((uint32_t)r, (uint32_t)(q4 * 2 + h2))) = u;
+            }
+        }
+        fence_proxy_async_smem();   // the tile leaves by a bulk copy (async proxy)
+        __syncthreads();            // every thread is also done with the scalars and A
+        if (tid == 0) {
+            bulk_store(ws + ((int64_t)v.z * nslot + tile_slot0(a, bh, v) + n) * TILE_BYTES,
+                       smem_u32(buf), TILE_BYTES);
+            bulk_commit();
+        }
+        it = nx;
+        bh = bh2;
+        n = n2;
+        v = v2;
+    }
+    if (tid == 0) {
+        if (s_abort) {   // let this thread's loads and products land before leaving
+            for (uint32_t i = 0; i < loads; ++i) {
+                // the buffers alternate; only the latest load of each can be pending
+                if (i + 2 >= loads)
+                    mbar_wait(bar(B_FULL0 + (i & 1)), (i >> 1) & 1u, kCleanupLimitNs);
+            }
+            if (products > 0) {
+                mma_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0u, kCleanupLimitNs);
+            }
+        }
+        bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+}  // namespace
+
+// Bytes of workspace the two-kernel path needs: one tile per chunk slot.
+size_t prep_workspace_bytes(int BH, int T, const int *cu_seqlens, int H, int total_T) {
+    FusedArgs a{};
+    a.T = T;
+    a.cu_seqlens = cu_seqlens;
+    a.H = H;
+    a.total_T = total_T;
+    if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return 0;
+    const int64_t zs = cu_seqlens ? H : BH;
+    return (size_t)(zs * tile_slots(a, BH)) * TILE_BYTES;
+}
+
+cudaError_t launch_prep(const void *q, const void *k, const float *g, const float *beta, float a_min,
+                        void *ws, int BH, int T, const int *cu_seqlens, int H, int total_T,
+                        cudaStream_t s) {
+    if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(ws)) & 15)
+        return cudaErrorMisalignedAddress;
+    CUtensorMap mq, mk;
+    const bool ok = cu_seqlens ? (make_map_packed(&mq, q, H, total_T) && make_map_packed(&mk, k, H, total_T))
+                               : (make_map(&mq, q, BH, T) && make_map(&mk, k, BH, T));
+    if (!ok) return cudaErrorInvalidValue;
+    FusedArgs a{g, beta, nullptr, nullptr, nullptr, a_min, T, wait_limit_ns()};
+    a.cu_seqlens = cu_seqlens;
+    a.H = H;
+    a.total_T = total_T;
+    const int64_t nslot = tile_slots(a, BH);
+    const int64_t items = (cu_seqlens ? (int64_t)H : (int64_t)BH) * nslot;
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
+    chunk_prep_kernel<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(mq, mk, a, static_cast<uint8_t *>(ws), BH,
+                                                              nslot, items);
+    return cudaGetLastError();
+}
+
+cudaError_t take_prep_error_word(unsigned *value) { return take_error_word(value); }
+
+}  // namespace gdr

@@ -235,6 +235,55 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
                        gdr_dtype_t dtype);
 
 /*
+ * The two-kernel prefill: a caller-owned workspace lets the preparation of
+ * every chunk -- [K;Q]K^T, A, the triangular solve T = (I + A)^-1, Lb =
+ * strict_lower(T) diag(beta) and P = lower_incl(Q K^T) / gamma_C ("What a
+ * Trillion-Parameter MoE Model Reveals About the Next Stage of LLM Scaling",
+ * sections 3.1-3.3) -- run as one fully parallel kernel that writes a 16 KB
+ * bf16 tile per chunk, so that the second kernel, the sequential state chain
+ * with the outputs, does nothing else.  Same arithmetic and results as
+ * gdr_chunk_fwd (the tiles are the bf16 operands the fused kernels compute in
+ * shared memory).
+ *
+ * gdr_chunk_fwd_workspace_size: bytes of workspace the two-kernel path needs
+ *   for these arguments (B * H * ceil(T / 64) tiles of 16 KB), or 0 where it
+ *   does not apply (anything but bf16, dk = dv = 128, chunk = 64, or empty
+ *   work).  Host-only.
+ * gdr_chunk_fwd_ws: gdr_chunk_fwd with a workspace.  `workspace` is device
+ *   memory owned by the caller, 16-byte aligned, at least the size above, not
+ *   shared with a call still running on another stream; its contents on entry
+ *   and exit are scratch.  With a null workspace, one that is too small, or
+ *   arguments the two-kernel path does not take, the call is exactly
+ *   gdr_chunk_fwd (the single-launch fused or staged path).  Two launches,
+ *   asynchronous on `stream`; errors as gdr_chunk_fwd.
+ * gdr_chunk_fwd_varlen_workspace_size / gdr_chunk_fwd_varlen_ws: the same for
+ *   packed sequences; the workspace holds H * (total_T / 64 + S + 1) tiles
+ *   (sequence s starts at tile total offset cu_seqlens[s] / 64 + s of its head).
+ * gdr_chunk_fwd_ws_path: the path gdr_chunk_fwd_ws takes given a large enough
+ *   workspace: 4 two kernels with two CTAs per head in the chain kernel (value
+ *   columns split), 5 two kernels with one CTA per head, else the value of
+ *   gdr_chunk_fwd_path.  The split is two CTAs per head while every CTA has an
+ *   SM of its own; GDR_CHAIN_SPLIT=1|2 forces one.  Launches nothing.
+ */
+size_t gdr_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                    gdr_dtype_t dtype);
+gdr_status_t gdr_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, float a_min, const float *init_state, void *out,
+                              float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                              gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                              void *stream);
+size_t gdr_chunk_fwd_varlen_workspace_size(int S, int H, int total_T, int dk, int dv, int chunk,
+                                           gdr_dtype_t dtype);
+gdr_status_t gdr_chunk_fwd_varlen_ws(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, float a_min, const float *init_state,
+                                     void *out, float *final_state, const int *cu_seqlens, int S,
+                                     int H, int total_T, int dk, int dv, int chunk,
+                                     gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
+                          gdr_dtype_t dtype);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word:
  * GDR_ERR_TIMEOUT if a kernel's bounded wait gave up since the last call,
  * GDR_ERR_CUDA if the stream reports an error, else GDR_OK.

@@ -1,5 +1,5 @@
 """Failure detection without a GPU fault: GDR_FAULT_INJECT=timeout makes every
-bounded wait of the fused kernel give up at once.  The kernel must unwind (let
+bounded wait of the prefill kernels give up at once.  The kernel must unwind (let
 its own copies land, free TMEM, return), gdr_last_device_error must report
 GDR_ERR_TIMEOUT, and the context must stay usable for the next call."""
 from __future__ import annotations
@@ -16,9 +16,19 @@ from gated_delta_rule_gdr_gb300 import inputs as I
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("variant", ["single", "pair"])
+# (environment, workspace): the fused kernels on the single-launch path, the
+# preparation and chain kernels on the two-kernel path
+VARIANTS = {"single": ({"GDR_FUSED_VARIANT": "single"}, None),
+            "pair": ({"GDR_FUSED_VARIANT": "pair"}, None),
+            "chain2": ({"GDR_CHAIN_SPLIT": "2"}, "auto"),
+            "chain1": ({"GDR_CHAIN_SPLIT": "1"}, "auto")}
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
 def test_injected_timeout_is_reported_and_recovers(variant, monkeypatch):
-    monkeypatch.setenv("GDR_FUSED_VARIANT", variant)
+    env, ws = VARIANTS[variant]
+    for k, val in env.items():
+        monkeypatch.setenv(k, val)
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     gdr.load(build_if_missing=True)
@@ -27,13 +37,14 @@ def test_injected_timeout_is_reported_and_recovers(variant, monkeypatch):
     assert gdr.last_device_error() == 0
     os.environ["GDR_FAULT_INJECT"] = "timeout"
     try:
-        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"])
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                      workspace=ws)
         assert gdr.last_device_error() == 5          # GDR_ERR_TIMEOUT
     finally:
         del os.environ["GDR_FAULT_INJECT"]
     assert gdr.last_device_error() == 0              # the word was cleared
     out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
-                             x["init_state"])
+                             x["init_state"], workspace=ws)
     torch.cuda.synchronize()
     cpu = {n: t.cpu() for n, t in x.items()}
     ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,

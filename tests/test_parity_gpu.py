@@ -33,10 +33,10 @@ def rel(x, ref):
     return oracle.rel_l2(x, ref)
 
 
-def run_gpu(x, w, init=None, chunk=None):
+def run_gpu(x, w, init=None, chunk=None, workspace="auto"):
     out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
                              x["init_state"] if init is None else init,
-                             chunk=chunk or w.chunk)
+                             chunk=chunk or w.chunk, workspace=workspace)
     torch.cuda.synchronize()
     return out, fin
 
@@ -45,19 +45,31 @@ def to(x, device):
     return {k_: (None if t is None else t.to(device)) for k_, t in x.items()}
 
 
+# The kernels of the bf16, d = 128, chunk 64 prefill: the single-launch fused kernel
+# with one CTA per head ("single") or a two-CTA cluster per head ("pair"), and the
+# two-kernel path (preparation, then the chain kernel) with two CTAs per head
+# ("chain2") or one ("chain1").  Value: (environment, workspace argument).
+VARIANTS = {"single": ({"GDR_FUSED_VARIANT": "single"}, None),
+            "pair": ({"GDR_FUSED_VARIANT": "pair"}, None),
+            "chain2": ({"GDR_CHAIN_SPLIT": "2"}, "auto"),
+            "chain1": ({"GDR_CHAIN_SPLIT": "1"}, "auto")}
+
+
 @contextlib.contextmanager
-def fused_variant(name):
-    """Force the one-CTA-per-head ("single") or the value-split ("pair") fused
-    kernel; by default the launcher picks by the number of heads."""
-    old = os.environ.get("GDR_FUSED_VARIANT")
-    os.environ["GDR_FUSED_VARIANT"] = name
+def path_variant(name):
+    """Force one of VARIANTS (by default the launchers pick by the number of
+    heads); yields the workspace argument that selects its path."""
+    env, ws = VARIANTS[name]
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
     try:
-        yield
+        yield ws
     finally:
-        if old is None:
-            del os.environ["GDR_FUSED_VARIANT"]
-        else:
-            os.environ["GDR_FUSED_VARIANT"] = old
+        for k, val in old.items():
+            if val is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = val
 
 
 # ------------------------------------------------------------------ the correctness workload
@@ -124,23 +136,23 @@ def test_ragged_and_tiny(dtype, T, d):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("variant", ["single", "pair"])
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("B,H,T", [(1, 1, 1), (1, 2, 63), (2, 1, 64), (1, 3, 65), (2, 2, 200),
                                    (1, 2, 700)])
 def test_fused_variants(variant, B, H, T):
-    """Both fused kernels (bf16, dk = dv = 128, chunk 64) against the oracle:
-    ragged tails, one to three input-stage rounds, several heads."""
+    """Every kernel of the bf16, dk = dv = 128, chunk 64 prefill against the oracle:
+    ragged tails, one to several input-stage rounds, several heads."""
     w = I.PREFILL.with_(B=B, H=H, T=T)
     x = to(I.prefill_inputs(w), "cuda")
-    with fused_variant(variant):
-        out, fin = run_gpu(x, w)
+    with path_variant(variant) as ws:
+        out, fin = run_gpu(x, w, workspace=ws)
     ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min,
                         x["init_state"].cpu())
     assert rel(out, ro) <= TOL["bf16"], rel(out, ro)
     assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
 
 
-@pytest.mark.parametrize("variant", ["single", "pair"])
+@pytest.mark.parametrize("variant", list(VARIANTS))
 def test_varlen_packed_sequences(variant):
     """Packed variable-length sequences (empty, 1-token, ragged and multi-chunk ones in
     one launch) against the oracle run on each sequence on its own; the final states
@@ -148,9 +160,9 @@ def test_varlen_packed_sequences(variant):
     w = I.PREFILL.with_(H=2)
     lengths = [1, 63, 64, 0, 65, 200, 700, 130]
     x = I.varlen_inputs(w, lengths, device="cuda")
-    with fused_variant(variant):
+    with path_variant(variant) as ws:
         out, fin = gdr.chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
-                                        x["cu_seqlens"], x["init_state"])
+                                        x["cu_seqlens"], x["init_state"], workspace=ws)
     torch.cuda.synchronize()
     cu = x["cu_seqlens"].tolist()
     ref_out, ref_fin = [], []
@@ -250,12 +262,13 @@ def test_prefill_b4h16t4096():
     e_o, e_f = rel(out, ro), rel(fin, rf)
     print(f"prefill rel-L2 out {e_o:.3e} final {e_f:.3e}")
     assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
-    # the other fused kernel on the same inputs
-    with fused_variant("single"):
-        out1, fin1 = run_gpu(x, w)
-    e_o, e_f = rel(out1, ro), rel(fin1, rf)
-    print(f"prefill (one CTA per head) rel-L2 out {e_o:.3e} final {e_f:.3e}")
-    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
+    # every other kernel on the same inputs
+    for name in VARIANTS:
+        with path_variant(name) as ws:
+            out1, fin1 = run_gpu(x, w, workspace=ws)
+        e_o, e_f = rel(out1, ro), rel(fin1, rf)
+        print(f"prefill ({name}) rel-L2 out {e_o:.3e} final {e_f:.3e}")
+        assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
 
 
 @pytest.mark.slow
