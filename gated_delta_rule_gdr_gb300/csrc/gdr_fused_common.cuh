@@ -111,11 +111,10 @@ __device__ __forceinline__ bool role_wait_cluster(uint32_t bar, uint32_t parity,
 // every product.  log alpha = log1p(-(1 - a_min) / (1 + e^g)) keeps alpha
 // close to 1 accurate; the exponentials and reciprocals use the hardware
 // approximations (relative error below 1e-5 over the range the range rule
-// allows, far inside the bf16 tolerance of the fused path).  Not inlined: the
-// copy warp calls it at two places and its code would otherwise crowd the
-// instruction cache the other warps share.
-__device__ __noinline__ void warp_decay(int lane, const float (&gv)[2], const float (&bv)[2],
-                                        int c, float a_min, Scal s, float *s_gC) {
+// allows, far inside the bf16 tolerance of the fused path).
+__device__ __forceinline__ void warp_decay_inl(int lane, float g0, float g1, float be0, float be1, int c,
+                                               float a_min, Scal s, float *s_gC) {
+    const float gv[2] = {g0, g1}, bv[2] = {be0, be1};
     const int r0 = 2 * lane;
     const float om = 1.0f - a_min;
     const float l0 = (r0 < c) ? log1pf(-__fdividef(om, 1.0f + __expf(gv[0]))) : 0.f;
@@ -145,6 +144,19 @@ __device__ __noinline__ void warp_decay(int lane, const float (&gv)[2], const fl
     }
     if (lane == 0) *s_gC = gC;
     __syncwarp();
+}
+// The same, not inlined, for the copy warps of the fused and chain kernels: they
+// call it at two places, and its code would otherwise crowd the instruction
+// cache the other warps share.  (A warp with many live registers inlines it
+// instead: a call would save and restore them.)  The values cross the call in
+// registers, so loads issued ahead of the call stay in flight until it.
+__device__ __noinline__ void warp_decay_v(int lane, float g0, float g1, float be0, float be1, int c,
+                                          float a_min, Scal s, float *s_gC) {
+    warp_decay_inl(lane, g0, g1, be0, be1, c, a_min, s, s_gC);
+}
+__device__ __forceinline__ void warp_decay(int lane, const float (&gv)[2], const float (&bv)[2],
+                                           int c, float a_min, Scal s, float *s_gC) {
+    warp_decay_v(lane, gv[0], gv[1], bv[0], bv[1], c, a_min, s, s_gC);
 }
 
 // tf32 warp-level MMA (m16n8k8) for the small merge products of the solve.

@@ -15,7 +15,9 @@
 // current one is prepared.
 //
 // CTA: 256 threads.  Thread 0 issues the TMA loads, the tensor-core product
-// and the bulk store of each tile; warp 0 computes the decay; all eight warps
+// and the bulk store of each tile; warp 7 computes the decay (away from the
+// warp that issues the product, whose later instructions wait behind it) and
+// loads the next item's g and beta; all eight warps
 // read the accumulator (TMEM lane quadrant warp % 4, column half warp / 4),
 // solve and convert.  Shared memory: 2 input buffers of 32 KB (K and Q in two
 // 64-column slabs; once the product is done, the first 16 KB of the buffer
@@ -45,9 +47,9 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t c8) {
 }
 
 // Work item -> (bh, n) of a chunk, false for a padding slot of the packed layout.
-__device__ bool item_chunk(const FusedArgs &a, int BH, int64_t nslot, int64_t item, int &bh, int &n,
+__device__ bool item_chunk(const FusedArgs &a, int BH, int nslot, int item, int &bh, int &n,
                            SeqView &v) {
-    const int z = (int)(item / nslot), u = (int)(item % nslot);
+    const int z = item / nslot, u = item - z * nslot;
     if (!a.cu_seqlens) {
         bh = z;
         n = u;
@@ -71,7 +73,7 @@ __device__ bool item_chunk(const FusedArgs &a, int BH, int64_t nslot, int64_t it
 
 __global__ void __launch_bounds__(NT, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const FusedArgs a, uint8_t *ws, int BH, int64_t nslot, int64_t items) {
+                  const FusedArgs a, uint8_t *ws, int BH, int nslot, int items) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
@@ -108,10 +110,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
 
     // the CTA's valid items, in order
-    auto next_valid = [&](int64_t it, int &bh, int &n, SeqView &v) -> int64_t {
-        for (; it < items; it += gridDim.x)
+    auto next_valid = [&](int it, int &bh, int &n, SeqView &v) -> int {
+        for (; it < items; it += (int)gridDim.x)
             if (item_chunk(a, BH, nslot, it, bh, n, v)) return it;
         return items;
+    };
+    // g, beta of a chunk, two rows per lane of warp 7 (loaded an item ahead of their use)
+    auto load_gb = [&](int n, const SeqView &v, float (&gv)[2], float (&bv)[2]) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = n * C + 2 * lane + e;
+            gv[e] = (t < v.T) ? a.g[v.gbase + (int64_t)t * v.stride] : 0.f;
+            bv[e] = (t < v.T) ? a.beta[v.gbase + (int64_t)t * v.stride] : 0.f;
+        }
     };
     auto issue = [&](int b, int n, const SeqView &v) {   // thread 0
         const uint32_t buf = sbase + OFF_IN + (uint32_t)b * IN_BYTES;
@@ -125,25 +136,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     int bh, n;
     SeqView v;
-    int64_t it = next_valid(blockIdx.x, bh, n, v);
+    int it = next_valid((int)blockIdx.x, bh, n, v);
     uint32_t loads = 0, products = 0;   // thread 0: TMA loads issued, products issued
+    float gv[2] = {0.f, 0.f}, bv[2] = {0.f, 0.f};
     if (tid == 0 && it < items) {
         issue(0, n, v);
         ++loads;
     }
+    if (warp == 7 && it < items) load_gb(n, v, gv, bv);
     for (int cnt = 0; it < items; ++cnt) {
         const int b = cnt & 1;
         uint8_t *buf = sm + OFF_IN + b * IN_BYTES;
-        int bh2, n2;
-        SeqView v2;
-        const int64_t nx = next_valid(it + gridDim.x, bh2, n2, v2);
         bool ok = true;
         if (tid == 0) {
-            if (nx < items) {   // the other buffer: its tile store has been read out
-                bulk_wait_read_all();
-                issue(b ^ 1, n2, v2);
-                ++loads;
-            }
             ok = role_wait(bar(B_FULL0 + b), (uint32_t)(cnt >> 1) & 1u, a.limit_ns, &s_abort);
             if (ok) {   // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
                 tc_fence_after();
@@ -157,18 +162,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ++products;
             }
         }
-        if (warp == 0) {   // the chunk's decay, while the product runs
-            float gv[2], bv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = n * C + 2 * lane + e;
-                gv[e] = (t < v.T) ? a.g[v.gbase + (int64_t)t * v.stride] : 0.f;
-                bv[e] = (t < v.T) ? a.beta[v.gbase + (int64_t)t * v.stride] : 0.f;
-            }
-            warp_decay(lane, gv, bv, min(C, v.T - n * C), a.a_min, S, &s_gC);
+        int bh2, n2;   // the next item, looked up while the product runs
+        SeqView v2;
+        const int nx = next_valid(it + (int)gridDim.x, bh2, n2, v2);
+        if (warp == 7) {   // the chunk's decay, while the product runs; then the next g, beta
+            warp_decay_inl(lane, gv[0], gv[1], bv[0], bv[1], min(C, v.T - n * C), a.a_min, S, &s_gC);
+            if (nx < items) load_gb(n2, v2, gv, bv);
         }
         if (tid == 0 && ok) ok = role_wait(bar(B_KQK), (uint32_t)cnt & 1u, a.limit_ns, &s_abort);
         if (!__syncthreads_and(ok)) break;
+        if (tid == 0 && nx < items) {   // the next item's K, Q into the other buffer, once
+            bulk_wait_read_all();       // that buffer's tile store has read it out
+            issue(b ^ 1, n2, v2);
+            ++loads;
+        }
         tc_fence_after();
         const int c = min(C, v.T - n * C);
         const float igC = 1.f / s_gC;
@@ -301,6 +308,7 @@ cudaError_t launch_prep(const void *q, const void *k, const float *g, const floa
     a.total_T = total_T;
     const int64_t nslot = tile_slots(a, BH);
     const int64_t items = (cu_seqlens ? (int64_t)H : (int64_t)BH) * nslot;
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;   // work items are counted in 32 bits
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -309,7 +317,7 @@ cudaError_t launch_prep(const void *q, const void *k, const float *g, const floa
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
     chunk_prep_kernel<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(mq, mk, a, static_cast<uint8_t *>(ws), BH,
-                                                              nslot, items);
+                                                              (int)nslot, (int)items);
     return cudaGetLastError();
 }
 
