@@ -181,6 +181,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // pattern of a non-transposed [m][k] load
         const uint32_t bt_r = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
         const uint32_t bt_c = (uint32_t)(lane >> 4);
+        // stmatrix lane roles: matrices (rows 0-7 | 8-15) x (columns 0-7 | 8-15), in the
+        // accumulator register order (row g, row g + 8) of one 8-column tile, then the next
+        const uint32_t st_r = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
+        const uint32_t st_c = (uint32_t)(lane >> 4);
         float s[16][4];   // S_J: rows jw + g (+ 8), columns i = 8 q + 2 t4 (+ 1)
         {
             const float *src = a.init ? a.init + (int64_t)bh * D * D + j0 + jw : nullptr;
@@ -206,14 +210,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         };
         // MS_m = bf16(S_J) into buffer m % MSB, rows j (K-major operand of the output product)
         auto publish_ms = [&](int m) {
-            uint8_t *ms = sm + Cfg::OFF_MS + (m % Cfg::MSB) * 2 * Cfg::MS_SLAB;
+            const uint32_t ms = sbase + Cfg::OFF_MS + (uint32_t)(m % Cfg::MSB) * 2 * Cfg::MS_SLAB;
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const uint32_t off = (uint32_t)(q >> 3) * Cfg::MS_SLAB + 4u * t4;
-                *reinterpret_cast<uint32_t *>(ms + off + swz((uint32_t)(jw + g), (uint32_t)(q & 7))) =
-                    pack_bf16x2(s[q][0], s[q][1]);
-                *reinterpret_cast<uint32_t *>(ms + off + swz((uint32_t)(jw + g + 8), (uint32_t)(q & 7))) =
-                    pack_bf16x2(s[q][2], s[q][3]);
+            for (int qp = 0; qp < 8; ++qp) {   // columns i = 16 qp .. 16 qp + 15
+                const int q = 2 * qp;
+                stsm_x4(ms + (uint32_t)(q >> 3) * Cfg::MS_SLAB + swz((uint32_t)jw + st_r, (uint32_t)(q & 7) + st_c),
+                        pack_bf16x2(s[q][0], s[q][1]), pack_bf16x2(s[q][2], s[q][3]),
+                        pack_bf16x2(s[q + 1][0], s[q + 1][1]), pack_bf16x2(s[q + 1][2], s[q + 1][3]));
             }
             fence_proxy_async_smem();   // read by the output's tensor-core product
             __syncwarp();
@@ -226,15 +229,14 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         };
         // the start of chunk n: its stage, and (n > 0) the buffers it overwrites
-        auto chunk_wait = [&](int n) -> bool {
+        auto chunk_wait = [&](int n) -> bool {   // lanes 0 and 1 test one barrier each
             bool ok = true;
-            if (lane == 0) {
+            if (lane == 0)
                 ok = role_wait(bar(B_FULL0 + n % NST), (uint32_t)(n / NST) & 1u, a.limit_ns, &s_abort);
-                if (ok && n > 0)
-                    ok = role_wait(bar(B_SAFE0 + (n & 1)), (uint32_t)((n - 1) >> 1) & 1u, a.limit_ns,
-                                   &s_abort);
-            }
-            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            else if (lane == 1 && n > 0)
+                ok = role_wait(bar(B_SAFE0 + (n & 1)), (uint32_t)((n - 1) >> 1) & 1u, a.limit_ns,
+                               &s_abort);
+            return __all_sync(0xffffffffu, ok);
         };
         if (NC == 0 && a.final_state) store_state();   // an empty sequence: final = initial
         if (NC > 0) publish_ms(0);
@@ -293,6 +295,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     uint32_t vf[4];
                     ldsm_x4_t(vf, vt + swz((uint32_t)(16 * sp) + (uint32_t)(lane & 7) + (uint32_t)((lane >> 4) * 8),
                                            vc + (uint32_t)((lane >> 3) & 1)));
+                    uint32_t eb[4];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int p = 2 * sp + h, sc0 = 8 * p + 2 * t4;
@@ -302,15 +305,15 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         const float2 vhi = bf16x2_to_float2(vf[2 * h + 1]);
                         const float e0 = fmaf(-ga.x, x[p][0], vlo.x), e1 = fmaf(-ga.y, x[p][1], vlo.y);
                         const float e2 = fmaf(-ga.x, x[p][2], vhi.x), e3 = fmaf(-ga.y, x[p][3], vhi.y);
-                        *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g), (uint32_t)p) + 4 * t4) =
-                            pack_bf16x2(e0, e1);
-                        *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g + 8), (uint32_t)p) + 4 * t4) =
-                            pack_bf16x2(e2, e3);
+                        eb[2 * h] = pack_bf16x2(e0, e1);
+                        eb[2 * h + 1] = pack_bf16x2(e2, e3);
                         x[p][0] = be.x * e0;
                         x[p][1] = be.y * e1;
                         x[p][2] = be.x * e2;
                         x[p][3] = be.y * e3;
                     }
+                    stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * sp) + st_c), eb[0], eb[1],
+                            eb[2], eb[3]);
                 }
             }
             __syncwarp();
@@ -346,13 +349,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int p = 0; p < 8; ++p) {
                     const int r0 = 8 * p + 2 * t4;
                     const float2 sc = *reinterpret_cast<const float2 *>(&S.sc[r0]);
-                    const uint32_t lo = pack_bf16x2(sc.x * x[p][0], sc.y * x[p][1]);
-                    const uint32_t hi = pack_bf16x2(sc.x * x[p][2], sc.y * x[p][3]);
-                    ef[p >> 1][2 * (p & 1) + 0] = lo;
-                    ef[p >> 1][2 * (p & 1) + 1] = hi;
-                    *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g), (uint32_t)p) + 4 * t4) = lo;
-                    *reinterpret_cast<uint32_t *>(wt + swz((uint32_t)(jw + g + 8), (uint32_t)p) + 4 * t4) = hi;
+                    ef[p >> 1][2 * (p & 1) + 0] = pack_bf16x2(sc.x * x[p][0], sc.y * x[p][1]);
+                    ef[p >> 1][2 * (p & 1) + 1] = pack_bf16x2(sc.x * x[p][2], sc.y * x[p][3]);
                 }
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * ks) + st_c), ef[ks][0],
+                            ef[ks][1], ef[ks][2], ef[ks][3]);
                 fence_proxy_async_smem();   // read by the output's tensor-core product
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_WTREADY0 + wb));

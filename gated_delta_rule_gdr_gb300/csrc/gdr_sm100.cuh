@@ -252,6 +252,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
+// Four 8x8 b16 matrices to shared memory, the inverse of ldsm_x4: lanes 8q ..
+// 8q+7 give the row addresses of matrix q, and register q of every lane holds
+// its two elements of matrix q (row lane/4, columns 2 (lane%4), +1).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
 // d += a b, m16n8k16, bf16 operands, fp32 accumulators: a = the 16 x 16 A
 // fragment (rows g, g+8 and k pairs 2t, 2t+8 of lane 4g+t), b0/b1 = the 16 x 8
 // B fragment (k pairs 2t and 2t+8 of column g), d = rows g, g+8, columns 2t, 2t+1.
