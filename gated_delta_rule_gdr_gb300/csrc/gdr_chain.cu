@@ -68,15 +68,15 @@ template <int DVH> struct ChainCfg {
 enum : int {
     B_FULL0 = 0,          // stage landed (TMA, bulk copy) and its scalars written (x3, count 2)
     B_FREE0 = 3,          // chain warps + output warps done with a stage (x3, count NCH + 1)
-    B_MSREADY = 6,        // chain warps: MS_n published (count NCH)
-    B_WTREADY0 = 7,       // chain warps: Wt_n published in buffer n % 2 (x2, count NCH)
-    B_QMS = 9,            // issue commit: [K;Q] MS_n done (single MS buffer: may be overwritten)
-    B_SAFE0 = 10,         // issue commit after [K;Q] MS_{n-1}: the output products that read
-                          //   Wt[n % 2] (chunk n-2) and MS[n % 2] (chunk n-1) are done (x2)
-    B_OFULL0 = 12,        // issue commit: accumulator buffer b complete (x2)
-    B_OFREE0 = 14,        // output warps: accumulator buffer b read out (x2)
-    B_DRAIN = 16,         // commit of the error path
-    NUM_BARS = 17
+    B_MSREADY0 = 6,       // chain warps: MS_m and Wt_{m-1} published, phase of m on buffer m % 2
+                          //   (x2, count NCH)
+    B_QMS = 8,            // issue commit: [K;Q] MS_n done (single MS buffer: may be overwritten)
+    B_SAFE0 = 9,          // issue commit after [K;Q] MS_{n-1} and [Lb;P] Wt_{n-2}: chunk n may
+                          //   overwrite Wt[n % 2] and MS[(n + 1) % 2] (x2)
+    B_OFULL0 = 11,        // issue commit: accumulator buffer b complete (x2)
+    B_OFREE0 = 13,        // output warps: accumulator buffer b read out (x2)
+    B_DRAIN = 15,         // commit of the error path
+    NUM_BARS = 16
 };
 constexpr uint32_t BAR_OUT = 5;   // named barrier of the two output warps
 
@@ -148,7 +148,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             uint32_t count = 1;
             if (i >= B_FULL0 && i < B_FULL0 + 3) count = 2;
             if (i >= B_FREE0 && i < B_FREE0 + 3) count = NCH + 1;
-            if (i == B_MSREADY || i == B_WTREADY0 || i == B_WTREADY0 + 1) count = NCH;
+            if (i == B_MSREADY0 || i == B_MSREADY0 + 1) count = NCH;
             mbar_init(bar(i), count);
         }
         s_abort = 0;
@@ -208,19 +208,23 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 fin[(int64_t)(i + 1) * D + g + 8] = s[q][3];
             }
         };
-        // MS_m = bf16(S_J) into buffer m % MSB, rows j (K-major operand of the output product)
-        auto publish_ms = [&](int m) {
-            const uint32_t ms = sbase + Cfg::OFF_MS + (uint32_t)(m % Cfg::MSB) * 2 * Cfg::MS_SLAB;
+        // Publication m, for the output products: MS_m = bf16(S_J) into buffer m % MSB
+        // (rows j, K-major; m < NC) and the Wt_{m-1} tile stored earlier, behind one
+        // fence (the products read them through the async proxy)
+        auto publish = [&](int m) {
+            if (m < NC) {
+                const uint32_t ms = sbase + Cfg::OFF_MS + (uint32_t)(m % Cfg::MSB) * 2 * Cfg::MS_SLAB;
 #pragma unroll
-            for (int qp = 0; qp < 8; ++qp) {   // columns i = 16 qp .. 16 qp + 15
-                const int q = 2 * qp;
-                stsm_x4(ms + (uint32_t)(q >> 3) * Cfg::MS_SLAB + swz((uint32_t)jw + st_r, (uint32_t)(q & 7) + st_c),
-                        pack_bf16x2(s[q][0], s[q][1]), pack_bf16x2(s[q][2], s[q][3]),
-                        pack_bf16x2(s[q + 1][0], s[q + 1][1]), pack_bf16x2(s[q + 1][2], s[q + 1][3]));
+                for (int qp = 0; qp < 8; ++qp) {   // columns i = 16 qp .. 16 qp + 15
+                    const int q = 2 * qp;
+                    stsm_x4(ms + (uint32_t)(q >> 3) * Cfg::MS_SLAB + swz((uint32_t)jw + st_r, (uint32_t)(q & 7) + st_c),
+                            pack_bf16x2(s[q][0], s[q][1]), pack_bf16x2(s[q][2], s[q][3]),
+                            pack_bf16x2(s[q + 1][0], s[q + 1][1]), pack_bf16x2(s[q + 1][2], s[q + 1][3]));
+                }
             }
-            fence_proxy_async_smem();   // read by the output's tensor-core product
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_MSREADY));
+            if (lane == 0) mbar_arrive(bar(B_MSREADY0 + (m & 1)));
         };
         // one lane waits; the warp learns the result
         auto warp_wait = [&](int b, uint32_t parity) -> bool {
@@ -239,7 +243,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             return __all_sync(0xffffffffu, ok);
         };
         if (NC == 0 && a.final_state) store_state();   // an empty sequence: final = initial
-        if (NC > 0) publish_ms(0);
+        if (NC > 0) publish(0);
 
         for (int n = 0; n < NC; ++n) {
             const int wb = n & 1;
@@ -356,9 +360,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int ks = 0; ks < 4; ++ks)
                     stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * ks) + st_c), ef[ks][0],
                             ef[ks][1], ef[ks][2], ef[ks][3]);
-                fence_proxy_async_smem();   // read by the output's tensor-core product
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_WTREADY0 + wb));
             }
 
             // ---- S_J = gamma_C S_J + Wt^T K: B = K[r][i] rows (transposed)
@@ -391,55 +392,52 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_FREE0 + n % NST));   // this warp is done with stage n
-            if (n + 1 < NC) {
-                // a single MS buffer is free once the output's [K;Q] MS_n has completed
-                if (Cfg::MSB == 1 && !warp_wait(B_QMS, (uint32_t)n & 1u)) break;
-                publish_ms(n + 1);
-            } else if (a.final_state) {
-                store_state();
-            }
+            // a single MS buffer is free once the output's [K;Q] MS_n has completed
+            if (Cfg::MSB == 1 && n + 1 < NC && !warp_wait(B_QMS, (uint32_t)n & 1u)) break;
+            publish(n + 1);   // MS_{n+1} (if any) and Wt_n
+            if (n + 1 == NC && a.final_state) store_state();
         }
     } else if (warp == NCH + 1) {
         // ================================================================ output products
         if (lane == 0) {
             const uint32_t idesc_o = idesc_bf16(128, DVH, false, false);   // K-major A and B
             bool issued = false;
-            for (int n = 0; n < NC; ++n) {
-                const uint32_t st_a = stage(n);
-                const uint32_t acc = tmem + (uint32_t)(n & 1) * DVH;
-                // O(n) = [K;Q] MS_n (rows 64-127: Q M_n), once MS_n is out and the
-                // accumulator buffer has been read out (chunk n-2)
-                bool ok = role_wait(bar(B_MSREADY), (uint32_t)n & 1u, a.limit_ns, &s_abort);
-                if (ok) ok = role_wait(bar(B_FULL0 + n % NST), (uint32_t)(n / NST) & 1u, a.limit_ns, &s_abort);
-                if (ok && n > 1)
-                    ok = role_wait(bar(B_OFREE0 + (n & 1)), (uint32_t)((n - 2) >> 1) & 1u, a.limit_ns, &s_abort);
-                if (!ok) break;
-                tc_fence_after();
-                {
-                    const uint64_t da = sdesc_sw128(st_a + Cfg::ST_K, 16, 1024);
-                    const uint64_t db = sdesc_sw128(sbase + Cfg::OFF_MS + (uint32_t)(n % Cfg::MSB) * 2 * Cfg::MS_SLAB,
-                                                    16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(acc, sdesc_add(da, (kk >> 2) * 16384 + (kk & 3) * 32),
-                                 sdesc_add(db, (kk >> 2) * Cfg::MS_SLAB + (kk & 3) * 32), idesc_o, kk > 0);
-                }
-                mma_commit(bar(B_QMS));
-                // chunk n+1 may overwrite Wt[(n+1) % 2] and MS[(n+1) % 2] once every
-                // product issued so far (up to this one) is done
-                if (n + 1 < NC) mma_commit(bar(B_SAFE0 + ((n + 1) & 1)));
-                issued = true;
-                // O(n) += [Lb;P] Wt_n (rows 64-127: P Wt_n)
-                if (!role_wait(bar(B_WTREADY0 + (n & 1)), (uint32_t)(n >> 1) & 1u, a.limit_ns, &s_abort)) break;
-                tc_fence_after();
-                {
-                    const uint64_t dl = sdesc_sw128(st_a + Cfg::ST_LP, 16, 1024);
+            // Iteration m: [Lb;P] Wt_{m-1} completes chunk m-1's accumulator, then
+            // O(m) = [K;Q] MS_m starts chunk m's (rows 64-127: Q M_m + P Wt_m / ...)
+            for (int m = 0; m <= NC && NC > 0; ++m) {
+                if (!role_wait(bar(B_MSREADY0 + (m & 1)), (uint32_t)(m >> 1) & 1u, a.limit_ns, &s_abort)) break;
+                if (m > 0) {
+                    const int n = m - 1;
+                    tc_fence_after();
+                    const uint64_t dl = sdesc_sw128(stage(n) + Cfg::ST_LP, 16, 1024);
                     const uint64_t dw = sdesc_sw128(sbase + Cfg::OFF_WT + (uint32_t)(n & 1) * Cfg::WT_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(acc, sdesc_add(dl, kk * 32), sdesc_add(dw, kk * 32), idesc_o, 1);
+                        mma_bf16(tmem + (uint32_t)(n & 1) * DVH, sdesc_add(dl, kk * 32), sdesc_add(dw, kk * 32),
+                                 idesc_o, 1);
+                    mma_commit(bar(B_OFULL0 + (n & 1)));
                 }
-                mma_commit(bar(B_OFULL0 + (n & 1)));
+                if (m == NC) break;
+                // O(m) = [K;Q] MS_m, once the accumulator buffer has been read out (chunk m-2)
+                bool ok = role_wait(bar(B_FULL0 + m % NST), (uint32_t)(m / NST) & 1u, a.limit_ns, &s_abort);
+                if (ok && m > 1)
+                    ok = role_wait(bar(B_OFREE0 + (m & 1)), (uint32_t)((m - 2) >> 1) & 1u, a.limit_ns, &s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    const uint64_t da = sdesc_sw128(stage(m) + Cfg::ST_K, 16, 1024);
+                    const uint64_t db = sdesc_sw128(sbase + Cfg::OFF_MS + (uint32_t)(m % Cfg::MSB) * 2 * Cfg::MS_SLAB,
+                                                    16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tmem + (uint32_t)(m & 1) * DVH, sdesc_add(da, (kk >> 2) * 16384 + (kk & 3) * 32),
+                                 sdesc_add(db, (kk >> 2) * Cfg::MS_SLAB + (kk & 3) * 32), idesc_o, kk > 0);
+                }
+                mma_commit(bar(B_QMS));
+                // chunk m+1 may overwrite Wt[(m+1) % 2] (read by Wt_{m-1}'s product) and
+                // MS[m % 2] once both products issued so far are done
+                if (m + 1 < NC) mma_commit(bar(B_SAFE0 + ((m + 1) & 1)));
+                issued = true;
             }
             if (s_abort && issued) {   // let this thread's MMAs land before TMEM goes away
                 mma_commit(bar(B_DRAIN));
