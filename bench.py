@@ -184,14 +184,18 @@ def time_steps(fn, K, W, flush, stream):
     return [s.elapsed_time(e) for s, e in times]
 
 
-def bench_prefill(gdr, w, K, W, dev, flush, stream):
+def bench_prefill(gdr, w, K, W, dev, flush, stream, workspace="auto"):
     x = I.prefill_inputs(w, device=dev)
     out = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype(), device=dev)
     fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
 
+    # the workspace of the two-kernel path, held across steps like the inputs
+    nws = gdr.chunk_fwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.torch_dtype())
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if (workspace and nws) else None
+
     def step(_):
         gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
-                      chunk=w.chunk, out=out, final_state=fin)
+                      chunk=w.chunk, out=out, final_state=fin, workspace=ws)
 
     ms = time_steps(step, K, W, flush, stream)
 
@@ -208,7 +212,7 @@ def bench_prefill(gdr, w, K, W, dev, flush, stream):
             if t is not None:
                 dx[n].copy_(t, non_blocking=True)
         gdr.chunk_fwd(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], w.a_min,
-                      dx["init_state"], chunk=w.chunk, out=out, final_state=fin)
+                      dx["init_state"], chunk=w.chunk, out=out, final_state=fin, workspace=ws)
         hout.copy_(out, non_blocking=True)
         hfin.copy_(fin, non_blocking=True)
 
@@ -216,7 +220,7 @@ def bench_prefill(gdr, w, K, W, dev, flush, stream):
     return ms, ms_e2e, h2d, d2h
 
 
-def bench_varlen(gdr, w, K, W, dev, flush, stream):
+def bench_varlen(gdr, w, K, W, dev, flush, stream, workspace="auto"):
     lengths = I.varlen_lengths(w)
     x = I.varlen_inputs(w, lengths, device=dev)
     del x["seqs"]
@@ -224,10 +228,13 @@ def bench_varlen(gdr, w, K, W, dev, flush, stream):
     out = torch.empty((total_T, w.H, w.dv), dtype=w.torch_dtype(), device=dev)
     fin = torch.empty((S, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
 
+    nws = gdr.chunk_fwd_varlen_workspace_size(S, w.H, total_T, w.dk, w.dv, w.chunk, w.torch_dtype())
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if (workspace and nws) else None
+
     def step(_):
         gdr.chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
                              x["cu_seqlens"], x["init_state"], chunk=w.chunk, out=out,
-                             final_state=fin)
+                             final_state=fin, workspace=ws)
 
     ms = time_steps(step, K, W, flush, stream)
 
@@ -245,7 +252,7 @@ def bench_varlen(gdr, w, K, W, dev, flush, stream):
                 dx[n].copy_(t, non_blocking=True)
         gdr.chunk_fwd_varlen(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], w.a_min,
                              dx["cu_seqlens"], dx["init_state"], chunk=w.chunk, out=out,
-                             final_state=fin)
+                             final_state=fin, workspace=ws)
         hout.copy_(out, non_blocking=True)
         hfin.copy_(fin, non_blocking=True)
 
@@ -387,10 +394,10 @@ def run_ours(args):
         t_wall0 = time.perf_counter()
         if varlen:
             ms, ms_e2e, h2d, d2h = bench_varlen(gdr, main_w, args.steps, args.warmup, dev, flush,
-                                                stream)
+                                                stream, workspace=not args.single_launch)
         elif main_w.steps == 0:
             ms, ms_e2e, h2d, d2h = bench_prefill(gdr, main_w, args.steps, args.warmup, dev, flush,
-                                                 stream)
+                                                 stream, workspace=not args.single_launch)
         else:
             ms, ms_e2e, h2d, d2h = bench_decode(gdr, main_w, args.steps, args.warmup, dev, flush,
                                                 stream)
@@ -415,7 +422,8 @@ def run_ours(args):
         nk = gdr.chunk_fwd_kernels(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
                                    main_w.chunk, main_w.a_min, main_w.torch_dtype())
         path = gdr.chunk_fwd_path(main_w.B, main_w.H, main_w.T, main_w.dk, main_w.dv,
-                                  main_w.chunk, main_w.a_min, main_w.torch_dtype())
+                                  main_w.chunk, main_w.a_min, main_w.torch_dtype(),
+                                  workspace=not args.single_launch)
         assert not varlen or path in (2, 3, 4, 5), "the packed call runs the fused or two-kernel path"
         csrc = "gated_delta_rule_gdr_gb300/csrc/"
         common = [csrc + "gdr_fused_common.cuh", csrc + "gdr_sm100.cuh"]
@@ -586,6 +594,8 @@ def main():
                     default="prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--single-launch", action="store_true",
+                    help="the one-launch fused path (no workspace) instead of prep + chain")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
