@@ -207,7 +207,9 @@ __device__ __forceinline__ void frag_store(float *M, int ld, int r0, int n0, con
 // MMAs.  On return the lower triangle of Ts holds T; the 16 x 16 blocks right
 // of the even diagonal blocks hold zeros (the merges read them).  T feeds
 // bf16 tensor-core operands, so the tf32 merges cost no accuracy that matters.
-__device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *Ts, float *Ys) {
+template <int NTH>   // 256 or 128 threads (a multiple of 4 warps)
+__device__ __forceinline__ void solve_unit_lower_t(int w, const float *As, float *Ts, float *Ys) {
+    static_assert(NTH == 256 || NTH == 128, "the solve runs on 4 or 8 warps");
     const int lane = w & 31, wp = w >> 5;
     if (w < 64) {
         const int b = w >> 4, l = w & 15, o = 16 * b;
@@ -230,7 +232,7 @@ __device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *
             if ((b & 1) == 0) Ts[(o + r) * LDA + o + 16 + l] = 0.f;
         }
     }
-    named_sync(BAR_PREP, NPREP);
+    named_sync(BAR_PREP, NTH);
     {   // level 1: T(1,0) and T(3,2); warps 0-3 -> (pair, 8-column tile)
         const int p = (wp >> 1) & 1, nt = wp & 1;
         const int R = 16 * (2 * p + 1), Cb = 16 * (2 * p);
@@ -245,7 +247,7 @@ __device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *
             }
             frag_store(Ys + p * 16 * LDY, LDY, 0, 8 * nt, d, 1.f, lane);
         }
-        named_sync(BAR_PREP, NPREP);
+        named_sync(BAR_PREP, NTH);
         if (wp < 4) {
             float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -258,31 +260,41 @@ __device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *
             frag_store(Ts, LDA, R, Cb + 8 * nt, e, -1.f, lane);
         }
     }
-    named_sync(BAR_PREP, NPREP);
+    named_sync(BAR_PREP, NTH);
     {   // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
-        // warp -> (16-row tile, 8-column tile)
-        const int m0 = 16 * (wp & 1), n0 = 8 * (wp >> 1);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        // task -> (16-row tile, 8-column tile), 8 tasks over the warps
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t fb[2], fa[4];
-            frag_b(fb, Ts, LDA, 8 * ks, n0, lane);
-            frag_a(fa, As, LDA, 32 + m0, 8 * ks, lane);
-            mma_tf32(d, fa, fb);
-        }
-        frag_store(Ys, LDY, m0, n0, d, 1.f, lane);
-        named_sync(BAR_PREP, NPREP);
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int task = wp; task < 8; task += NTH / 32) {
+            const int m0 = 16 * (task & 1), n0 = 8 * (task >> 1);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t fb[2], fa[4];
-            frag_b(fb, Ys, LDY, 8 * ks, n0, lane);
-            frag_a(fa, Ts, LDA, 32 + m0, 32 + 8 * ks, lane);
-            mma_tf32(e, fa, fb);
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t fb[2], fa[4];
+                frag_b(fb, Ts, LDA, 8 * ks, n0, lane);
+                frag_a(fa, As, LDA, 32 + m0, 8 * ks, lane);
+                mma_tf32(d, fa, fb);
+            }
+            frag_store(Ys, LDY, m0, n0, d, 1.f, lane);
         }
-        frag_store(Ts, LDA, 32 + m0, n0, e, -1.f, lane);
+        named_sync(BAR_PREP, NTH);
+#pragma unroll
+        for (int task = wp; task < 8; task += NTH / 32) {
+            const int m0 = 16 * (task & 1), n0 = 8 * (task >> 1);
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t fb[2], fa[4];
+                frag_b(fb, Ys, LDY, 8 * ks, n0, lane);
+                frag_a(fa, Ts, LDA, 32 + m0, 32 + 8 * ks, lane);
+                mma_tf32(e, fa, fb);
+            }
+            frag_store(Ts, LDA, 32 + m0, n0, e, -1.f, lane);
+        }
     }
-    named_sync(BAR_PREP, NPREP);
+    named_sync(BAR_PREP, NTH);
+}
+__device__ __forceinline__ void solve_unit_lower(int w, const float *As, float *Ts, float *Ys) {
+    solve_unit_lower_t<NPREP>(w, As, Ts, Ys);
 }
 
 struct FusedArgs {

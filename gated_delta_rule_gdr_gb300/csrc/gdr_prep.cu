@@ -11,36 +11,40 @@
 // and the [Lb | P] tile (16 KB, the 128-byte-swizzled shared-memory image the
 // chain kernel loads verbatim) goes to the workspace.  Nothing here depends on
 // the state, so every (sequence, head, chunk) is an independent work item; a
-// persistent grid walks them with the next item's K and Q loading while the
-// current one is prepared.
+// persistent grid walks them, each CTA loading its next item's K and Q while it
+// prepares the current one.
 //
-// CTA: 256 threads.  Thread 0 issues the TMA loads, the tensor-core product
-// and the bulk store of each tile; warp 7 computes the decay (away from the
-// warp that issues the product, whose later instructions wait behind it) and
-// loads the next item's g and beta; all eight warps
-// read the accumulator (TMEM lane quadrant warp % 4, column half warp / 4),
-// solve and convert.  Shared memory: 2 input buffers of 32 KB (K and Q in two
-// 64-column slabs; once the product is done, the first 16 KB of the buffer
-// receive the tile), the fp32 solve space, the chunk scalars.
+// CTA: 128 threads, three per SM.  Thread 0 issues the TMA loads, the
+// tensor-core product and the bulk store of each tile; warp 3 computes the
+// decay (away from the warp that issues the product, whose later instructions
+// wait behind it) and loads the next item's g and beta; the four warps read the
+// accumulator (TMEM lane quadrant = warp), solve and convert.  Shared memory:
+// the input buffer (K and Q in two 64-column slabs; the next item's load goes
+// in as soon as the product has consumed them), the tile buffer, the fp32
+// solve space, the chunk scalars.
 
 #include "gdr_fused_common.cuh"
 
 namespace gdr {
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 128;
+constexpr int CTAS_PER_SM = 3;
 constexpr uint32_t IN_BYTES = 32768;                    // [slab i/64][K rows | Q rows][128 B]
-constexpr uint32_t OFF_IN = 0;                          // 2 input buffers
-constexpr uint32_t OFF_AS = OFF_IN + 2 * IN_BYTES;      // 64 x 68 fp32: A, then T in place
+constexpr uint32_t OFF_IN = 0;
+constexpr uint32_t OFF_OUT = OFF_IN + IN_BYTES;         // the [Lb | P] tile (16 KB)
+constexpr uint32_t LP_TILE_P = 8192;                    // P within the tile
+constexpr uint32_t OFF_AS = OFF_OUT + TILE_BYTES;       // 64 x 68 fp32: A, then T in place
 constexpr uint32_t OFF_YS = OFF_AS + 64 * LDA * 4;      // 32 x 40 fp32 merge scratch
 constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;      // 5 x 64 fp32 chunk scalars
 constexpr uint32_t SMEM_USED = OFF_SC + 5 * 64 * 4;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // alignment slack
-static_assert(IN_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
-static_assert(2 * SMEM_ALLOC <= 232448, "two CTAs per SM");
+static_assert(IN_BYTES % 1024 == 0 && OFF_OUT % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+static_assert(CTAS_PER_SM * SMEM_ALLOC <= 232448, "CTAs per SM");
 constexpr uint32_t TM_COLS = 64;
 
-enum : int { B_FULL0 = 0, B_KQK = 2, B_DRAIN, NUM_BARS };
+enum : int { B_FULL = 0, B_KQK = 1, B_DRAIN = 2, NUM_BARS = 3 };
+
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t c8) {
     return row * 128u + ((c8 ^ (row & 7u)) << 4);
@@ -71,7 +75,7 @@ __device__ bool item_chunk(const FusedArgs &a, int BH, int nslot, int item, int 
     return n >= 0 && n * C < v.T;
 }
 
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(NT, CTAS_PER_SM)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const FusedArgs a, uint8_t *ws, int BH, int nslot, int items) {
     extern __shared__ uint8_t smem_raw[];
@@ -104,10 +108,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
     float *As = reinterpret_cast<float *>(sm + OFF_AS);
     float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
+    uint8_t *tile = sm + OFF_OUT;
     const Scal S = scal_at(reinterpret_cast<float *>(sm + OFF_SC));
-    const int qd = warp & 3, half = warp >> 2;   // TMEM lane quadrant, column half
-    const int lrow = qd * 32 + lane;             // TMEM lane = accumulator row
-    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+    const int lrow = warp * 32 + lane;           // TMEM lane (quadrant = warp) = accumulator row
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 
     // the CTA's valid items, in order
     auto next_valid = [&](int it, int &bh, int &n, SeqView &v) -> int {
@@ -115,7 +119,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (item_chunk(a, BH, nslot, it, bh, n, v)) return it;
         return items;
     };
-    // g, beta of a chunk, two rows per lane of warp 7 (loaded an item ahead of their use)
+    // g, beta of a chunk, two rows per lane of warp 3 (loaded an item ahead of their use)
     auto load_gb = [&](int n, const SeqView &v, float (&gv)[2], float (&bv)[2]) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -124,14 +128,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bv[e] = (t < v.T) ? a.beta[v.gbase + (int64_t)t * v.stride] : 0.f;
         }
     };
-    auto issue = [&](int b, int n, const SeqView &v) {   // thread 0
-        const uint32_t buf = sbase + OFF_IN + (uint32_t)b * IN_BYTES;
-        const uint32_t fb = bar(B_FULL0 + b);
-        mbar_arrive_expect_tx(fb, IN_BYTES);
-        tma_load_3d(buf + 0, &tm_k, fb, 0, v.tz + n * C, v.z);
-        tma_load_3d(buf + 8192, &tm_q, fb, 0, v.tz + n * C, v.z);
-        tma_load_3d(buf + 16384, &tm_k, fb, 64, v.tz + n * C, v.z);
-        tma_load_3d(buf + 24576, &tm_q, fb, 64, v.tz + n * C, v.z);
+    auto issue = [&](int n, const SeqView &v) {   // thread 0
+        const uint32_t buf = sbase + OFF_IN;
+        mbar_arrive_expect_tx(bar(B_FULL), IN_BYTES);
+        tma_load_3d(buf + 0, &tm_k, bar(B_FULL), 0, v.tz + n * C, v.z);
+        tma_load_3d(buf + 8192, &tm_q, bar(B_FULL), 0, v.tz + n * C, v.z);
+        tma_load_3d(buf + 16384, &tm_k, bar(B_FULL), 64, v.tz + n * C, v.z);
+        tma_load_3d(buf + 24576, &tm_q, bar(B_FULL), 64, v.tz + n * C, v.z);
     };
 
     int bh, n;
@@ -140,19 +143,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint32_t loads = 0, products = 0;   // thread 0: TMA loads issued, products issued
     float gv[2] = {0.f, 0.f}, bv[2] = {0.f, 0.f};
     if (tid == 0 && it < items) {
-        issue(0, n, v);
+        issue(n, v);
         ++loads;
     }
-    if (warp == 7 && it < items) load_gb(n, v, gv, bv);
+    if (warp == 3 && it < items) load_gb(n, v, gv, bv);
     for (int cnt = 0; it < items; ++cnt) {
-        const int b = cnt & 1;
-        uint8_t *buf = sm + OFF_IN + b * IN_BYTES;
         bool ok = true;
         if (tid == 0) {
-            ok = role_wait(bar(B_FULL0 + b), (uint32_t)(cnt >> 1) & 1u, a.limit_ns, &s_abort);
+            ok = role_wait(bar(B_FULL), (uint32_t)cnt & 1u, a.limit_ns, &s_abort);
             if (ok) {   // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
                 tc_fence_after();
-                const uint64_t dkq = sdesc_sw128(smem_u32(buf), 16, 1024);
+                const uint64_t dkq = sdesc_sw128(sbase + OFF_IN, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t d = sdesc_add(dkq, (kk >> 2) * 16384 + (kk & 3) * 32);
@@ -165,22 +166,27 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         int bh2, n2;   // the next item, looked up while the product runs
         SeqView v2;
         const int nx = next_valid(it + (int)gridDim.x, bh2, n2, v2);
-        if (warp == 7) {   // the chunk's decay, while the product runs; then the next g, beta
+        if (warp == 3) {   // the chunk's decay (away from the warp that issued the product),
+                           // then the next item's g, beta
             warp_decay_inl(lane, gv[0], gv[1], bv[0], bv[1], min(C, v.T - n * C), a.a_min, S, &s_gC);
             if (nx < items) load_gb(n2, v2, gv, bv);
         }
-        if (tid == 0 && ok) ok = role_wait(bar(B_KQK), (uint32_t)cnt & 1u, a.limit_ns, &s_abort);
+        if (tid == 0 && ok) {
+            ok = role_wait(bar(B_KQK), (uint32_t)cnt & 1u, a.limit_ns, &s_abort);
+            bulk_wait_read_all();   // the previous tile's store has read the tile buffer
+        }
         if (!__syncthreads_and(ok)) break;
-        if (tid == 0 && nx < items) {   // the next item's K, Q into the other buffer, once
-            bulk_wait_read_all();       // that buffer's tile store has read it out
-            issue(b ^ 1, n2, v2);
+        if (tid == 0 && nx < items) {   // K and Q are consumed: the next item's load goes in
+            issue(n2, v2);
             ++loads;
         }
         tc_fence_after();
         const int c = min(C, v.T - n * C);
         const float igC = 1.f / s_gC;
-        {   // A (rows 0-63) into the solve space, P (rows 64-127) into the tile's second half;
-            // this thread: accumulator row lrow, columns 32 half .. 32 half + 31
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            // A (rows 0-63) into the solve space, P (rows 64-127) into the tile's second
+            // half; this thread: accumulator row lrow, columns 32 half .. 32 half + 31
             float x[32];
             tmem_ld32(tl + half * 32, x);
             tmem_wait_ld();
@@ -213,15 +219,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     u.y = pack_bf16x2(p8[2], p8[3]);
                     u.z = pack_bf16x2(p8[4], p8[5]);
                     u.w = pack_bf16x2(p8[6], p8[7]);
-                    *reinterpret_cast<uint4 *>(buf + 8192 + swz((uint32_t)r, (uint32_t)(half * 4 + q4))) = u;
+                    *reinterpret_cast<uint4 *>(tile + LP_TILE_P + swz((uint32_t)r, (uint32_t)(half * 4 + q4))) = u;
                 }
             }
         }
         tc_fence_before();
-        named_sync(BAR_PREP, NPREP);
-        solve_unit_lower(tid, As, As, Ys);   // T = (I + A)^-1, in place
-        {   // Lb = strict_lower(T) diag(beta): thread -> row tid % 64, columns 16 (tid / 64) + 0..15
-            const int r = tid & 63, q4 = tid >> 6;
+        named_sync(BAR_PREP, NT);
+        solve_unit_lower_t<NT>(tid, As, As, Ys);   // T = (I + A)^-1, in place
+#pragma unroll 1
+        for (int q4 = tid >> 6; q4 < 4; q4 += NT / 64) {
+            // Lb = strict_lower(T) diag(beta): row tid % 64, columns 16 q4 + 0..15
+            const int r = tid & 63;
             float x[16];
 #pragma unroll
             for (int s4 = 0; s4 < 16; s4 += 4) {
@@ -240,14 +248,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 u.y = pack_bf16x2(x[h2 * 8 + 2], x[h2 * 8 + 3]);
                 u.z = pack_bf16x2(x[h2 * 8 + 4], x[h2 * 8 + 5]);
                 u.w = pack_bf16x2(x[h2 * 8 + 6], x[h2 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(buf + swz((uint32_t)r, (uint32_t)(q4 * 2 + h2))) = u;
+                *reinterpret_cast<uint4 *>(tile + swz((uint32_t)r, (uint32_t)(q4 * 2 + h2))) = u;
             }
         }
         fence_proxy_async_smem();   // the tile leaves by a bulk copy (async proxy)
         __syncthreads();            // every thread is also done with the scalars and A
         if (tid == 0) {
             bulk_store(ws + ((int64_t)v.z * nslot + tile_slot0(a, bh, v) + n) * TILE_BYTES,
-                       smem_u32(buf), TILE_BYTES);
+                       smem_u32(tile), TILE_BYTES);
             bulk_commit();
         }
         it = nx;
@@ -256,12 +264,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         v = v2;
     }
     if (tid == 0) {
-        if (s_abort) {   // let this thread's loads and products land before leaving
-            for (uint32_t i = 0; i < loads; ++i) {
-                // the buffers alternate; only the latest load of each can be pending
-                if (i + 2 >= loads)
-                    mbar_wait(bar(B_FULL0 + (i & 1)), (i >> 1) & 1u, kCleanupLimitNs);
-            }
+        if (s_abort) {   // let this thread's load and products land before leaving
+            if (loads > 0) mbar_wait(bar(B_FULL), (loads - 1) & 1u, kCleanupLimitNs);
             if (products > 0) {
                 mma_commit(bar(B_DRAIN));
                 mbar_wait(bar(B_DRAIN), 0u, kCleanupLimitNs);
@@ -315,7 +319,7 @@ cudaError_t launch_prep(const void *q, const void *k, const float *g, const floa
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
+    const int64_t grid = std::min<int64_t>(items, (int64_t)sms * CTAS_PER_SM);
     chunk_prep_kernel<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(mq, mk, a, static_cast<uint8_t *>(ws), BH,
                                                               (int)nslot, (int)items);
     return cudaGetLastError();
