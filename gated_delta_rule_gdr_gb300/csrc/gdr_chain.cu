@@ -50,6 +50,9 @@ template <int DVH> struct ChainCfg {
     static constexpr uint32_t ST_LP = ST_V + DVH * 128;    // [Lb | P]
     static constexpr uint32_t ST_BYTES = ST_LP + TILE_BYTES;
     static constexpr int MSB = DVH == 64 ? 2 : 1;           // MS buffers (as shared memory allows)
+    // E^T stays in registers as the A operand of E^T Lb^T where registers allow (the
+    // 256-thread CTA); else it goes through the warp's rows of the Wt tile
+    static constexpr bool E_REGS = DVH == 64;
     static constexpr uint32_t OFF_MS = NST * ST_BYTES;     // MSB x 2 slabs of DVH x 128 B
     static constexpr uint32_t MS_SLAB = DVH * 128;
     static constexpr uint32_t OFF_WT = OFF_MS + MSB * 2 * MS_SLAB;
@@ -287,6 +290,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // tile of this chunk (buffer n % 2);  X^T <- E^T diag(beta) (fp32: the
             // identity part of T)
             uint8_t *wt = sm + Cfg::OFF_WT + wb * Cfg::WT_BYTES;
+            uint32_t ea[4][4];   // E^T A fragments, 16-column steps (E_REGS)
             {
                 // v[s][J] (TMA, 64-column slabs; zero-filled past the end of a dense tensor)
                 const uint32_t vt = st_a + Cfg::ST_V + (uint32_t)(jw >> 6) * 8192u;
@@ -316,8 +320,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         x[p][2] = be.x * e2;
                         x[p][3] = be.y * e3;
                     }
-                    stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * sp) + st_c), eb[0], eb[1],
-                            eb[2], eb[3]);
+                    if constexpr (Cfg::E_REGS) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) ea[sp][e] = eb[e];
+                    } else {
+                        stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * sp) + st_c), eb[0],
+                                eb[1], eb[2], eb[3]);
+                    }
                 }
             }
             __syncwarp();
@@ -326,7 +335,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             {
                 const uint32_t lb_a = st_a + Cfg::ST_LP;
                 auto load_l = [&](uint32_t (&af)[4], uint32_t (&bf)[4][4], int ks) {
-                    ldsm_x4(af, smem_u32(wt) + swz((uint32_t)jw + bt_r, (uint32_t)(2 * ks) + bt_c));
+                    if constexpr (!Cfg::E_REGS)
+                        ldsm_x4(af, smem_u32(wt) + swz((uint32_t)jw + bt_r, (uint32_t)(2 * ks) + bt_c));
 #pragma unroll
                     for (int rp = 0; rp < 4; ++rp)
                         ldsm_x4(bf[rp], lb_a + swz((uint32_t)(16 * rp) + bn_r, (uint32_t)(2 * ks) + bn_c));
@@ -336,10 +346,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {   // s = 16 ks .. 16 ks + 15
                     if (ks + 1 < 4) load_l(aq[(ks + 1) & 1], bq[(ks + 1) & 1], ks + 1);
+                    const uint32_t (&af)[4] = Cfg::E_REGS ? ea[ks] : aq[ks & 1];
 #pragma unroll
                     for (int rp = 0; rp < 4; ++rp) {   // r = 16 rp .. 16 rp + 15
-                        mma16816(x[2 * rp], aq[ks & 1], bq[ks & 1][rp][0], bq[ks & 1][rp][1]);
-                        mma16816(x[2 * rp + 1], aq[ks & 1], bq[ks & 1][rp][2], bq[ks & 1][rp][3]);
+                        mma16816(x[2 * rp], af, bq[ks & 1][rp][0], bq[ks & 1][rp][1]);
+                        mma16816(x[2 * rp + 1], af, bq[ks & 1][rp][2], bq[ks & 1][rp][3]);
                     }
                 }
             }
