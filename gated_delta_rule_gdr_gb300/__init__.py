@@ -28,6 +28,7 @@ __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk
            "chunk_fwd_workspace_size", "chunk_fwd_varlen_workspace_size", "last_device_error",
            "status_string", "version", "library_path", "STATUS", "PATHS"]
 
+DECAY = {"affine": 0, "log": 1}   # gdr_decay_t
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
           4: "GDR_ERR_CUDA", 5: "GDR_ERR_TIMEOUT"}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
@@ -66,6 +67,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_fwd_varlen_ws": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp,
                                     sz, vp],
         "gdr_chunk_fwd_ws_path": [i, i, i, i, i, i, f, i],
+        "gdr_chunk_fwd_ex": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp],
+        "gdr_decode_step_ex": [vp, vp, vp, vp, vp, i, f, vp, vp, i, i, i, i, i, vp],
         "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
         "gdr_chunk_decay": [vp, f, vp, i, i, i, vp],
@@ -150,9 +153,11 @@ def chunk_fwd_varlen_workspace_size(S, H, total_T, dk, dv, chunk=64, dtype=torch
 
 
 def chunk_fwd(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 64,
-              out=None, final_state=None, want_final: bool = True, workspace="auto"):
+              out=None, final_state=None, want_final: bool = True, workspace="auto",
+              decay: str = "affine"):
     """Chunked prefill.  q,k [B,H,T,dk], v [B,H,T,dv] (fp32 or bf16), g,beta [B,H,T]
-    fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
+    fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state).
+    decay "log": a_min is the log-domain floor g_min <= 0, log alpha = g_min sigmoid(g)."""
     lib = load()
     B, H, T, dk = q.shape
     dv = v.shape[-1]
@@ -164,7 +169,15 @@ def chunk_fwd(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 6
     if final_state is None and want_final:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     ws = _workspace(chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, q.dtype), workspace, q.device)
-    if ws is None:
+    if decay != "affine":
+        if decay not in DECAY:
+            raise ValueError(f"unknown decay {decay!r}")
+        _check(lib.gdr_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), DECAY[decay],
+                                    float(a_min), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                    B, H, T, dk, dv, int(chunk), DTYPE[q.dtype], _ptr(ws),
+                                    0 if ws is None else ws.numel(), _stream(q.device)),
+               "gdr_chunk_fwd_ex")
+    elif ws is None:
         _check(lib.gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
                                  _ptr(init_state), _ptr(out), _ptr(final_state), B, H, T, dk, dv,
                                  int(chunk), DTYPE[q.dtype], _stream(q.device)), "gdr_chunk_fwd")
@@ -212,7 +225,7 @@ def chunk_fwd_varlen(q, k, v, g, beta, a_min: float, cu_seqlens, init_state=None
     return out, final_state
 
 
-def decode_step(q, k, v, g, beta, a_min: float, state, *, out=None):
+def decode_step(q, k, v, g, beta, a_min: float, state, *, out=None, decay: str = "affine"):
     """One token for N sequences.  q,k [N,H,dk], v [N,H,dv], g,beta [N,H] fp32,
     state [N,H,dk,dv] fp32 updated in place.  Returns out [N,H,dv]."""
     lib = load()
@@ -223,6 +236,13 @@ def decode_step(q, k, v, g, beta, a_min: float, state, *, out=None):
     _f32(g, "g"), _f32(beta, "beta"), _f32(state, "state")
     if out is None:
         out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if decay != "affine":
+        if decay not in DECAY:
+            raise ValueError(f"unknown decay {decay!r}")
+        _check(lib.gdr_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), DECAY[decay],
+                                      float(a_min), _ptr(state), _ptr(out), N, H, dk, dv,
+                                      DTYPE[q.dtype], _stream(q.device)), "gdr_decode_step_ex")
+        return out
     _check(lib.gdr_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(a_min),
                                _ptr(state), _ptr(out), N, H, dk, dv, DTYPE[q.dtype],
                                _stream(q.device)), "gdr_decode_step")

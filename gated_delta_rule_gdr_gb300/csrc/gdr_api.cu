@@ -21,9 +21,12 @@ bool a_min_ok(float a_min) { return a_min > 0.0f && a_min <= 1.0f; }
 
 // The pages' range argument allows a worst in-tile cumulative log-decay of
 // -80 (e^-80 ~ 1.8e-35 stays a normal fp32 number, its reciprocal ~5.5e34
-// stays finite).  With alpha >= a_min the worst is chunk * ln(a_min).
-bool range_ok(float a_min, int chunk) {
-    return (double)chunk * -std::log((double)a_min) <= 80.0;
+// stays finite).  With alpha >= a_min the worst is chunk * ln(a_min); with
+// log alpha >= g_min it is chunk * g_min.  The kernels take one decay parameter
+// d: d = a_min > 0 for the linear-domain form, d = g_min <= 0 for the log form.
+bool range_ok(float d, int chunk) {
+    const double worst = d > 0.0f ? std::log((double)d) : (double)d;
+    return (double)chunk * -worst <= 80.0;
 }
 
 gdr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
@@ -43,13 +46,23 @@ gdr_status_t check_staged(int BH, int T, int dk, int dv, int chunk) {
 
 extern "C" {
 
-gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
-                           const float *beta, float a_min, const float *init_state, void *out,
-                           float *final_state, int B, int H, int T, int dk, int dv, int chunk,
-                           gdr_dtype_t dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// The decay parameter of the kernels for an ABI decay mode and bound, or false.
+bool decay_param(gdr_decay_t decay, float bound, float *d) {
+    if (decay == GDR_DECAY_AFFINE && a_min_ok(bound)) { *d = bound; return true; }
+    if (decay == GDR_DECAY_LOG && bound <= 0.0f && bound >= -1e30f) { *d = bound; return true; }
+    return false;   // unknown mode, a bound out of its range, or NaN
+}
+
+gdr_status_t chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float a_min, const float *init_state, void *out,
+                            float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                            gdr_dtype_t dtype, void *stream) {
     if (B < 0 || H < 0 || T < 0) return GDR_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
-    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
     if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
     const int64_t BH = (int64_t)B * H;
@@ -96,18 +109,51 @@ gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v, const fl
     return from_cuda(err);
 }
 
-gdr_status_t gdr_decode_step(const void *q, const void *k, const void *v, const float *g,
-                             const float *beta, float a_min, float *state, void *out, int N,
-                             int H, int dk, int dv, gdr_dtype_t dtype, void *stream) {
+gdr_status_t decode_impl(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, float a_min, float *state, void *out, int N, int H,
+                         int dk, int dv, gdr_dtype_t dtype, void *stream) {
     if (N < 0 || H < 0) return GDR_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
-    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return GDR_ERR_UNSUPPORTED;
     if ((int64_t)N * H == 0) return GDR_OK;
     if (!q || !k || !v || !g || !beta || !state || !out) return GDR_ERR_INVALID_ARG;
     if ((int64_t)N * H > 0x7fffffff) return GDR_ERR_UNSUPPORTED;
     return from_cuda(gdr::launch_decode(q, k, v, g, beta, a_min, state, out, N, H, dk, dv,
                                         elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float a_min, const float *init_state, void *out,
+                           float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                           gdr_dtype_t dtype, void *stream) {
+    if (B < 0 || H < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk, dv,
+                          chunk, dtype, stream);
+}
+
+gdr_status_t gdr_decode_step(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, float a_min, float *state, void *out, int N,
+                             int H, int dk, int dv, gdr_dtype_t dtype, void *stream) {
+    if (N < 0 || H < 0) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    return decode_impl(q, k, v, g, beta, a_min, state, out, N, H, dk, dv, dtype, stream);
+}
+
+gdr_status_t gdr_decode_step_ex(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, gdr_decay_t decay, float bound, float *state,
+                                void *out,
+                                int N, int H, int dk, int dv, gdr_dtype_t dtype, void *stream) {
+    float d = 0.0f;
+    if (N < 0 || H < 0) return GDR_ERR_INVALID_ARG;
+    if (!decay_param(decay, bound, &d)) return GDR_ERR_INVALID_ARG;
+    return decode_impl(q, k, v, g, beta, d, state, out, N, H, dk, dv, dtype, stream);
 }
 
 gdr_status_t gdr_chunk_decay(const float *g, float a_min, float *gamma, int BH, int T,
@@ -209,16 +255,19 @@ size_t gdr_chunk_fwd_varlen_workspace_size(int S, int H, int total_T, int dk, in
     return gdr::prep_workspace_bytes((int)SH, 0, &marker, H, total_T);
 }
 
-gdr_status_t gdr_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *g,
-                              const float *beta, float a_min, const float *init_state, void *out,
-                              float *final_state, int B, int H, int T, int dk, int dv, int chunk,
-                              gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
-                              void *stream) {
+}  // extern "C"
+
+namespace {
+
+gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, float a_min, const float *init_state, void *out,
+                               float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                               gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                               void *stream) {
     const size_t need = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype);
     if (need == 0 || workspace == nullptr || workspace_bytes < need)
-        return gdr_chunk_fwd(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk,
-                             dv, chunk, dtype, stream);
-    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+        return chunk_fwd_impl(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk,
+                              dv, chunk, dtype, stream);
     if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
     if ((int64_t)T * B * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
@@ -229,6 +278,32 @@ gdr_status_t gdr_chunk_fwd_ws(const void *q, const void *k, const void *v, const
         e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace, BH,
                               T, nullptr, 0, 0, s);
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status_t gdr_chunk_fwd_ws(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, float a_min, const float *init_state, void *out,
+                              float *final_state, int B, int H, int T, int dk, int dv, int chunk,
+                              gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    return chunk_fwd_ws_impl(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk,
+                             dv, chunk, dtype, workspace, workspace_bytes, stream);
+}
+
+gdr_status_t gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, gdr_decay_t decay, float bound,
+                              const float *init_state,
+                              void *out, float *final_state, int B, int H, int T, int dk, int dv,
+                              int chunk, gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    float d = 0.0f;
+    if (!decay_param(decay, bound, &d)) return GDR_ERR_INVALID_ARG;
+    return chunk_fwd_ws_impl(q, k, v, g, beta, d, init_state, out, final_state, B, H, T, dk, dv,
+                             chunk, dtype, workspace, workspace_bytes, stream);
 }
 
 gdr_status_t gdr_chunk_fwd_varlen_ws(const void *q, const void *k, const void *v, const float *g,

@@ -18,6 +18,7 @@
 // reductions, and written back with streaming stores.
 
 #include "gdr_internal.h"
+#include "gdr_math.cuh"
 
 #include <cuda_bf16.h>
 
@@ -35,9 +36,6 @@ __device__ __forceinline__ void st_elem(__nv_bfloat16 *p, int64_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
 }
 
-__device__ __forceinline__ float decay_alpha(float g, float a_min) {
-    return a_min + (1.0f - a_min) / (1.0f + expf(-g));
-}
 
 // dk = dv = 128: 256 threads; warp w owns state rows 16w..16w+15, lane l owns
 // columns 4l..4l+3 (one float4 per row), so every warp load is one fully

@@ -104,7 +104,8 @@ __device__ __forceinline__ bool role_wait_cluster(uint32_t bar, uint32_t parity,
 }
 
 // Cumulative decay of one chunk by one warp (lane l owns rows 2l, 2l+1, whose
-// g and beta it already holds): alpha = a_min + (1 - a_min) sigmoid(g), the
+// g and beta it already holds): alpha = a_min + (1 - a_min) sigmoid(g) (or, for
+// a_min <= 0, the log-domain form log alpha = a_min sigmoid(g)), the
 // inclusive scan of log alpha, gamma = exp(scan), 1/gamma, beta, beta gamma,
 // gamma_C (the last valid row) and gamma_C / gamma.  Rows past the chunk's end
 // get gamma = 1, beta = 0 and gamma_C / gamma = 0 so that they drop out of
@@ -116,9 +117,14 @@ __device__ __forceinline__ void warp_decay_inl(int lane, float g0, float g1, flo
                                                float a_min, Scal s, float *s_gC) {
     const float gv[2] = {g0, g1}, bv[2] = {be0, be1};
     const int r0 = 2 * lane;
+    // a_min > 0: the linear-domain floor; a_min <= 0: log alpha = a_min sigmoid(g)
     const float om = 1.0f - a_min;
-    const float l0 = (r0 < c) ? log1pf(-__fdividef(om, 1.0f + __expf(gv[0]))) : 0.f;
-    const float l1 = (r0 + 1 < c) ? log1pf(-__fdividef(om, 1.0f + __expf(gv[1]))) : 0.f;
+    auto la = [&](float gg) {
+        return a_min > 0.0f ? log1pf(-__fdividef(om, 1.0f + __expf(gg)))
+                            : a_min * __fdividef(1.0f, 1.0f + __expf(-gg));
+    };
+    const float l0 = (r0 < c) ? la(gv[0]) : 0.f;
+    const float l1 = (r0 + 1 < c) ? la(gv[1]) : 0.f;
     float incl = l0 + l1;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {

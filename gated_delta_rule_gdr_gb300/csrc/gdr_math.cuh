@@ -4,13 +4,19 @@
 
 namespace gdr {
 
-// log(alpha) for alpha = a_min + (1 - a_min) sigmoid(g), the lower-bounded
-// decay ("Trillion-Parameter MoE Multimodal LLMs: How to Evaluate the New
-// Generation", section 3.1, read in the linear domain with floor a_min).
-// Written through 1 - alpha = (1 - a_min) / (1 + e^g) so that alpha close to
-// 1 keeps its relative accuracy.
-__device__ __forceinline__ float log_alpha(float g, float a_min) {
-    return log1pf(-(1.0f - a_min) / (1.0f + expf(g)));
+// The decay parameter d of every kernel selects one of the two lower-bounded
+// decays ("Trillion-Parameter MoE Multimodal LLMs: How to Evaluate the New
+// Generation", section 3.1; "What a Trillion-Parameter MoE Model Reveals About
+// the Next Stage of LLM Scaling", section 3.2):
+//   d > 0:  alpha = d + (1 - d) sigmoid(g)      (linear domain, floor a_min = d)
+//   d <= 0: log alpha = d sigmoid(g)             (log domain, floor g_min = d)
+// log(alpha) of the linear form is written through 1 - alpha = (1 - d)/(1 + e^g)
+// so that alpha close to 1 keeps its relative accuracy.
+__device__ __forceinline__ float log_alpha(float g, float d) {
+    return d > 0.0f ? log1pf(-(1.0f - d) / (1.0f + expf(g))) : d / (1.0f + expf(-g));
+}
+__device__ __forceinline__ float decay_alpha(float g, float d) {
+    return d > 0.0f ? d + (1.0f - d) / (1.0f + expf(-g)) : expf(d / (1.0f + expf(-g)));
 }
 
 }  // namespace gdr

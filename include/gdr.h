@@ -284,6 +284,35 @@ int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float 
                           gdr_dtype_t dtype);
 
 /*
+ * The two lower-bounded decays ("Trillion-Parameter MoE Multimodal LLMs: How to
+ * Evaluate the New Generation", section 3.1; "What a Trillion-Parameter MoE Model
+ * Reveals About the Next Stage of LLM Scaling", section 3.2):
+ *   GDR_DECAY_AFFINE: alpha = a_min + (1 - a_min) sigmoid(g), bound = a_min in (0, 1]
+ *                     (the decay of every other entry point);
+ *   GDR_DECAY_LOG:    log alpha = g_min sigmoid(g), bound = g_min <= 0 (the pages'
+ *                     own form; g_min = -5 with 16-token chunks is their setting).
+ * The range rule applies to both: chunk * (-ln a_min) or chunk * (-g_min) must not
+ * exceed 80 (GDR_ERR_RANGE otherwise), so g_min = -5 takes chunk 16 (the staged
+ * kernels), and a bound with chunk 64 allowed (g_min >= -1.25) also takes the
+ * fused and two-kernel paths.
+ *
+ * gdr_chunk_fwd_ex: gdr_chunk_fwd_ws with the decay chosen by (decay, bound);
+ *   workspace may be NULL (the single-launch or staged path).
+ * gdr_decode_step_ex: gdr_decode_step with the decay chosen by (decay, bound).
+ * An unknown mode or a bound outside its range returns GDR_ERR_INVALID_ARG.
+ */
+typedef enum { GDR_DECAY_AFFINE = 0, GDR_DECAY_LOG = 1 } gdr_decay_t;
+gdr_status_t gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, gdr_decay_t decay, float bound,
+                              const float *init_state, void *out, float *final_state, int B,
+                              int H, int T, int dk, int dv, int chunk, gdr_dtype_t dtype,
+                              void *workspace, size_t workspace_bytes, void *stream);
+gdr_status_t gdr_decode_step_ex(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, gdr_decay_t decay, float bound, float *state,
+                                void *out, int N, int H, int dk, int dv, gdr_dtype_t dtype,
+                                void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word:
  * GDR_ERR_TIMEOUT if a kernel's bounded wait gave up since the last call,
  * GDR_ERR_CUDA if the stream reports an error, else GDR_OK.

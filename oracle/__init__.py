@@ -13,7 +13,8 @@ Contents
                   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
                   o_t = S_t q_t.
 * ``decode``   -- one step of the same recurrence, in place on the state.
-* ``alpha``    -- the lower-bounded decay itself.
+* ``alpha``    -- the lower-bounded decay itself: the linear-domain floor a_min, or
+                  (decay="log") the pages' log-domain form alpha = exp(g_min sigmoid(g)).
 * ``chunkwise`` (module) -- the chunked reformulation in numpy fp64, used to
                   check the token loop and to export per-stage intermediates.
 
@@ -58,15 +59,18 @@ def _load():
             f64p = ctypes.POINTER(ctypes.c_double)
             lib.gdr_oracle_alpha.restype = ctypes.c_double
             lib.gdr_oracle_alpha.argtypes = [ctypes.c_double, ctypes.c_double]
+            lib.gdr_oracle_alpha_log.restype = ctypes.c_double
+            lib.gdr_oracle_alpha_log.argtypes = [ctypes.c_double, ctypes.c_double]
             lib.gdr_oracle_fwd.restype = ctypes.c_int
             lib.gdr_oracle_fwd.argtypes = [f32p, f32p, f32p, f32p, f32p, ctypes.c_double,
                                            f32p, f64p, f64p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                                           ctypes.c_int]
+                                           ctypes.c_int, ctypes.c_int]
             lib.gdr_oracle_decode.restype = ctypes.c_int
             lib.gdr_oracle_decode.argtypes = [f32p, f32p, f32p, f32p, f32p, ctypes.c_double,
                                               f64p, f64p, ctypes.c_int, ctypes.c_int,
-                                              ctypes.c_int, ctypes.c_int, ctypes.c_int]
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -93,19 +97,27 @@ def _ptr(a: np.ndarray, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
-def alpha(g, a_min: float):
-    """alpha = a_min + (1 - a_min) * sigmoid(g), elementwise, fp64."""
+DECAY = {"affine": 0, "log": 1}
+
+
+def alpha(g, a_min: float, decay: str = "affine"):
+    """The lower-bounded decay, elementwise, fp64: decay "affine":
+    alpha = a_min + (1 - a_min) sigmoid(g); decay "log": alpha = exp(g_min sigmoid(g))
+    with g_min = the bound."""
     lib = _load()
     g = np.asarray(g, dtype=np.float64)
-    return np.vectorize(lambda x: lib.gdr_oracle_alpha(float(x), float(a_min)),
-                        otypes=[np.float64])(g)
+    fn = lib.gdr_oracle_alpha_log if decay == "log" else lib.gdr_oracle_alpha
+    if decay not in DECAY:
+        raise ValueError(f"unknown decay {decay!r}")
+    return np.vectorize(lambda x: fn(float(x), float(a_min)), otypes=[np.float64])(g)
 
 
 def fwd(q, k, v, g, beta, a_min: float, init_state=None, *, want_out: bool = True,
-        want_final: bool = True, nthreads: int | None = None):
+        want_final: bool = True, nthreads: int | None = None, decay: str = "affine"):
     """Token-by-token forward.  Shapes: q,k [B,H,T,dk], v [B,H,T,dv], g,beta [B,H,T],
     init_state [B,H,dk,dv] or None (zeros).  Returns (out [B,H,T,dv] fp64 or None,
-    final_state [B,H,dk,dv] fp64 or None).
+    final_state [B,H,dk,dv] fp64 or None).  decay "log": a_min is g_min and
+    alpha = exp(g_min sigmoid(g)).
     """
     q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
     B, H, T, dk = q.shape
@@ -128,13 +140,14 @@ def fwd(q, k, v, g, beta, a_min: float, init_state=None, *, want_out: bool = Tru
                             None if init is None else _ptr(init, f32),
                             None if out is None else _ptr(out, f64),
                             None if fin is None else _ptr(fin, f64),
-                            B, H, T, dk, dv, int(nthreads))
+                            B, H, T, dk, dv, int(nthreads), DECAY[decay])
     if rc != 0:
         raise RuntimeError(f"gdr_oracle_fwd failed with code {rc}")
     return out, fin
 
 
-def decode(q, k, v, g, beta, a_min: float, state: np.ndarray, *, nthreads: int | None = None):
+def decode(q, k, v, g, beta, a_min: float, state: np.ndarray, *, nthreads: int | None = None,
+           decay: str = "affine"):
     """One decode step in place on ``state`` ([N,H,dk,dv] float64).  q,k [N,H,dk],
     v [N,H,dv], g,beta [N,H].  Returns out [N,H,dv] fp64."""
     q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
@@ -149,7 +162,7 @@ def decode(q, k, v, g, beta, a_min: float, state: np.ndarray, *, nthreads: int |
     rc = lib.gdr_oracle_decode(_ptr(q, f32), _ptr(k, f32), _ptr(v, f32), _ptr(g, f32),
                                _ptr(beta, f32), float(a_min), _ptr(state, f64),
                                _ptr(out, f64), N, H, dk, dv,
-                               int(nthreads or os.cpu_count() or 1))
+                               int(nthreads or os.cpu_count() or 1), DECAY[decay])
     if rc != 0:
         raise RuntimeError(f"gdr_oracle_decode failed with code {rc}")
     return out

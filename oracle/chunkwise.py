@@ -48,11 +48,20 @@ def alpha(g, a_min):
     return a_min + (1.0 - a_min) / (1.0 + np.exp(-g))
 
 
-def chunk_decay(g, a_min, C):
+def log_alpha(g, bound, decay="affine"):
+    """log alpha per token: the log of the linear-domain form above, or the pages'
+    log-domain form log alpha = g_min sigmoid(g) (decay "log", bound = g_min)."""
+    g = np.asarray(g, np.float64)
+    if decay == "log":
+        return bound / (1.0 + np.exp(-g))
+    return np.log(alpha(g, bound))
+
+
+def chunk_decay(g, a_min, C, decay="affine"):
     """Chunk-local cumulative log-decay for one head: returns (b, gamma, inv_gamma)
     over all T rows, each restarting at every chunk boundary (row 0 of a chunk
     has b = log alpha of that row)."""
-    lam = np.log(alpha(g, a_min))
+    lam = log_alpha(g, a_min, decay)
     T = lam.shape[0]
     b = np.empty(T, np.float64)
     for n0 in range(0, T, C):
@@ -61,7 +70,7 @@ def chunk_decay(g, a_min, C):
     return b, gam, 1.0 / gam
 
 
-def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False):
+def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False, decay="affine"):
     """Chunked forward for one head.  q,k [T,dk], v [T,dv], g,beta [T], M0 [dk,dv]
     or None.  Returns (out [T,dv], M_final [dk,dv], intermediates or None).
 
@@ -74,7 +83,7 @@ def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False):
     T, dk = k.shape
     dv = v.shape[1]
     M = np.zeros((dk, dv)) if M0 is None else np.array(M0, np.float64)
-    _, gam_all, _ = chunk_decay(g, a_min, C)
+    _, gam_all, _ = chunk_decay(g, a_min, C, decay)
     out = np.empty((T, dv))
     inter = {n: [] for n in ("gamma", "A", "T", "U", "Wk", "W", "M")} if keep else None
     for n0 in range(0, T, C):
@@ -99,7 +108,7 @@ def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False):
     return out, M, inter
 
 
-def fwd(q, k, v, g, beta, a_min, init_state=None, C=64):
+def fwd(q, k, v, g, beta, a_min, init_state=None, C=64, decay="affine"):
     """Chunked forward over [B,H,T,...] arrays (fp64 results)."""
     q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
     B, H, T, dk = q.shape
@@ -110,5 +119,5 @@ def fwd(q, k, v, g, beta, a_min, init_state=None, C=64):
         for h in range(H):
             M0 = None if init_state is None else np.asarray(init_state[b, h], np.float64)
             out[b, h], fin[b, h], _ = head(q[b, h], k[b, h], v[b, h], g[b, h], beta[b, h],
-                                           a_min, M0, C)
+                                           a_min, M0, C, decay=decay)
     return out, fin

@@ -9,6 +9,7 @@
  * What it computes (per head, one token at a time, all arithmetic in fp64):
  *
  *   alpha_t = a_min + (1 - a_min) * sigmoid(g_t)
+ *           (or, in the log-domain mode, alpha_t = exp(g_min * sigmoid(g_t)))
  *   S_t     = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
  *   o_t     = S_t q_t
  *
@@ -47,12 +48,31 @@ double gdr_oracle_alpha(double g, double a_min)
 }
 
 /*
+ * The pages' own form of the bound, in the log domain: log alpha = g_min *
+ * sigmoid(g) with g_min < 0 ("Trillion-Parameter MoE Multimodal LLMs: How to
+ * Evaluate the New Generation", section 3.1, with g_min = -5; "What a
+ * Trillion-Parameter MoE Model Reveals About the Next Stage of LLM Scaling",
+ * section 3.2), so alpha = exp(g_min * sigmoid(g)) lies in (e^{g_min}, 1).
+ */
+double gdr_oracle_alpha_log(double g, double g_min)
+{
+    return exp(g_min / (1.0 + exp(-g)));
+}
+
+/* decay 0: the linear-domain bound (bound = a_min); decay 1: the log-domain bound
+ * (bound = g_min). */
+static double decay_alpha(int decay, double g, double bound)
+{
+    return decay == 1 ? gdr_oracle_alpha_log(g, bound) : gdr_oracle_alpha(g, bound);
+}
+
+/*
  * One head.  q, k: [T][dk]; v: [T][dv]; g, beta: [T]; init: [dk][dv] (M
  * layout) or NULL for a zero state; out: [T][dv] or NULL; final_state:
  * [dk][dv] (M layout) or NULL.  S is held as S[j][i], j < dv, i < dk.
  */
 static void oracle_head(const float *q, const float *k, const float *v,
-                        const float *g, const float *beta, double a_min,
+                        const float *g, const float *beta, int decay, double a_min,
                         const float *init, double *out, double *final_state,
                         int64_t T, int dk, int dv, double *S, double *u)
 {
@@ -64,7 +84,7 @@ static void oracle_head(const float *q, const float *k, const float *v,
         const float *kt = k + t * dk;
         const float *qt = q + t * dk;
         const float *vt = v + t * dv;
-        const double a = gdr_oracle_alpha((double)g[t], a_min);
+        const double a = decay_alpha(decay, (double)g[t], a_min);
         const double b = (double)beta[t];
 
         /* u = S k_t */
@@ -104,6 +124,7 @@ static void oracle_head(const float *q, const float *k, const float *v,
 
 typedef struct {
     const float *q, *k, *v, *g, *beta, *init;
+    int decay;
     double a_min;
     double *out, *final_state;
     int B, H, dk, dv;
@@ -129,7 +150,7 @@ static void *worker(void *arg)
         const int64_t T = jb->T;
         oracle_head(jb->q + bh * T * jb->dk, jb->k + bh * T * jb->dk,
                     jb->v + bh * T * jb->dv, jb->g + bh * T, jb->beta + bh * T,
-                    jb->a_min,
+                    jb->decay, jb->a_min,
                     jb->init ? jb->init + bh * jb->dk * jb->dv : NULL,
                     jb->out ? jb->out + bh * T * jb->dv : NULL,
                     jb->final_state ? jb->final_state + bh * jb->dk * jb->dv : NULL,
@@ -149,13 +170,13 @@ static void *worker(void *arg)
 int gdr_oracle_fwd(const float *q, const float *k, const float *v,
                    const float *g, const float *beta, double a_min,
                    const float *init_state, double *out, double *final_state,
-                   int B, int H, int64_t T, int dk, int dv, int nthreads)
+                   int B, int H, int64_t T, int dk, int dv, int nthreads, int decay)
 {
     if (!q || !k || !v || !g || !beta || B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
         return -1;
     if (nthreads < 1)
         nthreads = 1;
-    job_t jb = {q, k, v, g, beta, init_state, a_min, out, final_state,
+    job_t jb = {q, k, v, g, beta, init_state, decay, a_min, out, final_state,
                 B, H, dk, dv, T, 0};
     const int64_t nbh = (int64_t)B * H;
     if (nthreads > nbh)
@@ -213,6 +234,7 @@ static void oracle_decode_one(const float *qt, const float *kt, const float *vt,
 
 typedef struct {
     const float *q, *k, *v, *g, *beta;
+    int decay;
     double a_min;
     double *state, *out;
     int64_t NH;
@@ -230,7 +252,7 @@ static void *decode_worker(void *arg)
         const int64_t nh = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
         if (nh >= jb->NH)
             break;
-        const double a = gdr_oracle_alpha((double)jb->g[nh], jb->a_min);
+        const double a = decay_alpha(jb->decay, (double)jb->g[nh], jb->a_min);
         oracle_decode_one(jb->q + nh * jb->dk, jb->k + nh * jb->dk, jb->v + nh * jb->dv, a,
                           (double)jb->beta[nh], jb->state + nh * jb->dk * jb->dv,
                           jb->out + nh * jb->dv, jb->dk, jb->dv, S);
@@ -249,12 +271,12 @@ static void *decode_worker(void *arg)
 int gdr_oracle_decode(const float *q, const float *k, const float *v,
                       const float *g, const float *beta, double a_min,
                       double *state, double *out, int N, int H, int dk, int dv,
-                      int nthreads)
+                      int nthreads, int decay)
 {
     if (!q || !k || !v || !g || !beta || !state || !out || N < 0 || H < 0 ||
         dk <= 0 || dv <= 0)
         return -1;
-    decode_job_t jb = {q, k, v, g, beta, a_min, state, out, (int64_t)N * H, dk, dv, 0};
+    decode_job_t jb = {q, k, v, g, beta, decay, a_min, state, out, (int64_t)N * H, dk, dv, 0};
     if (nthreads < 1)
         nthreads = 1;
     if (nthreads > jb.NH)

@@ -141,3 +141,44 @@ def test_varlen_rejects(lib):
     assert f(*args(cu=None)) == 1              # offsets required
     assert f(*args(q=None)) == 1
     assert f(*args(S=0)) == 0                  # no sequences: nothing to do
+
+
+def ex(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, decay=1, bound=-5.0, init=None, out=P, fin=None, B=1,
+             H=1, T=64, dk=128, dv=128, chunk=16, dtype=1, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    f = lib.gdr_chunk_fwd_ex
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_float] + [ctypes.c_void_p] * 3 + \
+        [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return f(a["q"], a["k"], a["v"], a["g"], a["beta"], a["decay"], a["bound"], a["init"],
+             a["out"], a["fin"], a["B"], a["H"], a["T"], a["dk"], a["dv"], a["chunk"], a["dtype"],
+             a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(decay=2), 1), (dict(decay=-1), 1),                  # no such decay mode
+    (dict(bound=0.5), 1), (dict(bound=float("nan")), 1),      # log floor must be <= 0
+    (dict(decay=0, bound=0.0), 1), (dict(decay=0, bound=1.5), 1),
+    (dict(chunk=64), 3),                                       # 64 * 5 = 320 > 80
+    (dict(bound=-5.01), 3),                                    # 16 * 5.01 > 80
+    (dict(q=None), 1),                                         # in range: the pages' setting
+    (dict(chunk=64, bound=-1.25, q=None), 1),                  # 64 * 1.25 = 80: in range
+    (dict(chunk=64, bound=-1.26), 3),
+    (dict(decay=0, bound=0.95, chunk=64, q=None), 1),          # the linear form through _ex
+])
+def test_chunk_fwd_ex_rejects(lib, kw, code):
+    """The decay-mode entry point (the pages' log-domain form log alpha = g_min sigmoid(g)
+    and the linear-domain floor) validates the mode, the bound and the range rule."""
+    assert ex(lib, **kw) == code
+
+
+def test_decode_ex_rejects(lib):
+    d = lib.gdr_decode_step_ex
+    d.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_float] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    d.restype = ctypes.c_int
+    assert d(P, P, P, P, P, 1, 0.5, P, P, 1, 1, 128, 128, 1, None) == 1      # log floor > 0
+    assert d(P, P, P, P, P, 3, -5.0, P, P, 1, 1, 128, 128, 1, None) == 1     # unknown mode
+    assert d(P, P, P, P, P, 1, -5.0, P, P, 0, 4, 128, 128, 1, None) == 0     # empty
+    assert d(P, P, P, P, P, 1, -5.0, None, P, 1, 1, 128, 128, 1, None) == 1  # no state

@@ -19,6 +19,9 @@ plants such slips in a copy of the oracle's C source and proves it.
   bounded reciprocal the pages' method relies on ('Trillion-Parameter MoE
   Multimodal LLMs: How to Evaluate the New Generation', 3.1), and the range
   figures the pages print (tests/golden/range_facts.json).
+* the log-domain decay -- the pages' own log alpha = g_min sigmoid(g): limits and
+  symmetry, both limits of g reproduced by the linear-domain form, the chunked
+  algebra on 16-token chunks at g_min = -5, and its range bound.
 """
 from __future__ import annotations
 
@@ -205,10 +208,63 @@ def check_split_resume_and_decode():
     assert np.allclose(st, fin, rtol=1e-13, atol=1e-13)
 
 
+# ----------------------------------------------------------------- the log-domain decay
+# The pages' own form of the bound: log alpha = g_min sigmoid(g), g_min = -5 on 16-token
+# tiles ('Trillion-Parameter MoE Multimodal LLMs: How to Evaluate the New Generation',
+# 3.1; 'What a Trillion-Parameter MoE Model Reveals About the Next Stage of LLM Scaling',
+# 3.2).  Its pins: the limits and the symmetry of the sigmoid, the two limits of g
+# reproduced by the (separately pinned) linear-domain oracle, and the chunked algebra
+# on 16-token chunks at the pages' floor.
+
+def check_log_alpha_limits():
+    for g_min in (-5.0, -1.0, -0.25):
+        a = oracle.alpha(np.array([0.0, 40.0, -40.0, 1.0, -1.0]), g_min, "log")
+        assert abs(a[0] - math.exp(g_min / 2.0)) < 1e-15          # sigmoid(0) = 1/2
+        assert abs(a[1] - math.exp(g_min)) < 1e-15                # g -> +inf: the floor e^g_min
+        assert abs(a[2] - 1.0) < 1e-15                            # g -> -inf: no decay
+        assert a[4] > a[0] > a[3]                                  # decreasing in g
+        assert abs(math.log(a[3]) + math.log(a[4]) - g_min) < 1e-14   # s(x) + s(-x) = 1
+
+
+def check_log_decay_limits_match_linear_form():
+    # g -> +inf: alpha = e^g_min, which the linear form gives at its floor (g -> -inf,
+    # a_min = e^g_min); g -> -inf: alpha = 1, the linear form with a_min = 1
+    rng = np.random.default_rng(33)
+    q, k, v, _, beta, M0 = _rand_inputs(rng, 1, 2, 40, 8, 6)
+    up, down = np.full((1, 2, 40), 40.0, np.float32), np.full((1, 2, 40), -40.0, np.float32)
+    for g_min in (-5.0, -0.5):
+        o_log, f_log = oracle.fwd(q, k, v, up, beta, g_min, M0, decay="log")
+        o_lin, f_lin = oracle.fwd(q, k, v, down, beta, math.exp(g_min), M0)
+        assert np.max(np.abs(o_log - o_lin)) < 1e-12 and np.max(np.abs(f_log - f_lin)) < 1e-12
+    o_log, f_log = oracle.fwd(q, k, v, down, beta, -5.0, M0, decay="log")
+    o_lin, f_lin = oracle.fwd(q, k, v, up, beta, 1.0, M0)
+    assert np.max(np.abs(o_log - o_lin)) < 1e-12 and np.max(np.abs(f_log - f_lin)) < 1e-12
+    # and the decode step takes the same decay
+    st = M0.astype(np.float64).copy()
+    o = oracle.decode(q[:, :, 0], k[:, :, 0], v[:, :, 0], up[:, :, 0], beta[:, :, 0], -5.0,
+                      st, decay="log")
+    o1, f1 = oracle.fwd(q[:, :, :1], k[:, :, :1], v[:, :, :1], up[:, :, :1], beta[:, :, :1],
+                        -5.0, M0, decay="log")
+    assert np.max(np.abs(o - o1[:, :, 0])) < 1e-13 and np.max(np.abs(st - f1)) < 1e-13
+
+
+def check_log_chunkwise_agrees():
+    # 16-token chunks at the pages' floor g_min = -5: in-chunk decay down to e^-80
+    rng = np.random.default_rng(44)
+    for (T, C, g_min) in ((70, 16, -5.0), (64, 16, -2.0), (33, 64, -1.25)):
+        q, k, v, g, beta, M0 = _rand_inputs(rng, 1, 2, T, 16, 8)
+        out, fin = oracle.fwd(q, k, v, g, beta, g_min, M0, decay="log")
+        oc, fc = chunkwise.fwd(q, k, v, g, beta, g_min, M0, C=C, decay="log")
+        scale = max(1.0, float(np.max(np.abs(out))))
+        assert np.max(np.abs(out - oc)) < 1e-9 * scale, (T, C, np.max(np.abs(out - oc)))
+        assert np.max(np.abs(fin - fc)) < 1e-9 * scale, (T, C)
+
+
 ALL_CHECKS = [check_alpha_limits, check_hand_worked, check_unrolled_products,
               check_orthonormal_write_read, check_beta_zero_is_pure_decay,
               check_a_min_one_ignores_g, check_chunkwise_agrees,
-              check_split_resume_and_decode]
+              check_split_resume_and_decode, check_log_alpha_limits,
+              check_log_decay_limits_match_linear_form, check_log_chunkwise_agrees]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda f: f.__name__)
@@ -230,6 +286,18 @@ def test_pages_range_facts():
     worst = fx["tile_tokens"] * fx["log_decay_floor"]
     assert math.exp(worst) > np.finfo(np.float32).tiny
     assert math.exp(-worst) < np.finfo(np.float32).max
+
+
+@pytest.mark.parametrize("g_min,C", [(-5.0, 16), (-1.25, 64)])
+def test_log_chunk_decay_bounds(g_min, C):
+    # the pages' range argument: with log alpha >= g_min, a C-row chunk keeps gamma >=
+    # e^(C g_min) >= e^-80 and 1/gamma <= e^80, both normal fp32 numbers
+    g = np.concatenate([np.full(70, 60.0), np.random.default_rng(1).normal(0, 3, 300)])
+    b, gam, inv = chunkwise.chunk_decay(g, g_min, C, decay="log")
+    r = (np.arange(len(g)) % C) + 1
+    assert np.all(gam <= 1.0) and np.all(gam >= np.exp(g_min * r) * (1 - 1e-12))
+    assert np.all(inv <= math.exp(-g_min * C) * (1 + 1e-12)) and C * -g_min <= 80.0
+    assert np.all(np.isfinite(np.float32(inv))) and np.all(np.float32(gam) > 0)
 
 
 @pytest.mark.parametrize("a_min,C", [(0.9, 64), (0.95, 64), (0.98, 64), (0.99, 64), (0.3, 64)])
@@ -274,6 +342,14 @@ MUTANTS = [
      "return (1.0 - a_min) + a_min / (1.0 + exp(-g));"),
     ("decode: alpha dropped", "*s = a * (*s - b * uj * ki) + b * vj * ki;",
      "*s = (*s - b * uj * ki) + b * vj * ki;"),
+    ("log form: sign of the floor flipped", "return exp(g_min / (1.0 + exp(-g)));",
+     "return exp(-g_min / (1.0 + exp(-g)));"),
+    ("log form: sigmoid flipped", "return exp(g_min / (1.0 + exp(-g)));",
+     "return exp(g_min / (1.0 + exp(g)));"),
+    ("log form: exponential dropped", "return exp(g_min / (1.0 + exp(-g)));",
+     "return 1.0 + g_min / (1.0 + exp(-g));"),
+    ("log form ignored by the forward", "return decay == 1 ? gdr_oracle_alpha_log(g, bound)",
+     "return decay == 2 ? gdr_oracle_alpha_log(g, bound)"),
 ]
 
 
@@ -281,7 +357,7 @@ MUTANTS = [
 def _oracle_lib(path):
     lib = ctypes.CDLL(path)
     saved = oracle._load()
-    for name in ("gdr_oracle_alpha", "gdr_oracle_fwd", "gdr_oracle_decode"):
+    for name in ("gdr_oracle_alpha", "gdr_oracle_alpha_log", "gdr_oracle_fwd", "gdr_oracle_decode"):
         getattr(lib, name).restype = getattr(saved, name).restype
         getattr(lib, name).argtypes = getattr(saved, name).argtypes
     oracle._lib = lib

@@ -195,6 +195,55 @@ def test_varlen_packed_sequences(variant):
     assert gdr.last_device_error() == 0   # no bounded wait ran out (e.g. on the empty sequence)
 
 
+# ------------------------------------------------------------------ the log-domain decay
+# The pages' own bound, log alpha = g_min sigmoid(g) (g_min = -5 on 16-token chunks), on
+# the staged kernels; a floor that chunk 64 allows (g_min = -1.25) on the four kernels of
+# the bf16, d = 128 prefill; and the decode step.
+
+@pytest.mark.parametrize("dtype,d,T,C,g_min", [("f32", 64, 100, 16, -5.0), ("bf16", 128, 100, 16, -5.0),
+                                               ("f32", 128, 70, 32, -2.5), ("bf16", 64, 33, 64, -1.0)])
+def test_log_decay_staged(dtype, d, T, C, g_min):
+    w = I.CORRECTNESS.with_(B=1, H=2, T=T, dk=d, dv=d, chunk=C, dtype=dtype, init_std=0.02)
+    x = to(I.prefill_inputs(w), "cuda")
+    out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], g_min, x["init_state"],
+                             chunk=C, decay="log", workspace=None)
+    torch.cuda.synchronize()
+    ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), g_min,
+                        x["init_state"].cpu(), decay="log")
+    assert rel(out, ro) <= TOL[dtype], rel(out, ro)
+    assert rel(fin, rf) <= TOL[dtype], rel(fin, rf)
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+def test_log_decay_fused_paths(variant):
+    g_min = -1.25
+    w = I.PREFILL.with_(B=1, H=2, T=300)
+    x = to(I.prefill_inputs(w), "cuda")
+    with path_variant(variant) as ws:
+        out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], g_min,
+                                 x["init_state"], decay="log", workspace=ws)
+    torch.cuda.synchronize()
+    ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), g_min,
+                        x["init_state"].cpu(), decay="log")
+    assert rel(out, ro) <= TOL["bf16"], rel(out, ro)
+    assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_log_decay_decode(dtype):
+    w = I.DECODE.with_(B=8, H=4, dtype=dtype)
+    state = I.decode_state(w, device="cuda")
+    ref = state.cpu().double().numpy().copy()
+    for s in range(3):
+        x = I.decode_step_inputs(w, s, device="cuda")
+        o = gdr.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], -5.0, state, decay="log")
+        torch.cuda.synchronize()
+        r = oracle.decode(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), -5.0, ref,
+                          decay="log")
+        assert rel(o, r) <= TOL[dtype], rel(o, r)
+    assert rel(state, ref) <= 1e-5
+
+
 def test_zero_length_copies_state():
     w = I.PREFILL.with_(B=2, H=3, T=0)
     init = torch.randn(2, 3, 128, 128, device="cuda")
