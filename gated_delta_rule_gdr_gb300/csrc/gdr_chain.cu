@@ -22,11 +22,15 @@
 // generation tensor cores (tcgen05, M = 128, N = DVH, accumulator in TMEM),
 // issued by an output thread once the chain warps have published MS_n =
 // bf16(S_J) and Wt_n; rows 64-127 of the accumulator are Q M_n + P Wt_n, which
-// the two output warps scale by gamma and store.
+// the two output warps scale by gamma into the Q slabs of the chunk's stage (Q is
+// dead once the products completed) and write out with tensor stores, so the
+// output leaves by the TMA engine instead of 32-row scattered stores that
+// would share the load/store pipe with the chain warps' ldmatrix traffic.
 //
 // Warps: chain 0 .. NCH-1 (NCH = DVH / 16), copy NCH (TMA of K, Q, v, the
 // [Lb | P] tile by a plain bulk copy, the decay of each stage, L2 prefetch),
-// NCH + 1 idle, output NCH + 2 and NCH + 3 (TMEM lane quadrants 2 and 3).
+// NCH + 1 output products (one thread), output rows NCH + 2 and NCH + 3 (TMEM
+// lane quadrants 2 and 3).
 // Every mbarrier wait is bounded in time; a timeout sets the device error
 // word and makes every role of the CTA leave its loop.
 //
@@ -116,10 +120,34 @@ __device__ __noinline__ void emit_rows(uint32_t x, int r, int c, const float *ga
     }
 }
 
+// Output row r of a chunk into a 128-byte-swizzled staging tile (64-column slabs
+// SLAB bytes apart) for a tensor store: row r = gamma_r X[64 + r][:], bf16.
+template <int NCOL>
+__device__ __noinline__ void stage_rows(uint32_t x, int r, const float *gam, uint32_t dst, uint32_t slab) {
+    const float gr = gam[r];
+#pragma unroll 1
+    for (int cb = 0; cb < NCOL / 32; ++cb) {
+        float v[32];
+        tmem_ld32(x + cb * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const uint32_t u0 = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
+            const uint32_t u1 = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
+            const uint32_t u2 = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
+            const uint32_t u3 = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+            const uint32_t addr = dst + (uint32_t)(cb >> 1) * slab + swz((uint32_t)r, (uint32_t)((cb & 1) * 4 + q4));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u0), "r"(u1), "r"(u2), "r"(u3)
+                         : "memory");
+        }
+    }
+}
+
 template <int DVH>
 __global__ void __launch_bounds__(ChainCfg<DVH>::NT, 1)
 chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             const __grid_constant__ CUtensorMap tm_v, const FusedArgs a, const uint8_t *ws,
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+             const FusedArgs a, const uint8_t *ws,
              int64_t nslot) {
     using Cfg = ChainCfg<DVH>;
     constexpr int NCH = Cfg::NCH, NST = Cfg::NST, SPLIT = 128 / DVH;
@@ -164,6 +192,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
         }
     }
     tc_fence_before();
@@ -260,19 +289,41 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             float x[8][4];
 #pragma unroll
             for (int p = 0; p < 8; ++p) x[p][0] = x[p][1] = x[p][2] = x[p][3] = 0.f;
+            // operands of the E step, loaded while the X^T products run: the v fragments
+            // (matrices (s 16sp+0..7 | 8..15) x (j jw+0..7 | jw+8..15), transposed: vfa[sp][0]
+            // s 16sp+2t.., j g;  [1] s 16sp+2t.., j g+8;  [2] s 16sp+8+2t.., j g;  [3] s
+            // 16sp+8+2t.., j g+8), gamma and beta at s = 8p + 2t4 (+1)
+            uint32_t vfa[4][4];
+            float2 gaa[8], bea[8];
+            const float gC = s_gC[n % NST];
             {
-                // B fragments of one k-step (16 i x 64 s), loaded a k-step ahead
+                // B fragments of one k-step (16 i x 64 s), loaded two k-steps ahead
                 auto load_k = [&](uint32_t (&bf)[4][4], int kt) {
                     const uint32_t kb = st_a + Cfg::ST_K + (uint32_t)(kt >> 2) * 16384u;
 #pragma unroll
                     for (int sp = 0; sp < 4; ++sp)
                         ldsm_x4(bf[sp], kb + swz((uint32_t)(16 * sp) + bn_r, (uint32_t)((kt & 3) * 2) + bn_c));
                 };
-                uint32_t bq[2][4][4];
+                uint32_t bq[3][4][4];
                 load_k(bq[0], 0);
+                load_k(bq[1], 1);
 #pragma unroll
                 for (int kt = 0; kt < 8; ++kt) {   // i = 16 kt .. 16 kt + 15
-                    if (kt + 1 < 8) load_k(bq[(kt + 1) & 1], kt + 1);
+                    if (kt + 2 < 8) load_k(bq[(kt + 2) % 3], kt + 2);
+                    if (kt == 1) {
+                        // v[s][J] (TMA, 64-column slabs; zero-filled past the end of a dense tensor)
+                        const uint32_t vt = st_a + Cfg::ST_V + (uint32_t)(jw >> 6) * 8192u;
+                        const uint32_t vc = (uint32_t)((jw >> 3) & 7);
+#pragma unroll
+                        for (int sp = 0; sp < 4; ++sp)
+                            ldsm_x4_t(vfa[sp], vt + swz((uint32_t)(16 * sp) + (uint32_t)(lane & 7) + (uint32_t)((lane >> 4) * 8),
+                                                        vc + (uint32_t)((lane >> 3) & 1)));
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            gaa[p] = *reinterpret_cast<const float2 *>(&S.gam[8 * p + 2 * t4]);
+                            bea[p] = *reinterpret_cast<const float2 *>(&S.bs[8 * p + 2 * t4]);
+                        }
+                    }
                     uint32_t af[4];
                     af[0] = pack_bf16x2(s[2 * kt][0], s[2 * kt][1]);
                     af[1] = pack_bf16x2(s[2 * kt][2], s[2 * kt][3]);
@@ -280,8 +331,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     af[3] = pack_bf16x2(s[2 * kt + 1][2], s[2 * kt + 1][3]);
 #pragma unroll
                     for (int sp = 0; sp < 4; ++sp) {   // s = 16 sp .. 16 sp + 15
-                        mma16816(x[2 * sp], af, bq[kt & 1][sp][0], bq[kt & 1][sp][1]);
-                        mma16816(x[2 * sp + 1], af, bq[kt & 1][sp][2], bq[kt & 1][sp][3]);
+                        mma16816(x[2 * sp], af, bq[kt % 3][sp][0], bq[kt % 3][sp][1]);
+                        mma16816(x[2 * sp + 1], af, bq[kt % 3][sp][2], bq[kt % 3][sp][3]);
                     }
                 }
             }
@@ -292,23 +343,15 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             uint8_t *wt = sm + Cfg::OFF_WT + wb * Cfg::WT_BYTES;
             uint32_t ea[4][4];   // E^T A fragments, 16-column steps (E_REGS)
             {
-                // v[s][J] (TMA, 64-column slabs; zero-filled past the end of a dense tensor)
-                const uint32_t vt = st_a + Cfg::ST_V + (uint32_t)(jw >> 6) * 8192u;
-                const uint32_t vc = (uint32_t)((jw >> 3) & 7);
 #pragma unroll
                 for (int sp = 0; sp < 4; ++sp) {
-                    // matrices (s 16sp+0..7 | 8..15) x (j jw+0..7 | jw+8..15), transposed:
-                    // vf[0] s 16sp+2t.., j g;  vf[1] s 16sp+2t.., j g+8;
-                    // vf[2] s 16sp+8+2t.., j g;  vf[3] s 16sp+8+2t.., j g+8
-                    uint32_t vf[4];
-                    ldsm_x4_t(vf, vt + swz((uint32_t)(16 * sp) + (uint32_t)(lane & 7) + (uint32_t)((lane >> 4) * 8),
-                                           vc + (uint32_t)((lane >> 3) & 1)));
+                    const uint32_t (&vf)[4] = vfa[sp];
                     uint32_t eb[4];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int p = 2 * sp + h, sc0 = 8 * p + 2 * t4;
-                        const float2 ga = *reinterpret_cast<const float2 *>(&S.gam[sc0]);
-                        const float2 be = *reinterpret_cast<const float2 *>(&S.bs[sc0]);
+                        const int p = 2 * sp + h;
+                        const float2 ga = gaa[p];
+                        const float2 be = bea[p];
                         const float2 vlo = bf16x2_to_float2(vf[2 * h]);
                         const float2 vhi = bf16x2_to_float2(vf[2 * h + 1]);
                         const float e0 = fmaf(-ga.x, x[p][0], vlo.x), e1 = fmaf(-ga.y, x[p][1], vlo.y);
@@ -332,6 +375,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             __syncwarp();
 
             // ---- W^T = X^T + E^T Lb^T: A = E^T (this warp's rows), B = Lb[r][s] rows
+            float2 sca[8];   // gamma_C / gamma at r = 8p + 2t4 (+1), loaded during the products
             {
                 const uint32_t lb_a = st_a + Cfg::ST_LP;
                 auto load_l = [&](uint32_t (&af)[4], uint32_t (&bf)[4][4], int ks) {
@@ -346,6 +390,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {   // s = 16 ks .. 16 ks + 15
                     if (ks + 1 < 4) load_l(aq[(ks + 1) & 1], bq[(ks + 1) & 1], ks + 1);
+                    if (ks == 1) {
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) sca[p] = *reinterpret_cast<const float2 *>(&S.sc[8 * p + 2 * t4]);
+                    }
                     const uint32_t (&af)[4] = Cfg::E_REGS ? ea[ks] : aq[ks & 1];
 #pragma unroll
                     for (int rp = 0; rp < 4; ++rp) {   // r = 16 rp .. 16 rp + 15
@@ -362,8 +410,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             {
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
-                    const int r0 = 8 * p + 2 * t4;
-                    const float2 sc = *reinterpret_cast<const float2 *>(&S.sc[r0]);
+                    const float2 sc = sca[p];
                     ef[p >> 1][2 * (p & 1) + 0] = pack_bf16x2(sc.x * x[p][0], sc.y * x[p][1]);
                     ef[p >> 1][2 * (p & 1) + 1] = pack_bf16x2(sc.x * x[p][2], sc.y * x[p][3]);
                 }
@@ -375,12 +422,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
             // ---- S_J = gamma_C S_J + Wt^T K: B = K[r][i] rows (transposed)
             {
-                const float gC = s_gC[n % NST];
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[q][e] *= gC;
-                // B fragments of a quarter step (16 r x 64 i), loaded a quarter ahead
+                // B fragments of a quarter step (16 r x 64 i), loaded two quarters ahead
                 auto load_kt = [&](uint32_t (&bf)[4][4], int qq) {
                     const int ks = qq >> 1, slab = qq & 1;
 #pragma unroll
@@ -388,16 +434,17 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         ldsm_x4_t(bf[ip], st_a + Cfg::ST_K + (uint32_t)slab * 16384u +
                                               swz((uint32_t)(16 * ks) + bt_r, (uint32_t)(ip * 2) + bt_c));
                 };
-                uint32_t bq[2][4][4];
+                uint32_t bq[3][4][4];
                 load_kt(bq[0], 0);
+                load_kt(bq[1], 1);
 #pragma unroll
                 for (int qq = 0; qq < 8; ++qq) {   // r = 16 (qq / 2) .., i = 64 (qq % 2) ..
-                    if (qq + 1 < 8) load_kt(bq[(qq + 1) & 1], qq + 1);
+                    if (qq + 2 < 8) load_kt(bq[(qq + 2) % 3], qq + 2);
                     const int ks = qq >> 1, slab = qq & 1;
 #pragma unroll
                     for (int ip = 0; ip < 4; ++ip) {   // i = 64 slab + 16 ip ..
-                        mma16816(s[8 * slab + 2 * ip], ef[ks], bq[qq & 1][ip][0], bq[qq & 1][ip][1]);
-                        mma16816(s[8 * slab + 2 * ip + 1], ef[ks], bq[qq & 1][ip][2], bq[qq & 1][ip][3]);
+                        mma16816(s[8 * slab + 2 * ip], ef[ks], bq[qq % 3][ip][0], bq[qq % 3][ip][1]);
+                        mma16816(s[8 * slab + 2 * ip + 1], ef[ks], bq[qq % 3][ip][2], bq[qq % 3][ip][3]);
                     }
                 }
             }
@@ -461,20 +508,40 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // thread r: accumulator row 64 + r (TMEM lane 64 + r) = output row r of a chunk
         const int r = tid - 32 * (NCH + 2);
         const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const bool packed = a.cu_seqlens != nullptr;
         for (int m = 0; m < NC; ++m) {
             bool ok = (r != 0) ||
                       role_wait(bar(B_OFULL0 + (m & 1)), (uint32_t)(m >> 1) & 1u, a.limit_ns, &s_abort);
             if (!named_and(BAR_OUT, 64, ok)) break;
             tc_fence_after();
-            emit_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, r, min(C, T - m * C), scal(m).gam,
-                           out0 + (int64_t)m * C * orow, orow);
+            const int c = min(C, T - m * C);
+            // A whole chunk, or the clipped tail of a dense sequence: staged in the Q slabs
+            // of its stage (the products that read Q_m are complete) and written by tensor
+            // stores; the tail of a packed sequence by plain stores.
+            const bool tiled = !packed || c == C;
+            const uint32_t stg = stage(m) + Cfg::ST_Q;
+            if (tiled) {
+                fence_proxy_async_smem();
+                stage_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, r, scal(m).gam, stg, 16384u);
+                fence_proxy_async_smem();
+            } else {
+                emit_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, r, c, scal(m).gam, out0 + (int64_t)m * C * orow, orow);
+            }
             tc_fence_before();
             named_sync(BAR_OUT, 64);
             if (r == 0) {
                 mbar_arrive(bar(B_OFREE0 + (m & 1)));   // the accumulator buffer is read out
+                if (tiled) {
+#pragma unroll
+                    for (int vs = 0; vs < DVH / 64; ++vs)
+                        tma_store_3d(&tm_o, stg + (uint32_t)vs * 16384u, j0 + 64 * vs, sv.tz + m * C, sv.z);
+                    bulk_commit();
+                    bulk_wait_read_all();   // the stage may be refilled once the store has read it
+                }
                 mbar_arrive(bar(B_FREE0 + m % NST));    // the products of chunk m are done
             }
         }
+        if (r == 0) bulk_wait_all();
     } else {
         // ================================================================ copy (warp NCH)
         // Stage n % NST of chunk n: K and Q (two slabs each) and v[., J] by TMA, the
@@ -562,13 +629,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
 template <int DVH>
 cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const FusedArgs &a, const void *ws, int64_t nslot, int BH, cudaStream_t s) {
+                           const CUtensorMap &mo, const FusedArgs &a, const void *ws, int64_t nslot, int BH, cudaStream_t s) {
     using Cfg = ChainCfg<DVH>;
     cudaError_t e = cudaFuncSetAttribute(chain_kernel<DVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     chain_kernel<DVH><<<(unsigned)(BH * (128 / DVH)), Cfg::NT, Cfg::SMEM_ALLOC, s>>>(
-        mq, mk, mv, a, static_cast<const uint8_t *>(ws), nslot);
+        mq, mk, mv, mo, a, static_cast<const uint8_t *>(ws), nslot);
     return cudaGetLastError();
 }
 
@@ -597,10 +664,11 @@ cudaError_t launch_chain(const void *q, const void *k, const void *v, const floa
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
          reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(ws)) & 15)
         return cudaErrorMisalignedAddress;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const bool ok = cu_seqlens ? (make_map_packed(&mq, q, H, total_T) && make_map_packed(&mk, k, H, total_T) &&
-                                  make_map_packed(&mv, v, H, total_T))
-                               : (make_map(&mq, q, BH, T) && make_map(&mk, k, BH, T) && make_map(&mv, v, BH, T));
+                                  make_map_packed(&mv, v, H, total_T) && make_map_packed(&mo, out, H, total_T))
+                               : (make_map(&mq, q, BH, T) && make_map(&mk, k, BH, T) && make_map(&mv, v, BH, T) &&
+                                  make_map(&mo, out, BH, T));
     if (!ok) return cudaErrorInvalidValue;
     FusedArgs a{g, beta, init, static_cast<__nv_bfloat16 *>(out), final_state, a_min, T, wait_limit_ns(),
                 static_cast<const __nv_bfloat16 *>(v)};
@@ -608,8 +676,8 @@ cudaError_t launch_chain(const void *q, const void *k, const void *v, const floa
     a.H = H;
     a.total_T = total_T;
     const int64_t nslot = tile_slots(a, BH);
-    return chain_split(BH) == 2 ? launch_chain_t<64>(mq, mk, mv, a, ws, nslot, BH, s)
-                                : launch_chain_t<128>(mq, mk, mv, a, ws, nslot, BH, s);
+    return chain_split(BH) == 2 ? launch_chain_t<64>(mq, mk, mv, mo, a, ws, nslot, BH, s)
+                                : launch_chain_t<128>(mq, mk, mv, mo, a, ws, nslot, BH, s);
 }
 
 cudaError_t take_chain_error_word(unsigned *value) { return take_error_word(value); }
