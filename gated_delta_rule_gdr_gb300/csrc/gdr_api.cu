@@ -28,6 +28,11 @@ bool range_ok(float d, int chunk) {
     const double worst = d > 0.0f ? std::log((double)d) : (double)d;
     return (double)chunk * -worst <= 80.0;
 }
+// The two-kernel path applies the bound over the pages' 16-token tile: its
+// preparation splits each chunk's position-pair decay at 16-row reference
+// points and its chain takes only factors at most 1, so the decay over a whole
+// chunk may fall below fp32's range.
+constexpr int kTile = 16;
 
 gdr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
@@ -268,7 +273,7 @@ gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, cons
     if (need == 0 || workspace == nullptr || workspace_bytes < need)
         return chunk_fwd_impl(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk,
                               dv, chunk, dtype, stream);
-    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    if (!range_ok(a_min, kTile)) return GDR_ERR_RANGE;
     if ((int64_t)T * B * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -317,7 +322,7 @@ gdr_status_t gdr_chunk_fwd_varlen_ws(const void *q, const void *k, const void *v
         return gdr_chunk_fwd_varlen(q, k, v, g, beta, a_min, init_state, out, final_state,
                                     cu_seqlens, S, H, total_T, dk, dv, chunk, dtype, stream);
     if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
-    if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+    if (!range_ok(a_min, kTile)) return GDR_ERR_RANGE;
     if ((int64_t)total_T * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     if (!cu_seqlens || !q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -332,9 +337,10 @@ gdr_status_t gdr_chunk_fwd_varlen_ws(const void *q, const void *k, const void *v
 
 int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
                           gdr_dtype_t dtype) {
-    const int p = gdr_chunk_fwd_path(B, H, T, dk, dv, chunk, a_min, dtype);
-    if (p < 2 || gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) == 0) return p;
-    return gdr::chain_split(B * H) == 2 ? 4 : 5;
+    if (gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) > 0 && a_min_ok(a_min) &&
+        range_ok(a_min, kTile))
+        return gdr::chain_split(B * H) == 2 ? 4 : 5;
+    return gdr_chunk_fwd_path(B, H, T, dk, dv, chunk, a_min, dtype);
 }
 
 int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float a_min,
@@ -369,7 +375,8 @@ const char *gdr_status_string(gdr_status_t status) {
         case GDR_OK: return "ok";
         case GDR_ERR_INVALID_ARG: return "invalid argument";
         case GDR_ERR_UNSUPPORTED: return "unsupported shape or dtype";
-        case GDR_ERR_RANGE: return "chunk * -ln(a_min) exceeds the in-chunk decay range (80)";
+        case GDR_ERR_RANGE:
+            return "the decay over a chunk (a 16-token tile on the workspace path) falls below e^-80";
         case GDR_ERR_CUDA: return "CUDA runtime error";
         case GDR_ERR_TIMEOUT: return "device-side bounded wait timed out";
     }

@@ -3,10 +3,13 @@
 // [Lb | P] tiles that gdr_prep.cu wrote for every chunk.
 //
 // Chunk algebra (sections 3.1-3.3 of "What a Trillion-Parameter MoE Model
-// Reveals About the Next Stage of LLM Scaling"; the lower-bounded decay keeps
-// 1/gamma finite):
+// Reveals About the Next Stage of LLM Scaling"):
 //   E = V - diag(gamma) K M_n,   W = diag(beta) E + Lb E,   Wt = diag(gamma_C/gamma) W,
-//   O = diag(gamma) (Q M_n + P Wt),   M_{n+1} = gamma_C M_n + K^T Wt.
+//   O = diag(gamma) Q M_n + P W,   M_{n+1} = gamma_C M_n + K^T Wt,
+// with P = lower_incl(D o Q K^T), D[r][s] = e^(b_r - b_s), from the preparation.
+// Every factor here is at most 1 (gamma, gamma_C / gamma, D), so the chain
+// holds however far the decay falls over a chunk; where gamma underflows, the
+// state's share of the row is below fp32's range anyway.
 //
 // Work split.  A CTA owns DVH value columns J of one head (DVH = 64: two CTAs
 // per head, independent of each other; DVH = 128: one).  The recurrence never
@@ -18,11 +21,12 @@
 // S_J = gamma_C S_J + Wt^T K directly.  No chain step waits for another warp
 // or for a tensor-memory round trip.
 //
-// The output leaves the chain: [K;Q] MS_n and [Lb;P] Wt_n run on the 5th-
-// generation tensor cores (tcgen05, M = 128, N = DVH, accumulator in TMEM),
-// issued by an output thread once the chain warps have published MS_n =
-// bf16(S_J) and Wt_n; rows 64-127 of the accumulator are Q M_n + P Wt_n, which
-// the two output warps scale by gamma into the Q slabs of the chunk's stage (Q is
+// The output leaves the chain: [K;Q] MS_n and [Lb;P] W_n run on the 5th-
+// generation tensor cores (tcgen05, M = 128, N = DVH, two accumulators in
+// TMEM), issued by an output thread once the chain warps have published MS_n =
+// bf16(S_J) and W_n; rows 64-127 of the accumulators are Q M_n and P W_n, which
+// the two output warps combine as gamma Q M_n + P W_n into the Q slabs of the
+// chunk's stage (Q is
 // dead once the products completed) and write out with tensor stores, so the
 // output leaves by the TMA engine instead of 32-row scattered stores that
 // would share the load/store pipe with the chain warps' ldmatrix traffic.
@@ -35,8 +39,9 @@
 // word and makes every role of the CTA leave its loop.
 //
 // Shared memory: NST stages of [K | Q (two 64-column slabs each) | v[s][J]
-// (64-column slabs) | Lb | P], MS ([slab i/64][j][64 i]), Wt[2] ([j][r]; a
-// chain warp's rows hold E^T first), the stage scalars.  Every bf16 tile has
+// (64-column slabs) | Lb | P], MS ([slab i/64][j][64 i]), the W tiles [2]
+// ([j][r]; a chain warp's rows hold E^T first where E is not kept in
+// registers), the stage scalars.  Every bf16 tile has
 // 128-byte rows with the 16-byte chunks XOR-swizzled by row (the TMA and UMMA
 // 128-byte swizzle).
 
@@ -64,7 +69,9 @@ template <int DVH> struct ChainCfg {
     static constexpr uint32_t OFF_SC = OFF_WT + 2 * WT_BYTES;   // a 5 x 64 fp32 slot per stage
     static constexpr uint32_t SMEM_USED = OFF_SC + NST * 5 * 64 * 4;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-    static constexpr uint32_t TM_COLS = DVH == 64 ? 128 : 256;  // output accumulator x 2
+    // accumulators Q M_n and P W_n, each for two chunks in flight
+    static constexpr uint32_t TM_COLS = 4 * DVH;
+    static constexpr uint32_t TM_PW = 2 * DVH;   // first column of the P W_n pair
     static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KB of shared memory per CTA");
     static_assert(ST_BYTES % 1024 == 0 && OFF_MS % 1024 == 0 && OFF_WT % 1024 == 0 &&
                       ST_LP % 1024 == 0 && MS_SLAB % 1024 == 0,
@@ -75,11 +82,11 @@ template <int DVH> struct ChainCfg {
 enum : int {
     B_FULL0 = 0,          // stage landed (TMA, bulk copy) and its scalars written (x3, count 2)
     B_FREE0 = 3,          // chain warps + output warps done with a stage (x3, count NCH + 1)
-    B_MSREADY0 = 6,       // chain warps: MS_m and Wt_{m-1} published, phase of m on buffer m % 2
+    B_MSREADY0 = 6,       // chain warps: MS_m and W_{m-1} published, phase of m on buffer m % 2
                           //   (x2, count NCH)
     B_QMS = 8,            // issue commit: [K;Q] MS_n done (single MS buffer: may be overwritten)
-    B_SAFE0 = 9,          // issue commit after [K;Q] MS_{n-1} and [Lb;P] Wt_{n-2}: chunk n may
-                          //   overwrite Wt[n % 2] and MS[(n + 1) % 2] (x2)
+    B_SAFE0 = 9,          // issue commit after [K;Q] MS_{n-1} and [Lb;P] W_{n-2}: chunk n may
+                          //   overwrite W[n % 2] and MS[(n + 1) % 2] (x2)
     B_OFULL0 = 11,        // issue commit: accumulator buffer b complete (x2)
     B_OFREE0 = 13,        // output warps: accumulator buffer b read out (x2)
     B_DRAIN = 15,         // commit of the error path
@@ -94,26 +101,28 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
 }
 
-// Output row r (< 64) of a chunk with c valid rows, NCOL columns from TMEM
-// column x (this thread's lane = 64 + r): out[r][:] = gamma_r X[64 + r][:].
+// Output row r (< 64) of a chunk with c valid rows, NCOL columns from the TMEM
+// accumulators at columns x (Q M_n) and y (P W_n), this thread's lane = 64 + r:
+// out[r][:] = gamma_r X[64 + r][:] + Y[64 + r][:].
 template <int NCOL>
-__device__ __noinline__ void emit_rows(uint32_t x, int r, int c, const float *gam, __nv_bfloat16 *out0,
-                                       int64_t orow) {
+__device__ __noinline__ void emit_rows(uint32_t x, uint32_t y, int r, int c, const float *gam,
+                                       __nv_bfloat16 *out0, int64_t orow) {
+    const float gr = gam[r];
 #pragma unroll 1
     for (int cb = 0; cb < NCOL / 32; ++cb) {
-        float v[32];
+        float v[32], w[32];
         tmem_ld32(x + cb * 32, v);
+        tmem_ld32(y + cb * 32, w);
         tmem_wait_ld();
         if (r < c) {
-            const float gr = gam[r];
             uint4 *dst = reinterpret_cast<uint4 *>(out0 + (int64_t)r * orow + cb * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint4 u;
-                u.x = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
-                u.y = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
-                u.z = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
-                u.w = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+                u.x = pack_bf16x2(fmaf(gr, v[q4 * 8 + 0], w[q4 * 8 + 0]), fmaf(gr, v[q4 * 8 + 1], w[q4 * 8 + 1]));
+                u.y = pack_bf16x2(fmaf(gr, v[q4 * 8 + 2], w[q4 * 8 + 2]), fmaf(gr, v[q4 * 8 + 3], w[q4 * 8 + 3]));
+                u.z = pack_bf16x2(fmaf(gr, v[q4 * 8 + 4], w[q4 * 8 + 4]), fmaf(gr, v[q4 * 8 + 5], w[q4 * 8 + 5]));
+                u.w = pack_bf16x2(fmaf(gr, v[q4 * 8 + 6], w[q4 * 8 + 6]), fmaf(gr, v[q4 * 8 + 7], w[q4 * 8 + 7]));
                 __stcs(dst + q4, u);
             }
         }
@@ -121,21 +130,23 @@ __device__ __noinline__ void emit_rows(uint32_t x, int r, int c, const float *ga
 }
 
 // Output row r of a chunk into a 128-byte-swizzled staging tile (64-column slabs
-// SLAB bytes apart) for a tensor store: row r = gamma_r X[64 + r][:], bf16.
+// SLAB bytes apart) for a tensor store: row r = gamma_r X[64 + r][:] + Y[64 + r][:], bf16.
 template <int NCOL>
-__device__ __noinline__ void stage_rows(uint32_t x, int r, const float *gam, uint32_t dst, uint32_t slab) {
+__device__ __noinline__ void stage_rows(uint32_t x, uint32_t y, int r, const float *gam, uint32_t dst,
+                                        uint32_t slab) {
     const float gr = gam[r];
 #pragma unroll 1
     for (int cb = 0; cb < NCOL / 32; ++cb) {
-        float v[32];
+        float v[32], w[32];
         tmem_ld32(x + cb * 32, v);
+        tmem_ld32(y + cb * 32, w);
         tmem_wait_ld();
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t u0 = pack_bf16x2(v[q4 * 8 + 0] * gr, v[q4 * 8 + 1] * gr);
-            const uint32_t u1 = pack_bf16x2(v[q4 * 8 + 2] * gr, v[q4 * 8 + 3] * gr);
-            const uint32_t u2 = pack_bf16x2(v[q4 * 8 + 4] * gr, v[q4 * 8 + 5] * gr);
-            const uint32_t u3 = pack_bf16x2(v[q4 * 8 + 6] * gr, v[q4 * 8 + 7] * gr);
+            const uint32_t u0 = pack_bf16x2(fmaf(gr, v[q4 * 8 + 0], w[q4 * 8 + 0]), fmaf(gr, v[q4 * 8 + 1], w[q4 * 8 + 1]));
+            const uint32_t u1 = pack_bf16x2(fmaf(gr, v[q4 * 8 + 2], w[q4 * 8 + 2]), fmaf(gr, v[q4 * 8 + 3], w[q4 * 8 + 3]));
+            const uint32_t u2 = pack_bf16x2(fmaf(gr, v[q4 * 8 + 4], w[q4 * 8 + 4]), fmaf(gr, v[q4 * 8 + 5], w[q4 * 8 + 5]));
+            const uint32_t u3 = pack_bf16x2(fmaf(gr, v[q4 * 8 + 6], w[q4 * 8 + 6]), fmaf(gr, v[q4 * 8 + 7], w[q4 * 8 + 7]));
             const uint32_t addr = dst + (uint32_t)(cb >> 1) * slab + swz((uint32_t)r, (uint32_t)((cb & 1) * 4 + q4));
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u0), "r"(u1), "r"(u2), "r"(u3)
                          : "memory");
@@ -241,7 +252,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
         };
         // Publication m, for the output products: MS_m = bf16(S_J) into buffer m % MSB
-        // (rows j, K-major; m < NC) and the Wt_{m-1} tile stored earlier, behind one
+        // (rows j, K-major; m < NC) and the W_{m-1} tile stored earlier, behind one
         // fence (the products read them through the async proxy)
         auto publish = [&](int m) {
             if (m < NC) {
@@ -404,20 +415,23 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             __syncwarp();   // every lane has read E^T: Wt may overwrite it
 
-            // ---- Wt^T = W^T diag(gamma_C / gamma) -> bf16: A fragments, and the Wt tile
-            // ([j][r], K-major) that the output product reads
+            // ---- W^T -> bf16 into the W tile ([j][r], K-major) that the output product
+            // P W reads;  Wt^T = W^T diag(gamma_C / gamma) -> bf16 A fragments of the
+            // state update
             uint32_t ef[4][4];
             {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * ks) + st_c),
+                            pack_bf16x2(x[2 * ks][0], x[2 * ks][1]), pack_bf16x2(x[2 * ks][2], x[2 * ks][3]),
+                            pack_bf16x2(x[2 * ks + 1][0], x[2 * ks + 1][1]),
+                            pack_bf16x2(x[2 * ks + 1][2], x[2 * ks + 1][3]));
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     const float2 sc = sca[p];
                     ef[p >> 1][2 * (p & 1) + 0] = pack_bf16x2(sc.x * x[p][0], sc.y * x[p][1]);
                     ef[p >> 1][2 * (p & 1) + 1] = pack_bf16x2(sc.x * x[p][2], sc.y * x[p][3]);
                 }
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    stsm_x4(smem_u32(wt) + swz((uint32_t)jw + st_r, (uint32_t)(2 * ks) + st_c), ef[ks][0],
-                            ef[ks][1], ef[ks][2], ef[ks][3]);
             }
 
             // ---- S_J = gamma_C S_J + Wt^T K: B = K[r][i] rows (transposed)
@@ -452,7 +466,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (lane == 0) mbar_arrive(bar(B_FREE0 + n % NST));   // this warp is done with stage n
             // a single MS buffer is free once the output's [K;Q] MS_n has completed
             if (Cfg::MSB == 1 && n + 1 < NC && !warp_wait(B_QMS, (uint32_t)n & 1u)) break;
-            publish(n + 1);   // MS_{n+1} (if any) and Wt_n
+            publish(n + 1);   // MS_{n+1} (if any) and W_n
             if (n + 1 == NC && a.final_state) store_state();
         }
     } else if (warp == NCH + 1) {
@@ -460,8 +474,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (lane == 0) {
             const uint32_t idesc_o = idesc_bf16(128, DVH, false, false);   // K-major A and B
             bool issued = false;
-            // Iteration m: [Lb;P] Wt_{m-1} completes chunk m-1's accumulator, then
-            // O(m) = [K;Q] MS_m starts chunk m's (rows 64-127: Q M_m + P Wt_m / ...)
+            // Iteration m: [Lb;P] W_{m-1} fills chunk m-1's second accumulator (rows
+            // 64-127: P W), then [K;Q] MS_m chunk m's first (rows 64-127: Q M_m)
             for (int m = 0; m <= NC && NC > 0; ++m) {
                 if (!role_wait(bar(B_MSREADY0 + (m & 1)), (uint32_t)(m >> 1) & 1u, a.limit_ns, &s_abort)) break;
                 if (m > 0) {
@@ -471,8 +485,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const uint64_t dw = sdesc_sw128(sbase + Cfg::OFF_WT + (uint32_t)(n & 1) * Cfg::WT_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + (uint32_t)(n & 1) * DVH, sdesc_add(dl, kk * 32), sdesc_add(dw, kk * 32),
-                                 idesc_o, 1);
+                        mma_bf16(tmem + Cfg::TM_PW + (uint32_t)(n & 1) * DVH, sdesc_add(dl, kk * 32),
+                                 sdesc_add(dw, kk * 32), idesc_o, kk > 0);
                     mma_commit(bar(B_OFULL0 + (n & 1)));
                 }
                 if (m == NC) break;
@@ -492,7 +506,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                  sdesc_add(db, (kk >> 2) * Cfg::MS_SLAB + (kk & 3) * 32), idesc_o, kk > 0);
                 }
                 mma_commit(bar(B_QMS));
-                // chunk m+1 may overwrite Wt[(m+1) % 2] (read by Wt_{m-1}'s product) and
+                // chunk m+1 may overwrite W[(m+1) % 2] (read by W_{m-1}'s product) and
                 // MS[m % 2] once both products issued so far are done
                 if (m + 1 < NC) mma_commit(bar(B_SAFE0 + ((m + 1) & 1)));
                 issued = true;
@@ -522,10 +536,12 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t stg = stage(m) + Cfg::ST_Q;
             if (tiled) {
                 fence_proxy_async_smem();
-                stage_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, r, scal(m).gam, stg, 16384u);
+                stage_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, tl + Cfg::TM_PW + (uint32_t)(m & 1) * DVH, r,
+                                scal(m).gam, stg, 16384u);
                 fence_proxy_async_smem();
             } else {
-                emit_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, r, c, scal(m).gam, out0 + (int64_t)m * C * orow, orow);
+                emit_rows<DVH>(tl + (uint32_t)(m & 1) * DVH, tl + Cfg::TM_PW + (uint32_t)(m & 1) * DVH, r, c,
+                               scal(m).gam, out0 + (int64_t)m * C * orow, orow);
             }
             tc_fence_before();
             named_sync(BAR_OUT, 64);

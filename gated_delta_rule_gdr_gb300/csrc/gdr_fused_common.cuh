@@ -146,11 +146,66 @@ __device__ __forceinline__ void warp_decay_inl(int lane, float g0, float g1, flo
         s.ig[r] = ig;
         s.bs[r] = b;
         s.bg[r] = b * gam;
-        s.sc[r] = valid ? gC * ig : 0.f;
+        // gamma_C / gamma as one exponential of the difference (at most 1), so that
+        // it stays exact where gamma alone underflows
+        s.sc[r] = valid ? __expf(bC - (e ? b1 : b0)) : 0.f;
     }
     if (lane == 0) *s_gC = gC;
     __syncwarp();
 }
+// Scalars of the preparation's diagonal tile with 16-row reference points.
+// The decay over a whole 64-row chunk may span far more than fp32 can hold as
+// gamma and 1/gamma (the pages bound it over 16-token tiles only), so the
+// position-pair factor e^(b_r - b_s) of row r in block R = r / 16 is split at
+// rho_R = b_{16 R}: a row factor e^(b_r - rho_R) in (e^-80, 1] and a column
+// factor e^(rho_R - b_s), at most e^80 for s in block R and at most 1 for s in
+// an earlier block.  Both stay finite whenever 16 |log alpha| <= 80, and their
+// product underflows only where the exact factor is below fp32's range.
+// Writes rf[r] = beta_r e^(b_r - rho_R), pf[r] = e^(b_r - rho_R), bs[r] = beta_r
+// (zero past the chunk's c rows) and cf[R * 64 + s] = e^(rho_R - b_s) for s <
+// min(16 R + 16, c), zero elsewhere.  Warp-wide; lane l holds rows 2l, 2l + 1.
+struct TileScal {
+    float *rf, *pf, *bs, *cf;   // 64, 64, 64 and 4 x 64 floats
+};
+__device__ __forceinline__ TileScal tile_scal_at(float *b) {   // 7 x 64 floats
+    return {b, b + 64, b + 128, b + 192};
+}
+__device__ __forceinline__ void warp_decay_tiles(int lane, float g0, float g1, float be0, float be1,
+                                                 int c, float a_min, TileScal s) {
+    const int r0 = 2 * lane;
+    const float om = 1.0f - a_min;
+    auto la = [&](float gg) {
+        return a_min > 0.0f ? log1pf(-__fdividef(om, 1.0f + __expf(gg)))
+                            : a_min * __fdividef(1.0f, 1.0f + __expf(-gg));
+    };
+    const float l0 = (r0 < c) ? la(g0) : 0.f;
+    const float l1 = (r0 + 1 < c) ? la(g1) : 0.f;
+    float incl = l0 + l1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const float b[2] = {incl - l1, incl};
+    float rho[4];   // b at rows 0, 16, 32, 48: the b[0] of lanes 0, 8, 16, 24
+#pragma unroll
+    for (int R = 0; R < 4; ++R) rho[R] = __shfl_sync(0xffffffffu, b[0], 8 * R);
+    const float bt[2] = {be0, be1};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = r0 + e;
+        const bool valid = r < c;
+        const float f = valid ? __expf(b[e] - rho[r >> 4]) : 0.f;
+        s.pf[r] = f;
+        s.rf[r] = valid ? bt[e] * f : 0.f;
+        s.bs[r] = valid ? bt[e] : 0.f;
+#pragma unroll
+        for (int R = 0; R < 4; ++R)
+            s.cf[R * 64 + r] = (valid && (r >> 4) <= R) ? __expf(rho[R] - b[e]) : 0.f;
+    }
+    __syncwarp();
+}
+
 // The same, not inlined, for the copy warps of the fused and chain kernels: they
 // call it at two places, and its code would otherwise crowd the instruction
 // cache the other warps share.  (A warp with many live registers inlines it

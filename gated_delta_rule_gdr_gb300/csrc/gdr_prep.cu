@@ -3,11 +3,16 @@
 // path; gdr_chain.cu is the second).
 //
 // Per chunk (sections 3.1-3.3 of "What a Trillion-Parameter MoE Model Reveals
-// About the Next Stage of LLM Scaling": with the lower-bounded decay, 1/gamma
-// stays finite and the causal tile is a dense product with diagonal scalings):
+// About the Next Stage of LLM Scaling": with the lower-bounded decay the
+// reciprocal decay stays finite over a 16-token tile, and the causal tile is a
+// dense product with diagonal scalings):
 //   [K;Q] K^T                                  (tcgen05, M = 128, N = 64, K = 128)
-//   A  = strict_lower(diag(beta gamma) K K^T diag(1/gamma)),  T = (I + A)^-1
-//   Lb = bf16(strict_lower(T) diag(beta)),  P = bf16(lower_incl(Q K^T) / gamma_C)
+//   A  = strict_lower(diag(beta) D o K K^T),  T = (I + A)^-1
+//   Lb = bf16(strict_lower(T) diag(beta)),  P = bf16(lower_incl(D o Q K^T))
+// with D[r][s] = e^(b_r - b_s) the decay between positions s <= r, applied as
+// the diagonal scalings of the pages' 16-token tiles: row r of 16-row block R
+// takes e^(b_r - b_{16R}), column s takes e^(b_{16R} - b_s) for that block, so
+// no factor leaves fp32's range however far the decay falls over the chunk.
 // and the [Lb | P] tile (16 KB, the 128-byte-swizzled shared-memory image the
 // chain kernel loads verbatim) goes to the workspace.  Nothing here depends on
 // the state, so every (sequence, head, chunk) is an independent work item; a
@@ -36,8 +41,8 @@ constexpr uint32_t OFF_OUT = OFF_IN + IN_BYTES;         // the [Lb | P] tile (16
 constexpr uint32_t LP_TILE_P = 8192;                    // P within the tile
 constexpr uint32_t OFF_AS = OFF_OUT + TILE_BYTES;       // 64 x 68 fp32: A, then T in place
 constexpr uint32_t OFF_YS = OFF_AS + 64 * LDA * 4;      // 32 x 40 fp32 merge scratch
-constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;      // 5 x 64 fp32 chunk scalars
-constexpr uint32_t SMEM_USED = OFF_SC + 5 * 64 * 4;
+constexpr uint32_t OFF_SC = OFF_YS + 32 * LDY * 4;      // 7 x 64 fp32 tile scalars
+constexpr uint32_t SMEM_USED = OFF_SC + 7 * 64 * 4;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;       // alignment slack
 static_assert(IN_BYTES % 1024 == 0 && OFF_OUT % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
 static_assert(CTAS_PER_SM * SMEM_ALLOC <= 232448, "CTAs per SM");
@@ -83,7 +88,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sbase = smem_u32(sm);
     __shared__ __align__(8) uint64_t s_bar[NUM_BARS];
     __shared__ uint32_t s_tmem;
-    __shared__ float s_gC;
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -109,7 +113,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float *As = reinterpret_cast<float *>(sm + OFF_AS);
     float *Ys = reinterpret_cast<float *>(sm + OFF_YS);
     uint8_t *tile = sm + OFF_OUT;
-    const Scal S = scal_at(reinterpret_cast<float *>(sm + OFF_SC));
+    const TileScal S = tile_scal_at(reinterpret_cast<float *>(sm + OFF_SC));
     const int lrow = warp * 32 + lane;           // TMEM lane (quadrant = warp) = accumulator row
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 
@@ -168,7 +172,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int nx = next_valid(it + (int)gridDim.x, bh2, n2, v2);
         if (warp == 3) {   // the chunk's decay (away from the warp that issued the product),
                            // then the next item's g, beta
-            warp_decay_inl(lane, gv[0], gv[1], bv[0], bv[1], min(C, v.T - n * C), a.a_min, S, &s_gC);
+            warp_decay_tiles(lane, gv[0], gv[1], bv[0], bv[1], min(C, v.T - n * C), a.a_min, S);
             if (nx < items) load_gb(n2, v2, gv, bv);
         }
         if (tid == 0 && ok) {
@@ -182,7 +186,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         tc_fence_after();
         const int c = min(C, v.T - n * C);
-        const float igC = 1.f / s_gC;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
             // A (rows 0-63) into the solve space, P (rows 64-127) into the tile's second
@@ -192,27 +195,34 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_wait_ld();
             if (lrow < 64) {
                 const int r = lrow;
-                const float br = (r < c) ? S.bg[r] : 0.f;
+                const float br = S.rf[r];                  // zero past the chunk's rows
+                const float *cf = S.cf + (r >> 4) * 64;    // this row block's column factors
 #pragma unroll
                 for (int s4 = 0; s4 < 32; s4 += 4) {
                     const int s0 = half * 32 + s4;
-                    const float4 ig4 = *reinterpret_cast<const float4 *>(&S.ig[s0]);
+                    const float4 f4 = *reinterpret_cast<const float4 *>(&cf[s0]);
                     float4 o;
-                    o.x = (s0 + 0 < r) ? br * x[s4 + 0] * ig4.x : 0.f;
-                    o.y = (s0 + 1 < r) ? br * x[s4 + 1] * ig4.y : 0.f;
-                    o.z = (s0 + 2 < r) ? br * x[s4 + 2] * ig4.z : 0.f;
-                    o.w = (s0 + 3 < r) ? br * x[s4 + 3] * ig4.w : 0.f;
+                    o.x = (s0 + 0 < r) ? br * x[s4 + 0] * f4.x : 0.f;
+                    o.y = (s0 + 1 < r) ? br * x[s4 + 1] * f4.y : 0.f;
+                    o.z = (s0 + 2 < r) ? br * x[s4 + 2] * f4.z : 0.f;
+                    o.w = (s0 + 3 < r) ? br * x[s4 + 3] * f4.w : 0.f;
                     *reinterpret_cast<float4 *>(&As[r * LDA + s0]) = o;
                 }
             } else {
                 const int r = lrow - 64;
+                const float pr = S.pf[r];                  // zero past the chunk's rows
+                const float *cf = S.cf + (r >> 4) * 64;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     float p8[8];
+                    const int sb = half * 32 + q4 * 8;
+                    const float4 fa = *reinterpret_cast<const float4 *>(&cf[sb]);
+                    const float4 fb = *reinterpret_cast<const float4 *>(&cf[sb + 4]);
+                    const float f8[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int s = half * 32 + q4 * 8 + e;
-                        p8[e] = (s <= r && r < c) ? x[q4 * 8 + e] * igC : 0.f;
+                        const int s = sb + e;
+                        p8[e] = (s <= r) ? pr * x[q4 * 8 + e] * f8[e] : 0.f;
                     }
                     uint4 u;
                     u.x = pack_bf16x2(p8[0], p8[1]);

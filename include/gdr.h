@@ -43,8 +43,10 @@
  *     any T >= 0 (a ragged last chunk is masked).  Others: GDR_ERR_UNSUPPORTED.
  *   - Range rule: chunk * (-ln a_min) must not exceed 80, the worst in-tile
  *     cumulative log-decay the pages' range argument allows (section 3.1 of
- *     the first page above); otherwise GDR_ERR_RANGE.  a_min must lie in
- *     (0, 1]: GDR_ERR_INVALID_ARG otherwise.
+ *     the first page above); otherwise GDR_ERR_RANGE.  The two-kernel
+ *     workspace path below applies it over a 16-token tile instead of the
+ *     chunk: 16 * (-ln a_min) <= 80.  a_min must lie in (0, 1]:
+ *     GDR_ERR_INVALID_ARG otherwise.
  */
 #ifndef GDR_H
 #define GDR_H
@@ -60,7 +62,7 @@ typedef enum {
     GDR_OK = 0,
     GDR_ERR_INVALID_ARG = 1,  /* null pointer, negative size, a_min out of (0,1] */
     GDR_ERR_UNSUPPORTED = 2,  /* shape or dtype this build does not implement   */
-    GDR_ERR_RANGE = 3,        /* chunk * (-ln a_min) > 80                        */
+    GDR_ERR_RANGE = 3,        /* chunk (or tile) * (-ln a_min) > 80              */
     GDR_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed            */
     GDR_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up              */
 } gdr_status_t;
@@ -237,13 +239,17 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
 /*
  * The two-kernel prefill: a caller-owned workspace lets the preparation of
  * every chunk -- [K;Q]K^T, A, the triangular solve T = (I + A)^-1, Lb =
- * strict_lower(T) diag(beta) and P = lower_incl(Q K^T) / gamma_C ("What a
- * Trillion-Parameter MoE Model Reveals About the Next Stage of LLM Scaling",
- * sections 3.1-3.3) -- run as one fully parallel kernel that writes a 16 KB
- * bf16 tile per chunk, so that the second kernel, the sequential state chain
- * with the outputs, does nothing else.  Same arithmetic and results as
- * gdr_chunk_fwd (the tiles are the bf16 operands the fused kernels compute in
- * shared memory).
+ * strict_lower(T) diag(beta) and P = lower_incl(D o Q K^T) with D[r][s] =
+ * gamma_r / gamma_s ("What a Trillion-Parameter MoE Model Reveals About the
+ * Next Stage of LLM Scaling", sections 3.1-3.3) -- run as one fully parallel
+ * kernel that writes a 16 KB bf16 tile per chunk, so that the second kernel,
+ * the sequential state chain with the outputs, does nothing else.  Same
+ * method and results as gdr_chunk_fwd, within the bf16 tolerance.  The
+ * preparation applies D as the diagonal scalings of the pages' 16-token tiles
+ * (reference points every 16 rows) and the chain uses only factors at most 1,
+ * so this path's range rule is 16 * (-ln a_min) <= 80 (a_min >= e^-5) or
+ * 16 * (-g_min) <= 80 (g_min >= -5): the decay over a 64-token chunk may fall
+ * far below fp32's range.
  *
  * gdr_chunk_fwd_workspace_size: bytes of workspace the two-kernel path needs
  *   for these arguments (B * H * ceil(T / 64) tiles of 16 KB), or 0 where it
@@ -254,8 +260,9 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  *   shared with a call still running on another stream; its contents on entry
  *   and exit are scratch.  With a null workspace, one that is too small, or
  *   arguments the two-kernel path does not take, the call is exactly
- *   gdr_chunk_fwd (the single-launch fused or staged path).  Two launches,
- *   asynchronous on `stream`; errors as gdr_chunk_fwd.
+ *   gdr_chunk_fwd (the single-launch fused or staged path, with its chunk
+ *   range rule).  Two launches, asynchronous on `stream`; errors as
+ *   gdr_chunk_fwd.
  * gdr_chunk_fwd_varlen_workspace_size / gdr_chunk_fwd_varlen_ws: the same for
  *   packed sequences; the workspace holds H * (total_T / 64 + S + 1) tiles
  *   (sequence s starts at tile total offset cu_seqlens[s] / 64 + s of its head).
@@ -292,9 +299,10 @@ int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float 
  *   GDR_DECAY_LOG:    log alpha = g_min sigmoid(g), bound = g_min <= 0 (the pages'
  *                     own form; g_min = -5 with 16-token chunks is their setting).
  * The range rule applies to both: chunk * (-ln a_min) or chunk * (-g_min) must not
- * exceed 80 (GDR_ERR_RANGE otherwise), so g_min = -5 takes chunk 16 (the staged
- * kernels), and a bound with chunk 64 allowed (g_min >= -1.25) also takes the
- * fused and two-kernel paths.
+ * exceed 80 (GDR_ERR_RANGE otherwise), over a 16-token tile on the two-kernel
+ * workspace path.  So the pages' setting g_min = -5 runs on the two-kernel path
+ * (bf16, d = 128, chunk 64, with a workspace) or with chunk 16 on the staged
+ * kernels; the single-launch fused kernels take g_min >= -1.25.
  *
  * gdr_chunk_fwd_ex: gdr_chunk_fwd_ws with the decay chosen by (decay, bound);
  *   workspace may be NULL (the single-launch or staged path).

@@ -173,6 +173,29 @@ def test_chunk_fwd_ex_rejects(lib, kw, code):
     assert ex(lib, **kw) == code
 
 
+def test_workspace_path_range_rule(lib):
+    """The two-kernel workspace path applies the range rule over a 16-token tile (its
+    preparation splits the decay at 16-row reference points), the other paths over the
+    chunk: with a workspace, g_min = -5 and a floor of 0.05 pass at chunk 64 (the null q
+    is then what fails), one step beyond the tile bound is GDR_ERR_RANGE."""
+    big = 1 << 40
+    assert ex(lib, chunk=64, bound=-5.0, ws=P, wsb=big, q=None) == 1
+    assert ex(lib, chunk=64, bound=-5.01, ws=P, wsb=big) == 3
+    assert ex(lib, chunk=64, bound=-5.0, ws=P, wsb=16) == 3      # too small: single-launch rule
+    assert ex(lib, decay=0, bound=0.05, chunk=64, ws=P, wsb=big, q=None) == 1
+    assert ex(lib, decay=0, bound=0.006, chunk=64, ws=P, wsb=big) == 3   # 16 * 5.12 > 80
+    wp = lib.gdr_chunk_fwd_ws_path
+    wp.argtypes = [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int]
+    wp.restype = ctypes.c_int
+    fp = lib.gdr_chunk_fwd_path
+    fp.argtypes = [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int]
+    fp.restype = ctypes.c_int
+    assert wp(1, 2, 300, 128, 128, 64, 0.05, 1) in (4, 5)
+    assert fp(1, 2, 300, 128, 128, 64, 0.05, 1) == -1
+    assert wp(1, 2, 300, 128, 128, 64, 0.006, 1) == -1
+    assert wp(1, 2, 300, 128, 128, 64, 0.95, 1) in (4, 5)
+
+
 def test_decode_ex_rejects(lib):
     d = lib.gdr_decode_step_ex
     d.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_float] + [ctypes.c_void_p] * 2 + \

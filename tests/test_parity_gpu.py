@@ -229,6 +229,63 @@ def test_log_decay_fused_paths(variant):
     assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
 
 
+@pytest.mark.parametrize("variant", ["chain2", "chain1"])
+@pytest.mark.parametrize("decay,bound", [("log", -5.0), ("affine", 0.05)])
+@pytest.mark.parametrize("T", [209, 700])
+def test_wide_range_two_kernel(variant, decay, bound, T):
+    """The pages' own setting, log alpha = -5 sigmoid(g), and a linear-domain floor of
+    0.05 on the two-kernel path, whose range rule spans a 16-token tile: over a 64-token
+    chunk the decay here falls to about e^-160, so gamma and gamma_C underflow fp32 and
+    1/gamma would overflow -- the preparation's 16-row reference points and the chain's
+    factors of at most 1 must still give the oracle's result.  Ragged last chunk, several
+    chunks, both chain splits."""
+    w = I.PREFILL.with_(B=1, H=2, T=T)
+    x = to(I.prefill_inputs(w), "cuda")
+    with path_variant(variant) as ws:
+        out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], bound,
+                                 x["init_state"], decay=decay, workspace=ws)
+    torch.cuda.synchronize()
+    assert gdr.last_device_error() == 0
+    ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), bound,
+                        x["init_state"].cpu(), decay=decay)
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    assert rel(out, ro) <= TOL["bf16"], rel(out, ro)
+    assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
+
+
+def test_wide_range_needs_the_workspace_path():
+    """Without a workspace the single-launch kernels keep the chunk-wide range rule."""
+    w = I.PREFILL.with_(B=1, H=1, T=64)
+    x = to(I.prefill_inputs(w), "cuda")
+    with pytest.raises(gdr.GdrError):
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], -5.0, None, decay="log",
+                      workspace=None)
+
+
+@pytest.mark.parametrize("variant", ["chain2", "chain1"])
+def test_wide_range_varlen(variant):
+    """Packed sequences on the two-kernel path with a floor of 0.05 (chunk-wide decay
+    far below fp32's range), each sequence against the oracle on its own."""
+    w = I.PREFILL.with_(H=2)
+    lengths = [1, 65, 0, 200, 130]
+    x = I.varlen_inputs(w, lengths, device="cuda")
+    with path_variant(variant) as ws:
+        out, fin = gdr.chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.05,
+                                        x["cu_seqlens"], x["init_state"], workspace=ws)
+    torch.cuda.synchronize()
+    cu = x["cu_seqlens"].tolist()
+    for s, xs in enumerate(x["seqs"]):
+        if lengths[s] == 0:
+            assert torch.equal(fin[s], x["init_state"][s])
+            continue
+        cpu = {n: (None if t is None else t.cpu()) for n, t in xs.items()}
+        ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], 0.05,
+                            cpu["init_state"])
+        e_o = rel(out[cu[s]:cu[s + 1]].cpu(), torch.as_tensor(ro)[0].transpose(0, 1))
+        e_f = rel(fin[s].cpu(), torch.as_tensor(rf)[0])
+        assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"], (s, e_o, e_f)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_log_decay_decode(dtype):
     w = I.DECODE.with_(B=8, H=4, dtype=dtype)
