@@ -13,6 +13,9 @@ Contents
                   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
                   o_t = S_t q_t.
 * ``decode``   -- one step of the same recurrence, in place on the state.
+* ``bwd``      -- the gradients of L = <d_out, out> + <d_final, final_state> with
+                  respect to q, k, v, g, beta and the initial state: reverse-mode
+                  differentiation of the token loop as written (C, fp64).
 * ``alpha``    -- the lower-bounded decay itself: the linear-domain floor a_min, or
                   (decay="log") the pages' log-domain form alpha = exp(g_min sigmoid(g)).
 * ``chunkwise`` (module) -- the chunked reformulation in numpy fp64, used to
@@ -66,6 +69,10 @@ def _load():
                                            f32p, f64p, f64p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int]
+            lib.gdr_oracle_bwd.restype = ctypes.c_int
+            lib.gdr_oracle_bwd.argtypes = [f32p] * 5 + [ctypes.c_double] + [f32p] * 3 + \
+                [f64p] * 6 + [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_int]
             lib.gdr_oracle_decode.restype = ctypes.c_int
             lib.gdr_oracle_decode.argtypes = [f32p, f32p, f32p, f32p, f32p, ctypes.c_double,
                                               f64p, f64p, ctypes.c_int, ctypes.c_int,
@@ -166,6 +173,47 @@ def decode(q, k, v, g, beta, a_min: float, state: np.ndarray, *, nthreads: int |
     if rc != 0:
         raise RuntimeError(f"gdr_oracle_decode failed with code {rc}")
     return out
+
+
+def bwd(q, k, v, g, beta, a_min: float, init_state=None, d_out=None, d_final=None, *,
+        nthreads: int | None = None, decay: str = "affine"):
+    """Gradients of L = sum <d_out, out> + <d_final, final_state> for the forward of
+    ``fwd`` with the same arguments.  d_out [B,H,T,dv] and d_final [B,H,dk,dv] may be
+    None (zero).  Returns (dq, dk, dv, dg, dbeta, dinit), fp64, shaped like q, k, v, g,
+    beta and the initial state."""
+    q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != (B, H, T, dk) or v.shape != (B, H, T, dv):
+        raise ValueError("q/k/v shape mismatch")
+    if g.shape != (B, H, T) or beta.shape != (B, H, T):
+        raise ValueError("g/beta shape mismatch")
+    init = None if init_state is None else _f32(init_state)
+    dout = None if d_out is None else _f32(d_out)
+    dfin = None if d_final is None else _f32(d_final)
+    if init is not None and init.shape != (B, H, dk, dv):
+        raise ValueError("init_state shape mismatch")
+    if dout is not None and dout.shape != (B, H, T, dv):
+        raise ValueError("d_out shape mismatch")
+    if dfin is not None and dfin.shape != (B, H, dk, dv):
+        raise ValueError("d_final shape mismatch")
+    gq = np.empty((B, H, T, dk), np.float64)
+    gk = np.empty((B, H, T, dk), np.float64)
+    gv = np.empty((B, H, T, dv), np.float64)
+    gg = np.empty((B, H, T), np.float64)
+    gb = np.empty((B, H, T), np.float64)
+    gi = np.empty((B, H, dk, dv), np.float64)
+    lib = _load()
+    f32, f64 = ctypes.c_float, ctypes.c_double
+    opt = lambda a: None if a is None else _ptr(a, f32)
+    rc = lib.gdr_oracle_bwd(_ptr(q, f32), _ptr(k, f32), _ptr(v, f32), _ptr(g, f32),
+                            _ptr(beta, f32), float(a_min), opt(init), opt(dout), opt(dfin),
+                            _ptr(gq, f64), _ptr(gk, f64), _ptr(gv, f64), _ptr(gg, f64),
+                            _ptr(gb, f64), _ptr(gi, f64), B, H, T, dk, dv,
+                            int(nthreads or os.cpu_count() or 1), DECAY[decay])
+    if rc != 0:
+        raise RuntimeError(f"gdr_oracle_bwd failed with code {rc}")
+    return gq, gk, gv, gg, gb, gi
 
 
 def rel_l2(x, ref) -> float:

@@ -33,7 +33,10 @@
  * Parity status: every function here is pinned by the CPU tests (explicit
  * unrolled matrix products, the orthonormal-key write/read invariant, closed
  * forms for beta = 0 and a_min = 1, a hand-worked two-step case, and agreement
- * with an independent chunkwise reformulation).
+ * with an independent chunkwise reformulation).  The backward (gdr_oracle_bwd)
+ * is pinned by central finite differences of the forward loss for every input
+ * element, by exactness in the inputs the loss is linear in (q, v, the initial
+ * state), and by the pure-decay closed form at beta = 0.
  */
 #include <math.h>
 #include <pthread.h>
@@ -291,6 +294,258 @@ int gdr_oracle_decode(const float *q, const float *k, const float *v,
         started = i;
     }
     if (decode_worker(&jb) != NULL)
+        rc = -2;
+    for (int i = 1; i <= started; ++i) {
+        void *r = NULL;
+        pthread_join(th[i], &r);
+        if (r != NULL)
+            rc = -2;
+    }
+    free(th);
+    return rc;
+}
+
+/* ------------------------------------------------------------------ backward
+ *
+ * The gradient of L = sum_t <dout_t, o_t> + <dfinal, M_T> with respect to
+ * every input, by reverse-mode differentiation of the token loop above: the
+ * forward steps are replayed as written and each step is then undone in
+ * reverse order.  With S = S_{t-1}, a = alpha_t, b = beta_t, the forward step
+ * is
+ *     u = S k_t,   r = v_t - a u,   w = b r,   S_t = a S + w k_t^T,   o_t = S_t q_t
+ * (S_t = a S (I - b k k^T) + b v k^T written out), so for G = dL/dS_t:
+ *     G      += dout_t q_t^T                      (o_t = S_t q_t)
+ *     dq_t    = S_t^T dout_t
+ *     dw      = G k_t,   dk_t = G^T w + S^T du,   du = -a b dw
+ *     dv_t    = b dw,    dbeta_t = dw . r
+ *     dalpha  = <G, S> - b (dw . u),   dg_t = dalpha * dalpha/dg
+ *     dL/dS_{t-1} = a G + du k_t^T
+ * and the initial state's gradient is dL/dS_0.  The states S_{t-1} are kept at
+ * every 64th token and the steps between two of them replayed from there,
+ * which changes no value: the replay repeats the forward's arithmetic.
+ */
+#define ORACLE_BWD_SEG 64
+
+/* d alpha / d g for the two decay forms. */
+static double decay_dalpha(int decay, double g, double bound)
+{
+    const double s = 1.0 / (1.0 + exp(-g));
+    if (decay == 1)
+        return gdr_oracle_alpha_log(g, bound) * bound * s * (1.0 - s);
+    return (1.0 - bound) * s * (1.0 - s);
+}
+
+/* One forward step of the loop above on S (dv x dk), in place; u is scratch. */
+static void oracle_step(double *S, const float *kt, const float *vt, double a, double b,
+                        int dk, int dv, double *u)
+{
+    for (int j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < dk; ++i)
+            acc += S[(int64_t)j * dk + i] * (double)kt[i];
+        u[j] = acc;
+    }
+    for (int j = 0; j < dv; ++j) {
+        const double uj = u[j];
+        const double vj = (double)vt[j];
+        for (int i = 0; i < dk; ++i) {
+            const double ki = (double)kt[i];
+            double *s = &S[(int64_t)j * dk + i];
+            *s = a * (*s - b * uj * ki) + b * vj * ki;
+        }
+    }
+}
+
+/*
+ * Backward of one head.  Inputs as oracle_head plus dout [T][dv] (or NULL =
+ * zero) and dfinal [dk][dv] (M layout, or NULL = zero).  Outputs (fp64):
+ * gq, gk [T][dk]; gv [T][dv]; gg, gb [T]; ginit [dk][dv] (M layout).
+ * Scratch: ck ((T / SEG + 1) states), st (SEG + 1 states), G (one state),
+ * vec (4 * max(dk, dv)).  Returns 0.
+ */
+static int oracle_head_bwd(const float *q, const float *k, const float *v, const float *g,
+                           const float *beta, int decay, double bound, const float *init,
+                           const float *dout, const float *dfinal, double *gq, double *gk,
+                           double *gv, double *gg, double *gb, double *ginit, int64_t T,
+                           int dk, int dv, double *ck, double *st, double *G, double *vec)
+{
+    const int64_t SZ = (int64_t)dk * dv;
+    double *u = vec, *w = vec + dv, *dw = vec + 2 * dv, *du = vec + 3 * dv;
+
+    /* forward, keeping S_{t-1} at every SEG-th token */
+    double *S = st;
+    for (int j = 0; j < dv; ++j)
+        for (int i = 0; i < dk; ++i)
+            S[(int64_t)j * dk + i] = init ? (double)init[(int64_t)i * dv + j] : 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        if (t % ORACLE_BWD_SEG == 0)
+            memcpy(ck + (t / ORACLE_BWD_SEG) * SZ, S, sizeof(double) * (size_t)SZ);
+        oracle_step(S, k + t * dk, v + t * dv, decay_alpha(decay, (double)g[t], bound),
+                    (double)beta[t], dk, dv, u);
+    }
+
+    /* G = dL/dS_T */
+    for (int j = 0; j < dv; ++j)
+        for (int i = 0; i < dk; ++i)
+            G[(int64_t)j * dk + i] = dfinal ? (double)dfinal[(int64_t)i * dv + j] : 0.0;
+
+    const int64_t nseg = (T + ORACLE_BWD_SEG - 1) / ORACLE_BWD_SEG;
+    for (int64_t sg = nseg - 1; sg >= 0; --sg) {
+        const int64_t t0 = sg * ORACLE_BWD_SEG;
+        const int64_t t1 = t0 + ORACLE_BWD_SEG < T ? t0 + ORACLE_BWD_SEG : T;
+        /* replay: st[m] = S_{t0 + m - 1}, m = 0 .. t1 - t0 */
+        memcpy(st, ck + sg * SZ, sizeof(double) * (size_t)SZ);
+        for (int64_t t = t0; t < t1; ++t) {
+            memcpy(st + (t - t0 + 1) * SZ, st + (t - t0) * SZ, sizeof(double) * (size_t)SZ);
+            oracle_step(st + (t - t0 + 1) * SZ, k + t * dk, v + t * dv,
+                        decay_alpha(decay, (double)g[t], bound), (double)beta[t], dk, dv, u);
+        }
+        for (int64_t t = t1 - 1; t >= t0; --t) {
+            const double *Sp = st + (t - t0) * SZ;      /* S_{t-1} */
+            const double *St = st + (t - t0 + 1) * SZ;  /* S_t */
+            const float *kt = k + t * dk, *qt = q + t * dk, *vt = v + t * dv;
+            const float *dot = dout ? dout + t * dv : NULL;
+            const double a = decay_alpha(decay, (double)g[t], bound);
+            const double b = (double)beta[t];
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i)
+                    acc += Sp[(int64_t)j * dk + i] * (double)kt[i];
+                u[j] = acc;
+                w[j] = b * ((double)vt[j] - a * acc);
+            }
+            /* o_t = S_t q_t */
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                if (dot)
+                    for (int j = 0; j < dv; ++j)
+                        acc += St[(int64_t)j * dk + i] * (double)dot[j];
+                gq[t * dk + i] = acc;
+            }
+            if (dot)
+                for (int j = 0; j < dv; ++j)
+                    for (int i = 0; i < dk; ++i)
+                        G[(int64_t)j * dk + i] += (double)dot[j] * (double)qt[i];
+            /* S_t = a S_{t-1} + w k_t^T */
+            double dalpha = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) {
+                    acc += G[(int64_t)j * dk + i] * (double)kt[i];
+                    dalpha += G[(int64_t)j * dk + i] * Sp[(int64_t)j * dk + i];
+                }
+                dw[j] = acc;
+            }
+            /* w = b (v - a u) */
+            double dbeta = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                gv[t * dv + j] = b * dw[j];
+                dbeta += dw[j] * ((double)vt[j] - a * u[j]);
+                dalpha -= b * dw[j] * u[j];
+                du[j] = -a * b * dw[j];
+            }
+            /* u = S_{t-1} k_t; w k_t^T */
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j)
+                    acc += G[(int64_t)j * dk + i] * w[j] + Sp[(int64_t)j * dk + i] * du[j];
+                gk[t * dk + i] = acc;
+            }
+            gb[t] = dbeta;
+            gg[t] = dalpha * decay_dalpha(decay, (double)g[t], bound);
+            /* dL/dS_{t-1} = a G + du k_t^T */
+            for (int j = 0; j < dv; ++j)
+                for (int i = 0; i < dk; ++i)
+                    G[(int64_t)j * dk + i] = a * G[(int64_t)j * dk + i] + du[j] * (double)kt[i];
+        }
+    }
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j)
+            ginit[(int64_t)i * dv + j] = G[(int64_t)j * dk + i];
+    return 0;
+}
+
+typedef struct {
+    const float *q, *k, *v, *g, *beta, *init, *dout, *dfinal;
+    int decay;
+    double bound;
+    double *gq, *gk, *gv, *gg, *gb, *ginit;
+    int B, H, dk, dv;
+    int64_t T;
+    int64_t next;
+} bwd_job_t;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job_t *jb = (bwd_job_t *)arg;
+    const int64_t nbh = (int64_t)jb->B * jb->H, T = jb->T;
+    const int64_t SZ = (int64_t)jb->dk * jb->dv;
+    const int64_t nck = T / ORACLE_BWD_SEG + 1;
+    const int mx = jb->dk > jb->dv ? jb->dk : jb->dv;
+    double *ck = (double *)malloc(sizeof(double) * (size_t)(nck * SZ));
+    double *st = (double *)malloc(sizeof(double) * (size_t)((ORACLE_BWD_SEG + 1) * SZ));
+    double *G = (double *)malloc(sizeof(double) * (size_t)SZ);
+    double *vec = (double *)malloc(sizeof(double) * (size_t)(4 * mx));
+    void *rc = NULL;
+    if (!ck || !st || !G || !vec) {
+        rc = (void *)1;
+        goto done;
+    }
+    for (;;) {
+        const int64_t bh = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (bh >= nbh)
+            break;
+        oracle_head_bwd(jb->q + bh * T * jb->dk, jb->k + bh * T * jb->dk, jb->v + bh * T * jb->dv,
+                        jb->g + bh * T, jb->beta + bh * T, jb->decay, jb->bound,
+                        jb->init ? jb->init + bh * SZ : NULL,
+                        jb->dout ? jb->dout + bh * T * jb->dv : NULL,
+                        jb->dfinal ? jb->dfinal + bh * SZ : NULL,
+                        jb->gq + bh * T * jb->dk, jb->gk + bh * T * jb->dk,
+                        jb->gv + bh * T * jb->dv, jb->gg + bh * T, jb->gb + bh * T,
+                        jb->ginit + bh * SZ, T, jb->dk, jb->dv, ck, st, G, vec);
+    }
+done:
+    free(ck);
+    free(st);
+    free(G);
+    free(vec);
+    return rc;
+}
+
+/*
+ * Backward over [B,H,T]: the gradients of L = sum <d_out, out> + <d_final,
+ * final_state> with respect to q, k [B,H,T,dk], v [B,H,T,dv], g, beta [B,H,T]
+ * and the initial state [B,H,dk,dv] (M layout), for the forward of
+ * gdr_oracle_fwd with the same (bound, decay).  d_out and d_final may be NULL
+ * (zero).  Heads are spread over nthreads host threads.  Returns 0 on
+ * success, -1 on bad arguments, -2 if memory ran out.
+ */
+int gdr_oracle_bwd(const float *q, const float *k, const float *v, const float *g,
+                   const float *beta, double bound, const float *init_state, const float *d_out,
+                   const float *d_final, double *gq, double *gk, double *gv, double *gg,
+                   double *gbeta, double *ginit, int B, int H, int64_t T, int dk, int dv,
+                   int nthreads, int decay)
+{
+    if (!q || !k || !v || !g || !beta || !gq || !gk || !gv || !gg || !gbeta || !ginit ||
+        B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    bwd_job_t jb = {q, k, v, g, beta, init_state, d_out, d_final, decay, bound,
+                    gq, gk, gv, gg, gbeta, ginit, B, H, dk, dv, T, 0};
+    const int64_t nbh = (int64_t)B * H;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > nbh)
+        nthreads = nbh > 0 ? (int)nbh : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th)
+        return -2;
+    int rc = 0, started = 0;
+    for (int i = 1; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, bwd_worker, &jb) != 0)
+            break;
+        started = i;
+    }
+    if (bwd_worker(&jb) != NULL)
         rc = -2;
     for (int i = 1; i <= started; ++i) {
         void *r = NULL;

@@ -260,11 +260,85 @@ def check_log_chunkwise_agrees():
         assert np.max(np.abs(fin - fc)) < 1e-9 * scale, (T, C)
 
 
+# ---- the backward: gradients of L = <d_out, out> + <d_final, final_state>
+
+def _loss(args, dout, dfin, bound, decay):
+    out, fin = oracle.fwd(*args[:5], bound, args[5], decay=decay)
+    return float((out * dout).sum() + (fin * dfin).sum())
+
+
+def _bwd_case(rng, T, dk, dv, bound, decay):
+    q, k, v, g, beta, M0 = _rand_inputs(rng, 1, 1, T, dk, dv)
+    dout = rng.standard_normal((1, 1, T, dv)).astype(np.float32)
+    dfin = rng.standard_normal((1, 1, dk, dv)).astype(np.float32)
+    return [q, k, v, g, beta, M0], dout, dfin
+
+
+def check_bwd_finite_differences():
+    # every gradient element against a central difference of the forward loss (fp32
+    # inputs perturbed by 2^-10, the exact perturbation as denominator); one case
+    # crosses the 64-token replay boundary, both decay forms
+    rng = np.random.default_rng(61)
+    for (T, dk, dv, bound, decay) in ((5, 3, 4, 0.9, "affine"), (6, 2, 3, -2.0, "log"),
+                                      (70, 2, 2, 0.8, "affine")):
+        args, dout, dfin = _bwd_case(rng, T, dk, dv, bound, decay)
+        grads = oracle.bwd(*args[:5], bound, args[5], dout, dfin, decay=decay)
+        for n, (a, gr) in enumerate(zip(args, grads)):
+            flat = a.reshape(-1)
+            fd = np.empty(flat.size)
+            for idx in range(flat.size):
+                x0 = flat[idx]
+                flat[idx] = x0 + np.float32(2.0 ** -10)
+                lp = _loss(args, dout, dfin, bound, decay)
+                xp = float(flat[idx])
+                flat[idx] = x0 - np.float32(2.0 ** -10)
+                lm = _loss(args, dout, dfin, bound, decay)
+                xm = float(flat[idx])
+                flat[idx] = x0
+                fd[idx] = (lp - lm) / (xp - xm)
+            err = np.max(np.abs(fd - gr.reshape(-1))) / max(1e-30, np.max(np.abs(fd)))
+            assert err < 1e-5, (T, decay, n, err)
+
+
+def check_bwd_exact_in_linear_inputs():
+    # L is exactly linear in q, in v and in the initial state (each alone): a finite
+    # step of any size changes L by exactly <grad, step>
+    rng = np.random.default_rng(62)
+    args, dout, dfin = _bwd_case(rng, 40, 8, 6, 0.85, "affine")
+    grads = oracle.bwd(*args[:5], 0.85, args[5], dout, dfin)
+    l0 = _loss(args, dout, dfin, 0.85, "affine")
+    for n in (0, 2, 5):
+        step = rng.standard_normal(args[n].shape).astype(np.float32)
+        moved = list(args)
+        moved[n] = (args[n] + step).astype(np.float32)
+        actual = moved[n].astype(np.float64) - args[n].astype(np.float64)
+        dl = _loss(moved, dout, dfin, 0.85, "affine") - l0
+        pred = float((grads[n] * actual).sum())
+        assert abs(dl - pred) < 1e-10 * max(1.0, abs(dl)), (n, dl, pred)
+
+
+def check_bwd_zero_cotangent_and_pure_decay():
+    # no cotangent gives zero gradients; with beta = 0 and only d_final, the state is
+    # pure decay M_T = prod(alpha) M_0: dinit = prod(alpha) d_final exactly, and
+    # dv = 0 (beta scales every write)
+    rng = np.random.default_rng(63)
+    args, dout, dfin = _bwd_case(rng, 9, 4, 5, 0.7, "affine")
+    for gr in oracle.bwd(*args[:5], 0.7, args[5], None, None):
+        assert not np.any(gr)
+    args[4] = np.zeros_like(args[4])
+    gq, gk, gv, gg, gb, gi = oracle.bwd(*args[:5], 0.7, args[5], None, dfin)
+    pa = float(np.prod(oracle.alpha(args[3].reshape(-1), 0.7)))
+    assert np.allclose(gi, pa * dfin.astype(np.float64), rtol=1e-13, atol=0)
+    assert not np.any(gv) and not np.any(gq)
+
+
 ALL_CHECKS = [check_alpha_limits, check_hand_worked, check_unrolled_products,
               check_orthonormal_write_read, check_beta_zero_is_pure_decay,
               check_a_min_one_ignores_g, check_chunkwise_agrees,
               check_split_resume_and_decode, check_log_alpha_limits,
-              check_log_decay_limits_match_linear_form, check_log_chunkwise_agrees]
+              check_log_decay_limits_match_linear_form, check_log_chunkwise_agrees,
+              check_bwd_finite_differences, check_bwd_exact_in_linear_inputs,
+              check_bwd_zero_cotangent_and_pure_decay]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda f: f.__name__)
@@ -350,6 +424,24 @@ MUTANTS = [
      "return 1.0 + g_min / (1.0 + exp(-g));"),
     ("log form ignored by the forward", "return decay == 1 ? gdr_oracle_alpha_log(g, bound)",
      "return decay == 2 ? gdr_oracle_alpha_log(g, bound)"),
+    ("bwd: query gradient read from S_{t-1}", "acc += St[(int64_t)j * dk + i] * (double)dot[j];",
+     "acc += Sp[(int64_t)j * dk + i] * (double)dot[j];"),
+    ("bwd: state gradient not decayed",
+     "G[(int64_t)j * dk + i] = a * G[(int64_t)j * dk + i] + du[j] * (double)kt[i];",
+     "G[(int64_t)j * dk + i] = G[(int64_t)j * dk + i] + du[j] * (double)kt[i];"),
+    ("bwd: correction path dropped from the key gradient",
+     "acc += G[(int64_t)j * dk + i] * w[j] + Sp[(int64_t)j * dk + i] * du[j];",
+     "acc += G[(int64_t)j * dk + i] * w[j];"),
+    ("bwd: sign of the decay's correction term", "dalpha -= b * dw[j] * u[j];",
+     "dalpha += b * dw[j] * u[j];"),
+    ("bwd: output cotangent not fed into the state",
+     "G[(int64_t)j * dk + i] += (double)dot[j] * (double)qt[i];",
+     "G[(int64_t)j * dk + i] += 0.0 * (double)qt[i];"),
+    ("bwd: log-form derivative without alpha",
+     "return gdr_oracle_alpha_log(g, bound) * bound * s * (1.0 - s);",
+     "return bound * s * (1.0 - s);"),
+    ("bwd: replay from the previous checkpoint", "memcpy(st, ck + sg * SZ,",
+     "memcpy(st, ck + (sg > 0 ? sg - 1 : 0) * SZ,"),
 ]
 
 
@@ -357,7 +449,8 @@ MUTANTS = [
 def _oracle_lib(path):
     lib = ctypes.CDLL(path)
     saved = oracle._load()
-    for name in ("gdr_oracle_alpha", "gdr_oracle_alpha_log", "gdr_oracle_fwd", "gdr_oracle_decode"):
+    for name in ("gdr_oracle_alpha", "gdr_oracle_alpha_log", "gdr_oracle_fwd", "gdr_oracle_decode",
+                 "gdr_oracle_bwd"):
         getattr(lib, name).restype = getattr(saved, name).restype
         getattr(lib, name).argtypes = getattr(saved, name).argtypes
     oracle._lib = lib
@@ -371,14 +464,19 @@ def _oracle_lib(path):
 def test_pins_catch_planted_mistakes(mutant, tmp_path):
     name, old, new = mutant
     src = open(os.path.join(os.path.dirname(oracle.__file__), "gdr_oracle.c")).read()
+    bwd_at = src.index("/* ------------------------------------------------------------------ backward")
     if "decode" in name:
         # only the copy inside the decode step
         idx = src.index("static void oracle_decode_one")
-        assert old in src[idx:], name
+        assert old in src[idx:bwd_at], name
         src = src[:idx] + src[idx:].replace(old, new, 1)
+    elif name.startswith("bwd:"):
+        assert old in src[bwd_at:], name
+        src = src[:bwd_at] + src[bwd_at:].replace(old, new)
     else:
-        assert old in src, name
-        src = src.replace(old, new)
+        # the forward loop (the backward replays its own copy of the step)
+        assert old in src[:bwd_at], name
+        src = src[:bwd_at].replace(old, new) + src[bwd_at:]
     c_path = tmp_path / "mutant.c"
     so_path = tmp_path / "mutant.so"
     c_path.write_text(src)
