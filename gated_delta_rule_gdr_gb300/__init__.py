@@ -69,6 +69,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_fwd_ws_path": [i, i, i, i, i, i, f, i],
         "gdr_chunk_fwd_ex": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_decode_step_ex": [vp, vp, vp, vp, vp, i, f, vp, vp, i, i, i, i, i, vp],
+        "gdr_chunk_bwd": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                          i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
         "gdr_chunk_decay": [vp, f, vp, i, i, i, vp],
@@ -85,7 +87,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
-    for name in ("gdr_chunk_fwd_workspace_size", "gdr_chunk_fwd_varlen_workspace_size"):
+    for name in ("gdr_chunk_fwd_workspace_size", "gdr_chunk_fwd_varlen_workspace_size",
+                 "gdr_chunk_bwd_workspace_size"):
         fn = getattr(lib, name)
         fn.argtypes = [i, i, i, i, i, i, i]
         fn.restype = sz
@@ -223,6 +226,41 @@ def chunk_fwd_varlen(q, k, v, g, beta, a_min: float, cu_seqlens, init_state=None
                                            dv, int(chunk), DTYPE[q.dtype], _ptr(ws), ws.numel(),
                                            _stream(q.device)), "gdr_chunk_fwd_varlen_ws")
     return out, final_state
+
+
+def chunk_bwd_workspace_size(B, H, T, dk, dv, chunk=64, dtype=torch.bfloat16) -> int:
+    """Bytes of workspace the backward needs (0 for empty work or unsupported shapes)."""
+    return int(load().gdr_chunk_bwd_workspace_size(B, H, T, dk, dv, chunk, DTYPE[dtype]))
+
+
+def chunk_bwd(q, k, v, g, beta, a_min: float, init_state, d_out, d_final=None, *,
+              chunk: int = 64, want_dinit: bool = True, workspace=None, decay: str = "affine"):
+    """Gradients of a loss through chunk_fwd: given d_out [B,H,T,dv] (q's dtype) and
+    d_final [B,H,dk,dv] fp32 or None, returns (dq, dk, dv, dg, dbeta, dinit) for the
+    forward with the same arguments (dinit None unless want_dinit).  workspace: None
+    (allocated here) or a uint8 CUDA tensor of at least chunk_bwd_workspace_size bytes."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype or d_out.dtype != q.dtype:
+        raise TypeError("q, k, v, d_out must share one dtype, float32 or bfloat16")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(init_state, "init_state"), _f32(d_final, "d_final")
+    if decay not in DECAY:
+        raise ValueError(f"unknown decay {decay!r}")
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg, db = torch.empty_like(g), torch.empty_like(beta)
+    dinit = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dinit else None
+    need = chunk_bwd_workspace_size(B, H, T, dk, dv, chunk, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    _check(lib.gdr_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), DECAY[decay],
+                             float(a_min), _ptr(init_state), _ptr(d_out), _ptr(d_final),
+                             _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db), _ptr(dinit),
+                             B, H, T, dk, dv, int(chunk), DTYPE[q.dtype], _ptr(workspace),
+                             workspace.numel(), _stream(q.device)), "gdr_chunk_bwd")
+    return dq, dk_, dv_, dg, db, dinit
 
 
 def decode_step(q, k, v, g, beta, a_min: float, state, *, out=None, decay: str = "affine"):

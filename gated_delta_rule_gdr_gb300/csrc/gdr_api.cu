@@ -362,6 +362,46 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
     return gdr::fused_uses_pair((int)BH) ? 3 : 2;
 }
 
+// ---- backward ----
+
+size_t gdr_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                    gdr_dtype_t dtype) {
+    if (B < 0 || H < 0 || T < 0 || !dtype_ok(dtype) || !gdr::bwd_supported(dk, dv, chunk)) return 0;
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0 || BH > 0x7fffffff || T == 0) return 0;
+    return gdr::bwd_workspace_bytes((int)BH, T, dk, dv, chunk);
+}
+
+gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, gdr_decay_t decay, float bound,
+                           const float *init_state, const void *d_out, const float *d_final,
+                           void *d_q, void *d_k, void *d_v, float *d_g, float *d_beta,
+                           float *d_init, int B, int H, int T, int dk, int dv, int chunk,
+                           gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    float d = 0.0f;
+    if (B < 0 || H < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!decay_param(decay, bound, &d)) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!gdr::bwd_supported(dk, dv, chunk)) return GDR_ERR_UNSUPPORTED;
+    if (!range_ok(d, chunk)) return GDR_ERR_RANGE;
+    const int64_t BH = (int64_t)B * H;
+    if (BH > 0x7fffffff || (int64_t)T * BH > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (BH == 0) return GDR_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > 0) {
+        if (!q || !k || !v || !g || !beta || !d_out || !d_q || !d_k || !d_v || !d_g || !d_beta)
+            return GDR_ERR_INVALID_ARG;
+        if (!workspace ||
+            workspace_bytes < gdr::bwd_workspace_bytes((int)BH, T, dk, dv, chunk) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 15))
+            return GDR_ERR_INVALID_ARG;
+    }
+    return from_cuda(gdr::launch_bwd(q, k, v, g, beta, d, init_state, d_out, d_final, d_q, d_k,
+                                     d_v, d_g, d_beta, d_init, (int)BH, T, dk, dv, chunk,
+                                     workspace, elem_of(dtype), s));
+}
+
 gdr_status_t gdr_last_device_error(void *stream) {
     unsigned word = 0;
     cudaError_t e = gdr::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &word);

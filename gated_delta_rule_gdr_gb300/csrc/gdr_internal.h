@@ -27,6 +27,15 @@ cudaError_t launch_output(const void *q, const void *k, const float *gamma, cons
 // final_state <- init (or zeros) for T == 0.
 cudaError_t launch_copy_state(const float *init, float *final_state, int64_t n, cudaStream_t s);
 
+// ---- backward of the chunked form (gdr_bwd.cu) ----
+bool bwd_supported(int dk, int dv, int C);
+size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C);
+cudaError_t launch_bwd(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float d, const float *init, const void *dout,
+                       const float *dfinal, void *dq, void *dk_out, void *dv_out, float *dg,
+                       float *dbeta, float *dinit, int BH, int T, int dk, int dv, int C,
+                       void *ws, Elem e, cudaStream_t s);
+
 // ---- single-token decode (gdr_decode.cu) ----
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float a_min, float *state, void *out, int N,

@@ -19,6 +19,9 @@ device, one generator per tensor seeded from (seed, tensor id)):
 
 Decode draws fresh q, k, v, g, beta every step from a seed derived from
 (seed, step); its starting state is N(0, 0.02).
+
+The backward takes cotangents: d_out ~ N(0, 1) in the compute dtype [B,H,T,dv] and
+d_final ~ N(0, 1) fp32 [B,H,dk,dv] (``cotangents``).
 """
 from __future__ import annotations
 
@@ -28,7 +31,8 @@ import math
 
 import torch
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "init": 6, "lengths": 7}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "init": 6, "lengths": 7,
+               "d_out": 8, "d_final": 9}
 
 
 @dataclass(frozen=True)
@@ -157,3 +161,13 @@ def varlen_lengths(w: Workload):
     u = torch.rand(w.B, generator=_gen("cpu", w.seed, "lengths"), dtype=torch.float64)
     lo, hi = math.log(16.0), math.log(float(w.T))
     return [int(round(math.exp(lo + (hi - lo) * float(x)))) for x in u]
+
+
+def cotangents(w: Workload, device="cpu"):
+    """Returns dict(d_out, d_final): the gradients of a loss with respect to the
+    prefill's output and final state, for the backward."""
+    d_out = torch.randn((w.B, w.H, w.T, w.dv), generator=_gen(device, w.seed, "d_out"),
+                        device=device, dtype=torch.float32).to(w.torch_dtype())
+    d_final = torch.randn((w.B, w.H, w.dk, w.dv), generator=_gen(device, w.seed, "d_final"),
+                          device=device, dtype=torch.float32)
+    return dict(d_out=d_out, d_final=d_final)

@@ -321,6 +321,41 @@ gdr_status_t gdr_decode_step_ex(const void *q, const void *k, const void *v, con
                                 void *stream);
 
 /*
+ * Backward of the chunked prefill: the gradients of a loss L with respect to
+ * every input of gdr_chunk_fwd, given dL/dout and dL/dfinal_state (the chain
+ * rule through the same chunk algebra, "What a Trillion-Parameter MoE Model
+ * Reveals About the Next Stage of LLM Scaling", sections 3.1-3.3, taken in
+ * reverse).  The forward's intermediates (the decay, the W tiles and the state
+ * at every chunk start) are recomputed from the inputs, then one sequential
+ * reverse pass over the chunks carries dL/dM, and one fully parallel pass
+ * forms every chunk's gradients.  fp32 arithmetic throughout.
+ *
+ * q, k, v, g, beta, (decay, bound), init_state: as gdr_chunk_fwd_ex (the
+ *          forward whose gradients are taken; init_state may be NULL = zeros).
+ * d_out    [B,H,T,dv] in dtype: dL/dout (required when T > 0).
+ * d_final  fp32 [B,H,dk,dv] (M layout) or NULL (zero): dL/dfinal_state.
+ * d_q, d_k [B,H,T,dk] and d_v [B,H,T,dv] in dtype; d_g, d_beta fp32 [B,H,T];
+ * d_init   fp32 [B,H,dk,dv] or NULL (not wanted): the gradients.  Every output
+ *          is overwritten (no accumulation into existing values).
+ * workspace  device memory of at least gdr_chunk_bwd_workspace_size bytes,
+ *          16-byte aligned, owned by the caller; scratch on entry and exit.
+ * Supported: dk in {32, 64, 128}, dv in {16, 32, 64, 128}, chunk in {16, 32,
+ * 64}, fp32 or bf16 (GDR_ERR_UNSUPPORTED otherwise); the range rule over the
+ * chunk (GDR_ERR_RANGE).  Five launches, asynchronous on `stream`.
+ * gdr_chunk_bwd_workspace_size returns 0 for unsupported arguments or empty
+ * work (T = 0 needs no workspace: d_init = d_final, or zeros).
+ */
+size_t gdr_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                    gdr_dtype_t dtype);
+gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, gdr_decay_t decay, float bound,
+                           const float *init_state, const void *d_out, const float *d_final,
+                           void *d_q, void *d_k, void *d_v, float *d_g, float *d_beta,
+                           float *d_init, int B, int H, int T, int dk, int dv, int chunk,
+                           gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word:
  * GDR_ERR_TIMEOUT if a kernel's bounded wait gave up since the last call,
  * GDR_ERR_CUDA if the stream reports an error, else GDR_OK.

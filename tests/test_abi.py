@@ -205,3 +205,45 @@ def test_decode_ex_rejects(lib):
     assert d(P, P, P, P, P, 3, -5.0, P, P, 1, 1, 128, 128, 1, None) == 1     # unknown mode
     assert d(P, P, P, P, P, 1, -5.0, P, P, 0, 4, 128, 128, 1, None) == 0     # empty
     assert d(P, P, P, P, P, 1, -5.0, None, P, 1, 1, 128, 128, 1, None) == 1  # no state
+
+
+def bwd(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, decay=0, bound=0.9, init=None, dout=P, dfin=None,
+             dq=P, dk_=P, dv_=P, dg=P, db=P, dinit=None, B=1, H=2, T=100, dk=64, dv=64,
+             chunk=64, dtype=0, ws=P, wsb=1 << 40, stream=None)
+    a.update(kw)
+    f = lib.gdr_chunk_bwd
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_float] + \
+        [ctypes.c_void_p] * 9 + [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                       ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return f(*(a[n] for n in ("q", "k", "v", "g", "beta", "decay", "bound", "init", "dout",
+                              "dfin", "dq", "dk_", "dv_", "dg", "db", "dinit", "B", "H", "T",
+                              "dk", "dv", "chunk", "dtype", "ws", "wsb", "stream")))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), 1), (dict(decay=5), 1), (dict(bound=0.0), 1),  # sizes, decay mode, floor
+    (dict(dtype=7), 2), (dict(dk=16), 2), (dict(dv=8), 2), (dict(chunk=128), 2),
+    (dict(bound=0.2), 3),                                        # 64 * -ln(0.2) > 80
+    (dict(decay=1, bound=-5.0), 3), (dict(decay=1, bound=-5.0, chunk=16, q=None), 1),
+    (dict(q=None), 1), (dict(dout=None), 1), (dict(dg=None), 1), (dict(db=None), 1),
+    (dict(ws=None), 1), (dict(wsb=1024), 1),                     # workspace missing / small
+    (dict(ws=ctypes.c_void_p(0x1008)), 1),                       # not 16-byte aligned
+    (dict(B=0), 0), (dict(H=0), 0),                              # no heads: nothing to do
+])
+def test_chunk_bwd_rejects(lib, kw, code):
+    """The backward's entry point validates everything before it enqueues anything."""
+    assert bwd(lib, **kw) == code
+
+
+def test_chunk_bwd_workspace_size(lib):
+    f = lib.gdr_chunk_bwd_workspace_size
+    f.argtypes = [ctypes.c_int] * 7
+    f.restype = ctypes.c_size_t
+    n = f(2, 3, 100, 128, 64, 64, 1)
+    # gamma, U, Wk, W, dR per token plus M_n and dM' per chunk, fp32
+    tok, st = 2 * 3 * 100, 2 * 3 * 2 * 128 * 64
+    assert n == 4 * (tok + 3 * tok * 64 + tok * 128 + 2 * st)
+    assert f(2, 3, 0, 128, 64, 64, 1) == 0 and f(0, 3, 10, 128, 64, 64, 1) == 0
+    assert f(1, 1, 10, 16, 64, 64, 1) == 0   # unsupported dk
