@@ -175,11 +175,18 @@ def time_steps(fn, K, W, flush, stream, prime=True):
     otherwise land inside the first step's device time).  The end-to-end legs run
     unprimed."""
     for _ in range(W):
+        if flush is not None:   # the timed steps' flush kernel is warm too
+            flush.zero_()
         fn(-1)
     torch.cuda.synchronize()
-    if prime and hasattr(torch.cuda, "_sleep"):
+    if prime:
         with torch.cuda.stream(stream):
-            torch.cuda._sleep(2_000_000)
+            if hasattr(torch.cuda, "_sleep"):
+                torch.cuda._sleep(2_000_000)
+            else:   # ~1 ms of device work by other means
+                a = torch.ones((4096, 4096), device=stream.device, dtype=torch.bfloat16)
+                for _ in range(8):
+                    a = a @ a * (1.0 / 4096)
     times = []
     for i in range(K):
         if flush is not None:
@@ -296,6 +303,50 @@ def bench_decode(gdr, w, K, W, dev, flush, stream):
 
     ms_e2e = time_steps(e2e_step, K, 2, None, stream, prime=False)
     return ms, ms_e2e, h2d, d2h
+
+
+def backward_algorithmic(w: I.Workload):
+    """Bytes one backward step must move at the least: q, k, v, g, beta and d_out in,
+    dq, dk, dv, dg, dbeta out per token and head; the initial state and d_final in and
+    the initial state's gradient out per head."""
+    es = 2 if w.dtype == "bf16" else 4
+    per_tok = (2 * w.dk + w.dv) * es + w.dv * es + (2 * w.dk + w.dv) * es + 4 * 4
+    return w.B * w.H * (w.T * per_tok + 3 * w.dk * w.dv * 4)
+
+
+def bench_backward(gdr, w, K, W, dev, flush, stream):
+    x = I.prefill_inputs(w, device=dev)
+    ct = I.cotangents(w, device=dev)
+    nws = gdr.chunk_bwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.torch_dtype())
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+
+    def step(_):
+        gdr.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                      ct["d_out"], ct["d_final"], chunk=w.chunk, workspace=ws)
+
+    return time_steps(step, K, W, flush, stream), nws
+
+
+def cpu_baseline_backward(w, budget_s=8.0):
+    """The fp64 oracle's backward on a bounded sample of the prefill workload: all
+    heads of sequence 0 over the first T_s tokens, T_s grown until ~budget_s."""
+    import oracle
+    x = I.prefill_inputs(w.with_(B=1), device="cpu")
+    ct = I.cotangents(w.with_(B=1), device="cpu")
+    cores = os.cpu_count() or 1
+    Ts = 64
+    while True:
+        sub = {n: x[n][:, :, :Ts] for n in ("q", "k", "v", "g", "beta")}
+        t0 = time.perf_counter()
+        oracle.bwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], w.a_min,
+                   x["init_state"], ct["d_out"][:, :, :Ts], ct["d_final"], nthreads=cores)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or Ts >= w.T:
+            break
+        Ts = min(w.T, Ts * 4)
+    return {"value": Ts / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"B=1 of {w.B}, all {w.H} heads, first {Ts} of {w.T} tokens "
+                      f"({w.H * Ts} head-tokens in {dt:.2f} s); value = head-tokens/s / H"}
 
 
 def cpu_baseline_prefill(w, budget_s=12.0):
@@ -416,6 +467,10 @@ def run_ours(args):
         if main_w.steps == 0 and not varlen and not args.no_decode:
             dec = bench_decode(gdr, I.DECODE, args.decode_steps, args.warmup, dev, flush, stream)
             barrier()
+        bwd = None
+        if main_w is I.PREFILL and not args.no_backward:
+            bwd = bench_backward(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
+            barrier()
     assert gdr.last_device_error(dev) == 0, "device error word set"
 
     ms_step = max_over_ranks(statistics.mean(ms))
@@ -514,12 +569,29 @@ def run_ours(args):
                     "unit": "tokens/s", "h2d_bytes_per_step": dh2d, "d2h_bytes_per_step": dd2h},
             "gpu_launches": args.decode_steps,
         }
+    if bwd is not None:
+        bms, bws = bwd
+        bmean = statistics.mean(bms)
+        bby = backward_algorithmic(main_w)
+        bgbs = bby / (bmean * 1e-3) / 1e9
+        line["backward"] = {
+            "metric": "backward tokens/s", "workload": main_w.name,
+            "value": round(world * main_w.B * main_w.T / (max_over_ranks(bmean) * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(bmean, 4), "steps": len(bms),
+            "roofline": {"bound": "hbm", "kernel": "bwd_chunk_kernel + bwd_chain_kernel + staged "
+                         "recompute", "achieved": round(bgbs, 1), "peak": pk["hbm_gbs"],
+                         "peak_kind": pk_kind, "unit": "GB/s", "frac": round(bgbs / pk["hbm_gbs"], 4),
+                         "traffic": None, "algorithmic_bytes": bby},
+            "workspace_bytes": bws, "gpu_launches": 5 * len(bms),
+        }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = (cpu_baseline_varlen(main_w) if varlen
                                 else cpu_baseline_prefill(main_w) if main_w.steps == 0
                                 else cpu_baseline_decode(main_w))
         if dec is not None:
             line["decode"]["cpu_baseline"] = cpu_baseline_decode(I.DECODE)
+        if bwd is not None:
+            line["backward"]["cpu_baseline"] = cpu_baseline_backward(main_w)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -603,6 +675,7 @@ def main():
                     default="prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--single-launch", action="store_true",
                     help="the one-launch fused path (no workspace) instead of prep + chain")
     args = ap.parse_args()
