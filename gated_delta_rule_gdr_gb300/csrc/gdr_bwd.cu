@@ -53,131 +53,336 @@ __device__ __forceinline__ float dlog_alpha_dg(float g, float d) {
     return d > 0.0f ? (1.0f - d) * s * (1.0f - s) / decay_alpha(g, d) : d * s * (1.0f - s);
 }
 
-// ---------------------------------------------------------------- reverse chain
-// One CTA per (value-column slice of DS, bh), sequential over chunks from the
-// last.  dM[:, slice] lives in shared memory for the whole pass.
+// ---------------------------------------------------------------- chunk tiles
+// One CTA per (chunk, bh), all in parallel: P[r][s] = (gamma_r / gamma_s) q_r.k_s
+// (s <= r), DK[r][s] = (gamma_r / gamma_s) k_r.k_s (s < r; A = diag(beta) DK) and
+// T = (I + A)^-1 (unit lower triangular) of every chunk, fp32 [BH][NC][C][C];
+// rows past a ragged chunk's end are zero in P and DK and identity in T.
 template <typename TE>
-__global__ void bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
+__global__ void bwd_tiles_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                                  const float *__restrict__ gamma, const float *__restrict__ beta,
-                                 const TE *__restrict__ dout, const float *dfinal,
-                                 float *__restrict__ dR, float *__restrict__ dMn1, float *dinit,
-                                 int T, int dk, int dv, int C, int DS) {
+                                 float *__restrict__ Pt, float *__restrict__ Tt,
+                                 float *__restrict__ DKt, int T, int dk, int C) {
     extern __shared__ float sm[];
-    const int j0 = blockIdx.x * DS, bh = blockIdx.y;
-    const int ldk = dk + 1, ldc = C + 1;
-    float *dMs = sm;                  // [dk][DS]
-    float *Ks = dMs + dk * DS;        // [C][dk+1]
-    float *Qs = Ks + C * ldk;         // [C][dk+1]
-    float *Ps = Qs + C * ldk;         // [C][C+1]  P[r][s], s <= r
-    float *As = Ps + C * ldc;         // [C][C+1]  A[r][s], s < r
-    float *dOs = As + C * ldc;        // [C][DS]
-    float *Xs = dOs + C * DS;         // [C][DS]   dW, then dR in place
-    float *gs = Xs + C * DS;          // [C] gamma
-    float *bs = gs + C;               // [C] beta
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int n = blockIdx.x, bh = blockIdx.y;
     const int NC = (T + C - 1) / C;
+    const int t0 = n * C, c = min(C, T - t0);
+    const int64_t row0 = (int64_t)bh * T + t0;
+    const int ldk = dk + 1, ldc = C + 1;
+    float *Qs = sm;                 // [C][dk+1]
+    float *Ks = Qs + C * ldk;       // [C][dk+1]
+    float *As = Ks + C * ldk;       // [C][C+1]
+    float *Ts = As + C * ldc;       // [C][C+1]
+    float *gs = Ts + C * ldc;       // [C]
+    float *bs = gs + C;             // [C]
+    const int tid = threadIdx.x, nt = blockDim.x;
+    float *Pp = Pt + ((int64_t)bh * NC + n) * C * C;
+    float *Tp = Tt + ((int64_t)bh * NC + n) * C * C;
+    float *DKp = DKt + ((int64_t)bh * NC + n) * C * C;
+    for (int x = tid; x < c * dk; x += nt) {
+        const int r = x / dk, i = x % dk;
+        Qs[r * ldk + i] = ldx(q, (row0 + r) * dk + i);
+        Ks[r * ldk + i] = ldx(k, (row0 + r) * dk + i);
+    }
+    for (int r = tid; r < c; r += nt) {
+        gs[r] = gamma[row0 + r];
+        bs[r] = beta[row0 + r];
+    }
+    __syncthreads();
+    for (int x = tid; x < C * C; x += nt) {
+        const int r = x / C, s = x % C;
+        float p = 0.f, a = 0.f, dkk = 0.f;
+        if (r < c && s <= r) {
+            float sqk = 0.f, skk = 0.f;
+            for (int i = 0; i < dk; ++i) {
+                sqk = fmaf(Qs[r * ldk + i], Ks[s * ldk + i], sqk);
+                skk = fmaf(Ks[r * ldk + i], Ks[s * ldk + i], skk);
+            }
+            const float D = gs[r] / gs[s];
+            p = D * sqk;
+            if (s < r) {
+                dkk = D * skk;
+                a = bs[r] * dkk;
+            }
+        }
+        Pp[x] = p;
+        DKp[x] = dkk;
+        As[r * ldc + s] = a;
+        Ts[r * ldc + s] = (r == s) ? 1.f : 0.f;
+    }
+    __syncthreads();
+    // forward substitution, one row at a time: T[r][s] = -sum_{m=s}^{r-1} A[r][m] T[m][s]
+    for (int r = 1; r < c; ++r) {
+        for (int s = tid; s < r; s += nt) {
+            float acc = 0.f;
+            for (int m = s; m < r; ++m) acc = fmaf(As[r * ldc + m], Ts[m * ldc + s], acc);
+            Ts[r * ldc + s] = -acc;
+        }
+        __syncthreads();
+    }
+    for (int x = tid; x < C * C; x += nt) Tp[x] = Ts[(x / C) * ldc + x % C];
+}
 
-    for (int x = tid; x < dk * DS; x += nt) {
+// ---------------------------------------------------------------- reverse chain
+// One CTA per (DS value columns, bh), sequential over chunks from the last;
+// dM[:, slice] lives in shared memory for the whole pass.  Each product is
+// register-tiled: a thread owns 2 x 4 outputs of dW and dR, 4 x 4 of dM.
+template <typename TE, int DS>
+__global__ void __launch_bounds__(256)
+bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
+                 const float *__restrict__ gamma, const float *__restrict__ beta,
+                 const TE *__restrict__ dout, const float *dfinal, const float *__restrict__ Pt,
+                 const float *__restrict__ Tt, float *__restrict__ dR, float *__restrict__ dMn1,
+                 float *dinit, int T, int dk, int dv, int C) {
+    extern __shared__ __align__(16) float sm[];
+    const int j0s = blockIdx.x * DS, bh = blockIdx.y;
+    const int ldk = dk + 4;               // 16-byte rows, rows 4 banks apart
+    float *dMs = sm;                      // [dk][DS]
+    float *Ks = dMs + dk * DS;            // [C][dk+4]  k
+    float *Qg = Ks + C * ldk;             // [C][dk+4]  gamma q
+    float *Kg = Qg + C * ldk;             // [C][dk+4]  gamma beta k
+    float *Ps = Kg + C * ldk;             // [C][C]
+    float *Tsm = Ps + C * C;              // [C][C]
+    float *dOs = Tsm + C * C;             // [C][DS]
+    float *dWs = dOs + C * DS;            // [C][DS]
+    float *dRs = dWs + C * DS;            // [C][DS]
+    float *gs = dRs + C * DS;             // [C]
+    float *scs = gs + C;                  // [C] gamma_C / gamma
+    const int tid = threadIdx.x;
+    const int NC = (T + C - 1) / C;
+    constexpr int JG = DS / 4;            // column groups of 4
+
+    for (int x = tid; x < dk * DS; x += 256) {
         const int i = x / DS, j = x % DS;
-        dMs[x] = dfinal ? dfinal[((int64_t)bh * dk + i) * dv + j0 + j] : 0.f;
+        dMs[x] = dfinal ? dfinal[((int64_t)bh * dk + i) * dv + j0s + j] : 0.f;
     }
     for (int n = NC - 1; n >= 0; --n) {
         const int t0 = n * C, c = min(C, T - t0);
         const int64_t row0 = (int64_t)bh * T + t0;
+        const float *Pp = Pt + ((int64_t)bh * NC + n) * C * C;
+        const float *Tp = Tt + ((int64_t)bh * NC + n) * C * C;
         __syncthreads();   // the previous chunk is done with every buffer
-        for (int x = tid; x < c * dk; x += nt) {
+        for (int x = tid; x < C * dk; x += 256) {
             const int r = x / dk, i = x % dk;
-            Ks[r * ldk + i] = ldx(k, (row0 + r) * dk + i);
-            Qs[r * ldk + i] = ldx(q, (row0 + r) * dk + i);
+            float kv = 0.f, qv = 0.f, g = 0.f, b = 0.f;
+            if (r < c) {
+                kv = ldx(k, (row0 + r) * dk + i);
+                qv = ldx(q, (row0 + r) * dk + i);
+                g = gamma[row0 + r];
+                b = beta[row0 + r];
+            }
+            Ks[r * ldk + i] = kv;
+            Qg[r * ldk + i] = g * qv;
+            Kg[r * ldk + i] = g * b * kv;
         }
-        for (int x = tid; x < c * DS; x += nt) {
+        for (int x = tid; x < C * DS; x += 256) {
             const int r = x / DS, j = x % DS;
-            dOs[x] = ldx(dout, (row0 + r) * dv + j0 + j);
+            dOs[x] = r < c ? ldx(dout, (row0 + r) * dv + j0s + j) : 0.f;
         }
-        for (int r = tid; r < c; r += nt) {
-            gs[r] = gamma[row0 + r];
-            bs[r] = beta[row0 + r];
+        for (int x = tid; x < C * C; x += 256) {
+            Ps[x] = Pp[x];
+            Tsm[x] = Tp[x];
         }
-        // dM' of this chunk, for the per-chunk gradients
-        for (int x = tid; x < dk * DS; x += nt) {
+        for (int r = tid; r < C; r += 256) gs[r] = r < c ? gamma[row0 + r] : 1.f;
+        for (int x = tid; x < dk * DS; x += 256) {   // dM' of this chunk
             const int i = x / DS, j = x % DS;
-            dMn1[(((int64_t)bh * NC + n) * dk + i) * dv + j0 + j] = dMs[x];
+            dMn1[(((int64_t)bh * NC + n) * dk + i) * dv + j0s + j] = dMs[x];
         }
         __syncthreads();
-        for (int x = tid; x < c * c; x += nt) {
-            const int r = x / c, s = x % c;
-            float p = 0.f, a = 0.f;
-            if (s <= r) {
-                float dq = 0.f, dkk = 0.f;
-                for (int i = 0; i < dk; ++i) {
-                    dq = fmaf(Qs[r * ldk + i], Ks[s * ldk + i], dq);
-                    dkk = fmaf(Ks[r * ldk + i], Ks[s * ldk + i], dkk);
-                }
-                const float d = gs[r] / gs[s];
-                p = d * dq;
-                if (s < r) a = bs[r] * d * dkk;
+        const float gC = gs[c - 1];
+        for (int r = tid; r < C; r += 256) scs[r] = r < c ? gC / gs[r] : 0.f;
+        __syncthreads();
+        // dW = P^T dO + diag(gamma_C / gamma) K dM'   (rows r0, r0 + 1; columns jq .. jq + 3)
+        for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
+            const int r0 = 2 * (tile / JG), jq = 4 * (tile % JG);
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int m = r0; m < C; ++m) {
+                const float2 p = *reinterpret_cast<const float2 *>(&Ps[m * C + r0]);
+                const float4 b = *reinterpret_cast<const float4 *>(&dOs[m * DS + jq]);
+                a0[0] = fmaf(p.x, b.x, a0[0]); a0[1] = fmaf(p.x, b.y, a0[1]);
+                a0[2] = fmaf(p.x, b.z, a0[2]); a0[3] = fmaf(p.x, b.w, a0[3]);
+                a1[0] = fmaf(p.y, b.x, a1[0]); a1[1] = fmaf(p.y, b.y, a1[1]);
+                a1[2] = fmaf(p.y, b.z, a1[2]); a1[3] = fmaf(p.y, b.w, a1[3]);
             }
-            Ps[r * ldc + s] = p;
-            As[r * ldc + s] = a;
+            float k0[4] = {0.f, 0.f, 0.f, 0.f}, k1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < dk; ++i) {
+                const float x0 = Ks[r0 * ldk + i], x1 = Ks[(r0 + 1) * ldk + i];
+                const float4 b = *reinterpret_cast<const float4 *>(&dMs[i * DS + jq]);
+                k0[0] = fmaf(x0, b.x, k0[0]); k0[1] = fmaf(x0, b.y, k0[1]);
+                k0[2] = fmaf(x0, b.z, k0[2]); k0[3] = fmaf(x0, b.w, k0[3]);
+                k1[0] = fmaf(x1, b.x, k1[0]); k1[1] = fmaf(x1, b.y, k1[1]);
+                k1[2] = fmaf(x1, b.z, k1[2]); k1[3] = fmaf(x1, b.w, k1[3]);
+            }
+            const float s0 = scs[r0], s1 = scs[r0 + 1];
+            float4 w0, w1;
+            w0.x = fmaf(s0, k0[0], a0[0]); w0.y = fmaf(s0, k0[1], a0[1]);
+            w0.z = fmaf(s0, k0[2], a0[2]); w0.w = fmaf(s0, k0[3], a0[3]);
+            w1.x = fmaf(s1, k1[0], a1[0]); w1.y = fmaf(s1, k1[1], a1[1]);
+            w1.z = fmaf(s1, k1[2], a1[2]); w1.w = fmaf(s1, k1[3], a1[3]);
+            *reinterpret_cast<float4 *>(&dWs[r0 * DS + jq]) = w0;
+            *reinterpret_cast<float4 *>(&dWs[(r0 + 1) * DS + jq]) = w1;
         }
         __syncthreads();
-        // dW = P^T dO + diag(gamma_C / gamma) K dM'
-        {
-            const float gC = gs[c - 1];
-            for (int x = tid; x < c * DS; x += nt) {
-                const int r = x / DS, j = x % DS;
-                float acc = 0.f;
-                for (int m = r; m < c; ++m) acc = fmaf(Ps[m * ldc + r], dOs[m * DS + j], acc);
-                float kd = 0.f;
-                for (int i = 0; i < dk; ++i) kd = fmaf(Ks[r * ldk + i], dMs[i * DS + j], kd);
-                Xs[x] = fmaf(gC / gs[r], kd, acc);
+        // dR = T^T dW, the gradient of diag(beta) E
+        for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
+            const int r0 = 2 * (tile / JG), jq = 4 * (tile % JG);
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int m = r0; m < C; ++m) {
+                const float2 t = *reinterpret_cast<const float2 *>(&Tsm[m * C + r0]);
+                const float4 b = *reinterpret_cast<const float4 *>(&dWs[m * DS + jq]);
+                a0[0] = fmaf(t.x, b.x, a0[0]); a0[1] = fmaf(t.x, b.y, a0[1]);
+                a0[2] = fmaf(t.x, b.z, a0[2]); a0[3] = fmaf(t.x, b.w, a0[3]);
+                a1[0] = fmaf(t.y, b.x, a1[0]); a1[1] = fmaf(t.y, b.y, a1[1]);
+                a1[2] = fmaf(t.y, b.z, a1[2]); a1[3] = fmaf(t.y, b.w, a1[3]);
             }
+            *reinterpret_cast<float4 *>(&dRs[r0 * DS + jq]) = make_float4(a0[0], a0[1], a0[2], a0[3]);
+            *reinterpret_cast<float4 *>(&dRs[(r0 + 1) * DS + jq]) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+            if (r0 < c)
+                for (int e = 0; e < 4; ++e) dR[(row0 + r0) * dv + j0s + jq + e] = a0[e];
+            if (r0 + 1 < c)
+                for (int e = 0; e < 4; ++e) dR[(row0 + r0 + 1) * dv + j0s + jq + e] = a1[e];
         }
         __syncthreads();
-        // (I + A)^T dR = dW: dR_r = dW_r - sum_{s > r} A[s][r] dR_s, from the last row;
-        // one thread per column
-        if (tid < DS) {
-            const int j = tid;
-            for (int r = c - 1; r >= 0; --r) {
-                float acc = Xs[r * DS + j];
-                for (int s = r + 1; s < c; ++s) acc = fmaf(-As[s * ldc + r], Xs[s * DS + j], acc);
-                Xs[r * DS + j] = acc;
+        // dM = gamma_C dM' + (gamma Q)^T dO - (gamma beta K)^T dR   (rows iq .. iq + 3)
+        for (int tile = tid; tile < (dk / 4) * JG; tile += 256) {
+            const int iq = 4 * (tile / JG), jq = 4 * (tile % JG);
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float4 m0 = *reinterpret_cast<const float4 *>(&dMs[(iq + a) * DS + jq]);
+                acc[a][0] = gC * m0.x; acc[a][1] = gC * m0.y; acc[a][2] = gC * m0.z; acc[a][3] = gC * m0.w;
             }
-        }
-        __syncthreads();
-        for (int x = tid; x < c * DS; x += nt) {
-            const int r = x / DS, j = x % DS;
-            dR[(row0 + r) * dv + j0 + j] = Xs[x];
-        }
-        // dM = gamma_C dM' + Q^T diag(gamma) dO - K^T diag(gamma beta) dR
-        {
-            const float gC = gs[c - 1];
-            for (int x = tid; x < dk * DS; x += nt) {
-                const int i = x / DS, j = x % DS;
-                float acc = 0.f;
-                for (int r = 0; r < c; ++r) {
-                    acc = fmaf(gs[r] * Qs[r * ldk + i], dOs[r * DS + j], acc);
-                    acc = fmaf(-gs[r] * bs[r] * Ks[r * ldk + i], Xs[r * DS + j], acc);
-                }
-                dMs[x] = fmaf(gC, dMs[x], acc);
+            for (int r = 0; r < c; ++r) {
+                const float4 qa = *reinterpret_cast<const float4 *>(&Qg[r * ldk + iq]);
+                const float4 ka = *reinterpret_cast<const float4 *>(&Kg[r * ldk + iq]);
+                const float4 ob = *reinterpret_cast<const float4 *>(&dOs[r * DS + jq]);
+                const float4 rb = *reinterpret_cast<const float4 *>(&dRs[r * DS + jq]);
+                const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, kv[4] = {ka.x, ka.y, ka.z, ka.w};
+                const float ov[4] = {ob.x, ob.y, ob.z, ob.w}, rv[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qv[a], ov[b], fmaf(-kv[a], rv[b], acc[a][b]));
             }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float4 *>(&dMs[(iq + a) * DS + jq]) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         }
     }
     __syncthreads();
     if (dinit) {
-        for (int x = tid; x < dk * DS; x += nt) {
+        for (int x = tid; x < dk * DS; x += 256) {
             const int i = x / DS, j = x % DS;
-            dinit[((int64_t)bh * dk + i) * dv + j0 + j] = dMs[x];
+            dinit[((int64_t)bh * dk + i) * dv + j0s + j] = dMs[x];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- forward states
+// The forward's state pass again, for the backward's recompute, register-tiled
+// like the reverse chain: per chunk W = U - Wk M (rows r0, r0 + 1), then
+// M <- gamma_C M + (diag(gamma_C / gamma) K)^T W (rows iq .. iq + 3); writes W
+// and the state at every chunk start.  One CTA per (DS value columns, bh).
+template <typename TE, int DS>
+__global__ void __launch_bounds__(256)
+bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
+                     const float *__restrict__ U, const float *__restrict__ Wk, const float *init,
+                     float *__restrict__ W, float *__restrict__ Mn, int T, int dk, int dv, int C) {
+    extern __shared__ __align__(16) float sm[];
+    const int j0s = blockIdx.x * DS, bh = blockIdx.y;
+    const int ldk = dk + 4;
+    float *Ms = sm;                       // [dk][DS]
+    float *Kt = Ms + dk * DS;             // [C][dk+4]  (gamma_C / gamma_r) k_r
+    float *Wks = Kt + C * ldk;            // [C][dk+4]  Wk
+    float *Ws = Wks + C * ldk;            // [C][DS]
+    const int tid = threadIdx.x;
+    const int NC = (T + C - 1) / C;
+    constexpr int JG = DS / 4;
+    for (int x = tid; x < dk * DS; x += 256) {
+        const int i = x / DS, j = x % DS;
+        Ms[x] = init ? init[((int64_t)bh * dk + i) * dv + j0s + j] : 0.f;
+    }
+    for (int n = 0; n < NC; ++n) {
+        const int t0 = n * C, c = min(C, T - t0);
+        const int64_t row0 = (int64_t)bh * T + t0;
+        const float gC = gamma[row0 + c - 1];
+        __syncthreads();
+        for (int x = tid; x < C * dk; x += 256) {
+            const int r = x / dk, i = x % dk;
+            float kv = 0.f, wk = 0.f;
+            if (r < c) {
+                kv = gC / gamma[row0 + r] * ldx(k, (row0 + r) * dk + i);
+                wk = Wk[(row0 + r) * dk + i];
+            }
+            Kt[r * ldk + i] = kv;
+            Wks[r * ldk + i] = wk;
+        }
+        for (int x = tid; x < dk * DS; x += 256) {
+            const int i = x / DS, j = x % DS;
+            Mn[(((int64_t)bh * NC + n) * dk + i) * dv + j0s + j] = Ms[x];
+        }
+        __syncthreads();
+        for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
+            const int r0 = 2 * (tile / JG), jq = 4 * (tile % JG);
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < dk; ++i) {
+                const float x0 = Wks[r0 * ldk + i], x1 = Wks[(r0 + 1) * ldk + i];
+                const float4 b = *reinterpret_cast<const float4 *>(&Ms[i * DS + jq]);
+                a0[0] = fmaf(x0, b.x, a0[0]); a0[1] = fmaf(x0, b.y, a0[1]);
+                a0[2] = fmaf(x0, b.z, a0[2]); a0[3] = fmaf(x0, b.w, a0[3]);
+                a1[0] = fmaf(x1, b.x, a1[0]); a1[1] = fmaf(x1, b.y, a1[1]);
+                a1[2] = fmaf(x1, b.z, a1[2]); a1[3] = fmaf(x1, b.w, a1[3]);
+            }
+            float w0[4], w1[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w0[e] = r0 < c ? U[(row0 + r0) * dv + j0s + jq + e] - a0[e] : 0.f;
+                w1[e] = r0 + 1 < c ? U[(row0 + r0 + 1) * dv + j0s + jq + e] - a1[e] : 0.f;
+            }
+            *reinterpret_cast<float4 *>(&Ws[r0 * DS + jq]) = make_float4(w0[0], w0[1], w0[2], w0[3]);
+            *reinterpret_cast<float4 *>(&Ws[(r0 + 1) * DS + jq]) = make_float4(w1[0], w1[1], w1[2], w1[3]);
+            if (r0 < c)
+                for (int e = 0; e < 4; ++e) W[(row0 + r0) * dv + j0s + jq + e] = w0[e];
+            if (r0 + 1 < c)
+                for (int e = 0; e < 4; ++e) W[(row0 + r0 + 1) * dv + j0s + jq + e] = w1[e];
+        }
+        __syncthreads();
+        for (int tile = tid; tile < (dk / 4) * JG; tile += 256) {
+            const int iq = 4 * (tile / JG), jq = 4 * (tile % JG);
+            float acc[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float4 m0 = *reinterpret_cast<const float4 *>(&Ms[(iq + a) * DS + jq]);
+                acc[a][0] = gC * m0.x; acc[a][1] = gC * m0.y; acc[a][2] = gC * m0.z; acc[a][3] = gC * m0.w;
+            }
+            for (int r = 0; r < c; ++r) {
+                const float4 ka = *reinterpret_cast<const float4 *>(&Kt[r * ldk + iq]);
+                const float4 wb = *reinterpret_cast<const float4 *>(&Ws[r * DS + jq]);
+                const float kv[4] = {ka.x, ka.y, ka.z, ka.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(kv[a], wv[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float4 *>(&Ms[(iq + a) * DS + jq]) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         }
     }
 }
 
 // ---------------------------------------------------------------- per-chunk gradients
-// One CTA per (chunk, bh), 256 threads.  Thread (i = tid % dk, rg = tid / dk)
-// owns the dQ and dK elements of key column i in rows r = rg, rg + RG, ...
-// (RG = 256 / dk), accumulated in registers over every term.
+// One CTA per (chunk, bh), 256 threads, every product register-tiled:
+//  1. the position pairs: dO W^T and dR W^T in 4 x 4 tiles, then FP = dP o D and
+//     FA = dA o beta D written over P and DK, with their db and dbeta terms;
+//  2. the state terms dO M^T, dR M^T and W dM'^T in 4 (rows) x 8 (key columns)
+//     tiles, M and dM' staged 16 value columns at a time, and the row dots
+//     q.(M dO), k.(M dR), k.(dM' w) the decay and beta gradients need;
+//  3. the in-chunk terms FP K, FP^T Q, FA K, FA^T K on the same tiles;
+//  4. dv, dbeta, db and dg per row.
 constexpr int kBwdThreads = 256;
-constexpr int kBwdMaxRows = 32;   // C * dk / 256 for C = 64, dk = 128
 constexpr int kBwdJB = 16;        // value columns of M and dM' staged at a time
 
 template <typename TE>
@@ -187,172 +392,263 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
                  const float *__restrict__ gamma, const float *__restrict__ W,
                  const float *__restrict__ Mn, const TE *__restrict__ dout,
                  const float *__restrict__ dR, const float *__restrict__ dMn1,
+                 const float *__restrict__ Pt, const float *__restrict__ DKt,
                  TE *__restrict__ dq, TE *__restrict__ dk_out, TE *__restrict__ dv_out,
                  float *__restrict__ dg, float *__restrict__ dbeta, int T, int dk, int dv, int C) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int n = blockIdx.x, bh = blockIdx.y;
     const int NC = (T + C - 1) / C;
     const int t0 = n * C, c = min(C, T - t0);
     const int64_t row0 = (int64_t)bh * T + t0;
-    const int ldk = dk + 1, ldv = dv + 1, ldc = C + 1, ldj = kBwdJB + 1;
-    float *Qs = sm;                     // [C][dk+1]
-    float *Ks = Qs + C * ldk;           // [C][dk+1]
-    float *Ws = Ks + C * ldk;           // [C][dv+1]
-    float *dOs = Ws + C * ldv;          // [C][dv+1]
-    float *dRs = dOs + C * ldv;         // [C][dv+1]
-    float *FP = dRs + C * ldv;          // [C][C+1]  dP o D
-    float *FA = FP + C * ldc;           // [C][C+1]  dA o beta D
-    float *Mt = FA + C * ldc;           // [dk][JB+1]  M[:, jb]
-    float *dMt = Mt + dk * ldj;         // [dk][JB+1]  dM'[:, jb]
-    float *gs = dMt + dk * ldj;         // [C] gamma
+    const int ldk = dk + 4, ldv = dv + 4;
+    float *Qs = sm;                     // [C][dk+4]
+    float *Ks = Qs + C * ldk;           // [C][dk+4]
+    float *Ws = Ks + C * ldk;           // [C][dv+4]
+    float *dOs = Ws + C * ldv;          // [C][dv+4]
+    float *dRs = dOs + C * ldv;         // [C][dv+4]
+    float *PF = dRs + C * ldv;          // [C][C]  P, then FP = dP o D
+    float *DF = PF + C * C;             // [C][C]  DK, then FA = dA o beta D
+    float *Mt = DF + C * C;             // [JB][dk+4]  M[:, jb + jj], transposed
+    float *dMt = Mt + kBwdJB * ldk;     // [JB][dk+4]  dM'[:, jb + jj], transposed
+    float *gs = dMt + kBwdJB * ldk;     // [C] gamma
     float *bs = gs + C;                 // [C] beta
     float *dbp = bs + C;                // [C] position-pair terms of db
     float *dbt = dbp + C;               // [C] position-pair terms of dbeta
     float *rq = dbt + C;                // [C] q_r^T M dO_r
     float *rk = rq + C;                 // [C] k_r^T M dR_r
     float *rz = rk + C;                 // [C] k_r^T dM' w_r
-    float *red = rz + C;                // [2]: <M, dM'>, sum_r z_r
+    float *red = rz + C;                // [1] <M, dM'>
     const int tid = threadIdx.x;
     const float *Mp = Mn + ((int64_t)bh * NC + n) * dk * dv;
     const float *dMp = dMn1 + ((int64_t)bh * NC + n) * dk * dv;
+    const float *Pp = Pt + ((int64_t)bh * NC + n) * C * C;
+    const float *DKp = DKt + ((int64_t)bh * NC + n) * C * C;
 
-    for (int x = tid; x < c * dk; x += kBwdThreads) {
+    for (int x = tid; x < C * dk; x += kBwdThreads) {
         const int r = x / dk, i = x % dk;
-        Qs[r * ldk + i] = ldx(q, (row0 + r) * dk + i);
-        Ks[r * ldk + i] = ldx(k, (row0 + r) * dk + i);
+        Qs[r * ldk + i] = r < c ? ldx(q, (row0 + r) * dk + i) : 0.f;
+        Ks[r * ldk + i] = r < c ? ldx(k, (row0 + r) * dk + i) : 0.f;
     }
-    for (int x = tid; x < c * dv; x += kBwdThreads) {
+    for (int x = tid; x < C * dv; x += kBwdThreads) {
         const int r = x / dv, j = x % dv;
-        Ws[r * ldv + j] = W[(row0 + r) * dv + j];
-        dOs[r * ldv + j] = ldx(dout, (row0 + r) * dv + j);
-        dRs[r * ldv + j] = dR[(row0 + r) * dv + j];
+        const bool in = r < c;
+        Ws[r * ldv + j] = in ? W[(row0 + r) * dv + j] : 0.f;
+        dOs[r * ldv + j] = in ? ldx(dout, (row0 + r) * dv + j) : 0.f;
+        dRs[r * ldv + j] = in ? dR[(row0 + r) * dv + j] : 0.f;
+    }
+    for (int x = tid; x < C * C; x += kBwdThreads) {
+        PF[x] = Pp[x];
+        DF[x] = DKp[x];
     }
     for (int r = tid; r < C; r += kBwdThreads) {
         gs[r] = r < c ? gamma[row0 + r] : 1.f;
         bs[r] = r < c ? beta[row0 + r] : 0.f;
         dbp[r] = dbt[r] = rq[r] = rk[r] = rz[r] = 0.f;
     }
-    if (tid < 2) red[tid] = 0.f;
+    if (tid == 0) red[0] = 0.f;
     __syncthreads();
 
-    // position pairs (r, s), s <= r: P, A, dP, dA and their decay and beta terms
-    for (int x = tid; x < C * C; x += kBwdThreads) {
-        const int r = x / C, s = x % C;
-        float fp = 0.f, fa = 0.f;
-        if (r < c && s <= r) {
-            float sqk = 0.f, skk = 0.f, dow = 0.f, drw = 0.f;
-            for (int i = 0; i < dk; ++i) {
-                sqk = fmaf(Qs[r * ldk + i], Ks[s * ldk + i], sqk);
-                skk = fmaf(Ks[r * ldk + i], Ks[s * ldk + i], skk);
+    // 1. position pairs (r, s) in 4 x 4 tiles on and below the diagonal
+    {
+        const int TB = C / 4;
+        for (int tile = tid; tile < TB * TB; tile += kBwdThreads) {
+            const int r0 = 4 * (tile / TB), s0 = 4 * (tile % TB);
+            if (s0 > r0 + 3) continue;
+            float ao[4][4], ar[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) ao[a][b] = ar[a][b] = 0.f;
+            for (int j = 0; j < dv; j += 4) {
+                float4 o[4], rr[4], w[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    o[a] = *reinterpret_cast<const float4 *>(&dOs[(r0 + a) * ldv + j]);
+                    rr[a] = *reinterpret_cast<const float4 *>(&dRs[(r0 + a) * ldv + j]);
+                    w[a] = *reinterpret_cast<const float4 *>(&Ws[(s0 + a) * ldv + j]);
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        ao[a][b] = fmaf(o[a].x, w[b].x, fmaf(o[a].y, w[b].y,
+                                   fmaf(o[a].z, w[b].z, fmaf(o[a].w, w[b].w, ao[a][b]))));
+                        ar[a][b] = fmaf(rr[a].x, w[b].x, fmaf(rr[a].y, w[b].y,
+                                   fmaf(rr[a].z, w[b].z, fmaf(rr[a].w, w[b].w, ar[a][b]))));
+                    }
             }
-            for (int j = 0; j < dv; ++j) {
-                dow = fmaf(dOs[r * ldv + j], Ws[s * ldv + j], dow);
-                drw = fmaf(dRs[r * ldv + j], Ws[s * ldv + j], drw);
-            }
-            const float D = gs[r] / gs[s];
-            float e = dow * D * sqk;          // dP P
-            fp = dow * D;
-            if (s < r) {
-                const float dA = -drw;
-                e += dA * bs[r] * D * skk;    // dA A
-                fa = dA * bs[r] * D;
-                atomicAdd(&dbt[r], dA * D * skk);
-            }
-            if (s < r) {                      // e is zero on the diagonal's net
-                atomicAdd(&dbp[r], e);
-                atomicAdd(&dbp[s], -e);
+            float re[4] = {0.f, 0.f, 0.f, 0.f}, ce[4] = {0.f, 0.f, 0.f, 0.f};
+            float rt[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int r = r0 + a, s = s0 + b;
+                    float fp = 0.f, fa = 0.f;
+                    if (r < c && s <= r) {
+                        const float D = gs[r] / gs[s];
+                        const float dP = ao[a][b];
+                        fp = dP * D;
+                        float e = dP * PF[r * C + s];
+                        if (s < r) {
+                            const float dA = -ar[a][b], dkk = DF[r * C + s];
+                            fa = dA * bs[r] * D;
+                            e = fmaf(dA * bs[r], dkk, e);
+                            rt[a] = fmaf(dA, dkk, rt[a]);
+                        }
+                        re[a] += e;
+                        ce[b] -= e;
+                    }
+                    PF[r * C + s] = fp;
+                    DF[r * C + s] = fa;
+                }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                if (r0 + a < c) {
+                    atomicAdd(&dbp[r0 + a], re[a]);
+                    atomicAdd(&dbt[r0 + a], rt[a]);
+                }
+                if (s0 + a < c) atomicAdd(&dbp[s0 + a], ce[a]);
             }
         }
-        FP[r * ldc + s] = fp;
-        FA[r * ldc + s] = fa;
     }
-    __syncthreads();
 
-    // state terms: aO = (dO M^T)[r][i], aR = (dR M^T)[r][i], aW = (W dM'^T)[r][i]
-    const int i = tid % dk, rg = tid / dk, RG = kBwdThreads / dk;
-    float aO[kBwdMaxRows], aR[kBwdMaxRows], aW[kBwdMaxRows];
+    // 2. state terms, tile (rows r0 .. r0 + 3) x (key columns i0 .. i0 + 7)
+    const int IG = dk / 8;
+    const int tile = tid, r0 = 4 * (tile / IG), i0 = 8 * (tile % IG);
+    const bool own = tile < (C / 4) * IG;
+    float aO[4][8], aR[4][8], aW[4][8];
 #pragma unroll
-    for (int m = 0; m < kBwdMaxRows; ++m) aO[m] = aR[m] = aW[m] = 0.f;
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) aO[a][e] = aR[a][e] = aW[a][e] = 0.f;
     float mdm = 0.f;   // this thread's share of <M, dM'>
     for (int jb = 0; jb < dv; jb += kBwdJB) {
+        __syncthreads();   // the previous block's M and dM' are read (and step 1 done)
         for (int x = tid; x < dk * kBwdJB; x += kBwdThreads) {
-            const int ii = x / kBwdJB, jj = x % kBwdJB;
-            const float mv = Mp[(int64_t)ii * dv + jb + jj], dmv = dMp[(int64_t)ii * dv + jb + jj];
-            Mt[ii * ldj + jj] = mv;
-            dMt[ii * ldj + jj] = dmv;
+            const int i = x / kBwdJB, jj = x % kBwdJB;
+            const float mv = Mp[(int64_t)i * dv + jb + jj], dmv = dMp[(int64_t)i * dv + jb + jj];
+            Mt[jj * ldk + i] = mv;
+            dMt[jj * ldk + i] = dmv;
             mdm = fmaf(mv, dmv, mdm);
         }
         __syncthreads();
+        if (own) {
+#pragma unroll 1
+            for (int j4 = 0; j4 < kBwdJB; j4 += 4) {
+                float4 o[4], rr[4], w[4];
 #pragma unroll
-        for (int m = 0; m < kBwdMaxRows; ++m) {
-            const int r = rg + RG * m;
-            if (r < c) {
-                float o = aO[m], rr = aR[m], w = aW[m];
-#pragma unroll
-                for (int jj = 0; jj < kBwdJB; ++jj) {
-                    const float mt = Mt[i * ldj + jj], dmt = dMt[i * ldj + jj];
-                    o = fmaf(dOs[r * ldv + jb + jj], mt, o);
-                    rr = fmaf(dRs[r * ldv + jb + jj], mt, rr);
-                    w = fmaf(Ws[r * ldv + jb + jj], dmt, w);
+                for (int a = 0; a < 4; ++a) {
+                    o[a] = *reinterpret_cast<const float4 *>(&dOs[(r0 + a) * ldv + jb + j4]);
+                    rr[a] = *reinterpret_cast<const float4 *>(&dRs[(r0 + a) * ldv + jb + j4]);
+                    w[a] = *reinterpret_cast<const float4 *>(&Ws[(r0 + a) * ldv + jb + j4]);
                 }
-                aO[m] = o;
-                aR[m] = rr;
-                aW[m] = w;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 m0 = *reinterpret_cast<const float4 *>(&Mt[(j4 + jj) * ldk + i0]);
+                    const float4 m1 = *reinterpret_cast<const float4 *>(&Mt[(j4 + jj) * ldk + i0 + 4]);
+                    const float4 d0 = *reinterpret_cast<const float4 *>(&dMt[(j4 + jj) * ldk + i0]);
+                    const float4 d1 = *reinterpret_cast<const float4 *>(&dMt[(j4 + jj) * ldk + i0 + 4]);
+                    const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                    const float dmv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        const float oa = jj == 0 ? o[a].x : jj == 1 ? o[a].y : jj == 2 ? o[a].z : o[a].w;
+                        const float ra = jj == 0 ? rr[a].x : jj == 1 ? rr[a].y : jj == 2 ? rr[a].z : rr[a].w;
+                        const float wa = jj == 0 ? w[a].x : jj == 1 ? w[a].y : jj == 2 ? w[a].z : w[a].w;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            aO[a][e] = fmaf(oa, mv[e], aO[a][e]);
+                            aR[a][e] = fmaf(ra, mv[e], aR[a][e]);
+                            aW[a][e] = fmaf(wa, dmv[e], aW[a][e]);
+                        }
+                    }
+                }
             }
         }
-        __syncthreads();
     }
-    // row reductions over i of q.(M dO_r), k.(M dR_r), k.(dM' w_r); then the
-    // state terms of dQ and dK in place of aO and aR
+    // row dots over the tile's key columns, reduced across the IG threads of a row
+    // group (consecutive lanes); then the state terms of dQ and dK in place
     {
         const float gC = gs[c - 1];
 #pragma unroll
-        for (int m = 0; m < kBwdMaxRows; ++m) {
-            const int r = rg + RG * m;   // uniform over each warp (dk >= 32)
-            if (r < c) {
-                float pq = Qs[r * ldk + i] * aO[m];
-                float pk = Ks[r * ldk + i] * aR[m];
-                float pz = Ks[r * ldk + i] * aW[m];
+        for (int a = 0; a < 4; ++a) {
+            float pq = 0.f, pk = 0.f, pz = 0.f;
+            if (own) {
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    pq += __shfl_xor_sync(0xffffffffu, pq, off);
-                    pk += __shfl_xor_sync(0xffffffffu, pk, off);
-                    pz += __shfl_xor_sync(0xffffffffu, pz, off);
+                for (int e = 0; e < 8; ++e) {
+                    const float qv = Qs[(r0 + a) * ldk + i0 + e], kv = Ks[(r0 + a) * ldk + i0 + e];
+                    pq = fmaf(qv, aO[a][e], pq);
+                    pk = fmaf(kv, aR[a][e], pk);
+                    pz = fmaf(kv, aW[a][e], pz);
                 }
-                if ((tid & 31) == 0) {
-                    atomicAdd(&rq[r], pq);
-                    atomicAdd(&rk[r], pk);
-                    atomicAdd(&rz[r], pz);
-                }
-                aO[m] *= gs[r];                                           // dQ
-                aR[m] = fmaf(gC / gs[r], aW[m], -gs[r] * bs[r] * aR[m]);  // dK
+            }
+            for (int off = 1; off < IG; off <<= 1) {
+                pq += __shfl_xor_sync(0xffffffffu, pq, off);
+                pk += __shfl_xor_sync(0xffffffffu, pk, off);
+                pz += __shfl_xor_sync(0xffffffffu, pz, off);
+            }
+            const int r = r0 + a;
+            if (own && (tile % IG) == 0 && r < c) {
+                rq[r] = pq;
+                rk[r] = pk;
+                rz[r] = pz;
+            }
+            const float gr = gs[r < C ? r : 0], sc = gC / gr, gb = gr * bs[r < C ? r : 0];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                aO[a][e] *= gr;                                   // dQ
+                aR[a][e] = fmaf(sc, aW[a][e], -gb * aR[a][e]);    // dK
             }
         }
     }
     for (int off = 16; off > 0; off >>= 1) mdm += __shfl_xor_sync(0xffffffffu, mdm, off);
     if ((tid & 31) == 0) atomicAdd(&red[0], mdm);
 
-    // in-chunk terms: dQ += FP K,  dK += FP^T Q + FA K + FA^T K
-#pragma unroll 4
-    for (int s = 0; s < c; ++s) {
-        const float ks = Ks[s * ldk + i], qs = Qs[s * ldk + i];
+    // 3. in-chunk terms: dQ += FP K,  dK += FP^T Q + FA K + FA^T K
+    if (own) {
+        for (int s4 = 0; s4 < C; s4 += 4) {
+            float4 fpr[4], far[4];
 #pragma unroll
-        for (int m = 0; m < kBwdMaxRows; ++m) {
-            const int r = rg + RG * m;
-            if (r < c) {
-                aO[m] = fmaf(FP[r * ldc + s], ks, aO[m]);
-                float t = fmaf(FP[s * ldc + r], qs, aR[m]);
-                t = fmaf(FA[r * ldc + s], ks, t);
-                aR[m] = fmaf(FA[s * ldc + r], ks, t);
+            for (int a = 0; a < 4; ++a) {
+                fpr[a] = *reinterpret_cast<const float4 *>(&PF[(r0 + a) * C + s4]);
+                far[a] = *reinterpret_cast<const float4 *>(&DF[(r0 + a) * C + s4]);
+            }
+#pragma unroll
+            for (int ss = 0; ss < 4; ++ss) {
+                const int s = s4 + ss;
+                const float4 k0 = *reinterpret_cast<const float4 *>(&Ks[s * ldk + i0]);
+                const float4 k1 = *reinterpret_cast<const float4 *>(&Ks[s * ldk + i0 + 4]);
+                const float4 q0 = *reinterpret_cast<const float4 *>(&Qs[s * ldk + i0]);
+                const float4 q1 = *reinterpret_cast<const float4 *>(&Qs[s * ldk + i0 + 4]);
+                const float4 fpt = *reinterpret_cast<const float4 *>(&PF[s * C + r0]);
+                const float4 fat = *reinterpret_cast<const float4 *>(&DF[s * C + r0]);
+                const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+                const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                const float ft[4] = {fpt.x, fpt.y, fpt.z, fpt.w}, at[4] = {fat.x, fat.y, fat.z, fat.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float fp = ss == 0 ? fpr[a].x : ss == 1 ? fpr[a].y : ss == 2 ? fpr[a].z : fpr[a].w;
+                    const float fa = ss == 0 ? far[a].x : ss == 1 ? far[a].y : ss == 2 ? far[a].z : far[a].w;
+                    const float fk = fa + at[a];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        aO[a][e] = fmaf(fp, kv[e], aO[a][e]);
+                        aR[a][e] = fmaf(ft[a], qv[e], fmaf(fk, kv[e], aR[a][e]));
+                    }
+                }
             }
         }
-    }
 #pragma unroll
-    for (int m = 0; m < kBwdMaxRows; ++m) {
-        const int r = rg + RG * m;
-        if (r < c) {
-            stx(dq, (row0 + r) * dk + i, aO[m]);
-            stx(dk_out, (row0 + r) * dk + i, aR[m]);
+        for (int a = 0; a < 4; ++a) {
+            const int r = r0 + a;
+            if (r < c) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    stx(dq, (row0 + r) * dk + i0 + e, aO[a][e]);
+                    stx(dk_out, (row0 + r) * dk + i0 + e, aR[a][e]);
+                }
+            }
         }
     }
     for (int x = tid; x < c * dv; x += kBwdThreads) {
@@ -361,7 +657,7 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
     }
     __syncthreads();
 
-    // per row: dbeta, db, then dlog(alpha) as the reverse cumulative sum and dg
+    // 4. per row: dbeta, db, then dlog(alpha) as the reverse cumulative sum and dg
     if (tid < 32) {
         const float gC = gs[c - 1];
         float zsum = 0.f;
@@ -383,16 +679,14 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
 #pragma unroll
         for (int e = 0; e < 2; ++e)
             if (2 * tid + e == c - 1) db[e] += last;
-        // suffix sums: dl_t = sum_{r >= t} db_r
-        float tot = db[0] + db[1];
-        float suf = tot;
+        // suffix sums: dlog(alpha_t) = sum_{r >= t} db_r
+        float suf = db[0] + db[1];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_down_sync(0xffffffffu, suf, off);
             if (tid + off < 32) suf += y;
         }
-        const float dl1 = suf - db[0], dl0 = suf;
-        const float dl[2] = {dl0, dl1};
+        const float dl[2] = {suf, suf - db[0]};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int r = 2 * tid + e;
@@ -406,13 +700,16 @@ cudaError_t bwd_set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+size_t tiles_smem(int dk, int C) {
+    return sizeof(float) * (2 * (size_t)C * (dk + 1) + 2 * (size_t)C * (C + 1) + 2 * (size_t)C);
+}
 size_t chain_smem(int dk, int DS, int C) {
-    return sizeof(float) * ((size_t)dk * DS + 2 * (size_t)C * (dk + 1) + 2 * (size_t)C * (C + 1) +
-                            2 * (size_t)C * DS + 2 * (size_t)C);
+    return sizeof(float) * ((size_t)dk * DS + 3 * (size_t)C * (dk + 4) + 2 * (size_t)C * C +
+                            3 * (size_t)C * DS + 2 * (size_t)C);
 }
 size_t chunk_smem(int dk, int dv, int C) {
-    return sizeof(float) * (2 * (size_t)C * (dk + 1) + 3 * (size_t)C * (dv + 1) +
-                            2 * (size_t)C * (C + 1) + 2 * (size_t)dk * (kBwdJB + 1) + 7 * (size_t)C + 2);
+    return sizeof(float) * (2 * (size_t)C * (dk + 4) + 3 * (size_t)C * (dv + 4) + 2 * (size_t)C * C +
+                            2 * (size_t)kBwdJB * (dk + 4) + 7 * (size_t)C + 4);
 }
 
 size_t round4(size_t n) { return (n + 3) & ~(size_t)3; }
@@ -431,21 +728,47 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     float *Mn = W + round4(tok * dv);
     float *dR = Mn + round4(st);
     float *dMn1 = dR + round4(tok * dv);
+    float *Pt = dMn1 + round4(st);
+    float *Tt = Pt + round4((size_t)BH * NC * C * C);
+    float *DKt = Tt + round4((size_t)BH * NC * C * C);
     cudaError_t err = launch_decay(g, d, gamma, BH, T, C, s);
     if (err == cudaSuccess) err = launch_wy(k, v, beta, gamma, U, Wk, BH, T, dk, dv, C, e, s);
-    if (err == cudaSuccess)
-        err = launch_state(k, gamma, U, Wk, init, W, Mn, nullptr, BH, T, dk, dv, C, e, s);
     if (err != cudaSuccess) return err;
-    const int DS = dv < 32 ? dv : 32;
-    const size_t s1 = chain_smem(dk, DS, C);
-    if ((err = bwd_set_smem(bwd_chain_kernel<TE>, s1)) != cudaSuccess) return err;
-    bwd_chain_kernel<TE><<<dim3(dv / DS, BH), 256, s1, s>>>(q, k, gamma, beta, dout, dfinal, dR,
-                                                           dMn1, dinit, T, dk, dv, C, DS);
+    {
+        const int DSf = dv >= 32 ? 32 : 16;
+        const size_t sf = sizeof(float) * ((size_t)dk * DSf + 2 * (size_t)C * (dk + 4) + (size_t)C * DSf);
+        if (DSf == 32) {
+            if ((err = bwd_set_smem(bwd_fwd_state_kernel<TE, 32>, sf)) != cudaSuccess) return err;
+            bwd_fwd_state_kernel<TE, 32><<<dim3(dv / 32, BH), 256, sf, s>>>(k, gamma, U, Wk, init, W,
+                                                                          Mn, T, dk, dv, C);
+        } else {
+            if ((err = bwd_set_smem(bwd_fwd_state_kernel<TE, 16>, sf)) != cudaSuccess) return err;
+            bwd_fwd_state_kernel<TE, 16><<<dim3(dv / 16, BH), 256, sf, s>>>(k, gamma, U, Wk, init, W,
+                                                                          Mn, T, dk, dv, C);
+        }
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    const size_t s0 = tiles_smem(dk, C);
+    if ((err = bwd_set_smem(bwd_tiles_kernel<TE>, s0)) != cudaSuccess) return err;
+    bwd_tiles_kernel<TE><<<dim3(NC, BH), 256, s0, s>>>(q, k, gamma, beta, Pt, Tt, DKt, T, dk, C);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (dv >= 32) {
+        const size_t s1 = chain_smem(dk, 32, C);
+        if ((err = bwd_set_smem(bwd_chain_kernel<TE, 32>, s1)) != cudaSuccess) return err;
+        bwd_chain_kernel<TE, 32><<<dim3(dv / 32, BH), 256, s1, s>>>(
+            q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
+    } else {
+        const size_t s1 = chain_smem(dk, 16, C);
+        if ((err = bwd_set_smem(bwd_chain_kernel<TE, 16>, s1)) != cudaSuccess) return err;
+        bwd_chain_kernel<TE, 16><<<dim3(dv / 16, BH), 256, s1, s>>>(
+            q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
+    }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t s2 = chunk_smem(dk, dv, C);
     if ((err = bwd_set_smem(bwd_chunk_kernel<TE>, s2)) != cudaSuccess) return err;
     bwd_chunk_kernel<TE><<<dim3(NC, BH), kBwdThreads, s2, s>>>(
-        q, k, v, g, beta, d, gamma, W, Mn, dout, dR, dMn1, dq, dk_out, dv_out, dg, dbeta, T, dk, dv, C);
+        q, k, v, g, beta, d, gamma, W, Mn, dout, dR, dMn1, Pt, DKt, dq, dk_out, dv_out, dg, dbeta, T,
+        dk, dv, C);
     return cudaGetLastError();
 }
 
@@ -461,7 +784,8 @@ size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C) {
     const int NC = (T + C - 1) / C;
     const size_t tok = (size_t)BH * T, st = (size_t)BH * NC * dk * dv;
     return sizeof(float) * (round4(tok) + round4(tok * dv) + round4(tok * dk) + round4(tok * dv) +
-                            round4(st) + round4(tok * dv) + round4(st));
+                            round4(st) + round4(tok * dv) + round4(st) +
+                            3 * round4((size_t)BH * NC * C * C));
 }
 
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const float *g,
