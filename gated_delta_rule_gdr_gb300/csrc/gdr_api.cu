@@ -392,6 +392,9 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
     if (T > 0) {
         if (!q || !k || !v || !g || !beta || !d_out || !d_q || !d_k || !d_v || !d_g || !d_beta)
             return GDR_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+            return GDR_ERR_INVALID_ARG;   // the kernels read them in 16-byte pieces
         if (!workspace ||
             workspace_bytes < gdr::bwd_workspace_bytes((int)BH, T, dk, dv, chunk) ||
             (reinterpret_cast<uintptr_t>(workspace) & 15))

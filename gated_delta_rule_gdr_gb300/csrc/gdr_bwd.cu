@@ -124,9 +124,117 @@ __global__ void bwd_tiles_kernel(const TE *__restrict__ q, const TE *__restrict_
 }
 
 // ---------------------------------------------------------------- reverse chain
+// 16-byte vector access to the element types.
+__device__ __forceinline__ uint4 ld16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ void widen16(const uint4 &u, float *f, const float *) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void widen16(const uint4 &u, float *f, const __nv_bfloat16 *) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+        f[2 * e] = t.x;
+        f[2 * e + 1] = t.y;
+    }
+}
+
+// One chunk's inputs of the reverse chain, held in registers between their load
+// and their store to shared memory, so that the loads of chunk n - 1 run while
+// chunk n computes.  Per thread: 16-byte pieces of K and Q, of P and T, of the dO
+// slice, and gamma, beta of row tid.
+template <typename TE, int DS>
+struct ChainStage {
+    static constexpr int V = 16 / (int)sizeof(TE);        // elements per 16 bytes
+    static constexpr int NKQ = 64 * 128 / V / 256;          // at most C = 64, dk = 128
+    static constexpr int NPT = 64 * 64 / 4 / 256;
+    static constexpr int NO = (64 * DS / V + 255) / 256;
+    uint4 kq[2][NKQ];
+    float4 pt[2][NPT];
+    uint4 o[NO];
+    float gb[2];
+
+    __device__ void load(const TE *q, const TE *k, const TE *dout, const float *gamma,
+                         const float *beta, const float *Pp, const float *Tp, int64_t row0, int c,
+                         int C, int dk, int dv, int j0s, int tid) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < NKQ; ++u) {
+            const int idx = tid + 256 * u;
+            if (idx < C * dk / V) {
+                const int r = idx * V / dk, col = idx * V % dk;
+                kq[0][u] = r < c ? ld16(k + (row0 + r) * dk + col) : z;
+                kq[1][u] = r < c ? ld16(q + (row0 + r) * dk + col) : z;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NPT; ++u) {
+            const int idx = tid + 256 * u;
+            if (idx < C * C / 4) {
+                pt[0][u] = __ldg(reinterpret_cast<const float4 *>(Pp) + idx);
+                pt[1][u] = __ldg(reinterpret_cast<const float4 *>(Tp) + idx);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NO; ++u) {
+            const int idx = tid + 256 * u;
+            if (idx < C * DS / V) {
+                const int r = idx * V / DS, col = idx * V % DS;
+                o[u] = r < c ? ld16(dout + (row0 + r) * dv + j0s + col) : z;
+            }
+        }
+        if (tid < C) {
+            gb[0] = tid < c ? gamma[row0 + tid] : 1.f;
+            gb[1] = tid < c ? beta[row0 + tid] : 0.f;
+        }
+    }
+    __device__ void store(float *Ks, float *Qs, float *Ps, float *Tsm, float *dOs, float *gs,
+                          float *bs, int C, int dk, int ldk, int tid) const {
+#pragma unroll
+        for (int u = 0; u < NKQ; ++u) {
+            const int idx = tid + 256 * u;
+            if (idx < C * dk / V) {
+                const int r = idx * V / dk, col = idx * V % dk;
+                float f[V];
+                widen16(kq[0][u], f, (const TE *)nullptr);
+#pragma unroll
+                for (int e = 0; e < V; ++e) Ks[r * ldk + col + e] = f[e];
+                widen16(kq[1][u], f, (const TE *)nullptr);
+#pragma unroll
+                for (int e = 0; e < V; ++e) Qs[r * ldk + col + e] = f[e];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NPT; ++u) {
+            const int idx = tid + 256 * u;
+            if (idx < C * C / 4) {
+                reinterpret_cast<float4 *>(Ps)[idx] = pt[0][u];
+                reinterpret_cast<float4 *>(Tsm)[idx] = pt[1][u];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NO; ++u) {
+            const int idx = tid + 256 * u;
+            if (idx < C * DS / V) {
+                const int r = idx * V / DS, col = idx * V % DS;
+                float f[V];
+                widen16(o[u], f, (const TE *)nullptr);
+#pragma unroll
+                for (int e = 0; e < V; ++e) dOs[r * DS + col + e] = f[e];
+            }
+        }
+        if (tid < C) {
+            gs[tid] = gb[0];
+            bs[tid] = gb[1];
+        }
+    }
+};
+
 // One CTA per (DS value columns, bh), sequential over chunks from the last;
 // dM[:, slice] lives in shared memory for the whole pass.  Each product is
-// register-tiled: a thread owns 2 x 4 outputs of dW and dR, 4 x 4 of dM.
+// register-tiled: a thread owns 2 x 4 outputs of dW and dR, 4 x 4 of dM.  The
+// gamma and gamma beta scalings ride on dO and dR, so K and Q stay as given.
 template <typename TE, int DS>
 __global__ void __launch_bounds__(256)
 bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
@@ -139,58 +247,47 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
     const int ldk = dk + 4;               // 16-byte rows, rows 4 banks apart
     float *dMs = sm;                      // [dk][DS]
     float *Ks = dMs + dk * DS;            // [C][dk+4]  k
-    float *Qg = Ks + C * ldk;             // [C][dk+4]  gamma q
-    float *Kg = Qg + C * ldk;             // [C][dk+4]  gamma beta k
-    float *Ps = Kg + C * ldk;             // [C][C]
+    float *Qs = Ks + C * ldk;             // [C][dk+4]  q
+    float *Ps = Qs + C * ldk;             // [C][C]
     float *Tsm = Ps + C * C;              // [C][C]
-    float *dOs = Tsm + C * C;             // [C][DS]
-    float *dWs = dOs + C * DS;            // [C][DS]
-    float *dRs = dWs + C * DS;            // [C][DS]
-    float *gs = dRs + C * DS;             // [C]
-    float *scs = gs + C;                  // [C] gamma_C / gamma
+    float *dOs = Tsm + C * C;             // [C][DS]  dO
+    float *dOg = dOs + C * DS;            // [C][DS]  gamma dO
+    float *dWs = dOg + C * DS;            // [C][DS]  dW
+    float *dRg = dWs + C * DS;            // [C][DS]  gamma beta dR
+    float *gs = dRg + C * DS;             // [C]
+    float *bs = gs + C;                   // [C]
+    float *scs = bs + C;                  // [C] gamma_C / gamma
     const int tid = threadIdx.x;
     const int NC = (T + C - 1) / C;
     constexpr int JG = DS / 4;            // column groups of 4
+    auto tile_p = [&](int n) { return Pt + ((int64_t)bh * NC + n) * C * C; };
+    auto tile_t = [&](int n) { return Tt + ((int64_t)bh * NC + n) * C * C; };
 
     for (int x = tid; x < dk * DS; x += 256) {
         const int i = x / DS, j = x % DS;
         dMs[x] = dfinal ? dfinal[((int64_t)bh * dk + i) * dv + j0s + j] : 0.f;
     }
+    ChainStage<TE, DS> stage;
+    {
+        const int n = NC - 1, c = T - n * C;
+        stage.load(q, k, dout, gamma, beta, tile_p(n), tile_t(n), (int64_t)bh * T + n * C, c, C, dk,
+                   dv, j0s, tid);
+        stage.store(Ks, Qs, Ps, Tsm, dOs, gs, bs, C, dk, ldk, tid);
+    }
     for (int n = NC - 1; n >= 0; --n) {
         const int t0 = n * C, c = min(C, T - t0);
         const int64_t row0 = (int64_t)bh * T + t0;
-        const float *Pp = Pt + ((int64_t)bh * NC + n) * C * C;
-        const float *Tp = Tt + ((int64_t)bh * NC + n) * C * C;
-        __syncthreads();   // the previous chunk is done with every buffer
-        for (int x = tid; x < C * dk; x += 256) {
-            const int r = x / dk, i = x % dk;
-            float kv = 0.f, qv = 0.f, g = 0.f, b = 0.f;
-            if (r < c) {
-                kv = ldx(k, (row0 + r) * dk + i);
-                qv = ldx(q, (row0 + r) * dk + i);
-                g = gamma[row0 + r];
-                b = beta[row0 + r];
-            }
-            Ks[r * ldk + i] = kv;
-            Qg[r * ldk + i] = g * qv;
-            Kg[r * ldk + i] = g * b * kv;
-        }
-        for (int x = tid; x < C * DS; x += 256) {
-            const int r = x / DS, j = x % DS;
-            dOs[x] = r < c ? ldx(dout, (row0 + r) * dv + j0s + j) : 0.f;
-        }
-        for (int x = tid; x < C * C; x += 256) {
-            Ps[x] = Pp[x];
-            Tsm[x] = Tp[x];
-        }
-        for (int r = tid; r < C; r += 256) gs[r] = r < c ? gamma[row0 + r] : 1.f;
+        __syncthreads();   // chunk n's inputs are in shared memory
+        if (n > 0)         // the previous chunk's loads run while this one computes
+            stage.load(q, k, dout, gamma, beta, tile_p(n - 1), tile_t(n - 1), row0 - C, C, C, dk, dv,
+                       j0s, tid);
         for (int x = tid; x < dk * DS; x += 256) {   // dM' of this chunk
             const int i = x / DS, j = x % DS;
             dMn1[(((int64_t)bh * NC + n) * dk + i) * dv + j0s + j] = dMs[x];
         }
-        __syncthreads();
         const float gC = gs[c - 1];
         for (int r = tid; r < C; r += 256) scs[r] = r < c ? gC / gs[r] : 0.f;
+        for (int x = tid; x < C * DS; x += 256) dOg[x] = gs[x / DS] * dOs[x];
         __syncthreads();
         // dW = P^T dO + diag(gamma_C / gamma) K dM'   (rows r0, r0 + 1; columns jq .. jq + 3)
         for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
@@ -214,16 +311,15 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                 k1[2] = fmaf(x1, b.z, k1[2]); k1[3] = fmaf(x1, b.w, k1[3]);
             }
             const float s0 = scs[r0], s1 = scs[r0 + 1];
-            float4 w0, w1;
-            w0.x = fmaf(s0, k0[0], a0[0]); w0.y = fmaf(s0, k0[1], a0[1]);
-            w0.z = fmaf(s0, k0[2], a0[2]); w0.w = fmaf(s0, k0[3], a0[3]);
-            w1.x = fmaf(s1, k1[0], a1[0]); w1.y = fmaf(s1, k1[1], a1[1]);
-            w1.z = fmaf(s1, k1[2], a1[2]); w1.w = fmaf(s1, k1[3], a1[3]);
-            *reinterpret_cast<float4 *>(&dWs[r0 * DS + jq]) = w0;
-            *reinterpret_cast<float4 *>(&dWs[(r0 + 1) * DS + jq]) = w1;
+            *reinterpret_cast<float4 *>(&dWs[r0 * DS + jq]) =
+                make_float4(fmaf(s0, k0[0], a0[0]), fmaf(s0, k0[1], a0[1]), fmaf(s0, k0[2], a0[2]),
+                            fmaf(s0, k0[3], a0[3]));
+            *reinterpret_cast<float4 *>(&dWs[(r0 + 1) * DS + jq]) =
+                make_float4(fmaf(s1, k1[0], a1[0]), fmaf(s1, k1[1], a1[1]), fmaf(s1, k1[2], a1[2]),
+                            fmaf(s1, k1[3], a1[3]));
         }
         __syncthreads();
-        // dR = T^T dW, the gradient of diag(beta) E
+        // dR = T^T dW, the gradient of diag(beta) E; gamma beta dR for the state update
         for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
             const int r0 = 2 * (tile / JG), jq = 4 * (tile % JG);
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -235,15 +331,20 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                 a1[0] = fmaf(t.y, b.x, a1[0]); a1[1] = fmaf(t.y, b.y, a1[1]);
                 a1[2] = fmaf(t.y, b.z, a1[2]); a1[3] = fmaf(t.y, b.w, a1[3]);
             }
-            *reinterpret_cast<float4 *>(&dRs[r0 * DS + jq]) = make_float4(a0[0], a0[1], a0[2], a0[3]);
-            *reinterpret_cast<float4 *>(&dRs[(r0 + 1) * DS + jq]) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+            const float g0 = gs[r0] * bs[r0], g1 = gs[r0 + 1] * bs[r0 + 1];
+            *reinterpret_cast<float4 *>(&dRg[r0 * DS + jq]) =
+                make_float4(g0 * a0[0], g0 * a0[1], g0 * a0[2], g0 * a0[3]);
+            *reinterpret_cast<float4 *>(&dRg[(r0 + 1) * DS + jq]) =
+                make_float4(g1 * a1[0], g1 * a1[1], g1 * a1[2], g1 * a1[3]);
             if (r0 < c)
-                for (int e = 0; e < 4; ++e) dR[(row0 + r0) * dv + j0s + jq + e] = a0[e];
+                *reinterpret_cast<float4 *>(&dR[(row0 + r0) * dv + j0s + jq]) =
+                    make_float4(a0[0], a0[1], a0[2], a0[3]);
             if (r0 + 1 < c)
-                for (int e = 0; e < 4; ++e) dR[(row0 + r0 + 1) * dv + j0s + jq + e] = a1[e];
+                *reinterpret_cast<float4 *>(&dR[(row0 + r0 + 1) * dv + j0s + jq]) =
+                    make_float4(a1[0], a1[1], a1[2], a1[3]);
         }
         __syncthreads();
-        // dM = gamma_C dM' + (gamma Q)^T dO - (gamma beta K)^T dR   (rows iq .. iq + 3)
+        // dM = gamma_C dM' + Q^T (gamma dO) - K^T (gamma beta dR)   (rows iq .. iq + 3)
         for (int tile = tid; tile < (dk / 4) * JG; tile += 256) {
             const int iq = 4 * (tile / JG), jq = 4 * (tile % JG);
             float acc[4][4];
@@ -253,10 +354,10 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                 acc[a][0] = gC * m0.x; acc[a][1] = gC * m0.y; acc[a][2] = gC * m0.z; acc[a][3] = gC * m0.w;
             }
             for (int r = 0; r < c; ++r) {
-                const float4 qa = *reinterpret_cast<const float4 *>(&Qg[r * ldk + iq]);
-                const float4 ka = *reinterpret_cast<const float4 *>(&Kg[r * ldk + iq]);
-                const float4 ob = *reinterpret_cast<const float4 *>(&dOs[r * DS + jq]);
-                const float4 rb = *reinterpret_cast<const float4 *>(&dRs[r * DS + jq]);
+                const float4 qa = *reinterpret_cast<const float4 *>(&Qs[r * ldk + iq]);
+                const float4 ka = *reinterpret_cast<const float4 *>(&Ks[r * ldk + iq]);
+                const float4 ob = *reinterpret_cast<const float4 *>(&dOg[r * DS + jq]);
+                const float4 rb = *reinterpret_cast<const float4 *>(&dRg[r * DS + jq]);
                 const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, kv[4] = {ka.x, ka.y, ka.z, ka.w};
                 const float ov[4] = {ob.x, ob.y, ob.z, ob.w}, rv[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
@@ -269,6 +370,8 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                 *reinterpret_cast<float4 *>(&dMs[(iq + a) * DS + jq]) =
                     make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         }
+        __syncthreads();   // every read of chunk n's inputs is done
+        if (n > 0) stage.store(Ks, Qs, Ps, Tsm, dOs, gs, bs, C, dk, ldk, tid);
     }
     __syncthreads();
     if (dinit) {
@@ -704,8 +807,8 @@ size_t tiles_smem(int dk, int C) {
     return sizeof(float) * (2 * (size_t)C * (dk + 1) + 2 * (size_t)C * (C + 1) + 2 * (size_t)C);
 }
 size_t chain_smem(int dk, int DS, int C) {
-    return sizeof(float) * ((size_t)dk * DS + 3 * (size_t)C * (dk + 4) + 2 * (size_t)C * C +
-                            3 * (size_t)C * DS + 2 * (size_t)C);
+    return sizeof(float) * ((size_t)dk * DS + 2 * (size_t)C * (dk + 4) + 2 * (size_t)C * C +
+                            4 * (size_t)C * DS + 3 * (size_t)C);
 }
 size_t chunk_smem(int dk, int dv, int C) {
     return sizeof(float) * (2 * (size_t)C * (dk + 4) + 3 * (size_t)C * (dv + 4) + 2 * (size_t)C * C +

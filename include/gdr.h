@@ -339,6 +339,7 @@ gdr_status_t gdr_decode_step_ex(const void *q, const void *k, const void *v, con
  *          is overwritten (no accumulation into existing values).
  * workspace  device memory of at least gdr_chunk_bwd_workspace_size bytes,
  *          16-byte aligned, owned by the caller; scratch on entry and exit.
+ * q, k, v and d_out must be 16-byte aligned (GDR_ERR_INVALID_ARG otherwise).
  * Supported: dk in {32, 64, 128}, dv in {16, 32, 64, 128}, chunk in {16, 32,
  * 64}, fp32 or bf16 (GDR_ERR_UNSUPPORTED otherwise); the range rule over the
  * chunk (GDR_ERR_RANGE).  Five launches, asynchronous on `stream`.

@@ -230,6 +230,7 @@ def bwd(lib, **kw):
     (dict(q=None), 1), (dict(dout=None), 1), (dict(dg=None), 1), (dict(db=None), 1),
     (dict(ws=None), 1), (dict(wsb=1024), 1),                     # workspace missing / small
     (dict(ws=ctypes.c_void_p(0x1008)), 1),                       # not 16-byte aligned
+    (dict(k=ctypes.c_void_p(0x1004)), 1), (dict(dout=ctypes.c_void_p(0x1002)), 1),
     (dict(B=0), 0), (dict(H=0), 0),                              # no heads: nothing to do
 ])
 def test_chunk_bwd_rejects(lib, kw, code):
