@@ -54,73 +54,154 @@ __device__ __forceinline__ float dlog_alpha_dg(float g, float d) {
 }
 
 // ---------------------------------------------------------------- chunk tiles
-// One CTA per (chunk, bh), all in parallel: P[r][s] = (gamma_r / gamma_s) q_r.k_s
-// (s <= r), DK[r][s] = (gamma_r / gamma_s) k_r.k_s (s < r; A = diag(beta) DK) and
-// T = (I + A)^-1 (unit lower triangular) of every chunk, fp32 [BH][NC][C][C];
-// rows past a ragged chunk's end are zero in P and DK and identity in T.
+// One CTA per (chunk, bh), all in parallel, 256 threads:
+//   P[r][s]  = (gamma_r / gamma_s) q_r.k_s  (s <= r),
+//   DK[r][s] = (gamma_r / gamma_s) k_r.k_s  (s < r; A = diag(beta) DK),
+//   T = (I + A)^-1 (unit lower triangular, row by row),
+//   U = T diag(beta) V,   Wk = T diag(beta gamma) K
+// of every chunk, fp32: P, DK, T [BH][NC][C][C] (rows past a ragged chunk's end
+// zero in P and DK, identity in T), U [BH,T,dv], Wk [BH,T,dk].  The products run in
+// 4 x 4 (pairs) and 4 x 8 (U, Wk) register tiles.
 template <typename TE>
-__global__ void bwd_tiles_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
-                                 const float *__restrict__ gamma, const float *__restrict__ beta,
-                                 float *__restrict__ Pt, float *__restrict__ Tt,
-                                 float *__restrict__ DKt, int T, int dk, int C) {
-    extern __shared__ float sm[];
+__global__ void __launch_bounds__(256)
+bwd_tiles_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__restrict__ v,
+                 const float *__restrict__ gamma, const float *__restrict__ beta,
+                 float *__restrict__ Pt, float *__restrict__ Tt, float *__restrict__ DKt,
+                 float *__restrict__ U, float *__restrict__ Wk, int T, int dk, int dv, int C) {
+    extern __shared__ __align__(16) float sm[];
     const int n = blockIdx.x, bh = blockIdx.y;
     const int NC = (T + C - 1) / C;
     const int t0 = n * C, c = min(C, T - t0);
     const int64_t row0 = (int64_t)bh * T + t0;
-    const int ldk = dk + 1, ldc = C + 1;
-    float *Qs = sm;                 // [C][dk+1]
-    float *Ks = Qs + C * ldk;       // [C][dk+1]
-    float *As = Ks + C * ldk;       // [C][C+1]
+    const int ldk = dk + 4, ldx4 = (dk > dv ? dk : dv) + 4, ldc = C + 1;
+    float *Ks = sm;                 // [C][dk+4]  k, then diag(beta gamma) k
+    float *QV = Ks + C * ldk;       // [C][max(dk,dv)+4]  q, then diag(beta) v
+    float *As = QV + C * ldx4;      // [C][C+1]
     float *Ts = As + C * ldc;       // [C][C+1]
     float *gs = Ts + C * ldc;       // [C]
     float *bs = gs + C;             // [C]
-    const int tid = threadIdx.x, nt = blockDim.x;
-    float *Pp = Pt + ((int64_t)bh * NC + n) * C * C;
-    float *Tp = Tt + ((int64_t)bh * NC + n) * C * C;
-    float *DKp = DKt + ((int64_t)bh * NC + n) * C * C;
-    for (int x = tid; x < c * dk; x += nt) {
+    const int tid = threadIdx.x;
+    const int64_t tb = ((int64_t)bh * NC + n) * C * C;
+    for (int x = tid; x < C * dk; x += 256) {
         const int r = x / dk, i = x % dk;
-        Qs[r * ldk + i] = ldx(q, (row0 + r) * dk + i);
-        Ks[r * ldk + i] = ldx(k, (row0 + r) * dk + i);
+        QV[r * ldx4 + i] = r < c ? ldx(q, (row0 + r) * dk + i) : 0.f;
+        Ks[r * ldk + i] = r < c ? ldx(k, (row0 + r) * dk + i) : 0.f;
     }
-    for (int r = tid; r < c; r += nt) {
-        gs[r] = gamma[row0 + r];
-        bs[r] = beta[row0 + r];
+    for (int r = tid; r < C; r += 256) {
+        gs[r] = r < c ? gamma[row0 + r] : 1.f;
+        bs[r] = r < c ? beta[row0 + r] : 0.f;
     }
+    for (int x = tid; x < C * C; x += 256) Ts[(x / C) * ldc + x % C] = (x / C == x % C) ? 1.f : 0.f;
     __syncthreads();
-    for (int x = tid; x < C * C; x += nt) {
-        const int r = x / C, s = x % C;
-        float p = 0.f, a = 0.f, dkk = 0.f;
-        if (r < c && s <= r) {
-            float sqk = 0.f, skk = 0.f;
-            for (int i = 0; i < dk; ++i) {
-                sqk = fmaf(Qs[r * ldk + i], Ks[s * ldk + i], sqk);
-                skk = fmaf(Ks[r * ldk + i], Ks[s * ldk + i], skk);
+    // position pairs in 4 x 4 tiles
+    {
+        const int TB = C / 4;
+        for (int tile = tid; tile < TB * TB; tile += 256) {
+            const int r0 = 4 * (tile / TB), s0 = 4 * (tile % TB);
+            float aq[4][4], ak[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) aq[a][b] = ak[a][b] = 0.f;
+            if (s0 <= r0 + 3) {
+                for (int i = 0; i < dk; i += 4) {
+                    float4 qr[4], kr[4], ks[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        qr[a] = *reinterpret_cast<const float4 *>(&QV[(r0 + a) * ldx4 + i]);
+                        kr[a] = *reinterpret_cast<const float4 *>(&Ks[(r0 + a) * ldk + i]);
+                        ks[a] = *reinterpret_cast<const float4 *>(&Ks[(s0 + a) * ldk + i]);
+                    }
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            aq[a][b] = fmaf(qr[a].x, ks[b].x, fmaf(qr[a].y, ks[b].y,
+                                       fmaf(qr[a].z, ks[b].z, fmaf(qr[a].w, ks[b].w, aq[a][b]))));
+                            ak[a][b] = fmaf(kr[a].x, ks[b].x, fmaf(kr[a].y, ks[b].y,
+                                       fmaf(kr[a].z, ks[b].z, fmaf(kr[a].w, ks[b].w, ak[a][b]))));
+                        }
+                }
             }
-            const float D = gs[r] / gs[s];
-            p = D * sqk;
-            if (s < r) {
-                dkk = D * skk;
-                a = bs[r] * dkk;
-            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int r = r0 + a, s = s0 + b;
+                    float p = 0.f, dkk = 0.f;
+                    if (r < c && s <= r) {
+                        const float D = gs[r] / gs[s];
+                        p = D * aq[a][b];
+                        if (s < r) dkk = D * ak[a][b];
+                    }
+                    Pt[tb + r * C + s] = p;
+                    DKt[tb + r * C + s] = dkk;
+                    As[r * ldc + s] = bs[r] * dkk;
+                }
         }
-        Pp[x] = p;
-        DKp[x] = dkk;
-        As[r * ldc + s] = a;
-        Ts[r * ldc + s] = (r == s) ? 1.f : 0.f;
     }
     __syncthreads();
+    // diag(beta) v over q, diag(beta gamma) k in place
+    for (int x = tid; x < C * dv; x += 256) {
+        const int r = x / dv, j = x % dv;
+        QV[r * ldx4 + j] = r < c ? bs[r] * ldx(v, (row0 + r) * dv + j) : 0.f;
+    }
+    for (int x = tid; x < C * dk; x += 256) {
+        const int r = x / dk, i = x % dk;
+        Ks[r * ldk + i] *= bs[r] * gs[r];
+    }
     // forward substitution, one row at a time: T[r][s] = -sum_{m=s}^{r-1} A[r][m] T[m][s]
     for (int r = 1; r < c; ++r) {
-        for (int s = tid; s < r; s += nt) {
+        __syncthreads();
+        for (int s = tid; s < r; s += 256) {
             float acc = 0.f;
             for (int m = s; m < r; ++m) acc = fmaf(As[r * ldc + m], Ts[m * ldc + s], acc);
             Ts[r * ldc + s] = -acc;
         }
-        __syncthreads();
     }
-    for (int x = tid; x < C * C; x += nt) Tp[x] = Ts[(x / C) * ldc + x % C];
+    __syncthreads();
+    for (int x = tid; x < C * C; x += 256) Tt[tb + x] = Ts[(x / C) * ldc + x % C];
+    // U = T diag(beta) V and Wk = T diag(beta gamma) K: tiles of 4 rows x 8 columns over
+    // the dv columns of U, then the dk columns of Wk
+    {
+        const int GV = dv / 8, GK = dk / 8, RB = C / 4;
+        for (int tile = tid; tile < RB * (GV + GK); tile += 256) {
+            const int r0 = 4 * (tile / (GV + GK)), cg = tile % (GV + GK);
+            const bool isU = cg < GV;
+            const int j0 = 8 * (isU ? cg : cg - GV);
+            const float *B = isU ? QV : Ks;
+            const int ldb = isU ? ldx4 : ldk;
+            float acc[4][8];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[a][e] = 0.f;
+            const int smax = min(r0 + 4, C);
+            for (int s = 0; s < smax; ++s) {
+                const float4 b0 = *reinterpret_cast<const float4 *>(&B[s * ldb + j0]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&B[s * ldb + j0 + 4]);
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float t = Ts[(r0 + a) * ldc + s];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[a][e] = fmaf(t, bv[e], acc[a][e]);
+                }
+            }
+            float *out = isU ? U : Wk;
+            const int ld = isU ? dv : dk;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int r = r0 + a;
+                if (r < c) {
+                    *reinterpret_cast<float4 *>(&out[(row0 + r) * ld + j0]) =
+                        make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+                    *reinterpret_cast<float4 *>(&out[(row0 + r) * ld + j0 + 4]) =
+                        make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
+                }
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- reverse chain
@@ -383,10 +464,81 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
 }
 
 // ---------------------------------------------------------------- forward states
+// One chunk's inputs of the forward-state pass, staged in registers like the
+// reverse chain's: K rows, Wk rows, the U slice, gamma of row tid.
+template <typename TE, int DS>
+struct FwdStage {
+    static constexpr int V = 16 / (int)sizeof(TE);
+    static constexpr int NK = 64 * 128 / V / 256;
+    static constexpr int NW = 64 * 128 / 4 / 256;
+    static constexpr int NU = (64 * DS / 4 + 255) / 256;
+    uint4 kk[NK];
+    float4 wk[NW], u[NU];
+    float gm;
+    __device__ void load(const TE *k, const float *Wk, const float *U, const float *gamma,
+                         int64_t row0, int c, int C, int dk, int dv, int j0s, int tid) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int x = 0; x < NK; ++x) {
+            const int idx = tid + 256 * x;
+            if (idx < C * dk / V) {
+                const int r = idx * V / dk, col = idx * V % dk;
+                kk[x] = r < c ? ld16(k + (row0 + r) * dk + col) : z;
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < NW; ++x) {
+            const int idx = tid + 256 * x;
+            if (idx < C * dk / 4) {
+                const int r = idx * 4 / dk, col = idx * 4 % dk;
+                wk[x] = r < c ? __ldg(reinterpret_cast<const float4 *>(Wk + (row0 + r) * dk + col)) : zf;
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < NU; ++x) {
+            const int idx = tid + 256 * x;
+            if (idx < C * DS / 4) {
+                const int r = idx * 4 / DS, col = idx * 4 % DS;
+                u[x] = r < c ? __ldg(reinterpret_cast<const float4 *>(U + (row0 + r) * dv + j0s + col)) : zf;
+            }
+        }
+        if (tid < C) gm = tid < c ? gamma[row0 + tid] : 1.f;
+    }
+    __device__ void store(float *Ks, float *Wks, float *Us, float *gs, int C, int dk, int ldk,
+                          int tid) const {
+#pragma unroll
+        for (int x = 0; x < NK; ++x) {
+            const int idx = tid + 256 * x;
+            if (idx < C * dk / V) {
+                const int r = idx * V / dk, col = idx * V % dk;
+                float f[V];
+                widen16(kk[x], f, (const TE *)nullptr);
+#pragma unroll
+                for (int e = 0; e < V; ++e) Ks[r * ldk + col + e] = f[e];
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < NW; ++x) {
+            const int idx = tid + 256 * x;
+            if (idx < C * dk / 4) {
+                const int r = idx * 4 / dk, col = idx * 4 % dk;
+                *reinterpret_cast<float4 *>(&Wks[r * ldk + col]) = wk[x];
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < NU; ++x) {
+            const int idx = tid + 256 * x;
+            if (idx < C * DS / 4) reinterpret_cast<float4 *>(Us)[idx] = u[x];
+        }
+        if (tid < C) gs[tid] = gm;
+    }
+};
+
 // The forward's state pass again, for the backward's recompute, register-tiled
 // like the reverse chain: per chunk W = U - Wk M (rows r0, r0 + 1), then
-// M <- gamma_C M + (diag(gamma_C / gamma) K)^T W (rows iq .. iq + 3); writes W
-// and the state at every chunk start.  One CTA per (DS value columns, bh).
+// M <- gamma_C M + K^T diag(gamma_C / gamma) W (rows iq .. iq + 3); writes W and
+// the state at every chunk start.  One CTA per (DS value columns, bh).
 template <typename TE, int DS>
 __global__ void __launch_bounds__(256)
 bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
@@ -396,9 +548,11 @@ bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
     const int j0s = blockIdx.x * DS, bh = blockIdx.y;
     const int ldk = dk + 4;
     float *Ms = sm;                       // [dk][DS]
-    float *Kt = Ms + dk * DS;             // [C][dk+4]  (gamma_C / gamma_r) k_r
-    float *Wks = Kt + C * ldk;            // [C][dk+4]  Wk
-    float *Ws = Wks + C * ldk;            // [C][DS]
+    float *Ks = Ms + dk * DS;             // [C][dk+4]  k
+    float *Wks = Ks + C * ldk;            // [C][dk+4]  Wk
+    float *Us = Wks + C * ldk;            // [C][DS]    U slice
+    float *Ws = Us + C * DS;              // [C][DS]    diag(gamma_C / gamma) W
+    float *gs = Ws + C * DS;              // [C]
     const int tid = threadIdx.x;
     const int NC = (T + C - 1) / C;
     constexpr int JG = DS / 4;
@@ -406,26 +560,20 @@ bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
         const int i = x / DS, j = x % DS;
         Ms[x] = init ? init[((int64_t)bh * dk + i) * dv + j0s + j] : 0.f;
     }
+    FwdStage<TE, DS> stage;
+    stage.load(k, Wk, U, gamma, (int64_t)bh * T, min(C, T), C, dk, dv, j0s, tid);
+    stage.store(Ks, Wks, Us, gs, C, dk, ldk, tid);
     for (int n = 0; n < NC; ++n) {
         const int t0 = n * C, c = min(C, T - t0);
         const int64_t row0 = (int64_t)bh * T + t0;
-        const float gC = gamma[row0 + c - 1];
-        __syncthreads();
-        for (int x = tid; x < C * dk; x += 256) {
-            const int r = x / dk, i = x % dk;
-            float kv = 0.f, wk = 0.f;
-            if (r < c) {
-                kv = gC / gamma[row0 + r] * ldx(k, (row0 + r) * dk + i);
-                wk = Wk[(row0 + r) * dk + i];
-            }
-            Kt[r * ldk + i] = kv;
-            Wks[r * ldk + i] = wk;
-        }
+        __syncthreads();   // chunk n's inputs are in shared memory
+        if (n + 1 < NC)
+            stage.load(k, Wk, U, gamma, row0 + C, min(C, T - t0 - C), C, dk, dv, j0s, tid);
         for (int x = tid; x < dk * DS; x += 256) {
             const int i = x / DS, j = x % DS;
             Mn[(((int64_t)bh * NC + n) * dk + i) * dv + j0s + j] = Ms[x];
         }
-        __syncthreads();
+        const float gC = gs[c - 1];
         for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
             const int r0 = 2 * (tile / JG), jq = 4 * (tile % JG);
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -437,18 +585,16 @@ bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
                 a1[0] = fmaf(x1, b.x, a1[0]); a1[1] = fmaf(x1, b.y, a1[1]);
                 a1[2] = fmaf(x1, b.z, a1[2]); a1[3] = fmaf(x1, b.w, a1[3]);
             }
-            float w0[4], w1[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                w0[e] = r0 < c ? U[(row0 + r0) * dv + j0s + jq + e] - a0[e] : 0.f;
-                w1[e] = r0 + 1 < c ? U[(row0 + r0 + 1) * dv + j0s + jq + e] - a1[e] : 0.f;
-            }
-            *reinterpret_cast<float4 *>(&Ws[r0 * DS + jq]) = make_float4(w0[0], w0[1], w0[2], w0[3]);
-            *reinterpret_cast<float4 *>(&Ws[(r0 + 1) * DS + jq]) = make_float4(w1[0], w1[1], w1[2], w1[3]);
-            if (r0 < c)
-                for (int e = 0; e < 4; ++e) W[(row0 + r0) * dv + j0s + jq + e] = w0[e];
-            if (r0 + 1 < c)
-                for (int e = 0; e < 4; ++e) W[(row0 + r0 + 1) * dv + j0s + jq + e] = w1[e];
+            const float4 u0 = *reinterpret_cast<const float4 *>(&Us[r0 * DS + jq]);
+            const float4 u1 = *reinterpret_cast<const float4 *>(&Us[(r0 + 1) * DS + jq]);
+            const float4 w0 = make_float4(u0.x - a0[0], u0.y - a0[1], u0.z - a0[2], u0.w - a0[3]);
+            const float4 w1 = make_float4(u1.x - a1[0], u1.y - a1[1], u1.z - a1[2], u1.w - a1[3]);
+            const float s0 = r0 < c ? gC / gs[r0] : 0.f, s1 = r0 + 1 < c ? gC / gs[r0 + 1] : 0.f;
+            *reinterpret_cast<float4 *>(&Ws[r0 * DS + jq]) = make_float4(s0 * w0.x, s0 * w0.y, s0 * w0.z, s0 * w0.w);
+            *reinterpret_cast<float4 *>(&Ws[(r0 + 1) * DS + jq]) =
+                make_float4(s1 * w1.x, s1 * w1.y, s1 * w1.z, s1 * w1.w);
+            if (r0 < c) *reinterpret_cast<float4 *>(&W[(row0 + r0) * dv + j0s + jq]) = w0;
+            if (r0 + 1 < c) *reinterpret_cast<float4 *>(&W[(row0 + r0 + 1) * dv + j0s + jq]) = w1;
         }
         __syncthreads();
         for (int tile = tid; tile < (dk / 4) * JG; tile += 256) {
@@ -460,7 +606,7 @@ bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
                 acc[a][0] = gC * m0.x; acc[a][1] = gC * m0.y; acc[a][2] = gC * m0.z; acc[a][3] = gC * m0.w;
             }
             for (int r = 0; r < c; ++r) {
-                const float4 ka = *reinterpret_cast<const float4 *>(&Kt[r * ldk + iq]);
+                const float4 ka = *reinterpret_cast<const float4 *>(&Ks[r * ldk + iq]);
                 const float4 wb = *reinterpret_cast<const float4 *>(&Ws[r * DS + jq]);
                 const float kv[4] = {ka.x, ka.y, ka.z, ka.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
@@ -473,6 +619,8 @@ bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
                 *reinterpret_cast<float4 *>(&Ms[(iq + a) * DS + jq]) =
                     make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         }
+        __syncthreads();   // every read of chunk n's inputs is done
+        if (n + 1 < NC) stage.store(Ks, Wks, Us, gs, C, dk, ldk, tid);
     }
 }
 
@@ -803,8 +951,9 @@ cudaError_t bwd_set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-size_t tiles_smem(int dk, int C) {
-    return sizeof(float) * (2 * (size_t)C * (dk + 1) + 2 * (size_t)C * (C + 1) + 2 * (size_t)C);
+size_t tiles_smem(int dk, int dv, int C) {
+    return sizeof(float) * ((size_t)C * (dk + 4) + (size_t)C * ((dk > dv ? dk : dv) + 4) +
+                            2 * (size_t)C * (C + 1) + 2 * (size_t)C);
 }
 size_t chain_smem(int dk, int DS, int C) {
     return sizeof(float) * ((size_t)dk * DS + 2 * (size_t)C * (dk + 4) + 2 * (size_t)C * C +
@@ -824,6 +973,7 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
                          int BH, int T, int dk, int dv, int C, float *ws, Elem e, cudaStream_t s) {
     const int NC = (T + C - 1) / C;
     const size_t tok = (size_t)BH * T, st = (size_t)BH * NC * dk * dv;
+    (void)e;
     float *gamma = ws;
     float *U = gamma + round4(tok);
     float *Wk = U + round4(tok * dv);
@@ -835,11 +985,16 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     float *Tt = Pt + round4((size_t)BH * NC * C * C);
     float *DKt = Tt + round4((size_t)BH * NC * C * C);
     cudaError_t err = launch_decay(g, d, gamma, BH, T, C, s);
-    if (err == cudaSuccess) err = launch_wy(k, v, beta, gamma, U, Wk, BH, T, dk, dv, C, e, s);
     if (err != cudaSuccess) return err;
+    const size_t s0 = tiles_smem(dk, dv, C);
+    if ((err = bwd_set_smem(bwd_tiles_kernel<TE>, s0)) != cudaSuccess) return err;
+    bwd_tiles_kernel<TE><<<dim3(NC, BH), 256, s0, s>>>(q, k, v, gamma, beta, Pt, Tt, DKt, U, Wk, T, dk,
+                                                      dv, C);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     {
         const int DSf = dv >= 32 ? 32 : 16;
-        const size_t sf = sizeof(float) * ((size_t)dk * DSf + 2 * (size_t)C * (dk + 4) + (size_t)C * DSf);
+        const size_t sf = sizeof(float) * ((size_t)dk * DSf + 2 * (size_t)C * (dk + 4) +
+                                           2 * (size_t)C * DSf + (size_t)C);
         if (DSf == 32) {
             if ((err = bwd_set_smem(bwd_fwd_state_kernel<TE, 32>, sf)) != cudaSuccess) return err;
             bwd_fwd_state_kernel<TE, 32><<<dim3(dv / 32, BH), 256, sf, s>>>(k, gamma, U, Wk, init, W,
@@ -851,10 +1006,6 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
         }
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    const size_t s0 = tiles_smem(dk, C);
-    if ((err = bwd_set_smem(bwd_tiles_kernel<TE>, s0)) != cudaSuccess) return err;
-    bwd_tiles_kernel<TE><<<dim3(NC, BH), 256, s0, s>>>(q, k, gamma, beta, Pt, Tt, DKt, T, dk, C);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (dv >= 32) {
         const size_t s1 = chain_smem(dk, 32, C);
         if ((err = bwd_set_smem(bwd_chain_kernel<TE, 32>, s1)) != cudaSuccess) return err;
