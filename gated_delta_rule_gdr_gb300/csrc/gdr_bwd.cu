@@ -636,6 +636,42 @@ bwd_fwd_state_kernel(const TE *__restrict__ k, const float *__restrict__ gamma,
 constexpr int kBwdThreads = 256;
 constexpr int kBwdJB = 16;        // value columns of M and dM' staged at a time
 
+// Rows 0 .. C-1 of a row-major matrix (width elements per row, source stride ld,
+// rows >= c read as zero) into shared fp32 rows of stride lds, in 16-byte pieces:
+// issue() puts every load in flight, commit() stores them, so the loads of several
+// matrices overlap.
+template <typename TE>
+struct RowLoader {
+    static constexpr int V = 16 / (int)sizeof(TE);
+    static constexpr int MAXV = 64 * 128 / V / kBwdThreads;
+    uint4 buf[MAXV];
+    __device__ __forceinline__ void issue(const TE *src, int64_t row0, int c, int C, int width, int ld,
+                                          int tid) {
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u) {
+            const int idx = tid + kBwdThreads * u;
+            buf[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (idx < C * width / V) {
+                const int r = idx * V / width, col = idx * V % width;
+                if (r < c) buf[u] = ld16(src + (row0 + r) * ld + col);
+            }
+        }
+    }
+    __device__ __forceinline__ void commit(float *dst, int lds, int C, int width, int tid) const {
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u) {
+            const int idx = tid + kBwdThreads * u;
+            if (idx < C * width / V) {
+                const int r = idx * V / width, col = idx * V % width;
+                float f[V];
+                widen16(buf[u], f, (const TE *)nullptr);
+#pragma unroll
+                for (int e = 0; e < V; ++e) dst[r * lds + col + e] = f[e];
+            }
+        }
+    }
+};
+
 template <typename TE>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__restrict__ v,
@@ -668,35 +704,39 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
     float *rq = dbt + C;                // [C] q_r^T M dO_r
     float *rk = rq + C;                 // [C] k_r^T M dR_r
     float *rz = rk + C;                 // [C] k_r^T dM' w_r
-    float *red = rz + C;                // [1] <M, dM'>
+    float *vdr = rz + C;                // [C] v_r . dR_r
+    float *red = vdr + C;               // [1] <M, dM'>
     const int tid = threadIdx.x;
     const float *Mp = Mn + ((int64_t)bh * NC + n) * dk * dv;
     const float *dMp = dMn1 + ((int64_t)bh * NC + n) * dk * dv;
     const float *Pp = Pt + ((int64_t)bh * NC + n) * C * C;
     const float *DKp = DKt + ((int64_t)bh * NC + n) * C * C;
 
-    for (int x = tid; x < C * dk; x += kBwdThreads) {
-        const int r = x / dk, i = x % dk;
-        Qs[r * ldk + i] = r < c ? ldx(q, (row0 + r) * dk + i) : 0.f;
-        Ks[r * ldk + i] = r < c ? ldx(k, (row0 + r) * dk + i) : 0.f;
+    {
+        RowLoader<TE> lq, lk, lo;
+        RowLoader<float> lw, lr;
+        lq.issue(q, row0, c, C, dk, dk, tid);
+        lk.issue(k, row0, c, C, dk, dk, tid);
+        lo.issue(dout, row0, c, C, dv, dv, tid);
+        lw.issue(W, row0, c, C, dv, dv, tid);
+        lr.issue(dR, row0, c, C, dv, dv, tid);
+        for (int r = tid; r < C; r += kBwdThreads) {
+            gs[r] = r < c ? gamma[row0 + r] : 1.f;
+            bs[r] = r < c ? beta[row0 + r] : 0.f;
+            dbp[r] = dbt[r] = rq[r] = rk[r] = rz[r] = vdr[r] = 0.f;
+        }
+        if (tid == 0) red[0] = 0.f;
+        lq.commit(Qs, ldk, C, dk, tid);
+        lk.commit(Ks, ldk, C, dk, tid);
+        lo.commit(dOs, ldv, C, dv, tid);
+        lw.commit(Ws, ldv, C, dv, tid);
+        lr.commit(dRs, ldv, C, dv, tid);
+        RowLoader<float> lp, ld;
+        lp.issue(Pp, 0, C, C, C, C, tid);
+        ld.issue(DKp, 0, C, C, C, C, tid);
+        lp.commit(PF, C, C, C, tid);
+        ld.commit(DF, C, C, C, tid);
     }
-    for (int x = tid; x < C * dv; x += kBwdThreads) {
-        const int r = x / dv, j = x % dv;
-        const bool in = r < c;
-        Ws[r * ldv + j] = in ? W[(row0 + r) * dv + j] : 0.f;
-        dOs[r * ldv + j] = in ? ldx(dout, (row0 + r) * dv + j) : 0.f;
-        dRs[r * ldv + j] = in ? dR[(row0 + r) * dv + j] : 0.f;
-    }
-    for (int x = tid; x < C * C; x += kBwdThreads) {
-        PF[x] = Pp[x];
-        DF[x] = DKp[x];
-    }
-    for (int r = tid; r < C; r += kBwdThreads) {
-        gs[r] = r < c ? gamma[row0 + r] : 1.f;
-        bs[r] = r < c ? beta[row0 + r] : 0.f;
-        dbp[r] = dbt[r] = rq[r] = rk[r] = rz[r] = 0.f;
-    }
-    if (tid == 0) red[0] = 0.f;
     __syncthreads();
 
     // 1. position pairs (r, s) in 4 x 4 tiles on and below the diagonal
@@ -774,15 +814,40 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
 #pragma unroll
         for (int e = 0; e < 8; ++e) aO[a][e] = aR[a][e] = aW[a][e] = 0.f;
     float mdm = 0.f;   // this thread's share of <M, dM'>
+    // M and dM' go through registers a block of 16 value columns at a time: the next
+    // block's loads run while the current one computes
+    constexpr int NMB = 128 * kBwdJB / 4 / kBwdThreads;
+    float4 mb[NMB], db[NMB];
+    auto load_blk = [&](int jb) {
+#pragma unroll
+        for (int u = 0; u < NMB; ++u) {
+            const int idx = tid + kBwdThreads * u;
+            if (idx < dk * kBwdJB / 4) {
+                const int i = idx / (kBwdJB / 4), j4 = 4 * (idx % (kBwdJB / 4));
+                mb[u] = __ldg(reinterpret_cast<const float4 *>(Mp + (int64_t)i * dv + jb + j4));
+                db[u] = __ldg(reinterpret_cast<const float4 *>(dMp + (int64_t)i * dv + jb + j4));
+            }
+        }
+    };
+    load_blk(0);
     for (int jb = 0; jb < dv; jb += kBwdJB) {
         __syncthreads();   // the previous block's M and dM' are read (and step 1 done)
-        for (int x = tid; x < dk * kBwdJB; x += kBwdThreads) {
-            const int i = x / kBwdJB, jj = x % kBwdJB;
-            const float mv = Mp[(int64_t)i * dv + jb + jj], dmv = dMp[(int64_t)i * dv + jb + jj];
-            Mt[jj * ldk + i] = mv;
-            dMt[jj * ldk + i] = dmv;
-            mdm = fmaf(mv, dmv, mdm);
+#pragma unroll
+        for (int u = 0; u < NMB; ++u) {
+            const int idx = tid + kBwdThreads * u;
+            if (idx < dk * kBwdJB / 4) {
+                const int i = idx / (kBwdJB / 4), j4 = 4 * (idx % (kBwdJB / 4));
+                const float mv[4] = {mb[u].x, mb[u].y, mb[u].z, mb[u].w};
+                const float dmv[4] = {db[u].x, db[u].y, db[u].z, db[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    Mt[(j4 + e) * ldk + i] = mv[e];
+                    dMt[(j4 + e) * ldk + i] = dmv[e];
+                    mdm = fmaf(mv[e], dmv[e], mdm);
+                }
+            }
         }
+        if (jb + kBwdJB < dv) load_blk(jb + kBwdJB);
         __syncthreads();
         if (own) {
 #pragma unroll 1
@@ -902,9 +967,20 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
             }
         }
     }
-    for (int x = tid; x < c * dv; x += kBwdThreads) {
-        const int r = x / dv, j = x % dv;
-        stx(dv_out, (row0 + r) * dv + j, bs[r] * dRs[r * ldv + j]);
+    {
+        // dv = diag(beta) dR, and v_r . dR_r reduced over groups of min(dv, 32) lanes
+        const int gw = dv < 32 ? dv : 32;
+        for (int x0 = 0; x0 < C * dv; x0 += kBwdThreads) {
+            const int x = x0 + tid, r = x / dv, j = x % dv;
+            float p = 0.f;
+            if (r < c) {
+                const float dr = dRs[r * ldv + j];
+                stx(dv_out, (row0 + r) * dv + j, bs[r] * dr);
+                p = ldx(v, (row0 + r) * dv + j) * dr;
+            }
+            for (int off = 1; off < gw; off <<= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if ((tid % gw) == 0 && r < c) atomicAdd(&vdr[r], p);
+        }
     }
     __syncthreads();
 
@@ -917,9 +993,7 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
         for (int e = 0; e < 2; ++e) {
             const int r = 2 * tid + e;
             if (r < c) {
-                float vdr = 0.f;
-                for (int j = 0; j < dv; ++j) vdr = fmaf(ldx(v, (row0 + r) * dv + j), dRs[r * ldv + j], vdr);
-                dbeta[row0 + r] = dbt[r] + vdr - gs[r] * rk[r];
+                dbeta[row0 + r] = dbt[r] + vdr[r] - gs[r] * rk[r];
                 const float z = gC / gs[r] * rz[r];
                 zsum += z;
                 db[e] = dbp[r] + gs[r] * rq[r] - gs[r] * bs[r] * rk[r] - z;
@@ -961,7 +1035,7 @@ size_t chain_smem(int dk, int DS, int C) {
 }
 size_t chunk_smem(int dk, int dv, int C) {
     return sizeof(float) * (2 * (size_t)C * (dk + 4) + 3 * (size_t)C * (dv + 4) + 2 * (size_t)C * C +
-                            2 * (size_t)kBwdJB * (dk + 4) + 7 * (size_t)C + 4);
+                            2 * (size_t)kBwdJB * (dk + 4) + 8 * (size_t)C + 4);
 }
 
 size_t round4(size_t n) { return (n + 3) & ~(size_t)3; }
