@@ -69,6 +69,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_fwd_ws_path": [i, i, i, i, i, i, f, i],
         "gdr_chunk_fwd_ex": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_decode_step_ex": [vp, vp, vp, vp, vp, i, f, vp, vp, i, i, i, i, i, vp],
+        "gdr_chunk_fwd_host": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_chunk_bwd": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                           i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
@@ -88,7 +89,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         fn.argtypes = args
         fn.restype = ctypes.c_int
     for name in ("gdr_chunk_fwd_workspace_size", "gdr_chunk_fwd_varlen_workspace_size",
-                 "gdr_chunk_bwd_workspace_size"):
+                 "gdr_chunk_bwd_workspace_size", "gdr_chunk_fwd_host_buffer_size"):
         fn = getattr(lib, name)
         fn.argtypes = [i, i, i, i, i, i, i]
         fn.restype = sz
@@ -225,6 +226,44 @@ def chunk_fwd_varlen(q, k, v, g, beta, a_min: float, cu_seqlens, init_state=None
                                            _ptr(final_state), _ptr(cu_seqlens), S, H, total_T, dk,
                                            dv, int(chunk), DTYPE[q.dtype], _ptr(ws), ws.numel(),
                                            _stream(q.device)), "gdr_chunk_fwd_varlen_ws")
+    return out, final_state
+
+
+def chunk_fwd_host_buffer_size(B, H, T, dk, dv, chunk=64, dtype=torch.bfloat16) -> int:
+    """Bytes of device memory chunk_fwd_host needs (inputs, outputs, workspace)."""
+    return int(load().gdr_chunk_fwd_host_buffer_size(B, H, T, dk, dv, chunk, DTYPE[dtype]))
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("chunk_fwd_host takes contiguous CPU tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def chunk_fwd_host(q, k, v, g, beta, a_min: float, init_state, out, final_state, device_buffer,
+                   *, chunk: int = 64, stream=None):
+    """Prefill from host tensors to host tensors (pinned memory for overlap): copies in,
+    computes and copies out on ``stream`` (default: the current stream of the buffer's
+    device).  ``device_buffer`` is a uint8 CUDA tensor of chunk_fwd_host_buffer_size
+    bytes; ``out`` [B,H,T,dv] and ``final_state`` [B,H,dk,dv] (or None) are CPU tensors
+    written when the stream reaches the end of the call."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype or out.dtype != q.dtype:
+        raise TypeError("q, k, v, out must share one dtype, float32 or bfloat16")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(init_state, "init_state"), _f32(final_state, "final_state")
+    if device_buffer.dtype != torch.uint8 or not device_buffer.is_cuda:
+        raise ValueError("device_buffer must be a uint8 CUDA tensor")
+    st = stream if stream is not None else torch.cuda.current_stream(device_buffer.device)
+    _check(lib.gdr_chunk_fwd_host(_host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(g),
+                                  _host_ptr(beta), float(a_min), _host_ptr(init_state),
+                                  _host_ptr(out), _host_ptr(final_state), B, H, T, dk, dv,
+                                  int(chunk), DTYPE[q.dtype], _ptr(device_buffer),
+                                  device_buffer.numel(), ctypes.c_void_p(st.cuda_stream)),
+           "gdr_chunk_fwd_host")
     return out, final_state
 
 

@@ -362,6 +362,84 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
     return gdr::fused_uses_pair((int)BH) ? 3 : 2;
 }
 
+// ---- host buffers in and out ----
+
+namespace {
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// Byte offsets of the pieces of the device buffer of gdr_chunk_fwd_host: q, k, v,
+// g, beta, init, out, final, workspace (each 256-byte aligned); returns the total.
+size_t host_layout(int B, int H, int T, int dk, int dv, int chunk, gdr_dtype_t dtype,
+                   size_t off[9]) {
+    const size_t es = dtype == GDR_DTYPE_F32 ? 4 : 2;
+    const size_t bht = (size_t)B * H * T, bh = (size_t)B * H;
+    const size_t sizes[9] = {bht * dk * es, bht * dk * es, bht * dv * es, bht * 4, bht * 4,
+                             bh * dk * dv * 4, bht * dv * es, bh * dk * dv * 4,
+                             gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype)};
+    size_t at = 0;
+    for (int i = 0; i < 9; ++i) {
+        off[i] = at;
+        at += align256(sizes[i]);
+    }
+    return at;
+}
+}  // namespace
+
+size_t gdr_chunk_fwd_host_buffer_size(int B, int H, int T, int dk, int dv, int chunk,
+                                      gdr_dtype_t dtype) {
+    if (B < 0 || H < 0 || T < 0 || !dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk))
+        return 0;
+    if ((int64_t)B * H > 0x7fffffff || (int64_t)T * B * H > ((int64_t)1 << 40)) return 0;
+    size_t off[9];
+    return host_layout(B, H, T, dk, dv, chunk, dtype, off);
+}
+
+gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float a_min, const float *init_state,
+                                void *out, float *final_state, int B, int H, int T, int dk, int dv,
+                                int chunk, gdr_dtype_t dtype, void *device_buffer,
+                                size_t device_bytes, void *stream) {
+    if (B < 0 || H < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return GDR_ERR_UNSUPPORTED;
+    if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
+    const size_t need = gdr_chunk_fwd_host_buffer_size(B, H, T, dk, dv, chunk, dtype);
+    if (need == 0 && (int64_t)B * H * T > 0) return GDR_ERR_UNSUPPORTED;
+    if ((int64_t)B * H == 0) return GDR_OK;
+    if (!device_buffer || device_bytes < need || (reinterpret_cast<uintptr_t>(device_buffer) & 255))
+        return GDR_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_INVALID_ARG;
+    // the chunk's range rule of whichever path the call takes, before anything is enqueued
+    const bool two = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) > 0;
+    if (!range_ok(a_min, two ? kTile : chunk)) return GDR_ERR_RANGE;
+    size_t off[9];
+    host_layout(B, H, T, dk, dv, chunk, dtype, off);
+    uint8_t *base = static_cast<uint8_t *>(device_buffer);
+    const size_t es = dtype == GDR_DTYPE_F32 ? 4 : 2;
+    const size_t bht = (size_t)B * H * T, st = (size_t)B * H * dk * dv * 4;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const void *src[6] = {q, k, v, g, beta, init_state};
+    const size_t bytes[6] = {bht * dk * es, bht * dk * es, bht * dv * es, bht * 4, bht * 4, st};
+    for (int i = 0; i < 6; ++i) {
+        if (!src[i] || bytes[i] == 0) continue;
+        if (cudaMemcpyAsync(base + off[i], src[i], bytes[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return GDR_ERR_CUDA;
+    }
+    gdr_status_t rc = chunk_fwd_ws_impl(
+        base + off[0], base + off[1], base + off[2], reinterpret_cast<float *>(base + off[3]),
+        reinterpret_cast<float *>(base + off[4]),
+        a_min, init_state ? reinterpret_cast<float *>(base + off[5]) : nullptr, base + off[6],
+        final_state ? reinterpret_cast<float *>(base + off[7]) : nullptr, B, H, T, dk, dv, chunk,
+        dtype, base + off[8], off[8] < need ? need - off[8] : 0, stream);
+    if (rc != GDR_OK) return rc;
+    if (T > 0 && cudaMemcpyAsync(out, base + off[6], bht * dv * es, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    if (final_state &&
+        cudaMemcpyAsync(final_state, base + off[7], st, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
 // ---- backward ----
 
 size_t gdr_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,

@@ -291,6 +291,34 @@ int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float 
                           gdr_dtype_t dtype);
 
 /*
+ * The prefill from host memory to host memory: the call a host-side caller makes
+ * when its q, k, v, g, beta (and initial state) are in host memory and it wants the
+ * output (and final state) back there.  On `stream`, in order: the host-to-device
+ * copies of the inputs into `device_buffer`, the prefill of gdr_chunk_fwd_ws (the
+ * two-kernel path when it applies, the buffer holding its workspace), and the
+ * device-to-host copies of out and final_state.  Asynchronous: the host inputs must
+ * stay unchanged and the host outputs untouched until `stream` reaches the end of
+ * the call.  Page-locked host memory lets the copies overlap other streams' work
+ * (two calls on two streams with two device buffers overlap one's copies with the
+ * other's kernels); pageable memory works but the copies are staged by the driver.
+ *
+ * Pointers: q, k, v, g, beta, init_state (may be NULL), out, final_state (may be
+ * NULL) are HOST pointers with the layouts of gdr_chunk_fwd.  device_buffer: device
+ * memory owned by the caller, 256-byte aligned, at least
+ * gdr_chunk_fwd_host_buffer_size bytes, not shared with a call still running on
+ * another stream.  Errors as gdr_chunk_fwd (a_min in (0, 1]; the range rule of the
+ * path taken: over a 16-token tile on the two-kernel path, over the chunk
+ * elsewhere); a missing or small buffer is GDR_ERR_INVALID_ARG.
+ */
+size_t gdr_chunk_fwd_host_buffer_size(int B, int H, int T, int dk, int dv, int chunk,
+                                      gdr_dtype_t dtype);
+gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float a_min, const float *init_state,
+                                void *out, float *final_state, int B, int H, int T, int dk, int dv,
+                                int chunk, gdr_dtype_t dtype, void *device_buffer,
+                                size_t device_bytes, void *stream);
+
+/*
  * The two lower-bounded decays ("Trillion-Parameter MoE Multimodal LLMs: How to
  * Evaluate the New Generation", section 3.1; "What a Trillion-Parameter MoE Model
  * Reveals About the Next Stage of LLM Scaling", section 3.2):

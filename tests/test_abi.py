@@ -248,3 +248,31 @@ def test_chunk_bwd_workspace_size(lib):
     assert n == 4 * (tok + 3 * tok * 64 + tok * 128 + 2 * st + 3 * tiles)
     assert f(2, 3, 0, 128, 64, 64, 1) == 0 and f(0, 3, 10, 128, 64, 64, 1) == 0
     assert f(1, 1, 10, 16, 64, 64, 1) == 0   # unsupported dk
+
+
+def test_chunk_fwd_host_rejects(lib):
+    f = lib.gdr_chunk_fwd_host
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3 + \
+        [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    sz = lib.gdr_chunk_fwd_host_buffer_size
+    sz.argtypes = [ctypes.c_int] * 7
+    sz.restype = ctypes.c_size_t
+    need = sz(1, 2, 100, 128, 128, 64, 1)
+    assert need > 0 and need % 256 == 0
+    buf = ctypes.c_void_p(0x100000)
+
+    def call(**kw):
+        a = dict(q=P, k=P, v=P, g=P, beta=P, a=0.95, init=None, out=P, fin=None, B=1, H=2, T=100,
+                 dk=128, dv=128, chunk=64, dt=1, buf=buf, n=need)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["g"], a["beta"], a["a"], a["init"], a["out"], a["fin"],
+                 a["B"], a["H"], a["T"], a["dk"], a["dv"], a["chunk"], a["dt"], a["buf"], a["n"], None)
+    assert call(n=need - 1) == 1                          # buffer too small
+    assert call(buf=ctypes.c_void_p(0x100010)) == 1       # not 256-byte aligned
+    assert call(buf=None) == 1
+    assert call(q=None) == 1 and call(out=None) == 1
+    assert call(a=0.0) == 1 and call(a=0.001) == 3        # floor; range over the 16-token tile
+    assert call(dk=48) == 2 and call(dt=5) == 2
+    assert call(B=0) == 0                                  # no heads: nothing to do
+    assert sz(1, 2, 100, 48, 128, 64, 1) == 0

@@ -286,6 +286,29 @@ def test_wide_range_varlen(variant):
         assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"], (s, e_o, e_f)
 
 
+@pytest.mark.parametrize("dtype,pinned", [("bf16", True), ("bf16", False), ("f32", True)])
+def test_host_buffers_match_device_call(dtype, pinned):
+    """gdr_chunk_fwd_host (host buffers in and out, copies on the stream) gives exactly
+    the device call's output and final state, and the oracle's within tolerance."""
+    w = (I.PREFILL.with_(B=2, H=2, T=300) if dtype == "bf16"
+         else I.CORRECTNESS.with_(T=200, dk=128, dv=128, init_std=0.3))
+    x = I.prefill_inputs(w)
+    host = {n: (None if t is None else (t.pin_memory() if pinned else t.contiguous()))
+            for n, t in x.items()}
+    buf = torch.empty(gdr.chunk_fwd_host_buffer_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk,
+                                                     w.torch_dtype()),
+                      dtype=torch.uint8, device="cuda")
+    out_h = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype(), pin_memory=pinned)
+    fin_h = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, pin_memory=pinned)
+    gdr.chunk_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"], w.a_min,
+                       host["init_state"], out_h, fin_h, buf, chunk=w.chunk)
+    torch.cuda.synchronize()
+    out_d, fin_d = run_gpu(to(x, "cuda"), w)
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
+    ro, rf = oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"])
+    assert rel(out_h, ro) <= TOL[dtype] and rel(fin_h, rf) <= TOL[dtype]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_log_decay_decode(dtype):
     w = I.DECODE.with_(B=8, H=4, dtype=dtype)
