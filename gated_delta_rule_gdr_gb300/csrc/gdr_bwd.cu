@@ -221,6 +221,18 @@ __device__ __forceinline__ void widen16(const uint4 &u, float *f, const __nv_bfl
     }
 }
 
+// Shared-memory copies of k and q keep the element type of the inputs (bf16 values
+// are exact as given): one element, or four consecutive ones, widened to fp32.
+__device__ __forceinline__ float sk1(const float *p) { return *p; }
+__device__ __forceinline__ float sk1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float4 sk4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 sk4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // One chunk's inputs of the reverse chain, held in registers between their load
 // and their store to shared memory, so that the loads of chunk n - 1 run while
 // chunk n computes.  Per thread: 16-byte pieces of K and Q, of P and T, of the dO
@@ -270,20 +282,15 @@ struct ChainStage {
             gb[1] = tid < c ? beta[row0 + tid] : 0.f;
         }
     }
-    __device__ void store(float *Ks, float *Qs, float *Ps, float *Tsm, float *dOs, float *gs,
+    __device__ void store(TE *Ks, TE *Qs, float *Ps, float *Tsm, float *dOs, float *gs,
                           float *bs, int C, int dk, int ldk, int tid) const {
 #pragma unroll
         for (int u = 0; u < NKQ; ++u) {
             const int idx = tid + 256 * u;
-            if (idx < C * dk / V) {
+            if (idx < C * dk / V) {   // k and q as given: 16 bytes as loaded
                 const int r = idx * V / dk, col = idx * V % dk;
-                float f[V];
-                widen16(kq[0][u], f, (const TE *)nullptr);
-#pragma unroll
-                for (int e = 0; e < V; ++e) Ks[r * ldk + col + e] = f[e];
-                widen16(kq[1][u], f, (const TE *)nullptr);
-#pragma unroll
-                for (int e = 0; e < V; ++e) Qs[r * ldk + col + e] = f[e];
+                *reinterpret_cast<uint4 *>(Ks + r * ldk + col) = kq[0][u];
+                *reinterpret_cast<uint4 *>(Qs + r * ldk + col) = kq[1][u];
             }
         }
 #pragma unroll
@@ -325,19 +332,18 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                  float *dinit, int T, int dk, int dv, int C) {
     extern __shared__ __align__(16) float sm[];
     const int j0s = blockIdx.x * DS, bh = blockIdx.y;
-    const int ldk = dk + 4;               // 16-byte rows, rows 4 banks apart
+    const int ldk = dk + 16 / (int)sizeof(TE);   // 16-byte rows, rows 4 banks apart
     float *dMs = sm;                      // [dk][DS]
-    float *Ks = dMs + dk * DS;            // [C][dk+4]  k
-    float *Qs = Ks + C * ldk;             // [C][dk+4]  q
-    float *Ps = Qs + C * ldk;             // [C][C]
+    float *Ps = dMs + dk * DS;            // [C][C]
     float *Tsm = Ps + C * C;              // [C][C]
     float *dOs = Tsm + C * C;             // [C][DS]  dO
-    float *dOg = dOs + C * DS;            // [C][DS]  gamma dO
-    float *dWs = dOg + C * DS;            // [C][DS]  dW
+    float *dWs = dOs + C * DS;            // [C][DS]  dW
     float *dRg = dWs + C * DS;            // [C][DS]  gamma beta dR
     float *gs = dRg + C * DS;             // [C]
     float *bs = gs + C;                   // [C]
     float *scs = bs + C;                  // [C] gamma_C / gamma
+    TE *Ks = reinterpret_cast<TE *>(sm + ((dk * DS + 2 * C * C + 3 * C * DS + 3 * C + 3) & ~3));
+    TE *Qs = Ks + C * ldk;                // [C][ldk]  k, q in the input element type
     const int tid = threadIdx.x;
     const int NC = (T + C - 1) / C;
     constexpr int JG = DS / 4;            // column groups of 4
@@ -368,7 +374,6 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
         }
         const float gC = gs[c - 1];
         for (int r = tid; r < C; r += 256) scs[r] = r < c ? gC / gs[r] : 0.f;
-        for (int x = tid; x < C * DS; x += 256) dOg[x] = gs[x / DS] * dOs[x];
         __syncthreads();
         // dW = P^T dO + diag(gamma_C / gamma) K dM'   (rows r0, r0 + 1; columns jq .. jq + 3)
         for (int tile = tid; tile < (C / 2) * JG; tile += 256) {
@@ -384,7 +389,7 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
             }
             float k0[4] = {0.f, 0.f, 0.f, 0.f}, k1[4] = {0.f, 0.f, 0.f, 0.f};
             for (int i = 0; i < dk; ++i) {
-                const float x0 = Ks[r0 * ldk + i], x1 = Ks[(r0 + 1) * ldk + i];
+                const float x0 = sk1(Ks + r0 * ldk + i), x1 = sk1(Ks + (r0 + 1) * ldk + i);
                 const float4 b = *reinterpret_cast<const float4 *>(&dMs[i * DS + jq]);
                 k0[0] = fmaf(x0, b.x, k0[0]); k0[1] = fmaf(x0, b.y, k0[1]);
                 k0[2] = fmaf(x0, b.z, k0[2]); k0[3] = fmaf(x0, b.w, k0[3]);
@@ -435,12 +440,14 @@ bwd_chain_kernel(const TE *__restrict__ q, const TE *__restrict__ k,
                 acc[a][0] = gC * m0.x; acc[a][1] = gC * m0.y; acc[a][2] = gC * m0.z; acc[a][3] = gC * m0.w;
             }
             for (int r = 0; r < c; ++r) {
-                const float4 qa = *reinterpret_cast<const float4 *>(&Qs[r * ldk + iq]);
-                const float4 ka = *reinterpret_cast<const float4 *>(&Ks[r * ldk + iq]);
-                const float4 ob = *reinterpret_cast<const float4 *>(&dOg[r * DS + jq]);
+                const float4 qa = sk4(Qs + r * ldk + iq);
+                const float4 ka = sk4(Ks + r * ldk + iq);
+                const float4 ob = *reinterpret_cast<const float4 *>(&dOs[r * DS + jq]);
                 const float4 rb = *reinterpret_cast<const float4 *>(&dRg[r * DS + jq]);
+                const float gr = gs[r];
                 const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, kv[4] = {ka.x, ka.y, ka.z, ka.w};
-                const float ov[4] = {ob.x, ob.y, ob.z, ob.w}, rv[4] = {rb.x, rb.y, rb.z, rb.w};
+                const float ov[4] = {gr * ob.x, gr * ob.y, gr * ob.z, gr * ob.w};
+                const float rv[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -1029,9 +1036,9 @@ size_t tiles_smem(int dk, int dv, int C) {
     return sizeof(float) * ((size_t)C * (dk + 4) + (size_t)C * ((dk > dv ? dk : dv) + 4) +
                             2 * (size_t)C * (C + 1) + 2 * (size_t)C);
 }
-size_t chain_smem(int dk, int DS, int C) {
-    return sizeof(float) * ((size_t)dk * DS + 2 * (size_t)C * (dk + 4) + 2 * (size_t)C * C +
-                            4 * (size_t)C * DS + 3 * (size_t)C);
+size_t chain_smem(int dk, int DS, int C, size_t es) {
+    const size_t fl = ((size_t)dk * DS + 2 * (size_t)C * C + 3 * (size_t)C * DS + 3 * (size_t)C + 3) & ~(size_t)3;
+    return sizeof(float) * fl + 2 * (size_t)C * (dk + 16 / es) * es;
 }
 size_t chunk_smem(int dk, int dv, int C) {
     return sizeof(float) * (2 * (size_t)C * (dk + 4) + 3 * (size_t)C * (dv + 4) + 2 * (size_t)C * C +
@@ -1081,12 +1088,12 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (dv >= 32) {
-        const size_t s1 = chain_smem(dk, 32, C);
+        const size_t s1 = chain_smem(dk, 32, C, sizeof(TE));
         if ((err = bwd_set_smem(bwd_chain_kernel<TE, 32>, s1)) != cudaSuccess) return err;
         bwd_chain_kernel<TE, 32><<<dim3(dv / 32, BH), 256, s1, s>>>(
             q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
     } else {
-        const size_t s1 = chain_smem(dk, 16, C);
+        const size_t s1 = chain_smem(dk, 16, C, sizeof(TE));
         if ((err = bwd_set_smem(bwd_chain_kernel<TE, 16>, s1)) != cudaSuccess) return err;
         bwd_chain_kernel<TE, 16><<<dim3(dv / 16, BH), 256, s1, s>>>(
             q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
