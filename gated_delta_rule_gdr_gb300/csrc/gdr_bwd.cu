@@ -746,12 +746,13 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
     }
     __syncthreads();
 
-    // 1. position pairs (r, s) in 4 x 4 tiles on and below the diagonal
+    // 1. position pairs (r, s): thread (rho, sig) owns rows rho + TB a and columns
+    //    sig + TB b (a, b < 4, TB = C / 4), so a warp's reads of W rows are 16 consecutive
+    //    rows (conflict-free); pairs above the diagonal are masked
     {
         const int TB = C / 4;
         for (int tile = tid; tile < TB * TB; tile += kBwdThreads) {
-            const int r0 = 4 * (tile / TB), s0 = 4 * (tile % TB);
-            if (s0 > r0 + 3) continue;
+            const int rho = tile / TB, sig = tile % TB;
             float ao[4][4], ar[4][4];
 #pragma unroll
             for (int a = 0; a < 4; ++a)
@@ -761,9 +762,9 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
                 float4 o[4], rr[4], w[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
-                    o[a] = *reinterpret_cast<const float4 *>(&dOs[(r0 + a) * ldv + j]);
-                    rr[a] = *reinterpret_cast<const float4 *>(&dRs[(r0 + a) * ldv + j]);
-                    w[a] = *reinterpret_cast<const float4 *>(&Ws[(s0 + a) * ldv + j]);
+                    o[a] = *reinterpret_cast<const float4 *>(&dOs[(rho + TB * a) * ldv + j]);
+                    rr[a] = *reinterpret_cast<const float4 *>(&dRs[(rho + TB * a) * ldv + j]);
+                    w[a] = *reinterpret_cast<const float4 *>(&Ws[(sig + TB * a) * ldv + j]);
                 }
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
@@ -781,7 +782,7 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
             for (int a = 0; a < 4; ++a)
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
-                    const int r = r0 + a, s = s0 + b;
+                    const int r = rho + TB * a, s = sig + TB * b;
                     float fp = 0.f, fa = 0.f;
                     if (r < c && s <= r) {
                         const float D = gs[r] / gs[s];
@@ -802,18 +803,20 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
                 }
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-                if (r0 + a < c) {
-                    atomicAdd(&dbp[r0 + a], re[a]);
-                    atomicAdd(&dbt[r0 + a], rt[a]);
+                if (rho + TB * a < c) {
+                    atomicAdd(&dbp[rho + TB * a], re[a]);
+                    atomicAdd(&dbt[rho + TB * a], rt[a]);
                 }
-                if (s0 + a < c) atomicAdd(&dbp[s0 + a], ce[a]);
+                if (sig + TB * a < c) atomicAdd(&dbp[sig + TB * a], ce[a]);
             }
         }
     }
 
-    // 2. state terms, tile (rows r0 .. r0 + 3) x (key columns i0 .. i0 + 7)
+    // 2. state terms, tile (rows r0 .. r0 + 3) x (key columns c0 .. c0 + 3 and c1 .. c1 + 3:
+    //    a half-warp's float4 reads of a row cover 256 contiguous bytes)
     const int IG = dk / 8;
-    const int tile = tid, r0 = 4 * (tile / IG), i0 = 8 * (tile % IG);
+    const int tile = tid, r0 = 4 * (tile / IG), c0 = 4 * (tile % IG), c1 = dk / 2 + c0;
+    auto colx = [&](int e) { return e < 4 ? c0 + e : c1 + e - 4; };
     const bool own = tile < (C / 4) * IG;
     float aO[4][8], aR[4][8], aW[4][8];
 #pragma unroll
@@ -868,10 +871,10 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
                 }
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
-                    const float4 m0 = *reinterpret_cast<const float4 *>(&Mt[(j4 + jj) * ldk + i0]);
-                    const float4 m1 = *reinterpret_cast<const float4 *>(&Mt[(j4 + jj) * ldk + i0 + 4]);
-                    const float4 d0 = *reinterpret_cast<const float4 *>(&dMt[(j4 + jj) * ldk + i0]);
-                    const float4 d1 = *reinterpret_cast<const float4 *>(&dMt[(j4 + jj) * ldk + i0 + 4]);
+                    const float4 m0 = *reinterpret_cast<const float4 *>(&Mt[(j4 + jj) * ldk + c0]);
+                    const float4 m1 = *reinterpret_cast<const float4 *>(&Mt[(j4 + jj) * ldk + c1]);
+                    const float4 d0 = *reinterpret_cast<const float4 *>(&dMt[(j4 + jj) * ldk + c0]);
+                    const float4 d1 = *reinterpret_cast<const float4 *>(&dMt[(j4 + jj) * ldk + c1]);
                     const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
                     const float dmv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
@@ -900,7 +903,7 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
             if (own) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float qv = Qs[(r0 + a) * ldk + i0 + e], kv = Ks[(r0 + a) * ldk + i0 + e];
+                    const float qv = Qs[(r0 + a) * ldk + colx(e)], kv = Ks[(r0 + a) * ldk + colx(e)];
                     pq = fmaf(qv, aO[a][e], pq);
                     pk = fmaf(kv, aR[a][e], pk);
                     pz = fmaf(kv, aW[a][e], pz);
@@ -940,10 +943,10 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
 #pragma unroll
             for (int ss = 0; ss < 4; ++ss) {
                 const int s = s4 + ss;
-                const float4 k0 = *reinterpret_cast<const float4 *>(&Ks[s * ldk + i0]);
-                const float4 k1 = *reinterpret_cast<const float4 *>(&Ks[s * ldk + i0 + 4]);
-                const float4 q0 = *reinterpret_cast<const float4 *>(&Qs[s * ldk + i0]);
-                const float4 q1 = *reinterpret_cast<const float4 *>(&Qs[s * ldk + i0 + 4]);
+                const float4 k0 = *reinterpret_cast<const float4 *>(&Ks[s * ldk + c0]);
+                const float4 k1 = *reinterpret_cast<const float4 *>(&Ks[s * ldk + c1]);
+                const float4 q0 = *reinterpret_cast<const float4 *>(&Qs[s * ldk + c0]);
+                const float4 q1 = *reinterpret_cast<const float4 *>(&Qs[s * ldk + c1]);
                 const float4 fpt = *reinterpret_cast<const float4 *>(&PF[s * C + r0]);
                 const float4 fat = *reinterpret_cast<const float4 *>(&DF[s * C + r0]);
                 const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
@@ -968,8 +971,8 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
             if (r < c) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    stx(dq, (row0 + r) * dk + i0 + e, aO[a][e]);
-                    stx(dk_out, (row0 + r) * dk + i0 + e, aR[a][e]);
+                    stx(dq, (row0 + r) * dk + colx(e), aO[a][e]);
+                    stx(dk_out, (row0 + r) * dk + colx(e), aR[a][e]);
                 }
             }
         }
