@@ -1,7 +1,8 @@
 // gdr_bwd.cu -- the backward of the chunked gated delta rule: the gradients of
 // a loss L with respect to q, k, v, g, beta and the initial state, given
 // dL/dout and dL/dfinal_state.  fp32 CUDA-core kernels (inputs and the output
-// gradients in the forward's element type, widened on load).
+// gradients in the forward's element type, widened on load), except the per-chunk
+// gradients of the bf16 d = 128, chunk-64 shape, which run on warp MMAs.
 //
 // The chunk algebra of the forward ("What a Trillion-Parameter MoE Model
 // Reveals About the Next Stage of LLM Scaling", sections 3.1-3.3; the staged
@@ -32,8 +33,10 @@
 
 #include "gdr_internal.h"
 #include "gdr_math.cuh"
+#include "gdr_sm100.cuh"
 
 #include <cuda_bf16.h>
+#include <type_traits>
 
 namespace gdr {
 namespace {
@@ -1030,6 +1033,411 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
     }
 }
 
+// ---------------------------------------------------------------- per-chunk gradients, warp MMA
+// The per-chunk gradients of the bf16 prefill shape (dk = dv = 128, C = 64) with every
+// product on warp-level MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
+// q, k and dO enter as given, W, dR, M and dM' are rounded to bf16 once, FP and FA
+// (formed in fp32) as operands.  Same four steps as bwd_chunk_kernel; 8 warps, the
+// pairs in 16 x 32 warp tiles, the state and in-chunk products in 32 x 32.  Shared
+// rows carry 16 bytes of padding, so each ldmatrix reads eight rows from eight
+// different bank groups.
+namespace mm {
+constexpr int C = 64, D = 128, LD = D + 8, LC = C + 8;
+constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + C * LD * 2, OFF_O = OFF_K + C * LD * 2,
+                   OFF_W = OFF_O + C * LD * 2, OFF_R = OFF_W + C * LD * 2,
+                   OFF_M = OFF_R + C * LD * 2, OFF_DM = OFF_M + D * LD * 2,
+                   OFF_FP = OFF_DM + D * LD * 2, OFF_FA = OFF_FP + C * LC * 2,
+                   OFF_SC = OFF_FA + C * LC * 2;
+constexpr uint32_t SMEM = OFF_SC + (8 * C + 4) * 4;
+}  // namespace mm
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+// A fragment (16 x 16 at row R, column Kc) of a row-major bf16 tile, ldmatrix address
+__device__ __forceinline__ uint32_t a_addr(uint32_t base, int ld, int R, int Kc, int lane) {
+    return base + 2u * (uint32_t)((R + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + Kc + (lane >> 4) * 8);
+}
+// A fragment of the transpose of a row-major tile X (A[r][s] = X[s][r]), for ldmatrix.trans
+__device__ __forceinline__ uint32_t at_addr(uint32_t base, int ld, int R, int Kc, int lane) {
+    return base + 2u * (uint32_t)((Kc + (lane & 7) + (lane >> 4) * 8) * ld + R + ((lane >> 3) & 1) * 8);
+}
+// B fragments of n-tiles N, N + 8 (k = Kc .. Kc + 15) from a row-major [n][k] tile
+__device__ __forceinline__ uint32_t b_addr(uint32_t base, int ld, int N, int Kc, int lane) {
+    return base + 2u * (uint32_t)((N + (lane & 7) + (lane >> 4) * 8) * ld + Kc + ((lane >> 3) & 1) * 8);
+}
+// ... and from a row-major [k][n] tile, for ldmatrix.trans
+__device__ __forceinline__ uint32_t bt_addr(uint32_t base, int ld, int N, int Kc, int lane) {
+    return base + 2u * (uint32_t)((Kc + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + N + (lane >> 4) * 8);
+}
+
+__global__ void __launch_bounds__(256)
+bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
+                     const float *__restrict__ beta, float d, const float *__restrict__ gamma,
+                     const float *__restrict__ W, const float *__restrict__ Mn,
+                     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ dR,
+                     const float *__restrict__ dMn1, const float *__restrict__ Pt,
+                     const float *__restrict__ DKt, __nv_bfloat16 *__restrict__ dq,
+                     __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
+                     float *__restrict__ dg, float *__restrict__ dbeta, int T) {
+    using namespace mm;
+    using sm100::ldsm_x4;
+    using sm100::ldsm_x4_t;
+    using sm100::mma16816;
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int NC = (T + C - 1) / C;
+    const int t0 = n * C, c = min(C, T - t0);
+    const int64_t row0 = (int64_t)bh * T + t0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const uint32_t sb = sm100::smem_u32(smb);
+    float *gs = reinterpret_cast<float *>(smb + OFF_SC);
+    float *bs = gs + C, *dbp = bs + C, *dbt = dbp + C, *rq = dbt + C, *rk = rq + C, *rz = rk + C;
+    float *vdr = rz + C, *red = vdr + C;
+    const float *Mp = Mn + ((int64_t)bh * NC + n) * D * D;
+    const float *dMp = dMn1 + ((int64_t)bh * NC + n) * D * D;
+    const int64_t tb = ((int64_t)bh * NC + n) * C * C;
+
+    // ---- 0. loads: q, k, dO as given; W, dR, M, dM' rounded to bf16
+    {
+        uint4 bq[4], bk[4], bo[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {   // 1024 16-byte pieces per C x 128 bf16 tile
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            const bool in = r < c;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            bq[u] = in ? ld16(q + (row0 + r) * D + col) : z;
+            bk[u] = in ? ld16(k + (row0 + r) * D + col) : z;
+            bo[u] = in ? ld16(dout + (row0 + r) * D + col) : z;
+        }
+        float4 fw[8], fr[8];
+        uint2 fv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {   // 2048 float4 per C x 128 fp32 tile: warp w, row w + 8u
+            const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
+            const bool in = r < c;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            fw[u] = in ? __ldg(reinterpret_cast<const float4 *>(W + (row0 + r) * D + col)) : z;
+            fr[u] = in ? __ldg(reinterpret_cast<const float4 *>(dR + (row0 + r) * D + col)) : z;
+            fv[u] = in ? __ldg(reinterpret_cast<const uint2 *>(v + (row0 + r) * D + col)) : make_uint2(0u, 0u);
+        }
+        for (int r = tid; r < C; r += 256) {
+            gs[r] = r < c ? gamma[row0 + r] : 1.f;
+            bs[r] = r < c ? beta[row0 + r] : 0.f;
+            dbp[r] = dbt[r] = rq[r] = rk[r] = rz[r] = 0.f;
+        }
+        if (tid == 0) red[0] = 0.f;
+        // dv = diag(beta) dR (from the fp32 dR) and v_r . dR_r, one warp per row
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
+            const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fv[u].x));
+            const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fv[u].y));
+            float p = fmaf(v01.x, fr[u].x, fmaf(v01.y, fr[u].y, fmaf(v23.x, fr[u].z, v23.y * fr[u].w)));
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if (lane == 0) vdr[r] = p;
+            if (r < c) {
+                const float br = beta[row0 + r];
+                *reinterpret_cast<uint2 *>(dv_out + (row0 + r) * D + col) =
+                    make_uint2(pack_bf2(br * fr[u].x, br * fr[u].y), pack_bf2(br * fr[u].z, br * fr[u].w));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            *reinterpret_cast<uint4 *>(smb + OFF_Q + 2 * (r * LD + col)) = bq[u];
+            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = bk[u];
+            *reinterpret_cast<uint4 *>(smb + OFF_O + 2 * (r * LD + col)) = bo[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
+            *reinterpret_cast<uint2 *>(smb + OFF_W + 2 * (r * LD + col)) =
+                make_uint2(pack_bf2(fw[u].x, fw[u].y), pack_bf2(fw[u].z, fw[u].w));
+            *reinterpret_cast<uint2 *>(smb + OFF_R + 2 * (r * LD + col)) =
+                make_uint2(pack_bf2(fr[u].x, fr[u].y), pack_bf2(fr[u].z, fr[u].w));
+        }
+        float mdm = 0.f;   // this thread's share of <M, dM'> (fp32, before rounding)
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {   // 4096 float4 per 128 x 128 tile, two batches
+            float4 fm[8], fd[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + 256 * (u + 8 * half), r = idx >> 5, col = (idx & 31) * 4;
+                fm[u] = __ldg(reinterpret_cast<const float4 *>(Mp + r * D + col));
+                fd[u] = __ldg(reinterpret_cast<const float4 *>(dMp + r * D + col));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + 256 * (u + 8 * half), r = idx >> 5, col = (idx & 31) * 4;
+                *reinterpret_cast<uint2 *>(smb + OFF_M + 2 * (r * LD + col)) =
+                    make_uint2(pack_bf2(fm[u].x, fm[u].y), pack_bf2(fm[u].z, fm[u].w));
+                *reinterpret_cast<uint2 *>(smb + OFF_DM + 2 * (r * LD + col)) =
+                    make_uint2(pack_bf2(fd[u].x, fd[u].y), pack_bf2(fd[u].z, fd[u].w));
+                mdm = fmaf(fm[u].x, fd[u].x, fmaf(fm[u].y, fd[u].y,
+                      fmaf(fm[u].z, fd[u].z, fmaf(fm[u].w, fd[u].w, mdm))));
+            }
+        }
+        for (int off = 16; off > 0; off >>= 1) mdm += __shfl_xor_sync(0xffffffffu, mdm, off);
+        __syncthreads();   // red[0] zeroed
+        if (lane == 0) atomicAdd(&red[0], mdm);
+    }
+    __syncthreads();
+
+    // ---- 1. position pairs: dP = dO W^T, dRW = dR W^T (rows mr .. mr + 15, columns nc .. nc + 31)
+    {
+        const int mr = 16 * (warp >> 1), nc = 32 * (warp & 1);
+        float ap[4][4], ar[4][4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ap[x][e] = ar[x][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t ao[4], aq[4];
+            ldsm_x4(ao, a_addr(sb + OFF_O, LD, mr, 16 * kk, lane));
+            ldsm_x4(aq, a_addr(sb + OFF_R, LD, mr, 16 * kk, lane));
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                uint32_t bw[4];
+                ldsm_x4(bw, b_addr(sb + OFF_W, LD, nc + 16 * np, 16 * kk, lane));
+                mma16816(ap[2 * np], ao, bw[0], bw[1]);
+                mma16816(ap[2 * np + 1], ao, bw[2], bw[3]);
+                mma16816(ar[2 * np], aq, bw[0], bw[1]);
+                mma16816(ar[2 * np + 1], aq, bw[2], bw[3]);
+            }
+        }
+        // FP = dP o D, FA = dA o beta D (dA = -dRW), the db and dbeta pair terms
+        float re[2] = {0.f, 0.f}, rt[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            float ce[2] = {0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {   // rows gq, gq + 8
+                const int r = mr + gq + 8 * h, s0 = nc + 8 * nt + 2 * t4;
+                const float2 pp = *reinterpret_cast<const float2 *>(Pt + tb + r * C + s0);
+                const float2 dd = *reinterpret_cast<const float2 *>(DKt + tb + r * C + s0);
+                const float pv[2] = {pp.x, pp.y}, dv2[2] = {dd.x, dd.y};
+                float fp[2] = {0.f, 0.f}, fa[2] = {0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int s = s0 + e;
+                    if (r < c && s <= r) {
+                        const float Dv = gs[r] / gs[s];
+                        const float dP = ap[nt][2 * h + e];
+                        fp[e] = dP * Dv;
+                        float ee = dP * pv[e];
+                        if (s < r) {
+                            const float dA = -ar[nt][2 * h + e];
+                            fa[e] = dA * bs[r] * Dv;
+                            ee = fmaf(dA * bs[r], dv2[e], ee);
+                            rt[h] = fmaf(dA, dv2[e], rt[h]);
+                        }
+                        re[h] += ee;
+                        ce[e] -= ee;
+                    }
+                }
+                *reinterpret_cast<uint32_t *>(smb + OFF_FP + 2 * (r * LC + s0)) = pack_bf2(fp[0], fp[1]);
+                *reinterpret_cast<uint32_t *>(smb + OFF_FA + 2 * (r * LC + s0)) = pack_bf2(fa[0], fa[1]);
+            }
+            // column sums over the 8 row lanes (gq) sharing the column
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float x = ce[e];
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                const int s = nc + 8 * nt + 2 * t4 + e;
+                if (gq == 0 && s < c) atomicAdd(&dbp[s], x);
+            }
+        }
+        // row sums over the 4 column lanes (t4) sharing the row
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float x = re[h], y = rt[h];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            y += __shfl_xor_sync(0xffffffffu, y, 1);
+            y += __shfl_xor_sync(0xffffffffu, y, 2);
+            const int r = mr + gq + 8 * h;
+            if (t4 == 0 && r < c) {
+                atomicAdd(&dbp[r], x);
+                atomicAdd(&dbt[r], y);
+            }
+        }
+    }
+    __syncthreads();   // FP and FA are in shared memory
+
+    // ---- 2. state terms (rows mr .. mr + 31, key columns nc .. nc + 31):
+    //         X1 = dO M^T, X2 = dR M^T, X3 = W dM'^T
+    const int mr = 32 * (warp >> 2), nc = 32 * (warp & 3);
+    float x1[2][4][4], x2[2][4][4], x3[2][4][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x1[a][b][e] = x2[a][b][e] = x3[a][b][e] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t ao[2][4], aq[2][4], aw[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            ldsm_x4(ao[mt], a_addr(sb + OFF_O, LD, mr + 16 * mt, 16 * kk, lane));
+            ldsm_x4(aq[mt], a_addr(sb + OFF_R, LD, mr + 16 * mt, 16 * kk, lane));
+            ldsm_x4(aw[mt], a_addr(sb + OFF_W, LD, mr + 16 * mt, 16 * kk, lane));
+        }
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+            uint32_t bm[4], bd[4];
+            ldsm_x4(bm, b_addr(sb + OFF_M, LD, nc + 16 * np, 16 * kk, lane));
+            ldsm_x4(bd, b_addr(sb + OFF_DM, LD, nc + 16 * np, 16 * kk, lane));
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                mma16816(x1[mt][2 * np], ao[mt], bm[0], bm[1]);
+                mma16816(x1[mt][2 * np + 1], ao[mt], bm[2], bm[3]);
+                mma16816(x2[mt][2 * np], aq[mt], bm[0], bm[1]);
+                mma16816(x2[mt][2 * np + 1], aq[mt], bm[2], bm[3]);
+                mma16816(x3[mt][2 * np], aw[mt], bd[0], bd[1]);
+                mma16816(x3[mt][2 * np + 1], aw[mt], bd[2], bd[3]);
+            }
+        }
+    }
+    // row dots q.(M dO), k.(M dR), k.(dM' w) over this warp's 32 key columns (the four
+    // column warps add up in shared memory); then the state terms of dQ (x1) and dK (x2)
+    {
+        const float gC = gs[c - 1];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = mr + 16 * mt + gq + 8 * h;
+                float pq = 0.f, pk = 0.f, pz = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int i = nc + 8 * nt + 2 * t4;
+                    const float2 qf = __bfloat1622float2(
+                        *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_Q + 2 * (r * LD + i)));
+                    const float2 kf = __bfloat1622float2(
+                        *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_K + 2 * (r * LD + i)));
+                    pq = fmaf(qf.x, x1[mt][nt][2 * h], fmaf(qf.y, x1[mt][nt][2 * h + 1], pq));
+                    pk = fmaf(kf.x, x2[mt][nt][2 * h], fmaf(kf.y, x2[mt][nt][2 * h + 1], pk));
+                    pz = fmaf(kf.x, x3[mt][nt][2 * h], fmaf(kf.y, x3[mt][nt][2 * h + 1], pz));
+                }
+                pq += __shfl_xor_sync(0xffffffffu, pq, 1);
+                pq += __shfl_xor_sync(0xffffffffu, pq, 2);
+                pk += __shfl_xor_sync(0xffffffffu, pk, 1);
+                pk += __shfl_xor_sync(0xffffffffu, pk, 2);
+                pz += __shfl_xor_sync(0xffffffffu, pz, 1);
+                pz += __shfl_xor_sync(0xffffffffu, pz, 2);
+                if (t4 == 0 && r < c) {
+                    atomicAdd(&rq[r], pq);
+                    atomicAdd(&rk[r], pk);
+                    atomicAdd(&rz[r], pz);
+                }
+                const float gr = gs[r], sc = gC / gr, gb = gr * bs[r];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        x1[mt][nt][2 * h + e] *= gr;
+                        x2[mt][nt][2 * h + e] = fmaf(sc, x3[mt][nt][2 * h + e], -gb * x2[mt][nt][2 * h + e]);
+                    }
+            }
+    }
+
+    // ---- 3. in-chunk terms: dQ += FP K,  dK += FP^T Q + FA K + FA^T K
+#pragma unroll
+    for (int ks = 0; ks < C / 16; ++ks) {
+        uint32_t afp[2][4], afpt[2][4], afa[2][4], afat[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            ldsm_x4(afp[mt], a_addr(sb + OFF_FP, LC, mr + 16 * mt, 16 * ks, lane));
+            ldsm_x4_t(afpt[mt], at_addr(sb + OFF_FP, LC, mr + 16 * mt, 16 * ks, lane));
+            ldsm_x4(afa[mt], a_addr(sb + OFF_FA, LC, mr + 16 * mt, 16 * ks, lane));
+            ldsm_x4_t(afat[mt], at_addr(sb + OFF_FA, LC, mr + 16 * mt, 16 * ks, lane));
+        }
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+            uint32_t bk[4], bq[4];
+            ldsm_x4_t(bk, bt_addr(sb + OFF_K, LD, nc + 16 * np, 16 * ks, lane));
+            ldsm_x4_t(bq, bt_addr(sb + OFF_Q, LD, nc + 16 * np, 16 * ks, lane));
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int nt = 2 * np + hh;
+                    const uint32_t k0 = bk[2 * hh], k1 = bk[2 * hh + 1], q0 = bq[2 * hh], q1 = bq[2 * hh + 1];
+                    mma16816(x1[mt][nt], afp[mt], k0, k1);
+                    mma16816(x2[mt][nt], afpt[mt], q0, q1);
+                    mma16816(x2[mt][nt], afa[mt], k0, k1);
+                    mma16816(x2[mt][nt], afat[mt], k0, k1);
+                }
+        }
+    }
+
+    // ---- 4. dQ and dK through shared memory (the dO and W tiles are dead) into
+    //         16-byte stores; then dbeta, db and dg per row
+    __syncthreads();
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = mr + 16 * mt + gq + 8 * h, i = nc + 8 * nt + 2 * t4;
+                *reinterpret_cast<uint32_t *>(smb + OFF_O + 2 * (r * LD + i)) =
+                    pack_bf2(x1[mt][nt][2 * h], x1[mt][nt][2 * h + 1]);
+                *reinterpret_cast<uint32_t *>(smb + OFF_W + 2 * (r * LD + i)) =
+                    pack_bf2(x2[mt][nt][2 * h], x2[mt][nt][2 * h + 1]);
+            }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+        if (r < c) {
+            *reinterpret_cast<uint4 *>(dq + (row0 + r) * D + col) =
+                *reinterpret_cast<const uint4 *>(smb + OFF_O + 2 * (r * LD + col));
+            *reinterpret_cast<uint4 *>(dk_out + (row0 + r) * D + col) =
+                *reinterpret_cast<const uint4 *>(smb + OFF_W + 2 * (r * LD + col));
+        }
+    }
+    if (warp == 0) {
+        const float gC = gs[c - 1];
+        float zsum = 0.f;
+        float db[2] = {0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * lane + e;
+            if (r < c) {
+                dbeta[row0 + r] = dbt[r] + vdr[r] - gs[r] * rk[r];
+                const float z = gC / gs[r] * rz[r];
+                zsum += z;
+                db[e] = dbp[r] + gs[r] * rq[r] - gs[r] * bs[r] * rk[r] - z;
+            }
+        }
+        for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
+        const float last = zsum + gC * red[0];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            if (2 * lane + e == c - 1) db[e] += last;
+        float suf = db[0] + db[1];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf += y;
+        }
+        const float dl[2] = {suf, suf - db[0]};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * lane + e;
+            if (r < c) dg[row0 + r] = dl[e] * dlog_alpha_dg(g[row0 + r], d);
+        }
+    }
+}
+
 template <typename K>
 cudaError_t bwd_set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -1102,6 +1510,17 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if constexpr (std::is_same<TE, __nv_bfloat16>::value) {
+        if (dk == mm::D && dv == mm::D && C == mm::C &&
+            ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk_out) |
+              reinterpret_cast<uintptr_t>(dv_out)) & 15) == 0) {
+            if ((err = bwd_set_smem(bwd_chunk_mma_kernel, mm::SMEM)) != cudaSuccess) return err;
+            bwd_chunk_mma_kernel<<<dim3(NC, BH), 256, mm::SMEM, s>>>(
+                q, k, v, g, beta, d, gamma, W, Mn, dout, dR, dMn1, Pt, DKt, dq, dk_out, dv_out, dg,
+                dbeta, T);
+            return cudaGetLastError();
+        }
+    }
     const size_t s2 = chunk_smem(dk, dv, C);
     if ((err = bwd_set_smem(bwd_chunk_kernel<TE>, s2)) != cudaSuccess) return err;
     bwd_chunk_kernel<TE><<<dim3(NC, BH), kBwdThreads, s2, s>>>(
