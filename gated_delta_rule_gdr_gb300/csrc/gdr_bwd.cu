@@ -1438,6 +1438,247 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     }
 }
 
+// ---------------------------------------------------------------- reverse chain, warp MMA
+// The reverse chain of the bf16 d = 128, chunk-64 shape on warp MMAs (m16n8k16, bf16
+// operands, fp32 accumulation).  One CTA per (32 value columns, bh), 8 warps.  The
+// running dM[:, slice] (128 x 32) stays in fp32 accumulator fragments for the whole
+// pass, warp w owning key rows 16w .. 16w + 15; its bf16 copy in shared memory is
+// the operand of the next chunk's K dM'.  Per chunk:
+//   1. dW = P^T dO + diag(gamma_C / gamma) K dM'  (warp: rows 16 (w >> 1), columns 16 (w & 1))
+//   2. dR = T^T dW (stored fp32); -gamma beta dR to shared memory as bf16
+//   3. dM = gamma_C dM' + Q^T (gamma dO) + K^T (-gamma beta dR)
+// P and T are unit-/lower-triangular, so their transposes' row block b only meets
+// column blocks >= b.  The next chunk's inputs wait in registers while this one
+// computes, as in bwd_chain_kernel.
+namespace mc {
+constexpr int C = 64, DK = 128, DS = 32, LD = DK + 8, LC = C + 8, LS = DS + 8;
+constexpr uint32_t OFF_K = 0, OFF_Q = OFF_K + C * LD * 2, OFF_P = OFF_Q + C * LD * 2,
+                   OFF_T = OFF_P + C * LC * 2, OFF_DO = OFF_T + C * LC * 2,
+                   OFF_GDO = OFF_DO + C * LS * 2, OFF_DW = OFF_GDO + C * LS * 2,
+                   OFF_RG = OFF_DW + C * LS * 2, OFF_DM = OFF_RG + C * LS * 2,
+                   OFF_G = OFF_DM + DK * LS * 2;
+constexpr uint32_t SMEM = OFF_G + 2 * C * 4;
+}  // namespace mc
+
+struct ChainStageMma {
+    uint4 kq[2][4];    // 1024 16-byte pieces of k and of q (64 x 128 bf16)
+    float4 pt[2][4];   // 1024 float4 of P and of T
+    uint4 o;           // dO row tid / 4, columns 8 (tid % 4) .. + 7 of the slice
+    float go;          // gamma of that row
+    float gb[2];       // gamma, beta of row tid (tid < 64)
+    __device__ __forceinline__ void load(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                         const __nv_bfloat16 *dout, const float *gamma,
+                                         const float *beta, const float *Pp, const float *Tp,
+                                         int64_t row0, int c, int dv, int j0s, int tid) {
+        using namespace mc;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            kq[0][u] = r < c ? ld16(k + (row0 + r) * DK + col) : z;
+            kq[1][u] = r < c ? ld16(q + (row0 + r) * DK + col) : z;
+            pt[0][u] = __ldg(reinterpret_cast<const float4 *>(Pp) + idx);
+            pt[1][u] = __ldg(reinterpret_cast<const float4 *>(Tp) + idx);
+        }
+        const int r = tid >> 2, col = (tid & 3) * 8;
+        o = r < c ? ld16(dout + (row0 + r) * dv + j0s + col) : z;
+        go = r < c ? gamma[row0 + r] : 0.f;
+        if (tid < C) {
+            gb[0] = tid < c ? gamma[row0 + tid] : 1.f;
+            gb[1] = tid < c ? beta[row0 + tid] : 0.f;
+        }
+    }
+    __device__ __forceinline__ void store(uint8_t *smb, int tid) const {
+        using namespace mc;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = kq[0][u];
+            *reinterpret_cast<uint4 *>(smb + OFF_Q + 2 * (r * LD + col)) = kq[1][u];
+            const int rp = idx >> 4, cp = (idx & 15) * 4;
+            *reinterpret_cast<uint2 *>(smb + OFF_P + 2 * (rp * LC + cp)) =
+                make_uint2(pack_bf2(pt[0][u].x, pt[0][u].y), pack_bf2(pt[0][u].z, pt[0][u].w));
+            *reinterpret_cast<uint2 *>(smb + OFF_T + 2 * (rp * LC + cp)) =
+                make_uint2(pack_bf2(pt[1][u].x, pt[1][u].y), pack_bf2(pt[1][u].z, pt[1][u].w));
+        }
+        const int r = tid >> 2, col = (tid & 3) * 8;
+        *reinterpret_cast<uint4 *>(smb + OFF_DO + 2 * (r * LS + col)) = o;
+        float f[8];
+        widen16(o, f, (const __nv_bfloat16 *)nullptr);
+        *reinterpret_cast<uint4 *>(smb + OFF_GDO + 2 * (r * LS + col)) =
+            make_uint4(pack_bf2(go * f[0], go * f[1]), pack_bf2(go * f[2], go * f[3]),
+                       pack_bf2(go * f[4], go * f[5]), pack_bf2(go * f[6], go * f[7]));
+        if (tid < C) {
+            float *gs = reinterpret_cast<float *>(smb + OFF_G);
+            gs[tid] = gb[0];
+            gs[C + tid] = gb[1];
+        }
+    }
+};
+
+__global__ void __launch_bounds__(256, 2)
+bwd_chain_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                     const float *__restrict__ gamma, const float *__restrict__ beta,
+                     const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
+                     const float *__restrict__ Pt, const float *__restrict__ Tt,
+                     float *__restrict__ dR, float *__restrict__ dMn1, float *dinit, int T, int dv) {
+    using namespace mc;
+    using sm100::ldsm_x4;
+    using sm100::ldsm_x4_t;
+    using sm100::mma16816;
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int j0s = blockIdx.x * DS, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const uint32_t sb = sm100::smem_u32(smb);
+    const float *gs = reinterpret_cast<const float *>(smb + OFF_G), *bs = gs + C;
+    const int NC = (T + C - 1) / C;
+    const int m1 = warp >> 1, n1 = 16 * (warp & 1);   // steps 1 and 2: row block, first column
+    auto tile_p = [&](int n) { return Pt + ((int64_t)bh * NC + n) * C * C; };
+    auto tile_t = [&](int n) { return Tt + ((int64_t)bh * NC + n) * C * C; };
+    // dM fragments: rows 16 warp + gq (+ 8 for elements 2, 3), columns 8 nt + 2 t4 (+ 1),
+    // as offsets into one head's dk x dv state
+    auto dm_off = [&](int nt, int h) {
+        return (int64_t)(16 * warp + gq + 8 * h) * dv + j0s + 8 * nt + 2 * t4;
+    };
+    const int64_t head = (int64_t)DK * dv;
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float *src = dfinal + bh * head + dm_off(nt, h);   // 4-byte aligned only
+            acc[nt][2 * h] = dfinal ? src[0] : 0.f;
+            acc[nt][2 * h + 1] = dfinal ? src[1] : 0.f;
+        }
+    auto publish_dm = [&]() {   // bf16 copy of dM for the next chunk's K dM'
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                *reinterpret_cast<uint32_t *>(smb + OFF_DM + 2 * ((16 * warp + gq + 8 * h) * LS + 8 * nt + 2 * t4)) =
+                    pack_bf2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+    };
+    publish_dm();
+    ChainStageMma stage;
+    {
+        const int n = NC - 1;
+        stage.load(q, k, dout, gamma, beta, tile_p(n), tile_t(n), (int64_t)bh * T + n * C, T - n * C,
+                   dv, j0s, tid);
+        stage.store(smb, tid);
+    }
+    for (int n = NC - 1; n >= 0; --n) {
+        const int t0 = n * C, c = min(C, T - t0);
+        const int64_t row0 = (int64_t)bh * T + t0;
+        __syncthreads();   // chunk n's inputs and dM' (bf16) are in shared memory
+        if (n > 0)
+            stage.load(q, k, dout, gamma, beta, tile_p(n - 1), tile_t(n - 1), row0 - C, C, dv, j0s, tid);
+        {   // dM' of chunk n, fp32
+            float *dst = dMn1 + ((int64_t)bh * NC + n) * head;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2 *>(dst + dm_off(nt, h)) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+        }
+        const float gC = gs[c - 1];
+        // 1. dW
+        {
+            float a1[2][4], a2[2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a1[x][e] = a2[x][e] = 0.f;
+            for (int ks = m1; ks < C / 16; ++ks) {
+                uint32_t a[4], b[4];
+                ldsm_x4_t(a, at_addr(sb + OFF_P, LC, 16 * m1, 16 * ks, lane));
+                ldsm_x4_t(b, bt_addr(sb + OFF_DO, LS, n1, 16 * ks, lane));
+                mma16816(a1[0], a, b[0], b[1]);
+                mma16816(a1[1], a, b[2], b[3]);
+            }
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                uint32_t a[4], b[4];
+                ldsm_x4(a, a_addr(sb + OFF_K, LD, 16 * m1, 16 * kk, lane));
+                ldsm_x4_t(b, bt_addr(sb + OFF_DM, LS, n1, 16 * kk, lane));
+                mma16816(a2[0], a, b[0], b[1]);
+                mma16816(a2[1], a, b[2], b[3]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = 16 * m1 + gq + 8 * h;
+                const float sc = r < c ? gC / gs[r] : 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                    *reinterpret_cast<uint32_t *>(smb + OFF_DW + 2 * (r * LS + n1 + 8 * nt + 2 * t4)) =
+                        pack_bf2(fmaf(sc, a2[nt][2 * h], a1[nt][2 * h]), fmaf(sc, a2[nt][2 * h + 1], a1[nt][2 * h + 1]));
+            }
+        }
+        __syncthreads();
+        // 2. dR = T^T dW
+        {
+            float a1[2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a1[x][e] = 0.f;
+            for (int ks = m1; ks < C / 16; ++ks) {
+                uint32_t a[4], b[4];
+                ldsm_x4_t(a, at_addr(sb + OFF_T, LC, 16 * m1, 16 * ks, lane));
+                ldsm_x4_t(b, bt_addr(sb + OFF_DW, LS, n1, 16 * ks, lane));
+                mma16816(a1[0], a, b[0], b[1]);
+                mma16816(a1[1], a, b[2], b[3]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = 16 * m1 + gq + 8 * h;
+                const float ngb = -gs[r] * bs[r];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = n1 + 8 * nt + 2 * t4;
+                    const float x0 = a1[nt][2 * h], x1 = a1[nt][2 * h + 1];
+                    *reinterpret_cast<uint32_t *>(smb + OFF_RG + 2 * (r * LS + j)) = pack_bf2(ngb * x0, ngb * x1);
+                    if (r < c) *reinterpret_cast<float2 *>(dR + (row0 + r) * dv + j0s + j) = make_float2(x0, x1);
+                }
+            }
+        }
+        __syncthreads();
+        // 3. dM = gamma_C dM' + Q^T (gamma dO) + K^T (-gamma beta dR)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] *= gC;
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+            uint32_t aq[4], ak[4];
+            ldsm_x4_t(aq, at_addr(sb + OFF_Q, LD, 16 * warp, 16 * ks, lane));
+            ldsm_x4_t(ak, at_addr(sb + OFF_K, LD, 16 * warp, 16 * ks, lane));
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                uint32_t bo[4], br[4];
+                ldsm_x4_t(bo, bt_addr(sb + OFF_GDO, LS, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(br, bt_addr(sb + OFF_RG, LS, 16 * np, 16 * ks, lane));
+                mma16816(acc[2 * np], aq, bo[0], bo[1]);
+                mma16816(acc[2 * np + 1], aq, bo[2], bo[3]);
+                mma16816(acc[2 * np], ak, br[0], br[1]);
+                mma16816(acc[2 * np + 1], ak, br[2], br[3]);
+            }
+        }
+        publish_dm();   // step 1 of this chunk read the old copy before the second barrier
+        __syncthreads();   // every read of chunk n's inputs is done
+        if (n > 0) stage.store(smb, tid);
+    }
+    if (dinit) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float *dst = dinit + bh * head + dm_off(nt, h);
+                dst[0] = acc[nt][2 * h];
+                dst[1] = acc[nt][2 * h + 1];
+            }
+    }
+}
+
 template <typename K>
 cudaError_t bwd_set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -1498,7 +1739,15 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
         }
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    if (dv >= 32) {
+    constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
+    const bool mma_shape = kBf16 && dk == 128 && dv == 128 && C == 64;
+    if (mma_shape) {
+        if constexpr (kBf16) {
+            if ((err = bwd_set_smem(bwd_chain_mma_kernel, mc::SMEM)) != cudaSuccess) return err;
+            bwd_chain_mma_kernel<<<dim3(dv / mc::DS, BH), 256, mc::SMEM, s>>>(
+                q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dv);
+        }
+    } else if (dv >= 32) {
         const size_t s1 = chain_smem(dk, 32, C, sizeof(TE));
         if ((err = bwd_set_smem(bwd_chain_kernel<TE, 32>, s1)) != cudaSuccess) return err;
         bwd_chain_kernel<TE, 32><<<dim3(dv / 32, BH), 256, s1, s>>>(
@@ -1510,8 +1759,8 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if constexpr (std::is_same<TE, __nv_bfloat16>::value) {
-        if (dk == mm::D && dv == mm::D && C == mm::C &&
+    if constexpr (kBf16) {
+        if (mma_shape &&
             ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk_out) |
               reinterpret_cast<uintptr_t>(dv_out)) & 15) == 0) {
             if ((err = bwd_set_smem(bwd_chunk_mma_kernel, mm::SMEM)) != cudaSuccess) return err;

@@ -3,12 +3,12 @@ oracle's reverse-mode gradients on the same seeded inputs and cotangents.
 
 Tolerance (relative L2 per gradient tensor): the forward's, 1e-5 on the fp32
 path (every gradient is formed in fp32; measured ~3e-7), and 5e-3 on the bf16
-path.  There dq, dk, dv are rounded to bf16 (2^-9 relative per element: dv, a
-scaled copy of the fp32 dR, measures 1.7e-3), and the per-chunk products of the
-d = 128, chunk-64 shape run on tensor cores with the fp32 intermediates (W, dR,
-the chunk states M and dM', the masked pair gradients) rounded to bf16 operands:
-dq and dk measure ~3e-3, dg ~2e-3 and dbeta ~5e-4; the initial state's gradient
-comes from the fp32 reverse chain (~3e-7)."""
+path.  There dq, dk, dv are rounded to bf16 (2^-9 relative per element), and the
+reverse chain and the per-chunk products of the d = 128, chunk-64 shape run on
+tensor cores with the fp32 intermediates (P, T, dW, dR, W, the chunk states M and
+dM', the masked pair gradients) rounded to bf16 operands and fp32 accumulation
+(the running dM stays fp32): dq, dk, dv and dbeta measure ~3e-3, dg ~2e-3 and the
+initial state's gradient ~1.8e-3."""
 from __future__ import annotations
 
 import numpy as np
