@@ -1679,6 +1679,468 @@ bwd_chain_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     }
 }
 
+// ---------------------------------------------------------------- forward state, warp MMA
+// The forward's state pass of the bf16 d = 128, chunk-64 shape on warp MMAs.  Its
+// fp32 operands go in as two bf16 terms x = hi + lo (hi = bf16(x), lo = bf16(x - hi),
+// relative error ~2^-17): W = U - (Wk_hi + Wk_lo)(M_hi + M_lo) drops only the lo x lo
+// product, and M' = gamma_C M + K^T diag(gamma_C / gamma) W takes k exactly, so W and
+// the chunk states keep near-fp32 accuracy.  M[:, slice] (128 x 32) stays in fp32
+// accumulator fragments, warp w owning key rows 16w .. 16w + 15; W in 16 x 16 warp
+// tiles (rows 16 (w >> 1), columns 16 (w & 1)).  One CTA per (32 value columns, bh).
+namespace mf {
+constexpr int C = 64, DK = 128, DS = 32, LD = DK + 8, LS = DS + 8;
+constexpr uint32_t OFF_K = 0, OFF_WKH = OFF_K + C * LD * 2, OFF_WKL = OFF_WKH + C * LD * 2,
+                   OFF_MH = OFF_WKL + C * LD * 2, OFF_ML = OFF_MH + DK * LS * 2,
+                   OFF_WSH = OFF_ML + DK * LS * 2, OFF_WSL = OFF_WSH + C * LS * 2,
+                   OFF_G = OFF_WSL + C * LS * 2;
+constexpr uint32_t SMEM = OFF_G + C * 4;
+}  // namespace mf
+
+// x = hi + lo in bf16 pairs
+__device__ __forceinline__ void split_bf2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = pack_bf2(a - hf.x, b - hf.y);
+}
+
+struct FwdStageMma {
+    uint4 kk[4];     // 1024 16-byte pieces of k (64 x 128 bf16)
+    float4 wk[8];    // 2048 float4 of Wk
+    float u[2][2][2];   // U at this lane's W fragment: [h][nt] pairs
+    float gm;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *k, const float *Wk, const float *U,
+                                         const float *gamma, int64_t row0, int c, int dv, int j0s,
+                                         int tid, int ur0, int uc0) {
+        using namespace mf;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int idx = tid + 256 * x, r = idx >> 4, col = (idx & 15) * 8;
+            kk[x] = r < c ? ld16(k + (row0 + r) * DK + col) : z;
+        }
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const int idx = tid + 256 * x, r = idx >> 5, col = (idx & 31) * 4;
+            wk[x] = r < c ? __ldg(reinterpret_cast<const float4 *>(Wk + (row0 + r) * DK + col))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int r = ur0 + 8 * h;
+                float2 x = make_float2(0.f, 0.f);
+                if (r < c) x = __ldg(reinterpret_cast<const float2 *>(U + (row0 + r) * dv + j0s + uc0 + 8 * nt));
+                u[h][nt][0] = x.x;
+                u[h][nt][1] = x.y;
+            }
+        if (tid < C) gm = tid < c ? gamma[row0 + tid] : 1.f;
+    }
+    __device__ __forceinline__ void store(uint8_t *smb, int tid) const {
+        using namespace mf;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int idx = tid + 256 * x, r = idx >> 4, col = (idx & 15) * 8;
+            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = kk[x];
+        }
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const int idx = tid + 256 * x, r = idx >> 5, col = (idx & 31) * 4;
+            uint32_t h0, l0, h1, l1;
+            split_bf2(wk[x].x, wk[x].y, h0, l0);
+            split_bf2(wk[x].z, wk[x].w, h1, l1);
+            *reinterpret_cast<uint2 *>(smb + OFF_WKH + 2 * (r * LD + col)) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(smb + OFF_WKL + 2 * (r * LD + col)) = make_uint2(l0, l1);
+        }
+        if (tid < C) reinterpret_cast<float *>(smb + OFF_G)[tid] = gm;
+    }
+};
+
+__global__ void __launch_bounds__(256, 2)
+bwd_fwd_state_mma_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ gamma,
+                         const float *__restrict__ U, const float *__restrict__ Wk, const float *init,
+                         float *__restrict__ W, float *__restrict__ Mn, int T, int dv) {
+    using namespace mf;
+    using sm100::ldsm_x4;
+    using sm100::ldsm_x4_t;
+    using sm100::mma16816;
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int j0s = blockIdx.x * DS, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const uint32_t sb = sm100::smem_u32(smb);
+    const float *gs = reinterpret_cast<const float *>(smb + OFF_G);
+    const int NC = (T + C - 1) / C;
+    const int m1 = warp >> 1, n1 = 16 * (warp & 1);
+    const int ur0 = 16 * m1 + gq, uc0 = n1 + 2 * t4;   // this lane's W fragment origin
+    const int64_t head = (int64_t)DK * dv;
+    auto m_off = [&](int nt, int h) {
+        return (int64_t)(16 * warp + gq + 8 * h) * dv + j0s + 8 * nt + 2 * t4;
+    };
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float *src = init + bh * head + m_off(nt, h);   // 4-byte aligned only
+            acc[nt][2 * h] = init ? src[0] : 0.f;
+            acc[nt][2 * h + 1] = init ? src[1] : 0.f;
+        }
+    auto publish_m = [&]() {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t hi, lo;
+                split_bf2(acc[nt][2 * h], acc[nt][2 * h + 1], hi, lo);
+                const uint32_t o = 2 * ((16 * warp + gq + 8 * h) * LS + 8 * nt + 2 * t4);
+                *reinterpret_cast<uint32_t *>(smb + OFF_MH + o) = hi;
+                *reinterpret_cast<uint32_t *>(smb + OFF_ML + o) = lo;
+            }
+    };
+    publish_m();
+    FwdStageMma stage;
+    stage.load(k, Wk, U, gamma, (int64_t)bh * T, min(C, T), dv, j0s, tid, ur0, uc0);
+    stage.store(smb, tid);
+    float uc[2][2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) uc[h][nt][0] = stage.u[h][nt][0], uc[h][nt][1] = stage.u[h][nt][1];
+    for (int n = 0; n < NC; ++n) {
+        const int t0 = n * C, c = min(C, T - t0);
+        const int64_t row0 = (int64_t)bh * T + t0;
+        __syncthreads();   // chunk n's inputs and M (hi, lo) are in shared memory
+        if (n + 1 < NC)
+            stage.load(k, Wk, U, gamma, row0 + C, min(C, T - t0 - C), dv, j0s, tid, ur0, uc0);
+        {
+            float *dst = Mn + ((int64_t)bh * NC + n) * head;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2 *>(dst + m_off(nt, h)) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+        }
+        const float gC = gs[c - 1];
+        // W = U - Wk M
+        {
+            float w[2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[x][e] = 0.f;
+#pragma unroll 4
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                uint32_t ah[4], al[4], bh4[4], bl4[4];
+                ldsm_x4(ah, a_addr(sb + OFF_WKH, LD, 16 * m1, 16 * kk, lane));
+                ldsm_x4(al, a_addr(sb + OFF_WKL, LD, 16 * m1, 16 * kk, lane));
+                ldsm_x4_t(bh4, bt_addr(sb + OFF_MH, LS, n1, 16 * kk, lane));
+                ldsm_x4_t(bl4, bt_addr(sb + OFF_ML, LS, n1, 16 * kk, lane));
+                mma16816(w[0], ah, bh4[0], bh4[1]);
+                mma16816(w[1], ah, bh4[2], bh4[3]);
+                mma16816(w[0], al, bh4[0], bh4[1]);
+                mma16816(w[1], al, bh4[2], bh4[3]);
+                mma16816(w[0], ah, bl4[0], bl4[1]);
+                mma16816(w[1], ah, bl4[2], bl4[3]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = ur0 + 8 * h;
+                const float sc = r < c ? gC / gs[r] : 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = uc0 + 8 * nt;
+                    const float w0 = uc[h][nt][0] - w[nt][2 * h], w1 = uc[h][nt][1] - w[nt][2 * h + 1];
+                    if (r < c) *reinterpret_cast<float2 *>(W + (row0 + r) * dv + j0s + j) = make_float2(w0, w1);
+                    uint32_t hi, lo;
+                    split_bf2(sc * w0, sc * w1, hi, lo);
+                    *reinterpret_cast<uint32_t *>(smb + OFF_WSH + 2 * (r * LS + j)) = hi;
+                    *reinterpret_cast<uint32_t *>(smb + OFF_WSL + 2 * (r * LS + j)) = lo;
+                }
+            }
+        }
+        __syncthreads();
+        // M <- gamma_C M + K^T diag(gamma_C / gamma) W
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] *= gC;
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+            uint32_t ak[4];
+            ldsm_x4_t(ak, at_addr(sb + OFF_K, LD, 16 * warp, 16 * ks, lane));
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                uint32_t bh4[4], bl4[4];
+                ldsm_x4_t(bh4, bt_addr(sb + OFF_WSH, LS, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bl4, bt_addr(sb + OFF_WSL, LS, 16 * np, 16 * ks, lane));
+                mma16816(acc[2 * np], ak, bh4[0], bh4[1]);
+                mma16816(acc[2 * np + 1], ak, bh4[2], bh4[3]);
+                mma16816(acc[2 * np], ak, bl4[0], bl4[1]);
+                mma16816(acc[2 * np + 1], ak, bl4[2], bl4[3]);
+            }
+        }
+        publish_m();   // step W of this chunk read the old copy before the second barrier
+        __syncthreads();   // every read of chunk n's inputs is done
+        if (n + 1 < NC) {
+            stage.store(smb, tid);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) uc[h][nt][0] = stage.u[h][nt][0], uc[h][nt][1] = stage.u[h][nt][1];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- chunk tiles, warp MMA
+// The chunk tiles of the bf16 d = 128, chunk-64 shape: Q K^T and K K^T on warp MMAs
+// (bf16 inputs, exact products, fp32 sums), T = (I + A)^-1 solved blockwise in fp32
+// (the four 16 x 16 diagonal blocks a column per lane, then the off-diagonal blocks
+// by distance from the diagonal: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj), and
+// U = (T diag(beta)) V, Wk = (T diag(beta gamma)) K on warp MMAs with the fp32 left
+// factors as bf16 hi + lo pairs (v and k exact).  Outputs as bwd_tiles_kernel.
+namespace mt {
+constexpr int C = 64, DK = 128, LD = DK + 8, LA = C + 4, LC = C + 8;
+constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + C * LD * 2, OFF_R1 = OFF_V + C * LD * 2,
+                   R_BYTES = 2 * C * LC * 2, OFF_R2 = OFF_R1 + R_BYTES, OFF_X = OFF_R2 + R_BYTES,
+                   OFF_G = OFF_X + 3 * 16 * 20 * 4;
+constexpr uint32_t SMEM = OFF_G + 2 * C * 4;
+static_assert(C * LD * 2 <= R_BYTES && C * LA * 4 <= R_BYTES, "region 1 holds q, then A");
+}  // namespace mt
+
+// T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj for one 16 x 16 block, by one warp: lane owns
+// row lane / 2, columns 8 (lane % 2) .. + 7; X goes through the warp's scratch tile.
+__device__ __forceinline__ void solve_offdiag(const float *As, float *Ts, float *Xs, int i, int j,
+                                              int lane) {
+    using namespace mt;
+    const int rr = lane >> 1, cc = 8 * (lane & 1);
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+    for (int m = j; m < i; ++m) {
+#pragma unroll 4
+        for (int q = 0; q < 16; ++q) {
+            const float a = As[(16 * i + rr) * LA + 16 * m + q];
+            const float4 t0 = *reinterpret_cast<const float4 *>(Ts + (16 * m + q) * LA + 16 * j + cc);
+            const float4 t1 = *reinterpret_cast<const float4 *>(Ts + (16 * m + q) * LA + 16 * j + cc + 4);
+            x[0] = fmaf(a, t0.x, x[0]); x[1] = fmaf(a, t0.y, x[1]);
+            x[2] = fmaf(a, t0.z, x[2]); x[3] = fmaf(a, t0.w, x[3]);
+            x[4] = fmaf(a, t1.x, x[4]); x[5] = fmaf(a, t1.y, x[5]);
+            x[6] = fmaf(a, t1.z, x[6]); x[7] = fmaf(a, t1.w, x[7]);
+        }
+    }
+    *reinterpret_cast<float4 *>(Xs + rr * 20 + cc) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4 *>(Xs + rr * 20 + cc + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    __syncwarp();
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < 16; ++q) {
+        const float a = Ts[(16 * i + rr) * LA + 16 * i + q];
+        const float4 x0 = *reinterpret_cast<const float4 *>(Xs + q * 20 + cc);
+        const float4 x1 = *reinterpret_cast<const float4 *>(Xs + q * 20 + cc + 4);
+        y[0] = fmaf(a, x0.x, y[0]); y[1] = fmaf(a, x0.y, y[1]);
+        y[2] = fmaf(a, x0.z, y[2]); y[3] = fmaf(a, x0.w, y[3]);
+        y[4] = fmaf(a, x1.x, y[4]); y[5] = fmaf(a, x1.y, y[5]);
+        y[6] = fmaf(a, x1.z, y[6]); y[7] = fmaf(a, x1.w, y[7]);
+    }
+    *reinterpret_cast<float4 *>(Ts + (16 * i + rr) * LA + 16 * j + cc) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+    *reinterpret_cast<float4 *>(Ts + (16 * i + rr) * LA + 16 * j + cc + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+}
+
+__global__ void __launch_bounds__(256, 2)
+bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
+                     const float *__restrict__ beta, float *__restrict__ Pt, float *__restrict__ Tt,
+                     float *__restrict__ DKt, float *__restrict__ U, float *__restrict__ Wk, int T) {
+    using namespace mt;
+    using sm100::ldsm_x4;
+    using sm100::ldsm_x4_t;
+    using sm100::mma16816;
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int NC = (T + C - 1) / C;
+    const int t0 = n * C, c = min(C, T - t0);
+    const int64_t row0 = (int64_t)bh * T + t0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const uint32_t sb = sm100::smem_u32(smb);
+    float *As = reinterpret_cast<float *>(smb + OFF_R1);   // after the pair products
+    float *Ts = reinterpret_cast<float *>(smb + OFF_R2);
+    float *gs = reinterpret_cast<float *>(smb + OFF_G), *bs = gs + C;
+    const int64_t tb = ((int64_t)bh * NC + n) * C * C;
+
+    {   // q (into region 1), k, v as given; rows past the chunk's end zero
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        uint4 bq[4], bk[4], bv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            const bool in = r < c;
+            bq[u] = in ? ld16(q + (row0 + r) * DK + col) : z;
+            bk[u] = in ? ld16(k + (row0 + r) * DK + col) : z;
+            bv[u] = in ? ld16(v + (row0 + r) * DK + col) : z;
+        }
+        if (tid < C) {
+            gs[tid] = tid < c ? gamma[row0 + tid] : 1.f;
+            bs[tid] = tid < c ? beta[row0 + tid] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            *reinterpret_cast<uint4 *>(smb + OFF_R1 + 2 * (r * LD + col)) = bq[u];
+            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = bk[u];
+            *reinterpret_cast<uint4 *>(smb + OFF_V + 2 * (r * LD + col)) = bv[u];
+        }
+    }
+    __syncthreads();
+
+    // Q K^T and K K^T: warp tile rows 16 (w >> 1), columns 32 (w & 1) (the two tiles
+    // wholly above the diagonal skip the products)
+    const int mb = warp >> 1, nh = warp & 1;
+    float aq[4][4], ak[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) aq[x][e] = ak[x][e] = 0.f;
+    if (32 * nh <= 16 * mb + 15) {
+#pragma unroll 2
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            uint32_t a_q[4], a_k[4];
+            ldsm_x4(a_q, a_addr(sb + OFF_R1, LD, 16 * mb, 16 * kk, lane));
+            ldsm_x4(a_k, a_addr(sb + OFF_K, LD, 16 * mb, 16 * kk, lane));
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                uint32_t b[4];
+                ldsm_x4(b, b_addr(sb + OFF_K, LD, 32 * nh + 16 * np, 16 * kk, lane));
+                mma16816(aq[2 * np], a_q, b[0], b[1]);
+                mma16816(aq[2 * np + 1], a_q, b[2], b[3]);
+                mma16816(ak[2 * np], a_k, b[0], b[1]);
+                mma16816(ak[2 * np + 1], a_k, b[2], b[3]);
+            }
+        }
+    }
+    __syncthreads();   // q is read: region 1 takes A
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = 16 * mb + gq + 8 * h, s0 = 32 * nh + 8 * nt + 2 * t4;
+            float p[2], dd[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int s = s0 + e;
+                const float D = gs[r] / gs[s];
+                p[e] = (r < c && s <= r) ? D * aq[nt][2 * h + e] : 0.f;
+                dd[e] = (r < c && s < r) ? D * ak[nt][2 * h + e] : 0.f;
+            }
+            *reinterpret_cast<float2 *>(Pt + tb + r * C + s0) = make_float2(p[0], p[1]);
+            *reinterpret_cast<float2 *>(DKt + tb + r * C + s0) = make_float2(dd[0], dd[1]);
+            *reinterpret_cast<float2 *>(As + r * LA + s0) = make_float2(bs[r] * dd[0], bs[r] * dd[1]);
+        }
+    // the blocks of T above the diagonal are zero
+    for (int x = tid; x < 6 * 256; x += 256) {
+        const int b = x >> 8, e = x & 255;   // blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2), bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+        Ts[(16 * bi + (e >> 4)) * LA + 16 * bj + (e & 15)] = 0.f;
+    }
+    __syncthreads();
+    // diagonal blocks: warp 0 blocks 0, 1, warp 1 blocks 2, 3; lane % 16 = the column
+    if (warp < 2) {
+        const int b = 2 * warp + (lane >> 4), s = lane & 15;
+        const float *Ab = As + 16 * b * LA + 16 * b;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float a = 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) a = fmaf(Ab[r * LA + m], t[m], a);
+            t[r] = r == s ? 1.f : (r > s ? -a : 0.f);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * LA + 16 * b + s] = t[r];
+    }
+    __syncthreads();
+    float *Xs = reinterpret_cast<float *>(smb + OFF_X) + (warp < 3 ? warp : 0) * 16 * 20;
+    if (warp < 3) solve_offdiag(As, Ts, Xs, warp + 1, warp, lane);   // (1,0) (2,1) (3,2)
+    __syncthreads();
+    if (warp < 2) solve_offdiag(As, Ts, Xs, warp + 2, warp, lane);   // (2,0) (3,1)
+    __syncthreads();
+    if (warp == 0) solve_offdiag(As, Ts, Xs, 3, 0, lane);            // (3,0)
+    __syncthreads();
+
+    // T out (fp32); T diag(beta) and T diag(beta gamma) as hi + lo pairs into regions 1, 2
+    {
+        float4 tv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, s = (idx & 15) * 4;
+            tv[u] = *reinterpret_cast<const float4 *>(Ts + r * LA + s);
+            *reinterpret_cast<float4 *>(Tt + tb + r * C + s) = tv[u];
+        }
+        __syncthreads();   // T is read: region 2 takes T diag(beta gamma)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, s = (idx & 15) * 4;
+            const float tt[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
+            float xb[4], xg[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                xb[e] = tt[e] * bs[s + e];
+                xg[e] = xb[e] * gs[s + e];
+            }
+            uint32_t h0, l0, h1, l1;
+            const uint32_t o = 2 * (r * LC + s);
+            split_bf2(xb[0], xb[1], h0, l0);
+            split_bf2(xb[2], xb[3], h1, l1);
+            *reinterpret_cast<uint2 *>(smb + OFF_R1 + o) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(smb + OFF_R1 + C * LC * 2 + o) = make_uint2(l0, l1);
+            split_bf2(xg[0], xg[1], h0, l0);
+            split_bf2(xg[2], xg[3], h1, l1);
+            *reinterpret_cast<uint2 *>(smb + OFF_R2 + o) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(smb + OFF_R2 + C * LC * 2 + o) = make_uint2(l0, l1);
+        }
+    }
+    __syncthreads();
+
+    // U = (T diag(beta)) V, Wk = (T diag(beta gamma)) K: warp tile rows 16 (w >> 1),
+    // columns 64 (w & 1); T is lower triangular, so row block mb meets k blocks <= mb
+#pragma unroll 1
+    for (int pr = 0; pr < 2; ++pr) {
+        const uint32_t ah_base = sb + (pr == 0 ? OFF_R1 : OFF_R2), al_base = ah_base + C * LC * 2;
+        const uint32_t b_base = sb + (pr == 0 ? OFF_V : OFF_K);
+        float acc[8][4];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[x][e] = 0.f;
+        for (int ks = 0; ks <= mb; ++ks) {
+            uint32_t ah[4], al[4];
+            ldsm_x4(ah, a_addr(ah_base, LC, 16 * mb, 16 * ks, lane));
+            ldsm_x4(al, a_addr(al_base, LC, 16 * mb, 16 * ks, lane));
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t b[4];
+                ldsm_x4_t(b, bt_addr(b_base, LD, 64 * nh + 16 * np, 16 * ks, lane));
+                mma16816(acc[2 * np], ah, b[0], b[1]);
+                mma16816(acc[2 * np + 1], ah, b[2], b[3]);
+                mma16816(acc[2 * np], al, b[0], b[1]);
+                mma16816(acc[2 * np + 1], al, b[2], b[3]);
+            }
+        }
+        float *out = pr == 0 ? U : Wk;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = 16 * mb + gq + 8 * h, j = 64 * nh + 8 * nt + 2 * t4;
+                if (r < c)
+                    *reinterpret_cast<float2 *>(out + (row0 + r) * DK + j) =
+                        make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+            }
+    }
+}
+
 template <typename K>
 cudaError_t bwd_set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -1719,12 +2181,29 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     float *DKt = Tt + round4((size_t)BH * NC * C * C);
     cudaError_t err = launch_decay(g, d, gamma, BH, T, C, s);
     if (err != cudaSuccess) return err;
-    const size_t s0 = tiles_smem(dk, dv, C);
-    if ((err = bwd_set_smem(bwd_tiles_kernel<TE>, s0)) != cudaSuccess) return err;
-    bwd_tiles_kernel<TE><<<dim3(NC, BH), 256, s0, s>>>(q, k, v, gamma, beta, Pt, Tt, DKt, U, Wk, T, dk,
-                                                      dv, C);
+    constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
+    const bool mma_shape = kBf16 && dk == 128 && dv == 128 && C == 64;
+    if (mma_shape) {
+        if constexpr (kBf16) {
+            if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
+            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, Pt, Tt, DKt,
+                                                                    U, Wk, T);
+        }
+    } else {
+        const size_t s0 = tiles_smem(dk, dv, C);
+        if ((err = bwd_set_smem(bwd_tiles_kernel<TE>, s0)) != cudaSuccess) return err;
+        bwd_tiles_kernel<TE><<<dim3(NC, BH), 256, s0, s>>>(q, k, v, gamma, beta, Pt, Tt, DKt, U, Wk, T,
+                                                          dk, dv, C);
+    }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    {
+    if (mma_shape) {
+        if constexpr (kBf16) {
+            if ((err = bwd_set_smem(bwd_fwd_state_mma_kernel, mf::SMEM)) != cudaSuccess) return err;
+            bwd_fwd_state_mma_kernel<<<dim3(dv / mf::DS, BH), 256, mf::SMEM, s>>>(k, gamma, U, Wk, init,
+                                                                                 W, Mn, T, dv);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
+    } else {
         const int DSf = dv >= 32 ? 32 : 16;
         const size_t sf = sizeof(float) * ((size_t)dk * DSf + 2 * (size_t)C * (dk + 4) +
                                            2 * (size_t)C * DSf + (size_t)C);
@@ -1739,8 +2218,6 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
         }
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
-    const bool mma_shape = kBf16 && dk == 128 && dv == 128 && C == 64;
     if (mma_shape) {
         if constexpr (kBf16) {
             if ((err = bwd_set_smem(bwd_chain_mma_kernel, mc::SMEM)) != cudaSuccess) return err;
