@@ -1291,9 +1291,9 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         }
 #pragma unroll
         for (int np = 0; np < 2; ++np) {
-            uint32_t bm[4], bd[4];
-            ldsm_x4(bm, b_addr(sb + OFF_M, LD, nc + 16 * np, 16 * kk, lane));
-            ldsm_x4(bd, b_addr(sb + OFF_DM, LD, nc + 16 * np, 16 * kk, lane));
+            uint32_t bm[4], bd[4];   // the states are value-major: S[j][i] = M[i][j]
+            ldsm_x4_t(bm, bt_addr(sb + OFF_M, LD, nc + 16 * np, 16 * kk, lane));
+            ldsm_x4_t(bd, bt_addr(sb + OFF_DM, LD, nc + 16 * np, 16 * kk, lane));
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 mma16816(x1[mt][2 * np], ao[mt], bm[0], bm[1]);
@@ -1438,264 +1438,6 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     }
 }
 
-// ---------------------------------------------------------------- reverse chain, warp MMA
-// The reverse chain of the bf16 d = 128, chunk-64 shape on warp MMAs (m16n8k16, bf16
-// operands, fp32 accumulation).  One CTA per (32 value columns, bh), 8 warps.  The
-// running dM[:, slice] (128 x 32) stays in fp32 accumulator fragments for the whole
-// pass, warp w owning key rows 16w .. 16w + 15; its bf16 copy in shared memory is
-// the operand of the next chunk's K dM'.  Per chunk:
-//   1. dW = P^T dO + diag(gamma_C / gamma) K dM'  (warp: rows 16 (w >> 1), columns 16 (w & 1))
-//   2. dR = T^T dW (stored fp32); -gamma beta dR to shared memory as bf16
-//   3. dM = gamma_C dM' + Q^T (gamma dO) + K^T (-gamma beta dR)
-// P and T are unit-/lower-triangular, so their transposes' row block b only meets
-// column blocks >= b.  The next chunk's inputs wait in registers while this one
-// computes, as in bwd_chain_kernel.
-namespace mc {
-constexpr int C = 64, DK = 128, DS = 32, LD = DK + 8, LC = C + 8, LS = DS + 8;
-constexpr uint32_t OFF_K = 0, OFF_Q = OFF_K + C * LD * 2, OFF_P = OFF_Q + C * LD * 2,
-                   OFF_T = OFF_P + C * LC * 2, OFF_DO = OFF_T + C * LC * 2,
-                   OFF_GDO = OFF_DO + C * LS * 2, OFF_DW = OFF_GDO + C * LS * 2,
-                   OFF_RG = OFF_DW + C * LS * 2, OFF_DM = OFF_RG + C * LS * 2,
-                   OFF_G = OFF_DM + DK * LS * 2;
-constexpr uint32_t SMEM = OFF_G + 2 * C * 4;
-}  // namespace mc
-
-struct ChainStageMma {
-    uint4 kq[2][4];    // 1024 16-byte pieces of k and of q (64 x 128 bf16)
-    float4 pt[2][4];   // 1024 float4 of P and of T
-    uint4 o;           // dO row tid / 4, columns 8 (tid % 4) .. + 7 of the slice
-    float go;          // gamma of that row
-    float gb[2];       // gamma, beta of row tid (tid < 64)
-    __device__ __forceinline__ void load(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                                         const __nv_bfloat16 *dout, const float *gamma,
-                                         const float *beta, const float *Pp, const float *Tp,
-                                         int64_t row0, int c, int dv, int j0s, int tid) {
-        using namespace mc;
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
-            kq[0][u] = r < c ? ld16(k + (row0 + r) * DK + col) : z;
-            kq[1][u] = r < c ? ld16(q + (row0 + r) * DK + col) : z;
-            pt[0][u] = __ldg(reinterpret_cast<const float4 *>(Pp) + idx);
-            pt[1][u] = __ldg(reinterpret_cast<const float4 *>(Tp) + idx);
-        }
-        const int r = tid >> 2, col = (tid & 3) * 8;
-        o = r < c ? ld16(dout + (row0 + r) * dv + j0s + col) : z;
-        go = r < c ? gamma[row0 + r] : 0.f;
-        if (tid < C) {
-            gb[0] = tid < c ? gamma[row0 + tid] : 1.f;
-            gb[1] = tid < c ? beta[row0 + tid] : 0.f;
-        }
-    }
-    __device__ __forceinline__ void store(uint8_t *smb, int tid) const {
-        using namespace mc;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
-            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = kq[0][u];
-            *reinterpret_cast<uint4 *>(smb + OFF_Q + 2 * (r * LD + col)) = kq[1][u];
-            const int rp = idx >> 4, cp = (idx & 15) * 4;
-            *reinterpret_cast<uint2 *>(smb + OFF_P + 2 * (rp * LC + cp)) =
-                make_uint2(pack_bf2(pt[0][u].x, pt[0][u].y), pack_bf2(pt[0][u].z, pt[0][u].w));
-            *reinterpret_cast<uint2 *>(smb + OFF_T + 2 * (rp * LC + cp)) =
-                make_uint2(pack_bf2(pt[1][u].x, pt[1][u].y), pack_bf2(pt[1][u].z, pt[1][u].w));
-        }
-        const int r = tid >> 2, col = (tid & 3) * 8;
-        *reinterpret_cast<uint4 *>(smb + OFF_DO + 2 * (r * LS + col)) = o;
-        float f[8];
-        widen16(o, f, (const __nv_bfloat16 *)nullptr);
-        *reinterpret_cast<uint4 *>(smb + OFF_GDO + 2 * (r * LS + col)) =
-            make_uint4(pack_bf2(go * f[0], go * f[1]), pack_bf2(go * f[2], go * f[3]),
-                       pack_bf2(go * f[4], go * f[5]), pack_bf2(go * f[6], go * f[7]));
-        if (tid < C) {
-            float *gs = reinterpret_cast<float *>(smb + OFF_G);
-            gs[tid] = gb[0];
-            gs[C + tid] = gb[1];
-        }
-    }
-};
-
-__global__ void __launch_bounds__(256, 2)
-bwd_chain_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                     const float *__restrict__ gamma, const float *__restrict__ beta,
-                     const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
-                     const float *__restrict__ Pt, const float *__restrict__ Tt,
-                     float *__restrict__ dR, float *__restrict__ dMn1, float *dinit, int T, int dv) {
-    using namespace mc;
-    using sm100::ldsm_x4;
-    using sm100::ldsm_x4_t;
-    using sm100::mma16816;
-    extern __shared__ __align__(16) uint8_t smb[];
-    const int j0s = blockIdx.x * DS, bh = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
-    const uint32_t sb = sm100::smem_u32(smb);
-    const float *gs = reinterpret_cast<const float *>(smb + OFF_G), *bs = gs + C;
-    const int NC = (T + C - 1) / C;
-    const int m1 = warp >> 1, n1 = 16 * (warp & 1);   // steps 1 and 2: row block, first column
-    auto tile_p = [&](int n) { return Pt + ((int64_t)bh * NC + n) * C * C; };
-    auto tile_t = [&](int n) { return Tt + ((int64_t)bh * NC + n) * C * C; };
-    // dM fragments: rows 16 warp + gq (+ 8 for elements 2, 3), columns 8 nt + 2 t4 (+ 1),
-    // as offsets into one head's dk x dv state
-    auto dm_off = [&](int nt, int h) {
-        return (int64_t)(16 * warp + gq + 8 * h) * dv + j0s + 8 * nt + 2 * t4;
-    };
-    const int64_t head = (int64_t)DK * dv;
-    float acc[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float *src = dfinal + bh * head + dm_off(nt, h);   // 4-byte aligned only
-            acc[nt][2 * h] = dfinal ? src[0] : 0.f;
-            acc[nt][2 * h + 1] = dfinal ? src[1] : 0.f;
-        }
-    auto publish_dm = [&]() {   // bf16 copy of dM for the next chunk's K dM'
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                *reinterpret_cast<uint32_t *>(smb + OFF_DM + 2 * ((16 * warp + gq + 8 * h) * LS + 8 * nt + 2 * t4)) =
-                    pack_bf2(acc[nt][2 * h], acc[nt][2 * h + 1]);
-    };
-    publish_dm();
-    ChainStageMma stage;
-    {
-        const int n = NC - 1;
-        stage.load(q, k, dout, gamma, beta, tile_p(n), tile_t(n), (int64_t)bh * T + n * C, T - n * C,
-                   dv, j0s, tid);
-        stage.store(smb, tid);
-    }
-    for (int n = NC - 1; n >= 0; --n) {
-        const int t0 = n * C, c = min(C, T - t0);
-        const int64_t row0 = (int64_t)bh * T + t0;
-        __syncthreads();   // chunk n's inputs and dM' (bf16) are in shared memory
-        if (n > 0)
-            stage.load(q, k, dout, gamma, beta, tile_p(n - 1), tile_t(n - 1), row0 - C, C, dv, j0s, tid);
-        {   // dM' of chunk n, fp32
-            float *dst = dMn1 + ((int64_t)bh * NC + n) * head;
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    *reinterpret_cast<float2 *>(dst + dm_off(nt, h)) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
-        }
-        const float gC = gs[c - 1];
-        // 1. dW
-        {
-            float a1[2][4], a2[2][4];
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) a1[x][e] = a2[x][e] = 0.f;
-            for (int ks = m1; ks < C / 16; ++ks) {
-                uint32_t a[4], b[4];
-                ldsm_x4_t(a, at_addr(sb + OFF_P, LC, 16 * m1, 16 * ks, lane));
-                ldsm_x4_t(b, bt_addr(sb + OFF_DO, LS, n1, 16 * ks, lane));
-                mma16816(a1[0], a, b[0], b[1]);
-                mma16816(a1[1], a, b[2], b[3]);
-            }
-#pragma unroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                uint32_t a[4], b[4];
-                ldsm_x4(a, a_addr(sb + OFF_K, LD, 16 * m1, 16 * kk, lane));
-                ldsm_x4_t(b, bt_addr(sb + OFF_DM, LS, n1, 16 * kk, lane));
-                mma16816(a2[0], a, b[0], b[1]);
-                mma16816(a2[1], a, b[2], b[3]);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = 16 * m1 + gq + 8 * h;
-                const float sc = r < c ? gC / gs[r] : 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-                    *reinterpret_cast<uint32_t *>(smb + OFF_DW + 2 * (r * LS + n1 + 8 * nt + 2 * t4)) =
-                        pack_bf2(fmaf(sc, a2[nt][2 * h], a1[nt][2 * h]), fmaf(sc, a2[nt][2 * h + 1], a1[nt][2 * h + 1]));
-            }
-        }
-        __syncthreads();
-        // 2. dR = T^T dW
-        {
-            float a1[2][4];
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) a1[x][e] = 0.f;
-            for (int ks = m1; ks < C / 16; ++ks) {
-                uint32_t a[4], b[4];
-                ldsm_x4_t(a, at_addr(sb + OFF_T, LC, 16 * m1, 16 * ks, lane));
-                ldsm_x4_t(b, bt_addr(sb + OFF_DW, LS, n1, 16 * ks, lane));
-                mma16816(a1[0], a, b[0], b[1]);
-                mma16816(a1[1], a, b[2], b[3]);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = 16 * m1 + gq + 8 * h;
-                const float ngb = -gs[r] * bs[r];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int j = n1 + 8 * nt + 2 * t4;
-                    const float x0 = a1[nt][2 * h], x1 = a1[nt][2 * h + 1];
-                    *reinterpret_cast<uint32_t *>(smb + OFF_RG + 2 * (r * LS + j)) = pack_bf2(ngb * x0, ngb * x1);
-                    if (r < c) *reinterpret_cast<float2 *>(dR + (row0 + r) * dv + j0s + j) = make_float2(x0, x1);
-                }
-            }
-        }
-        __syncthreads();
-        // 3. dM = gamma_C dM' + Q^T (gamma dO) + K^T (-gamma beta dR)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] *= gC;
-#pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {
-            uint32_t aq[4], ak[4];
-            ldsm_x4_t(aq, at_addr(sb + OFF_Q, LD, 16 * warp, 16 * ks, lane));
-            ldsm_x4_t(ak, at_addr(sb + OFF_K, LD, 16 * warp, 16 * ks, lane));
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t bo[4], br[4];
-                ldsm_x4_t(bo, bt_addr(sb + OFF_GDO, LS, 16 * np, 16 * ks, lane));
-                ldsm_x4_t(br, bt_addr(sb + OFF_RG, LS, 16 * np, 16 * ks, lane));
-                mma16816(acc[2 * np], aq, bo[0], bo[1]);
-                mma16816(acc[2 * np + 1], aq, bo[2], bo[3]);
-                mma16816(acc[2 * np], ak, br[0], br[1]);
-                mma16816(acc[2 * np + 1], ak, br[2], br[3]);
-            }
-        }
-        publish_dm();   // step 1 of this chunk read the old copy before the second barrier
-        __syncthreads();   // every read of chunk n's inputs is done
-        if (n > 0) stage.store(smb, tid);
-    }
-    if (dinit) {
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float *dst = dinit + bh * head + dm_off(nt, h);
-                dst[0] = acc[nt][2 * h];
-                dst[1] = acc[nt][2 * h + 1];
-            }
-    }
-}
-
-// ---------------------------------------------------------------- forward state, warp MMA
-// The forward's state pass of the bf16 d = 128, chunk-64 shape on warp MMAs.  Its
-// fp32 operands go in as two bf16 terms x = hi + lo (hi = bf16(x), lo = bf16(x - hi),
-// relative error ~2^-17): W = U - (Wk_hi + Wk_lo)(M_hi + M_lo) drops only the lo x lo
-// product, and M' = gamma_C M + K^T diag(gamma_C / gamma) W takes k exactly, so W and
-// the chunk states keep near-fp32 accuracy.  M[:, slice] (128 x 32) stays in fp32
-// accumulator fragments, warp w owning key rows 16w .. 16w + 15; W in 16 x 16 warp
-// tiles (rows 16 (w >> 1), columns 16 (w & 1)).  One CTA per (32 value columns, bh).
-namespace mf {
-constexpr int C = 64, DK = 128, DS = 32, LD = DK + 8, LS = DS + 8;
-constexpr uint32_t OFF_K = 0, OFF_WKH = OFF_K + C * LD * 2, OFF_WKL = OFF_WKH + C * LD * 2,
-                   OFF_MH = OFF_WKL + C * LD * 2, OFF_ML = OFF_MH + DK * LS * 2,
-                   OFF_WSH = OFF_ML + DK * LS * 2, OFF_WSL = OFF_WSH + C * LS * 2,
-                   OFF_G = OFF_WSL + C * LS * 2;
-constexpr uint32_t SMEM = OFF_G + C * 4;
-}  // namespace mf
-
 // x = hi + lo in bf16 pairs
 __device__ __forceinline__ void split_bf2(float a, float b, uint32_t &hi, uint32_t &lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -1704,193 +1446,6 @@ __device__ __forceinline__ void split_bf2(float a, float b, uint32_t &hi, uint32
     lo = pack_bf2(a - hf.x, b - hf.y);
 }
 
-struct FwdStageMma {
-    uint4 kk[4];     // 1024 16-byte pieces of k (64 x 128 bf16)
-    float4 wk[8];    // 2048 float4 of Wk
-    float u[2][2][2];   // U at this lane's W fragment: [h][nt] pairs
-    float gm;
-    __device__ __forceinline__ void load(const __nv_bfloat16 *k, const float *Wk, const float *U,
-                                         const float *gamma, int64_t row0, int c, int dv, int j0s,
-                                         int tid, int ur0, int uc0) {
-        using namespace mf;
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int idx = tid + 256 * x, r = idx >> 4, col = (idx & 15) * 8;
-            kk[x] = r < c ? ld16(k + (row0 + r) * DK + col) : z;
-        }
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int idx = tid + 256 * x, r = idx >> 5, col = (idx & 31) * 4;
-            wk[x] = r < c ? __ldg(reinterpret_cast<const float4 *>(Wk + (row0 + r) * DK + col))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int r = ur0 + 8 * h;
-                float2 x = make_float2(0.f, 0.f);
-                if (r < c) x = __ldg(reinterpret_cast<const float2 *>(U + (row0 + r) * dv + j0s + uc0 + 8 * nt));
-                u[h][nt][0] = x.x;
-                u[h][nt][1] = x.y;
-            }
-        if (tid < C) gm = tid < c ? gamma[row0 + tid] : 1.f;
-    }
-    __device__ __forceinline__ void store(uint8_t *smb, int tid) const {
-        using namespace mf;
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int idx = tid + 256 * x, r = idx >> 4, col = (idx & 15) * 8;
-            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = kk[x];
-        }
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int idx = tid + 256 * x, r = idx >> 5, col = (idx & 31) * 4;
-            uint32_t h0, l0, h1, l1;
-            split_bf2(wk[x].x, wk[x].y, h0, l0);
-            split_bf2(wk[x].z, wk[x].w, h1, l1);
-            *reinterpret_cast<uint2 *>(smb + OFF_WKH + 2 * (r * LD + col)) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(smb + OFF_WKL + 2 * (r * LD + col)) = make_uint2(l0, l1);
-        }
-        if (tid < C) reinterpret_cast<float *>(smb + OFF_G)[tid] = gm;
-    }
-};
-
-__global__ void __launch_bounds__(256, 2)
-bwd_fwd_state_mma_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ gamma,
-                         const float *__restrict__ U, const float *__restrict__ Wk, const float *init,
-                         float *__restrict__ W, float *__restrict__ Mn, int T, int dv) {
-    using namespace mf;
-    using sm100::ldsm_x4;
-    using sm100::ldsm_x4_t;
-    using sm100::mma16816;
-    extern __shared__ __align__(16) uint8_t smb[];
-    const int j0s = blockIdx.x * DS, bh = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
-    const uint32_t sb = sm100::smem_u32(smb);
-    const float *gs = reinterpret_cast<const float *>(smb + OFF_G);
-    const int NC = (T + C - 1) / C;
-    const int m1 = warp >> 1, n1 = 16 * (warp & 1);
-    const int ur0 = 16 * m1 + gq, uc0 = n1 + 2 * t4;   // this lane's W fragment origin
-    const int64_t head = (int64_t)DK * dv;
-    auto m_off = [&](int nt, int h) {
-        return (int64_t)(16 * warp + gq + 8 * h) * dv + j0s + 8 * nt + 2 * t4;
-    };
-    float acc[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float *src = init + bh * head + m_off(nt, h);   // 4-byte aligned only
-            acc[nt][2 * h] = init ? src[0] : 0.f;
-            acc[nt][2 * h + 1] = init ? src[1] : 0.f;
-        }
-    auto publish_m = [&]() {
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t hi, lo;
-                split_bf2(acc[nt][2 * h], acc[nt][2 * h + 1], hi, lo);
-                const uint32_t o = 2 * ((16 * warp + gq + 8 * h) * LS + 8 * nt + 2 * t4);
-                *reinterpret_cast<uint32_t *>(smb + OFF_MH + o) = hi;
-                *reinterpret_cast<uint32_t *>(smb + OFF_ML + o) = lo;
-            }
-    };
-    publish_m();
-    FwdStageMma stage;
-    stage.load(k, Wk, U, gamma, (int64_t)bh * T, min(C, T), dv, j0s, tid, ur0, uc0);
-    stage.store(smb, tid);
-    float uc[2][2][2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) uc[h][nt][0] = stage.u[h][nt][0], uc[h][nt][1] = stage.u[h][nt][1];
-    for (int n = 0; n < NC; ++n) {
-        const int t0 = n * C, c = min(C, T - t0);
-        const int64_t row0 = (int64_t)bh * T + t0;
-        __syncthreads();   // chunk n's inputs and M (hi, lo) are in shared memory
-        if (n + 1 < NC)
-            stage.load(k, Wk, U, gamma, row0 + C, min(C, T - t0 - C), dv, j0s, tid, ur0, uc0);
-        {
-            float *dst = Mn + ((int64_t)bh * NC + n) * head;
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    *reinterpret_cast<float2 *>(dst + m_off(nt, h)) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
-        }
-        const float gC = gs[c - 1];
-        // W = U - Wk M
-        {
-            float w[2][4];
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) w[x][e] = 0.f;
-#pragma unroll 4
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                uint32_t ah[4], al[4], bh4[4], bl4[4];
-                ldsm_x4(ah, a_addr(sb + OFF_WKH, LD, 16 * m1, 16 * kk, lane));
-                ldsm_x4(al, a_addr(sb + OFF_WKL, LD, 16 * m1, 16 * kk, lane));
-                ldsm_x4_t(bh4, bt_addr(sb + OFF_MH, LS, n1, 16 * kk, lane));
-                ldsm_x4_t(bl4, bt_addr(sb + OFF_ML, LS, n1, 16 * kk, lane));
-                mma16816(w[0], ah, bh4[0], bh4[1]);
-                mma16816(w[1], ah, bh4[2], bh4[3]);
-                mma16816(w[0], al, bh4[0], bh4[1]);
-                mma16816(w[1], al, bh4[2], bh4[3]);
-                mma16816(w[0], ah, bl4[0], bl4[1]);
-                mma16816(w[1], ah, bl4[2], bl4[3]);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = ur0 + 8 * h;
-                const float sc = r < c ? gC / gs[r] : 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int j = uc0 + 8 * nt;
-                    const float w0 = uc[h][nt][0] - w[nt][2 * h], w1 = uc[h][nt][1] - w[nt][2 * h + 1];
-                    if (r < c) *reinterpret_cast<float2 *>(W + (row0 + r) * dv + j0s + j) = make_float2(w0, w1);
-                    uint32_t hi, lo;
-                    split_bf2(sc * w0, sc * w1, hi, lo);
-                    *reinterpret_cast<uint32_t *>(smb + OFF_WSH + 2 * (r * LS + j)) = hi;
-                    *reinterpret_cast<uint32_t *>(smb + OFF_WSL + 2 * (r * LS + j)) = lo;
-                }
-            }
-        }
-        __syncthreads();
-        // M <- gamma_C M + K^T diag(gamma_C / gamma) W
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] *= gC;
-#pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {
-            uint32_t ak[4];
-            ldsm_x4_t(ak, at_addr(sb + OFF_K, LD, 16 * warp, 16 * ks, lane));
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t bh4[4], bl4[4];
-                ldsm_x4_t(bh4, bt_addr(sb + OFF_WSH, LS, 16 * np, 16 * ks, lane));
-                ldsm_x4_t(bl4, bt_addr(sb + OFF_WSL, LS, 16 * np, 16 * ks, lane));
-                mma16816(acc[2 * np], ak, bh4[0], bh4[1]);
-                mma16816(acc[2 * np + 1], ak, bh4[2], bh4[3]);
-                mma16816(acc[2 * np], ak, bl4[0], bl4[1]);
-                mma16816(acc[2 * np + 1], ak, bl4[2], bl4[3]);
-            }
-        }
-        publish_m();   // step W of this chunk read the old copy before the second barrier
-        __syncthreads();   // every read of chunk n's inputs is done
-        if (n + 1 < NC) {
-            stage.store(smb, tid);
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) uc[h][nt][0] = stage.u[h][nt][0], uc[h][nt][1] = stage.u[h][nt][1];
-        }
-    }
-}
 
 // ---------------------------------------------------------------- chunk tiles, warp MMA
 // The chunk tiles of the bf16 d = 128, chunk-64 shape: Q K^T and K K^T on warp MMAs
@@ -1898,7 +1453,10 @@ bwd_fwd_state_mma_kernel(const __nv_bfloat16 *__restrict__ k, const float *__res
 // (the four 16 x 16 diagonal blocks a column per lane, then the off-diagonal blocks
 // by distance from the diagonal: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj), and
 // U = (T diag(beta)) V, Wk = (T diag(beta gamma)) K on warp MMAs with the fp32 left
-// factors as bf16 hi + lo pairs (v and k exact).  Outputs as bwd_tiles_kernel.
+// factors as bf16 hi + lo pairs (v and k exact).  Outputs as bwd_tiles_kernel, except
+// that T and P also go out as bf16 tiles for the reverse chain (TPb: per chunk T then P,
+// C x C each) and T not as fp32, and Wk goes out as bf16 hi + lo rows (Wk2: per token
+// dk hi values, then dk lo values) for the forward state pass.
 namespace mt {
 constexpr int C = 64, DK = 128, LD = DK + 8, LA = C + 4, LC = C + 8;
 constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + C * LD * 2, OFF_R1 = OFF_V + C * LD * 2,
@@ -1952,8 +1510,9 @@ __device__ __forceinline__ void solve_offdiag(const float *As, float *Ts, float 
 __global__ void __launch_bounds__(256, 2)
 bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
-                     const float *__restrict__ beta, float *__restrict__ Pt, float *__restrict__ Tt,
-                     float *__restrict__ DKt, float *__restrict__ U, float *__restrict__ Wk, int T) {
+                     const float *__restrict__ beta, float *__restrict__ Pt,
+                     __nv_bfloat16 *__restrict__ TPb, float *__restrict__ DKt, float *__restrict__ U,
+                     __nv_bfloat16 *__restrict__ Wk2, int T) {
     using namespace mt;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1969,6 +1528,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     float *Ts = reinterpret_cast<float *>(smb + OFF_R2);
     float *gs = reinterpret_cast<float *>(smb + OFF_G), *bs = gs + C;
     const int64_t tb = ((int64_t)bh * NC + n) * C * C;
+    __nv_bfloat16 *Tb = TPb + 2 * tb, *Pb = Tb + C * C;
 
     {   // q (into region 1), k, v as given; rows past the chunk's end zero
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -2035,6 +1595,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                 dd[e] = (r < c && s < r) ? D * ak[nt][2 * h + e] : 0.f;
             }
             *reinterpret_cast<float2 *>(Pt + tb + r * C + s0) = make_float2(p[0], p[1]);
+            *reinterpret_cast<uint32_t *>(Pb + r * C + s0) = pack_bf2(p[0], p[1]);
             *reinterpret_cast<float2 *>(DKt + tb + r * C + s0) = make_float2(dd[0], dd[1]);
             *reinterpret_cast<float2 *>(As + r * LA + s0) = make_float2(bs[r] * dd[0], bs[r] * dd[1]);
         }
@@ -2076,7 +1637,8 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         for (int u = 0; u < 4; ++u) {
             const int idx = tid + 256 * u, r = idx >> 4, s = (idx & 15) * 4;
             tv[u] = *reinterpret_cast<const float4 *>(Ts + r * LA + s);
-            *reinterpret_cast<float4 *>(Tt + tb + r * C + s) = tv[u];
+            *reinterpret_cast<uint2 *>(Tb + r * C + s) =
+                make_uint2(pack_bf2(tv[u].x, tv[u].y), pack_bf2(tv[u].z, tv[u].w));
         }
         __syncthreads();   // T is read: region 2 takes T diag(beta gamma)
 #pragma unroll
@@ -2128,15 +1690,374 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                 mma16816(acc[2 * np + 1], al, b[2], b[3]);
             }
         }
-        float *out = pr == 0 ? U : Wk;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int r = 16 * mb + gq + 8 * h, j = 64 * nh + 8 * nt + 2 * t4;
-                if (r < c)
-                    *reinterpret_cast<float2 *>(out + (row0 + r) * DK + j) =
+                if (r >= c) continue;
+                if (pr == 0) {
+                    *reinterpret_cast<float2 *>(U + (row0 + r) * DK + j) =
                         make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+                } else {
+                    uint32_t hi, lo;
+                    split_bf2(acc[nt][2 * h], acc[nt][2 * h + 1], hi, lo);
+                    __nv_bfloat16 *row = Wk2 + (row0 + r) * 2 * DK;
+                    *reinterpret_cast<uint32_t *>(row + j) = hi;
+                    *reinterpret_cast<uint32_t *>(row + DK + j) = lo;
+                }
+            }
+    }
+}
+
+// ---------------------------------------------------------------- value-column chains
+// The two sequential passes of the bf16 d = 128, chunk-64 shape, value-column parallel:
+// the state's value columns never mix, so warp w of a CTA owns 16 of them (the CTA 64,
+// grid (dv / 64, BH), one CTA per SM) and keeps its 16 x 128 slice of the state
+// TRANSPOSED in fp32 MMA accumulator fragments.  The accumulator fragment of a 16-row
+// tile is the A fragment of the next product over its columns (rows g, g + 8; columns
+// 2t, 2t + 1 and 2t + 8, 2t + 9 of two adjacent 8-column tiles), so a chunk's products
+// chain inside the warp without shared memory or barriers.  The chunk's shared inputs
+// arrive by cp.async into padded, double-buffered shared memory (the next chunk's copy
+// runs under this chunk's products): two barriers per chunk.  The chunk states are
+// stored value-major, S[j][i] = M[i][j], for the per-chunk gradients.
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// rows 0 .. 63 of a row-major matrix (bytes_per_row a multiple of 16) into shared rows of
+// pitch sp bytes; rows >= c are zero-filled (their source clamped to row 0)
+__device__ __forceinline__ void stage_rows(uint32_t dst, const void *src, int64_t src_pitch, int row_bytes,
+                                           int sp, int c, int tid, int nthreads) {
+    const int per_row = row_bytes / 16;
+    for (int x = tid; x < 64 * per_row; x += nthreads) {
+        const int r = x / per_row, p = x % per_row;
+        const bool in = r < c;
+        const char *s = static_cast<const char *>(src) + (in ? r * src_pitch : 0) + 16 * p;
+        cp_async16(dst + r * sp + 16 * p, s, in ? 16u : 0u);
+    }
+}
+
+namespace vc {
+constexpr int C = 64, DK = 128, NW = 4, NT = 32 * NW, DSC = 16 * NW, LD = DK + 8, LC = C + 8;
+// forward state stage: k, Wk hi, Wk lo (bf16 [C][LD]); U[:, slice] (fp32 [C][DSC + 4]); gamma
+constexpr int LU = DSC + 4;
+constexpr uint32_t F_K = 0, F_WH = F_K + C * LD * 2, F_WL = F_WH + C * LD * 2, F_U = F_WL + C * LD * 2,
+                   F_G = F_U + C * LU * 4, F_STAGE = F_G + C * 4;
+// reverse chain stage: k, q (bf16 [C][LD]); P, T (bf16 [C][LC]); dO[:, slice] (bf16 [C][LC]); gamma, beta
+constexpr uint32_t R_K = 0, R_Q = R_K + C * LD * 2, R_P = R_Q + C * LD * 2, R_T = R_P + C * LC * 2,
+                   R_O = R_T + C * LC * 2, R_G = R_O + C * LC * 2, R_B = R_G + C * 4, R_STAGE = R_B + C * 4;
+static_assert(F_STAGE % 16 == 0 && R_STAGE % 16 == 0, "16-byte stages");
+}  // namespace vc
+
+// A fragment (k block kk) from a 16-row accumulator tile acc[2 kk], acc[2 kk + 1]
+__device__ __forceinline__ void acc_to_a(const float (&x0)[4], const float (&x1)[4], uint32_t (&a)[4]) {
+    a[0] = pack_bf2(x0[0], x0[1]);
+    a[1] = pack_bf2(x0[2], x0[3]);
+    a[2] = pack_bf2(x1[0], x1[1]);
+    a[3] = pack_bf2(x1[2], x1[3]);
+}
+__device__ __forceinline__ void acc_to_a_split(const float (&x0)[4], const float (&x1)[4], uint32_t (&h)[4],
+                                               uint32_t (&l)[4]) {
+    split_bf2(x0[0], x0[1], h[0], l[0]);
+    split_bf2(x0[2], x0[3], h[1], l[1]);
+    split_bf2(x1[0], x1[1], h[2], l[2]);
+    split_bf2(x1[2], x1[3], h[3], l[3]);
+}
+
+// Forward state: per chunk W^T = U^T - M^T Wk^T (M^T and Wk as hi + lo, three products)
+// and M^T <- gamma_C M^T + (W diag(gamma_C / gamma))^T K (W as hi + lo); writes W
+// ([token][dv], fp32) and the state at every chunk start (value-major, fp32).
+__global__ void __launch_bounds__(vc::NT, 1)
+bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ gamma,
+                        const float *__restrict__ U, const __nv_bfloat16 *__restrict__ Wk2,
+                        const float *init, float *__restrict__ W, float *__restrict__ Sn, int T, int dv) {
+    using namespace vc;
+    using sm100::ldsm_x4;
+    using sm100::ldsm_x4_t;
+    using sm100::mma16816;
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const uint32_t sb = sm100::smem_u32(smb);
+    const int NC = (T + C - 1) / C;
+    const int jw = j0 + 16 * warp;   // this warp's first value column
+    auto issue = [&](int n) {
+        if (n < NC) {
+            const uint32_t st = sb + (uint32_t)(n & 1) * F_STAGE;
+            const int c = min(C, T - n * C);
+            const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
+            stage_rows(st + F_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, c, tid, NT);
+            stage_rows(st + F_WH, Wk2 + row0 * 2 * DK, 4 * DK, DK * 2, LD * 2, c, tid, NT);
+            stage_rows(st + F_WL, Wk2 + row0 * 2 * DK + DK, 4 * DK, DK * 2, LD * 2, c, tid, NT);
+            stage_rows(st + F_U, U + row0 * dv + j0, (int64_t)dv * 4, DSC * 4, LU * 4, c, tid, NT);
+            if (tid < C) cp_async4(st + F_G + 4 * tid, gamma + row0 + (tid < c ? tid : 0), tid < c ? 4u : 0u);
+        }
+        cp_async_commit();
+    };
+    // M^T: rows jw + gq (+ 8), key columns 8 nt + 2 t4 (+ 1)
+    float mt[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
+            mt[nt][e] = init ? init[((int64_t)bh * DK + i) * dv + j] : 0.f;
+        }
+    issue(0);
+    issue(1);
+    for (int n = 0; n < NC; ++n) {
+        const int c = min(C, T - n * C);
+        const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
+        const uint32_t st = sb + (uint32_t)(n & 1) * F_STAGE;
+        const float *gs = reinterpret_cast<const float *>(smb + (n & 1) * F_STAGE + F_G);
+        const float *us = reinterpret_cast<const float *>(smb + (n & 1) * F_STAGE + F_U);
+        {   // the state at this chunk's start, value-major
+            float *dst = Sn + ((int64_t)bh * NC + n) * DK * dv;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2 *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
+                        make_float2(mt[nt][2 * h], mt[nt][2 * h + 1]);
+        }
+        cp_async_wait1();
+        __syncthreads();   // chunk n's stage has landed
+        const float gC = gs[c - 1];
+        // W^T (16 x 64): w the hi x hi products, w2 the two correction terms
+        float w[8][4], w2[8][4];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[x][e] = w2[x][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            uint32_t ah[4], al[4];
+            acc_to_a_split(mt[2 * kk], mt[2 * kk + 1], ah, al);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bh4[4], bl4[4];
+                ldsm_x4(bh4, b_addr(st + F_WH, LD, 16 * np, 16 * kk, lane));
+                ldsm_x4(bl4, b_addr(st + F_WL, LD, 16 * np, 16 * kk, lane));
+                mma16816(w[2 * np], ah, bh4[0], bh4[1]);
+                mma16816(w[2 * np + 1], ah, bh4[2], bh4[3]);
+                mma16816(w2[2 * np], al, bh4[0], bh4[1]);
+                mma16816(w2[2 * np + 1], al, bh4[2], bh4[3]);
+                mma16816(w2[2 * np], ah, bl4[0], bl4[1]);
+                mma16816(w2[2 * np + 1], ah, bl4[2], bl4[3]);
+            }
+        }
+        // W = U - (w + w2), stored; then the columns scaled by gamma_C / gamma_r
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 8 * nt + 2 * t4 + (e & 1), jl = 16 * warp + gq + 8 * (e >> 1);
+                const float x = us[r * LU + jl] - (w[nt][e] + w2[nt][e]);
+                if (r < c) W[(row0 + r) * dv + j0 + jl] = x;
+                w[nt][e] = r < c ? x * (gC / gs[r]) : 0.f;
+            }
+        // M^T <- gamma_C M^T + (W diag(sc))^T K
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mt[nt][e] *= gC;
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+            uint32_t ah[4], al[4];
+            acc_to_a_split(w[2 * ks], w[2 * ks + 1], ah, al);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                uint32_t b[4];
+                ldsm_x4_t(b, bt_addr(st + F_K, LD, 16 * np, 16 * ks, lane));
+                mma16816(mt[2 * np], ah, b[0], b[1]);
+                mma16816(mt[2 * np + 1], ah, b[2], b[3]);
+                mma16816(mt[2 * np], al, b[0], b[1]);
+                mma16816(mt[2 * np + 1], al, b[2], b[3]);
+            }
+        }
+        __syncthreads();   // every warp is done with this stage
+        issue(n + 2);
+    }
+}
+
+// Reverse chain: per chunk dW^T = dO^T P + (dM'^T K^T) diag(gamma_C / gamma),
+// dR^T = dW^T T (stored as dR [token][dv], fp32), and
+// dM^T <- gamma_C dM'^T + (diag(gamma) dO)^T Q + (-diag(gamma beta) dR)^T K; writes dM'
+// of every chunk (value-major) and the initial state's gradient.
+__global__ void __launch_bounds__(vc::NT, 1)
+bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                    const float *__restrict__ gamma, const float *__restrict__ beta,
+                    const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
+                    const __nv_bfloat16 *__restrict__ TPb, float *__restrict__ dR,
+                    float *__restrict__ dSn1, float *dinit, int T, int dv) {
+    using namespace vc;
+    using sm100::ldsm_x4;
+    using sm100::ldsm_x4_t;
+    using sm100::mma16816;
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const uint32_t sb = sm100::smem_u32(smb);
+    const int NC = (T + C - 1) / C;
+    const int jw = j0 + 16 * warp;
+    auto issue = [&](int s, int n) {   // stage s takes chunk n (n < 0: nothing)
+        if (n >= 0) {
+            const uint32_t st = sb + (uint32_t)s * R_STAGE;
+            const int c = min(C, T - n * C);
+            const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
+            const __nv_bfloat16 *tp = TPb + ((int64_t)bh * NC + n) * 2 * C * C;
+            stage_rows(st + R_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, c, tid, NT);
+            stage_rows(st + R_Q, q + row0 * DK, DK * 2, DK * 2, LD * 2, c, tid, NT);
+            stage_rows(st + R_T, tp, C * 2, C * 2, LC * 2, C, tid, NT);
+            stage_rows(st + R_P, tp + C * C, C * 2, C * 2, LC * 2, C, tid, NT);
+            stage_rows(st + R_O, dout + row0 * dv + j0, (int64_t)dv * 2, DSC * 2, LC * 2, c, tid, NT);
+            if (tid < C) {
+                const int r = tid < c ? tid : 0;
+                cp_async4(st + R_G + 4 * tid, gamma + row0 + r, tid < c ? 4u : 0u);
+                cp_async4(st + R_B + 4 * tid, beta + row0 + r, tid < c ? 4u : 0u);
+            }
+        }
+        cp_async_commit();
+    };
+    float dm[16][4];   // dM'^T: rows jw + gq (+ 8), key columns 8 nt + 2 t4 (+ 1)
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
+            dm[nt][e] = dfinal ? dfinal[((int64_t)bh * DK + i) * dv + j] : 0.f;
+        }
+    issue(0, NC - 1);
+    issue(1, NC - 2);
+    for (int it = 0; it < NC; ++it) {
+        const int n = NC - 1 - it, s = it & 1;
+        const int c = min(C, T - n * C);
+        const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
+        const uint32_t st = sb + (uint32_t)s * R_STAGE;
+        const float *gs = reinterpret_cast<const float *>(smb + s * R_STAGE + R_G);
+        const float *bs = reinterpret_cast<const float *>(smb + s * R_STAGE + R_B);
+        {   // dM' of this chunk, value-major
+            float *dst = dSn1 + ((int64_t)bh * NC + n) * DK * dv;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2 *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
+                        make_float2(dm[nt][2 * h], dm[nt][2 * h + 1]);
+        }
+        cp_async_wait1();
+        __syncthreads();
+        const float gC = gs[c - 1];
+        // dO^T fragments (k = token) and their gamma-scaled copies
+        uint32_t ao[4][4], ag[4][4];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            ldsm_x4_t(ao[ks], at_addr(st + R_O, LC, 16 * warp, 16 * ks, lane));
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int r = 16 * ks + 2 * t4 + 8 * (x >> 1);
+                const float2 o = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ao[ks][x]));
+                ag[ks][x] = pack_bf2(gs[r] * o.x, gs[r + 1] * o.y);
+            }
+        }
+        // dW^T = dO^T P (+) dM'^T K^T, the second scaled by gamma_C / gamma_r per column r
+        float a1[8][4], a2[8][4];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a1[x][e] = a2[x][e] = 0.f;
+#pragma unroll
+        for (int np = 0; np < 4; ++np)
+#pragma unroll
+            for (int ks = np; ks < 4; ++ks) {   // P is lower triangular: P[m][r] = 0 for m < r
+                uint32_t b[4];
+                ldsm_x4_t(b, bt_addr(st + R_P, LC, 16 * np, 16 * ks, lane));
+                mma16816(a1[2 * np], ao[ks], b[0], b[1]);
+                mma16816(a1[2 * np + 1], ao[ks], b[2], b[3]);
+            }
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            uint32_t a[4];
+            acc_to_a(dm[2 * kk], dm[2 * kk + 1], a);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t b[4];
+                ldsm_x4(b, b_addr(st + R_K, LD, 16 * np, 16 * kk, lane));
+                mma16816(a2[2 * np], a, b[0], b[1]);
+                mma16816(a2[2 * np + 1], a, b[2], b[3]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 8 * nt + 2 * t4 + (e & 1);
+                a1[nt][e] = fmaf(r < c ? gC / gs[r] : 0.f, a2[nt][e], a1[nt][e]);
+            }
+        // dR^T = dW^T T (T unit lower triangular)
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a2[x][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t a[4];
+            acc_to_a(a1[2 * ks], a1[2 * ks + 1], a);
+#pragma unroll
+            for (int np = 0; np <= ks; ++np) {
+                uint32_t b[4];
+                ldsm_x4_t(b, bt_addr(st + R_T, LC, 16 * np, 16 * ks, lane));
+                mma16816(a2[2 * np], a, b[0], b[1]);
+                mma16816(a2[2 * np + 1], a, b[2], b[3]);
+            }
+        }
+        // dR out; -gamma beta dR as the A operand of the state update
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
+                if (r < c) dR[(row0 + r) * dv + j] = a2[nt][e];
+                a2[nt][e] *= -gs[r] * bs[r];
+            }
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dm[nt][e] *= gC;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t ar[4];
+            acc_to_a(a2[2 * ks], a2[2 * ks + 1], ar);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                uint32_t bq[4], bk[4];
+                ldsm_x4_t(bq, bt_addr(st + R_Q, LD, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bk, bt_addr(st + R_K, LD, 16 * np, 16 * ks, lane));
+                mma16816(dm[2 * np], ag[ks], bq[0], bq[1]);
+                mma16816(dm[2 * np + 1], ag[ks], bq[2], bq[3]);
+                mma16816(dm[2 * np], ar, bk[0], bk[1]);
+                mma16816(dm[2 * np + 1], ar, bk[2], bk[3]);
+            }
+        }
+        __syncthreads();   // every warp is done with this stage
+        issue(s, n - 2);
+    }
+    if (dinit) {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
+                dinit[((int64_t)bh * DK + i) * dv + j] = dm[nt][e];
             }
     }
 }
@@ -2182,28 +2103,35 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     cudaError_t err = launch_decay(g, d, gamma, BH, T, C, s);
     if (err != cudaSuccess) return err;
     constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
-    const bool mma_shape = kBf16 && dk == 128 && dv == 128 && C == 64;
+    // the warp-MMA kernels: bf16, d = 128, chunk 64, gradient outputs 16-byte aligned (their
+    // 16-byte stores); the states they pass on are value-major, so all four go together
+    const bool mma_shape = kBf16 && dk == 128 && dv == 128 && C == 64 &&
+                           ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk_out) |
+                             reinterpret_cast<uintptr_t>(dv_out)) & 15) == 0;
     if (mma_shape) {
         if constexpr (kBf16) {
+            __nv_bfloat16 *TPb = reinterpret_cast<__nv_bfloat16 *>(Tt);   // bf16 T, P tiles
+            __nv_bfloat16 *Wk2 = reinterpret_cast<__nv_bfloat16 *>(Wk);   // bf16 hi, lo rows
             if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
-            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, Pt, Tt, DKt,
-                                                                    U, Wk, T);
+            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, Pt, TPb, DKt,
+                                                                    U, Wk2, T);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            const size_t sf = 2 * (size_t)vc::F_STAGE, sr = 2 * (size_t)vc::R_STAGE;
+            if ((err = bwd_set_smem(bwd_fwd_state_vc_kernel, sf)) != cudaSuccess) return err;
+            bwd_fwd_state_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sf, s>>>(k, gamma, U, Wk2, init, W,
+                                                                              Mn, T, dv);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            if ((err = bwd_set_smem(bwd_chain_vc_kernel, sr)) != cudaSuccess) return err;
+            bwd_chain_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sr, s>>>(q, k, gamma, beta, dout, dfinal,
+                                                                          TPb, dR, dMn1, dinit, T, dv);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {
         const size_t s0 = tiles_smem(dk, dv, C);
         if ((err = bwd_set_smem(bwd_tiles_kernel<TE>, s0)) != cudaSuccess) return err;
         bwd_tiles_kernel<TE><<<dim3(NC, BH), 256, s0, s>>>(q, k, v, gamma, beta, Pt, Tt, DKt, U, Wk, T,
                                                           dk, dv, C);
-    }
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (mma_shape) {
-        if constexpr (kBf16) {
-            if ((err = bwd_set_smem(bwd_fwd_state_mma_kernel, mf::SMEM)) != cudaSuccess) return err;
-            bwd_fwd_state_mma_kernel<<<dim3(dv / mf::DS, BH), 256, mf::SMEM, s>>>(k, gamma, U, Wk, init,
-                                                                                 W, Mn, T, dv);
-            if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        }
-    } else {
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
         const int DSf = dv >= 32 ? 32 : 16;
         const size_t sf = sizeof(float) * ((size_t)dk * DSf + 2 * (size_t)C * (dk + 4) +
                                            2 * (size_t)C * DSf + (size_t)C);
@@ -2217,29 +2145,21 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
                                                                           Mn, T, dk, dv, C);
         }
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    if (mma_shape) {
-        if constexpr (kBf16) {
-            if ((err = bwd_set_smem(bwd_chain_mma_kernel, mc::SMEM)) != cudaSuccess) return err;
-            bwd_chain_mma_kernel<<<dim3(dv / mc::DS, BH), 256, mc::SMEM, s>>>(
-                q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dv);
+        if (dv >= 32) {
+            const size_t s1 = chain_smem(dk, 32, C, sizeof(TE));
+            if ((err = bwd_set_smem(bwd_chain_kernel<TE, 32>, s1)) != cudaSuccess) return err;
+            bwd_chain_kernel<TE, 32><<<dim3(dv / 32, BH), 256, s1, s>>>(
+                q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
+        } else {
+            const size_t s1 = chain_smem(dk, 16, C, sizeof(TE));
+            if ((err = bwd_set_smem(bwd_chain_kernel<TE, 16>, s1)) != cudaSuccess) return err;
+            bwd_chain_kernel<TE, 16><<<dim3(dv / 16, BH), 256, s1, s>>>(
+                q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
         }
-    } else if (dv >= 32) {
-        const size_t s1 = chain_smem(dk, 32, C, sizeof(TE));
-        if ((err = bwd_set_smem(bwd_chain_kernel<TE, 32>, s1)) != cudaSuccess) return err;
-        bwd_chain_kernel<TE, 32><<<dim3(dv / 32, BH), 256, s1, s>>>(
-            q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
-    } else {
-        const size_t s1 = chain_smem(dk, 16, C, sizeof(TE));
-        if ((err = bwd_set_smem(bwd_chain_kernel<TE, 16>, s1)) != cudaSuccess) return err;
-        bwd_chain_kernel<TE, 16><<<dim3(dv / 16, BH), 256, s1, s>>>(
-            q, k, gamma, beta, dout, dfinal, Pt, Tt, dR, dMn1, dinit, T, dk, dv, C);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if constexpr (kBf16) {
-        if (mma_shape &&
-            ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk_out) |
-              reinterpret_cast<uintptr_t>(dv_out)) & 15) == 0) {
+        if (mma_shape) {
             if ((err = bwd_set_smem(bwd_chunk_mma_kernel, mm::SMEM)) != cudaSuccess) return err;
             bwd_chunk_mma_kernel<<<dim3(NC, BH), 256, mm::SMEM, s>>>(
                 q, k, v, g, beta, d, gamma, W, Mn, dout, dR, dMn1, Pt, DKt, dq, dk_out, dv_out, dg,

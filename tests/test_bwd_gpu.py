@@ -81,6 +81,21 @@ def test_bwd_bf16_prefill_shape(T):
     check(*run(w), TOL["bf16"])
 
 
+@pytest.mark.parametrize("init,final", [(False, False), (True, False), (False, True)])
+def test_bwd_bf16_prefill_shape_optional_state_terms(init, final):
+    """The tensor-core kernels of the prefill shape without an initial state and / or a
+    final-state cotangent."""
+    w = I.PREFILL.with_(B=1, H=2, T=200)
+    check(*run(w, init=init, final=final), TOL["bf16"])
+
+
+@pytest.mark.parametrize("dk,dv,chunk", [(64, 64, 64), (128, 64, 32)])
+def test_bwd_bf16_other_shapes(dk, dv, chunk):
+    """bf16 shapes outside the tensor-core kernels' (d = 128, chunk 64): the CUDA-core path."""
+    w = I.PREFILL.with_(B=1, H=2, T=150, dk=dk, dv=dv, chunk=chunk)
+    check(*run(w), TOL["bf16"])
+
+
 @pytest.mark.parametrize("chunk,bound", [(16, -5.0), (64, -1.25)])
 def test_bwd_log_decay(chunk, bound):
     """The pages' log-domain decay: g_min = -5 on 16-token chunks, -1.25 on 64."""
