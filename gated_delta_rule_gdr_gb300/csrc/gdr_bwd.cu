@@ -1855,7 +1855,16 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
                 mma16816(w2[2 * np + 1], ah, bl4[2], bl4[3]);
             }
         }
-        // W = U - (w + w2), stored; then the columns scaled by gamma_C / gamma_r
+        // W = U - (w + w2), stored; then the columns scaled by gamma_C / gamma_r (this
+        // lane's 16 rows r = 8 nt + 2 t4 + e, e < 2)
+        float sc[8][2];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 8 * nt + 2 * t4 + e;
+                sc[nt][e] = r < c ? __fdividef(gC, gs[r]) : 0.f;
+            }
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -1863,7 +1872,7 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
                 const int r = 8 * nt + 2 * t4 + (e & 1), jl = 16 * warp + gq + 8 * (e >> 1);
                 const float x = us[r * LU + jl] - (w[nt][e] + w2[nt][e]);
                 if (r < c) W[(row0 + r) * dv + j0 + jl] = x;
-                w[nt][e] = r < c ? x * (gC / gs[r]) : 0.f;
+                w[nt][e] = x * sc[nt][e & 1];
             }
         // M^T <- gamma_C M^T + (W diag(sc))^T K
 #pragma unroll
@@ -1996,13 +2005,19 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
                 mma16816(a2[2 * np + 1], a, b[2], b[3]);
             }
         }
+        float sc[8][2], gb[8][2];   // this lane's rows r = 8 nt + 2 t4 + e, e < 2
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 8 * nt + 2 * t4 + (e & 1);
-                a1[nt][e] = fmaf(r < c ? gC / gs[r] : 0.f, a2[nt][e], a1[nt][e]);
+            for (int e = 0; e < 2; ++e) {
+                const int r = 8 * nt + 2 * t4 + e;
+                sc[nt][e] = r < c ? __fdividef(gC, gs[r]) : 0.f;
+                gb[nt][e] = -gs[r] * bs[r];
             }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a1[nt][e] = fmaf(sc[nt][e & 1], a2[nt][e], a1[nt][e]);
         // dR^T = dW^T T (T unit lower triangular)
 #pragma unroll
         for (int x = 0; x < 8; ++x)
@@ -2027,7 +2042,7 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
             for (int e = 0; e < 4; ++e) {
                 const int r = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
                 if (r < c) dR[(row0 + r) * dv + j] = a2[nt][e];
-                a2[nt][e] *= -gs[r] * bs[r];
+                a2[nt][e] *= gb[nt][e & 1];
             }
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
