@@ -1033,6 +1033,31 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
     }
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// rows 0 .. rows-1 of a row-major matrix (row_bytes a multiple of 16) into shared rows of
+// pitch sp bytes by cp.async; rows >= c are zero-filled (their source clamped to row 0)
+__device__ __forceinline__ void stage_rows(uint32_t dst, const void *src, int64_t src_pitch, int row_bytes,
+                                           int sp, int rows, int c, int tid, int nthreads) {
+    const int per_row = row_bytes / 16;
+    for (int x = tid; x < rows * per_row; x += nthreads) {
+        const int r = x / per_row, p = x % per_row;
+        const bool in = r < c;
+        const char *s = static_cast<const char *>(src) + (in ? r * src_pitch : 0) + 16 * p;
+        cp_async16(dst + r * sp + 16 * p, s, in ? 16u : 0u);
+    }
+}
+
 // ---------------------------------------------------------------- per-chunk gradients, warp MMA
 // The per-chunk gradients of the bf16 prefill shape (dk = dv = 128, C = 64) with every
 // product on warp-level MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
@@ -1044,10 +1069,11 @@ bwd_chunk_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *_
 namespace mm {
 constexpr int C = 64, D = 128, LD = D + 8, LC = C + 8;
 constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + C * LD * 2, OFF_O = OFF_K + C * LD * 2,
-                   OFF_W = OFF_O + C * LD * 2, OFF_R = OFF_W + C * LD * 2,
+                   OFF_W = OFF_O + C * LD * 2, OFF_R = OFF_W + D * LC * 2,
                    OFF_M = OFF_R + C * LD * 2, OFF_DM = OFF_M + D * LD * 2,
                    OFF_FP = OFF_DM + D * LD * 2, OFF_FA = OFF_FP + C * LC * 2,
-                   OFF_SC = OFF_FA + C * LC * 2;
+                   OFF_PT = OFF_FA + C * LC * 2, OFF_DK = OFF_PT + C * LC * 4,
+                   OFF_SC = OFF_DK + C * LC * 4;
 constexpr uint32_t SMEM = OFF_SC + (8 * C + 4) * 4;
 }  // namespace mm
 
@@ -1076,9 +1102,9 @@ __global__ void __launch_bounds__(256)
 bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
                      const float *__restrict__ beta, float d, const float *__restrict__ gamma,
-                     const float *__restrict__ W, const float *__restrict__ Mn,
+                     const __nv_bfloat16 *__restrict__ Wt, const __nv_bfloat16 *__restrict__ Sb,
                      const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ dR,
-                     const float *__restrict__ dMn1, const float *__restrict__ Pt,
+                     const __nv_bfloat16 *__restrict__ dSb, const float *__restrict__ Pt,
                      const float *__restrict__ DKt, __nv_bfloat16 *__restrict__ dq,
                      __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
                      float *__restrict__ dg, float *__restrict__ dbeta, int T) {
@@ -1096,32 +1122,35 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     float *gs = reinterpret_cast<float *>(smb + OFF_SC);
     float *bs = gs + C, *dbp = bs + C, *dbt = dbp + C, *rq = dbt + C, *rk = rq + C, *rz = rk + C;
     float *vdr = rz + C, *red = vdr + C;
-    const float *Mp = Mn + ((int64_t)bh * NC + n) * D * D;
-    const float *dMp = dMn1 + ((int64_t)bh * NC + n) * D * D;
+    const __nv_bfloat16 *Wp = Wt + ((int64_t)bh * NC + n) * D * C;    // W^T [j][r]
+    const __nv_bfloat16 *Sp = Sb + ((int64_t)bh * NC + n) * D * D;    // S = M^T [j][i]
+    const __nv_bfloat16 *dSp = dSb + ((int64_t)bh * NC + n) * D * D;  // dM'^T [j][i]
     const int64_t tb = ((int64_t)bh * NC + n) * C * C;
 
-    // ---- 0. loads: q, k, dO as given; W, dR, M, dM' rounded to bf16
+    // ---- 0. loads: q, k, dO, the bf16 tiles W^T, S, dS' and the fp32 P, DK tiles straight
+    //         into shared memory (one cp.async group, every copy in flight at once); dR
+    //         (rounded to bf16 on the way), v and beta through registers for dv and v.dR
     {
-        uint4 bq[4], bk[4], bo[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {   // 1024 16-byte pieces per C x 128 bf16 tile
-            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
-            const bool in = r < c;
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            bq[u] = in ? ld16(q + (row0 + r) * D + col) : z;
-            bk[u] = in ? ld16(k + (row0 + r) * D + col) : z;
-            bo[u] = in ? ld16(dout + (row0 + r) * D + col) : z;
-        }
-        float4 fw[8], fr[8];
+        stage_rows(sb + OFF_Q, q + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
+        stage_rows(sb + OFF_K, k + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
+        stage_rows(sb + OFF_O, dout + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
+        stage_rows(sb + OFF_W, Wp, C * 2, C * 2, LC * 2, D, D, tid, 256);
+        stage_rows(sb + OFF_M, Sp, D * 2, D * 2, LD * 2, D, D, tid, 256);
+        stage_rows(sb + OFF_DM, dSp, D * 2, D * 2, LD * 2, D, D, tid, 256);
+        stage_rows(sb + OFF_PT, Pt + tb, C * 4, C * 4, LC * 4, C, C, tid, 256);
+        stage_rows(sb + OFF_DK, DKt + tb, C * 4, C * 4, LC * 4, C, C, tid, 256);
+        cp_async_commit();
+        float4 fr[8];
         uint2 fv[8];
+        float br[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {   // 2048 float4 per C x 128 fp32 tile: warp w, row w + 8u
             const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
             const bool in = r < c;
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            fw[u] = in ? __ldg(reinterpret_cast<const float4 *>(W + (row0 + r) * D + col)) : z;
             fr[u] = in ? __ldg(reinterpret_cast<const float4 *>(dR + (row0 + r) * D + col)) : z;
             fv[u] = in ? __ldg(reinterpret_cast<const uint2 *>(v + (row0 + r) * D + col)) : make_uint2(0u, 0u);
+            br[u] = in ? beta[row0 + r] : 0.f;
         }
         for (int r = tid; r < C; r += 256) {
             gs[r] = r < c ? gamma[row0 + r] : 1.f;
@@ -1138,53 +1167,29 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
             float p = fmaf(v01.x, fr[u].x, fmaf(v01.y, fr[u].y, fmaf(v23.x, fr[u].z, v23.y * fr[u].w)));
             for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
             if (lane == 0) vdr[r] = p;
-            if (r < c) {
-                const float br = beta[row0 + r];
+            if (r < c)
                 *reinterpret_cast<uint2 *>(dv_out + (row0 + r) * D + col) =
-                    make_uint2(pack_bf2(br * fr[u].x, br * fr[u].y), pack_bf2(br * fr[u].z, br * fr[u].w));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
-            *reinterpret_cast<uint4 *>(smb + OFF_Q + 2 * (r * LD + col)) = bq[u];
-            *reinterpret_cast<uint4 *>(smb + OFF_K + 2 * (r * LD + col)) = bk[u];
-            *reinterpret_cast<uint4 *>(smb + OFF_O + 2 * (r * LD + col)) = bo[u];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
-            *reinterpret_cast<uint2 *>(smb + OFF_W + 2 * (r * LD + col)) =
-                make_uint2(pack_bf2(fw[u].x, fw[u].y), pack_bf2(fw[u].z, fw[u].w));
+                    make_uint2(pack_bf2(br[u] * fr[u].x, br[u] * fr[u].y), pack_bf2(br[u] * fr[u].z, br[u] * fr[u].w));
             *reinterpret_cast<uint2 *>(smb + OFF_R + 2 * (r * LD + col)) =
                 make_uint2(pack_bf2(fr[u].x, fr[u].y), pack_bf2(fr[u].z, fr[u].w));
         }
-        float mdm = 0.f;   // this thread's share of <M, dM'> (fp32, before rounding)
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {   // 4096 float4 per 128 x 128 tile, two batches
-            float4 fm[8], fd[8];
+        cp_async_wait0();
+        __syncthreads();   // the copies have landed; red[0] and the row sums are zeroed
+        float mdm = 0.f;   // this thread's share of <M, dM'>, from the bf16 copies
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int idx = tid + 256 * (u + 8 * half), r = idx >> 5, col = (idx & 31) * 4;
-                fm[u] = __ldg(reinterpret_cast<const float4 *>(Mp + r * D + col));
-                fd[u] = __ldg(reinterpret_cast<const float4 *>(dMp + r * D + col));
-            }
+        for (int u = 0; u < 8; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+            float fm[8], fd[8];
+            widen16(*reinterpret_cast<const uint4 *>(smb + OFF_M + 2 * (r * LD + col)), fm,
+                    (const __nv_bfloat16 *)nullptr);
+            widen16(*reinterpret_cast<const uint4 *>(smb + OFF_DM + 2 * (r * LD + col)), fd,
+                    (const __nv_bfloat16 *)nullptr);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int idx = tid + 256 * (u + 8 * half), r = idx >> 5, col = (idx & 31) * 4;
-                *reinterpret_cast<uint2 *>(smb + OFF_M + 2 * (r * LD + col)) =
-                    make_uint2(pack_bf2(fm[u].x, fm[u].y), pack_bf2(fm[u].z, fm[u].w));
-                *reinterpret_cast<uint2 *>(smb + OFF_DM + 2 * (r * LD + col)) =
-                    make_uint2(pack_bf2(fd[u].x, fd[u].y), pack_bf2(fd[u].z, fd[u].w));
-                mdm = fmaf(fm[u].x, fd[u].x, fmaf(fm[u].y, fd[u].y,
-                      fmaf(fm[u].z, fd[u].z, fmaf(fm[u].w, fd[u].w, mdm))));
-            }
+            for (int e = 0; e < 8; ++e) mdm = fmaf(fm[e], fd[e], mdm);
         }
         for (int off = 16; off > 0; off >>= 1) mdm += __shfl_xor_sync(0xffffffffu, mdm, off);
-        __syncthreads();   // red[0] zeroed
         if (lane == 0) atomicAdd(&red[0], mdm);
     }
-    __syncthreads();
 
     // ---- 1. position pairs: dP = dO W^T, dRW = dR W^T (rows mr .. mr + 15, columns nc .. nc + 31)
     {
@@ -1202,7 +1207,7 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 #pragma unroll
             for (int np = 0; np < 2; ++np) {
                 uint32_t bw[4];
-                ldsm_x4(bw, b_addr(sb + OFF_W, LD, nc + 16 * np, 16 * kk, lane));
+                ldsm_x4_t(bw, bt_addr(sb + OFF_W, LC, nc + 16 * np, 16 * kk, lane));   // W^T [j][s]
                 mma16816(ap[2 * np], ao, bw[0], bw[1]);
                 mma16816(ap[2 * np + 1], ao, bw[2], bw[3]);
                 mma16816(ar[2 * np], aq, bw[0], bw[1]);
@@ -1217,15 +1222,15 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 #pragma unroll
             for (int h = 0; h < 2; ++h) {   // rows gq, gq + 8
                 const int r = mr + gq + 8 * h, s0 = nc + 8 * nt + 2 * t4;
-                const float2 pp = *reinterpret_cast<const float2 *>(Pt + tb + r * C + s0);
-                const float2 dd = *reinterpret_cast<const float2 *>(DKt + tb + r * C + s0);
+                const float2 pp = *reinterpret_cast<const float2 *>(smb + OFF_PT + 4 * (r * LC + s0));
+                const float2 dd = *reinterpret_cast<const float2 *>(smb + OFF_DK + 4 * (r * LC + s0));
                 const float pv[2] = {pp.x, pp.y}, dv2[2] = {dd.x, dd.y};
                 float fp[2] = {0.f, 0.f}, fa[2] = {0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int s = s0 + e;
                     if (r < c && s <= r) {
-                        const float Dv = gs[r] / gs[s];
+                        const float Dv = __fdividef(gs[r], gs[s]);
                         const float dP = ap[nt][2 * h + e];
                         fp[e] = dP * Dv;
                         float ee = dP * pv[e];
@@ -1287,7 +1292,7 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         for (int mt = 0; mt < 2; ++mt) {
             ldsm_x4(ao[mt], a_addr(sb + OFF_O, LD, mr + 16 * mt, 16 * kk, lane));
             ldsm_x4(aq[mt], a_addr(sb + OFF_R, LD, mr + 16 * mt, 16 * kk, lane));
-            ldsm_x4(aw[mt], a_addr(sb + OFF_W, LD, mr + 16 * mt, 16 * kk, lane));
+            ldsm_x4_t(aw[mt], at_addr(sb + OFF_W, LC, mr + 16 * mt, 16 * kk, lane));
         }
 #pragma unroll
         for (int np = 0; np < 2; ++np) {
@@ -1337,7 +1342,7 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                     atomicAdd(&rk[r], pk);
                     atomicAdd(&rz[r], pz);
                 }
-                const float gr = gs[r], sc = gC / gr, gb = gr * bs[r];
+                const float gr = gs[r], sc = __fdividef(gC, gr), gb = gr * bs[r];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -1590,7 +1595,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int s = s0 + e;
-                const float D = gs[r] / gs[s];
+                const float D = __fdividef(gs[r], gs[s]);
                 p[e] = (r < c && s <= r) ? D * aq[nt][2 * h + e] : 0.f;
                 dd[e] = (r < c && s < r) ? D * ak[nt][2 * h + e] : 0.f;
             }
@@ -1719,32 +1724,8 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 // 2t, 2t + 1 and 2t + 8, 2t + 9 of two adjacent 8-column tiles), so a chunk's products
 // chain inside the warp without shared memory or barriers.  The chunk's shared inputs
 // arrive by cp.async into padded, double-buffered shared memory (the next chunk's copy
-// runs under this chunk's products): two barriers per chunk.  The chunk states are
-// stored value-major, S[j][i] = M[i][j], for the per-chunk gradients.
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
-// rows 0 .. 63 of a row-major matrix (bytes_per_row a multiple of 16) into shared rows of
-// pitch sp bytes; rows >= c are zero-filled (their source clamped to row 0)
-__device__ __forceinline__ void stage_rows(uint32_t dst, const void *src, int64_t src_pitch, int row_bytes,
-                                           int sp, int c, int tid, int nthreads) {
-    const int per_row = row_bytes / 16;
-    for (int x = tid; x < 64 * per_row; x += nthreads) {
-        const int r = x / per_row, p = x % per_row;
-        const bool in = r < c;
-        const char *s = static_cast<const char *>(src) + (in ? r * src_pitch : 0) + 16 * p;
-        cp_async16(dst + r * sp + 16 * p, s, in ? 16u : 0u);
-    }
-}
+// runs under this chunk's products): two barriers per chunk.  The chunk states go out
+// value-major in bf16, S[j][i] = M[i][j], for the per-chunk gradients.
 
 namespace vc {
 constexpr int C = 64, DK = 128, NW = 4, NT = 32 * NW, DSC = 16 * NW, LD = DK + 8, LC = C + 8;
@@ -1774,12 +1755,14 @@ __device__ __forceinline__ void acc_to_a_split(const float (&x0)[4], const float
 }
 
 // Forward state: per chunk W^T = U^T - M^T Wk^T (M^T and Wk as hi + lo, three products)
-// and M^T <- gamma_C M^T + (W diag(gamma_C / gamma))^T K (W as hi + lo); writes W
-// ([token][dv], fp32) and the state at every chunk start (value-major, fp32).
+// and M^T <- gamma_C M^T + (W diag(gamma_C / gamma))^T K (W as hi + lo); writes W^T per
+// chunk ([dv][C], bf16) and the state at every chunk start (value-major, bf16): the
+// per-chunk gradients take both as bf16 operands.
 __global__ void __launch_bounds__(vc::NT, 1)
 bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ gamma,
                         const float *__restrict__ U, const __nv_bfloat16 *__restrict__ Wk2,
-                        const float *init, float *__restrict__ W, float *__restrict__ Sn, int T, int dv) {
+                        const float *init, __nv_bfloat16 *__restrict__ Wt, __nv_bfloat16 *__restrict__ Sb,
+                        int T, int dv) {
     using namespace vc;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1795,10 +1778,10 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
             const uint32_t st = sb + (uint32_t)(n & 1) * F_STAGE;
             const int c = min(C, T - n * C);
             const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
-            stage_rows(st + F_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, c, tid, NT);
-            stage_rows(st + F_WH, Wk2 + row0 * 2 * DK, 4 * DK, DK * 2, LD * 2, c, tid, NT);
-            stage_rows(st + F_WL, Wk2 + row0 * 2 * DK + DK, 4 * DK, DK * 2, LD * 2, c, tid, NT);
-            stage_rows(st + F_U, U + row0 * dv + j0, (int64_t)dv * 4, DSC * 4, LU * 4, c, tid, NT);
+            stage_rows(st + F_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
+            stage_rows(st + F_WH, Wk2 + row0 * 2 * DK, 4 * DK, DK * 2, LD * 2, C, c, tid, NT);
+            stage_rows(st + F_WL, Wk2 + row0 * 2 * DK + DK, 4 * DK, DK * 2, LD * 2, C, c, tid, NT);
+            stage_rows(st + F_U, U + row0 * dv + j0, (int64_t)dv * 4, DSC * 4, LU * 4, C, c, tid, NT);
             if (tid < C) cp_async4(st + F_G + 4 * tid, gamma + row0 + (tid < c ? tid : 0), tid < c ? 4u : 0u);
         }
         cp_async_commit();
@@ -1820,14 +1803,14 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
         const uint32_t st = sb + (uint32_t)(n & 1) * F_STAGE;
         const float *gs = reinterpret_cast<const float *>(smb + (n & 1) * F_STAGE + F_G);
         const float *us = reinterpret_cast<const float *>(smb + (n & 1) * F_STAGE + F_U);
-        {   // the state at this chunk's start, value-major
-            float *dst = Sn + ((int64_t)bh * NC + n) * DK * dv;
+        {   // the state at this chunk's start, value-major bf16
+            __nv_bfloat16 *dst = Sb + ((int64_t)bh * NC + n) * DK * dv;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    *reinterpret_cast<float2 *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
-                        make_float2(mt[nt][2 * h], mt[nt][2 * h + 1]);
+                    *reinterpret_cast<uint32_t *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
+                        pack_bf2(mt[nt][2 * h], mt[nt][2 * h + 1]);
         }
         cp_async_wait1();
         __syncthreads();   // chunk n's stage has landed
@@ -1865,14 +1848,17 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
                 const int r = 8 * nt + 2 * t4 + e;
                 sc[nt][e] = r < c ? __fdividef(gC, gs[r]) : 0.f;
             }
+        __nv_bfloat16 *wt = Wt + ((int64_t)bh * NC + n) * dv * C;   // W^T [j][r], bf16, zero past c
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 8 * nt + 2 * t4 + (e & 1), jl = 16 * warp + gq + 8 * (e >> 1);
-                const float x = us[r * LU + jl] - (w[nt][e] + w2[nt][e]);
-                if (r < c) W[(row0 + r) * dv + j0 + jl] = x;
-                w[nt][e] = x * sc[nt][e & 1];
+            for (int h = 0; h < 2; ++h) {
+                const int r = 8 * nt + 2 * t4, jl = 16 * warp + gq + 8 * h;
+                const float x0 = us[r * LU + jl] - (w[nt][2 * h] + w2[nt][2 * h]);
+                const float x1 = us[(r + 1) * LU + jl] - (w[nt][2 * h + 1] + w2[nt][2 * h + 1]);
+                *reinterpret_cast<uint32_t *>(wt + (int64_t)(j0 + jl) * C + r) = pack_bf2(x0, x1);
+                w[nt][2 * h] = x0 * sc[nt][0];
+                w[nt][2 * h + 1] = x1 * sc[nt][1];
             }
         // M^T <- gamma_C M^T + (W diag(sc))^T K
 #pragma unroll
@@ -1901,13 +1887,13 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
 // Reverse chain: per chunk dW^T = dO^T P + (dM'^T K^T) diag(gamma_C / gamma),
 // dR^T = dW^T T (stored as dR [token][dv], fp32), and
 // dM^T <- gamma_C dM'^T + (diag(gamma) dO)^T Q + (-diag(gamma beta) dR)^T K; writes dM'
-// of every chunk (value-major) and the initial state's gradient.
+// of every chunk (value-major bf16) and the initial state's gradient (fp32).
 __global__ void __launch_bounds__(vc::NT, 1)
 bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                     const float *__restrict__ gamma, const float *__restrict__ beta,
                     const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
                     const __nv_bfloat16 *__restrict__ TPb, float *__restrict__ dR,
-                    float *__restrict__ dSn1, float *dinit, int T, int dv) {
+                    __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv) {
     using namespace vc;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1924,11 +1910,11 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
             const int c = min(C, T - n * C);
             const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
             const __nv_bfloat16 *tp = TPb + ((int64_t)bh * NC + n) * 2 * C * C;
-            stage_rows(st + R_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, c, tid, NT);
-            stage_rows(st + R_Q, q + row0 * DK, DK * 2, DK * 2, LD * 2, c, tid, NT);
-            stage_rows(st + R_T, tp, C * 2, C * 2, LC * 2, C, tid, NT);
-            stage_rows(st + R_P, tp + C * C, C * 2, C * 2, LC * 2, C, tid, NT);
-            stage_rows(st + R_O, dout + row0 * dv + j0, (int64_t)dv * 2, DSC * 2, LC * 2, c, tid, NT);
+            stage_rows(st + R_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
+            stage_rows(st + R_Q, q + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
+            stage_rows(st + R_T, tp, C * 2, C * 2, LC * 2, C, C, tid, NT);
+            stage_rows(st + R_P, tp + C * C, C * 2, C * 2, LC * 2, C, C, tid, NT);
+            stage_rows(st + R_O, dout + row0 * dv + j0, (int64_t)dv * 2, DSC * 2, LC * 2, C, c, tid, NT);
             if (tid < C) {
                 const int r = tid < c ? tid : 0;
                 cp_async4(st + R_G + 4 * tid, gamma + row0 + r, tid < c ? 4u : 0u);
@@ -1954,14 +1940,14 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
         const uint32_t st = sb + (uint32_t)s * R_STAGE;
         const float *gs = reinterpret_cast<const float *>(smb + s * R_STAGE + R_G);
         const float *bs = reinterpret_cast<const float *>(smb + s * R_STAGE + R_B);
-        {   // dM' of this chunk, value-major
-            float *dst = dSn1 + ((int64_t)bh * NC + n) * DK * dv;
+        {   // dM' of this chunk, value-major bf16
+            __nv_bfloat16 *dst = dSb + ((int64_t)bh * NC + n) * DK * dv;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    *reinterpret_cast<float2 *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
-                        make_float2(dm[nt][2 * h], dm[nt][2 * h + 1]);
+                    *reinterpret_cast<uint32_t *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
+                        pack_bf2(dm[nt][2 * h], dm[nt][2 * h + 1]);
         }
         cp_async_wait1();
         __syncthreads();
@@ -2109,7 +2095,7 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     float *U = gamma + round4(tok);
     float *Wk = U + round4(tok * dv);
     float *W = Wk + round4(tok * dk);
-    float *Mn = W + round4(tok * dv);
+    float *Mn = W + round4((size_t)BH * NC * C * dv);   // padded tokens: the bf16 W^T tiles
     float *dR = Mn + round4(st);
     float *dMn1 = dR + round4(tok * dv);
     float *Pt = dMn1 + round4(st);
@@ -2127,18 +2113,21 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
         if constexpr (kBf16) {
             __nv_bfloat16 *TPb = reinterpret_cast<__nv_bfloat16 *>(Tt);   // bf16 T, P tiles
             __nv_bfloat16 *Wk2 = reinterpret_cast<__nv_bfloat16 *>(Wk);   // bf16 hi, lo rows
+            __nv_bfloat16 *Wtb = reinterpret_cast<__nv_bfloat16 *>(W);    // bf16 W^T per chunk
+            __nv_bfloat16 *Sbb = reinterpret_cast<__nv_bfloat16 *>(Mn);   // bf16 value-major states
+            __nv_bfloat16 *dSbb = reinterpret_cast<__nv_bfloat16 *>(dMn1);
             if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
             bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, Pt, TPb, DKt,
                                                                     U, Wk2, T);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             const size_t sf = 2 * (size_t)vc::F_STAGE, sr = 2 * (size_t)vc::R_STAGE;
             if ((err = bwd_set_smem(bwd_fwd_state_vc_kernel, sf)) != cudaSuccess) return err;
-            bwd_fwd_state_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sf, s>>>(k, gamma, U, Wk2, init, W,
-                                                                              Mn, T, dv);
+            bwd_fwd_state_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sf, s>>>(k, gamma, U, Wk2, init, Wtb,
+                                                                              Sbb, T, dv);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             if ((err = bwd_set_smem(bwd_chain_vc_kernel, sr)) != cudaSuccess) return err;
             bwd_chain_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sr, s>>>(q, k, gamma, beta, dout, dfinal,
-                                                                          TPb, dR, dMn1, dinit, T, dv);
+                                                                          TPb, dR, dSbb, dinit, T, dv);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {
@@ -2177,8 +2166,9 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
         if (mma_shape) {
             if ((err = bwd_set_smem(bwd_chunk_mma_kernel, mm::SMEM)) != cudaSuccess) return err;
             bwd_chunk_mma_kernel<<<dim3(NC, BH), 256, mm::SMEM, s>>>(
-                q, k, v, g, beta, d, gamma, W, Mn, dout, dR, dMn1, Pt, DKt, dq, dk_out, dv_out, dg,
-                dbeta, T);
+                q, k, v, g, beta, d, gamma, reinterpret_cast<const __nv_bfloat16 *>(W),
+                reinterpret_cast<const __nv_bfloat16 *>(Mn), dout, dR,
+                reinterpret_cast<const __nv_bfloat16 *>(dMn1), Pt, DKt, dq, dk_out, dv_out, dg, dbeta, T);
             return cudaGetLastError();
         }
     }
@@ -2201,8 +2191,8 @@ size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C) {
     if (BH <= 0 || T <= 0) return 0;
     const int NC = (T + C - 1) / C;
     const size_t tok = (size_t)BH * T, st = (size_t)BH * NC * dk * dv;
-    return sizeof(float) * (round4(tok) + round4(tok * dv) + round4(tok * dk) + round4(tok * dv) +
-                            round4(st) + round4(tok * dv) + round4(st) +
+    return sizeof(float) * (round4(tok) + round4(tok * dv) + round4(tok * dk) +
+                            round4((size_t)BH * NC * C * dv) + round4(st) + round4(tok * dv) + round4(st) +
                             3 * round4((size_t)BH * NC * C * C));
 }
 

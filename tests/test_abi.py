@@ -243,9 +243,10 @@ def test_chunk_bwd_workspace_size(lib):
     f.argtypes = [ctypes.c_int] * 7
     f.restype = ctypes.c_size_t
     n = f(2, 3, 100, 128, 64, 64, 1)
-    # gamma, U, Wk, W, dR per token; M_n, dM' and the P, T, DK tiles per chunk; fp32
-    tok, st, tiles = 2 * 3 * 100, 2 * 3 * 2 * 128 * 64, 2 * 3 * 2 * 64 * 64
-    assert n == 4 * (tok + 3 * tok * 64 + tok * 128 + 2 * st + 3 * tiles)
+    # gamma, U, Wk, dR per token; W per token padded to whole chunks; M_n, dM' and the
+    # P, T, DK tiles per chunk; fp32 words
+    tok, pad, st, tiles = 2 * 3 * 100, 2 * 3 * 128, 2 * 3 * 2 * 128 * 64, 2 * 3 * 2 * 64 * 64
+    assert n == 4 * (tok + 2 * tok * 64 + tok * 128 + pad * 64 + 2 * st + 3 * tiles)
     assert f(2, 3, 0, 128, 64, 64, 1) == 0 and f(0, 3, 10, 128, 64, 64, 1) == 0
     assert f(1, 1, 10, 16, 64, 64, 1) == 0   # unsupported dk
 
