@@ -1,8 +1,8 @@
 // gdr_bwd.cu -- the backward of the chunked gated delta rule: the gradients of
 // a loss L with respect to q, k, v, g, beta and the initial state, given
 // dL/dout and dL/dfinal_state.  fp32 CUDA-core kernels (inputs and the output
-// gradients in the forward's element type, widened on load), except the per-chunk
-// gradients of the bf16 d = 128, chunk-64 shape, which run on warp MMAs.
+// gradients in the forward's element type, widened on load), except for the bf16
+// d = 128, chunk-64 shape, whose four kernels run on warp MMAs (below).
 //
 // The chunk algebra of the forward ("What a Trillion-Parameter MoE Model
 // Reveals About the Next Stage of LLM Scaling", sections 3.1-3.3; the staged

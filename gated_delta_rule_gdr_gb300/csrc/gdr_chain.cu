@@ -609,6 +609,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         float gv[2], bv[2];
         if (lane == 0)
             for (int n = 0; n < NST + kAhead; ++n) prefetch_l2(n);
+        grid_dependency_wait();   // the preparation kernel's tiles are complete and visible
         for (int n = 0; n < NST && n < NC; ++n) {
             load_gb(n, gv, bv);
             if (lane == 0) issue(n);
@@ -650,9 +651,21 @@ cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
     cudaError_t e = cudaFuncSetAttribute(chain_kernel<DVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    chain_kernel<DVH><<<(unsigned)(BH * (128 / DVH)), Cfg::NT, Cfg::SMEM_ALLOC, s>>>(
-        mq, mk, mv, mo, a, static_cast<const uint8_t *>(ws), nslot);
-    return cudaGetLastError();
+    // launched as a programmatic dependent of the preparation kernel before it: the CTAs
+    // set up (barriers, tensor memory, the initial state, L2 prefetch) while its last
+    // CTAs finish, and the copy warp waits for its tiles before the first read
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(BH * (128 / DVH)));
+    cfg.blockDim = dim3(Cfg::NT);
+    cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chain_kernel<DVH>, mq, mk, mv, mo, a, static_cast<const uint8_t *>(ws),
+                              nslot);
 }
 
 }  // namespace

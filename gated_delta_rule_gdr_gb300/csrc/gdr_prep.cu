@@ -108,6 +108,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_launch_dependents();   // the chain kernel after this one may start its set-up
     const uint32_t tmem = s_tmem;
     const uint32_t idesc_kqk = idesc_bf16(128, 64, false, false);
     float *As = reinterpret_cast<float *>(sm + OFF_AS);
