@@ -1460,8 +1460,8 @@ __device__ __forceinline__ void split_bf2(float a, float b, uint32_t &hi, uint32
 // U = (T diag(beta)) V, Wk = (T diag(beta gamma)) K on warp MMAs with the fp32 left
 // factors as bf16 hi + lo pairs (v and k exact).  Outputs as bwd_tiles_kernel, except
 // that T and P also go out as bf16 tiles for the reverse chain (TPb: per chunk T then P,
-// C x C each) and T not as fp32, and Wk goes out as bf16 hi + lo rows (Wk2: per token
-// dk hi values, then dk lo values) for the forward state pass.
+// C x C each) and T not as fp32, and Wk goes out as bf16 rows (Wk2) for the forward
+// state pass.
 namespace mt {
 constexpr int C = 64, DK = 128, LD = DK + 8, LA = C + 4, LC = C + 8;
 constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + C * LD * 2, OFF_R1 = OFF_V + C * LD * 2,
@@ -1705,11 +1705,8 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                     *reinterpret_cast<float2 *>(U + (row0 + r) * DK + j) =
                         make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
                 } else {
-                    uint32_t hi, lo;
-                    split_bf2(acc[nt][2 * h], acc[nt][2 * h + 1], hi, lo);
-                    __nv_bfloat16 *row = Wk2 + (row0 + r) * 2 * DK;
-                    *reinterpret_cast<uint32_t *>(row + j) = hi;
-                    *reinterpret_cast<uint32_t *>(row + DK + j) = lo;
+                    *reinterpret_cast<uint32_t *>(Wk2 + (row0 + r) * DK + j) =
+                        pack_bf2(acc[nt][2 * h], acc[nt][2 * h + 1]);
                 }
             }
     }
@@ -1729,9 +1726,9 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 
 namespace vc {
 constexpr int C = 64, DK = 128, NW = 4, NT = 32 * NW, DSC = 16 * NW, LD = DK + 8, LC = C + 8;
-// forward state stage: k, Wk hi, Wk lo (bf16 [C][LD]); U[:, slice] (fp32 [C][DSC + 4]); gamma
+// forward state stage: k, Wk (bf16 [C][LD]); U[:, slice] (fp32 [C][DSC + 4]); gamma
 constexpr int LU = DSC + 4;
-constexpr uint32_t F_K = 0, F_WH = F_K + C * LD * 2, F_WL = F_WH + C * LD * 2, F_U = F_WL + C * LD * 2,
+constexpr uint32_t F_K = 0, F_WH = F_K + C * LD * 2, F_U = F_WH + C * LD * 2,
                    F_G = F_U + C * LU * 4, F_STAGE = F_G + C * 4;
 // reverse chain stage: k, q (bf16 [C][LD]); P, T (bf16 [C][LC]); dO[:, slice] (bf16 [C][LC]); gamma, beta
 constexpr uint32_t R_K = 0, R_Q = R_K + C * LD * 2, R_P = R_Q + C * LD * 2, R_T = R_P + C * LC * 2,
@@ -1754,12 +1751,12 @@ __device__ __forceinline__ void acc_to_a_split(const float (&x0)[4], const float
     split_bf2(x1[2], x1[3], h[3], l[3]);
 }
 
-// Forward state: per chunk W^T = U^T - M^T Wk^T (M^T and Wk as hi + lo, three products)
+// Forward state: per chunk W^T = U^T - M^T Wk^T (M^T as hi + lo, Wk bf16: two products)
 // and M^T <- gamma_C M^T + (W diag(gamma_C / gamma))^T K (W as hi + lo); writes W^T per
 // chunk ([dv][C], bf16) and the state at every chunk start (value-major, bf16): the
 // per-chunk gradients take both as bf16 operands.
-__global__ void __launch_bounds__(vc::NT, 1)
-bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ gamma,
+__device__ __forceinline__ void
+fwd_state_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restrict__ k, const float *__restrict__ gamma,
                         const float *__restrict__ U, const __nv_bfloat16 *__restrict__ Wk2,
                         const float *init, __nv_bfloat16 *__restrict__ Wt, __nv_bfloat16 *__restrict__ Sb,
                         int T, int dv) {
@@ -1767,9 +1764,8 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
     using sm100::mma16816;
-    extern __shared__ __align__(16) uint8_t smb[];
     const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
     const uint32_t sb = sm100::smem_u32(smb);
     const int NC = (T + C - 1) / C;
     const int jw = j0 + 16 * warp;   // this warp's first value column
@@ -1779,8 +1775,7 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
             const int c = min(C, T - n * C);
             const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
             stage_rows(st + F_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
-            stage_rows(st + F_WH, Wk2 + row0 * 2 * DK, 4 * DK, DK * 2, LD * 2, C, c, tid, NT);
-            stage_rows(st + F_WL, Wk2 + row0 * 2 * DK + DK, 4 * DK, DK * 2, LD * 2, C, c, tid, NT);
+            stage_rows(st + F_WH, Wk2 + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
             stage_rows(st + F_U, U + row0 * dv + j0, (int64_t)dv * 4, DSC * 4, LU * 4, C, c, tid, NT);
             if (tid < C) cp_async4(st + F_G + 4 * tid, gamma + row0 + (tid < c ? tid : 0), tid < c ? 4u : 0u);
         }
@@ -1813,9 +1808,9 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
                         pack_bf2(mt[nt][2 * h], mt[nt][2 * h + 1]);
         }
         cp_async_wait1();
-        __syncthreads();   // chunk n's stage has landed
+        sm100::named_sync(bar_id, NT);   // chunk n's stage has landed
         const float gC = gs[c - 1];
-        // W^T (16 x 64): w the hi x hi products, w2 the two correction terms
+        // W^T (16 x 64): w from M^T hi, w2 from M^T lo
         float w[8][4], w2[8][4];
 #pragma unroll
         for (int x = 0; x < 8; ++x)
@@ -1827,15 +1822,12 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
             acc_to_a_split(mt[2 * kk], mt[2 * kk + 1], ah, al);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
-                uint32_t bh4[4], bl4[4];
+                uint32_t bh4[4];
                 ldsm_x4(bh4, b_addr(st + F_WH, LD, 16 * np, 16 * kk, lane));
-                ldsm_x4(bl4, b_addr(st + F_WL, LD, 16 * np, 16 * kk, lane));
                 mma16816(w[2 * np], ah, bh4[0], bh4[1]);
                 mma16816(w[2 * np + 1], ah, bh4[2], bh4[3]);
                 mma16816(w2[2 * np], al, bh4[0], bh4[1]);
                 mma16816(w2[2 * np + 1], al, bh4[2], bh4[3]);
-                mma16816(w2[2 * np], ah, bl4[0], bl4[1]);
-                mma16816(w2[2 * np + 1], ah, bl4[2], bl4[3]);
             }
         }
         // W = U - (w + w2), stored; then the columns scaled by gamma_C / gamma_r (this
@@ -1879,7 +1871,7 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
                 mma16816(mt[2 * np + 1], al, b[2], b[3]);
             }
         }
-        __syncthreads();   // every warp is done with this stage
+        sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
         issue(n + 2);
     }
 }
@@ -1888,8 +1880,8 @@ bwd_fwd_state_vc_kernel(const __nv_bfloat16 *__restrict__ k, const float *__rest
 // dR^T = dW^T T (stored as dR [token][dv], fp32), and
 // dM^T <- gamma_C dM'^T + (diag(gamma) dO)^T Q + (-diag(gamma beta) dR)^T K; writes dM'
 // of every chunk (value-major bf16) and the initial state's gradient (fp32).
-__global__ void __launch_bounds__(vc::NT, 1)
-bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+__device__ __forceinline__ void
+chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                     const float *__restrict__ gamma, const float *__restrict__ beta,
                     const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
                     const __nv_bfloat16 *__restrict__ TPb, float *__restrict__ dR,
@@ -1898,9 +1890,8 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
     using sm100::mma16816;
-    extern __shared__ __align__(16) uint8_t smb[];
     const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
     const uint32_t sb = sm100::smem_u32(smb);
     const int NC = (T + C - 1) / C;
     const int jw = j0 + 16 * warp;
@@ -1950,7 +1941,7 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
                         pack_bf2(dm[nt][2 * h], dm[nt][2 * h + 1]);
         }
         cp_async_wait1();
-        __syncthreads();
+        sm100::named_sync(bar_id, NT);
         const float gC = gs[c - 1];
         // dO^T fragments (k = token) and their gamma-scaled copies
         uint32_t ao[4][4], ag[4][4];
@@ -2049,7 +2040,7 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
                 mma16816(dm[2 * np + 1], ar, bk[2], bk[3]);
             }
         }
-        __syncthreads();   // every warp is done with this stage
+        sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
         issue(s, n - 2);
     }
     if (dinit) {
@@ -2061,6 +2052,27 @@ bwd_chain_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
                 dinit[((int64_t)bh * DK + i) * dv + j] = dm[nt][e];
             }
     }
+}
+
+// The two sequential passes in one launch: they are independent (both need only the
+// tiles), so warps 0-3 of a CTA run the forward state pass and warps 4-7 the reverse
+// chain for the same 64 value columns, each role with its own stages and named barrier:
+// every SM sub-partition gets one warp of each, whose latencies hide each other.
+__global__ void __launch_bounds__(2 * vc::NT, 1)
+bwd_passes_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ gamma,
+                     const float *__restrict__ beta, const float *__restrict__ U,
+                     const __nv_bfloat16 *__restrict__ Wk2, const __nv_bfloat16 *__restrict__ TPb,
+                     const float *init, const float *dfinal, __nv_bfloat16 *__restrict__ Wt,
+                     __nv_bfloat16 *__restrict__ Sb, float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb,
+                     float *dinit, int T, int dv) {
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int tid = threadIdx.x;
+    if (tid < vc::NT)
+        fwd_state_pass(smb, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
+    else
+        chain_pass(smb + 2 * vc::F_STAGE, tid - vc::NT, 2, q, k, gamma, beta, dout, dfinal, TPb, dR, dSb,
+                   dinit, T, dv);
 }
 
 template <typename K>
@@ -2112,7 +2124,7 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     if (mma_shape) {
         if constexpr (kBf16) {
             __nv_bfloat16 *TPb = reinterpret_cast<__nv_bfloat16 *>(Tt);   // bf16 T, P tiles
-            __nv_bfloat16 *Wk2 = reinterpret_cast<__nv_bfloat16 *>(Wk);   // bf16 hi, lo rows
+            __nv_bfloat16 *Wk2 = reinterpret_cast<__nv_bfloat16 *>(Wk);   // bf16 rows
             __nv_bfloat16 *Wtb = reinterpret_cast<__nv_bfloat16 *>(W);    // bf16 W^T per chunk
             __nv_bfloat16 *Sbb = reinterpret_cast<__nv_bfloat16 *>(Mn);   // bf16 value-major states
             __nv_bfloat16 *dSbb = reinterpret_cast<__nv_bfloat16 *>(dMn1);
@@ -2120,14 +2132,10 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, Pt, TPb, DKt,
                                                                     U, Wk2, T);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
-            const size_t sf = 2 * (size_t)vc::F_STAGE, sr = 2 * (size_t)vc::R_STAGE;
-            if ((err = bwd_set_smem(bwd_fwd_state_vc_kernel, sf)) != cudaSuccess) return err;
-            bwd_fwd_state_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sf, s>>>(k, gamma, U, Wk2, init, Wtb,
-                                                                              Sbb, T, dv);
-            if ((err = cudaGetLastError()) != cudaSuccess) return err;
-            if ((err = bwd_set_smem(bwd_chain_vc_kernel, sr)) != cudaSuccess) return err;
-            bwd_chain_vc_kernel<<<dim3(dv / vc::DSC, BH), vc::NT, sr, s>>>(q, k, gamma, beta, dout, dfinal,
-                                                                          TPb, dR, dSbb, dinit, T, dv);
+            const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE;
+            if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
+            bwd_passes_vc_kernel<<<dim3(dv / vc::DSC, BH), 2 * vc::NT, sp, s>>>(
+                q, k, dout, gamma, beta, U, Wk2, TPb, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {
