@@ -74,7 +74,7 @@ def test_bwd_optional_state_terms(init, final):
     check(*run(w, init=init, final=final), TOL["f32"])
 
 
-@pytest.mark.parametrize("T", [65, 300])
+@pytest.mark.parametrize("T", [1, 64, 65, 300])
 def test_bwd_bf16_prefill_shape(T):
     """The prefill workload's head shape (bf16, d = 128, chunk 64, init N(0, 0.02))."""
     w = I.PREFILL.with_(B=1, H=2, T=T)
@@ -87,6 +87,13 @@ def test_bwd_bf16_prefill_shape_optional_state_terms(init, final):
     final-state cotangent."""
     w = I.PREFILL.with_(B=1, H=2, T=200)
     check(*run(w, init=init, final=final), TOL["bf16"])
+
+
+def test_bwd_bf16_prefill_shape_log_decay():
+    """The tensor-core kernels with the pages' log-domain decay (g_min = -1.25 on 64-token
+    chunks, the range rule's limit)."""
+    w = I.PREFILL.with_(B=1, H=2, T=200)
+    check(*run(w, bound=-1.25, decay="log"), TOL["bf16"])
 
 
 @pytest.mark.parametrize("dk,dv,chunk", [(64, 64, 64), (128, 64, 32)])
