@@ -1075,6 +1075,8 @@ constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + C * LD * 2, OFF_O = OFF_K + C * LD
                    OFF_PT = OFF_FA + C * LC * 2, OFF_DK = OFF_PT + C * LC * 4,
                    OFF_SC = OFF_DK + C * LC * 4;
 constexpr uint32_t SMEM = OFF_SC + (8 * C + 4) * 4;
+static_assert(OFF_PT - OFF_FP >= C * LD * 2 && OFF_M - OFF_R >= C * LD * 2,
+              "dQ and dK leave through the FP, FA and dR tiles");
 }  // namespace mm
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -1107,339 +1109,364 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                      const __nv_bfloat16 *__restrict__ dSb, const float *__restrict__ Pt,
                      const float *__restrict__ DKt, __nv_bfloat16 *__restrict__ dq,
                      __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
-                     float *__restrict__ dg, float *__restrict__ dbeta, int T) {
+                     float *__restrict__ dg, float *__restrict__ dbeta, int T, int BH) {
     using namespace mm;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
     using sm100::mma16816;
     extern __shared__ __align__(16) uint8_t smb[];
-    const int n = blockIdx.x, bh = blockIdx.y;
     const int NC = (T + C - 1) / C;
-    const int t0 = n * C, c = min(C, T - t0);
-    const int64_t row0 = (int64_t)bh * T + t0;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
-    const uint32_t sb = sm100::smem_u32(smb);
-    float *gs = reinterpret_cast<float *>(smb + OFF_SC);
-    float *bs = gs + C, *dbp = bs + C, *dbt = dbp + C, *rq = dbt + C, *rk = rq + C, *rz = rk + C;
-    float *vdr = rz + C, *red = vdr + C;
-    const __nv_bfloat16 *Wp = Wt + ((int64_t)bh * NC + n) * D * C;    // W^T [j][r]
-    const __nv_bfloat16 *Sp = Sb + ((int64_t)bh * NC + n) * D * D;    // S = M^T [j][i]
-    const __nv_bfloat16 *dSp = dSb + ((int64_t)bh * NC + n) * D * D;  // dM'^T [j][i]
-    const int64_t tb = ((int64_t)bh * NC + n) * C * C;
-
-    // ---- 0. loads: q, k, dO, the bf16 tiles W^T, S, dS' and the fp32 P, DK tiles straight
-    //         into shared memory (one cp.async group, every copy in flight at once); dR
-    //         (rounded to bf16 on the way), v and beta through registers for dv and v.dR
-    {
-        stage_rows(sb + OFF_Q, q + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
-        stage_rows(sb + OFF_K, k + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
-        stage_rows(sb + OFF_O, dout + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
-        stage_rows(sb + OFF_W, Wp, C * 2, C * 2, LC * 2, D, D, tid, 256);
-        stage_rows(sb + OFF_M, Sp, D * 2, D * 2, LD * 2, D, D, tid, 256);
-        stage_rows(sb + OFF_DM, dSp, D * 2, D * 2, LD * 2, D, D, tid, 256);
-        stage_rows(sb + OFF_PT, Pt + tb, C * 4, C * 4, LC * 4, C, C, tid, 256);
-        stage_rows(sb + OFF_DK, DKt + tb, C * 4, C * 4, LC * 4, C, C, tid, 256);
+    const int ntask = NC * BH;
+    const int tid0 = threadIdx.x;
+    const uint32_t sb0 = sm100::smem_u32(smb);
+    // Persistent: one CTA per SM walks the chunks (task = bh * NC + n, stride gridDim.x).
+    // The tiles a chunk is done with early (P, DK after the position pairs; S, dS' after
+    // the state terms) take the next chunk's by cp.async while this one computes on.
+    auto stage_late_pt = [&](int t) {
+        if (t < ntask) {
+            const int64_t x = t;   // the tile index bh * NC + n
+            stage_rows(sb0 + OFF_PT, Pt + x * C * C, C * 4, C * 4, LC * 4, C, C, tid0, 256);
+            stage_rows(sb0 + OFF_DK, DKt + x * C * C, C * 4, C * 4, LC * 4, C, C, tid0, 256);
+        }
         cp_async_commit();
-        float4 fr[8];
-        uint2 fv[8];
-        float br[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {   // 2048 float4 per C x 128 fp32 tile: warp w, row w + 8u
-            const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
-            const bool in = r < c;
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            fr[u] = in ? __ldg(reinterpret_cast<const float4 *>(dR + (row0 + r) * D + col)) : z;
-            fv[u] = in ? __ldg(reinterpret_cast<const uint2 *>(v + (row0 + r) * D + col)) : make_uint2(0u, 0u);
-            br[u] = in ? beta[row0 + r] : 0.f;
+    };
+    auto stage_late_s = [&](int t) {   // S, dS', dO, W^T
+        if (t < ntask) {
+            const int64_t x = t;   // the tile index bh * NC + n
+            const int n2 = t % NC, c2 = min(C, T - n2 * C);
+            const int64_t r2 = (int64_t)(t / NC) * T + (int64_t)n2 * C;
+            stage_rows(sb0 + OFF_M, Sb + x * D * D, D * 2, D * 2, LD * 2, D, D, tid0, 256);
+            stage_rows(sb0 + OFF_DM, dSb + x * D * D, D * 2, D * 2, LD * 2, D, D, tid0, 256);
+            stage_rows(sb0 + OFF_O, dout + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
+            stage_rows(sb0 + OFF_W, Wt + x * D * C, C * 2, C * 2, LC * 2, D, D, tid0, 256);
         }
-        for (int r = tid; r < C; r += 256) {
-            gs[r] = r < c ? gamma[row0 + r] : 1.f;
-            bs[r] = r < c ? beta[row0 + r] : 0.f;
-            dbp[r] = dbt[r] = rq[r] = rk[r] = rz[r] = 0.f;
-        }
-        if (tid == 0) red[0] = 0.f;
-        // dv = diag(beta) dR (from the fp32 dR) and v_r . dR_r, one warp per row
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
-            const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fv[u].x));
-            const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fv[u].y));
-            float p = fmaf(v01.x, fr[u].x, fmaf(v01.y, fr[u].y, fmaf(v23.x, fr[u].z, v23.y * fr[u].w)));
-            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-            if (lane == 0) vdr[r] = p;
-            if (r < c)
-                *reinterpret_cast<uint2 *>(dv_out + (row0 + r) * D + col) =
-                    make_uint2(pack_bf2(br[u] * fr[u].x, br[u] * fr[u].y), pack_bf2(br[u] * fr[u].z, br[u] * fr[u].w));
-            *reinterpret_cast<uint2 *>(smb + OFF_R + 2 * (r * LD + col)) =
-                make_uint2(pack_bf2(fr[u].x, fr[u].y), pack_bf2(fr[u].z, fr[u].w));
-        }
-        cp_async_wait0();
-        __syncthreads();   // the copies have landed; red[0] and the row sums are zeroed
-        float mdm = 0.f;   // this thread's share of <M, dM'>, from the bf16 copies
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
-            float fm[8], fd[8];
-            widen16(*reinterpret_cast<const uint4 *>(smb + OFF_M + 2 * (r * LD + col)), fm,
-                    (const __nv_bfloat16 *)nullptr);
-            widen16(*reinterpret_cast<const uint4 *>(smb + OFF_DM + 2 * (r * LD + col)), fd,
-                    (const __nv_bfloat16 *)nullptr);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mdm = fmaf(fm[e], fd[e], mdm);
-        }
-        for (int off = 16; off > 0; off >>= 1) mdm += __shfl_xor_sync(0xffffffffu, mdm, off);
-        if (lane == 0) atomicAdd(&red[0], mdm);
-    }
+        cp_async_commit();
+    };
+    stage_late_pt(blockIdx.x);
+    stage_late_s(blockIdx.x);
+    for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
+        const int n = task % NC, bh = task / NC;
+        const int t0 = n * C, c = min(C, T - t0);
+        const int64_t row0 = (int64_t)bh * T + t0;
+        const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
+        const uint32_t sb = sm100::smem_u32(smb);
+        float *gs = reinterpret_cast<float *>(smb + OFF_SC);
+        float *bs = gs + C, *dbp = bs + C, *dbt = dbp + C, *rq = dbt + C, *rk = rq + C, *rz = rk + C;
+        float *vdr = rz + C, *red = vdr + C;
 
-    // ---- 1. position pairs: dP = dO W^T, dRW = dR W^T (rows mr .. mr + 15, columns nc .. nc + 31)
-    {
-        const int mr = 16 * (warp >> 1), nc = 32 * (warp & 1);
-        float ap[4][4], ar[4][4];
+        // ---- 0. loads: q, k straight into shared memory by cp.async (dO, W^T, S, dS', P,
+        //         DK are on their way since the previous chunk); dR
+        //         (rounded to bf16 on the way), v and beta through registers for dv and v.dR
+        {
+            stage_rows(sb + OFF_Q, q + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
+            stage_rows(sb + OFF_K, k + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
+            cp_async_commit();
+            float4 fr[8];
+            uint2 fv[8];
+            float br[8];
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ap[x][e] = ar[x][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            uint32_t ao[4], aq[4];
-            ldsm_x4(ao, a_addr(sb + OFF_O, LD, mr, 16 * kk, lane));
-            ldsm_x4(aq, a_addr(sb + OFF_R, LD, mr, 16 * kk, lane));
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t bw[4];
-                ldsm_x4_t(bw, bt_addr(sb + OFF_W, LC, nc + 16 * np, 16 * kk, lane));   // W^T [j][s]
-                mma16816(ap[2 * np], ao, bw[0], bw[1]);
-                mma16816(ap[2 * np + 1], ao, bw[2], bw[3]);
-                mma16816(ar[2 * np], aq, bw[0], bw[1]);
-                mma16816(ar[2 * np + 1], aq, bw[2], bw[3]);
+            for (int u = 0; u < 8; ++u) {   // 2048 float4 per C x 128 fp32 tile: warp w, row w + 8u
+                const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
+                const bool in = r < c;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                fr[u] = in ? __ldg(reinterpret_cast<const float4 *>(dR + (row0 + r) * D + col)) : z;
+                fv[u] = in ? __ldg(reinterpret_cast<const uint2 *>(v + (row0 + r) * D + col)) : make_uint2(0u, 0u);
+                br[u] = in ? beta[row0 + r] : 0.f;
             }
+            for (int r = tid; r < C; r += 256) {
+                gs[r] = r < c ? gamma[row0 + r] : 1.f;
+                bs[r] = r < c ? beta[row0 + r] : 0.f;
+                dbp[r] = dbt[r] = rq[r] = rk[r] = rz[r] = 0.f;
+            }
+            if (tid == 0) red[0] = 0.f;
+            // dv = diag(beta) dR (from the fp32 dR) and v_r . dR_r, one warp per row
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + 256 * u, r = idx >> 5, col = (idx & 31) * 4;
+                const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fv[u].x));
+                const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&fv[u].y));
+                float p = fmaf(v01.x, fr[u].x, fmaf(v01.y, fr[u].y, fmaf(v23.x, fr[u].z, v23.y * fr[u].w)));
+                for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+                if (lane == 0) vdr[r] = p;
+                if (r < c)
+                    *reinterpret_cast<uint2 *>(dv_out + (row0 + r) * D + col) =
+                        make_uint2(pack_bf2(br[u] * fr[u].x, br[u] * fr[u].y), pack_bf2(br[u] * fr[u].z, br[u] * fr[u].w));
+                *reinterpret_cast<uint2 *>(smb + OFF_R + 2 * (r * LD + col)) =
+                    make_uint2(pack_bf2(fr[u].x, fr[u].y), pack_bf2(fr[u].z, fr[u].w));
+            }
+            cp_async_wait0();
+            __syncthreads();   // the copies have landed; red[0] and the row sums are zeroed
+            float mdm = 0.f;   // this thread's share of <M, dM'>, from the bf16 copies
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
+                float fm[8], fd[8];
+                widen16(*reinterpret_cast<const uint4 *>(smb + OFF_M + 2 * (r * LD + col)), fm,
+                        (const __nv_bfloat16 *)nullptr);
+                widen16(*reinterpret_cast<const uint4 *>(smb + OFF_DM + 2 * (r * LD + col)), fd,
+                        (const __nv_bfloat16 *)nullptr);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mdm = fmaf(fm[e], fd[e], mdm);
+            }
+            for (int off = 16; off > 0; off >>= 1) mdm += __shfl_xor_sync(0xffffffffu, mdm, off);
+            if (lane == 0) atomicAdd(&red[0], mdm);
         }
-        // FP = dP o D, FA = dA o beta D (dA = -dRW), the db and dbeta pair terms
-        float re[2] = {0.f, 0.f}, rt[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            float ce[2] = {0.f, 0.f};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {   // rows gq, gq + 8
-                const int r = mr + gq + 8 * h, s0 = nc + 8 * nt + 2 * t4;
-                const float2 pp = *reinterpret_cast<const float2 *>(smb + OFF_PT + 4 * (r * LC + s0));
-                const float2 dd = *reinterpret_cast<const float2 *>(smb + OFF_DK + 4 * (r * LC + s0));
-                const float pv[2] = {pp.x, pp.y}, dv2[2] = {dd.x, dd.y};
-                float fp[2] = {0.f, 0.f}, fa[2] = {0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int s = s0 + e;
-                    if (r < c && s <= r) {
-                        const float Dv = __fdividef(gs[r], gs[s]);
-                        const float dP = ap[nt][2 * h + e];
-                        fp[e] = dP * Dv;
-                        float ee = dP * pv[e];
-                        if (s < r) {
-                            const float dA = -ar[nt][2 * h + e];
-                            fa[e] = dA * bs[r] * Dv;
-                            ee = fmaf(dA * bs[r], dv2[e], ee);
-                            rt[h] = fmaf(dA, dv2[e], rt[h]);
-                        }
-                        re[h] += ee;
-                        ce[e] -= ee;
-                    }
-                }
-                *reinterpret_cast<uint32_t *>(smb + OFF_FP + 2 * (r * LC + s0)) = pack_bf2(fp[0], fp[1]);
-                *reinterpret_cast<uint32_t *>(smb + OFF_FA + 2 * (r * LC + s0)) = pack_bf2(fa[0], fa[1]);
-            }
-            // column sums over the 8 row lanes (gq) sharing the column
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float x = ce[e];
-                x += __shfl_xor_sync(0xffffffffu, x, 4);
-                x += __shfl_xor_sync(0xffffffffu, x, 8);
-                x += __shfl_xor_sync(0xffffffffu, x, 16);
-                const int s = nc + 8 * nt + 2 * t4 + e;
-                if (gq == 0 && s < c) atomicAdd(&dbp[s], x);
-            }
-        }
-        // row sums over the 4 column lanes (t4) sharing the row
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float x = re[h], y = rt[h];
-            x += __shfl_xor_sync(0xffffffffu, x, 1);
-            x += __shfl_xor_sync(0xffffffffu, x, 2);
-            y += __shfl_xor_sync(0xffffffffu, y, 1);
-            y += __shfl_xor_sync(0xffffffffu, y, 2);
-            const int r = mr + gq + 8 * h;
-            if (t4 == 0 && r < c) {
-                atomicAdd(&dbp[r], x);
-                atomicAdd(&dbt[r], y);
-            }
-        }
-    }
-    __syncthreads();   // FP and FA are in shared memory
 
-    // ---- 2. state terms (rows mr .. mr + 31, key columns nc .. nc + 31):
-    //         X1 = dO M^T, X2 = dR M^T, X3 = W dM'^T
-    const int mr = 32 * (warp >> 2), nc = 32 * (warp & 3);
-    float x1[2][4][4], x2[2][4][4], x3[2][4][4];
+        // ---- 1. position pairs: dP = dO W^T, dRW = dR W^T (rows mr .. mr + 15, columns nc .. nc + 31)
+        {
+            const int mr = 16 * (warp >> 1), nc = 32 * (warp & 1);
+            float ap[4][4], ar[4][4];
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+            for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
+                for (int e = 0; e < 4; ++e) ap[x][e] = ar[x][e] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x1[a][b][e] = x2[a][b][e] = x3[a][b][e] = 0.f;
-#pragma unroll 2
-    for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t ao[2][4], aq[2][4], aw[2][4];
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t ao[4], aq[4];
+                ldsm_x4(ao, a_addr(sb + OFF_O, LD, mr, 16 * kk, lane));
+                ldsm_x4(aq, a_addr(sb + OFF_R, LD, mr, 16 * kk, lane));
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            ldsm_x4(ao[mt], a_addr(sb + OFF_O, LD, mr + 16 * mt, 16 * kk, lane));
-            ldsm_x4(aq[mt], a_addr(sb + OFF_R, LD, mr + 16 * mt, 16 * kk, lane));
-            ldsm_x4_t(aw[mt], at_addr(sb + OFF_W, LC, mr + 16 * mt, 16 * kk, lane));
-        }
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-            uint32_t bm[4], bd[4];   // the states are value-major: S[j][i] = M[i][j]
-            ldsm_x4_t(bm, bt_addr(sb + OFF_M, LD, nc + 16 * np, 16 * kk, lane));
-            ldsm_x4_t(bd, bt_addr(sb + OFF_DM, LD, nc + 16 * np, 16 * kk, lane));
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                mma16816(x1[mt][2 * np], ao[mt], bm[0], bm[1]);
-                mma16816(x1[mt][2 * np + 1], ao[mt], bm[2], bm[3]);
-                mma16816(x2[mt][2 * np], aq[mt], bm[0], bm[1]);
-                mma16816(x2[mt][2 * np + 1], aq[mt], bm[2], bm[3]);
-                mma16816(x3[mt][2 * np], aw[mt], bd[0], bd[1]);
-                mma16816(x3[mt][2 * np + 1], aw[mt], bd[2], bd[3]);
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t bw[4];
+                    ldsm_x4_t(bw, bt_addr(sb + OFF_W, LC, nc + 16 * np, 16 * kk, lane));   // W^T [j][s]
+                    mma16816(ap[2 * np], ao, bw[0], bw[1]);
+                    mma16816(ap[2 * np + 1], ao, bw[2], bw[3]);
+                    mma16816(ar[2 * np], aq, bw[0], bw[1]);
+                    mma16816(ar[2 * np + 1], aq, bw[2], bw[3]);
+                }
             }
-        }
-    }
-    // row dots q.(M dO), k.(M dR), k.(dM' w) over this warp's 32 key columns (the four
-    // column warps add up in shared memory); then the state terms of dQ (x1) and dK (x2)
-    {
-        const float gC = gs[c - 1];
+            // FP = dP o D, FA = dA o beta D (dA = -dRW), the db and dbeta pair terms
+            float re[2] = {0.f, 0.f}, rt[2] = {0.f, 0.f};
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+            for (int nt = 0; nt < 4; ++nt) {
+                float ce[2] = {0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = mr + 16 * mt + gq + 8 * h;
-                float pq = 0.f, pk = 0.f, pz = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    const int i = nc + 8 * nt + 2 * t4;
-                    const float2 qf = __bfloat1622float2(
-                        *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_Q + 2 * (r * LD + i)));
-                    const float2 kf = __bfloat1622float2(
-                        *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_K + 2 * (r * LD + i)));
-                    pq = fmaf(qf.x, x1[mt][nt][2 * h], fmaf(qf.y, x1[mt][nt][2 * h + 1], pq));
-                    pk = fmaf(kf.x, x2[mt][nt][2 * h], fmaf(kf.y, x2[mt][nt][2 * h + 1], pk));
-                    pz = fmaf(kf.x, x3[mt][nt][2 * h], fmaf(kf.y, x3[mt][nt][2 * h + 1], pz));
-                }
-                pq += __shfl_xor_sync(0xffffffffu, pq, 1);
-                pq += __shfl_xor_sync(0xffffffffu, pq, 2);
-                pk += __shfl_xor_sync(0xffffffffu, pk, 1);
-                pk += __shfl_xor_sync(0xffffffffu, pk, 2);
-                pz += __shfl_xor_sync(0xffffffffu, pz, 1);
-                pz += __shfl_xor_sync(0xffffffffu, pz, 2);
-                if (t4 == 0 && r < c) {
-                    atomicAdd(&rq[r], pq);
-                    atomicAdd(&rk[r], pk);
-                    atomicAdd(&rz[r], pz);
-                }
-                const float gr = gs[r], sc = __fdividef(gC, gr), gb = gr * bs[r];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
+                for (int h = 0; h < 2; ++h) {   // rows gq, gq + 8
+                    const int r = mr + gq + 8 * h, s0 = nc + 8 * nt + 2 * t4;
+                    const float2 pp = *reinterpret_cast<const float2 *>(smb + OFF_PT + 4 * (r * LC + s0));
+                    const float2 dd = *reinterpret_cast<const float2 *>(smb + OFF_DK + 4 * (r * LC + s0));
+                    const float pv[2] = {pp.x, pp.y}, dv2[2] = {dd.x, dd.y};
+                    float fp[2] = {0.f, 0.f}, fa[2] = {0.f, 0.f};
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        x1[mt][nt][2 * h + e] *= gr;
-                        x2[mt][nt][2 * h + e] = fmaf(sc, x3[mt][nt][2 * h + e], -gb * x2[mt][nt][2 * h + e]);
+                        const int s = s0 + e;
+                        if (r < c && s <= r) {
+                            const float Dv = __fdividef(gs[r], gs[s]);
+                            const float dP = ap[nt][2 * h + e];
+                            fp[e] = dP * Dv;
+                            float ee = dP * pv[e];
+                            if (s < r) {
+                                const float dA = -ar[nt][2 * h + e];
+                                fa[e] = dA * bs[r] * Dv;
+                                ee = fmaf(dA * bs[r], dv2[e], ee);
+                                rt[h] = fmaf(dA, dv2[e], rt[h]);
+                            }
+                            re[h] += ee;
+                            ce[e] -= ee;
+                        }
                     }
+                    *reinterpret_cast<uint32_t *>(smb + OFF_FP + 2 * (r * LC + s0)) = pack_bf2(fp[0], fp[1]);
+                    *reinterpret_cast<uint32_t *>(smb + OFF_FA + 2 * (r * LC + s0)) = pack_bf2(fa[0], fa[1]);
+                }
+                // column sums over the 8 row lanes (gq) sharing the column
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float x = ce[e];
+                    x += __shfl_xor_sync(0xffffffffu, x, 4);
+                    x += __shfl_xor_sync(0xffffffffu, x, 8);
+                    x += __shfl_xor_sync(0xffffffffu, x, 16);
+                    const int s = nc + 8 * nt + 2 * t4 + e;
+                    if (gq == 0 && s < c) atomicAdd(&dbp[s], x);
+                }
             }
-    }
-
-    // ---- 3. in-chunk terms: dQ += FP K,  dK += FP^T Q + FA K + FA^T K
+            // row sums over the 4 column lanes (t4) sharing the row
 #pragma unroll
-    for (int ks = 0; ks < C / 16; ++ks) {
-        uint32_t afp[2][4], afpt[2][4], afa[2][4], afat[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            ldsm_x4(afp[mt], a_addr(sb + OFF_FP, LC, mr + 16 * mt, 16 * ks, lane));
-            ldsm_x4_t(afpt[mt], at_addr(sb + OFF_FP, LC, mr + 16 * mt, 16 * ks, lane));
-            ldsm_x4(afa[mt], a_addr(sb + OFF_FA, LC, mr + 16 * mt, 16 * ks, lane));
-            ldsm_x4_t(afat[mt], at_addr(sb + OFF_FA, LC, mr + 16 * mt, 16 * ks, lane));
+            for (int h = 0; h < 2; ++h) {
+                float x = re[h], y = rt[h];
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                y += __shfl_xor_sync(0xffffffffu, y, 1);
+                y += __shfl_xor_sync(0xffffffffu, y, 2);
+                const int r = mr + gq + 8 * h;
+                if (t4 == 0 && r < c) {
+                    atomicAdd(&dbp[r], x);
+                    atomicAdd(&dbt[r], y);
+                }
+            }
         }
+        __syncthreads();   // FP and FA are in shared memory
+        stage_late_pt(task + (int)gridDim.x);   // P and DK are read: the next chunk's
+
+        // ---- 2. state terms (rows mr .. mr + 31, key columns nc .. nc + 31):
+        //         X1 = dO M^T, X2 = dR M^T, X3 = W dM'^T
+        const int mr = 32 * (warp >> 2), nc = 32 * (warp & 3);
+        float x1[2][4][4], x2[2][4][4], x3[2][4][4];
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {
-            uint32_t bk[4], bq[4];
-            ldsm_x4_t(bk, bt_addr(sb + OFF_K, LD, nc + 16 * np, 16 * ks, lane));
-            ldsm_x4_t(bq, bt_addr(sb + OFF_Q, LD, nc + 16 * np, 16 * ks, lane));
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x1[a][b][e] = x2[a][b][e] = x3[a][b][e] = 0.f;
+#pragma unroll 2
+        for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t ao[2][4], aq[2][4], aw[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                ldsm_x4(ao[mt], a_addr(sb + OFF_O, LD, mr + 16 * mt, 16 * kk, lane));
+                ldsm_x4(aq[mt], a_addr(sb + OFF_R, LD, mr + 16 * mt, 16 * kk, lane));
+                ldsm_x4_t(aw[mt], at_addr(sb + OFF_W, LC, mr + 16 * mt, 16 * kk, lane));
+            }
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                uint32_t bm[4], bd[4];   // the states are value-major: S[j][i] = M[i][j]
+                ldsm_x4_t(bm, bt_addr(sb + OFF_M, LD, nc + 16 * np, 16 * kk, lane));
+                ldsm_x4_t(bd, bt_addr(sb + OFF_DM, LD, nc + 16 * np, 16 * kk, lane));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    mma16816(x1[mt][2 * np], ao[mt], bm[0], bm[1]);
+                    mma16816(x1[mt][2 * np + 1], ao[mt], bm[2], bm[3]);
+                    mma16816(x2[mt][2 * np], aq[mt], bm[0], bm[1]);
+                    mma16816(x2[mt][2 * np + 1], aq[mt], bm[2], bm[3]);
+                    mma16816(x3[mt][2 * np], aw[mt], bd[0], bd[1]);
+                    mma16816(x3[mt][2 * np + 1], aw[mt], bd[2], bd[3]);
+                }
+            }
+        }
+        // row dots q.(M dO), k.(M dR), k.(dM' w) over this warp's 32 key columns (the four
+        // column warps add up in shared memory); then the state terms of dQ (x1) and dK (x2)
+        {
+            const float gC = gs[c - 1];
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int nt = 2 * np + hh;
-                    const uint32_t k0 = bk[2 * hh], k1 = bk[2 * hh + 1], q0 = bq[2 * hh], q1 = bq[2 * hh + 1];
-                    mma16816(x1[mt][nt], afp[mt], k0, k1);
-                    mma16816(x2[mt][nt], afpt[mt], q0, q1);
-                    mma16816(x2[mt][nt], afa[mt], k0, k1);
-                    mma16816(x2[mt][nt], afat[mt], k0, k1);
+                for (int h = 0; h < 2; ++h) {
+                    const int r = mr + 16 * mt + gq + 8 * h;
+                    float pq = 0.f, pk = 0.f, pz = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const int i = nc + 8 * nt + 2 * t4;
+                        const float2 qf = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_Q + 2 * (r * LD + i)));
+                        const float2 kf = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_K + 2 * (r * LD + i)));
+                        pq = fmaf(qf.x, x1[mt][nt][2 * h], fmaf(qf.y, x1[mt][nt][2 * h + 1], pq));
+                        pk = fmaf(kf.x, x2[mt][nt][2 * h], fmaf(kf.y, x2[mt][nt][2 * h + 1], pk));
+                        pz = fmaf(kf.x, x3[mt][nt][2 * h], fmaf(kf.y, x3[mt][nt][2 * h + 1], pz));
+                    }
+                    pq += __shfl_xor_sync(0xffffffffu, pq, 1);
+                    pq += __shfl_xor_sync(0xffffffffu, pq, 2);
+                    pk += __shfl_xor_sync(0xffffffffu, pk, 1);
+                    pk += __shfl_xor_sync(0xffffffffu, pk, 2);
+                    pz += __shfl_xor_sync(0xffffffffu, pz, 1);
+                    pz += __shfl_xor_sync(0xffffffffu, pz, 2);
+                    if (t4 == 0 && r < c) {
+                        atomicAdd(&rq[r], pq);
+                        atomicAdd(&rk[r], pk);
+                        atomicAdd(&rz[r], pz);
+                    }
+                    const float gr = gs[r], sc = __fdividef(gC, gr), gb = gr * bs[r];
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            x1[mt][nt][2 * h + e] *= gr;
+                            x2[mt][nt][2 * h + e] = fmaf(sc, x3[mt][nt][2 * h + e], -gb * x2[mt][nt][2 * h + e]);
+                        }
                 }
         }
-    }
 
-    // ---- 4. dQ and dK through shared memory (the dO and W tiles are dead) into
-    //         16-byte stores; then dbeta, db and dg per row
-    __syncthreads();
+        __syncthreads();                         // S and dS' are read: the next chunk's
+        stage_late_s(task + (int)gridDim.x);
+
+        // ---- 3. in-chunk terms: dQ += FP K,  dK += FP^T Q + FA K + FA^T K
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+        for (int ks = 0; ks < C / 16; ++ks) {
+            uint32_t afp[2][4], afpt[2][4], afa[2][4], afat[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = mr + 16 * mt + gq + 8 * h, i = nc + 8 * nt + 2 * t4;
-                *reinterpret_cast<uint32_t *>(smb + OFF_O + 2 * (r * LD + i)) =
-                    pack_bf2(x1[mt][nt][2 * h], x1[mt][nt][2 * h + 1]);
-                *reinterpret_cast<uint32_t *>(smb + OFF_W + 2 * (r * LD + i)) =
-                    pack_bf2(x2[mt][nt][2 * h], x2[mt][nt][2 * h + 1]);
+            for (int mt = 0; mt < 2; ++mt) {
+                ldsm_x4(afp[mt], a_addr(sb + OFF_FP, LC, mr + 16 * mt, 16 * ks, lane));
+                ldsm_x4_t(afpt[mt], at_addr(sb + OFF_FP, LC, mr + 16 * mt, 16 * ks, lane));
+                ldsm_x4(afa[mt], a_addr(sb + OFF_FA, LC, mr + 16 * mt, 16 * ks, lane));
+                ldsm_x4_t(afat[mt], at_addr(sb + OFF_FA, LC, mr + 16 * mt, 16 * ks, lane));
             }
-    __syncthreads();
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
-        if (r < c) {
-            *reinterpret_cast<uint4 *>(dq + (row0 + r) * D + col) =
-                *reinterpret_cast<const uint4 *>(smb + OFF_O + 2 * (r * LD + col));
-            *reinterpret_cast<uint4 *>(dk_out + (row0 + r) * D + col) =
-                *reinterpret_cast<const uint4 *>(smb + OFF_W + 2 * (r * LD + col));
+            for (int np = 0; np < 2; ++np) {
+                uint32_t bk[4], bq[4];
+                ldsm_x4_t(bk, bt_addr(sb + OFF_K, LD, nc + 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bq, bt_addr(sb + OFF_Q, LD, nc + 16 * np, 16 * ks, lane));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int nt = 2 * np + hh;
+                        const uint32_t k0 = bk[2 * hh], k1 = bk[2 * hh + 1], q0 = bq[2 * hh], q1 = bq[2 * hh + 1];
+                        mma16816(x1[mt][nt], afp[mt], k0, k1);
+                        mma16816(x2[mt][nt], afpt[mt], q0, q1);
+                        mma16816(x2[mt][nt], afa[mt], k0, k1);
+                        mma16816(x2[mt][nt], afat[mt], k0, k1);
+                    }
+            }
         }
-    }
-    if (warp == 0) {
-        const float gC = gs[c - 1];
-        float zsum = 0.f;
-        float db[2] = {0.f, 0.f};
+
+        // ---- 4. dQ and dK through shared memory (into the dead FP, FA and dR tiles) into
+        //         16-byte stores; then dbeta, db and dg per row
+        __syncthreads();
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = 2 * lane + e;
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = mr + 16 * mt + gq + 8 * h, i = nc + 8 * nt + 2 * t4;
+                    *reinterpret_cast<uint32_t *>(smb + OFF_FP + 2 * (r * LD + i)) =
+                        pack_bf2(x1[mt][nt][2 * h], x1[mt][nt][2 * h + 1]);
+                    *reinterpret_cast<uint32_t *>(smb + OFF_R + 2 * (r * LD + i)) =
+                        pack_bf2(x2[mt][nt][2 * h], x2[mt][nt][2 * h + 1]);
+                }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u, r = idx >> 4, col = (idx & 15) * 8;
             if (r < c) {
-                dbeta[row0 + r] = dbt[r] + vdr[r] - gs[r] * rk[r];
-                const float z = gC / gs[r] * rz[r];
-                zsum += z;
-                db[e] = dbp[r] + gs[r] * rq[r] - gs[r] * bs[r] * rk[r] - z;
+                *reinterpret_cast<uint4 *>(dq + (row0 + r) * D + col) =
+                    *reinterpret_cast<const uint4 *>(smb + OFF_FP + 2 * (r * LD + col));
+                *reinterpret_cast<uint4 *>(dk_out + (row0 + r) * D + col) =
+                    *reinterpret_cast<const uint4 *>(smb + OFF_R + 2 * (r * LD + col));
             }
         }
-        for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
-        const float last = zsum + gC * red[0];
+        if (warp == 0) {
+            const float gC = gs[c - 1];
+            float zsum = 0.f;
+            float db[2] = {0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-            if (2 * lane + e == c - 1) db[e] += last;
-        float suf = db[0] + db[1];
+            for (int e = 0; e < 2; ++e) {
+                const int r = 2 * lane + e;
+                if (r < c) {
+                    dbeta[row0 + r] = dbt[r] + vdr[r] - gs[r] * rk[r];
+                    const float z = gC / gs[r] * rz[r];
+                    zsum += z;
+                    db[e] = dbp[r] + gs[r] * rq[r] - gs[r] * bs[r] * rk[r] - z;
+                }
+            }
+            for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
+            const float last = zsum + gC * red[0];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_down_sync(0xffffffffu, suf, off);
-            if (lane + off < 32) suf += y;
+            for (int e = 0; e < 2; ++e)
+                if (2 * lane + e == c - 1) db[e] += last;
+            float suf = db[0] + db[1];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, suf, off);
+                if (lane + off < 32) suf += y;
+            }
+            const float dl[2] = {suf, suf - db[0]};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 2 * lane + e;
+                if (r < c) dg[row0 + r] = dl[e] * dlog_alpha_dg(g[row0 + r], d);
+            }
         }
-        const float dl[2] = {suf, suf - db[0]};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = 2 * lane + e;
-            if (r < c) dg[row0 + r] = dl[e] * dlog_alpha_dg(g[row0 + r], d);
-        }
+        __syncthreads();   // shared memory is free for the next chunk
     }
 }
 
@@ -2173,10 +2200,15 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     if constexpr (kBf16) {
         if (mma_shape) {
             if ((err = bwd_set_smem(bwd_chunk_mma_kernel, mm::SMEM)) != cudaSuccess) return err;
-            bwd_chunk_mma_kernel<<<dim3(NC, BH), 256, mm::SMEM, s>>>(
+            int dev = 0, nsm = 0;
+            if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+            if ((err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                return err;
+            const int ntask = NC * BH, grid = ntask < nsm ? ntask : nsm;
+            bwd_chunk_mma_kernel<<<grid, 256, mm::SMEM, s>>>(
                 q, k, v, g, beta, d, gamma, reinterpret_cast<const __nv_bfloat16 *>(W),
                 reinterpret_cast<const __nv_bfloat16 *>(Mn), dout, dR,
-                reinterpret_cast<const __nv_bfloat16 *>(dMn1), Pt, DKt, dq, dk_out, dv_out, dg, dbeta, T);
+                reinterpret_cast<const __nv_bfloat16 *>(dMn1), Pt, DKt, dq, dk_out, dv_out, dg, dbeta, T, BH);
             return cudaGetLastError();
         }
     }
