@@ -1142,8 +1142,18 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         }
         cp_async_commit();
     };
+    auto stage_late_qk = [&](int t) {   // q, k
+        if (t < ntask) {
+            const int n2 = t % NC, c2 = min(C, T - n2 * C);
+            const int64_t r2 = (int64_t)(t / NC) * T + (int64_t)n2 * C;
+            stage_rows(sb0 + OFF_Q, q + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
+            stage_rows(sb0 + OFF_K, k + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
+        }
+        cp_async_commit();
+    };
     stage_late_pt(blockIdx.x);
     stage_late_s(blockIdx.x);
+    stage_late_qk(blockIdx.x);
     for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
         const int n = task % NC, bh = task / NC;
         const int t0 = n * C, c = min(C, T - t0);
@@ -1154,13 +1164,10 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         float *bs = gs + C, *dbp = bs + C, *dbt = dbp + C, *rq = dbt + C, *rk = rq + C, *rz = rk + C;
         float *vdr = rz + C, *red = vdr + C;
 
-        // ---- 0. loads: q, k straight into shared memory by cp.async (dO, W^T, S, dS', P,
-        //         DK are on their way since the previous chunk); dR
+        // ---- 0. loads: every tile is on its way since the previous chunk (by cp.async into
+        //         shared memory as soon as that chunk was done with it); dR
         //         (rounded to bf16 on the way), v and beta through registers for dv and v.dR
         {
-            stage_rows(sb + OFF_Q, q + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
-            stage_rows(sb + OFF_K, k + row0 * D, D * 2, D * 2, LD * 2, C, c, tid, 256);
-            cp_async_commit();
             float4 fr[8];
             uint2 fv[8];
             float br[8];
@@ -1410,7 +1417,8 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 
         // ---- 4. dQ and dK through shared memory (into the dead FP, FA and dR tiles) into
         //         16-byte stores; then dbeta, db and dg per row
-        __syncthreads();
+        __syncthreads();                          // q and k are read: the next chunk's
+        stage_late_qk(task + (int)gridDim.x);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
