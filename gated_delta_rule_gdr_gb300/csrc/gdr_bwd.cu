@@ -1058,6 +1058,11 @@ __device__ __forceinline__ void stage_rows(uint32_t dst, const void *src, int64_
     }
 }
 
+// [p, p + bytes) towards L2 (16-byte aligned, a multiple of 16 bytes)
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- per-chunk gradients, warp MMA
 // The per-chunk gradients of the bf16 prefill shape (dk = dv = 128, C = 64) with every
 // product on warp-level MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
@@ -1139,6 +1144,10 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
             stage_rows(sb0 + OFF_DM, dSb + x * D * D, D * 2, D * 2, LD * 2, D, D, tid0, 256);
             stage_rows(sb0 + OFF_O, dout + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
             stage_rows(sb0 + OFF_W, Wt + x * D * C, C * 2, C * 2, LC * 2, D, D, tid0, 256);
+            if (tid0 == 0) {   // dR and v go through registers: towards L2 for now
+                l2_prefetch(dR + r2 * D, (uint32_t)c2 * D * 4);
+                l2_prefetch(v + r2 * D, (uint32_t)c2 * D * 2);
+            }
         }
         cp_async_commit();
     };
