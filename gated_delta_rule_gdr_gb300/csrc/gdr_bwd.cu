@@ -1077,10 +1077,10 @@ constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + C * LD * 2, OFF_O = OFF_K + C * LD
                    OFF_W = OFF_O + C * LD * 2, OFF_R = OFF_W + D * LC * 2,
                    OFF_M = OFF_R + C * LD * 2, OFF_DM = OFF_M + D * LD * 2,
                    OFF_FP = OFF_DM + D * LD * 2, OFF_FA = OFF_FP + C * LC * 2,
-                   OFF_PT = OFF_FA + C * LC * 2, OFF_DK = OFF_PT + C * LC * 4,
-                   OFF_SC = OFF_DK + C * LC * 4;
+                   OFF_Q2 = OFF_FA + C * LC * 2, OFF_K2 = OFF_Q2 + C * LD * 2,   // q, k: second slot
+                   OFF_SC = OFF_K2 + C * LD * 2;
 constexpr uint32_t SMEM = OFF_SC + (8 * C + 4) * 4;
-static_assert(OFF_PT - OFF_FP >= C * LD * 2 && OFF_M - OFF_R >= C * LD * 2,
+static_assert(OFF_Q2 - OFF_FP >= C * LD * 2 && OFF_M - OFF_R >= C * LD * 2,
               "dQ and dK leave through the FP, FA and dR tiles");
 }  // namespace mm
 
@@ -1111,8 +1111,7 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                      const float *__restrict__ beta, float d, const float *__restrict__ gamma,
                      const __nv_bfloat16 *__restrict__ Wt, const __nv_bfloat16 *__restrict__ Sb,
                      const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ dR,
-                     const __nv_bfloat16 *__restrict__ dSb, const float *__restrict__ Pt,
-                     const float *__restrict__ DKt, __nv_bfloat16 *__restrict__ dq,
+                     const __nv_bfloat16 *__restrict__ dSb, __nv_bfloat16 *__restrict__ dq,
                      __nv_bfloat16 *__restrict__ dk_out, __nv_bfloat16 *__restrict__ dv_out,
                      float *__restrict__ dg, float *__restrict__ dbeta, int T, int BH) {
     using namespace mm;
@@ -1125,16 +1124,8 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     const int tid0 = threadIdx.x;
     const uint32_t sb0 = sm100::smem_u32(smb);
     // Persistent: one CTA per SM walks the chunks (task = bh * NC + n, stride gridDim.x).
-    // The tiles a chunk is done with early (P, DK after the position pairs; S, dS' after
-    // the state terms) take the next chunk's by cp.async while this one computes on.
-    auto stage_late_pt = [&](int t) {
-        if (t < ntask) {
-            const int64_t x = t;   // the tile index bh * NC + n
-            stage_rows(sb0 + OFF_PT, Pt + x * C * C, C * 4, C * 4, LC * 4, C, C, tid0, 256);
-            stage_rows(sb0 + OFF_DK, DKt + x * C * C, C * 4, C * 4, LC * 4, C, C, tid0, 256);
-        }
-        cp_async_commit();
-    };
+    // The next chunk's tiles arrive by cp.async while this one computes: q, k into a
+    // second slot right away, S, dS', dO, W^T once this chunk's state terms are done.
     auto stage_late_s = [&](int t) {   // S, dS', dO, W^T
         if (t < ntask) {
             const int64_t x = t;   // the tile index bh * NC + n
@@ -1151,20 +1142,20 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         }
         cp_async_commit();
     };
-    auto stage_late_qk = [&](int t) {   // q, k
+    auto stage_late_qk = [&](int t, int slot) {   // q, k into slot 0 or 1 (alternating chunks)
         if (t < ntask) {
             const int n2 = t % NC, c2 = min(C, T - n2 * C);
             const int64_t r2 = (int64_t)(t / NC) * T + (int64_t)n2 * C;
-            stage_rows(sb0 + OFF_Q, q + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
-            stage_rows(sb0 + OFF_K, k + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
+            stage_rows(sb0 + (slot ? OFF_Q2 : OFF_Q), q + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
+            stage_rows(sb0 + (slot ? OFF_K2 : OFF_K), k + r2 * D, D * 2, D * 2, LD * 2, C, c2, tid0, 256);
         }
         cp_async_commit();
     };
-    stage_late_pt(blockIdx.x);
     stage_late_s(blockIdx.x);
-    stage_late_qk(blockIdx.x);
-    for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
+    stage_late_qk(blockIdx.x, 0);
+    for (int task = blockIdx.x, it = 0; task < ntask; task += gridDim.x, ++it) {
         const int n = task % NC, bh = task / NC;
+        const uint32_t oq = (it & 1) ? OFF_Q2 : OFF_Q, ok = (it & 1) ? OFF_K2 : OFF_K;   // this chunk's q, k
         const int t0 = n * C, c = min(C, T - t0);
         const int64_t row0 = (int64_t)bh * T + t0;
         const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
@@ -1212,6 +1203,7 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
             }
             cp_async_wait0();
             __syncthreads();   // the copies have landed; red[0] and the row sums are zeroed
+            stage_late_qk(task + (int)gridDim.x, (it + 1) & 1);   // the next chunk's q, k: the other slot
             float mdm = 0.f;   // this thread's share of <M, dM'>, from the bf16 copies
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -1231,11 +1223,11 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         // ---- 1. position pairs: dP = dO W^T, dRW = dR W^T (rows mr .. mr + 15, columns nc .. nc + 31)
         {
             const int mr = 16 * (warp >> 1), nc = 32 * (warp & 1);
-            float ap[4][4], ar[4][4];
+            float ap[4][4], ar[4][4], xq[4][4], xk[4][4];
 #pragma unroll
             for (int x = 0; x < 4; ++x)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ap[x][e] = ar[x][e] = 0.f;
+                for (int e = 0; e < 4; ++e) ap[x][e] = ar[x][e] = xq[x][e] = xk[x][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 uint32_t ao[4], aq[4];
@@ -1251,6 +1243,26 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                     mma16816(ar[2 * np + 1], aq, bw[2], bw[3]);
                 }
             }
+            // Q K^T and K K^T again (exact products of the bf16 inputs): the P and D o K K^T
+            // of the pair terms, without a round trip through memory; the two tiles wholly
+            // above the diagonal skip them
+            if (nc <= mr + 15) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t a_q[4], a_k[4];
+                    ldsm_x4(a_q, a_addr(sb + oq, LD, mr, 16 * kk, lane));
+                    ldsm_x4(a_k, a_addr(sb + ok, LD, mr, 16 * kk, lane));
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        uint32_t b[4];
+                        ldsm_x4(b, b_addr(sb + ok, LD, nc + 16 * np, 16 * kk, lane));
+                        mma16816(xq[2 * np], a_q, b[0], b[1]);
+                        mma16816(xq[2 * np + 1], a_q, b[2], b[3]);
+                        mma16816(xk[2 * np], a_k, b[0], b[1]);
+                        mma16816(xk[2 * np + 1], a_k, b[2], b[3]);
+                    }
+                }
+            }
             // FP = dP o D, FA = dA o beta D (dA = -dRW), the db and dbeta pair terms
             float re[2] = {0.f, 0.f}, rt[2] = {0.f, 0.f};
 #pragma unroll
@@ -1259,9 +1271,6 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // rows gq, gq + 8
                     const int r = mr + gq + 8 * h, s0 = nc + 8 * nt + 2 * t4;
-                    const float2 pp = *reinterpret_cast<const float2 *>(smb + OFF_PT + 4 * (r * LC + s0));
-                    const float2 dd = *reinterpret_cast<const float2 *>(smb + OFF_DK + 4 * (r * LC + s0));
-                    const float pv[2] = {pp.x, pp.y}, dv2[2] = {dd.x, dd.y};
                     float fp[2] = {0.f, 0.f}, fa[2] = {0.f, 0.f};
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -1270,12 +1279,12 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                             const float Dv = __fdividef(gs[r], gs[s]);
                             const float dP = ap[nt][2 * h + e];
                             fp[e] = dP * Dv;
-                            float ee = dP * pv[e];
+                            float ee = dP * (Dv * xq[nt][2 * h + e]);   // dP P
                             if (s < r) {
-                                const float dA = -ar[nt][2 * h + e];
+                                const float dA = -ar[nt][2 * h + e], dkk = Dv * xk[nt][2 * h + e];
                                 fa[e] = dA * bs[r] * Dv;
-                                ee = fmaf(dA * bs[r], dv2[e], ee);
-                                rt[h] = fmaf(dA, dv2[e], rt[h]);
+                                ee = fmaf(dA * bs[r], dkk, ee);
+                                rt[h] = fmaf(dA, dkk, rt[h]);
                             }
                             re[h] += ee;
                             ce[e] -= ee;
@@ -1311,7 +1320,6 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
             }
         }
         __syncthreads();   // FP and FA are in shared memory
-        stage_late_pt(task + (int)gridDim.x);   // P and DK are read: the next chunk's
 
         // ---- 2. state terms (rows mr .. mr + 31, key columns nc .. nc + 31):
         //         X1 = dO M^T, X2 = dR M^T, X3 = W dM'^T
@@ -1362,9 +1370,9 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                     for (int nt = 0; nt < 4; ++nt) {
                         const int i = nc + 8 * nt + 2 * t4;
                         const float2 qf = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_Q + 2 * (r * LD + i)));
+                            *reinterpret_cast<const __nv_bfloat162 *>(smb + oq + 2 * (r * LD + i)));
                         const float2 kf = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162 *>(smb + OFF_K + 2 * (r * LD + i)));
+                            *reinterpret_cast<const __nv_bfloat162 *>(smb + ok + 2 * (r * LD + i)));
                         pq = fmaf(qf.x, x1[mt][nt][2 * h], fmaf(qf.y, x1[mt][nt][2 * h + 1], pq));
                         pk = fmaf(kf.x, x2[mt][nt][2 * h], fmaf(kf.y, x2[mt][nt][2 * h + 1], pk));
                         pz = fmaf(kf.x, x3[mt][nt][2 * h], fmaf(kf.y, x3[mt][nt][2 * h + 1], pz));
@@ -1408,8 +1416,8 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 #pragma unroll
             for (int np = 0; np < 2; ++np) {
                 uint32_t bk[4], bq[4];
-                ldsm_x4_t(bk, bt_addr(sb + OFF_K, LD, nc + 16 * np, 16 * ks, lane));
-                ldsm_x4_t(bq, bt_addr(sb + OFF_Q, LD, nc + 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bk, bt_addr(sb + ok, LD, nc + 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bq, bt_addr(sb + oq, LD, nc + 16 * np, 16 * ks, lane));
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -1426,8 +1434,7 @@ bwd_chunk_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 
         // ---- 4. dQ and dK through shared memory (into the dead FP, FA and dR tiles) into
         //         16-byte stores; then dbeta, db and dg per row
-        __syncthreads();                          // q and k are read: the next chunk's
-        stage_late_qk(task + (int)gridDim.x);
+        __syncthreads();
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -1502,10 +1509,10 @@ __device__ __forceinline__ void split_bf2(float a, float b, uint32_t &hi, uint32
 // (the four 16 x 16 diagonal blocks a column per lane, then the off-diagonal blocks
 // by distance from the diagonal: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj), and
 // U = (T diag(beta)) V, Wk = (T diag(beta gamma)) K on warp MMAs with the fp32 left
-// factors as bf16 hi + lo pairs (v and k exact).  Outputs as bwd_tiles_kernel, except
-// that T and P also go out as bf16 tiles for the reverse chain (TPb: per chunk T then P,
-// C x C each) and T not as fp32, and Wk goes out as bf16 rows (Wk2) for the forward
-// state pass.
+// factors as bf16 hi + lo pairs (v and k exact).  Outputs: T and P as bf16 tiles for
+// the reverse chain (TPb: per chunk T then P, C x C each), U (fp32) and Wk as bf16 rows
+// (Wk2) for the forward state pass; the per-chunk kernel forms its fp32 P and D o K K^T
+// itself from q and k.
 namespace mt {
 constexpr int C = 64, DK = 128, LD = DK + 8, LA = C + 4, LC = C + 8;
 constexpr uint32_t OFF_K = 0, OFF_V = OFF_K + C * LD * 2, OFF_R1 = OFF_V + C * LD * 2,
@@ -1559,9 +1566,8 @@ __device__ __forceinline__ void solve_offdiag(const float *As, float *Ts, float 
 __global__ void __launch_bounds__(256, 2)
 bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
-                     const float *__restrict__ beta, float *__restrict__ Pt,
-                     __nv_bfloat16 *__restrict__ TPb, float *__restrict__ DKt, float *__restrict__ U,
-                     __nv_bfloat16 *__restrict__ Wk2, int T) {
+                     const float *__restrict__ beta, __nv_bfloat16 *__restrict__ TPb,
+                     float *__restrict__ U, __nv_bfloat16 *__restrict__ Wk2, int T) {
     using namespace mt;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1643,9 +1649,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                 p[e] = (r < c && s <= r) ? D * aq[nt][2 * h + e] : 0.f;
                 dd[e] = (r < c && s < r) ? D * ak[nt][2 * h + e] : 0.f;
             }
-            *reinterpret_cast<float2 *>(Pt + tb + r * C + s0) = make_float2(p[0], p[1]);
             *reinterpret_cast<uint32_t *>(Pb + r * C + s0) = pack_bf2(p[0], p[1]);
-            *reinterpret_cast<float2 *>(DKt + tb + r * C + s0) = make_float2(dd[0], dd[1]);
             *reinterpret_cast<float2 *>(As + r * LA + s0) = make_float2(bs[r] * dd[0], bs[r] * dd[1]);
         }
     // the blocks of T above the diagonal are zero
@@ -1838,7 +1842,6 @@ fwd_state_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__re
     issue(1);
     for (int n = 0; n < NC; ++n) {
         const int c = min(C, T - n * C);
-        const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
         const uint32_t st = sb + (uint32_t)(n & 1) * F_STAGE;
         const float *gs = reinterpret_cast<const float *>(smb + (n & 1) * F_STAGE + F_G);
         const float *us = reinterpret_cast<const float *>(smb + (n & 1) * F_STAGE + F_U);
@@ -2173,8 +2176,7 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             __nv_bfloat16 *Sbb = reinterpret_cast<__nv_bfloat16 *>(Mn);   // bf16 value-major states
             __nv_bfloat16 *dSbb = reinterpret_cast<__nv_bfloat16 *>(dMn1);
             if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
-            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, Pt, TPb, DKt,
-                                                                    U, Wk2, T);
+            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE;
             if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
@@ -2225,7 +2227,7 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             bwd_chunk_mma_kernel<<<grid, 256, mm::SMEM, s>>>(
                 q, k, v, g, beta, d, gamma, reinterpret_cast<const __nv_bfloat16 *>(W),
                 reinterpret_cast<const __nv_bfloat16 *>(Mn), dout, dR,
-                reinterpret_cast<const __nv_bfloat16 *>(dMn1), Pt, DKt, dq, dk_out, dv_out, dg, dbeta, T, BH);
+                reinterpret_cast<const __nv_bfloat16 *>(dMn1), dq, dk_out, dv_out, dg, dbeta, T, BH);
             return cudaGetLastError();
         }
     }
