@@ -439,6 +439,24 @@ def cpu_baseline_decode(w, budget_s=8.0):
             "ms_per_step": 1e3 * t_tot / steps}
 
 
+def rank_barrier(dist, sync=None):
+    """The device's work done (sync), then every rank at the same point."""
+    if sync is not None:
+        sync()
+    if dist is not None:
+        dist.barrier()
+
+
+def rank_max(dist, x: float) -> float:
+    """The maximum of x over the ranks (x itself with one process): the timed region
+    ends when the slowest replica ends."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args):
     import gated_delta_rule_gdr_gb300 as gdr
     rank = int(os.environ.get("RANK", "0"))
@@ -459,16 +477,10 @@ def run_ours(args):
     varlen = main_w is I.VARLEN
 
     def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
+        rank_barrier(dist, torch.cuda.synchronize)
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(dist, x)
 
     result = {}
     with ClockSampler(dev.index) as clocks:
