@@ -9,7 +9,10 @@ prefill over B=4, H=16, T=4096, d=128, bf16 (cumulative decay, WY/UT
 transform, state pass and output); ``value`` is prefill tokens/s (B*T per
 step).  The same line carries a ``decode`` object for the single-token decode
 workload (N=256 sequences x H=32 heads, one token per step), because the
-metric asks for both.  ``--workload varlen`` times the packed variable-length
+metric asks for both, a ``backward`` object (the gradients of the prefill
+workload), and ``long`` (B=1, H=32, T=65536) and ``million`` (B=1, H=16,
+T=1,048,576) objects for the two long prefill workloads, each with its own
+roofline and oracle baseline.  ``--workload varlen`` times the packed variable-length
 prefill instead: 32 sequences of seeded lengths in [16, 4096] (34,599 tokens),
 H=16, through ``chunk_fwd_varlen``; ``value`` is packed tokens/s.
 
@@ -145,15 +148,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def committed_traffic(kernel: str, source_files):
-    """ncu DRAM bytes per launch committed under profiles/, valid only while the
-    kernel's source is unchanged (sha256 of its files)."""
+def committed_traffic(kernel: str, source_files, workload: str | None = None):
+    """ncu DRAM bytes per launch committed under profiles/ (keyed "kernel @ workload",
+    or by the kernel alone), valid only while the kernel's source is unchanged (sha256
+    of its files)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    ent = d.get(kernel)
+    ent = d.get(f"{kernel} @ {workload}") if workload else None
+    ent = ent or d.get(kernel)
     if not ent:
         return None
     h = hashlib.sha256()
@@ -298,6 +303,74 @@ def bench_varlen(gdr, w, K, W, dev, flush, stream, workspace="auto"):
     return ms, ms_e2e, h2d, d2h
 
 
+def bench_prefill_leg(gdr, w, K, W, dev, stream):
+    """Device-resident prefill of a long workload through the binding's default path
+    (the caller-owned workspace of the two-kernel path); per-step CUDA-event times.
+    Its inputs (2.2 GB, 17.3 GB) are far larger than L2, so no flush is needed."""
+    x = I.prefill_inputs(w, device=dev)
+    out = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.torch_dtype(), device=dev)
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    nws = gdr.chunk_fwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.torch_dtype())
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+
+    def step(_):
+        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                      chunk=w.chunk, out=out, final_state=fin, workspace=ws)
+
+    ms = time_steps(step, K, W, None, stream)
+    return ms, x
+
+
+def prefill_leg_line(gdr, w, ms, pk, pk_kind, world, max_over_ranks):
+    """The JSON object of a prefill leg: value, roofline of its kernels, launches."""
+    path = gdr.chunk_fwd_path(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.a_min, w.torch_dtype())
+    kname, srcs, nk = path_kernels(path)
+    mean = statistics.mean(ms)
+    by, fl = prefill_algorithmic(w)
+    gbs = by / (mean * 1e-3) / 1e9
+    return {
+        "metric": "prefill tokens/s", "workload": w.name,
+        "value": round(world * w.B * w.T / (max_over_ranks(mean) * 1e-3), 1), "unit": "tokens/s",
+        "ms_per_step": round(mean, 4), "steps": len(ms), "path": gdr.PATHS.get(path, str(path)),
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(gbs, 1),
+                     "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm_gbs"], 4),
+                     "traffic": committed_traffic(kname, srcs, w.name),
+                     "algorithmic_bytes": by, "algorithmic_flops": fl,
+                     "achieved_tflops": round(fl / (mean * 1e-3) / 1e12, 2),
+                     "nominal_hbm_frac": round(gbs / 7900.0, 4)},
+        "l2": "inputs far larger than L2, no flush",
+        "gpu_launches": nk * len(ms),
+        "ms_per_step_all": [round(t, 4) for t in ms],
+    }
+
+
+CSRC = "gated_delta_rule_gdr_gb300/csrc/"
+# the four launches of one backward step on the bf16, d = 128, chunk 64 shape
+BWD_KERNELS = ("backward: decay_kernel + bwd_tiles_mma_kernel + bwd_passes_vc_kernel + "
+               "bwd_chunk_mma_kernel")
+_COMMON = [CSRC + "gdr_fused_common.cuh", CSRC + "gdr_sm100.cuh"]
+
+
+def path_kernels(path):
+    """(kernel name as ncu lists it, source files, launches per call) of a prefill path."""
+    return {
+        1: ("staged: decay_kernel + wy_kernel + state_kernel + output_kernel",
+            [CSRC + "gdr_staged.cu"], 4),
+        2: ("fused_prefill_kernel", [CSRC + "gdr_fused.cu"] + _COMMON, 1),
+        3: ("fused_pair_kernel", [CSRC + "gdr_fused_pair.cu"] + _COMMON, 1),
+        # the two-kernel step is timed as one unit (its two launches back to back)
+        4: ("chunk_prep_kernel + chain_kernel<64>",
+            [CSRC + "gdr_prep.cu", CSRC + "gdr_chain.cu"] + _COMMON, 2),
+        5: ("chunk_prep_kernel + chain_kernel<128>",
+            [CSRC + "gdr_prep.cu", CSRC + "gdr_chain.cu"] + _COMMON, 2),
+        6: ("onepass_kernel", [CSRC + "gdr_onepass.cu"], 1),
+        # sequence segments: preparation, the segment maps, the scan, every segment's chain
+        7: ("chunk_prep_kernel + seg_pass1_kernel + seg_scan_kernel + chain_kernel",
+            [CSRC + "gdr_prep.cu", CSRC + "gdr_segment.cu", CSRC + "gdr_chain.cu"] + _COMMON, 4),
+    }[path]
+
+
 def bench_decode(gdr, w, K, W, dev, flush, stream):
     state = I.decode_state(w, device=dev)
     nsteps = max(K, 1)
@@ -371,16 +444,18 @@ def cpu_baseline_backward(w, budget_s=8.0):
                       f"({w.H * Ts} head-tokens in {dt:.2f} s); value = head-tokens/s / H"}
 
 
-def cpu_baseline_prefill(w, budget_s=12.0):
+def cpu_baseline_prefill(w, budget_s=12.0, x=None):
     """fp64 oracle on a bounded sample of the prefill workload: all heads of
-    sequence 0 over the first T_s tokens, T_s grown until ~budget_s of work."""
+    sequence 0 over the first T_s tokens, T_s grown until ~budget_s of work.  x: the
+    workload's inputs already drawn (on any device; the sample is sliced and copied)."""
     import oracle
-    x = I.prefill_inputs(w.with_(B=1), device="cpu")
+    if x is None:
+        x = I.prefill_inputs(w.with_(B=1), device="cpu")
     cores = os.cpu_count() or 1
     Ts = 128
     while True:
-        sub = {n: x[n][:, :, :Ts] for n in ("q", "k", "v", "g", "beta")}
-        init = x["init_state"]
+        sub = {n: x[n][:1, :, :Ts].cpu().contiguous() for n in ("q", "k", "v", "g", "beta")}
+        init = None if x["init_state"] is None else x["init_state"][:1].cpu()
         t0 = time.perf_counter()
         oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], w.a_min, init,
                    nthreads=cores)
@@ -505,6 +580,15 @@ def run_ours(args):
         if main_w is I.PREFILL and not args.no_backward:
             bwd = bench_backward(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
             barrier()
+        legs = {}
+        if main_w is I.PREFILL and not args.no_long:
+            for key, lw, k in (("long", I.LONG_PREFILL, max(3, args.steps // 2)),
+                               ("million", I.MILLION_PREFILL, max(3, args.steps // 4))):
+                legs[key] = bench_prefill_leg(gdr, lw, k, 3, dev, stream)
+                barrier()
+                if not (rank == 0 and world == 1 and not args.no_cpu_baseline):
+                    legs[key] = (legs[key][0], None)   # the inputs are not needed any more
+                torch.cuda.empty_cache()
     assert gdr.last_device_error(dev) == 0, "device error word set"
 
     ms_step = max_over_ranks(statistics.mean(ms))
@@ -523,20 +607,7 @@ def run_ours(args):
                                   main_w.chunk, main_w.a_min, main_w.torch_dtype(),
                                   workspace=not args.single_launch)
         assert not varlen or path in (2, 3, 4, 5), "the packed call runs the fused or two-kernel path"
-        csrc = "gated_delta_rule_gdr_gb300/csrc/"
-        common = [csrc + "gdr_fused_common.cuh", csrc + "gdr_sm100.cuh"]
-        kname, srcs = {
-            1: ("gdr_chunk_fwd staged (4 kernels)", [csrc + "gdr_staged.cu"]),
-            2: ("fused_prefill_kernel", [csrc + "gdr_fused.cu"] + common),
-            3: ("fused_pair_kernel", [csrc + "gdr_fused_pair.cu"] + common),
-            # the two-kernel step is timed as one unit (its two launches back to back)
-            4: ("chunk_prep_kernel + chain_kernel<64>",
-                [csrc + "gdr_prep.cu", csrc + "gdr_chain.cu"] + common),
-            5: ("chunk_prep_kernel + chain_kernel<128>",
-                [csrc + "gdr_prep.cu", csrc + "gdr_chain.cu"] + common),
-        }[path]
-        if path in (4, 5):
-            nk = 2
+        kname, srcs, nk = path_kernels(path)
         metric = "packed prefill tokens/s" if varlen else "prefill tokens/s"
     else:
         tokens = main_w.B
@@ -556,7 +627,7 @@ def run_ours(args):
         "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
         "peak_kind": pk_kind,
         "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-        "frac": None, "traffic": committed_traffic(kname, srcs),
+        "frac": None, "traffic": committed_traffic(kname, srcs, main_w.name),
         "algorithmic_bytes": by, "algorithmic_flops": fl,
         "frac_of_roofline_time": round(t_roof / (statistics.mean(ms) * 1e-3), 4),
         "achieved_tflops": round(achieved_tf, 2),
@@ -598,8 +669,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": "decode128_kernel", "achieved": round(dgbs, 1),
                          "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
                          "frac": round(dgbs / pk["hbm_gbs"], 4),
-                         "traffic": committed_traffic(
-                             "decode128_kernel", ["gated_delta_rule_gdr_gb300/csrc/gdr_decode.cu"]),
+                         "traffic": committed_traffic("decode128_kernel", [CSRC + "gdr_decode.cu"]),
                          "algorithmic_bytes": dby, "nominal_hbm_frac": round(dgbs / 7900.0, 4)},
             "e2e": {"value": round(world * w4.B / (max_over_ranks(statistics.mean(dms_e2e)) * 1e-3), 1),
                     "unit": "tokens/s", "h2d_bytes_per_step": dh2d, "d2h_bytes_per_step": dd2h},
@@ -614,12 +684,18 @@ def run_ours(args):
             "metric": "backward tokens/s", "workload": main_w.name,
             "value": round(world * main_w.B * main_w.T / (max_over_ranks(bmean) * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(bmean, 4), "steps": len(bms),
-            "roofline": {"bound": "hbm", "kernel": "whole step: bwd_tiles_mma + bwd_fwd_state_mma + "
-                         "bwd_chain_mma + bwd_chunk_mma", "achieved": round(bgbs, 1), "peak": pk["hbm_gbs"],
-                         "peak_kind": pk_kind, "unit": "GB/s", "frac": round(bgbs / pk["hbm_gbs"], 4),
-                         "traffic": None, "algorithmic_bytes": bby},
-            "workspace_bytes": bws, "gpu_launches": 5 * len(bms),
+            "roofline": {"bound": "hbm", "kernel": BWD_KERNELS, "achieved": round(bgbs, 1),
+                         "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
+                         "frac": round(bgbs / pk["hbm_gbs"], 4),
+                         "traffic": committed_traffic(BWD_KERNELS, [CSRC + "gdr_bwd.cu",
+                                                                    CSRC + "gdr_staged.cu"],
+                                                      main_w.name),
+                         "algorithmic_bytes": bby},
+            "workspace_bytes": bws, "gpu_launches": 4 * len(bms),
         }
+    for key, (lms, _) in legs.items():
+        line[key] = prefill_leg_line(gdr, {"long": I.LONG_PREFILL, "million": I.MILLION_PREFILL}[key],
+                                     lms, pk, pk_kind, world, max_over_ranks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = (cpu_baseline_varlen(main_w) if varlen
                                 else cpu_baseline_prefill(main_w) if main_w.steps == 0
@@ -628,6 +704,10 @@ def run_ours(args):
             line["decode"]["cpu_baseline"] = cpu_baseline_decode(I.DECODE)
         if bwd is not None:
             line["backward"]["cpu_baseline"] = cpu_baseline_backward(main_w)
+        for key, (_, lx) in legs.items():
+            lw = {"long": I.LONG_PREFILL, "million": I.MILLION_PREFILL}[key]
+            line[key]["cpu_baseline"] = cpu_baseline_prefill(lw, budget_s=6.0, x=lx)
+            legs[key] = None
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -712,6 +792,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long (B1 H32 T65536) and million-token (B1 H16 T1048576) legs")
     ap.add_argument("--single-launch", action="store_true",
                     help="the one-launch fused path (no workspace) instead of prep + chain")
     args = ap.parse_args()

@@ -16,6 +16,7 @@ single-launch path, a uint8 CUDA tensor supplies the workspace.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -26,12 +27,15 @@ from . import build as _build
 __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk_wy",
            "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "chunk_fwd_varlen",
            "chunk_fwd_workspace_size", "chunk_fwd_varlen_workspace_size", "last_device_error",
-           "status_string", "version", "library_path", "STATUS", "PATHS"]
+           "status_string", "version", "library_path", "STATUS", "PATHS", "OPTIONS",
+           "set_option", "get_option", "option"]
 
 DECAY = {"affine": 0, "log": 1}   # gdr_decay_t
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
           4: "GDR_ERR_CUDA", 5: "GDR_ERR_TIMEOUT"}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+# gdr_option_t
+OPTIONS = {"wait_limit_ns": 0, "fused_variant": 1, "chain_split": 2, "segments": 3}
 
 _lib = None
 
@@ -73,6 +77,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_bwd": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                           i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
+        "gdr_chunk_fwd_static": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
         "gdr_chunk_decay": [vp, f, vp, i, i, i, vp],
         "gdr_chunk_wy": [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
@@ -83,6 +88,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_fwd_path": [i, i, i, i, i, i, f, i],
         "gdr_status_string": [i],
         "gdr_version": [],
+        "gdr_set_option": [i, ctypes.c_int64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -93,6 +99,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [i, i, i, i, i, i, i]
         fn.restype = sz
+    lib.gdr_get_option.argtypes = [i]
+    lib.gdr_get_option.restype = ctypes.c_int64
     lib.gdr_status_string.restype = ctypes.c_char_p
     lib.gdr_version.restype = ctypes.c_char_p
     _lib = lib
@@ -105,6 +113,31 @@ def status_string(code: int) -> str:
 
 def version() -> str:
     return load().gdr_version().decode()
+
+
+def set_option(name: str, value: int) -> None:
+    """Set a process-wide option of the library (gdr_set_option): "wait_limit_ns"
+    (0 = every device-side wait gives up at once), "fused_variant" (0 auto, 1 one CTA
+    per head, 2 cluster pair), "chain_split" (0 auto, 1, 2), "segments" (0 auto, else
+    the sequence segments of the two-kernel path)."""
+    _check(load().gdr_set_option(OPTIONS[name], int(value)), "gdr_set_option")
+
+
+def get_option(name: str) -> int:
+    return int(load().gdr_get_option(OPTIONS[name]))
+
+
+@contextlib.contextmanager
+def option(**values):
+    """Set options for the duration of a with-block, then restore them."""
+    old = {n: get_option(n) for n in values}
+    try:
+        for n, val in values.items():
+            set_option(n, val)
+        yield
+    finally:
+        for n, val in old.items():
+            set_option(n, val)
 
 
 def _ptr(t):
@@ -388,8 +421,10 @@ def chunk_fwd_kernels(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat1
     return int(load().gdr_chunk_fwd_kernels(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
 
 
-PATHS = {0: "none", 1: "staged", 2: "fused one CTA per head", 3: "fused two-CTA cluster per head",
-         4: "prep + chain, two CTAs per head", 5: "prep + chain, one CTA per head"}
+PATHS = {0: "none", 1: "staged (on the workspace)", 2: "fused one CTA per head",
+         3: "fused two-CTA cluster per head", 4: "prep + chain, two CTAs per head",
+         5: "prep + chain, one CTA per head", 6: "one-pass CUDA-core kernel",
+         7: "prep + segment maps + scan + chain over sequence segments"}
 
 
 def chunk_fwd_path(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16,

@@ -5,6 +5,7 @@
 #include "gdr.h"
 #include "gdr_internal.h"
 
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -47,9 +48,55 @@ gdr_status_t check_staged(int BH, int T, int dk, int dv, int chunk) {
     return GDR_OK;
 }
 
+// Process-wide options (gdr_set_option).  Relaxed atomics: a value set before a
+// call is seen by that call's launches on any thread.
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_fused_variant{0};
+std::atomic<int> g_chain_split{0};
+std::atomic<int> g_segments{0};
+
 }  // namespace
 
+namespace gdr {
+uint64_t opt_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int opt_fused_variant() { return g_fused_variant.load(std::memory_order_relaxed); }
+int opt_chain_split() { return g_chain_split.load(std::memory_order_relaxed); }
+int opt_segments() { return g_segments.load(std::memory_order_relaxed); }
+}  // namespace gdr
+
 extern "C" {
+
+gdr_status_t gdr_set_option(gdr_option_t option, int64_t value) {
+    switch (option) {
+        case GDR_OPT_WAIT_LIMIT_NS:
+            if (value < 0) return GDR_ERR_INVALID_ARG;
+            g_wait_limit_ns.store((uint64_t)value, std::memory_order_relaxed);
+            return GDR_OK;
+        case GDR_OPT_FUSED_VARIANT:
+            if (value < 0 || value > 2) return GDR_ERR_INVALID_ARG;
+            g_fused_variant.store((int)value, std::memory_order_relaxed);
+            return GDR_OK;
+        case GDR_OPT_CHAIN_SPLIT:
+            if (value < 0 || value > 2) return GDR_ERR_INVALID_ARG;
+            g_chain_split.store((int)value, std::memory_order_relaxed);
+            return GDR_OK;
+        case GDR_OPT_SEGMENTS:
+            if (value < 0 || value > 4096) return GDR_ERR_INVALID_ARG;
+            g_segments.store((int)value, std::memory_order_relaxed);
+            return GDR_OK;
+    }
+    return GDR_ERR_INVALID_ARG;
+}
+
+int64_t gdr_get_option(gdr_option_t option) {
+    switch (option) {
+        case GDR_OPT_WAIT_LIMIT_NS: return (int64_t)gdr::opt_wait_limit_ns();
+        case GDR_OPT_FUSED_VARIANT: return gdr::opt_fused_variant();
+        case GDR_OPT_CHAIN_SPLIT: return gdr::opt_chain_split();
+        case GDR_OPT_SEGMENTS: return gdr::opt_segments();
+    }
+    return -1;
+}
 
 }  // extern "C"
 
@@ -84,34 +131,9 @@ gdr_status_t chunk_fwd_impl(const void *q, const void *k, const void *v, const f
     if (gdr::fused_supported(dk, dv, chunk, e))
         return from_cuda(gdr::launch_fused(q, k, v, g, beta, a_min, init_state, out,
                                            final_state, B, H, T, dk, dv, chunk, s));
-
-    // Staged path on stream-ordered scratch.
-    const int NC = (T + chunk - 1) / chunk;
-    const size_t n_tok = (size_t)BH * (size_t)T;
-    const size_t bytes = sizeof(float) * (n_tok                       // gamma
-                                          + n_tok * (size_t)dv        // U
-                                          + n_tok * (size_t)dk        // Wk
-                                          + n_tok * (size_t)dv        // W
-                                          + (size_t)BH * NC * (size_t)dk * dv);  // Mn
-    void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return GDR_ERR_CUDA;
-    float *gamma = static_cast<float *>(scratch);
-    float *U = gamma + n_tok;
-    float *Wk = U + n_tok * dv;
-    float *W = Wk + n_tok * dk;
-    float *Mn = W + n_tok * dv;
-    const int bh = (int)BH;
-    cudaError_t err = gdr::launch_decay(g, a_min, gamma, bh, T, chunk, s);
-    if (err == cudaSuccess)
-        err = gdr::launch_wy(k, v, beta, gamma, U, Wk, bh, T, dk, dv, chunk, e, s);
-    if (err == cudaSuccess)
-        err = gdr::launch_state(k, gamma, U, Wk, init_state, W, Mn, final_state, bh, T, dk, dv,
-                                chunk, e, s);
-    if (err == cudaSuccess)
-        err = gdr::launch_output(q, k, gamma, Mn, W, out, bh, T, dk, dv, chunk, e, s);
-    const cudaError_t ferr = cudaFreeAsync(scratch, s);
-    if (err == cudaSuccess) err = ferr;
-    return from_cuda(err);
+    // every other shape and fp32: one CUDA-core launch, no scratch
+    return from_cuda(gdr::launch_onepass(q, k, v, g, beta, a_min, init_state, out, final_state,
+                                         (int)BH, T, dk, dv, chunk, e, s));
 }
 
 gdr_status_t decode_impl(const void *q, const void *k, const void *v, const float *g,
@@ -243,10 +265,13 @@ gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
 size_t gdr_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
                                     gdr_dtype_t dtype) {
     if (B < 0 || H < 0 || T < 0 || !dtype_ok(dtype)) return 0;
-    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return 0;
+    if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return 0;
     const int64_t BH = (int64_t)B * H;
-    if (BH == 0 || BH > 0x7fffffff || T == 0) return 0;
-    return gdr::prep_workspace_bytes((int)BH, T, nullptr, 0, 0);
+    if (BH == 0 || BH > 0x7fffffff || T == 0 || (int64_t)T * BH > ((int64_t)1 << 40)) return 0;
+    if (gdr::fused_supported(dk, dv, chunk, elem_of(dtype)))   // tiles, then segment maps
+        return gdr::prep_workspace_bytes((int)BH, T, nullptr, 0, 0) +
+               gdr::segment_workspace_bytes((int)BH, gdr::segment_count((int)BH, T));
+    return gdr::staged_scratch_bytes(BH, T, dk, dv, chunk);   // the staged kernels' scratch
 }
 
 size_t gdr_chunk_fwd_varlen_workspace_size(int S, int H, int total_T, int dk, int dv, int chunk,
@@ -270,18 +295,40 @@ gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, cons
                                gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
                                void *stream) {
     const size_t need = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype);
-    if (need == 0 || workspace == nullptr || workspace_bytes < need)
+    if (need == 0 || workspace == nullptr || workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15))
         return chunk_fwd_impl(q, k, v, g, beta, a_min, init_state, out, final_state, B, H, T, dk,
                               dv, chunk, dtype, stream);
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) {
+        // the four staged kernels (parallel WY/UT and output steps) on the workspace
+        if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
+        if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
+        return from_cuda(gdr::launch_staged(q, k, v, g, beta, a_min, init_state, out, final_state,
+                                            workspace, B * H, T, dk, dv, chunk, elem_of(dtype),
+                                            static_cast<cudaStream_t>(stream)));
+    }
     if (!range_ok(a_min, kTile)) return GDR_ERR_RANGE;
     if ((int64_t)T * B * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int BH = B * H;
+    const int S = gdr::segment_count(BH, T);
     cudaError_t e = gdr::launch_prep(q, k, g, beta, a_min, workspace, BH, T, nullptr, 0, 0, s);
+    if (S <= 1) {
+        if (e == cudaSuccess)
+            e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace,
+                                  BH, T, nullptr, 0, 0, s);
+        return from_cuda(e);
+    }
+    // sequence segments: their maps and the scan, then every segment's chain at once
+    float *seg_ws = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                              gdr::prep_workspace_bytes(BH, T, nullptr, 0, 0));
+    if (e == cudaSuccess)
+        e = gdr::launch_segment_states(k, v, g, beta, a_min, init_state, workspace, seg_ws, BH, T,
+                                       S, s);
     if (e == cudaSuccess)
         e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace, BH,
-                              T, nullptr, 0, 0, s);
+                              T, nullptr, 0, 0, s, S, gdr::segment_states(seg_ws, BH, S));
     return from_cuda(e);
 }
 
@@ -337,9 +384,15 @@ gdr_status_t gdr_chunk_fwd_varlen_ws(const void *q, const void *k, const void *v
 
 int gdr_chunk_fwd_ws_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
                           gdr_dtype_t dtype) {
-    if (gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) > 0 && a_min_ok(a_min) &&
-        range_ok(a_min, kTile))
-        return gdr::chain_split(B * H) == 2 ? 4 : 5;
+    if (gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) > 0 && a_min_ok(a_min)) {
+        if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype)))
+            return range_ok(a_min, chunk) ? 1 : -1;
+        if (range_ok(a_min, kTile)) {
+            const int S = gdr::segment_count(B * H, T);
+            if (S > 1) return 7;
+            return gdr::chain_split(B * H) == 2 ? 4 : 5;
+        }
+    }
     return gdr_chunk_fwd_path(B, H, T, dk, dv, chunk, a_min, dtype);
 }
 
@@ -349,16 +402,16 @@ int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float 
     if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk) || !range_ok(a_min, chunk)) return -1;
     if ((int64_t)B * H == 0) return 0;
     if (T == 0) return 0;  // a copy or memset, no kernel
-    return gdr::fused_supported(dk, dv, chunk, elem_of(dtype)) ? 1 : 4;
+    return 1;              // the fused tensor-core kernel or the one-pass CUDA-core kernel
 }
 
 int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
                        gdr_dtype_t dtype) {
     const int n = gdr_chunk_fwd_kernels(B, H, T, dk, dv, chunk, a_min, dtype);
     if (n <= 0) return n;
-    if (n == 4) return 1;
     const int64_t BH = (int64_t)B * H;
     if (BH > 0x7fffffff) return -1;
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return 6;
     return gdr::fused_uses_pair((int)BH) ? 3 : 2;
 }
 
@@ -410,7 +463,7 @@ gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, con
         return GDR_ERR_INVALID_ARG;
     if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_INVALID_ARG;
     // the chunk's range rule of whichever path the call takes, before anything is enqueued
-    const bool two = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype) > 0;
+    const bool two = gdr::fused_supported(dk, dv, chunk, elem_of(dtype));
     if (!range_ok(a_min, two ? kTile : chunk)) return GDR_ERR_RANGE;
     size_t off[9];
     host_layout(B, H, T, dk, dv, chunk, dtype, off);

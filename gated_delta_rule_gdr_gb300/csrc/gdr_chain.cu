@@ -229,8 +229,12 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const uint32_t st_r = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
         const uint32_t st_c = (uint32_t)(lane >> 4);
         float s[16][4];   // S_J: rows jw + g (+ 8), columns i = 8 q + 2 t4 (+ 1)
+        float *const fin_view = view_final(a, bh);
         {
-            const float *src = a.init ? a.init + (int64_t)bh * D * D + j0 + jw : nullptr;
+            // a segment's initial state comes from the scan kernel just before this one
+            if (a.nseg > 1) grid_dependency_wait();
+            const float *v0 = view_init(a, bh);
+            const float *src = v0 ? v0 + j0 + jw : nullptr;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
                 const int i = 8 * q + 2 * t4;
@@ -241,7 +245,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
         }
         auto store_state = [&]() {   // S_J^T into the fp32 [dk][dv] final state
-            float *fin = a.final_state + (int64_t)bh * D * D + j0 + jw;
+            float *fin = fin_view + j0 + jw;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
                 const int i = 8 * q + 2 * t4;
@@ -285,7 +289,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                &s_abort);
             return __all_sync(0xffffffffu, ok);
         };
-        if (NC == 0 && a.final_state) store_state();   // an empty sequence: final = initial
+        if (NC == 0 && fin_view) store_state();   // an empty sequence: final = initial
         if (NC > 0) publish(0);
 
         for (int n = 0; n < NC; ++n) {
@@ -467,7 +471,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // a single MS buffer is free once the output's [K;Q] MS_n has completed
             if (Cfg::MSB == 1 && n + 1 < NC && !warp_wait(B_QMS, (uint32_t)n & 1u)) break;
             publish(n + 1);   // MS_{n+1} (if any) and W_n
-            if (n + 1 == NC && a.final_state) store_state();
+            if (n + 1 == NC && fin_view) store_state();
         }
     } else if (warp == NCH + 1) {
         // ================================================================ output products
@@ -671,12 +675,11 @@ cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
 }  // namespace
 
 // Value columns per CTA: two CTAs per head while every CTA has an SM of its
-// own, one CTA per head beyond that.  GDR_CHAIN_SPLIT=1|2 overrides it (the
-// tests cover both on small shapes).
+// own, one CTA per head beyond that.  The GDR_OPT_CHAIN_SPLIT option forces
+// one (the tests cover both on small shapes).
 int chain_split(int BH) {
-    const char *env = std::getenv("GDR_CHAIN_SPLIT");
-    if (env && std::strcmp(env, "1") == 0) return 1;
-    if (env && std::strcmp(env, "2") == 0) return 2;
+    const int forced = opt_chain_split();
+    if (forced == 1 || forced == 2) return forced;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -688,7 +691,8 @@ int chain_split(int BH) {
 
 cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
-                         int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s) {
+                         int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
+                         int nseg, const float *seg_init) {
     if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;   // callers copy the state
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
          reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(ws)) & 15)
@@ -705,8 +709,14 @@ cudaError_t launch_chain(const void *q, const void *k, const void *v, const floa
     a.H = H;
     a.total_T = total_T;
     const int64_t nslot = tile_slots(a, BH);
-    return chain_split(BH) == 2 ? launch_chain_t<64>(mq, mk, mv, mo, a, ws, nslot, BH, s)
-                                : launch_chain_t<128>(mq, mk, mv, mo, a, ws, nslot, BH, s);
+    if (!cu_seqlens && nseg > 1) {   // one view per (head, segment)
+        a.nseg = nseg;
+        a.seg_chunks = segment_chunks(T, nseg);
+        a.seg_init = seg_init;
+    }
+    const int views = BH * a.nseg;
+    return chain_split(views) == 2 ? launch_chain_t<64>(mq, mk, mv, mo, a, ws, nslot, views, s)
+                                   : launch_chain_t<128>(mq, mk, mv, mo, a, ws, nslot, views, s);
 }
 
 cudaError_t take_chain_error_word(unsigned *value) { return take_error_word(value); }

@@ -584,12 +584,12 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
 // A cluster of two CTAs per head while every head's cluster is resident at
 // once; one CTA per head beyond that, where every SM already has a head.
-// GDR_FUSED_VARIANT=single|pair overrides the choice (used by the tests to
-// cover both kernels on small shapes).
+// The GDR_OPT_FUSED_VARIANT option forces one (the tests cover both kernels
+// on small shapes).
 bool use_pair(int BH) {
-    const char *env = std::getenv("GDR_FUSED_VARIANT");
-    if (env && std::strcmp(env, "single") == 0) return false;
-    if (env && std::strcmp(env, "pair") == 0) return true;
+    const int forced = opt_fused_variant();
+    if (forced == 1) return false;
+    if (forced == 2) return true;
     return BH <= fused_pair_max_clusters();
 }
 
@@ -631,12 +631,13 @@ cudaError_t launch_fused(const void *q, const void *k, const void *v, const floa
 cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;
-    unsigned a = 0, b = 0, c = 0, d = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0, f = 0;
     e = take_error_word(&a);
     if (e == cudaSuccess) e = take_pair_error_word(&b);
     if (e == cudaSuccess) e = take_prep_error_word(&c);
     if (e == cudaSuccess) e = take_chain_error_word(&d);
-    *value = a | b | c | d;
+    if (e == cudaSuccess) e = take_segment_error_word(&f);
+    *value = a | b | c | d | f;
     return e;
 }
 

@@ -371,6 +371,12 @@ struct FusedArgs {
     // state index is s H + h.  nullptr = the dense [B][H][T] layout.
     const int *cu_seqlens = nullptr;
     int H = 0, total_T = 0;
+    // Sequence segments of the dense layout (nseg > 1, the two-kernel path only):
+    // view v = bh nseg + s covers chunks s seg_chunks .. of head bh, starts from
+    // seg_init[v] ([dk][dv] fp32, written by the segment scan) and, for the last
+    // segment only, writes the head's final state.
+    int nseg = 1, seg_chunks = 0;
+    const float *seg_init = nullptr;
 };
 
 // Where the tokens of the (sequence, head) with state index bh live.  Token t
@@ -382,7 +388,15 @@ struct SeqView {
 };
 __device__ __forceinline__ SeqView seq_view(const FusedArgs &a, int bh) {
     SeqView v;
-    if (!a.cu_seqlens) {
+    if (!a.cu_seqlens && a.nseg > 1) {   // segment bh % nseg of head bh / nseg
+        const int h = bh / a.nseg, sg = bh % a.nseg;
+        const int t0 = sg * a.seg_chunks * C;
+        v.T = max(0, min(a.seg_chunks * C, a.T - t0));
+        v.tz = t0;
+        v.z = h;
+        v.stride = 1;
+        v.gbase = (int64_t)h * a.T + t0;
+    } else if (!a.cu_seqlens) {
         v.T = a.T;
         v.tz = 0;
         v.z = bh;
@@ -417,7 +431,20 @@ __host__ __device__ __forceinline__ int64_t tile_slots(const FusedArgs &a, int B
     return a.cu_seqlens ? (int64_t)(a.total_T / C + BH / a.H + 1) : (int64_t)((a.T + C - 1) / C);
 }
 __device__ __forceinline__ int tile_slot0(const FusedArgs &a, int bh, const SeqView &v) {
-    return a.cu_seqlens ? v.tz / C + bh / a.H : 0;
+    return a.cu_seqlens ? v.tz / C + bh / a.H : v.tz / C;
+}
+// Initial state of view bh ([dk][dv] fp32, or nullptr = zeros) and its final state
+// (nullptr = not written).  Segment views start from the scan's states and only the
+// last segment of a head writes the final state.
+__device__ __forceinline__ const float *view_init(const FusedArgs &a, int bh) {
+    if (a.nseg > 1) return a.seg_init + (int64_t)bh * D * D;
+    return a.init ? a.init + (int64_t)bh * D * D : nullptr;
+}
+__device__ __forceinline__ float *view_final(const FusedArgs &a, int bh) {
+    if (!a.final_state) return nullptr;
+    if (a.nseg > 1)
+        return bh % a.nseg == a.nseg - 1 ? a.final_state + (int64_t)(bh / a.nseg) * D * D : nullptr;
+    return a.final_state + (int64_t)bh * D * D;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -461,13 +488,10 @@ bool make_map_packed(CUtensorMap *m, const void *ptr, int H, int total_T) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-uint64_t wait_limit_ns() {
-    // Test hook: GDR_FAULT_INJECT=timeout makes every bounded wait give up at
-    // once, exercising the error path without any GPU fault.
-    const char *e = std::getenv("GDR_FAULT_INJECT");
-    if (e && std::strcmp(e, "timeout") == 0) return 0;
-    return 2000000000ull;   // 2 s
-}
+// Bound of every device-side wait: 2 s unless gdr_set_option changed it (0
+// makes every wait give up at once, which drives the error path in tests
+// without any GPU fault).
+uint64_t wait_limit_ns() { return opt_wait_limit_ns(); }
 
 // Reads and clears this translation unit's device error word (synchronous).
 cudaError_t take_error_word(unsigned *value) {

@@ -26,6 +26,35 @@ cudaError_t launch_output(const void *q, const void *k, const float *gamma, cons
                           Elem e, cudaStream_t s);
 // final_state <- init (or zeros) for T == 0.
 cudaError_t launch_copy_state(const float *init, float *final_state, int64_t n, cudaStream_t s);
+// Bytes of fp32 intermediates the four staged steps need for one prefill:
+// gamma, U, Wk, W per token-head and the state at every chunk start.
+size_t staged_scratch_bytes(int64_t BH, int T, int dk, int dv, int C);
+// The whole prefill as the four staged steps on caller-provided scratch of at
+// least staged_scratch_bytes (16-byte aligned); every value in it is written
+// before it is read.
+cudaError_t launch_staged(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float d, const float *init, void *out,
+                          float *final_state, void *scratch, int BH, int T, int dk, int dv,
+                          int C, Elem e, cudaStream_t s);
+
+// ---- the prefill in one CUDA-core launch with no scratch (gdr_onepass.cu):
+// fp32, and every shape the tensor-core kernels do not take ----
+cudaError_t launch_onepass(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float d, const float *init, void *out,
+                           float *final_state, int BH, int T, int dk, int dv, int C, Elem e,
+                           cudaStream_t s);
+
+// ---- process-wide options (gdr_set_option in gdr_api.cu) ----
+// Bound of every device-side wait in ns (0: every wait gives up at once, the
+// fault-injection setting of the tests).
+uint64_t opt_wait_limit_ns();
+// Single-launch fused kernel: 0 by head count, 1 one CTA per head, 2 cluster pair.
+int opt_fused_variant();
+// CTAs per head of the chain kernel: 0 by head count, else 1 or 2.
+int opt_chain_split();
+// Sequence segments of the two-kernel path: 0 by head count, else that many (at
+// most the sequence's chunk count).
+int opt_segments();
 
 // ---- backward of the chunked form (gdr_bwd.cu) ----
 bool bwd_supported(int dk, int dv, int C);
@@ -77,11 +106,33 @@ size_t prep_workspace_bytes(int BH, int T, const int *cu_seqlens, int H, int tot
 cudaError_t launch_prep(const void *q, const void *k, const float *g, const float *beta, float a_min,
                         void *ws, int BH, int T, const int *cu_seqlens, int H, int total_T,
                         cudaStream_t s);
+// nseg > 1 (dense only): the chain of every segment of every head at once, each
+// from its state in seg_init ([BH][nseg][dk][dv], from launch_segment_states).
 cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
-                         int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s);
-// CTAs per head of the chain kernel for BH heads on the current device (2 or 1).
+                         int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
+                         int nseg = 1, const float *seg_init = nullptr);
+// CTAs per view of the chain kernel for BH views on the current device (2 or 1).
 int chain_split(int BH);
+
+// ---- sequence segments of the two-kernel path (gdr_segment.cu) ----
+// Segments per head for BH heads of T tokens on the current device (1 = none).
+int segment_count(int BH, int T);
+// Chunks per segment (the last segment may have fewer).
+int segment_chunks(int T, int S);
+// Workspace bytes of the segment maps and states (0 for S <= 1).
+size_t segment_workspace_bytes(int BH, int S);
+// Pass 1 (each segment's offset map Delta and transition Phi, every segment at once)
+// and the scan over segments, writing every segment's initial state into the last
+// part of seg_ws ([BH][S][dk][dv]); ws_tiles holds the preparation's tiles.
+cudaError_t launch_segment_states(const void *k, const void *v, const float *g, const float *beta,
+                                  float a_min, const float *init, const void *ws_tiles,
+                                  float *seg_ws, int BH, int T, int S, cudaStream_t s);
+// The segment states of seg_ws (its last BH S dk dv floats).
+inline float *segment_states(float *seg_ws, int BH, int S) {
+    return seg_ws + (size_t)2 * BH * (S - 1) * 128 * 128;
+}
+cudaError_t take_segment_error_word(unsigned *value);
 // Read and clear the device error words of the two kernels (synchronous).
 cudaError_t take_prep_error_word(unsigned *value);
 cudaError_t take_chain_error_word(unsigned *value);

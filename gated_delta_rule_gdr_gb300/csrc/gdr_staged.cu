@@ -372,6 +372,31 @@ cudaError_t launch_output(const void *q, const void *k, const float *gamma, cons
     return cudaGetLastError();
 }
 
+size_t staged_scratch_bytes(int64_t BH, int T, int dk, int dv, int C) {
+    const int64_t NC = ((int64_t)T + C - 1) / C;
+    const int64_t n_tok = BH * (int64_t)T;
+    return sizeof(float) * (size_t)(n_tok * (1 + (int64_t)dv + dk + dv) + BH * NC * (int64_t)dk * dv);
+}
+
+cudaError_t launch_staged(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float d, const float *init, void *out,
+                          float *final_state, void *scratch, int BH, int T, int dk, int dv,
+                          int C, Elem e, cudaStream_t s) {
+    if (BH == 0 || T == 0) return cudaSuccess;
+    const size_t n_tok = (size_t)BH * (size_t)T;
+    float *gamma = static_cast<float *>(scratch);   // [BH][T]
+    float *U = gamma + n_tok;                      // [BH][T][dv]
+    float *Wk = U + n_tok * dv;                    // [BH][T][dk]
+    float *W = Wk + n_tok * dk;                    // [BH][T][dv]
+    float *Mn = W + n_tok * dv;                    // [BH][NC][dk][dv]
+    cudaError_t err = launch_decay(g, d, gamma, BH, T, C, s);
+    if (err == cudaSuccess) err = launch_wy(k, v, beta, gamma, U, Wk, BH, T, dk, dv, C, e, s);
+    if (err == cudaSuccess)
+        err = launch_state(k, gamma, U, Wk, init, W, Mn, final_state, BH, T, dk, dv, C, e, s);
+    if (err == cudaSuccess) err = launch_output(q, k, gamma, Mn, W, out, BH, T, dk, dv, C, e, s);
+    return err;
+}
+
 cudaError_t launch_copy_state(const float *init, float *final_state, int64_t n, cudaStream_t s) {
     if (!final_state || n == 0) return cudaSuccess;
     if (init == final_state) return cudaSuccess;

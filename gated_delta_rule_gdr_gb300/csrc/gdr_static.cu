@@ -1,6 +1,6 @@
 // gdr_static.cu -- chunked prefill that allocates nothing: the staged kernels
 // (decay, WY/UT, state pass, output) run on a fixed scratch area that the
-// library owns, instead of on stream-ordered scratch from cudaMallocAsync.
+// library owns, instead of on scratch that the caller (or an allocator) provides.
 //
 // Who needs it: callers that must not allocate device memory while they run.
 // Examples are a plugin inside a host framework that owns every byte of
@@ -13,6 +13,8 @@
 #include "gdr.h"
 #include "gdr_internal.h"
 
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -22,29 +24,81 @@ namespace {
 // Fixed scratch: 32 MiB of device memory, held by every GPU that loads the
 // library until the process exits.  Host code must never pass the symbol
 // itself to a kernel (on the host it is only a stand-in, not a device
-// address); it resolves the device address once per device below.
+// address); it resolves the device address below.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
+// The array's device address is a property of the CUDA context the library's
+// module is loaded in: another context on the same device, or the primary
+// context re-created after cudaDeviceReset, loads the module again and may
+// place the array elsewhere.  So the address is cached per context, keyed by
+// the context's unique ID (cuCtxGetId: IDs are never reused within a process,
+// unlike context handles), and looked up once in each context.
+constexpr int kMaxContexts = 64;
+struct CtxAddr {
+    unsigned long long id;
+    void *addr;
+};
+CtxAddr g_cache[kMaxContexts];
+int g_cache_n = 0;
+std::mutex g_cache_mu;
 
-// Device address of the scratch array on the calling thread's current device,
-// looked up with that device current the first time and cached afterwards.
-cudaError_t scratch_on_current_device(void **addr) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = [] {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        cudaDriverEntryPointQueryResult q;
+        return (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                                 &q) == cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                   ? reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p)
+                   : nullptr;
+    }();
+    return fn;
+}
+PFN_cuCtxGetId_v12000 ctx_get_id() {
+    static PFN_cuCtxGetId_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault,
+                                                 &q) == cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                   ? reinterpret_cast<PFN_cuCtxGetId_v12000>(p)
+                   : nullptr;
+    }();
+    return fn;
+}
+
+// Unique ID of the calling thread's current context (making the device's
+// primary context current first if the thread has none yet).
+bool current_context_id(unsigned long long *id) {
+    auto get = ctx_get_current();
+    auto getid = ctx_get_id();
+    if (!get || !getid) return false;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return false;
+    if (ctx == nullptr) {
+        int dev = 0;   // no context yet: bind the current device's primary context
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+        if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
     }
-    *addr = g_scratch_addr[dev];
+    return getid(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the calling thread's current context.
+cudaError_t scratch_in_current_context(void **addr) {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return cudaErrorDeviceUninitialized;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    for (int i = 0; i < g_cache_n; ++i)
+        if (g_cache[i].id == id) {
+            *addr = g_cache[i].addr;
+            return cudaSuccess;
+        }
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    if (g_cache_n < kMaxContexts) g_cache[g_cache_n++] = {id, p};   // else look up every call
+    *addr = p;
     return cudaSuccess;
 }
 
@@ -65,17 +119,17 @@ extern "C" gdr_status_t gdr_chunk_fwd_static(const void *q, const void *k, const
     if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
     if ((double)chunk * -std::log((double)a_min) > 80.0) return GDR_ERR_RANGE;
     const int64_t BH = (int64_t)B * H;
-    if (BH > 0x7fffffff) return GDR_ERR_UNSUPPORTED;
-    const int64_t NC = ((int64_t)T + chunk - 1) / chunk;
-    const int64_t n_tok = BH * (int64_t)T;
-    // gamma, U, Wk, W per token-head and one state per chunk start, all fp32
-    const int64_t need = (int64_t)sizeof(float) *
-                         (n_tok * (1 + (int64_t)dv + dk + dv) + BH * NC * (int64_t)dk * dv);
-    if (need > (int64_t)kStaticScratchBytes) return GDR_ERR_UNSUPPORTED;
+    // Every token-head needs at least one fp32 value of scratch, so work with more
+    // token-heads than the array has floats cannot fit; rejecting it first also keeps
+    // the size formula below far from int64 overflow.
+    if (BH > 0x7fffffff || BH * (int64_t)T > (int64_t)(kStaticScratchBytes / sizeof(float)))
+        return GDR_ERR_UNSUPPORTED;
+    if (gdr::staged_scratch_bytes(BH, T, dk, dv, chunk) > kStaticScratchBytes)
+        return GDR_ERR_UNSUPPORTED;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *scratch = nullptr;
-    if (scratch_on_current_device(&scratch) != cudaSuccess) return GDR_ERR_CUDA;
+    if (scratch_in_current_context(&scratch) != cudaSuccess) return GDR_ERR_CUDA;
     if (BH == 0) return GDR_OK;
     if (T == 0) {
         if (final_state == nullptr) return GDR_OK;
@@ -88,19 +142,8 @@ extern "C" gdr_status_t gdr_chunk_fwd_static(const void *q, const void *k, const
     // Every intermediate is written before it is read, so nothing left over
     // from an earlier call needs clearing.
     const gdr::Elem e = dtype == GDR_DTYPE_F32 ? gdr::Elem::F32 : gdr::Elem::BF16;
-    float *gamma = static_cast<float *>(scratch);
-    float *U = gamma + n_tok;
-    float *Wk = U + n_tok * dv;
-    float *W = Wk + n_tok * dk;
-    float *Mn = W + n_tok * dv;
-    const int bh = (int)BH;
-    cudaError_t err = gdr::launch_decay(g, a_min, gamma, bh, T, chunk, s);
-    if (err == cudaSuccess)
-        err = gdr::launch_wy(k, v, beta, gamma, U, Wk, bh, T, dk, dv, chunk, e, s);
-    if (err == cudaSuccess)
-        err = gdr::launch_state(k, gamma, U, Wk, init_state, W, Mn, final_state, bh, T, dk, dv,
-                                chunk, e, s);
-    if (err == cudaSuccess)
-        err = gdr::launch_output(q, k, gamma, Mn, W, out, bh, T, dk, dv, chunk, e, s);
-    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    return gdr::launch_staged(q, k, v, g, beta, a_min, init_state, out, final_state, scratch,
+                              (int)BH, T, dk, dv, chunk, e, s) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
 }

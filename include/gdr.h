@@ -86,10 +86,11 @@ typedef enum {
  * Work: the chunked form of the recurrence (per chunk: cumulative decay, the
  * intra-chunk WY/UT transform, the inter-chunk state step and the output),
  * which equals the token recurrence in exact arithmetic.
- * bf16 with dk = dv = 128 and chunk = 64 runs one fused tensor-core kernel
- * and allocates nothing.  Other shapes and fp32 run the staged kernels (the
- * four gdr_chunk_* steps below) on stream-ordered scratch from the device's
- * default memory pool (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * One launch, and the library allocates nothing: bf16 with dk = dv = 128 and
+ * chunk = 64 runs a fused tensor-core kernel; fp32 and every other shape run
+ * one CUDA-core kernel (one CTA per head and block of 32 value columns, walking
+ * the chunks in order, every intermediate in shared memory).  With a
+ * caller-owned workspace, gdr_chunk_fwd_ws runs faster multi-kernel paths.
  * T == 0 copies init_state (or zeros) to final_state.
  */
 gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v,
@@ -100,20 +101,31 @@ gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v,
 
 /*
  * One token per sequence: N sequences x H heads, state updated in place.
+ * This is the inference step the fixed-size state exists for: the state does
+ * not grow with the context, so a token costs one read and one write of it
+ * however long the sequence already is ("Trillion-Parameter MoE Multimodal
+ * LLMs: How to Evaluate the New Generation", section 2.1; the incremental
+ * correct-on-write update of "How to Think About Trillion-Parameter Sparse
+ * Multimodal LLMs", section 2.2).
  *   q, k [N,H,dk] dtype; v [N,H,dv] dtype; g, beta [N,H] fp32;
- *   state [N,H,dk,dv] fp32 (in/out); out [N,H,dv] dtype.
+ *   state [N,H,dk,dv] fp32 (in/out, the M = S^T layout of the prefill's final
+ *   state); out [N,H,dv] dtype.
  * Work: p = S k and r = S q in one pass over the state, u = v - alpha p,
  * o = alpha r + beta (q.k) u, S <- alpha S + beta u k^T (the same recurrence
- * with T = 1).  state must not alias q, k, v or out.
+ * with T = 1).  state must not alias q, k, v or out.  One launch; allocates
+ * nothing.  Errors: N or H negative, a_min outside (0, 1] or a null pointer
+ * (N H > 0): GDR_ERR_INVALID_ARG; dk or dv outside {16, 32, 64, 128}:
+ * GDR_ERR_UNSUPPORTED.
  */
 gdr_status_t gdr_decode_step(const void *q, const void *k, const void *v,
                              const float *g, const float *beta, float a_min,
                              float *state, void *out, int N, int H, int dk, int dv,
                              gdr_dtype_t dtype, void *stream);
 
-/* ---- the staged steps of the chunked form (what gdr_chunk_fwd runs for fp32
- *      and for shapes the fused kernel does not cover), exposed so each step
- *      can be checked on its own.  BH = B * H; NC = ceil(T / chunk). ---- */
+/* ---- the staged steps of the chunked form (what gdr_chunk_fwd_ws runs, on
+ *      its workspace, for fp32 and for shapes the tensor-core kernels do not
+ *      cover), exposed so each step can be checked on its own.  BH = B * H;
+ *      NC = ceil(T / chunk). ---- */
 
 /*
  * Step 1, cumulative decay inside each chunk (the Gamma = exp(cumsum(log
@@ -175,9 +187,12 @@ gdr_status_t gdr_chunk_output(const void *q, const void *k, const float *gamma,
  *   - Size limit: 4 * (B*H*T*(1 + dk + 2*dv) + B*H*ceil(T/chunk)*dk*dv) bytes
  *     must not exceed 32 MiB (33554432); larger work returns
  *     GDR_ERR_UNSUPPORTED before anything is enqueued.
- *   - The first call on a device, with that device current on the calling
- *     thread, looks up the array's device address (cudaGetSymbolAddress) and
- *     caches it; make that first call before any stream capture.
+ *   - The array's device address depends on the CUDA context the library is
+ *     loaded in (another context on the device, or the primary context made
+ *     again after cudaDeviceReset, may place it elsewhere).  The first call in
+ *     each context, on a thread where that context is current, looks the
+ *     address up (cudaGetSymbolAddress) and caches it under the context's
+ *     unique ID; make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents
  *     (every value is rewritten before it is read, so nothing needs
  *     clearing).  Calls whose work overlaps on the GPU -- on different
@@ -225,13 +240,13 @@ int gdr_chunk_fwd_kernels(int B, int H, int T, int dk, int dv, int chunk, float 
 
 /*
  * Which code path one gdr_chunk_fwd call with these arguments takes on the
- * calling thread's current device: 0 no kernel (empty work), 1 the staged
- * kernels, 2 the fused kernel with one CTA per head, 3 the fused kernel with a
- * cluster of two CTAs per head (value columns split, chunk preparation
- * alternated between the two), or -1 if the call would be rejected.  The
- * choice between 2 and 3 depends on how many two-CTA clusters the device holds
- * at once (queried once per process) and on the GDR_FUSED_VARIANT environment
- * variable ("single" or "pair" forces one).  Launches nothing.
+ * calling thread's current device: 0 no kernel (empty work), 2 the fused kernel
+ * with one CTA per head, 3 the fused kernel with a cluster of two CTAs per head
+ * (value columns split, chunk preparation alternated between the two), 6 the
+ * one-pass CUDA-core kernel (fp32 and the other shapes), or -1 if the call
+ * would be rejected.  The choice between 2 and 3 depends on how many two-CTA
+ * clusters the device holds at once (queried once per process) and on the
+ * GDR_OPT_FUSED_VARIANT option.  Launches nothing.
  */
 int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_min,
                        gdr_dtype_t dtype);
@@ -251,10 +266,14 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  * 16 * (-g_min) <= 80 (g_min >= -5): the decay over a 64-token chunk may fall
  * far below fp32's range.
  *
- * gdr_chunk_fwd_workspace_size: bytes of workspace the two-kernel path needs
- *   for these arguments (B * H * ceil(T / 64) tiles of 16 KB), or 0 where it
- *   does not apply (anything but bf16, dk = dv = 128, chunk = 64, or empty
- *   work).  Host-only.
+ * gdr_chunk_fwd_workspace_size: bytes of workspace gdr_chunk_fwd_ws uses for
+ *   these arguments, or 0 for empty work or unsupported arguments.  Host-only.
+ *   bf16 with dk = dv = 128 and chunk = 64: the two-kernel path (B * H *
+ *   ceil(T / 64) tiles of 16 KB).  fp32 and the other shapes: the four staged
+ *   kernels (gdr_chunk_decay .. gdr_chunk_output) with their intermediates in
+ *   the workspace, 4 * (B*H*T*(1 + dk + 2*dv) + B*H*ceil(T/chunk)*dk*dv) bytes;
+ *   their WY/UT and output steps run every chunk in parallel, so they beat the
+ *   one-pass kernel of gdr_chunk_fwd on long sequences.
  * gdr_chunk_fwd_ws: gdr_chunk_fwd with a workspace.  `workspace` is device
  *   memory owned by the caller, 16-byte aligned, at least the size above, not
  *   shared with a call still running on another stream; its contents on entry
@@ -267,10 +286,11 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  *   packed sequences; the workspace holds H * (total_T / 64 + S + 1) tiles
  *   (sequence s starts at tile total offset cu_seqlens[s] / 64 + s of its head).
  * gdr_chunk_fwd_ws_path: the path gdr_chunk_fwd_ws takes given a large enough
- *   workspace: 4 two kernels with two CTAs per head in the chain kernel (value
- *   columns split), 5 two kernels with one CTA per head, else the value of
- *   gdr_chunk_fwd_path.  The split is two CTAs per head while every CTA has an
- *   SM of its own; GDR_CHAIN_SPLIT=1|2 forces one.  Launches nothing.
+ *   workspace: 1 the staged kernels, 4 two kernels with two CTAs per head in
+ *   the chain kernel (value columns split), 5 two kernels with one CTA per
+ *   head, else the value of gdr_chunk_fwd_path.  The split is two CTAs per
+ *   head while every CTA has an SM of its own; the GDR_OPT_CHAIN_SPLIT option
+ *   forces one.  Launches nothing.
  */
 size_t gdr_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
                                     gdr_dtype_t dtype);
@@ -389,6 +409,33 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
                            float *d_init, int B, int H, int T, int dk, int dv, int chunk,
                            gdr_dtype_t dtype, void *workspace, size_t workspace_bytes,
                            void *stream);
+
+/*
+ * Process-wide options, for tests and tuning.  Each takes effect for calls made
+ * after it is set, on every thread; the defaults suit production use.
+ *   GDR_OPT_WAIT_LIMIT_NS  bound of every device-side wait, in ns (default
+ *                          2e9).  0 makes every wait give up at once: the
+ *                          kernels unwind and gdr_last_device_error reports
+ *                          GDR_ERR_TIMEOUT, which drives the error path without
+ *                          a GPU fault.
+ *   GDR_OPT_FUSED_VARIANT  the single-launch bf16 kernel: 0 chosen by head count
+ *                          (default), 1 one CTA per head, 2 cluster pair.
+ *   GDR_OPT_CHAIN_SPLIT    CTAs per head in the chain kernel of the two-kernel
+ *                          path: 0 chosen by head count (default), 1 or 2.
+ *   GDR_OPT_SEGMENTS       sequence segments of the two-kernel path: 0 chosen by
+ *                          head count (default), else that many (at most 4096).
+ * gdr_set_option returns GDR_ERR_INVALID_ARG for an unknown option or a value
+ * out of its range; gdr_get_option returns the current value (-1 if unknown).
+ * The library reads no environment variable.
+ */
+typedef enum {
+    GDR_OPT_WAIT_LIMIT_NS = 0,
+    GDR_OPT_FUSED_VARIANT = 1,
+    GDR_OPT_CHAIN_SPLIT = 2,
+    GDR_OPT_SEGMENTS = 3
+} gdr_option_t;
+gdr_status_t gdr_set_option(gdr_option_t option, int64_t value);
+int64_t gdr_get_option(gdr_option_t option);
 
 /*
  * Synchronises `stream`, then returns and clears the device error word:

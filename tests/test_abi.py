@@ -116,15 +116,40 @@ def test_binding_fails_loudly_without_cuda_tensors(lib):
         gdr.chunk_fwd(q, q, q, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4), 0.9, chunk=16)
 
 
-def test_path_query(lib, monkeypatch):
+def test_path_query(lib):
     q = lib.gdr_chunk_fwd_path
-    assert q(1, 2, 256, 64, 64, 64, 0.9, 0) == 1          # fp32: staged kernels
+    assert q(1, 2, 256, 64, 64, 64, 0.9, 0) == 6          # fp32: one-pass CUDA-core kernel
     assert q(1, 2, 0, 128, 128, 64, 0.95, 1) == 0         # empty: no kernel
     assert q(1, 2, 256, 48, 128, 64, 0.95, 1) == -1       # rejected
-    monkeypatch.setenv("GDR_FUSED_VARIANT", "single")
-    assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 2
-    monkeypatch.setenv("GDR_FUSED_VARIANT", "pair")
-    assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 3
+    with gdr.option(fused_variant=1):
+        assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 2
+    with gdr.option(fused_variant=2):
+        assert q(4, 16, 4096, 128, 128, 64, 0.95, 1) == 3
+    assert lib.gdr_chunk_fwd_ws_path(1, 2, 256, 64, 64, 64, 0.9, 0) == 1   # staged, workspace
+    assert lib.gdr_chunk_fwd_kernels(1, 2, 256, 64, 64, 64, 0.9, 0) == 1
+
+
+def test_options(lib):
+    assert gdr.get_option("wait_limit_ns") == 2_000_000_000
+    for name in ("fused_variant", "chain_split", "segments"):
+        assert gdr.get_option(name) == 0
+    with gdr.option(chain_split=2, segments=5):
+        assert gdr.get_option("chain_split") == 2 and gdr.get_option("segments") == 5
+    assert gdr.get_option("chain_split") == 0 and gdr.get_option("segments") == 0
+    assert lib.gdr_set_option(1, 3) == 1                  # fused_variant out of range
+    assert lib.gdr_set_option(0, -1) == 1                 # negative wait limit
+    assert lib.gdr_set_option(99, 0) == 1                 # unknown option
+    assert lib.gdr_get_option(99) == -1
+
+
+def test_workspace_sizes(lib):
+    ws = lib.gdr_chunk_fwd_workspace_size
+    # staged shapes: 4 (BH T (1 + dk + 2 dv) + BH ceil(T / C) dk dv) bytes
+    assert ws(1, 2, 256, 64, 64, 64, 0) == 4 * (2 * 256 * (1 + 64 + 128) + 2 * 4 * 64 * 64)
+    assert ws(1, 1, 100, 32, 16, 32, 1) == 4 * (100 * (1 + 32 + 32) + 4 * 32 * 16)
+    # two-kernel path: 16 KB per chunk
+    assert ws(4, 16, 4096, 128, 128, 64, 1) >= 64 * 64 * 16384
+    assert ws(1, 2, 0, 64, 64, 64, 0) == 0 and ws(1, 2, 64, 48, 64, 64, 0) == 0
 
 
 def test_varlen_rejects(lib):
@@ -277,3 +302,20 @@ def test_chunk_fwd_host_rejects(lib):
     assert call(dk=48) == 2 and call(dt=5) == 2
     assert call(B=0) == 0                                  # no heads: nothing to do
     assert sz(1, 2, 100, 48, 128, 64, 1) == 0
+
+
+def test_static_entry_rejects_oversized_work_before_any_device_call(lib):
+    """The allocation-free prefill checks its size limit on the host, in 64-bit
+    arithmetic that cannot overflow, before it touches a device."""
+    f = lib.gdr_chunk_fwd_static
+    args = lambda B, H, T, d=128, C=64: (P, P, P, P, P, 0.95, None, P, None, B, H, T, d, d, C, 1,
+                                         None)
+    assert f(*args(65536, 65536, 1)) == 2                 # B H beyond int32
+    assert f(*args(46340, 46340, 2**31 - 1)) == 2         # B H T far beyond the array
+    assert f(*args(1, 2**20, 2**20)) == 2
+    assert f(*args(4, 16, 4096)) == 2                     # the prefill workload: ~ 2.3 GB
+    # 4 (B H T (1 + dk + 2 dv) + B H ceil(T / C) dk dv) against 32 MiB at d = 64, C = 64:
+    # T = 16320 for two heads needs 512 bytes less than the array, T = 16321 more
+    assert f(*args(1, 2, 16321, d=64)) == 2
+    assert f(*args(1, 2, 16320, d=64, C=48)) == 2         # unsupported chunk
+    assert f(*args(1, 2, 64, d=64)[:5] + (0.0,) + args(1, 2, 64, d=64)[6:]) == 1   # a_min

@@ -1,10 +1,8 @@
-"""Failure detection without a GPU fault: GDR_FAULT_INJECT=timeout makes every
-bounded wait of the prefill kernels give up at once.  The kernel must unwind (let
+"""Failure detection without a GPU fault: the wait_limit_ns option set to 0 makes
+every bounded wait of the prefill kernels give up at once.  The kernel must unwind (let
 its own copies land, free TMEM, return), gdr_last_device_error must report
 GDR_ERR_TIMEOUT, and the context must stay usable for the next call."""
 from __future__ import annotations
-
-import os
 
 import pytest
 import torch
@@ -16,36 +14,33 @@ from gated_delta_rule_gdr_gb300 import inputs as I
 pytestmark = pytest.mark.gpu
 
 
-# (environment, workspace): the fused kernels on the single-launch path, the
+# (library options, workspace): the fused kernels on the single-launch path, the
 # preparation and chain kernels on the two-kernel path
-VARIANTS = {"single": ({"GDR_FUSED_VARIANT": "single"}, None),
-            "pair": ({"GDR_FUSED_VARIANT": "pair"}, None),
-            "chain2": ({"GDR_CHAIN_SPLIT": "2"}, "auto"),
-            "chain1": ({"GDR_CHAIN_SPLIT": "1"}, "auto")}
+VARIANTS = {"single": ({"fused_variant": 1}, None),
+            "pair": ({"fused_variant": 2}, None),
+            "chain2": ({"chain_split": 2}, "auto"),
+            "chain1": ({"chain_split": 1}, "auto"),
+            "segments": ({"segments": 3}, "auto")}
 
 
 @pytest.mark.parametrize("variant", list(VARIANTS))
-def test_injected_timeout_is_reported_and_recovers(variant, monkeypatch):
-    env, ws = VARIANTS[variant]
-    for k, val in env.items():
-        monkeypatch.setenv(k, val)
+def test_injected_timeout_is_reported_and_recovers(variant):
+    opts, ws = VARIANTS[variant]
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     gdr.load(build_if_missing=True)
     w = I.PREFILL.with_(B=1, H=2, T=300)
     x = I.prefill_inputs(w, device="cuda")
-    assert gdr.last_device_error() == 0
-    os.environ["GDR_FAULT_INJECT"] = "timeout"
-    try:
-        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
-                      workspace=ws)
-        assert gdr.last_device_error() == 5          # GDR_ERR_TIMEOUT
-    finally:
-        del os.environ["GDR_FAULT_INJECT"]
-    assert gdr.last_device_error() == 0              # the word was cleared
-    out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
-                             x["init_state"], workspace=ws)
-    torch.cuda.synchronize()
+    with gdr.option(**opts):
+        assert gdr.last_device_error() == 0
+        with gdr.option(wait_limit_ns=0):
+            gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                          workspace=ws)
+            assert gdr.last_device_error() == 5          # GDR_ERR_TIMEOUT
+        assert gdr.last_device_error() == 0              # the word was cleared
+        out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                                 x["init_state"], workspace=ws)
+        torch.cuda.synchronize()
     cpu = {n: t.cpu() for n, t in x.items()}
     ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,
                         cpu["init_state"])

@@ -4,7 +4,6 @@ fp32 path, 5e-3 for the bf16 paths, for outputs and final states alike."""
 from __future__ import annotations
 
 import contextlib
-import os
 
 import numpy as np
 import pytest
@@ -48,35 +47,33 @@ def to(x, device):
 # The kernels of the bf16, d = 128, chunk 64 prefill: the single-launch fused kernel
 # with one CTA per head ("single") or a two-CTA cluster per head ("pair"), and the
 # two-kernel path (preparation, then the chain kernel) with two CTAs per head
-# ("chain2") or one ("chain1").  Value: (environment, workspace argument).
-VARIANTS = {"single": ({"GDR_FUSED_VARIANT": "single"}, None),
-            "pair": ({"GDR_FUSED_VARIANT": "pair"}, None),
-            "chain2": ({"GDR_CHAIN_SPLIT": "2"}, "auto"),
-            "chain1": ({"GDR_CHAIN_SPLIT": "1"}, "auto")}
+# ("chain2") or one ("chain1").  Value: (library options, workspace argument).
+VARIANTS = {"single": ({"fused_variant": 1}, None),
+            "pair": ({"fused_variant": 2}, None),
+            "chain2": ({"chain_split": 2}, "auto"),
+            "chain1": ({"chain_split": 1}, "auto")}
 
 
 @contextlib.contextmanager
 def path_variant(name):
     """Force one of VARIANTS (by default the launchers pick by the number of
     heads); yields the workspace argument that selects its path."""
-    env, ws = VARIANTS[name]
-    old = {k: os.environ.get(k) for k in env}
-    os.environ.update(env)
-    try:
+    opts, ws = VARIANTS[name]
+    with gdr.option(**opts):
         yield ws
-    finally:
-        for k, val in old.items():
-            if val is None:
-                del os.environ[k]
-            else:
-                os.environ[k] = val
 
 
 # ------------------------------------------------------------------ the correctness workload
-def test_correctness_workload_fp32():
+# workspace "auto": the staged kernels on a caller-owned workspace (gdr_chunk_fwd_ws);
+# None: the one-pass kernel of gdr_chunk_fwd, which allocates nothing
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_correctness_workload_fp32(workspace):
     w = I.CORRECTNESS
     x = to(I.prefill_inputs(w), "cuda")
-    out, fin = run_gpu(x, w)
+    expect = 1 if workspace else 6
+    assert gdr.chunk_fwd_path(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.a_min, torch.float32,
+                              workspace=bool(workspace)) == expect
+    out, fin = run_gpu(x, w, workspace=workspace)
     ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min, None)
     assert rel(out, ro) <= TOL["f32"], rel(out, ro)
     assert rel(fin, rf) <= TOL["f32"], rel(fin, rf)
@@ -122,13 +119,14 @@ def test_decay_bounds_on_device():
 
 
 # ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("workspace", ["auto", None])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 100, 200])
 @pytest.mark.parametrize("d", [64, 128])
-def test_ragged_and_tiny(dtype, T, d):
+def test_ragged_and_tiny(dtype, T, d, workspace):
     w = I.CORRECTNESS.with_(B=1, H=1, T=T, dk=d, dv=d, dtype=dtype, init_std=0.02)
     x = to(I.prefill_inputs(w), "cuda")
-    out, fin = run_gpu(x, w)
+    out, fin = run_gpu(x, w, workspace=workspace)
     ro, rf = oracle.fwd(*(x[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min,
                         x["init_state"].cpu())
     assert rel(out, ro) <= TOL[dtype]
@@ -427,8 +425,17 @@ def test_million_prefill_b1h16t1048576():
     _, rf = oracle.fwd(h0["q"], h0["k"], h0["v"], h0["g"], h0["beta"], w.a_min, None,
                        want_out=False)
     e_f = rel(fin[:, :1], rf)
-    print(f"million prefill rel-L2 out[h0-1,:32768] {e_o:.3e} final[h0] {e_f:.3e}")
-    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"]
+    # head 0 over the first 2^18 tokens: the boundary between the first two segments
+    # of the default segment split lies inside (at most 2^18 tokens per segment for
+    # five segments and more)
+    P2 = 1 << 18
+    s2 = {n: x[n][:, :1, :P2].cpu() for n in ("q", "k", "v", "g", "beta")}
+    r2, _ = oracle.fwd(s2["q"], s2["k"], s2["v"], s2["g"], s2["beta"], w.a_min, None,
+                       want_final=False)
+    e_2 = rel(out[:, :1, :P2], r2)
+    print(f"million prefill rel-L2 out[h0-1,:32768] {e_o:.3e} out[h0,:2^18] {e_2:.3e} "
+          f"final[h0] {e_f:.3e}")
+    assert e_o <= TOL["bf16"] and e_f <= TOL["bf16"] and e_2 <= TOL["bf16"]
 
 
 # ------------------------------------------------------------------ the decode workload
@@ -464,3 +471,79 @@ def test_decode_shapes(dtype, d):
                            ref_state)
         assert rel(out, ro) <= (1e-5 if dtype == "f32" else TOL["bf16"])
     assert rel(state, ref_state) <= 1e-5
+
+
+# the one-pass kernel on every dimension and chunk it takes, ragged, with and without
+# an initial state, against the oracle at the fp32 tolerance
+@pytest.mark.parametrize("dk,dv,C,T", [(16, 16, 16, 37), (32, 128, 32, 130), (128, 16, 64, 129),
+                                       (64, 32, 16, 300), (128, 128, 64, 200)])
+@pytest.mark.parametrize("init", [None, 0.3])
+def test_one_pass_kernel_shapes(dk, dv, C, T, init):
+    w = I.CORRECTNESS.with_(B=2, H=2, T=T, dk=dk, dv=dv, chunk=C, dtype="f32", init_std=init)
+    x = to(I.prefill_inputs(w), "cuda")
+    out, fin = run_gpu(x, w, workspace=None)
+    cpu = {n: (None if t is None else t.cpu()) for n, t in x.items()}
+    ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,
+                        cpu["init_state"])
+    assert rel(out, ro) <= TOL["f32"], rel(out, ro)
+    assert rel(fin, rf) <= TOL["f32"], rel(fin, rf)
+
+
+# ------------------------------------------------------------------ sequence segments
+# The two-kernel path with S segments per head: every segment's offset map and
+# transition at once, the scan over segments, then every segment's chain at once.
+# Forced segment counts on small shapes: several chunks per segment, ragged last
+# segments, with and without an initial state, both chain splits, both decay forms
+# (the pages' g_min = -5 included, where the decay over a chunk underflows fp32).
+@pytest.mark.parametrize("S", [2, 3, 5])
+@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("decay,bound", [("affine", 0.95), ("log", -5.0)])
+@pytest.mark.parametrize("T,init", [(64 * 12, 0.02), (64 * 10 + 17, None), (64 * 7 + 1, 0.3)])
+def test_segmented_two_kernel(S, split, decay, bound, T, init):
+    w = I.PREFILL.with_(B=2, H=2, T=T, init_std=init)
+    x = to(I.prefill_inputs(w), "cuda")
+    with gdr.option(segments=S, chain_split=split):
+        # (the path query takes the linear-domain floor; the path is the same for both forms)
+        assert gdr.chunk_fwd_path(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.a_min) == 7
+        out, fin = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], bound,
+                                 x["init_state"], decay=decay, workspace="auto")
+    torch.cuda.synchronize()
+    cpu = {n: (None if t is None else t.cpu()) for n, t in x.items()}
+    ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], bound,
+                        cpu["init_state"], decay=decay)
+    assert rel(out, ro) <= TOL["bf16"], rel(out, ro)
+    assert rel(fin, rf) <= TOL["bf16"], rel(fin, rf)
+    # every segment's rows on their own: a wrong segment state would show in its rows
+    nc = (T + 63) // 64
+    L = (nc + S - 1) // S
+    for s0 in range(0, nc, L):
+        a, b = s0 * 64, min(T, (s0 + L) * 64)
+        assert rel(out[:, :, a:b], ro[:, :, a:b]) <= TOL["bf16"], (s0, rel(out[:, :, a:b], ro[:, :, a:b]))
+
+
+def test_segmented_matches_unsegmented_and_may_alias():
+    """The segmented path against the single-segment chain (same tiles, same chain
+    arithmetic: they differ only by the scan's fp32 products and the segment maps'
+    roundings), and the initial state aliasing the final state."""
+    w = I.PREFILL.with_(B=1, H=3, T=64 * 20 + 5)
+    x = to(I.prefill_inputs(w), "cuda")
+    with gdr.option(segments=1):
+        ref_out, ref_fin = run_gpu(x, w)
+    with gdr.option(segments=4):
+        out, fin = run_gpu(x, w)
+        st = x["init_state"].clone()
+        out2, _ = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, st,
+                                final_state=st)
+        torch.cuda.synchronize()
+    assert rel(out, ref_out) <= 3e-3 and rel(fin, ref_fin) <= 3e-3
+    assert torch.equal(out2, out) and torch.equal(st, fin)
+
+
+def test_segment_count_is_automatic_for_few_heads():
+    """Few heads and long sequences take the segmented path by default; many heads
+    do not (every SM already has a chain)."""
+    props = torch.cuda.get_device_properties(0)
+    sms = props.multi_processor_count
+    assert gdr.chunk_fwd_path(1, 16, 1 << 20, 128, 128, 64, 0.99) == (7 if sms >= 48 else 4)
+    assert gdr.chunk_fwd_path(4, 16, 4096, 128, 128, 64, 0.95) in (4, 5)
+    assert gdr.chunk_fwd_path(1, 16, 256, 128, 128, 64, 0.99) in (4, 5)   # too short to split
