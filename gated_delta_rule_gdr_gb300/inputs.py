@@ -22,6 +22,13 @@ Decode draws fresh q, k, v, g, beta every step from a seed derived from
 
 The backward takes cotangents: d_out ~ N(0, 1) in the compute dtype [B,H,T,dv] and
 d_final ~ N(0, 1) fp32 [B,H,dk,dv] (``cotangents``).
+
+Gated multi-head latent attention, one decode step (``mla_inputs``): the absorbed
+query q_abs ~ N(0, 1) bf16 [N,H,dc], the latent cache ckv ~ N(0, 1) bf16 [N,L,dc]
+(unit-variance latents, as after a normalisation), the value up-projection
+w_uv ~ N(0, 1/dc) bf16 [H,dh,dc] (fan-in scaled), the gate's pre-activation
+z ~ N(0, 1) fp32 [N,H,dh], cache lengths L for every sequence or (ragged) uniform in
+[1, L], and the score scale 1/sqrt(dh).
 """
 from __future__ import annotations
 
@@ -32,7 +39,8 @@ import math
 import torch
 
 _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "init": 6, "lengths": 7,
-               "d_out": 8, "d_final": 9}
+               "d_out": 8, "d_final": 9, "q_abs": 10, "ckv": 11, "w_uv": 12, "gate": 13,
+               "seqlens": 14}
 
 
 @dataclass(frozen=True)
@@ -171,3 +179,46 @@ def cotangents(w: Workload, device="cpu"):
     d_final = torch.randn((w.B, w.H, w.dk, w.dv), generator=_gen(device, w.seed, "d_final"),
                           device=device, dtype=torch.float32)
     return dict(d_out=d_out, d_final=d_final)
+
+
+@dataclass(frozen=True)
+class MlaWorkload:
+    """One decode step of gated multi-head latent attention: N sequences, H heads, a
+    latent cache of up to L tokens of dc values per sequence, dh values per head after
+    the value up-projection."""
+    name: str
+    N: int
+    H: int
+    L: int
+    dc: int
+    dh: int
+    ragged: bool = False      # cache lengths uniform in [1, L] instead of all L
+    seed: int = 0
+
+    def with_(self, **kw) -> "MlaWorkload":
+        return replace(self, **kw)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.dh)
+
+
+MLA_DECODE = MlaWorkload("mla_decode_n32h64_l32768_dc512_dh128_bf16", 32, 64, 32768, 512, 128)
+
+
+def mla_inputs(w: MlaWorkload, device="cpu"):
+    """Returns dict(q_abs, ckv, w_uv, gate, seqlens) for a latent-attention decode step."""
+    q_abs = torch.randn((w.N, w.H, w.dc), generator=_gen(device, w.seed, "q_abs"), device=device,
+                        dtype=torch.float32).to(torch.bfloat16)
+    ckv = torch.randn((w.N, w.L, w.dc), generator=_gen(device, w.seed, "ckv"), device=device,
+                      dtype=torch.float32).to(torch.bfloat16)
+    w_uv = (torch.randn((w.H, w.dh, w.dc), generator=_gen(device, w.seed, "w_uv"), device=device,
+                        dtype=torch.float32) / math.sqrt(w.dc)).to(torch.bfloat16)
+    gate = torch.randn((w.N, w.H, w.dh), generator=_gen(device, w.seed, "gate"), device=device,
+                       dtype=torch.float32)
+    if w.ragged:
+        lens = torch.randint(1, w.L + 1, (w.N,), generator=_gen("cpu", w.seed, "seqlens"),
+                             dtype=torch.int32)
+    else:
+        lens = torch.full((w.N,), w.L, dtype=torch.int32)
+    return dict(q_abs=q_abs, ckv=ckv, w_uv=w_uv, gate=gate, seqlens=lens.to(device))

@@ -20,6 +20,9 @@ Contents
                   (decay="log") the pages' log-domain form alpha = exp(g_min sigmoid(g)).
 * ``chunkwise`` (module) -- the chunked reformulation in numpy fp64, used to
                   check the token loop and to export per-stage intermediates.
+* ``mla_decode`` -- one decode step of gated multi-head latent attention (C, fp64,
+                  ``mla_oracle.c``): softmax attention of the absorbed query over the
+                  latent cache, the value up-projection, the sigmoid output gate.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (see the module
 docstrings there for which mathematical fact pins which part).
@@ -38,19 +41,73 @@ _SRC = os.path.join(_HERE, "gdr_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libgdr_oracle.so")
 _lib = None
 _lock = threading.Lock()
+_MLA_SRC = os.path.join(_HERE, "mla_oracle.c")
+_MLA_LIB_PATH = os.path.join(_HERE, "libmla_oracle.so")
+_mla_lib = None
+
+
+def _compile(src: str, out: str, force: bool) -> str:
+    if (not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
 
 
 def build(force: bool = False) -> str:
-    """Compile ``gdr_oracle.c`` with the host C compiler (fp64, no fast-math)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
-           "-ffp-contract=off", "-o", tmp, _SRC, "-lm", "-lpthread"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    """Compile ``gdr_oracle.c`` and ``mla_oracle.c`` with the host C compiler (fp64, no
+    fast-math); returns the path of the recurrence's library."""
+    _compile(_MLA_SRC, _MLA_LIB_PATH, force)
+    return _compile(_SRC, _LIB_PATH, force)
+
+
+def _load_mla():
+    global _mla_lib
+    with _lock:
+        if _mla_lib is None:
+            build()
+            lib = ctypes.CDLL(_MLA_LIB_PATH)
+            set_mla_signature(lib)
+            _mla_lib = lib
+    return _mla_lib
+
+
+def set_mla_signature(lib):
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.gdr_oracle_mla_decode.restype = ctypes.c_int
+    lib.gdr_oracle_mla_decode.argtypes = [f32p, f32p, ctypes.POINTER(ctypes.c_int), f32p, f32p,
+                                          ctypes.c_double, ctypes.POINTER(ctypes.c_double)] + \
+        [ctypes.c_int] * 6
+
+
+def mla_decode(q_abs, ckv, seqlens, w_uv, gate, scale: float, *, nthreads: int | None = None):
+    """One decode step of gated multi-head latent attention, fp64.  q_abs [N,H,dc] (the
+    query with the key up-projection absorbed), ckv [N,Lmax,dc] (latent cache),
+    seqlens [N] (cache rows in use), w_uv [H,dh,dc], gate [N,H,dh] (the gate's
+    pre-activation).  Returns out [N,H,dh] fp64:
+    out[n,h] = sigmoid(gate[n,h]) * (w_uv[h] @ sum_t softmax_t(scale q_abs[n,h].ckv[n,t]) ckv[n,t])."""
+    qa, c, w, z = (_f32(x) for x in (q_abs, ckv, w_uv, gate))
+    N, H, dc = qa.shape
+    Lmax = c.shape[1]
+    dh = w.shape[1]
+    if c.shape != (N, Lmax, dc) or w.shape != (H, dh, dc) or z.shape != (N, H, dh):
+        raise ValueError("mla_decode shape mismatch")
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().cpu().numpy()
+    lens = np.ascontiguousarray(np.asarray(seqlens), dtype=np.int32)
+    if lens.shape != (N,):
+        raise ValueError("seqlens must have N entries")
+    out = np.empty((N, H, dh), np.float64)
+    rc = _load_mla().gdr_oracle_mla_decode(
+        _ptr(qa, ctypes.c_float), _ptr(c, ctypes.c_float), _ptr(lens, ctypes.c_int),
+        _ptr(w, ctypes.c_float), _ptr(z, ctypes.c_float), float(scale), _ptr(out, ctypes.c_double),
+        N, H, Lmax, dc, dh, int(nthreads or os.cpu_count() or 1))
+    if rc != 0:
+        raise RuntimeError(f"gdr_oracle_mla_decode failed with code {rc}")
+    return out
 
 
 def _load():
