@@ -12,7 +12,8 @@ workload (N=256 sequences x H=32 heads, one token per step), because the
 metric asks for both, a ``backward`` object (the gradients of the prefill
 workload), and ``long`` (B=1, H=32, T=65536) and ``million`` (B=1, H=16,
 T=1,048,576) objects for the two long prefill workloads, each with its own
-roofline and oracle baseline.  ``--workload varlen`` times the packed variable-length
+roofline and oracle baseline, and ``mla``: one decode step of gated multi-head
+latent attention (N=32 sequences, H=64 heads, 32768 cached latents of 512 values).  ``--workload varlen`` times the packed variable-length
 prefill instead: 32 sequences of seeded lengths in [16, 4096] (34,599 tokens),
 H=16, through ``chunk_fwd_varlen``; ``value`` is packed tokens/s.
 
@@ -371,6 +372,49 @@ def path_kernels(path):
     }[path]
 
 
+def mla_algorithmic(w: I.MlaWorkload):
+    """Bytes and FLOPs of one latent-attention decode step: the latent cache, the
+    queries, W_uv, the gate and the output once each; QK and PV over every cached
+    token (2 dc MACs each per head) plus the up-projection."""
+    by = (w.N * w.L * w.dc * 2 + w.N * w.H * w.dc * 2 + w.H * w.dh * w.dc * 2
+          + w.N * w.H * w.dh * (4 + 2))
+    fl = 4 * w.N * w.H * w.L * w.dc + 2 * w.N * w.H * w.dh * w.dc
+    return by, fl
+
+
+def bench_mla(gdr, w, K, W, dev, stream):
+    """One decode step of gated latent attention over the device-resident cache (1 GiB,
+    far larger than L2: no flush)."""
+    x = I.mla_inputs(w, device=dev)
+    ws = torch.empty(max(gdr.mla_decode_workspace_size(w.N, w.H, w.L, w.dc, w.dh), 16),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((w.N, w.H, w.dh), dtype=torch.bfloat16, device=dev)
+
+    def step(_):
+        gdr.mla_decode(x["q_abs"], x["ckv"], x["seqlens"], x["w_uv"], x["gate"], w.scale, out=out,
+                       workspace=ws)
+
+    return time_steps(step, K, W, None, stream), x
+
+
+def cpu_baseline_mla(w, x, budget_s=6.0):
+    """The fp64 oracle on whole sequences of the decode step, every head, until about
+    budget_s of work; value in the leg's unit (sequences' tokens per second)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    n, dt = 0, 0.0
+    while dt < budget_s and n < w.N:
+        sub = {k: (t if k == "w_uv" else t[n:n + 1]).cpu() for k, t in x.items()}
+        t0 = time.perf_counter()
+        oracle.mla_decode(sub["q_abs"], sub["ckv"], sub["seqlens"], sub["w_uv"], sub["gate"],
+                          w.scale, nthreads=cores)
+        dt += time.perf_counter() - t0
+        n += 1
+    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.N} sequences, all {w.H} heads, {w.L} cached tokens each "
+                      f"({dt:.2f} s); value = decoded tokens per second"}
+
+
 def bench_decode(gdr, w, K, W, dev, flush, stream):
     state = I.decode_state(w, device=dev)
     nsteps = max(K, 1)
@@ -580,6 +624,10 @@ def run_ours(args):
         if main_w is I.PREFILL and not args.no_backward:
             bwd = bench_backward(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
             barrier()
+        mla = None
+        if main_w is I.PREFILL and not args.no_mla:
+            mla = bench_mla(gdr, I.MLA_DECODE, max(3, args.steps // 2), 3, dev, stream)
+            barrier()
         legs = {}
         if main_w is I.PREFILL and not args.no_long:
             for key, lw, k in (("long", I.LONG_PREFILL, max(3, args.steps // 2)),
@@ -693,6 +741,28 @@ def run_ours(args):
                          "algorithmic_bytes": bby},
             "workspace_bytes": bws, "gpu_launches": 4 * len(bms),
         }
+    if mla is not None:
+        wm = I.MLA_DECODE
+        mms, _ = mla
+        mmean = statistics.mean(mms)
+        mby, mfl = mla_algorithmic(wm)
+        mgbs = mby / (mmean * 1e-3) / 1e9
+        line["mla"] = {
+            "metric": "latent-attention decode tokens/s", "workload": wm.name,
+            "value": round(world * wm.N / (max_over_ranks(mmean) * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(mmean, 4), "steps": len(mms),
+            "roofline": {"bound": "hbm", "kernel": "mla_attn_kernel + mla_combine_kernel",
+                         "achieved": round(mgbs, 1), "peak": pk["hbm_gbs"], "peak_kind": pk_kind,
+                         "unit": "GB/s", "frac": round(mgbs / pk["hbm_gbs"], 4),
+                         "traffic": committed_traffic("mla_attn_kernel + mla_combine_kernel",
+                                                      [CSRC + "gdr_mla.cu"] + _COMMON, wm.name),
+                         "algorithmic_bytes": mby, "algorithmic_flops": mfl,
+                         "achieved_tflops": round(mfl / (mmean * 1e-3) / 1e12, 2),
+                         "tensor_frac": round(mfl / (mmean * 1e-3) / 1e12 / pk["bf16_tflops"], 4)},
+            "l2": "cache (1 GiB) larger than L2, no flush",
+            "gpu_launches": 2 * len(mms),
+            "ms_per_step_all": [round(t, 4) for t in mms],
+        }
     for key, (lms, _) in legs.items():
         line[key] = prefill_leg_line(gdr, {"long": I.LONG_PREFILL, "million": I.MILLION_PREFILL}[key],
                                      lms, pk, pk_kind, world, max_over_ranks)
@@ -704,6 +774,9 @@ def run_ours(args):
             line["decode"]["cpu_baseline"] = cpu_baseline_decode(I.DECODE)
         if bwd is not None:
             line["backward"]["cpu_baseline"] = cpu_baseline_backward(main_w)
+        if mla is not None:
+            line["mla"]["cpu_baseline"] = cpu_baseline_mla(I.MLA_DECODE, mla[1])
+            mla = None
         for key, (_, lx) in legs.items():
             lw = {"long": I.LONG_PREFILL, "million": I.MILLION_PREFILL}[key]
             line[key]["cpu_baseline"] = cpu_baseline_prefill(lw, budget_s=6.0, x=lx)
@@ -792,6 +865,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-mla", action="store_true",
+                    help="skip the gated latent-attention decode leg")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the long (B1 H32 T65536) and million-token (B1 H16 T1048576) legs")
     ap.add_argument("--single-launch", action="store_true",

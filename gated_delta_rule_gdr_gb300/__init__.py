@@ -28,7 +28,7 @@ __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk
            "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "chunk_fwd_varlen",
            "chunk_fwd_workspace_size", "chunk_fwd_varlen_workspace_size", "last_device_error",
            "status_string", "version", "library_path", "STATUS", "PATHS", "OPTIONS",
-           "set_option", "get_option", "option"]
+           "set_option", "get_option", "option", "mla_decode", "mla_decode_workspace_size"]
 
 DECAY = {"affine": 0, "log": 1}   # gdr_decay_t
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
@@ -89,6 +89,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_status_string": [i],
         "gdr_version": [],
         "gdr_set_option": [i, ctypes.c_int64],
+        "gdr_mla_decode": [vp, vp, vp, vp, vp, f, vp, i, i, i, i, i, vp, sz, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -99,6 +100,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [i, i, i, i, i, i, i]
         fn.restype = sz
+    lib.gdr_mla_decode_workspace_size.argtypes = [i, i, i, i, i]
+    lib.gdr_mla_decode_workspace_size.restype = sz
     lib.gdr_get_option.argtypes = [i]
     lib.gdr_get_option.restype = ctypes.c_int64
     lib.gdr_status_string.restype = ctypes.c_char_p
@@ -433,6 +436,40 @@ def chunk_fwd_path(B, H, T, dk, dv, chunk=64, a_min=0.95, dtype=torch.bfloat16,
     device (see PATHS; -1 = rejected); workspace=False: the single-launch path."""
     fn = load().gdr_chunk_fwd_ws_path if workspace else load().gdr_chunk_fwd_path
     return int(fn(B, H, T, dk, dv, chunk, float(a_min), DTYPE[dtype]))
+
+
+def mla_decode_workspace_size(N, H, Lmax, dc=512, dh=128) -> int:
+    """Bytes of workspace one latent-attention decode step needs (0 if unsupported)."""
+    return int(load().gdr_mla_decode_workspace_size(N, H, Lmax, dc, dh))
+
+
+def mla_decode(q_abs, ckv, seqlens, w_uv, gate, scale: float, *, out=None, workspace=None):
+    """One decode step of gated multi-head latent attention.  q_abs [N,H,dc] bf16 (the
+    query with the key up-projection absorbed), ckv [N,Lmax,dc] bf16 (latent cache),
+    seqlens [N] int32 on the device, w_uv [H,dh,dc] bf16, gate [N,H,dh] fp32 (the gate's
+    pre-activation).  Returns out [N,H,dh] bf16.  workspace: None (from torch's caching
+    allocator) or a uint8 CUDA tensor of at least mla_decode_workspace_size bytes."""
+    lib = load()
+    N, H, dc = q_abs.shape
+    Lmax = ckv.shape[1]
+    dh = w_uv.shape[1]
+    for t, name in ((q_abs, "q_abs"), (ckv, "ckv"), (w_uv, "w_uv")):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+    _f32(gate, "gate")
+    if seqlens.dtype != torch.int32:
+        raise TypeError("seqlens must be int32")
+    if out is None:
+        out = torch.empty((N, H, dh), dtype=torch.bfloat16, device=q_abs.device)
+    need = mla_decode_workspace_size(N, H, Lmax, dc, dh)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_abs.device)
+    elif workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    _check(lib.gdr_mla_decode(_ptr(q_abs), _ptr(ckv), _ptr(seqlens), _ptr(w_uv), _ptr(gate),
+                              float(scale), _ptr(out), N, H, Lmax, dc, dh, _ptr(workspace),
+                              workspace.numel(), _stream(q_abs.device)), "gdr_mla_decode")
+    return out
 
 
 def last_device_error(device=None) -> int:

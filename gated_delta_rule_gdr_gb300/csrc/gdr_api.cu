@@ -536,6 +536,35 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
                                      workspace, elem_of(dtype), s));
 }
 
+// ---- gated multi-head latent attention, one decode step ----
+
+size_t gdr_mla_decode_workspace_size(int N, int H, int Lmax, int dc, int dh) {
+    if (N <= 0 || H <= 0 || Lmax <= 0 || !gdr::mla_supported(H, dc, dh)) return 0;
+    if ((int64_t)N * H > 0x7fffffff || (int64_t)N * Lmax > ((int64_t)1 << 40)) return 0;
+    return gdr::mla_workspace_bytes(N, H, Lmax);
+}
+
+gdr_status_t gdr_mla_decode(const void *q_abs, const void *ckv, const int *seqlens,
+                            const void *w_uv, const float *gate, float scale, void *out, int N,
+                            int H, int Lmax, int dc, int dh, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    if (N < 0 || H < 0 || Lmax < 0 || dc < 0 || dh < 0) return GDR_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return GDR_ERR_INVALID_ARG;
+    if ((int64_t)N * H == 0) return GDR_OK;
+    if (Lmax == 0 || !gdr::mla_supported(H, dc, dh)) return GDR_ERR_UNSUPPORTED;
+    if ((int64_t)N * H > 0x7fffffff || (int64_t)N * Lmax > ((int64_t)1 << 40))
+        return GDR_ERR_UNSUPPORTED;
+    if (!q_abs || !ckv || !seqlens || !w_uv || !gate || !out) return GDR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q_abs) | reinterpret_cast<uintptr_t>(ckv) |
+         reinterpret_cast<uintptr_t>(w_uv)) & 15)
+        return GDR_ERR_INVALID_ARG;   // TMA and 16-byte loads
+    const size_t need = gdr::mla_workspace_bytes(N, H, Lmax);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+        return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_mla_decode(q_abs, ckv, seqlens, w_uv, gate, scale, out, N, H, Lmax,
+                                            dh, workspace, static_cast<cudaStream_t>(stream)));
+}
+
 gdr_status_t gdr_last_device_error(void *stream) {
     unsigned word = 0;
     cudaError_t e = gdr::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &word);

@@ -137,6 +137,16 @@ cudaError_t take_segment_error_word(unsigned *value);
 cudaError_t take_prep_error_word(unsigned *value);
 cudaError_t take_chain_error_word(unsigned *value);
 
+// ---- one decode step of gated multi-head latent attention (gdr_mla.cu) ----
+bool mla_supported(int H, int dc, int dh);
+// Splits of each sequence's cache (CTAs per (sequence, group of 64 heads)).
+int mla_splits(int N, int H, int Lmax);
+size_t mla_workspace_bytes(int N, int H, int Lmax);
+cudaError_t launch_mla_decode(const void *q_abs, const void *ckv, const int *seqlens, const void *w_uv,
+                              const float *gate, float scale, void *out, int N, int H, int Lmax, int dh,
+                              void *ws, cudaStream_t s);
+cudaError_t take_mla_error_word(unsigned *value);
+
 // Device error word shared by every kernel with a bounded wait.
 // Returns the word's value and clears it (synchronous on `s`).
 cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value);

@@ -411,6 +411,43 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
                            void *stream);
 
 /*
+ * One decode step of gated multi-head latent attention, the exact-attention
+ * layer the pages interleave with the linear attention: the key/value
+ * projections are compressed into a latent space so the cache holds one latent
+ * vector per token, exact softmax attention keeps precise retrieval, and a gate
+ * is added ("Trillion-Parameter MoE Multimodal LLMs: How to Evaluate the New
+ * Generation", section 2.1; "How to Think About Trillion-Parameter Sparse
+ * Multimodal LLMs", section 2.3).  With the key up-projection absorbed into the
+ * query (q_abs = W_uk,h^T q_h), per sequence n and head h:
+ *   s_t = scale * q_abs[n,h] . ckv[n,t]            for t < seqlens[n]
+ *   o   = w_uv[h] * sum_t softmax(s)_t ckv[n,t]     (dh values)
+ *   out[n,h] = sigmoid(gate[n,h]) * o              (elementwise)
+ * A sequence of length 0 gives a zero output.
+ *
+ *   q_abs   bf16 [N,H,dc]      the absorbed queries
+ *   ckv     bf16 [N,Lmax,dc]   the latent cache (rows at and past seqlens[n] are
+ *                              never used, whatever they hold)
+ *   seqlens DEVICE int32 [N]   cache rows in use, clamped into [0, Lmax]
+ *   w_uv    bf16 [H,dh,dc]     the value up-projection
+ *   gate    fp32 [N,H,dh]      the gate's pre-activation
+ *   scale   score scale, > 0 (typically 1/sqrt(dh))
+ *   out     bf16 [N,H,dh]
+ *   workspace  device memory owned by the caller, 16-byte aligned, of at least
+ *           gdr_mla_decode_workspace_size bytes (each split of a sequence's cache
+ *           leaves its unnormalised partial result there); scratch on entry and exit.
+ * Supported: dc = 512, H a multiple of 64, dh a multiple of 4 up to 1024
+ * (GDR_ERR_UNSUPPORTED otherwise).  q_abs, ckv and w_uv must be 16-byte aligned
+ * (GDR_ERR_INVALID_ARG).  Two launches: the split attention on tensor cores,
+ * then the merge of the splits with the up-projection and the gate.
+ * gdr_mla_decode_workspace_size returns 0 for unsupported arguments.
+ */
+size_t gdr_mla_decode_workspace_size(int N, int H, int Lmax, int dc, int dh);
+gdr_status_t gdr_mla_decode(const void *q_abs, const void *ckv, const int *seqlens,
+                            const void *w_uv, const float *gate, float scale, void *out, int N,
+                            int H, int Lmax, int dc, int dh, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
  * Process-wide options, for tests and tuning.  Each takes effect for calls made
  * after it is set, on every thread; the defaults suit production use.
  *   GDR_OPT_WAIT_LIMIT_NS  bound of every device-side wait, in ns (default

@@ -319,3 +319,26 @@ def test_static_entry_rejects_oversized_work_before_any_device_call(lib):
     assert f(*args(1, 2, 16321, d=64)) == 2
     assert f(*args(1, 2, 16320, d=64, C=48)) == 2         # unsupported chunk
     assert f(*args(1, 2, 64, d=64)[:5] + (0.0,) + args(1, 2, 64, d=64)[6:]) == 1   # a_min
+
+
+def test_mla_decode_rejects(lib):
+    f = lib.gdr_mla_decode
+    args = lambda **kw: [kw.get(n, d) for n, d in (
+        ("q", P), ("c", P), ("lens", P), ("w", P), ("z", P), ("scale", 0.088), ("out", P),
+        ("N", 2), ("H", 64), ("L", 100), ("dc", 512), ("dh", 128), ("ws", P), ("wsb", 1 << 40),
+        ("stream", None))]
+    assert f(*args(N=-1)) == 1
+    assert f(*args(scale=0.0)) == 1
+    assert f(*args(scale=float("nan"))) == 1
+    assert f(*args(N=0)) == 0                              # nothing to do
+    assert f(*args(dc=256)) == 2                           # latent width 512 only
+    assert f(*args(H=48)) == 2                             # heads in groups of 64
+    assert f(*args(dh=130)) == 2
+    assert f(*args(L=0)) == 2
+    assert f(*args(q=None)) == 1
+    assert f(*args(q=ctypes.c_void_p(0x1008))) == 1        # not 16-byte aligned
+    assert f(*args(ws=None)) == 1
+    assert f(*args(wsb=16)) == 1                           # workspace too small
+    ws = lib.gdr_mla_decode_workspace_size
+    assert ws(2, 64, 100, 512, 128) > 0 and ws(2, 64, 100, 256, 128) == 0
+    assert ws(0, 64, 100, 512, 128) == 0
