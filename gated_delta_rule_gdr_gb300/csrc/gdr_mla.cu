@@ -181,12 +181,8 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t idesc_o = idesc_bf16(128, HG, true, true);    // O^T: C MN-major, P^T MN-major
             bool ok = role_wait(bar(B_Q), 0u, a.limit_ns, &s_abort);
             bool issued = false;
-            auto issue_s = [&](int j) -> bool {
+            auto issue_s = [&](int j) {
                 const int st = j & 1;
-                const bool w = partial(j) ? role_wait(bar(B_CREADY0 + st), 0u, a.limit_ns, &s_abort)
-                                          : role_wait(bar(B_CFULL0 + st), (uint32_t)(j >> 1) & 1u, a.limit_ns,
-                                                      &s_abort);
-                if (!w) return false;
                 tc_fence_after();
                 const uint64_t da = sdesc_sw128(cstage(st), 16, 1024);
                 const uint64_t db = sdesc_sw128(sbase + OFF_Q, 16, 1024);
@@ -196,14 +192,10 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                              sdesc_add(db, (kk >> 2) * SLAB + (kk & 3) * 32), idesc_s, kk > 0);
                 mma_commit(bar(B_SFULL0 + st));
                 issued = true;
-                return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < nt; ++j) {
-                if (j + 1 < nt && !issue_s(j + 1)) break;
-                if (!role_wait(bar(B_PREADY0 + (j & 1)), (uint32_t)(j >> 1) & 1u, a.limit_ns, &s_abort)) break;
-                tc_fence_after();
+            auto issue_pv = [&](int j) {
                 const int st = j & 1;
+                tc_fence_after();
                 const uint64_t dp = sdesc_sw128(sbase + OFF_P + (uint32_t)st * SLAB, 8192, 1024);
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
@@ -215,6 +207,43 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 mma_commit(bar(B_CFREE0 + st));
                 mma_commit(bar(B_PVDONE0 + st));
+            };
+            // Issue whichever product is ready: S^T of tile js once its tile has landed
+            // (and the softmax has read S^T(js - 2) from the same buffer, which it had
+            // when it published P(js - 2)), the second product of tile jp once the
+            // softmax has published P(jp).  Neither waits for the other's condition.
+            int js = 0, jp = 0;
+            uint64_t t_idle = 0;
+            while (ok && jp < nt) {
+                bool progress = false;
+                if (js < nt && js <= jp + 1) {
+                    const bool ready = partial(js) ? mbar_test_wait(bar(B_CREADY0 + (js & 1)), 0u)
+                                                   : mbar_test_wait(bar(B_CFULL0 + (js & 1)), (uint32_t)(js >> 1) & 1u);
+                    if (ready) {
+                        issue_s(js);
+                        ++js;
+                        progress = true;
+                    }
+                }
+                if (jp < js && mbar_test_wait(bar(B_PREADY0 + (jp & 1)), (uint32_t)(jp >> 1) & 1u)) {
+                    issue_pv(jp);
+                    ++jp;
+                    progress = true;
+                }
+                if (progress) {
+                    t_idle = 0;
+                    continue;
+                }
+                // nothing ready: a bounded wait, as every other wait
+                if (s_abort) break;
+                const uint64_t now = global_timer_ns();
+                if (t_idle == 0) t_idle = now;
+                if (a.limit_ns == 0 || now - t_idle > a.limit_ns) {
+                    s_abort = 1;
+                    atomicOr(&g_device_error_word, kDevErrTimeout);
+                    break;
+                }
+                __nanosleep(32);
             }
             if (s_abort && issued) {   // let this thread's MMAs land before TMEM goes away
                 mma_commit(bar(B_DRAIN));
@@ -239,17 +268,14 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (lane == 0) ok = role_wait(bar(b), parity, a.limit_ns, &s_abort);
             return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         };
-        // Every softmax thread passes every named barrier of an iteration; the loop is
-        // left only on a decision all 128 threads reduce together, so a failed wait in
-        // one warp (raising the abort flag) can never strand the others at a barrier.
+        // Every softmax thread passes the same named barriers in an iteration (the votes
+        // are reductions over all 128 threads, so all take the same branch); the loop is
+        // left only on such a vote, so a failed wait in one warp (raising the abort flag)
+        // can never strand the others at a barrier.
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
             const int sb = j & 1;
-            if (!named_and(BAR_SOFT, 128, ok && !s_abort)) {
-                ok = false;
-                break;
-            }
-            ok = warp_wait(B_SFULL0 + sb, (uint32_t)(j >> 1) & 1u);
+            ok = ok && warp_wait(B_SFULL0 + sb, (uint32_t)(j >> 1) & 1u);
             float v[32];
             if (ok) {
                 tc_fence_after();
@@ -259,55 +285,68 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool valid = ok && (tok0 + TT * j + r < len);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = valid ? v[i] * a.scale : -INFINITY;
-            {   // the tile's maximum per head: over this warp's 16 rows, then the four warps
-                float mx[32];
+            // Fast path: no score exceeds its head's reference maximum by more than TAU,
+            // so the reference stays and no reduction is needed (one vote).
+            bool exceed = j == 0;
+            if (j > 0)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx[i] = v[i];
-#pragma unroll
-                for (int off = 1; off < 16; off <<= 1)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
-                if ((lane & 15) == 0)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s_tmax[qd * 64 + 32 * hf + i] = mx[i];
-            }
-            named_sync(BAR_SOFT, 128);
-            bool need = false;
-            if (ts < 64) {
-                const float tm = fmaxf(fmaxf(s_tmax[ts], s_tmax[64 + ts]), fmaxf(s_tmax[128 + ts], s_tmax[192 + ts]));
-                const float mo = s_m[ts];
-                if (j == 0) {
-                    s_m[ts] = tm;           // O^T is written fresh by the first product
-                    s_alpha[ts] = 1.f;
-                } else if (tm > mo + TAU) {
-                    s_m[ts] = tm;
-                    s_alpha[ts] = __expf(mo - tm);
-                    need = true;
-                } else {
-                    s_alpha[ts] = 1.f;
+                for (int i = 0; i < 32; ++i) exceed |= v[i] > s_m[32 * hf + i] + TAU;
+            if (!named_and(BAR_SOFT, 128, ok && !s_abort && !exceed)) {
+                if (!named_and(BAR_SOFT, 128, ok && !s_abort)) {
+                    ok = false;
+                    break;
                 }
-            }
-            const bool rescale = !named_and(BAR_SOFT, 128, !need);
-            if (ok && rescale) {
-                // O^T may change only once the product of the previous tile has landed
-                ok = warp_wait(B_PVDONE0 + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u);
-                if (ok) {
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int b = 0; b < 4; ++b)
-#pragma unroll 1
-                        for (int cb = 0; cb < 2; ++cb) {
-                            float o[32];
-                            const uint32_t ta = tl + TM_O + (uint32_t)b * 64u + (uint32_t)cb * 32u;
-                            tmem_ld32(ta, o);
-                            tmem_wait_ld();
+                // the tile's maximum per head: over this warp's 16 rows, then the four warps
+                {
+                    float mx[32];
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= s_alpha[32 * cb + i];
-                            tmem_st32(ta, o);
-                        }
-                    tmem_wait_st();
+                    for (int i = 0; i < 32; ++i) mx[i] = v[i];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) lp[i] *= s_alpha[32 * hf + i];
+                    for (int off = 1; off < 16; off <<= 1)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
+                    if ((lane & 15) == 0)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s_tmax[qd * 64 + 32 * hf + i] = mx[i];
+                }
+                named_sync(BAR_SOFT, 128);
+                bool need = false;
+                if (ts < 64) {
+                    const float tm = fmaxf(fmaxf(s_tmax[ts], s_tmax[64 + ts]), fmaxf(s_tmax[128 + ts], s_tmax[192 + ts]));
+                    const float mo = s_m[ts];
+                    if (j == 0) {
+                        s_m[ts] = tm;           // O^T is written fresh by the first product
+                        s_alpha[ts] = 1.f;
+                    } else if (tm > mo + TAU) {
+                        s_m[ts] = tm;
+                        s_alpha[ts] = __expf(mo - tm);
+                        need = true;
+                    } else {
+                        s_alpha[ts] = 1.f;
+                    }
+                }
+                const bool rescale = !named_and(BAR_SOFT, 128, !need);
+                if (ok && rescale) {
+                    // O^T may change only once the product of the previous tile has landed
+                    ok = warp_wait(B_PVDONE0 + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u);
+                    if (ok) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int b = 0; b < 4; ++b)
+#pragma unroll 1
+                            for (int cb = 0; cb < 2; ++cb) {
+                                float o[32];
+                                const uint32_t ta = tl + TM_O + (uint32_t)b * 64u + (uint32_t)cb * 32u;
+                                tmem_ld32(ta, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) o[i] *= s_alpha[32 * cb + i];
+                                tmem_st32(ta, o);
+                            }
+                        tmem_wait_st();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) lp[i] *= s_alpha[32 * hf + i];
+                    }
                 }
             }
             // P buffer sb was last read by the product of tile j - 2
@@ -459,9 +498,11 @@ bool mla_supported(int H, int dc, int dh) {
 }
 
 int mla_splits(int N, int H, int Lmax) {
-    // Splits of each sequence's cache: enough CTAs for about two waves on the
-    // device, each split at least 8 tiles long (the split's partial result,
-    // 128 KB, is then at most a quarter of the latents it streams).
+    // Splits of each sequence's cache.  One CTA per (split, head group, sequence)
+    // fills an SM, so the step takes ceil(CTAs / SMs) rounds of ceil(tiles / S)
+    // tiles each; a split's partial result (128 KB written, then read by the merge)
+    // moves as many bytes as about four tiles.  The count minimising
+    // rounds x (tiles + 4) wins, which favours whole waves.
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -469,12 +510,18 @@ int mla_splits(int N, int H, int Lmax) {
         sms = 148;
     }
     const int64_t groups = (int64_t)N * (H / ml::HG);
-    const int tiles = (Lmax + ml::TT - 1) / ml::TT;
-    int64_t s = (2 * (int64_t)sms + groups - 1) / (groups > 0 ? groups : 1);
-    const int64_t cap = tiles / 8 > 0 ? tiles / 8 : 1;
-    if (s > cap) s = cap;
-    if (s > 64) s = 64;
-    return (int)(s < 1 ? 1 : s);
+    const int64_t tiles = (Lmax + ml::TT - 1) / ml::TT;
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= 64 && s <= tiles; ++s) {
+        const int64_t rounds = (groups * s + sms - 1) / sms;
+        const int64_t cost = rounds * ((tiles + s - 1) / s + 4);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
 }
 
 size_t mla_workspace_bytes(int N, int H, int Lmax) {
