@@ -594,6 +594,11 @@ def run_ours(args):
 
     main_w = WORKLOAD_ARG[args.workload]
     varlen = main_w is I.VARLEN
+    if main_w.steps == 0 and not varlen and (args.B or args.H or args.T):
+        # a smaller case of the same prefill workload (for profiling); the line names it
+        main_w = main_w.with_(B=args.B or main_w.B, H=args.H or main_w.H, T=args.T or main_w.T,
+                              name=f"{main_w.name} (B={args.B or main_w.B} H={args.H or main_w.H} "
+                                   f"T={args.T or main_w.T})")
 
     def barrier():
         rank_barrier(dist, torch.cuda.synchronize)
@@ -621,15 +626,15 @@ def run_ours(args):
             dec = bench_decode(gdr, I.DECODE, args.decode_steps, args.warmup, dev, flush, stream)
             barrier()
         bwd = None
-        if main_w is I.PREFILL and not args.no_backward:
+        if main_w == I.PREFILL and not args.no_backward:
             bwd = bench_backward(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
             barrier()
         mla = None
-        if main_w is I.PREFILL and not args.no_mla:
+        if main_w == I.PREFILL and not args.no_mla:
             mla = bench_mla(gdr, I.MLA_DECODE, max(3, args.steps // 2), 3, dev, stream)
             barrier()
         legs = {}
-        if main_w is I.PREFILL and not args.no_long:
+        if main_w == I.PREFILL and not args.no_long:
             for key, lw, k in (("long", I.LONG_PREFILL, max(3, args.steps // 2)),
                                ("million", I.MILLION_PREFILL, max(3, args.steps // 4))):
                 legs[key] = bench_prefill_leg(gdr, lw, k, 3, dev, stream)
@@ -869,6 +874,9 @@ def main():
                     help="skip the gated latent-attention decode leg")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the long (B1 H32 T65536) and million-token (B1 H16 T1048576) legs")
+    ap.add_argument("--B", type=int, default=0, help="override B of a prefill workload (profiling)")
+    ap.add_argument("--H", type=int, default=0, help="override H of a prefill workload (profiling)")
+    ap.add_argument("--T", type=int, default=0, help="override T of a prefill workload (profiling)")
     ap.add_argument("--single-launch", action="store_true",
                     help="the one-launch fused path (no workspace) instead of prep + chain")
     args = ap.parse_args()

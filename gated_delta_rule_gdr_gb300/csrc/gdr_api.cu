@@ -245,7 +245,6 @@ gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
     if (!a_min_ok(a_min)) return GDR_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return GDR_ERR_UNSUPPORTED;
     if (!range_ok(a_min, chunk)) return GDR_ERR_RANGE;
-    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return GDR_ERR_UNSUPPORTED;
     const int64_t SH = (int64_t)S * H;
     if (SH > 0x7fffffff || (int64_t)total_T * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -256,6 +255,10 @@ gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
         return from_cuda(gdr::launch_copy_state(init_state, final_state, SH * dk * dv, s));
     }
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype)))   // fp32 and the other shapes
+        return from_cuda(gdr::launch_onepass(q, k, v, g, beta, a_min, init_state, out, final_state,
+                                             (int)SH, 0, dk, dv, chunk, elem_of(dtype), s,
+                                             cu_seqlens, H, total_T));
     return from_cuda(gdr::launch_fused_varlen(q, k, v, g, beta, a_min, init_state, out,
                                               final_state, cu_seqlens, S, H, total_T, s));
 }

@@ -39,10 +39,13 @@ cudaError_t launch_staged(const void *q, const void *k, const void *v, const flo
 
 // ---- the prefill in one CUDA-core launch with no scratch (gdr_onepass.cu):
 // fp32, and every shape the tensor-core kernels do not take ----
+// cu_seqlens != nullptr: packed sequences (BH = S H states, tokens [total_T][H], as
+// gdr_chunk_fwd_varlen; T unused).
 cudaError_t launch_onepass(const void *q, const void *k, const void *v, const float *g,
                            const float *beta, float d, const float *init, void *out,
                            float *final_state, int BH, int T, int dk, int dv, int C, Elem e,
-                           cudaStream_t s);
+                           cudaStream_t s, const int *cu_seqlens = nullptr, int H = 0,
+                           int total_T = 0);
 
 // ---- process-wide options (gdr_set_option in gdr_api.cu) ----
 // Bound of every device-side wait in ns (0: every wait gives up at once, the

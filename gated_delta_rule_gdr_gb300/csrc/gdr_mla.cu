@@ -422,59 +422,99 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // Merge the splits of one (head, sequence), normalise, apply W_uv,h and the gate.
+// The splits' maxima and sums are staged first (one thread each), the partial sums
+// are read with several splits in flight per thread, and each warp takes four rows
+// of W_uv at a time, so that the loads overlap instead of following each other.
 __global__ void __launch_bounds__(128)
 mla_combine_kernel(const float *__restrict__ o_part, const float *__restrict__ ml_part,
                    const __nv_bfloat16 *__restrict__ w_uv, const float *__restrict__ gate,
                    __nv_bfloat16 *__restrict__ out, int H, int HGn, int S, int dh) {
     constexpr int DC = ml::DC;
     __shared__ float s_o[DC];
-    __shared__ float s_w[64];
+    __shared__ float s_w[64];   // e^(m_s - M), then the weight of split s
+    __shared__ float s_l[64];
+    __shared__ float s_inv;
     const int h = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
     const int hg = h / ml::HG, hl = h % ml::HG;
     const int64_t p0 = ((int64_t)n * HGn + hg) * S;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ml_part[((p0 + s) * ml::HG + hl) * 2]);
-    float lt = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 64) {
-        __syncthreads();
-        if (tid < 64 && s0 + tid < S) {
-            const float m = ml_part[((p0 + s0 + tid) * ml::HG + hl) * 2];
-            s_w[tid] = M == -INFINITY ? 0.f : __expf(m - M);
-        }
-        __syncthreads();
-        for (int s = s0; s < min(S, s0 + 64); ++s) lt += s_w[s - s0] * ml_part[((p0 + s) * ml::HG + hl) * 2 + 1];
-        for (int c = tid; c < DC; c += 128) {
-            float acc = s0 == 0 ? 0.f : s_o[c];
-            for (int s = s0; s < min(S, s0 + 64); ++s)
-                acc = fmaf(s_w[s - s0], o_part[((p0 + s) * ml::HG + hl) * DC + c], acc);
-            s_o[c] = acc;
-        }
+    if (tid < S) {
+        const float2 ml2 = *reinterpret_cast<const float2 *>(ml_part + ((p0 + tid) * ml::HG + hl) * 2);
+        s_w[tid] = ml2.x;
+        s_l[tid] = ml2.y;
     }
     __syncthreads();
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;   // an empty cache contributes zero
-    for (int c = tid; c < DC; c += 128) s_o[c] *= inv;
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int j = warp; j < dh; j += 4) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(w_uv + ((int64_t)h * dh + j) * DC) + 2 * lane;
-        float acc = 0.f;
+    if (tid < 32) {   // M, the split weights and 1 / (sum of the weights), one warp
+        float M = -INFINITY;
+        for (int s = tid; s < S; s += 32) M = fmaxf(M, s_w[s]);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const uint4 u = row[e];
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[k]));
-                const int c = 16 * lane + 8 * e + 2 * k;
-                acc = fmaf(f.x, s_o[c], fmaf(f.y, s_o[c + 1], acc));
-            }
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float lt = 0.f;
+        for (int s = tid; s < S; s += 32) {
+            const float w = M == -INFINITY ? 0.f : __expf(s_w[s] - M);
+            s_w[s] = w;
+            lt = fmaf(w, s_l[s], lt);
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            const int64_t idx = ((int64_t)n * H + h) * dh + j;
-            const float z = gate[idx];
-            out[idx] = __float2bfloat16_rn(acc / (1.f + __expf(-z)));
+        for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+        if (tid == 0) s_inv = lt > 0.f ? 1.f / lt : 0.f;   // an empty cache contributes zero
+    }
+    __syncthreads();
+    {
+        const float *src = o_part + (p0 * ml::HG + hl) * DC + tid;
+        const int64_t stride = (int64_t)ml::HG * DC;   // between splits
+        float acc[DC / 128] = {};
+        int s = 0;
+        for (; s + 4 <= S; s += 4) {
+            float x[4][DC / 128];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < DC / 128; ++e) x[u][e] = src[(s + u) * stride + 128 * e];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < DC / 128; ++e) acc[e] = fmaf(s_w[s + u], x[u][e], acc[e]);
+        }
+        for (; s < S; ++s)
+#pragma unroll
+            for (int e = 0; e < DC / 128; ++e) acc[e] = fmaf(s_w[s], src[s * stride + 128 * e], acc[e]);
+        const float inv = s_inv;
+#pragma unroll
+        for (int e = 0; e < DC / 128; ++e) s_o[tid + 128 * e] = acc[e] * inv;
+    }
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    float o16[16];   // this lane's latent values 16 lane .. 16 lane + 15
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o16[e] = s_o[16 * lane + e];
+    for (int j0 = 4 * warp; j0 < dh; j0 += 16) {   // rows j0 .. j0 + 3 of this warp
+        uint4 u[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int j = min(j0 + rr, dh - 1);
+            const uint4 *row = reinterpret_cast<const uint4 *>(w_uv + ((int64_t)h * dh + j) * DC) + 2 * lane;
+            u[rr][0] = row[0];
+            u[rr][1] = row[1];
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t w4[4] = {u[rr][e].x, u[rr][e].y, u[rr][e].z, u[rr][e].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[k]));
+                    acc = fmaf(f.x, o16[8 * e + 2 * k], fmaf(f.y, o16[8 * e + 2 * k + 1], acc));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const int j = j0 + rr;
+            if (lane == 0 && j < dh) {
+                const int64_t idx = ((int64_t)n * H + h) * dh + j;
+                out[idx] = __float2bfloat16_rn(acc / (1.f + __expf(-gate[idx])));
+            }
         }
     }
 }

@@ -53,15 +53,29 @@ __host__ __device__ inline size_t onepass_smem_floats(int dk, int C, int DS) {
            + 4 * (size_t)C;                  // gamma, 1/gamma, beta, gamma_C / gamma
 }
 
+// Packed sequences (cu_seqlens != nullptr): q, k, v, out [total_T][H][d], g, beta
+// [total_T][H], states [S][H][dk][dv]; blockIdx.y = s H + h.  Offsets are clamped
+// into [0, total_T], so a malformed array cannot take a CTA out of the tensors.
 template <typename TE>
 __global__ void __launch_bounds__(kThreads)
 onepass_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, float d,
                const float *init, TE *__restrict__ out, float *final_state, int T, int dk,
-               int dv, int C, int DS) {
+               int dv, int C, int DS, const int *__restrict__ cu_seqlens, int H, int total_T) {
     extern __shared__ float sm[];
     const int j0 = blockIdx.x * DS;
     const int64_t bh = blockIdx.y;
+    // token t of this (sequence, head): row (tbase + t * tstride) of q, k, v, out and
+    // element (tbase + t * tstride) of g, beta
+    int64_t tbase = bh * T, tstride = 1;
+    if (cu_seqlens) {
+        const int sq = (int)(bh / H), h = (int)(bh % H);
+        const int t0 = min(max(cu_seqlens[sq], 0), total_T);
+        const int t1 = min(max(cu_seqlens[sq + 1], t0), total_T);
+        T = t1 - t0;
+        tbase = (int64_t)t0 * H + h;
+        tstride = H;
+    }
     const int tid = threadIdx.x;
     const int ldk = dk + 1, ldc = C + 1;
     float *Ms = sm;                       // [dk][DS]
@@ -86,16 +100,16 @@ onepass_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__r
     const int NC = (T + C - 1) / C;
     for (int n = 0; n < NC; ++n) {
         const int t0 = n * C, c = min(C, T - t0);
-        const int64_t row0 = bh * T + t0;
+        auto row = [&](int r) { return tbase + (int64_t)(t0 + r) * tstride; };   // token t0 + r
         __syncthreads();   // the previous chunk is done with every buffer
         for (int x = tid; x < c * dk; x += kThreads) {
             const int r = x / dk, i = x % dk;
-            Ks[r * ldk + i] = ld_elem(k, (row0 + r) * dk + i);
-            Qs[r * ldk + i] = ld_elem(q, (row0 + r) * dk + i);
+            Ks[r * ldk + i] = ld_elem(k, row(r) * dk + i);
+            Qs[r * ldk + i] = ld_elem(q, row(r) * dk + i);
         }
         for (int x = tid; x < c * DS; x += kThreads) {
             const int r = x / DS, j = x % DS;
-            Vs[x] = ld_elem(v, (row0 + r) * dv + j0 + j);
+            Vs[x] = ld_elem(v, row(r) * dv + j0 + j);
         }
         if (tid < 32) {
             // chunk-local inclusive scan of log alpha; lane l owns rows l, l + 32
@@ -104,7 +118,7 @@ onepass_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__r
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int r = lane + 32 * e;
-                la[e] = (r < c) ? log_alpha(g[row0 + r], d) : 0.f;
+                la[e] = (r < c) ? log_alpha(g[row(r)], d) : 0.f;
                 incl[e] = la[e];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -120,7 +134,7 @@ onepass_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__r
                 if (r < c) {
                     gs[r] = expf(incl[e]);
                     ig[r] = expf(-incl[e]);
-                    bs[r] = beta[row0 + r];
+                    bs[r] = beta[row(r)];
                     sc[r] = expf(bC - incl[e]);
                 }
             }
@@ -184,7 +198,7 @@ onepass_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__r
             for (int i = 0; i < dk; ++i) qm = fmaf(Qs[r * ldk + i], Ms[i * DS + j], qm);
             float acc = gs[r] * qm;
             for (int s = 0; s <= r; ++s) acc = fmaf(Ps[r * ldc + s], Ws[s * DS + j], acc);
-            st_elem(out, (row0 + r) * dv + j0 + j, acc);
+            st_elem(out, row(r) * dv + j0 + j, acc);
         }
         __syncthreads();
 
@@ -211,8 +225,8 @@ onepass_kernel(const TE *__restrict__ q, const TE *__restrict__ k, const TE *__r
 cudaError_t launch_onepass(const void *q, const void *k, const void *v, const float *g,
                            const float *beta, float d, const float *init, void *out,
                            float *final_state, int BH, int T, int dk, int dv, int C, Elem e,
-                           cudaStream_t s) {
-    if (BH == 0 || T == 0) return cudaSuccess;
+                           cudaStream_t s, const int *cu_seqlens, int H, int total_T) {
+    if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;
     if (C > 64) return cudaErrorInvalidValue;   // the decay scan covers two rows per lane
     const int DS = dv < 32 ? dv : 32;
     const size_t smem = sizeof(float) * onepass_smem_floats(dk, C, DS);
@@ -225,7 +239,7 @@ cudaError_t launch_onepass(const void *q, const void *k, const void *v, const fl
             return err;
         onepass_kernel<float><<<grid, kThreads, smem, s>>>(
             (const float *)q, (const float *)k, (const float *)v, g, beta, d, init, (float *)out,
-            final_state, T, dk, dv, C, DS);
+            final_state, T, dk, dv, C, DS, cu_seqlens, H, total_T);
     } else {
         if ((err = cudaFuncSetAttribute(onepass_kernel<__nv_bfloat16>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -233,7 +247,8 @@ cudaError_t launch_onepass(const void *q, const void *k, const void *v, const fl
             return err;
         onepass_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g,
-            beta, d, init, (__nv_bfloat16 *)out, final_state, T, dk, dv, C, DS);
+            beta, d, init, (__nv_bfloat16 *)out, final_state, T, dk, dv, C, DS, cu_seqlens, H,
+            total_T);
     }
     return cudaGetLastError();
 }

@@ -209,10 +209,10 @@ gdr_status_t gdr_chunk_fwd_static(const void *q, const void *k, const void *v,
  * the prompts of several requests in one launch, no padding).  Same method,
  * per sequence and head, as gdr_chunk_fwd.
  *
- * q, k, v  bf16 [total_T][H][dk | dv], row-major, token-major: the tokens of
+ * q, k, v  dtype [total_T][H][dk | dv], row-major, token-major: the tokens of
  *          sequence s are cu_seqlens[s] .. cu_seqlens[s+1] - 1.
  * g, beta  fp32 [total_T][H].
- * out      bf16 [total_T][H][dv].
+ * out      dtype [total_T][H][dv].
  * init_state, final_state  fp32 [S][H][dk][dv] (init may be NULL = zeros,
  *          final may be NULL; they may alias).  The final states are directly
  *          the decode states of gdr_decode_step with N = S.
@@ -221,8 +221,11 @@ gdr_status_t gdr_chunk_fwd_static(const void *q, const void *k, const void *v,
  *          (that would need a copy).  Offsets outside [0, total_T] are clamped, so
  *          a malformed array gives wrong results but no out-of-bounds access.
  *          An empty sequence gets final = init.
- * Supported: bf16, dk = dv = 128, chunk = 64 (the fused kernels); anything
- * else returns GDR_ERR_UNSUPPORTED.  Other errors as gdr_chunk_fwd.
+ * Every shape and dtype of gdr_chunk_fwd: bf16 with dk = dv = 128 and chunk =
+ * 64 on the fused tensor-core kernels (and on the two-kernel path of
+ * gdr_chunk_fwd_varlen_ws), fp32 and the other shapes on the one-pass CUDA-core
+ * kernel (one CTA per sequence, head and 32 value columns).  One launch, no
+ * allocation.  Errors as gdr_chunk_fwd.
  */
 gdr_status_t gdr_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, float a_min, const float *init_state,
@@ -284,7 +287,9 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  *   gdr_chunk_fwd.
  * gdr_chunk_fwd_varlen_workspace_size / gdr_chunk_fwd_varlen_ws: the same for
  *   packed sequences; the workspace holds H * (total_T / 64 + S + 1) tiles
- *   (sequence s starts at tile total offset cu_seqlens[s] / 64 + s of its head).
+ *   (sequence s starts at tile total offset cu_seqlens[s] / 64 + s of its head);
+ *   the size is 0 (no workspace needed) for fp32 and the other shapes, which
+ *   gdr_chunk_fwd_varlen runs on the one-pass kernel.
  * gdr_chunk_fwd_ws_path: the path gdr_chunk_fwd_ws takes given a large enough
  *   workspace: 1 the staged kernels, 4 two kernels with two CTAs per head in
  *   the chain kernel (value columns split), 5 two kernels with one CTA per

@@ -159,9 +159,9 @@ def test_varlen_rejects(lib):
         ("out", P), ("fin", None), ("cu", P), ("S", 2), ("H", 2), ("tt", 100), ("dk", 128),
         ("dv", 128), ("chunk", 64), ("dtype", 1), ("stream", None))]
     assert f(*args(S=-1)) == 1                 # GDR_ERR_INVALID_ARG
-    assert f(*args(dtype=0)) == 2              # fp32: not on the fused path
-    assert f(*args(dk=64, dv=64)) == 2         # only dk = dv = 128
-    assert f(*args(chunk=32)) == 2             # only chunk 64
+    assert f(*args(dtype=2)) == 2              # unknown dtype
+    assert f(*args(dk=48)) == 2                # dimensions 16, 32, 64, 128 only
+    assert f(*args(chunk=48)) == 2             # chunks 16, 32, 64 only
     assert f(*args(a_min=0.2)) == 3            # range rule
     assert f(*args(cu=None)) == 1              # offsets required
     assert f(*args(q=None)) == 1

@@ -193,6 +193,41 @@ def test_varlen_packed_sequences(variant):
     assert gdr.last_device_error() == 0   # no bounded wait ran out (e.g. on the empty sequence)
 
 
+@pytest.mark.parametrize("dtype,d,C", [("f32", 64, 32), ("bf16", 64, 64), ("f32", 128, 16),
+                                       ("bf16", 32, 16)])
+def test_varlen_one_pass_kernel(dtype, d, C):
+    """Packed sequences of fp32 and of the shapes the tensor-core kernels do not take run
+    on the one-pass kernel: each sequence against the oracle on its own (fp32 at 1e-5),
+    an empty sequence keeps its initial state, and the final states feed a decode step."""
+    w = I.CORRECTNESS.with_(H=2, dk=d, dv=d, chunk=C, dtype=dtype, init_std=0.1)
+    lengths = [1, C - 1, C, 0, C + 1, 3 * C + 7, 130]
+    x = I.varlen_inputs(w, lengths, device="cuda")
+    out, fin = gdr.chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                                    x["cu_seqlens"], x["init_state"], chunk=C)
+    torch.cuda.synchronize()
+    cu = x["cu_seqlens"].tolist()
+    ref_fin = []
+    for s, xs in enumerate(x["seqs"]):
+        cpu = {n: (None if t is None else t.cpu()) for n, t in xs.items()}
+        if lengths[s] == 0:
+            ref_fin.append(cpu["init_state"][0].double())
+            assert torch.equal(fin[s], x["init_state"][s])
+            continue
+        ro, rf = oracle.fwd(cpu["q"], cpu["k"], cpu["v"], cpu["g"], cpu["beta"], w.a_min,
+                            cpu["init_state"])
+        got = out[cu[s]:cu[s + 1]].transpose(0, 1).unsqueeze(0).cpu()
+        assert rel(got, ro) <= TOL[dtype], (s, rel(got, ro))
+        assert rel(fin[s:s + 1].cpu(), rf) <= TOL[dtype]
+        ref_fin.append(torch.as_tensor(rf)[0])
+    nxt = I.decode_step_inputs(w.with_(B=len(lengths)), 0, device="cuda")
+    st = fin.clone()
+    o1 = gdr.decode_step(nxt["q"], nxt["k"], nxt["v"], nxt["g"], nxt["beta"], w.a_min, st)
+    torch.cuda.synchronize()
+    ref_st = torch.stack(ref_fin, 0).numpy().copy()
+    r1 = oracle.decode(*(nxt[n].cpu() for n in ("q", "k", "v", "g", "beta")), w.a_min, ref_st)
+    assert rel(o1.cpu(), r1) <= TOL[dtype]
+
+
 # ------------------------------------------------------------------ the log-domain decay
 # The pages' own bound, log alpha = g_min sigmoid(g) (g_min = -5 on 16-token chunks), on
 # the staged kernels; a floor that chunk 64 allows (g_min = -1.25) on the four kernels of
