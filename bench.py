@@ -466,6 +466,41 @@ def bench_backward(gdr, w, K, W, dev, flush, stream):
     return time_steps(step, K, W, flush, stream), nws
 
 
+def bench_training(gdr, w, K, W, dev, flush, stream):
+    """One training step of the prefill workload: the forward that saves its chunk states
+    (gdr_chunk_fwd_train) and the backward that reads them (gdr_chunk_bwd_saved); each
+    half is also timed alone."""
+    x = I.prefill_inputs(w, device=dev)
+    ct = I.cotangents(w, device=dev)
+    td = w.torch_dtype()
+    wsf = torch.empty(max(gdr.chunk_fwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk, td), 16),
+                      dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(gdr.chunk_bwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk, td), 16),
+                      dtype=torch.uint8, device=dev)
+    nsv = gdr.chunk_saved_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk, td)
+    saved = torch.empty(max(nsv, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev)
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+
+    def fwd(_):
+        gdr.chunk_fwd_train(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                            out=out, final_state=fin, workspace=wsf, saved=saved)
+
+    def bwd(_):
+        gdr.chunk_bwd_saved(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"],
+                            ct["d_out"], saved, ct["d_final"], workspace=wsb)
+
+    def step(i):
+        fwd(i)
+        bwd(i)
+
+    ms = time_steps(step, K, W, flush, stream)
+    ms_f = time_steps(fwd, K, W, flush, stream)
+    ms_b = time_steps(bwd, K, W, flush, stream)
+    path = gdr.chunk_fwd_path(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.a_min, td, workspace=True)
+    return ms, ms_f, ms_b, nsv, (4 if path == 7 else 2) + 4
+
+
 def cpu_baseline_backward(w, budget_s=8.0):
     """The fp64 oracle's backward on a bounded sample of the prefill workload: all
     heads of sequence 0 over the first T_s tokens, T_s grown until ~budget_s."""
@@ -629,6 +664,10 @@ def run_ours(args):
         if main_w == I.PREFILL and not args.no_backward:
             bwd = bench_backward(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
             barrier()
+        train = None
+        if main_w == I.PREFILL and not args.no_backward:
+            train = bench_training(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
+            barrier()
         mla = None
         if main_w == I.PREFILL and not args.no_mla:
             mla = bench_mla(gdr, I.MLA_DECODE, max(3, args.steps // 2), 3, dev, stream)
@@ -745,6 +784,24 @@ def run_ours(args):
                                                       main_w.name),
                          "algorithmic_bytes": bby},
             "workspace_bytes": bws, "gpu_launches": 4 * len(bms),
+        }
+    if train is not None:
+        tms, tfm, tbm, tsv, tnk = train
+        tmean = statistics.mean(tms)
+        tby = prefill_algorithmic(main_w)[0] + backward_algorithmic(main_w)
+        tgbs = tby / (tmean * 1e-3) / 1e9
+        line["training"] = {
+            "metric": "training tokens/s", "workload": main_w.name,
+            "what": "forward saving its chunk states + backward reading them, per step",
+            "value": round(world * main_w.B * main_w.T / (max_over_ranks(tmean) * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(tmean, 4), "steps": len(tms),
+            "forward_ms": round(statistics.mean(tfm), 4),
+            "backward_ms": round(statistics.mean(tbm), 4),
+            "roofline": {"bound": "hbm", "achieved": round(tgbs, 1), "peak": pk["hbm_gbs"],
+                         "peak_kind": pk_kind, "unit": "GB/s",
+                         "frac": round(tgbs / pk["hbm_gbs"], 4), "algorithmic_bytes": tby,
+                         "traffic": None},
+            "saved_bytes": tsv, "gpu_launches": tnk * len(tms),
         }
     if mla is not None:
         wm = I.MLA_DECODE

@@ -28,7 +28,9 @@ __all__ = ["GdrError", "load", "chunk_fwd", "decode_step", "chunk_decay", "chunk
            "chunk_state", "chunk_output", "chunk_fwd_kernels", "chunk_fwd_path", "chunk_fwd_varlen",
            "chunk_fwd_workspace_size", "chunk_fwd_varlen_workspace_size", "last_device_error",
            "status_string", "version", "library_path", "STATUS", "PATHS", "OPTIONS",
-           "set_option", "get_option", "option", "mla_decode", "mla_decode_workspace_size"]
+           "set_option", "get_option", "option", "mla_decode", "mla_decode_workspace_size",
+           "chunk_bwd", "chunk_bwd_workspace_size", "chunk_saved_size", "chunk_fwd_train",
+           "chunk_bwd_saved"]
 
 DECAY = {"affine": 0, "log": 1}   # gdr_decay_t
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_RANGE",
@@ -76,6 +78,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "gdr_chunk_fwd_host": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp],
         "gdr_chunk_bwd": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                           i, i, i, i, i, i, i, vp, sz, vp],
+        "gdr_chunk_fwd_train": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, i, i, i, i, i, i, i, vp, sz,
+                                vp, sz, vp],
+        "gdr_chunk_bwd_saved": [vp, vp, vp, vp, vp, i, f, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                i, i, i, i, i, i, i, vp, sz, vp, sz, vp],
         "gdr_chunk_fwd_varlen": [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_chunk_fwd_static": [vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, i, i, vp],
         "gdr_decode_step": [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp],
@@ -96,7 +102,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         fn.argtypes = args
         fn.restype = ctypes.c_int
     for name in ("gdr_chunk_fwd_workspace_size", "gdr_chunk_fwd_varlen_workspace_size",
-                 "gdr_chunk_bwd_workspace_size", "gdr_chunk_fwd_host_buffer_size"):
+                 "gdr_chunk_bwd_workspace_size", "gdr_chunk_fwd_host_buffer_size",
+                 "gdr_chunk_saved_size"):
         fn = getattr(lib, name)
         fn.argtypes = [i, i, i, i, i, i, i]
         fn.restype = sz
@@ -335,6 +342,79 @@ def chunk_bwd(q, k, v, g, beta, a_min: float, init_state, d_out, d_final=None, *
                              _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db), _ptr(dinit),
                              B, H, T, dk, dv, int(chunk), DTYPE[q.dtype], _ptr(workspace),
                              workspace.numel(), _stream(q.device)), "gdr_chunk_bwd")
+    return dq, dk_, dv_, dg, db, dinit
+
+
+def chunk_saved_size(B, H, T, dk, dv, chunk=64, dtype=torch.bfloat16) -> int:
+    """Bytes of the buffer chunk_fwd_train fills for chunk_bwd_saved (0: not supported)."""
+    return int(load().gdr_chunk_saved_size(B, H, T, dk, dv, chunk, DTYPE[dtype]))
+
+
+def chunk_fwd_train(q, k, v, g, beta, a_min: float, init_state=None, *, chunk: int = 64,
+                    out=None, final_state=None, want_final: bool = True, workspace=None,
+                    saved=None, decay: str = "affine"):
+    """chunk_fwd (bf16, d = 128, chunk 64, two-kernel path) that also keeps every chunk's
+    state and W tile for chunk_bwd_saved.  workspace / saved: None (allocated here) or
+    uint8 CUDA tensors of at least chunk_fwd_workspace_size / chunk_saved_size bytes.
+    Returns (out, final_state, saved)."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(init_state, "init_state")
+    if decay not in DECAY:
+        raise ValueError(f"unknown decay {decay!r}")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and want_final:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need_ws = chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, q.dtype)
+    need_sv = chunk_saved_size(B, H, T, dk, dv, chunk, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need_ws, 16), dtype=torch.uint8, device=q.device)
+    if saved is None:
+        saved = torch.empty(max(need_sv, 16), dtype=torch.uint8, device=q.device)
+    for name, t, need in (("workspace", workspace, need_ws), ("saved", saved, need_sv)):
+        if t.dtype != torch.uint8 or t.numel() < need:
+            raise ValueError(f"{name} must be a uint8 tensor of at least {need} bytes")
+    _check(lib.gdr_chunk_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), DECAY[decay],
+                                   float(a_min), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                   B, H, T, dk, dv, int(chunk), DTYPE[q.dtype], _ptr(workspace),
+                                   workspace.numel(), _ptr(saved), saved.numel(),
+                                   _stream(q.device)), "gdr_chunk_fwd_train")
+    return out, final_state, saved
+
+
+def chunk_bwd_saved(q, k, v, g, beta, a_min: float, init_state, d_out, saved, d_final=None, *,
+                    chunk: int = 64, want_dinit: bool = True, workspace=None,
+                    decay: str = "affine"):
+    """chunk_bwd reading the states chunk_fwd_train saved (same arguments as that
+    forward) instead of recomputing them.  Returns (dq, dk, dv, dg, dbeta, dinit)."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in DTYPE or k.dtype != q.dtype or v.dtype != q.dtype or d_out.dtype != q.dtype:
+        raise TypeError("q, k, v, d_out must share one dtype")
+    _f32(g, "g"), _f32(beta, "beta"), _f32(init_state, "init_state"), _f32(d_final, "d_final")
+    if decay not in DECAY:
+        raise ValueError(f"unknown decay {decay!r}")
+    if saved.dtype != torch.uint8 or not saved.is_cuda:
+        raise ValueError("saved must be the uint8 CUDA tensor chunk_fwd_train filled")
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg, db = torch.empty_like(g), torch.empty_like(beta)
+    dinit = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dinit else None
+    need = chunk_bwd_workspace_size(B, H, T, dk, dv, chunk, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    _check(lib.gdr_chunk_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), DECAY[decay],
+                                   float(a_min), _ptr(init_state), _ptr(d_out), _ptr(d_final),
+                                   _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db),
+                                   _ptr(dinit), B, H, T, dk, dv, int(chunk), DTYPE[q.dtype],
+                                   _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
+                                   _stream(q.device)), "gdr_chunk_bwd_saved")
     return dq, dk_, dv_, dg, db, dinit
 
 

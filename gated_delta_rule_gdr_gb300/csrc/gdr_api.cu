@@ -292,6 +292,11 @@ size_t gdr_chunk_fwd_varlen_workspace_size(int S, int H, int total_T, int dk, in
 
 namespace {
 
+gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float a_min, const float *init_state, void *out,
+                            float *final_state, int BH, int T, void *workspace, void *saved,
+                            cudaStream_t s);
+
 gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, const float *g,
                                const float *beta, float a_min, const float *init_state, void *out,
                                float *final_state, int B, int H, int T, int dk, int dv, int chunk,
@@ -312,15 +317,24 @@ gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, cons
     }
     if (!range_ok(a_min, kTile)) return GDR_ERR_RANGE;
     if ((int64_t)T * B * H > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    return two_kernel_fwd(q, k, v, g, beta, a_min, init_state, out, final_state, B * H, T,
+                          workspace, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+// The two-kernel path (dense, arguments checked): the preparation, the segment states when
+// the sequence is cut into segments, the chain; saved != nullptr also writes the states and
+// W tiles the saved-state backward reads.
+gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float a_min, const float *init_state, void *out,
+                            float *final_state, int BH, int T, void *workspace, void *saved,
+                            cudaStream_t s) {
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int BH = B * H;
     const int S = gdr::segment_count(BH, T);
     cudaError_t e = gdr::launch_prep(q, k, g, beta, a_min, workspace, BH, T, nullptr, 0, 0, s);
     if (S <= 1) {
         if (e == cudaSuccess)
             e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace,
-                                  BH, T, nullptr, 0, 0, s);
+                                  BH, T, nullptr, 0, 0, s, 1, nullptr, saved);
         return from_cuda(e);
     }
     // sequence segments: their maps and the scan, then every segment's chain at once
@@ -331,7 +345,7 @@ gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, cons
                                        S, s);
     if (e == cudaSuccess)
         e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace, BH,
-                              T, nullptr, 0, 0, s, S, gdr::segment_states(seg_ws, BH, S));
+                              T, nullptr, 0, 0, s, S, gdr::segment_states(seg_ws, BH, S), saved);
     return from_cuda(e);
 }
 
@@ -537,6 +551,78 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
     return from_cuda(gdr::launch_bwd(q, k, v, g, beta, d, init_state, d_out, d_final, d_q, d_k,
                                      d_v, d_g, d_beta, d_init, (int)BH, T, dk, dv, chunk,
                                      workspace, elem_of(dtype), s));
+}
+
+// ---- training: the forward saves its chunk states, the backward reads them ----
+
+size_t gdr_chunk_saved_size(int B, int H, int T, int dk, int dv, int chunk, gdr_dtype_t dtype) {
+    if (B < 0 || H < 0 || T <= 0 || !dtype_ok(dtype)) return 0;
+    if (!gdr::fused_supported(dk, dv, chunk, elem_of(dtype))) return 0;
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0 || BH > 0x7fffffff || (int64_t)T * BH > ((int64_t)1 << 40)) return 0;
+    return gdr::saved_bytes(BH, T);
+}
+
+gdr_status_t gdr_chunk_fwd_train(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, gdr_decay_t decay, float bound,
+                                 const float *init_state, void *out, float *final_state, int B,
+                                 int H, int T, int dk, int dv, int chunk, gdr_dtype_t dtype,
+                                 void *workspace, size_t workspace_bytes, void *saved,
+                                 size_t saved_bytes, void *stream) {
+    float d = 0.0f;
+    if (B < 0 || H < 0 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (!decay_param(decay, bound, &d)) return GDR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || !gdr::fused_supported(dk, dv, chunk, elem_of(dtype)))
+        return GDR_ERR_UNSUPPORTED;
+    const int64_t BH = (int64_t)B * H;
+    if (BH > 0x7fffffff || (int64_t)T * BH > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (BH == 0 || T == 0)   // nothing to save: the final state is the initial one
+        return chunk_fwd_impl(q, k, v, g, beta, d, init_state, out, final_state, B, H, T, dk, dv,
+                              chunk, dtype, stream);
+    if (!range_ok(d, kTile)) return GDR_ERR_RANGE;
+    const size_t need = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+        return GDR_ERR_INVALID_ARG;
+    if (!saved || saved_bytes < gdr::saved_bytes(BH, T) ||
+        (reinterpret_cast<uintptr_t>(saved) & 15))
+        return GDR_ERR_INVALID_ARG;
+    return two_kernel_fwd(q, k, v, g, beta, d, init_state, out, final_state, (int)BH, T,
+                          workspace, saved, static_cast<cudaStream_t>(stream));
+}
+
+gdr_status_t gdr_chunk_bwd_saved(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, gdr_decay_t decay, float bound,
+                                 const float *init_state, const void *d_out, const float *d_final,
+                                 void *d_q, void *d_k, void *d_v, float *d_g, float *d_beta,
+                                 float *d_init, int B, int H, int T, int dk, int dv, int chunk,
+                                 gdr_dtype_t dtype, const void *saved, size_t saved_bytes,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+    if (!dtype_ok(dtype) || !gdr::fused_supported(dk, dv, chunk, elem_of(dtype)))
+        return GDR_ERR_UNSUPPORTED;
+    const int64_t BH = (int64_t)B * H;
+    if (B < 0 || H < 0 || T < 0 || BH == 0 || T == 0)   // no chunk: nothing was saved
+        return gdr_chunk_bwd(q, k, v, g, beta, decay, bound, init_state, d_out, d_final, d_q, d_k,
+                             d_v, d_g, d_beta, d_init, B, H, T, dk, dv, chunk, dtype, workspace,
+                             workspace_bytes, stream);
+    float d = 0.0f;
+    if (!decay_param(decay, bound, &d)) return GDR_ERR_INVALID_ARG;
+    if (!range_ok(d, chunk)) return GDR_ERR_RANGE;
+    if (BH > 0x7fffffff || (int64_t)T * BH > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !g || !beta || !d_out || !d_q || !d_k || !d_v || !d_g || !d_beta)
+        return GDR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(d_out) |
+         reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_k) |
+         reinterpret_cast<uintptr_t>(d_v) | reinterpret_cast<uintptr_t>(saved)) & 15)
+        return GDR_ERR_INVALID_ARG;
+    if (!saved || saved_bytes < gdr::saved_bytes(BH, T)) return GDR_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < gdr::bwd_workspace_bytes((int)BH, T, dk, dv, chunk) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15))
+        return GDR_ERR_INVALID_ARG;
+    return from_cuda(gdr::launch_bwd(q, k, v, g, beta, d, init_state, d_out, d_final, d_q, d_k,
+                                     d_v, d_g, d_beta, d_init, (int)BH, T, dk, dv, chunk,
+                                     workspace, elem_of(dtype), static_cast<cudaStream_t>(stream),
+                                     saved));
 }
 
 // ---- gated multi-head latent attention, one decode step ----

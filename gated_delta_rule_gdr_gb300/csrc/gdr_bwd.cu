@@ -1567,7 +1567,7 @@ __global__ void __launch_bounds__(256, 2)
 bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
                      const float *__restrict__ beta, __nv_bfloat16 *__restrict__ TPb,
-                     float *__restrict__ U, __nv_bfloat16 *__restrict__ Wk2, int T) {
+                     float *__restrict__ U, __nv_bfloat16 *__restrict__ Wk2, int T, int want_uw) {
     using namespace mt;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1693,6 +1693,9 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
             *reinterpret_cast<uint2 *>(Tb + r * C + s) =
                 make_uint2(pack_bf2(tv[u].x, tv[u].y), pack_bf2(tv[u].z, tv[u].w));
         }
+        // U and Wk feed only the forward-state recomputation, which saved states replace
+        // (want_uw is uniform over the CTA: every thread leaves here together)
+        if (!want_uw) return;
         __syncthreads();   // T is read: region 2 takes T diag(beta gamma)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -2112,12 +2115,14 @@ bwd_passes_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                      const __nv_bfloat16 *__restrict__ Wk2, const __nv_bfloat16 *__restrict__ TPb,
                      const float *init, const float *dfinal, __nv_bfloat16 *__restrict__ Wt,
                      __nv_bfloat16 *__restrict__ Sb, float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb,
-                     float *dinit, int T, int dv) {
+                     float *dinit, int T, int dv, int fwd_role) {
     extern __shared__ __align__(16) uint8_t smb[];
     const int tid = threadIdx.x;
-    if (tid < vc::NT)
-        fwd_state_pass(smb, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
-    else
+    // fwd_role = 0: the forward saved W^T and the states; only the reverse chain runs (the
+    // two roles share no barrier, so the first four warps simply leave)
+    if (tid < vc::NT) {
+        if (fwd_role) fwd_state_pass(smb, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
+    } else
         chain_pass(smb + 2 * vc::F_STAGE, tid - vc::NT, 2, q, k, gamma, beta, dout, dfinal, TPb, dR, dSb,
                    dinit, T, dv);
 }
@@ -2146,7 +2151,8 @@ template <typename TE>
 cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, const float *beta,
                          float d, const float *init, const TE *dout, const float *dfinal, TE *dq,
                          TE *dk_out, TE *dv_out, float *dg, float *dbeta, float *dinit,
-                         int BH, int T, int dk, int dv, int C, float *ws, Elem e, cudaStream_t s) {
+                         int BH, int T, int dk, int dv, int C, float *ws, Elem e, cudaStream_t s,
+                         const void *saved) {
     const int NC = (T + C - 1) / C;
     const size_t tok = (size_t)BH * T, st = (size_t)BH * NC * dk * dv;
     (void)e;
@@ -2176,12 +2182,14 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             __nv_bfloat16 *Sbb = reinterpret_cast<__nv_bfloat16 *>(Mn);   // bf16 value-major states
             __nv_bfloat16 *dSbb = reinterpret_cast<__nv_bfloat16 *>(dMn1);
             if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
-            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T);
+            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T,
+                                                                     saved ? 0 : 1);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE;
             if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
             bwd_passes_vc_kernel<<<dim3(dv / vc::DSC, BH), 2 * vc::NT, sp, s>>>(
-                q, k, dout, gamma, beta, U, Wk2, TPb, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv);
+                q, k, dout, gamma, beta, U, Wk2, TPb, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv,
+                saved ? 0 : 1);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {
@@ -2224,9 +2232,15 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             if ((err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
                 return err;
             const int ntask = NC * BH, grid = ntask < nsm ? ntask : nsm;
+            // the states and W^T: the forward's saved tiles, or the ones just recomputed
+            const __nv_bfloat16 *Sb_in = saved ? static_cast<const __nv_bfloat16 *>(saved)
+                                               : reinterpret_cast<const __nv_bfloat16 *>(Mn);
+            const __nv_bfloat16 *Wt_in =
+                saved ? reinterpret_cast<const __nv_bfloat16 *>(static_cast<const uint8_t *>(saved) +
+                                                               saved_state_bytes(BH, T))
+                      : reinterpret_cast<const __nv_bfloat16 *>(W);
             bwd_chunk_mma_kernel<<<grid, 256, mm::SMEM, s>>>(
-                q, k, v, g, beta, d, gamma, reinterpret_cast<const __nv_bfloat16 *>(W),
-                reinterpret_cast<const __nv_bfloat16 *>(Mn), dout, dR,
+                q, k, v, g, beta, d, gamma, Wt_in, Sb_in, dout, dR,
                 reinterpret_cast<const __nv_bfloat16 *>(dMn1), dq, dk_out, dv_out, dg, dbeta, T, BH);
             return cudaGetLastError();
         }
@@ -2255,11 +2269,19 @@ size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C) {
                             3 * round4((size_t)BH * NC * C * C));
 }
 
+bool bwd_saved_shape(int dk, int dv, int C, Elem e, const void *dq, const void *dk_out,
+                     const void *dv_out) {
+    return e == Elem::BF16 && dk == 128 && dv == 128 && C == 64 &&
+           ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk_out) |
+             reinterpret_cast<uintptr_t>(dv_out)) & 15) == 0;
+}
+
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const float *g,
                        const float *beta, float d, const float *init, const void *dout,
                        const float *dfinal, void *dq, void *dk_out, void *dv_out, float *dg,
                        float *dbeta, float *dinit, int BH, int T, int dk, int dv, int C,
-                       void *ws, Elem e, cudaStream_t s) {
+                       void *ws, Elem e, cudaStream_t s, const void *saved) {
+    if (saved && !bwd_saved_shape(dk, dv, C, e, dq, dk_out, dv_out)) return cudaErrorInvalidValue;
     if (BH == 0) return cudaSuccess;
     if (T == 0) {   // no tokens: dinit = dfinal
         if (!dinit) return cudaSuccess;
@@ -2272,11 +2294,12 @@ cudaError_t launch_bwd(const void *q, const void *k, const void *v, const float 
     if (e == Elem::F32)
         return launch_bwd_t<float>((const float *)q, (const float *)k, (const float *)v, g, beta, d,
                                    init, (const float *)dout, dfinal, (float *)dq, (float *)dk_out,
-                                   (float *)dv_out, dg, dbeta, dinit, BH, T, dk, dv, C, w, e, s);
+                                   (float *)dv_out, dg, dbeta, dinit, BH, T, dk, dv, C, w, e, s,
+                                   nullptr);
     return launch_bwd_t<__nv_bfloat16>(
         (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g, beta, d,
         init, (const __nv_bfloat16 *)dout, dfinal, (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk_out,
-        (__nv_bfloat16 *)dv_out, dg, dbeta, dinit, BH, T, dk, dv, C, w, e, s);
+        (__nv_bfloat16 *)dv_out, dg, dbeta, dinit, BH, T, dk, dv, C, w, e, s, saved);
 }
 
 }  // namespace gdr

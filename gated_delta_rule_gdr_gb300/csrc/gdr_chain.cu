@@ -158,6 +158,7 @@ template <int DVH>
 __global__ void __launch_bounds__(ChainCfg<DVH>::NT, 1)
 chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+             const __grid_constant__ CUtensorMap tm_sm, const __grid_constant__ CUtensorMap tm_sw,
              const FusedArgs a, const uint8_t *ws,
              int64_t nslot) {
     using Cfg = ChainCfg<DVH>;
@@ -478,6 +479,16 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (lane == 0) {
             const uint32_t idesc_o = idesc_bf16(128, DVH, false, false);   // K-major A and B
             bool issued = false;
+            // saving: chunk n's tiles go to row x(n) of the saved tensors (value columns J)
+            const int64_t x0 = (int64_t)sv.z * ((a.T + C - 1) / C) + sv.tz / C;
+            auto save_ms = [&](int n) {   // M_n^T: 2 slabs of 64 key columns, DVH value rows
+                const uint32_t ms = sbase + Cfg::OFF_MS + (uint32_t)(n % Cfg::MSB) * 2 * Cfg::MS_SLAB;
+                tma_store_3d(&tm_sm, ms, 0, j0, (int)(x0 + n));
+                tma_store_3d(&tm_sm, ms + Cfg::MS_SLAB, 64, j0, (int)(x0 + n));
+            };
+            auto save_w = [&](int n) {    // W_n^T: DVH value rows of 64 tokens
+                tma_store_3d(&tm_sw, sbase + Cfg::OFF_WT + (uint32_t)(n & 1) * Cfg::WT_BYTES, 0, j0, (int)(x0 + n));
+            };
             // Iteration m: [Lb;P] W_{m-1} fills chunk m-1's second accumulator (rows
             // 64-127: P W), then [K;Q] MS_m chunk m's first (rows 64-127: Q M_m)
             for (int m = 0; m <= NC && NC > 0; ++m) {
@@ -493,7 +504,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                  sdesc_add(dw, kk * 32), idesc_o, kk > 0);
                     mma_commit(bar(B_OFULL0 + (n & 1)));
                 }
-                if (m == NC) break;
+                if (m == NC) {
+                    if (a.save) {
+                        save_w(m - 1);
+                        bulk_commit();
+                    }
+                    break;
+                }
                 // O(m) = [K;Q] MS_m, once the accumulator buffer has been read out (chunk m-2)
                 bool ok = role_wait(bar(B_FULL0 + m % NST), (uint32_t)(m / NST) & 1u, a.limit_ns, &s_abort);
                 if (ok && m > 1)
@@ -509,6 +526,14 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         mma_bf16(tmem + (uint32_t)(m & 1) * DVH, sdesc_add(da, (kk >> 2) * 16384 + (kk & 3) * 32),
                                  sdesc_add(db, (kk >> 2) * Cfg::MS_SLAB + (kk & 3) * 32), idesc_o, kk > 0);
                 }
+                if (a.save) {
+                    // the tiles the two products just read, before their buffers are released:
+                    // the stores must have read them before the commits below
+                    save_ms(m);
+                    if (m > 0) save_w(m - 1);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
                 mma_commit(bar(B_QMS));
                 // chunk m+1 may overwrite W[(m+1) % 2] (read by W_{m-1}'s product) and
                 // MS[m % 2] once both products issued so far are done
@@ -519,6 +544,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mma_commit(bar(B_DRAIN));
                 mbar_wait(bar(B_DRAIN), 0u, kCleanupLimitNs);
             }
+            if (a.save) bulk_wait_all();   // the saved tiles are written before the CTA leaves
         }
         __syncwarp();
     } else if (warp >= NCH + 2) {
@@ -650,7 +676,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
 template <int DVH>
 cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mo, const FusedArgs &a, const void *ws, int64_t nslot, int BH, cudaStream_t s) {
+                           const CUtensorMap &mo, const CUtensorMap &msm, const CUtensorMap &msw,
+                           const FusedArgs &a, const void *ws, int64_t nslot, int BH, cudaStream_t s) {
     using Cfg = ChainCfg<DVH>;
     cudaError_t e = cudaFuncSetAttribute(chain_kernel<DVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::SMEM_ALLOC);
@@ -668,8 +695,8 @@ cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chain_kernel<DVH>, mq, mk, mv, mo, a, static_cast<const uint8_t *>(ws),
-                              nslot);
+    return cudaLaunchKernelEx(&cfg, chain_kernel<DVH>, mq, mk, mv, mo, msm, msw, a,
+                              static_cast<const uint8_t *>(ws), nslot);
 }
 
 }  // namespace
@@ -689,10 +716,24 @@ int chain_split(int BH) {
     return 2 * BH <= sms ? 2 : 1;
 }
 
+// A bf16 [rows][n][inner] tensor viewed as 3-D for 64 x box_rows tensor stores with the
+// 128-byte swizzle (the smem tile's layout), so that the global copy is row-major.
+bool make_map_saved(CUtensorMap *m, void *ptr, int inner, int n, int64_t rows, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)n, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * n * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
                          int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
-                         int nseg, const float *seg_init) {
+                         int nseg, const float *seg_init, void *saved) {
     if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;   // callers copy the state
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
          reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(ws)) & 15)
@@ -715,8 +756,19 @@ cudaError_t launch_chain(const void *q, const void *k, const void *v, const floa
         a.seg_init = seg_init;
     }
     const int views = BH * a.nseg;
-    return chain_split(views) == 2 ? launch_chain_t<64>(mq, mk, mv, mo, a, ws, nslot, views, s)
-                                   : launch_chain_t<128>(mq, mk, mv, mo, a, ws, nslot, views, s);
+    const int split = chain_split(views);
+    CUtensorMap msm = mo, msw = mo;   // placeholders when nothing is saved
+    if (saved) {
+        if (cu_seqlens || (reinterpret_cast<uintptr_t>(saved) & 15)) return cudaErrorInvalidValue;
+        const int64_t xs = (int64_t)BH * ((T + C - 1) / C);   // (head, chunk) tiles
+        uint8_t *sb = static_cast<uint8_t *>(saved);
+        if (!make_map_saved(&msm, sb, D, D, xs, 128 / split) ||
+            !make_map_saved(&msw, sb + saved_state_bytes(BH, T), C, D, xs, 128 / split))
+            return cudaErrorInvalidValue;
+        a.save = 1;
+    }
+    return split == 2 ? launch_chain_t<64>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s)
+                      : launch_chain_t<128>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s);
 }
 
 cudaError_t take_chain_error_word(unsigned *value) { return take_error_word(value); }

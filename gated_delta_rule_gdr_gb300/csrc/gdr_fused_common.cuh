@@ -377,6 +377,9 @@ struct FusedArgs {
     // segment only, writes the head's final state.
     int nseg = 1, seg_chunks = 0;
     const float *seg_init = nullptr;
+    // Saving for the backward (the two-kernel chain, dense layout): every chunk's state
+    // M_n^T and W_n^T leave as value-major bf16 tiles through two tensor maps.
+    int save = 0;
 };
 
 // Where the tokens of the (sequence, head) with state index bh live.  Token t

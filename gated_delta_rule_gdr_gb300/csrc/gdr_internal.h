@@ -62,11 +62,16 @@ int opt_segments();
 // ---- backward of the chunked form (gdr_bwd.cu) ----
 bool bwd_supported(int dk, int dv, int C);
 size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C);
+// saved != nullptr: the states and W^T saved by the forward (launch_chain's saved
+// buffer); the forward-state recomputation is skipped.  Only the bf16 d = 128 chunk-64
+// shape with 16-byte aligned d_q, d_k, d_v (bwd_saved_shape).
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const float *g,
                        const float *beta, float d, const float *init, const void *dout,
                        const float *dfinal, void *dq, void *dk_out, void *dv_out, float *dg,
                        float *dbeta, float *dinit, int BH, int T, int dk, int dv, int C,
-                       void *ws, Elem e, cudaStream_t s);
+                       void *ws, Elem e, cudaStream_t s, const void *saved = nullptr);
+bool bwd_saved_shape(int dk, int dv, int C, Elem e, const void *dq, const void *dk_out,
+                     const void *dv_out);
 
 // ---- single-token decode (gdr_decode.cu) ----
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
@@ -111,10 +116,15 @@ cudaError_t launch_prep(const void *q, const void *k, const float *g, const floa
                         cudaStream_t s);
 // nseg > 1 (dense only): the chain of every segment of every head at once, each
 // from its state in seg_init ([BH][nseg][dk][dv], from launch_segment_states).
+// saved != nullptr (dense only): every chunk's state M_n^T ([BH][NC][128 j][128 i]) and
+// W_n^T ([BH][NC][128 j][64 s]) as value-major bf16 tiles, for gdr_chunk_bwd_saved.
 cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
                          int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
-                         int nseg = 1, const float *seg_init = nullptr);
+                         int nseg = 1, const float *seg_init = nullptr, void *saved = nullptr);
+// Bytes of the saved states (the first part of the saved buffer), and of all of it.
+inline size_t saved_state_bytes(int64_t BH, int T) { return (size_t)BH * ((T + 63) / 64) * 128 * 128 * 2; }
+inline size_t saved_bytes(int64_t BH, int T) { return (size_t)BH * ((T + 63) / 64) * 128 * (128 + 64) * 2; }
 // CTAs per view of the chain kernel for BH views on the current device (2 or 1).
 int chain_split(int BH);
 

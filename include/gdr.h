@@ -416,6 +416,57 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
                            void *stream);
 
 /*
+ * Training: a forward that keeps what its backward needs.  The chain of the
+ * two-kernel path already forms, chunk by chunk, the state M_n at every chunk
+ * start and the tile W_n = T diag(beta) E of the chunk ("What a Trillion-Parameter
+ * MoE Model Reveals About the Next Stage of LLM Scaling", sections 3.2-3.3); the
+ * backward of gdr_chunk_bwd recomputes both from the inputs in a sequential pass
+ * of its own.  gdr_chunk_fwd_train writes them out as it goes, and
+ * gdr_chunk_bwd_saved reads them instead of recomputing: one sequential pass
+ * fewer and no U / W products in the backward.
+ *
+ * Shape: bf16, dk = dv = 128, chunk 64 (GDR_ERR_UNSUPPORTED otherwise), dense
+ * [B,H,T,d] tensors.
+ *
+ * gdr_chunk_saved_size: bytes of the saved buffer, B * H * ceil(T / 64) *
+ *   128 * (128 + 64) * 2: per (b, h, chunk n) the state M_n transposed (bf16
+ *   [128 value rows][128 key columns], all the states first) and then W_n
+ *   transposed (bf16 [128 value rows][64 chunk positions], zero past T).  0 for
+ *   unsupported arguments or empty work.  Host-only.
+ * gdr_chunk_fwd_train: gdr_chunk_fwd_ex on the two-kernel path (sequence
+ *   segments included) that also fills `saved`.  The workspace is required (at
+ *   least gdr_chunk_fwd_workspace_size bytes) and so is `saved` (device memory
+ *   owned by the caller, 16-byte aligned, at least gdr_chunk_saved_size bytes):
+ *   GDR_ERR_INVALID_ARG when either is missing, small or misaligned.  The range
+ *   rule is over the 16-token tile as on the two-kernel path.  Two to four
+ *   launches, asynchronous on `stream`; out and final_state as gdr_chunk_fwd.
+ * gdr_chunk_bwd_saved: gdr_chunk_bwd given the saved buffer of the forward with
+ *   the same q, k, v, g, beta, decay, bound, init_state and sizes (not checked:
+ *   another forward's buffer gives wrong gradients, not an error).  `saved` is
+ *   read only and may be released once `stream` has passed the call.  d_q, d_k,
+ *   d_v must be 16-byte aligned as well (GDR_ERR_INVALID_ARG otherwise); the
+ *   workspace is gdr_chunk_bwd_workspace_size bytes; the range rule over the
+ *   chunk as gdr_chunk_bwd.  Four launches.  The states are the forward's bf16
+ *   operands, so the gradients differ from gdr_chunk_bwd's by about the bf16
+ *   rounding of the states (both ~3e-3 relative L2 against an fp64 reference).
+ *   B * H = 0 or T = 0 is gdr_chunk_bwd.
+ */
+size_t gdr_chunk_saved_size(int B, int H, int T, int dk, int dv, int chunk, gdr_dtype_t dtype);
+gdr_status_t gdr_chunk_fwd_train(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, gdr_decay_t decay, float bound,
+                                 const float *init_state, void *out, float *final_state, int B,
+                                 int H, int T, int dk, int dv, int chunk, gdr_dtype_t dtype,
+                                 void *workspace, size_t workspace_bytes, void *saved,
+                                 size_t saved_bytes, void *stream);
+gdr_status_t gdr_chunk_bwd_saved(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, gdr_decay_t decay, float bound,
+                                 const float *init_state, const void *d_out, const float *d_final,
+                                 void *d_q, void *d_k, void *d_v, float *d_g, float *d_beta,
+                                 float *d_init, int B, int H, int T, int dk, int dv, int chunk,
+                                 gdr_dtype_t dtype, const void *saved, size_t saved_bytes,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * One decode step of gated multi-head latent attention, the exact-attention
  * layer the pages interleave with the linear attention: the key/value
  * projections are compressed into a latent space so the cache holds one latent

@@ -342,3 +342,72 @@ def test_mla_decode_rejects(lib):
     ws = lib.gdr_mla_decode_workspace_size
     assert ws(2, 64, 100, 512, 128) > 0 and ws(2, 64, 100, 256, 128) == 0
     assert ws(0, 64, 100, 512, 128) == 0
+
+
+def test_chunk_saved_size(lib):
+    f = lib.gdr_chunk_saved_size
+    f.argtypes = [ctypes.c_int] * 7
+    f.restype = ctypes.c_size_t
+    # per (b, h, chunk): the state transposed (128 x 128) and W transposed (128 x 64), bf16
+    assert f(2, 3, 100, 128, 128, 64, 1) == 2 * 3 * 2 * 128 * (128 + 64) * 2
+    assert f(1, 1, 64, 128, 128, 64, 1) == 128 * 192 * 2
+    assert f(1, 1, 0, 128, 128, 64, 1) == 0 and f(0, 1, 64, 128, 128, 64, 1) == 0
+    assert f(1, 1, 64, 128, 128, 64, 0) == 0      # fp32: not the two-kernel path
+    assert f(1, 1, 64, 64, 128, 64, 1) == 0 and f(1, 1, 64, 128, 128, 32, 1) == 0
+
+
+def train(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, decay=0, bound=0.95, init=None, out=P, fin=None, B=1,
+             H=2, T=100, dk=128, dv=128, chunk=64, dtype=1, ws=P, wsb=1 << 40, sv=P,
+             svb=1 << 40, stream=None)
+    a.update(kw)
+    f = lib.gdr_chunk_fwd_train
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_float] + \
+        [ctypes.c_void_p] * 3 + [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_size_t] * 2 + \
+        [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return f(*(a[n] for n in ("q", "k", "v", "g", "beta", "decay", "bound", "init", "out", "fin",
+                              "B", "H", "T", "dk", "dv", "chunk", "dtype", "ws", "wsb", "sv",
+                              "svb", "stream")))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), 1), (dict(decay=5), 1), (dict(bound=0.0), 1),
+    (dict(dtype=0), 2), (dict(dk=64), 2), (dict(chunk=32), 2),   # not the two-kernel shape
+    (dict(bound=0.001), 3),                                      # 16 * -ln(0.001) > 80
+    (dict(ws=None), 1), (dict(wsb=1024), 1), (dict(ws=ctypes.c_void_p(0x1008)), 1),
+    (dict(sv=None), 1), (dict(svb=1024), 1), (dict(sv=ctypes.c_void_p(0x1004)), 1),
+    (dict(q=None), 1), (dict(out=None), 1),
+    (dict(B=0), 0),                                              # no heads: nothing to do
+])
+def test_chunk_fwd_train_rejects(lib, kw, code):
+    assert train(lib, **kw) == code
+
+
+def bwd_saved(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, decay=0, bound=0.95, init=None, dout=P, dfin=None,
+             dq=P, dk_=P, dv_=P, dg=P, db=P, dinit=None, B=1, H=2, T=100, dk=128, dv=128,
+             chunk=64, dtype=1, sv=P, svb=1 << 40, ws=P, wsb=1 << 40, stream=None)
+    a.update(kw)
+    f = lib.gdr_chunk_bwd_saved
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_float] + \
+        [ctypes.c_void_p] * 9 + [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_size_t] * 2 + \
+        [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return f(*(a[n] for n in ("q", "k", "v", "g", "beta", "decay", "bound", "init", "dout",
+                              "dfin", "dq", "dk_", "dv_", "dg", "db", "dinit", "B", "H", "T",
+                              "dk", "dv", "chunk", "dtype", "sv", "svb", "ws", "wsb", "stream")))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(decay=5), 1), (dict(bound=0.0), 1),
+    (dict(dtype=0), 2), (dict(dv=64), 2), (dict(chunk=16), 2),
+    (dict(bound=0.2), 3),                                        # 64 * -ln(0.2) > 80
+    (dict(sv=None), 1), (dict(svb=1024), 1), (dict(sv=ctypes.c_void_p(0x1008)), 1),
+    (dict(ws=None), 1), (dict(wsb=1024), 1),
+    (dict(dq=ctypes.c_void_p(0x1002)), 1), (dict(dv_=ctypes.c_void_p(0x1008)), 1),
+    (dict(q=None), 1), (dict(dout=None), 1), (dict(dg=None), 1),
+    (dict(B=0), 0),
+])
+def test_chunk_bwd_saved_rejects(lib, kw, code):
+    assert bwd_saved(lib, **kw) == code
