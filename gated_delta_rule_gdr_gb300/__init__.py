@@ -37,7 +37,8 @@ STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "G
           4: "GDR_ERR_CUDA", 5: "GDR_ERR_TIMEOUT"}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 # gdr_option_t
-OPTIONS = {"wait_limit_ns": 0, "fused_variant": 1, "chain_split": 2, "segments": 3}
+OPTIONS = {"wait_limit_ns": 0, "fused_variant": 1, "chain_split": 2, "segments": 3,
+           "bwd_variant": 4}
 
 _lib = None
 

@@ -54,6 +54,7 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_fused_variant{0};
 std::atomic<int> g_chain_split{0};
 std::atomic<int> g_segments{0};
+std::atomic<int> g_bwd_variant{0};
 
 }  // namespace
 
@@ -62,6 +63,7 @@ uint64_t opt_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_rel
 int opt_fused_variant() { return g_fused_variant.load(std::memory_order_relaxed); }
 int opt_chain_split() { return g_chain_split.load(std::memory_order_relaxed); }
 int opt_segments() { return g_segments.load(std::memory_order_relaxed); }
+int opt_bwd_variant() { return g_bwd_variant.load(std::memory_order_relaxed); }
 }  // namespace gdr
 
 extern "C" {
@@ -84,6 +86,10 @@ gdr_status_t gdr_set_option(gdr_option_t option, int64_t value) {
             if (value < 0 || value > 4096) return GDR_ERR_INVALID_ARG;
             g_segments.store((int)value, std::memory_order_relaxed);
             return GDR_OK;
+        case GDR_OPT_BWD_VARIANT:
+            if (value < 0 || value > 2) return GDR_ERR_INVALID_ARG;
+            g_bwd_variant.store((int)value, std::memory_order_relaxed);
+            return GDR_OK;
     }
     return GDR_ERR_INVALID_ARG;
 }
@@ -94,6 +100,7 @@ int64_t gdr_get_option(gdr_option_t option) {
         case GDR_OPT_FUSED_VARIANT: return gdr::opt_fused_variant();
         case GDR_OPT_CHAIN_SPLIT: return gdr::opt_chain_split();
         case GDR_OPT_SEGMENTS: return gdr::opt_segments();
+        case GDR_OPT_BWD_VARIANT: return gdr::opt_bwd_variant();
     }
     return -1;
 }

@@ -1567,7 +1567,8 @@ __global__ void __launch_bounds__(256, 2)
 bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
                      const float *__restrict__ beta, __nv_bfloat16 *__restrict__ TPb,
-                     float *__restrict__ U, __nv_bfloat16 *__restrict__ Wk2, int T, int want_uw) {
+                     float *__restrict__ U, __nv_bfloat16 *__restrict__ Wk2, int T, int want_uw,
+                     const float *__restrict__ g, float d, float *__restrict__ tsc) {
     using namespace mt;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1599,6 +1600,13 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         if (tid < C) {
             gs[tid] = tid < c ? gamma[row0 + tid] : 1.f;
             bs[tid] = tid < c ? beta[row0 + tid] : 0.f;
+            if (tsc) {   // the chunk's row scalars for the per-chunk gradient kernel
+                float *blk = tsc + ((int64_t)bh * NC + n) * 4 * C;
+                blk[tid] = gs[tid];
+                blk[C + tid] = 1.0f / gs[tid];
+                blk[2 * C + tid] = bs[tid];
+                blk[3 * C + tid] = tid < c ? dlog_alpha_dg(g[row0 + tid], d) : 0.f;
+            }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -2182,8 +2190,11 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             __nv_bfloat16 *Sbb = reinterpret_cast<__nv_bfloat16 *>(Mn);   // bf16 value-major states
             __nv_bfloat16 *dSbb = reinterpret_cast<__nv_bfloat16 *>(dMn1);
             if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
+            // the tensor-core per-chunk kernel takes each chunk's row scalars (gamma, 1 / gamma,
+            // beta, d log(alpha) / dg; 1 KB) from the P-tile region, which this shape leaves unused
+            const bool tc_chunk = opt_bwd_variant() != 1;
             bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T,
-                                                                     saved ? 0 : 1);
+                                                                     saved ? 0 : 1, g, d, tc_chunk ? Pt : nullptr);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE;
             if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
@@ -2239,6 +2250,9 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
                 saved ? reinterpret_cast<const __nv_bfloat16 *>(static_cast<const uint8_t *>(saved) +
                                                                saved_state_bytes(BH, T))
                       : reinterpret_cast<const __nv_bfloat16 *>(W);
+            if (opt_bwd_variant() != 1)
+                return launch_bwd_chunk_tc(q, k, v, Pt, Wt_in, Sb_in, dout, dR, dMn1, dq, dk_out, dv_out, dg,
+                                           dbeta, BH, T, s);
             bwd_chunk_mma_kernel<<<grid, 256, mm::SMEM, s>>>(
                 q, k, v, g, beta, d, gamma, Wt_in, Sb_in, dout, dR,
                 reinterpret_cast<const __nv_bfloat16 *>(dMn1), dq, dk_out, dv_out, dg, dbeta, T, BH);

@@ -637,9 +637,10 @@ cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value) {
     if (e == cudaSuccess) e = take_prep_error_word(&c);
     if (e == cudaSuccess) e = take_chain_error_word(&d);
     if (e == cudaSuccess) e = take_segment_error_word(&f);
-    unsigned m = 0;
+    unsigned m = 0, t = 0;
     if (e == cudaSuccess) e = take_mla_error_word(&m);
-    *value = a | b | c | d | f | m;
+    if (e == cudaSuccess) e = take_bwd_tc_error_word(&t);
+    *value = a | b | c | d | f | m | t;
     return e;
 }
 

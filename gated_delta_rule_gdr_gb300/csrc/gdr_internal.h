@@ -58,6 +58,7 @@ int opt_chain_split();
 // Sequence segments of the two-kernel path: 0 by head count, else that many (at
 // most the sequence's chunk count).
 int opt_segments();
+int opt_bwd_variant();
 
 // ---- backward of the chunked form (gdr_bwd.cu) ----
 bool bwd_supported(int dk, int dv, int C);
@@ -159,6 +160,17 @@ cudaError_t launch_mla_decode(const void *q_abs, const void *ckv, const int *seq
                               const float *gate, float scale, void *out, int N, int H, int Lmax, int dh,
                               void *ws, cudaStream_t s);
 cudaError_t take_mla_error_word(unsigned *value);
+
+// ---- the per-chunk gradients of the bf16 d = 128 chunk-64 backward on tcgen05
+// (gdr_bwd_tc.cu): Wt, Sb, dSb are the value-major bf16 tiles [BH][NC][128][64 / 128]
+// (W^T, the states, the state gradients), dR the fp32 [BH][T][128] rows of the reverse
+// chain, tsc the fp32 row scalars [BH][NC][4][64] of every chunk (gamma, 1 / gamma, beta,
+// d log(alpha) / dg; rows past the end 1, 1, 0, 0); writes dq, dk, dv, dg, dbeta.
+cudaError_t launch_bwd_chunk_tc(const void *q, const void *k, const void *v, const float *tsc,
+                                const void *Wt, const void *Sb, const void *dout, const float *dR,
+                                const void *dSb, void *dq, void *dk, void *dv, float *dg,
+                                float *dbeta, int BH, int T, cudaStream_t s);
+cudaError_t take_bwd_tc_error_word(unsigned *value);
 
 // Device error word shared by every kernel with a bounded wait.
 // Returns the word's value and clears it (synchronous on `s`).

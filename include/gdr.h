@@ -517,6 +517,9 @@ gdr_status_t gdr_mla_decode(const void *q_abs, const void *ckv, const int *seqle
  *                          path: 0 chosen by head count (default), 1 or 2.
  *   GDR_OPT_SEGMENTS       sequence segments of the two-kernel path: 0 chosen by
  *                          head count (default), else that many (at most 4096).
+ *   GDR_OPT_BWD_VARIANT    the per-chunk gradient kernel of the bf16 d = 128
+ *                          chunk-64 backward: 0 default (tensor cores), 1 warp-level
+ *                          MMAs, 2 tensor cores.
  * gdr_set_option returns GDR_ERR_INVALID_ARG for an unknown option or a value
  * out of its range; gdr_get_option returns the current value (-1 if unknown).
  * The library reads no environment variable.
@@ -525,7 +528,8 @@ typedef enum {
     GDR_OPT_WAIT_LIMIT_NS = 0,
     GDR_OPT_FUSED_VARIANT = 1,
     GDR_OPT_CHAIN_SPLIT = 2,
-    GDR_OPT_SEGMENTS = 3
+    GDR_OPT_SEGMENTS = 3,
+    GDR_OPT_BWD_VARIANT = 4
 } gdr_option_t;
 gdr_status_t gdr_set_option(gdr_option_t option, int64_t value);
 int64_t gdr_get_option(gdr_option_t option);

@@ -89,6 +89,40 @@ def test_bwd_bf16_prefill_shape_optional_state_terms(init, final):
     check(*run(w, init=init, final=final), TOL["bf16"])
 
 
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 300])
+def test_bwd_bf16_per_chunk_kernels(variant, T):
+    """Both per-chunk gradient kernels of the prefill shape: 1 warp-level MMAs, 2 the
+    tensor cores (the default), with ragged and single-chunk sequences, several heads
+    (the persistent grid walks several tasks per CTA at B = 3, H = 64, T = 300)."""
+    w = I.PREFILL.with_(B=1, H=2, T=T) if T != 300 else I.PREFILL.with_(B=3, H=64, T=300)
+    with gdr.option(bwd_variant=variant):
+        got, ref = run(w)
+    if T == 300:   # the oracle on sampled heads: (0, 0), (1, 17), (2, 63)
+        for b, h in ((0, 0), (1, 17), (2, 63)):
+            check([t[b:b + 1, h:h + 1] for t in got], [t[b:b + 1, h:h + 1] for t in ref], TOL["bf16"])
+    else:
+        check(got, ref, TOL["bf16"])
+
+
+def test_bwd_bf16_per_chunk_kernels_agree():
+    """The tensor-core and warp-MMA per-chunk kernels take the same bf16 operands and
+    accumulate in fp32: their gradients agree far inside the oracle tolerance (the
+    bf16 outputs differ by the rounding of sums taken in another order)."""
+    w = I.PREFILL.with_(B=2, H=8, T=1000)
+    x = I.prefill_inputs(w, device="cuda")
+    ct = I.cotangents(w, device="cuda")
+    outs = []
+    for variant in (1, 2):
+        with gdr.option(bwd_variant=variant):
+            outs.append(gdr.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min,
+                                      x["init_state"], ct["d_out"], ct["d_final"]))
+    torch.cuda.synchronize()
+    for n, a, b in zip(NAMES, *outs):
+        e = oracle.rel_l2(a, b)
+        assert e <= 2e-3, (n, e)
+
+
 def test_bwd_bf16_prefill_shape_log_decay():
     """The tensor-core kernels with the pages' log-domain decay (g_min = -1.25 on 64-token
     chunks, the range rule's limit)."""

@@ -46,3 +46,29 @@ def test_injected_timeout_is_reported_and_recovers(variant):
                         cpu["init_state"])
     assert oracle.rel_l2(out, ro) <= 5e-3 and oracle.rel_l2(fin, rf) <= 5e-3
     assert gdr.last_device_error() == 0
+
+
+def test_backward_injected_timeout_is_reported_and_recovers():
+    """The tensor-core per-chunk gradient kernel of the backward under the same injection:
+    its loads land, its products drain, and the next call is correct."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdr.load(build_if_missing=True)
+    w = I.PREFILL.with_(B=1, H=2, T=300)
+    x = I.prefill_inputs(w, device="cuda")
+    ct = I.cotangents(w, device="cuda")
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, x["init_state"], ct["d_out"],
+            ct["d_final"])
+    assert gdr.last_device_error() == 0
+    with gdr.option(wait_limit_ns=0):
+        gdr.chunk_bwd(*args)
+        assert gdr.last_device_error() == 5          # GDR_ERR_TIMEOUT
+    assert gdr.last_device_error() == 0
+    got = gdr.chunk_bwd(*args)
+    torch.cuda.synchronize()
+    cpu = lambda t: None if t is None else t.cpu()
+    ref = oracle.bwd(*(cpu(x[n]) for n in ("q", "k", "v", "g", "beta")), w.a_min,
+                     cpu(x["init_state"]), cpu(ct["d_out"]), cpu(ct["d_final"]))
+    for a, b in zip(got, ref):
+        assert oracle.rel_l2(a, b) <= 5e-3
+    assert gdr.last_device_error() == 0
