@@ -173,7 +173,10 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     if (warp == 0) {
         // ================================================================ loads
-        if (lane == 0) {
+        // Lane 0: the products' operands; lane 1: the converter's rows and the scalar blocks.
+        // Each lane waits for its own regions, so a late scalar block never holds back a
+        // tile the tensor cores wait for.
+        if (lane < 2) {
             int last[F_SC1 + 1];   // the last task whose load each barrier tracks (-1: none)
             for (int b = 0; b <= F_SC1; ++b) last[b] = -1;
             for (int task = blockIdx.x, it = 0; task < ntask; task += gridDim.x, ++it) {
@@ -182,51 +185,54 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const int64_t grow0 = (int64_t)bh * T + row0;
                 const uint32_t pe = (uint32_t)(it - 1) & 1u;
                 auto free_of = [&](int b) { return it == 0 || role_wait(bar(b), pe, a.limit_ns, &s_abort); };
-                if (!free_of(E_WT)) break;
-                mbar_arrive_expect_tx(bar(F_WT), 16384);
-                tma_load_3d(sbase + OFF_WT, &tm_w, bar(F_WT), 0, 0, task);
-                last[F_WT] = it;
-                if (!free_of(E_DS)) break;
-                mbar_arrive_expect_tx(bar(F_DS), 32768);
-                tma_load_3d(sbase + OFF_DS, &tm_ds, bar(F_DS), 0, 0, task);
-                tma_load_3d(sbase + OFF_DS + 16384, &tm_ds, bar(F_DS), 64, 0, task);
-                last[F_DS] = it;
-                if (!free_of(E_S)) break;
-                mbar_arrive_expect_tx(bar(F_S), 32768);
-                tma_load_3d(sbase + OFF_S, &tm_s, bar(F_S), 0, 0, task);
-                tma_load_3d(sbase + OFF_S + 16384, &tm_s, bar(F_S), 64, 0, task);
-                last[F_S] = it;
-                if (!free_of(E_RO)) break;
-                mbar_arrive_expect_tx(bar(F_DO), 16384);
-                tma_load_3d(sbase + OFF_RO + 8192, &tm_o, bar(F_DO), 0, row0, bh);
-                tma_load_3d(sbase + OFF_RO + 24576, &tm_o, bar(F_DO), 64, row0, bh);
-                last[F_DO] = it;
-                if (!free_of(E_DR)) break;
-                mbar_arrive_expect_tx(bar(F_DR), (uint32_t)c * 512u);
-                bulk_load(sbase + OFF_DR, a.dR + grow0 * D, (uint32_t)c * 512u, bar(F_DR));
-                last[F_DR] = it;
-                if (!free_of(E_V)) break;
-                mbar_arrive_expect_tx(bar(F_V), (uint32_t)c * 256u);
-                bulk_load(sbase + OFF_V, a.v + grow0 * D, (uint32_t)c * 256u, bar(F_V));
-                last[F_V] = it;
-                // the scalar block of this parity: free once the task two back has used it
-                if (it > 1 && !role_wait(bar(B_SFREE0 + (it & 1)), (uint32_t)((it - 2) >> 1) & 1u, a.limit_ns,
-                                         &s_abort))
-                    break;
-                mbar_arrive_expect_tx(bar(F_SC0 + (it & 1)), 4 * C * 4);
-                bulk_load(sbase + OFF_SC + (uint32_t)(it & 1) * SC_N * 4, a.tsc + (int64_t)task * 4 * C, 4 * C * 4,
-                          bar(F_SC0 + (it & 1)));
-                last[F_SC0 + (it & 1)] = it;
-                if (!free_of(E_KQ)) break;
-                mbar_arrive_expect_tx(bar(F_KQ), 32768);
-                tma_load_3d(sbase + OFF_KQ, &tm_k, bar(F_KQ), 0, row0, bh);
-                tma_load_3d(sbase + OFF_KQ + 8192, &tm_q, bar(F_KQ), 0, row0, bh);
-                tma_load_3d(sbase + OFF_KQ + 16384, &tm_k, bar(F_KQ), 64, row0, bh);
-                tma_load_3d(sbase + OFF_KQ + 24576, &tm_q, bar(F_KQ), 64, row0, bh);
-                last[F_KQ] = it;
+                if (lane == 0) {
+                    if (!free_of(E_WT)) break;
+                    mbar_arrive_expect_tx(bar(F_WT), 16384);
+                    tma_load_3d(sbase + OFF_WT, &tm_w, bar(F_WT), 0, 0, task);
+                    last[F_WT] = it;
+                    if (!free_of(E_DS)) break;
+                    mbar_arrive_expect_tx(bar(F_DS), 32768);
+                    tma_load_3d(sbase + OFF_DS, &tm_ds, bar(F_DS), 0, 0, task);
+                    tma_load_3d(sbase + OFF_DS + 16384, &tm_ds, bar(F_DS), 64, 0, task);
+                    last[F_DS] = it;
+                    if (!free_of(E_RO)) break;
+                    mbar_arrive_expect_tx(bar(F_DO), 16384);
+                    tma_load_3d(sbase + OFF_RO + 8192, &tm_o, bar(F_DO), 0, row0, bh);
+                    tma_load_3d(sbase + OFF_RO + 24576, &tm_o, bar(F_DO), 64, row0, bh);
+                    last[F_DO] = it;
+                    if (!free_of(E_S)) break;
+                    mbar_arrive_expect_tx(bar(F_S), 32768);
+                    tma_load_3d(sbase + OFF_S, &tm_s, bar(F_S), 0, 0, task);
+                    tma_load_3d(sbase + OFF_S + 16384, &tm_s, bar(F_S), 64, 0, task);
+                    last[F_S] = it;
+                    if (!free_of(E_KQ)) break;
+                    mbar_arrive_expect_tx(bar(F_KQ), 32768);
+                    tma_load_3d(sbase + OFF_KQ, &tm_k, bar(F_KQ), 0, row0, bh);
+                    tma_load_3d(sbase + OFF_KQ + 8192, &tm_q, bar(F_KQ), 0, row0, bh);
+                    tma_load_3d(sbase + OFF_KQ + 16384, &tm_k, bar(F_KQ), 64, row0, bh);
+                    tma_load_3d(sbase + OFF_KQ + 24576, &tm_q, bar(F_KQ), 64, row0, bh);
+                    last[F_KQ] = it;
+                } else {
+                    if (!free_of(E_DR)) break;
+                    mbar_arrive_expect_tx(bar(F_DR), (uint32_t)c * 512u);
+                    bulk_load(sbase + OFF_DR, a.dR + grow0 * D, (uint32_t)c * 512u, bar(F_DR));
+                    last[F_DR] = it;
+                    if (!free_of(E_V)) break;
+                    mbar_arrive_expect_tx(bar(F_V), (uint32_t)c * 256u);
+                    bulk_load(sbase + OFF_V, a.v + grow0 * D, (uint32_t)c * 256u, bar(F_V));
+                    last[F_V] = it;
+                    // the scalar block of this parity: free once the task two back has used it
+                    if (it > 1 && !role_wait(bar(B_SFREE0 + (it & 1)), (uint32_t)((it - 2) >> 1) & 1u,
+                                             a.limit_ns, &s_abort))
+                        break;
+                    mbar_arrive_expect_tx(bar(F_SC0 + (it & 1)), 4 * C * 4);
+                    bulk_load(sbase + OFF_SC + (uint32_t)(it & 1) * SC_N * 4, a.tsc + (int64_t)task * 4 * C,
+                              4 * C * 4, bar(F_SC0 + (it & 1)));
+                    last[F_SC0 + (it & 1)] = it;
+                }
             }
-            // on the error path: wait (bounded) for every load issued, so none lands after
-            // the CTA has left
+            // on the error path: wait (bounded) for every load this lane issued, so none
+            // lands after the CTA has left
             if (s_abort) {
                 for (int b = 0; b <= F_SC1; ++b) {
                     if (last[b] < 0) continue;
