@@ -349,7 +349,11 @@ def prefill_leg_line(gdr, w, ms, pk, pk_kind, world, max_over_ranks):
 CSRC = "gated_delta_rule_gdr_gb300/csrc/"
 # the four launches of one backward step on the bf16, d = 128, chunk 64 shape
 BWD_KERNELS = ("backward: decay_kernel + bwd_tiles_mma_kernel + bwd_passes_vc_kernel + "
-               "bwd_chunk_mma_kernel")
+               "bwd_chunk_tc_kernel")
+# one training step: the forward with saves (two-kernel path) and the saved-state backward
+TRAIN_KERNELS = ("training: chunk_prep_kernel + chain_kernel<64> + decay_kernel + bwd_tiles_mma_kernel + "
+                 "bwd_passes_vc_kernel + bwd_chunk_tc_kernel")
+BWD_SRCS = [CSRC + "gdr_bwd.cu", CSRC + "gdr_bwd_tc.cu", CSRC + "gdr_staged.cu"]
 _COMMON = [CSRC + "gdr_fused_common.cuh", CSRC + "gdr_sm100.cuh"]
 
 
@@ -628,6 +632,7 @@ def run_ours(args):
     pk, pk_kind = peaks()
 
     main_w = WORKLOAD_ARG[args.workload]
+    prefill_family = main_w is I.PREFILL   # the backward and training legs follow its sizes
     varlen = main_w is I.VARLEN
     if main_w.steps == 0 and not varlen and (args.B or args.H or args.T):
         # a smaller case of the same prefill workload (for profiling); the line names it
@@ -661,11 +666,11 @@ def run_ours(args):
             dec = bench_decode(gdr, I.DECODE, args.decode_steps, args.warmup, dev, flush, stream)
             barrier()
         bwd = None
-        if main_w == I.PREFILL and not args.no_backward:
+        if prefill_family and not args.no_backward:
             bwd = bench_backward(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
             barrier()
         train = None
-        if main_w == I.PREFILL and not args.no_backward:
+        if prefill_family and not args.no_backward:
             train = bench_training(gdr, main_w, max(3, args.steps // 2), 3, dev, flush, stream)
             barrier()
         mla = None
@@ -779,9 +784,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": BWD_KERNELS, "achieved": round(bgbs, 1),
                          "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
                          "frac": round(bgbs / pk["hbm_gbs"], 4),
-                         "traffic": committed_traffic(BWD_KERNELS, [CSRC + "gdr_bwd.cu",
-                                                                    CSRC + "gdr_staged.cu"],
-                                                      main_w.name),
+                         "traffic": committed_traffic(BWD_KERNELS, BWD_SRCS + _COMMON, main_w.name),
                          "algorithmic_bytes": bby},
             "workspace_bytes": bws, "gpu_launches": 4 * len(bms),
         }
@@ -797,10 +800,13 @@ def run_ours(args):
             "unit": "tokens/s", "ms_per_step": round(tmean, 4), "steps": len(tms),
             "forward_ms": round(statistics.mean(tfm), 4),
             "backward_ms": round(statistics.mean(tbm), 4),
-            "roofline": {"bound": "hbm", "achieved": round(tgbs, 1), "peak": pk["hbm_gbs"],
-                         "peak_kind": pk_kind, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "kernel": TRAIN_KERNELS, "achieved": round(tgbs, 1),
+                         "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
                          "frac": round(tgbs / pk["hbm_gbs"], 4), "algorithmic_bytes": tby,
-                         "traffic": None},
+                         "traffic": committed_traffic(TRAIN_KERNELS,
+                                                      BWD_SRCS + _COMMON + [CSRC + "gdr_prep.cu",
+                                                                            CSRC + "gdr_chain.cu"],
+                                                      main_w.name)},
             "saved_bytes": tsv, "gpu_launches": tnk * len(tms),
         }
     if mla is not None:
