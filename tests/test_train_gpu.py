@@ -66,11 +66,14 @@ def test_train_forward_matches_the_prefill(T, segments):
     assert torch.equal(fin, ref_fin)
 
 
-@pytest.mark.parametrize("T,segments", [(64, 1), (130, 1), (777, 1), (1600, 3)])
-def test_saved_states_and_w_tiles(T, segments):
+@pytest.mark.parametrize("T,segments,split", [(64, 1, 0), (130, 1, 0), (777, 1, 0), (1600, 3, 0),
+                                              (200, 1, 1), (1300, 3, 1)])
+def test_saved_states_and_w_tiles(T, segments, split):
+    """split 1 forces one chain CTA per head (all 128 value columns: the chain's other
+    shape, taken when two CTAs per head would not all fit on the GPU)."""
     w = I.PREFILL.with_(B=1, H=2, T=T)
     x = I.prefill_inputs(w, device="cuda")
-    with gdr.option(segments=segments):
+    with gdr.option(segments=segments, chain_split=split):
         _, _, saved = train_fwd(x, w)
     torch.cuda.synchronize()
     st, wt = saved_views(saved, w.B, w.H, T)
@@ -86,13 +89,13 @@ def test_saved_states_and_w_tiles(T, segments):
             assert not wt[h, n, c:].any()                     # past the end: zero
 
 
-def bwd_pair(w, *, segments=1, init=True, final=True, bound=None, decay="affine"):
+def bwd_pair(w, *, segments=1, init=True, final=True, bound=None, decay="affine", split=0):
     x = I.prefill_inputs(w, device="cuda")
     ct = I.cotangents(w, device="cuda")
     bound = w.a_min if bound is None else bound
     init_state = x["init_state"] if init else None
     d_final = ct["d_final"] if final else None
-    with gdr.option(segments=segments):
+    with gdr.option(segments=segments, chain_split=split):
         _, _, saved = train_fwd(x, w, bound, decay, init)
     got = gdr.chunk_bwd_saved(x["q"], x["k"], x["v"], x["g"], x["beta"], bound, init_state,
                               ct["d_out"], saved, d_final, decay=decay)
@@ -112,10 +115,11 @@ def check(got, ref):
     assert all(e <= TOL for e in errs.values()), errs
 
 
-@pytest.mark.parametrize("T,segments", [(1, 1), (64, 1), (65, 1), (300, 1), (2048, 4)])
-def test_bwd_saved_matches_oracle(T, segments):
+@pytest.mark.parametrize("T,segments,split", [(1, 1, 0), (64, 1, 0), (65, 1, 0), (300, 1, 0),
+                                              (2048, 4, 0), (300, 1, 1)])
+def test_bwd_saved_matches_oracle(T, segments, split):
     w = I.PREFILL.with_(B=1, H=2, T=T)
-    x, ct, init_state, d_final, got = bwd_pair(w, segments=segments)
+    x, ct, init_state, d_final, got = bwd_pair(w, segments=segments, split=split)
     cpu = lambda t: None if t is None else t.cpu()
     ref = oracle.bwd(*(cpu(x[n]) for n in ("q", "k", "v", "g", "beta")), w.a_min,
                      cpu(init_state), cpu(ct["d_out"]), cpu(d_final))
