@@ -351,8 +351,10 @@ CSRC = "gated_delta_rule_gdr_gb300/csrc/"
 BWD_KERNELS = ("backward: decay_kernel + bwd_tiles_mma_kernel + bwd_passes_vc_kernel + "
                "bwd_chunk_tc_kernel")
 # one training step: the forward with saves (two-kernel path) and the saved-state backward
-TRAIN_KERNELS = ("training: chunk_prep_kernel + chain_kernel<64> + decay_kernel + bwd_tiles_mma_kernel + "
-                 "bwd_passes_vc_kernel + bwd_chunk_tc_kernel")
+# (the forward's prep kernel also writes T, P and the row scalars, so the backward runs
+# neither the decay nor the tiles kernel)
+TRAIN_KERNELS = ("training: chunk_prep_kernel<true> + chain_kernel<64> + bwd_passes_vc_kernel + "
+                 "bwd_chunk_tc_kernel")
 BWD_SRCS = [CSRC + "gdr_bwd.cu", CSRC + "gdr_bwd_tc.cu", CSRC + "gdr_staged.cu"]
 _COMMON = [CSRC + "gdr_fused_common.cuh", CSRC + "gdr_sm100.cuh"]
 
@@ -502,7 +504,7 @@ def bench_training(gdr, w, K, W, dev, flush, stream):
     ms_f = time_steps(fwd, K, W, flush, stream)
     ms_b = time_steps(bwd, K, W, flush, stream)
     path = gdr.chunk_fwd_path(w.B, w.H, w.T, w.dk, w.dv, w.chunk, w.a_min, td, workspace=True)
-    return ms, ms_f, ms_b, nsv, (4 if path == 7 else 2) + 4
+    return ms, ms_f, ms_b, nsv, (4 if path == 7 else 2) + 2
 
 
 def cpu_baseline_backward(w, budget_s=8.0):

@@ -337,7 +337,12 @@ gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const f
                             cudaStream_t s) {
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
     const int S = gdr::segment_count(BH, T);
-    cudaError_t e = gdr::launch_prep(q, k, g, beta, a_min, workspace, BH, T, nullptr, 0, 0, s);
+    // training: the preparation also leaves T, P and the row scalars in the saved buffer
+    uint8_t *sv = static_cast<uint8_t *>(saved);
+    cudaError_t e = gdr::launch_prep(q, k, g, beta, a_min, workspace, BH, T, nullptr, 0, 0, s,
+                                     sv ? sv + gdr::saved_tp_offset(BH, T) : nullptr,
+                                     sv ? reinterpret_cast<float *>(sv + gdr::saved_sc_offset(BH, T))
+                                        : nullptr);
     if (S <= 1) {
         if (e == cudaSuccess)
             e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace,

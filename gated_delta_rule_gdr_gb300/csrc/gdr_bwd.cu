@@ -51,10 +51,7 @@ __device__ __forceinline__ void stx(__nv_bfloat16 *p, int64_t i, float x) {
 }
 
 // d log(alpha) / d g for the two decay forms (parameter d as in gdr_math.cuh).
-__device__ __forceinline__ float dlog_alpha_dg(float g, float d) {
-    const float s = 1.0f / (1.0f + expf(-g));
-    return d > 0.0f ? (1.0f - d) * s * (1.0f - s) / decay_alpha(g, d) : d * s * (1.0f - s);
-}
+__device__ __forceinline__ float dlog_alpha_dg(float g, float d) { return decay_dlog_dg(g, d); }
 
 // ---------------------------------------------------------------- chunk tiles
 // One CTA per (chunk, bh), all in parallel, 256 threads:
@@ -1595,7 +1592,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
             const bool in = r < c;
             bq[u] = in ? ld16(q + (row0 + r) * DK + col) : z;
             bk[u] = in ? ld16(k + (row0 + r) * DK + col) : z;
-            bv[u] = in ? ld16(v + (row0 + r) * DK + col) : z;
+            bv[u] = (in && want_uw) ? ld16(v + (row0 + r) * DK + col) : z;   // v only feeds U
         }
         if (tid < C) {
             gs[tid] = tid < c ? gamma[row0 + tid] : 1.f;
@@ -1943,7 +1940,8 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
                     const float *__restrict__ gamma, const float *__restrict__ beta,
                     const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
                     const __nv_bfloat16 *__restrict__ TPb, float *__restrict__ dR,
-                    __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv) {
+                    __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv,
+                    const float *__restrict__ rows) {
     using namespace vc;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -1966,8 +1964,11 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
             stage_rows(st + R_O, dout + row0 * dv + j0, (int64_t)dv * 2, DSC * 2, LC * 2, C, c, tid, NT);
             if (tid < C) {
                 const int r = tid < c ? tid : 0;
-                cp_async4(st + R_G + 4 * tid, gamma + row0 + r, tid < c ? 4u : 0u);
-                cp_async4(st + R_B + 4 * tid, beta + row0 + r, tid < c ? 4u : 0u);
+                // gamma and beta: the decay's rows, or the forward's saved block of the chunk
+                const float *gsrc = rows ? rows + ((int64_t)bh * NC + n) * 4 * C + r : gamma + row0 + r;
+                const float *bsrc = rows ? rows + ((int64_t)bh * NC + n) * 4 * C + 2 * C + r : beta + row0 + r;
+                cp_async4(st + R_G + 4 * tid, gsrc, tid < c ? 4u : 0u);
+                cp_async4(st + R_B + 4 * tid, bsrc, tid < c ? 4u : 0u);
             }
         }
         cp_async_commit();
@@ -2123,7 +2124,7 @@ bwd_passes_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                      const __nv_bfloat16 *__restrict__ Wk2, const __nv_bfloat16 *__restrict__ TPb,
                      const float *init, const float *dfinal, __nv_bfloat16 *__restrict__ Wt,
                      __nv_bfloat16 *__restrict__ Sb, float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb,
-                     float *dinit, int T, int dv, int fwd_role) {
+                     float *dinit, int T, int dv, int fwd_role, const float *__restrict__ rows) {
     extern __shared__ __align__(16) uint8_t smb[];
     const int tid = threadIdx.x;
     // fwd_role = 0: the forward saved W^T and the states; only the reverse chain runs (the
@@ -2132,7 +2133,7 @@ bwd_passes_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         if (fwd_role) fwd_state_pass(smb, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
     } else
         chain_pass(smb + 2 * vc::F_STAGE, tid - vc::NT, 2, q, k, gamma, beta, dout, dfinal, TPb, dR, dSb,
-                   dinit, T, dv);
+                   dinit, T, dv, rows);
 }
 
 template <typename K>
@@ -2174,9 +2175,13 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
     float *Pt = dMn1 + round4(st);
     float *Tt = Pt + round4((size_t)BH * NC * C * C);
     float *DKt = Tt + round4((size_t)BH * NC * C * C);
-    cudaError_t err = launch_decay(g, d, gamma, BH, T, C, s);
-    if (err != cudaSuccess) return err;
     constexpr bool kBf16 = std::is_same<TE, __nv_bfloat16>::value;
+    const bool tc_chunk = opt_bwd_variant() != 1;
+    // From the forward's saved buffer the tensor-core per-chunk kernel needs neither the decay
+    // nor the tiles kernel: the forward left T, P and every chunk's row scalars there.
+    const bool from_saves = saved && tc_chunk;
+    cudaError_t err = cudaSuccess;
+    if (!from_saves && (err = launch_decay(g, d, gamma, BH, T, C, s)) != cudaSuccess) return err;
     // the warp-MMA kernels: bf16, d = 128, chunk 64, gradient outputs 16-byte aligned (their
     // 16-byte stores); the states they pass on are value-major, so all four go together
     const bool mma_shape = kBf16 && dk == 128 && dv == 128 && C == 64 &&
@@ -2189,18 +2194,25 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
             __nv_bfloat16 *Wtb = reinterpret_cast<__nv_bfloat16 *>(W);    // bf16 W^T per chunk
             __nv_bfloat16 *Sbb = reinterpret_cast<__nv_bfloat16 *>(Mn);   // bf16 value-major states
             __nv_bfloat16 *dSbb = reinterpret_cast<__nv_bfloat16 *>(dMn1);
-            if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
-            // the tensor-core per-chunk kernel takes each chunk's row scalars (gamma, 1 / gamma,
-            // beta, d log(alpha) / dg; 1 KB) from the P-tile region, which this shape leaves unused
-            const bool tc_chunk = opt_bwd_variant() != 1;
-            bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T,
-                                                                     saved ? 0 : 1, g, d, tc_chunk ? Pt : nullptr);
-            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            const uint8_t *sv = static_cast<const uint8_t *>(saved);
+            const __nv_bfloat16 *TPin = TPb;
+            const float *rows = nullptr;   // the chain's gamma, beta rows from saved scalar blocks
+            if (from_saves) {
+                TPin = reinterpret_cast<const __nv_bfloat16 *>(sv + saved_tp_offset(BH, T));
+                rows = reinterpret_cast<const float *>(sv + saved_sc_offset(BH, T));
+            } else {
+                if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
+                // the tensor-core per-chunk kernel takes each chunk's row scalars (gamma, 1 / gamma,
+                // beta, d log(alpha) / dg; 1 KB) from the P-tile region, which this shape leaves unused
+                bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T,
+                                                                         saved ? 0 : 1, g, d, tc_chunk ? Pt : nullptr);
+                if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            }
             const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE;
             if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
             bwd_passes_vc_kernel<<<dim3(dv / vc::DSC, BH), 2 * vc::NT, sp, s>>>(
-                q, k, dout, gamma, beta, U, Wk2, TPb, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv,
-                saved ? 0 : 1);
+                q, k, dout, gamma, beta, U, Wk2, TPin, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv,
+                saved ? 0 : 1, rows);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {
@@ -2250,9 +2262,13 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
                 saved ? reinterpret_cast<const __nv_bfloat16 *>(static_cast<const uint8_t *>(saved) +
                                                                saved_state_bytes(BH, T))
                       : reinterpret_cast<const __nv_bfloat16 *>(W);
-            if (opt_bwd_variant() != 1)
-                return launch_bwd_chunk_tc(q, k, v, Pt, Wt_in, Sb_in, dout, dR, dMn1, dq, dk_out, dv_out, dg,
-                                           dbeta, BH, T, s);
+            if (tc_chunk)
+                return launch_bwd_chunk_tc(q, k, v,
+                                           from_saves ? reinterpret_cast<const float *>(
+                                                            static_cast<const uint8_t *>(saved) +
+                                                            saved_sc_offset(BH, T))
+                                                      : Pt,
+                                           Wt_in, Sb_in, dout, dR, dMn1, dq, dk_out, dv_out, dg, dbeta, BH, T, s);
             bwd_chunk_mma_kernel<<<grid, 256, mm::SMEM, s>>>(
                 q, k, v, g, beta, d, gamma, Wt_in, Sb_in, dout, dR,
                 reinterpret_cast<const __nv_bfloat16 *>(dMn1), dq, dk_out, dv_out, dg, dbeta, T, BH);

@@ -112,9 +112,12 @@ cudaError_t take_pair_error_word(unsigned *value);
 // then the state chain and outputs (gdr_chain.cu).  Same dense / packed layouts as
 // launch_fused_pair.
 size_t prep_workspace_bytes(int BH, int T, const int *cu_seqlens, int H, int total_T);
+// tpb, tsc (training, dense only): also every chunk's T and P as plain bf16 [64][64] tiles
+// ([BH][NC][2][64][64]) and its row scalars ([BH][NC][4][64] fp32: gamma, 1/gamma, beta,
+// d log(alpha)/dg), the inputs the backward's tiles and decay kernels would recompute.
 cudaError_t launch_prep(const void *q, const void *k, const float *g, const float *beta, float a_min,
                         void *ws, int BH, int T, const int *cu_seqlens, int H, int total_T,
-                        cudaStream_t s);
+                        cudaStream_t s, void *tpb = nullptr, float *tsc = nullptr);
 // nseg > 1 (dense only): the chain of every segment of every head at once, each
 // from its state in seg_init ([BH][nseg][dk][dv], from launch_segment_states).
 // saved != nullptr (dense only): every chunk's state M_n^T ([BH][NC][128 j][128 i]) and
@@ -123,9 +126,16 @@ cudaError_t launch_chain(const void *q, const void *k, const void *v, const floa
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
                          int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
                          int nseg = 1, const float *seg_init = nullptr, void *saved = nullptr);
-// Bytes of the saved states (the first part of the saved buffer), and of all of it.
-inline size_t saved_state_bytes(int64_t BH, int T) { return (size_t)BH * ((T + 63) / 64) * 128 * 128 * 2; }
-inline size_t saved_bytes(int64_t BH, int T) { return (size_t)BH * ((T + 63) / 64) * 128 * (128 + 64) * 2; }
+// The saved buffer, per (head, chunk) tile x of X = BH ceil(T / 64), in four parts: the
+// states M_x^T (bf16 [128][128]), then W_x^T (bf16 [128][64]), then T_x and P_x (bf16
+// [2][64][64]), then the row scalars (fp32 [4][64]).  Offsets of the parts and the size.
+inline size_t saved_tiles(int64_t BH, int T) { return (size_t)BH * ((T + 63) / 64); }
+inline size_t saved_state_bytes(int64_t BH, int T) { return saved_tiles(BH, T) * 128 * 128 * 2; }
+inline size_t saved_tp_offset(int64_t BH, int T) { return saved_tiles(BH, T) * 128 * (128 + 64) * 2; }
+inline size_t saved_sc_offset(int64_t BH, int T) {
+    return saved_tp_offset(BH, T) + saved_tiles(BH, T) * 2 * 64 * 64 * 2;
+}
+inline size_t saved_bytes(int64_t BH, int T) { return saved_sc_offset(BH, T) + saved_tiles(BH, T) * 4 * 64 * 4; }
 // CTAs per view of the chain kernel for BH views on the current device (2 or 1).
 int chain_split(int BH);
 

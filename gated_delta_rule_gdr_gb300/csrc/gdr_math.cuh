@@ -18,5 +18,10 @@ __device__ __forceinline__ float log_alpha(float g, float d) {
 __device__ __forceinline__ float decay_alpha(float g, float d) {
     return d > 0.0f ? d + (1.0f - d) / (1.0f + expf(-g)) : expf(d / (1.0f + expf(-g)));
 }
+// d log(alpha) / d g of the two forms: (1 - d) s (1 - s) / alpha and d s (1 - s), s = sigmoid(g).
+__device__ __forceinline__ float decay_dlog_dg(float g, float d) {
+    const float s = 1.0f / (1.0f + expf(-g));
+    return d > 0.0f ? (1.0f - d) * s * (1.0f - s) / decay_alpha(g, d) : d * s * (1.0f - s);
+}
 
 }  // namespace gdr

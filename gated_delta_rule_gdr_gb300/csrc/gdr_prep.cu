@@ -19,6 +19,11 @@
 // persistent grid walks them, each CTA loading its next item's K and Q while it
 // prepares the current one.
 //
+// For training (tpb, tsc given) it also writes what the backward's tiles and
+// decay kernels would recompute: T and P as plain bf16 [64][64] tiles, and the
+// chunk's row scalars gamma, 1/gamma, beta, d log(alpha)/dg (rows past the
+// chunk's end 1, 1, 0, 0).
+//
 // CTA: 128 threads, three per SM.  Thread 0 issues the TMA loads, the
 // tensor-core product and the bulk store of each tile; warp 3 computes the
 // decay (away from the warp that issues the product, whose later instructions
@@ -80,9 +85,39 @@ __device__ bool item_chunk(const FusedArgs &a, int BH, int nslot, int item, int 
     return n >= 0 && n * C < v.T;
 }
 
+// The chunk's row scalars for the backward (training): gamma_r = e^(b_r) with b the
+// chunk-local cumulative log-decay, 1 / gamma_r, beta_r and d log(alpha_r) / dg_r, in
+// the full-precision functions of the backward's own decay; rows past the chunk's c
+// rows 1, 1, 0, 0.  Warp-wide: lane l holds rows 2 l, 2 l + 1.
+__device__ __noinline__ void chunk_row_scalars(int lane, const float (&gv)[2], const float (&bv)[2], int c,
+                                               float d, float *blk) {
+    const int r0 = 2 * lane;
+    const float l0 = (r0 < c) ? log_alpha(gv[0], d) : 0.f;
+    const float l1 = (r0 + 1 < c) ? log_alpha(gv[1], d) : 0.f;
+    float incl = l0 + l1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const float b[2] = {incl - l1, incl};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = r0 + e;
+        const bool valid = r < c;
+        const float ga = valid ? expf(b[e]) : 1.f;
+        blk[r] = ga;
+        blk[C + r] = 1.0f / ga;
+        blk[2 * C + r] = valid ? bv[e] : 0.f;
+        blk[3 * C + r] = valid ? decay_dlog_dg(gv[e], d) : 0.f;
+    }
+}
+
+template <bool kTrain>
 __global__ void __launch_bounds__(NT, CTAS_PER_SM)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const FusedArgs a, uint8_t *ws, int BH, int nslot, int items) {
+                  const FusedArgs a, uint8_t *ws, int BH, int nslot, int items, __nv_bfloat16 *tpb,
+                  float *tsc) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
@@ -174,6 +209,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (warp == 3) {   // the chunk's decay (away from the warp that issued the product),
                            // then the next item's g, beta
             warp_decay_tiles(lane, gv[0], gv[1], bv[0], bv[1], min(C, v.T - n * C), a.a_min, S);
+            if (kTrain) chunk_row_scalars(lane, gv, bv, min(C, v.T - n * C), a.a_min,
+                                       tsc + ((int64_t)bh * (int64_t)nslot + n) * 4 * C);
             if (nx < items) load_gb(n2, v2, gv, bv);
         }
         if (tid == 0 && ok) {
@@ -231,6 +268,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     u.z = pack_bf16x2(p8[4], p8[5]);
                     u.w = pack_bf16x2(p8[6], p8[7]);
                     *reinterpret_cast<uint4 *>(tile + LP_TILE_P + swz((uint32_t)r, (uint32_t)(half * 4 + q4))) = u;
+                    if (kTrain)   // training: the plain P tile for the backward
+                        *reinterpret_cast<uint4 *>(tpb + (((int64_t)bh * nslot + n) * 2 + 1) * C * C + r * C + sb) = u;
                 }
             }
         }
@@ -242,6 +281,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // Lb = strict_lower(T) diag(beta): row tid % 64, columns 16 q4 + 0..15
             const int r = tid & 63;
             float x[16];
+            float tt[16];   // T itself (lower triangle with the unit diagonal) for training
 #pragma unroll
             for (int s4 = 0; s4 < 16; s4 += 4) {
                 const int s0 = q4 * 16 + s4;
@@ -251,6 +291,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 x[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
                 x[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
                 x[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
+                tt[s4 + 0] = (s0 + 0 <= r) ? t.x : 0.f;
+                tt[s4 + 1] = (s0 + 1 <= r) ? t.y : 0.f;
+                tt[s4 + 2] = (s0 + 2 <= r) ? t.z : 0.f;
+                tt[s4 + 3] = (s0 + 3 <= r) ? t.w : 0.f;
+            }
+            if (kTrain) {
+                __nv_bfloat16 *trow = tpb + ((int64_t)bh * nslot + n) * 2 * C * C + r * C + q4 * 16;
+                *reinterpret_cast<uint4 *>(trow) =
+                    make_uint4(pack_bf16x2(tt[0], tt[1]), pack_bf16x2(tt[2], tt[3]),
+                               pack_bf16x2(tt[4], tt[5]), pack_bf16x2(tt[6], tt[7]));
+                *reinterpret_cast<uint4 *>(trow + 8) =
+                    make_uint4(pack_bf16x2(tt[8], tt[9]), pack_bf16x2(tt[10], tt[11]),
+                               pack_bf16x2(tt[12], tt[13]), pack_bf16x2(tt[14], tt[15]));
             }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -308,7 +361,10 @@ size_t prep_workspace_bytes(int BH, int T, const int *cu_seqlens, int H, int tot
 
 cudaError_t launch_prep(const void *q, const void *k, const float *g, const float *beta, float a_min,
                         void *ws, int BH, int T, const int *cu_seqlens, int H, int total_T,
-                        cudaStream_t s) {
+                        cudaStream_t s, void *tpb, float *tsc) {
+    if ((tpb || tsc) && (cu_seqlens || !tpb || !tsc ||
+                         ((reinterpret_cast<uintptr_t>(tpb) | reinterpret_cast<uintptr_t>(tsc)) & 15)))
+        return cudaErrorInvalidValue;   // the training outputs: dense layout, both, aligned
     if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
          reinterpret_cast<uintptr_t>(ws)) & 15)
@@ -324,15 +380,15 @@ cudaError_t launch_prep(const void *q, const void *k, const float *g, const floa
     const int64_t nslot = tile_slots(a, BH);
     const int64_t items = (cu_seqlens ? (int64_t)H : (int64_t)BH) * nslot;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;   // work items are counted in 32 bits
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_ALLOC);
+    const auto kern = tpb ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(items, (int64_t)sms * CTAS_PER_SM);
-    chunk_prep_kernel<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(mq, mk, a, static_cast<uint8_t *>(ws), BH,
-                                                              (int)nslot, (int)items);
+    kern<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(mq, mk, a, static_cast<uint8_t *>(ws), BH, (int)nslot,
+                                                (int)items, static_cast<__nv_bfloat16 *>(tpb), tsc);
     return cudaGetLastError();
 }
 

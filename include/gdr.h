@@ -419,20 +419,24 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
  * Training: a forward that keeps what its backward needs.  The chain of the
  * two-kernel path already forms, chunk by chunk, the state M_n at every chunk
  * start and the tile W_n = T diag(beta) E of the chunk ("What a Trillion-Parameter
- * MoE Model Reveals About the Next Stage of LLM Scaling", sections 3.2-3.3); the
- * backward of gdr_chunk_bwd recomputes both from the inputs in a sequential pass
- * of its own.  gdr_chunk_fwd_train writes them out as it goes, and
- * gdr_chunk_bwd_saved reads them instead of recomputing: one sequential pass
- * fewer and no U / W products in the backward.
+ * MoE Model Reveals About the Next Stage of LLM Scaling", sections 3.2-3.3), and
+ * its per-chunk kernel the triangular inverse T = (I + A)^-1, the masked decayed
+ * scores P and the cumulative decay; the backward of gdr_chunk_bwd recomputes all
+ * of them from the inputs.  gdr_chunk_fwd_train writes them out as it goes, and
+ * gdr_chunk_bwd_saved reads them instead of recomputing: no forward-state pass,
+ * no decay or per-chunk tile kernel in the backward.
  *
  * Shape: bf16, dk = dv = 128, chunk 64 (GDR_ERR_UNSUPPORTED otherwise), dense
  * [B,H,T,d] tensors.
  *
- * gdr_chunk_saved_size: bytes of the saved buffer, B * H * ceil(T / 64) *
- *   128 * (128 + 64) * 2: per (b, h, chunk n) the state M_n transposed (bf16
- *   [128 value rows][128 key columns], all the states first) and then W_n
- *   transposed (bf16 [128 value rows][64 chunk positions], zero past T).  0 for
- *   unsupported arguments or empty work.  Host-only.
+ * gdr_chunk_saved_size: bytes of the saved buffer, B * H * ceil(T / 64) * 66560,
+ *   four regions each over (b, h, chunk n) in that order: the states M_n
+ *   transposed (bf16 [128 value rows][128 key columns]); the tiles W_n
+ *   transposed (bf16 [128 value rows][64 chunk positions], zero past T); T_n and
+ *   P_n (bf16 [64][64] each, T first; past T the rows of T are the identity's and
+ *   those of P zero); the row scalars (fp32 [4][64]: gamma_r, 1 / gamma_r, beta_r,
+ *   d log(alpha_r) / d g_r; 1, 1, 0, 0 past T).  0 for unsupported arguments or
+ *   empty work.  Host-only.
  * gdr_chunk_fwd_train: gdr_chunk_fwd_ex on the two-kernel path (sequence
  *   segments included) that also fills `saved`.  The workspace is required (at
  *   least gdr_chunk_fwd_workspace_size bytes) and so is `saved` (device memory
@@ -446,7 +450,7 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
  *   read only and may be released once `stream` has passed the call.  d_q, d_k,
  *   d_v must be 16-byte aligned as well (GDR_ERR_INVALID_ARG otherwise); the
  *   workspace is gdr_chunk_bwd_workspace_size bytes; the range rule over the
- *   chunk as gdr_chunk_bwd.  Four launches.  The states are the forward's bf16
+ *   chunk as gdr_chunk_bwd.  Two launches.  The states are the forward's bf16
  *   operands, so the gradients differ from gdr_chunk_bwd's by about the bf16
  *   rounding of the states (both ~3e-3 relative L2 against an fp64 reference).
  *   B * H = 0 or T = 0 is gdr_chunk_bwd.

@@ -75,8 +75,9 @@ def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False, decay="affine"):
     or None.  Returns (out [T,dv], M_final [dk,dv], intermediates or None).
 
     With ``keep`` the per-chunk intermediates are returned as a dict of lists:
-    gamma, A, T, U, Wk, W, M (state at each chunk start).  The last chunk may be
-    shorter than C (ragged tail): it is the same algebra on fewer rows.
+    gamma, A, T, U, Wk, W, M (state at each chunk start), P (the masked decayed
+    scores).  The last chunk may be shorter than C (ragged tail): it is the same
+    algebra on fewer rows.
     """
     q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
     g, beta = np.asarray(g, np.float64), np.asarray(beta, np.float64)
@@ -85,7 +86,7 @@ def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False, decay="affine"):
     M = np.zeros((dk, dv)) if M0 is None else np.array(M0, np.float64)
     _, gam_all, _ = chunk_decay(g, a_min, C, decay)
     out = np.empty((T, dv))
-    inter = {n: [] for n in ("gamma", "A", "T", "U", "Wk", "W", "M")} if keep else None
+    inter = {n: [] for n in ("gamma", "A", "T", "U", "Wk", "W", "M", "P")} if keep else None
     for n0 in range(0, T, C):
         sl = slice(n0, min(n0 + C, T))
         K, Q, V, bt, gam = k[sl], q[sl], v[sl], beta[sl], gam_all[sl]
@@ -99,10 +100,11 @@ def head(q, k, v, g, beta, a_min, M0=None, C=64, keep=False, decay="affine"):
         U = Tm @ (bt[:, None] * V)
         Wk = Tm @ ((bt * gam)[:, None] * K)
         W = U - Wk @ M
-        out[sl] = Q_hat @ M + np.tril(Q_hat @ K_hat.T) @ W
+        P = np.tril(Q_hat @ K_hat.T)
+        out[sl] = Q_hat @ M + P @ W
         if keep:
             for name, val in (("gamma", gam), ("A", A), ("T", Tm), ("U", U),
-                              ("Wk", Wk), ("W", W), ("M", M.copy())):
+                              ("Wk", Wk), ("W", W), ("M", M.copy()), ("P", P)):
                 inter[name].append(val)
         M = gC * M + K_til.T @ W
     return out, M, inter

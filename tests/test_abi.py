@@ -348,9 +348,12 @@ def test_chunk_saved_size(lib):
     f = lib.gdr_chunk_saved_size
     f.argtypes = [ctypes.c_int] * 7
     f.restype = ctypes.c_size_t
-    # per (b, h, chunk): the state transposed (128 x 128) and W transposed (128 x 64), bf16
-    assert f(2, 3, 100, 128, 128, 64, 1) == 2 * 3 * 2 * 128 * (128 + 64) * 2
-    assert f(1, 1, 64, 128, 128, 64, 1) == 128 * 192 * 2
+    # per (b, h, chunk): the state transposed (128 x 128) and W transposed (128 x 64),
+    # T and P (64 x 64 each), bf16; four rows of 64 fp32 scalars
+    per = 128 * (128 + 64) * 2 + 2 * 64 * 64 * 2 + 4 * 64 * 4
+    assert per == 66560
+    assert f(2, 3, 100, 128, 128, 64, 1) == 2 * 3 * 2 * per
+    assert f(1, 1, 64, 128, 128, 64, 1) == per
     assert f(1, 1, 0, 128, 128, 64, 1) == 0 and f(0, 1, 64, 128, 128, 64, 1) == 0
     assert f(1, 1, 64, 128, 128, 64, 0) == 0      # fp32: not the two-kernel path
     assert f(1, 1, 64, 64, 128, 64, 1) == 0 and f(1, 1, 64, 128, 128, 32, 1) == 0

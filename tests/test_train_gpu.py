@@ -3,10 +3,12 @@ the C ABI) against the oracles on the same seeded inputs.
 
 * The training forward's out and final state are bit-identical to gdr_chunk_fwd_ws
   (the same kernels; saving only adds stores).
-* The saved buffer: every chunk's state M_n and tile W_n against the chunked oracle's
-  intermediates (oracle.chunkwise.head, itself checked against the token loop), to
-  5e-3 relative L2 (bf16 tiles of fp32 values, 2^-9 per element, plus the forward's
-  own bf16 operand rounding); rows of W past the end of the sequence are zero.
+* The saved buffer: every chunk's state M_n, tile W_n, triangular inverse T_n and
+  masked decayed scores P_n against the chunked oracle's intermediates
+  (oracle.chunkwise.head, itself checked against the token loop), to 5e-3 relative
+  L2 (bf16 tiles of fp32 values, 2^-9 per element, plus the forward's own bf16
+  operand rounding), with the padding past the end of the sequence exact; the row
+  scalars against the oracle's decay and a difference quotient of its log alpha.
 * The saved-state backward against the fp64 oracle's gradients, 5e-3 relative L2
   per gradient (the tolerance of the recomputing bf16 backward, which it tracks:
   both read bf16 states), with ragged tails, sequence segments on and off, no
@@ -38,13 +40,19 @@ def _lib():
 
 
 def saved_views(saved, B, H, T):
-    """(states [B*H, NC, dk, dv] as M, W [B*H, NC, 64, dv]) from the saved buffer."""
+    """The saved buffer's four regions: states [B*H, NC, dk, dv] as M, W [B*H, NC, 64, dv],
+    T and P [B*H, NC, 64, 64], row scalars [B*H, NC, 4, 64] (gamma, 1 / gamma, beta,
+    d log(alpha) / dg)."""
     NC = (T + 63) // 64
     BH = B * H
-    flat = saved[: gdr.chunk_saved_size(B, H, T, 128, 128)].view(torch.bfloat16)
-    st = flat[: BH * NC * 128 * 128].view(BH, NC, 128, 128)        # [j][i] = M[i][j]
-    wt = flat[BH * NC * 128 * 128:].view(BH, NC, 128, 64)          # [j][s] = W[s][j]
-    return st.transpose(-1, -2).float(), wt.transpose(-1, -2).float()
+    raw = saved[: gdr.chunk_saved_size(B, H, T, 128, 128)]
+    n_st, n_w, n_tp = BH * NC * 128 * 128, BH * NC * 128 * 64, BH * NC * 2 * 64 * 64
+    flat = raw[: 2 * (n_st + n_w + n_tp)].view(torch.bfloat16)
+    st = flat[:n_st].view(BH, NC, 128, 128)                        # [j][i] = M[i][j]
+    wt = flat[n_st:n_st + n_w].view(BH, NC, 128, 64)               # [j][s] = W[s][j]
+    tp = flat[n_st + n_w:].view(BH, NC, 2, 64, 64).float()
+    sc = raw[2 * (n_st + n_w + n_tp):].view(torch.float32).view(BH, NC, 4, 64)
+    return st.transpose(-1, -2).float(), wt.transpose(-1, -2).float(), tp[:, :, 0], tp[:, :, 1], sc
 
 
 def train_fwd(x, w, bound=None, decay="affine", init=True):
@@ -76,7 +84,7 @@ def test_saved_states_and_w_tiles(T, segments, split):
     with gdr.option(segments=segments, chain_split=split):
         _, _, saved = train_fwd(x, w)
     torch.cuda.synchronize()
-    st, wt = saved_views(saved, w.B, w.H, T)
+    st, wt, tt, pt, sc = saved_views(saved, w.B, w.H, T)
     cpu = {n: t.float().cpu().numpy() for n, t in x.items()}
     for h in range(w.H):
         _, _, inter = chunkwise.head(cpu["q"][0, h], cpu["k"][0, h], cpu["v"][0, h],
@@ -87,6 +95,46 @@ def test_saved_states_and_w_tiles(T, segments, split):
             c = W.shape[0]
             assert oracle.rel_l2(wt[h, n, :c], W) <= TOL, (h, n)
             assert not wt[h, n, c:].any()                     # past the end: zero
+            # T, P: bf16 tiles; past the end, the identity's rows and zero rows
+            assert oracle.rel_l2(tt[h, n, :c, :c], inter["T"][n]) <= TOL, (h, n)
+            assert oracle.rel_l2(pt[h, n, :c, :c], inter["P"][n]) <= TOL, (h, n)
+            assert not tt[h, n, :c, c:].any() and not pt[h, n, :, c:].any()
+            assert torch.equal(tt[h, n, c:, c:], torch.eye(64 - c, device=tt.device)) and not tt[h, n, c:, :c].any()
+            assert not pt[h, n, c:].any()
+
+
+@pytest.mark.parametrize("T,segments,decay", [(64, 1, "affine"), (333, 1, "affine"),
+                                              (1600, 3, "affine"), (257, 1, "log")])
+def test_saved_row_scalars(T, segments, decay):
+    """The forward's per-chunk row scalars: gamma and 1 / gamma against the oracle's
+    cumulative decay (fp32 exponent of an fp32 sum: 1e-5 relative), beta exactly, and
+    d log(alpha) / dg against a central difference of the oracle's log alpha in fp64
+    (step 1e-4: error ~1e-9; 1e-4 relative for the fp32 1 - sigmoid); past the end
+    1, 1, 0, 0."""
+    w = I.PREFILL.with_(B=1, H=2, T=T)
+    x = I.prefill_inputs(w, device="cuda")
+    bound = w.a_min if decay == "affine" else -1.25
+    with gdr.option(segments=segments):
+        _, _, saved = train_fwd(x, w, bound, decay)
+    torch.cuda.synchronize()
+    sc = saved_views(saved, w.B, w.H, T)[4].cpu().double().numpy()
+    g = x["g"].cpu().double().numpy()
+    beta = x["beta"].cpu().numpy()
+    eps = 1e-4
+    for h in range(w.H):
+        _, gam, _ = chunkwise.chunk_decay(g[0, h], bound, 64, decay)
+        dla = (chunkwise.log_alpha(g[0, h] + eps, bound, decay)
+               - chunkwise.log_alpha(g[0, h] - eps, bound, decay)) / (2 * eps)
+        for n in range((T + 63) // 64):
+            sl = slice(64 * n, min(64 * n + 64, T))
+            c = sl.stop - sl.start
+            blk = sc[h, n]
+            np.testing.assert_allclose(blk[0, :c], gam[sl], rtol=1e-5)
+            np.testing.assert_allclose(blk[1, :c], 1.0 / gam[sl], rtol=1e-5)
+            assert np.array_equal(blk[2, :c], beta[0, h, sl].astype(np.float64))
+            np.testing.assert_allclose(blk[3, :c], dla[sl], rtol=1e-4, atol=1e-7)
+            assert (blk[0, c:] == 1).all() and (blk[1, c:] == 1).all()
+            assert not blk[2:, c:].any()
 
 
 def bwd_pair(w, *, segments=1, init=True, final=True, bound=None, decay="affine", split=0):
