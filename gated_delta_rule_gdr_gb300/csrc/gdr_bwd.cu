@@ -1055,6 +1055,15 @@ __device__ __forceinline__ void stage_rows(uint32_t dst, const void *src, int64_
     }
 }
 
+// 64 rows of 128 bytes whose 16-byte chunks are swizzled by row (chunk p of row r at
+// byte r * 128 + 16 (p ^ (r mod 8))) into plain rows sp bytes apart
+__device__ __forceinline__ void stage_rows_sw128(uint32_t dst, const void *src, int sp, int tid, int nthreads) {
+    for (int x = tid; x < 64 * 8; x += nthreads) {
+        const int r = x >> 3, p = x & 7;
+        cp_async16(dst + r * sp + 16 * p, static_cast<const char *>(src) + r * 128 + ((p ^ (r & 7)) << 4), 16u);
+    }
+}
+
 // [p, p + bytes) towards L2 (16-byte aligned, a multiple of 16 bytes)
 __device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -1960,7 +1969,10 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
             stage_rows(st + R_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
             stage_rows(st + R_Q, q + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
             stage_rows(st + R_T, tp, C * 2, C * 2, LC * 2, C, C, tid, NT);
-            stage_rows(st + R_P, tp + C * C, C * 2, C * 2, LC * 2, C, C, tid, NT);
+            if (rows)   // the forward's P: its tile half, swizzled
+                stage_rows_sw128(st + R_P, tp + C * C, LC * 2, tid, NT);
+            else
+                stage_rows(st + R_P, tp + C * C, C * 2, C * 2, LC * 2, C, C, tid, NT);
             stage_rows(st + R_O, dout + row0 * dv + j0, (int64_t)dv * 2, DSC * 2, LC * 2, C, c, tid, NT);
             if (tid < C) {
                 const int r = tid < c ? tid : 0;

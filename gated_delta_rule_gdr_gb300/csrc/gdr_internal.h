@@ -112,8 +112,8 @@ cudaError_t take_pair_error_word(unsigned *value);
 // then the state chain and outputs (gdr_chain.cu).  Same dense / packed layouts as
 // launch_fused_pair.
 size_t prep_workspace_bytes(int BH, int T, const int *cu_seqlens, int H, int total_T);
-// tpb, tsc (training, dense only): also every chunk's T and P as plain bf16 [64][64] tiles
-// ([BH][NC][2][64][64]) and its row scalars ([BH][NC][4][64] fp32: gamma, 1/gamma, beta,
+// tpb, tsc (training, dense only): also every chunk's T and P as bf16 [64][64] tiles
+// ([BH][NC][2][64][64]; T plain, P with the 128-byte swizzle of the prep tile) and its row scalars ([BH][NC][4][64] fp32: gamma, 1/gamma, beta,
 // d log(alpha)/dg), the inputs the backward's tiles and decay kernels would recompute.
 cudaError_t launch_prep(const void *q, const void *k, const float *g, const float *beta, float a_min,
                         void *ws, int BH, int T, const int *cu_seqlens, int H, int total_T,

@@ -20,9 +20,9 @@
 // prepares the current one.
 //
 // For training (tpb, tsc given) it also writes what the backward's tiles and
-// decay kernels would recompute: T and P as plain bf16 [64][64] tiles, and the
-// chunk's row scalars gamma, 1/gamma, beta, d log(alpha)/dg (rows past the
-// chunk's end 1, 1, 0, 0).
+// decay kernels would recompute: T as a plain bf16 [64][64] tile, P as the tile's
+// 128-byte-swizzled half, and the chunk's row scalars gamma, 1/gamma, beta,
+// d log(alpha)/dg (rows past the chunk's end 1, 1, 0, 0).
 //
 // CTA: 128 threads, three per SM.  Thread 0 issues the TMA loads, the
 // tensor-core product and the bulk store of each tile; warp 3 computes the
@@ -268,8 +268,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     u.z = pack_bf16x2(p8[4], p8[5]);
                     u.w = pack_bf16x2(p8[6], p8[7]);
                     *reinterpret_cast<uint4 *>(tile + LP_TILE_P + swz((uint32_t)r, (uint32_t)(half * 4 + q4))) = u;
-                    if (kTrain)   // training: the plain P tile for the backward
-                        *reinterpret_cast<uint4 *>(tpb + (((int64_t)bh * nslot + n) * 2 + 1) * C * C + r * C + sb) = u;
                 }
             }
         }
@@ -281,7 +279,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // Lb = strict_lower(T) diag(beta): row tid % 64, columns 16 q4 + 0..15
             const int r = tid & 63;
             float x[16];
-            float tt[16];   // T itself (lower triangle with the unit diagonal) for training
 #pragma unroll
             for (int s4 = 0; s4 < 16; s4 += 4) {
                 const int s0 = q4 * 16 + s4;
@@ -291,19 +288,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 x[s4 + 1] = (s0 + 1 < r) ? t.y * f.y : 0.f;
                 x[s4 + 2] = (s0 + 2 < r) ? t.z * f.z : 0.f;
                 x[s4 + 3] = (s0 + 3 < r) ? t.w * f.w : 0.f;
-                tt[s4 + 0] = (s0 + 0 <= r) ? t.x : 0.f;
-                tt[s4 + 1] = (s0 + 1 <= r) ? t.y : 0.f;
-                tt[s4 + 2] = (s0 + 2 <= r) ? t.z : 0.f;
-                tt[s4 + 3] = (s0 + 3 <= r) ? t.w : 0.f;
-            }
-            if (kTrain) {
-                __nv_bfloat16 *trow = tpb + ((int64_t)bh * nslot + n) * 2 * C * C + r * C + q4 * 16;
-                *reinterpret_cast<uint4 *>(trow) =
-                    make_uint4(pack_bf16x2(tt[0], tt[1]), pack_bf16x2(tt[2], tt[3]),
-                               pack_bf16x2(tt[4], tt[5]), pack_bf16x2(tt[6], tt[7]));
-                *reinterpret_cast<uint4 *>(trow + 8) =
-                    make_uint4(pack_bf16x2(tt[8], tt[9]), pack_bf16x2(tt[10], tt[11]),
-                               pack_bf16x2(tt[12], tt[13]), pack_bf16x2(tt[14], tt[15]));
             }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -315,11 +299,32 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *reinterpret_cast<uint4 *>(tile + swz((uint32_t)r, (uint32_t)(q4 * 2 + h2))) = u;
             }
         }
+        if (kTrain) {
+            // training: T (the unit lower triangle) as plain bf16 rows, each warp store
+            // covering four whole rows
+            __nv_bfloat16 *tdst = tpb + ((int64_t)bh * nslot + n) * 2 * C * C;
+#pragma unroll 1
+            for (int x = tid; x < C * 8; x += NT) {
+                const int r = x >> 3, c8 = x & 7;
+                const float4 t0 = *reinterpret_cast<const float4 *>(&As[r * LDA + 8 * c8]);
+                const float4 t1 = *reinterpret_cast<const float4 *>(&As[r * LDA + 8 * c8 + 4]);
+                const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                float m[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m[e] = (8 * c8 + e <= r) ? tv[e] : 0.f;
+                *reinterpret_cast<uint4 *>(tdst + r * C + 8 * c8) =
+                    make_uint4(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]), pack_bf16x2(m[4], m[5]),
+                               pack_bf16x2(m[6], m[7]));
+            }
+        }
         fence_proxy_async_smem();   // the tile leaves by a bulk copy (async proxy)
         __syncthreads();            // every thread is also done with the scalars and A
         if (tid == 0) {
             bulk_store(ws + ((int64_t)v.z * nslot + tile_slot0(a, bh, v) + n) * TILE_BYTES,
                        smem_u32(tile), TILE_BYTES);
+            // training: the P half as it is (128-byte rows, 16-byte chunks swizzled by row)
+            if (kTrain)
+                bulk_store(tpb + (((int64_t)bh * nslot + n) * 2 + 1) * C * C, smem_u32(tile) + LP_TILE_P, 8192);
             bulk_commit();
         }
         it = nx;
