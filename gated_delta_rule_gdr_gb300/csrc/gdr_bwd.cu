@@ -1098,6 +1098,12 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
 __device__ __forceinline__ uint32_t a_addr(uint32_t base, int ld, int R, int Kc, int lane) {
     return base + 2u * (uint32_t)((R + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + Kc + (lane >> 4) * 8);
 }
+// Element offset of (r, col) in a bf16 [64][64] tile of 128-byte rows whose 16-byte chunks
+// are swizzled by row (chunk c of row r at chunk c ^ (r mod 8)): the layout of the T and P
+// tiles the reverse chain copies in whole
+__device__ __forceinline__ int sw_elem(int r, int col) {
+    return r * 64 + ((((col >> 3) ^ (r & 7))) << 3) + (col & 7);
+}
 // A fragment of the transpose of a row-major tile X (A[r][s] = X[s][r]), for ldmatrix.trans
 __device__ __forceinline__ uint32_t at_addr(uint32_t base, int ld, int R, int Kc, int lane) {
     return base + 2u * (uint32_t)((Kc + (lane & 7) + (lane >> 4) * 8) * ld + R + ((lane >> 3) & 1) * 8);
@@ -1663,7 +1669,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
                 p[e] = (r < c && s <= r) ? D * aq[nt][2 * h + e] : 0.f;
                 dd[e] = (r < c && s < r) ? D * ak[nt][2 * h + e] : 0.f;
             }
-            *reinterpret_cast<uint32_t *>(Pb + r * C + s0) = pack_bf2(p[0], p[1]);
+            *reinterpret_cast<uint32_t *>(Pb + sw_elem(r, s0)) = pack_bf2(p[0], p[1]);
             *reinterpret_cast<float2 *>(As + r * LA + s0) = make_float2(bs[r] * dd[0], bs[r] * dd[1]);
         }
     // the blocks of T above the diagonal are zero
@@ -1704,7 +1710,7 @@ bwd_tiles_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         for (int u = 0; u < 4; ++u) {
             const int idx = tid + 256 * u, r = idx >> 4, s = (idx & 15) * 4;
             tv[u] = *reinterpret_cast<const float4 *>(Ts + r * LA + s);
-            *reinterpret_cast<uint2 *>(Tb + r * C + s) =
+            *reinterpret_cast<uint2 *>(Tb + sw_elem(r, s)) =
                 make_uint2(pack_bf2(tv[u].x, tv[u].y), pack_bf2(tv[u].z, tv[u].w));
         }
         // U and Wk feed only the forward-state recomputation, which saved states replace
@@ -1795,11 +1801,48 @@ constexpr int C = 64, DK = 128, NW = 4, NT = 32 * NW, DSC = 16 * NW, LD = DK + 8
 constexpr int LU = DSC + 4;
 constexpr uint32_t F_K = 0, F_WH = F_K + C * LD * 2, F_U = F_WH + C * LD * 2,
                    F_G = F_U + C * LU * 4, F_STAGE = F_G + C * 4;
-// reverse chain stage: k, q (bf16 [C][LD]); P, T (bf16 [C][LC]); dO[:, slice] (bf16 [C][LC]); gamma, beta
-constexpr uint32_t R_K = 0, R_Q = R_K + C * LD * 2, R_P = R_Q + C * LD * 2, R_T = R_P + C * LC * 2,
-                   R_O = R_T + C * LC * 2, R_G = R_O + C * LC * 2, R_B = R_G + C * 4, R_STAGE = R_B + C * 4;
-static_assert(F_STAGE % 16 == 0 && R_STAGE % 16 == 0, "16-byte stages");
+// reverse chain stage, filled by TMA and bulk copies: k, q (two 64-column slabs of [C rows]
+// [128 B] each), P, T, dO[:, slice] ([C rows][128 B]), all with the 128-byte swizzle; then
+// gamma and beta (the chunk's scalar block: 1 and 0 past its end)
+constexpr uint32_t R_K = 0, R_Q = 16384, R_P = 32768, R_T = 40960, R_O = 49152, R_G = 57344, R_B = R_G + C * 4,
+                   R_STAGE = 58368;
+constexpr uint32_t R_TX = 2 * 16384 + 3 * 8192 + 2 * C * 4;   // bytes landing per stage
+static_assert(F_STAGE % 16 == 0 && R_STAGE % 1024 == 0 && R_B + C * 4 <= R_STAGE, "stage layout");
 }  // namespace vc
+
+// Byte offset of element (row, col) (col a multiple of 8) of a tile of 64-column slabs
+// ([rows][128 B] each, slab bytes apart) whose 16-byte chunks are swizzled by row: the
+// layout TMA writes with the 128-byte swizzle, and in which eight consecutive rows of one
+// column block fall in eight different bank groups.
+__device__ __forceinline__ uint32_t sw_off(int row, int col, uint32_t slab) {
+    return (uint32_t)(col >> 6) * slab + (uint32_t)row * 128u +
+           ((((uint32_t)(col & 63) >> 3) ^ ((uint32_t)row & 7u)) << 4);
+}
+// at_addr, b_addr, bt_addr on such tiles
+__device__ __forceinline__ uint32_t at_sw(uint32_t base, uint32_t slab, int R, int Kc, int lane) {
+    return base + sw_off(Kc + (lane & 7) + (lane >> 4) * 8, R + ((lane >> 3) & 1) * 8, slab);
+}
+__device__ __forceinline__ uint32_t b_sw(uint32_t base, uint32_t slab, int N, int Kc, int lane) {
+    return base + sw_off(N + (lane & 7) + (lane >> 4) * 8, Kc + ((lane >> 3) & 1) * 8, slab);
+}
+__device__ __forceinline__ uint32_t bt_sw(uint32_t base, uint32_t slab, int N, int Kc, int lane) {
+    return base + sw_off(Kc + (lane & 7) + ((lane >> 3) & 1) * 8, N + (lane >> 4) * 8, slab);
+}
+
+// Sticky error word of this file's kernels (the reverse chain's bounded waits)
+__device__ unsigned g_bwd_error_word = 0;
+// Bounded wait of one thread on an mbarrier phase: false (and the error word raised)
+// once limit_ns pass; limit_ns = 0 gives up at once unless the phase is complete.
+__device__ __noinline__ bool pass_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (sm100::mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = sm100::global_timer_ns();
+    while (limit_ns > 0) {
+        if (sm100::mbar_try_wait_hint(bar, parity, 20000)) return true;
+        if (sm100::global_timer_ns() - t0 > limit_ns) break;
+    }
+    atomicOr(&g_bwd_error_word, kDevErrTimeout);
+    return false;
+}
 
 // A fragment (k block kk) from a 16-row accumulator tile acc[2 kk], acc[2 kk + 1]
 __device__ __forceinline__ void acc_to_a(const float (&x0)[4], const float (&x1)[4], uint32_t (&a)[4]) {
@@ -1943,47 +1986,43 @@ fwd_state_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__re
 // Reverse chain: per chunk dW^T = dO^T P + (dM'^T K^T) diag(gamma_C / gamma),
 // dR^T = dW^T T (stored as dR [token][dv], fp32), and
 // dM^T <- gamma_C dM'^T + (diag(gamma) dO)^T Q + (-diag(gamma beta) dR)^T K; writes dM'
-// of every chunk (value-major bf16) and the initial state's gradient (fp32).
+// of every chunk (value-major bf16) and the initial state's gradient (fp32).  Thread 0
+// of the pass fills the two stages by TMA (k, q, dO) and bulk copies (the swizzled T and
+// P tiles, the chunk's scalar block); each warp's lane 0 waits (bounded) on the stage's
+// mbarrier, and the warps leave together if a wait runs out.
 __device__ __forceinline__ void
-chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                    const float *__restrict__ gamma, const float *__restrict__ beta,
-                    const __nv_bfloat16 *__restrict__ dout, const float *dfinal,
-                    const __nv_bfloat16 *__restrict__ TPb, float *__restrict__ dR,
-                    __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv,
-                    const float *__restrict__ rows) {
+chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+           const CUtensorMap *tm_o, const float *dfinal, const __nv_bfloat16 *__restrict__ TPb,
+           float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv,
+           const float *__restrict__ rows, uint64_t limit_ns) {
     using namespace vc;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
     using sm100::mma16816;
+    __shared__ __align__(8) uint64_t r_bar[2];
     const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
     const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
     const uint32_t sb = sm100::smem_u32(smb);
     const int NC = (T + C - 1) / C;
     const int jw = j0 + 16 * warp;
-    auto issue = [&](int s, int n) {   // stage s takes chunk n (n < 0: nothing)
-        if (n >= 0) {
-            const uint32_t st = sb + (uint32_t)s * R_STAGE;
-            const int c = min(C, T - n * C);
-            const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
-            const __nv_bfloat16 *tp = TPb + ((int64_t)bh * NC + n) * 2 * C * C;
-            stage_rows(st + R_K, k + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
-            stage_rows(st + R_Q, q + row0 * DK, DK * 2, DK * 2, LD * 2, C, c, tid, NT);
-            stage_rows(st + R_T, tp, C * 2, C * 2, LC * 2, C, C, tid, NT);
-            if (rows)   // the forward's P: its tile half, swizzled
-                stage_rows_sw128(st + R_P, tp + C * C, LC * 2, tid, NT);
-            else
-                stage_rows(st + R_P, tp + C * C, C * 2, C * 2, LC * 2, C, C, tid, NT);
-            stage_rows(st + R_O, dout + row0 * dv + j0, (int64_t)dv * 2, DSC * 2, LC * 2, C, c, tid, NT);
-            if (tid < C) {
-                const int r = tid < c ? tid : 0;
-                // gamma and beta: the decay's rows, or the forward's saved block of the chunk
-                const float *gsrc = rows ? rows + ((int64_t)bh * NC + n) * 4 * C + r : gamma + row0 + r;
-                const float *bsrc = rows ? rows + ((int64_t)bh * NC + n) * 4 * C + 2 * C + r : beta + row0 + r;
-                cp_async4(st + R_G + 4 * tid, gsrc, tid < c ? 4u : 0u);
-                cp_async4(st + R_B + 4 * tid, bsrc, tid < c ? 4u : 0u);
-            }
-        }
-        cp_async_commit();
+    auto bar = [&](int s) { return sm100::smem_u32(&r_bar[s]); };
+    int issued[2] = {0, 0};   // thread 0: loads issued per stage
+    auto issue = [&](int s, int n) {   // stage s takes chunk n (n < 0: nothing); thread 0
+        if (n < 0) return;
+        const uint32_t st = sb + (uint32_t)s * R_STAGE, b = bar(s);
+        const __nv_bfloat16 *tp = TPb + ((int64_t)bh * NC + n) * 2 * C * C;
+        const float *blk = rows + ((int64_t)bh * NC + n) * 4 * C;
+        sm100::mbar_arrive_expect_tx(b, R_TX);
+        sm100::tma_load_3d(st + R_K, tm_k, b, 0, n * C, bh);
+        sm100::tma_load_3d(st + R_K + 8192, tm_k, b, 64, n * C, bh);
+        sm100::tma_load_3d(st + R_Q, tm_q, b, 0, n * C, bh);
+        sm100::tma_load_3d(st + R_Q + 8192, tm_q, b, 64, n * C, bh);
+        sm100::tma_load_3d(st + R_O, tm_o, b, j0, n * C, bh);
+        sm100::bulk_load(st + R_T, tp, 8192, b);
+        sm100::bulk_load(st + R_P, tp + C * C, 8192, b);
+        sm100::bulk_load(st + R_G, blk, C * 4, b);
+        sm100::bulk_load(st + R_B, blk + 2 * C, C * 4, b);
+        ++issued[s];
     };
     float dm[16][4];   // dM'^T: rows jw + gq (+ 8), key columns 8 nt + 2 t4 (+ 1)
 #pragma unroll
@@ -1993,8 +2032,15 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
             const int i = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
             dm[nt][e] = dfinal ? dfinal[((int64_t)bh * DK + i) * dv + j] : 0.f;
         }
-    issue(0, NC - 1);
-    issue(1, NC - 2);
+    if (tid == 0) {
+        sm100::mbar_init(bar(0), 1);
+        sm100::mbar_init(bar(1), 1);
+        sm100::fence_mbar_init();
+        issue(0, NC - 1);
+        issue(1, NC - 2);
+    }
+    sm100::named_sync(bar_id, NT);   // the barriers are initialised
+    bool ok = true;
     for (int it = 0; it < NC; ++it) {
         const int n = NC - 1 - it, s = it & 1;
         const int c = min(C, T - n * C);
@@ -2011,14 +2057,19 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
                     *reinterpret_cast<uint32_t *>(dst + (int64_t)(jw + gq + 8 * h) * DK + 8 * nt + 2 * t4) =
                         pack_bf2(dm[nt][2 * h], dm[nt][2 * h + 1]);
         }
-        cp_async_wait1();
-        sm100::named_sync(bar_id, NT);
+        // the stage has landed (each warp's lane 0 waits); all warps leave together otherwise
+        bool landed = true;
+        if (lane == 0) landed = pass_wait(bar(s), (uint32_t)(it >> 1) & 1u, limit_ns);
+        if (!sm100::named_and(bar_id, NT, landed)) {
+            ok = false;
+            break;
+        }
         const float gC = gs[c - 1];
         // dO^T fragments (k = token) and their gamma-scaled copies
         uint32_t ao[4][4], ag[4][4];
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            ldsm_x4_t(ao[ks], at_addr(st + R_O, LC, 16 * warp, 16 * ks, lane));
+            ldsm_x4_t(ao[ks], at_sw(st + R_O, 8192, 16 * warp, 16 * ks, lane));
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
                 const int r = 16 * ks + 2 * t4 + 8 * (x >> 1);
@@ -2037,7 +2088,7 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
 #pragma unroll
             for (int ks = np; ks < 4; ++ks) {   // P is lower triangular: P[m][r] = 0 for m < r
                 uint32_t b[4];
-                ldsm_x4_t(b, bt_addr(st + R_P, LC, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(b, bt_sw(st + R_P, 8192, 16 * np, 16 * ks, lane));
                 mma16816(a1[2 * np], ao[ks], b[0], b[1]);
                 mma16816(a1[2 * np + 1], ao[ks], b[2], b[3]);
             }
@@ -2048,7 +2099,7 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 uint32_t b[4];
-                ldsm_x4(b, b_addr(st + R_K, LD, 16 * np, 16 * kk, lane));
+                ldsm_x4(b, b_sw(st + R_K, 8192, 16 * np, 16 * kk, lane));
                 mma16816(a2[2 * np], a, b[0], b[1]);
                 mma16816(a2[2 * np + 1], a, b[2], b[3]);
             }
@@ -2078,7 +2129,7 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
 #pragma unroll
             for (int np = 0; np <= ks; ++np) {
                 uint32_t b[4];
-                ldsm_x4_t(b, bt_addr(st + R_T, LC, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(b, bt_sw(st + R_T, 8192, 16 * np, 16 * ks, lane));
                 mma16816(a2[2 * np], a, b[0], b[1]);
                 mma16816(a2[2 * np + 1], a, b[2], b[3]);
             }
@@ -2103,8 +2154,8 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
 #pragma unroll
             for (int np = 0; np < 8; ++np) {
                 uint32_t bq[4], bk[4];
-                ldsm_x4_t(bq, bt_addr(st + R_Q, LD, 16 * np, 16 * ks, lane));
-                ldsm_x4_t(bk, bt_addr(st + R_K, LD, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bq, bt_sw(st + R_Q, 8192, 16 * np, 16 * ks, lane));
+                ldsm_x4_t(bk, bt_sw(st + R_K, 8192, 16 * np, 16 * ks, lane));
                 mma16816(dm[2 * np], ag[ks], bq[0], bq[1]);
                 mma16816(dm[2 * np + 1], ag[ks], bq[2], bq[3]);
                 mma16816(dm[2 * np], ar, bk[0], bk[1]);
@@ -2112,9 +2163,15 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
             }
         }
         sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
-        issue(s, n - 2);
+        if (tid == 0) issue(s, n - 2);
     }
-    if (dinit) {
+    if (!ok && tid == 0) {
+        // a wait ran out: the latest copies of each stage (its phases complete in order)
+        // land before the CTA leaves
+        for (int x = 0; x < 2; ++x)
+            if (issued[x] > 0) sm100::mbar_wait(bar(x), (uint32_t)(issued[x] - 1) & 1u, 2000000000ull);
+    }
+    if (ok && dinit) {
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
@@ -2130,22 +2187,25 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const __nv_bfloat16 *__restri
 // chain for the same 64 value columns, each role with its own stages and named barrier:
 // every SM sub-partition gets one warp of each, whose latencies hide each other.
 __global__ void __launch_bounds__(2 * vc::NT, 1)
-bwd_passes_vc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ gamma,
-                     const float *__restrict__ beta, const float *__restrict__ U,
+bwd_passes_vc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_o, const __nv_bfloat16 *__restrict__ k,
+                     const float *__restrict__ gamma, const float *__restrict__ U,
                      const __nv_bfloat16 *__restrict__ Wk2, const __nv_bfloat16 *__restrict__ TPb,
                      const float *init, const float *dfinal, __nv_bfloat16 *__restrict__ Wt,
                      __nv_bfloat16 *__restrict__ Sb, float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb,
-                     float *dinit, int T, int dv, int fwd_role, const float *__restrict__ rows) {
-    extern __shared__ __align__(16) uint8_t smb[];
+                     float *dinit, int T, int dv, int fwd_role, const float *__restrict__ rows,
+                     uint64_t limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base (the reverse chain's swizzled tiles), derived from the
+    // __shared__ array so that accesses through it stay shared-memory accesses
+    uint8_t *smb = smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x;
     // fwd_role = 0: the forward saved W^T and the states; only the reverse chain runs (the
     // two roles share no barrier, so the first four warps simply leave)
     if (tid < vc::NT) {
-        if (fwd_role) fwd_state_pass(smb, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
+        if (fwd_role) fwd_state_pass(smb + 2 * vc::R_STAGE, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
     } else
-        chain_pass(smb + 2 * vc::F_STAGE, tid - vc::NT, 2, q, k, gamma, beta, dout, dfinal, TPb, dR, dSb,
-                   dinit, T, dv, rows);
+        chain_pass(smb, tid - vc::NT, 2, &tm_q, &tm_k, &tm_o, dfinal, TPb, dR, dSb, dinit, T, dv, rows, limit_ns);
 }
 
 template <typename K>
@@ -2216,15 +2276,20 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
                 if ((err = bwd_set_smem(bwd_tiles_mma_kernel, mt::SMEM)) != cudaSuccess) return err;
                 // the tensor-core per-chunk kernel takes each chunk's row scalars (gamma, 1 / gamma,
                 // beta, d log(alpha) / dg; 1 KB) from the P-tile region, which this shape leaves unused
+                // (also the reverse chain's gamma and beta)
                 bwd_tiles_mma_kernel<<<dim3(NC, BH), 256, mt::SMEM, s>>>(q, k, v, gamma, beta, TPb, U, Wk2, T,
-                                                                         saved ? 0 : 1, g, d, tc_chunk ? Pt : nullptr);
+                                                                         saved ? 0 : 1, g, d, Pt);
                 if ((err = cudaGetLastError()) != cudaSuccess) return err;
+                rows = Pt;
             }
-            const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE;
+            CUtensorMap mq, mk, mo;
+            if (!make_rows_map(&mq, q, BH, T) || !make_rows_map(&mk, k, BH, T) || !make_rows_map(&mo, dout, BH, T))
+                return cudaErrorInvalidValue;
+            const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE + 1024;
             if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
             bwd_passes_vc_kernel<<<dim3(dv / vc::DSC, BH), 2 * vc::NT, sp, s>>>(
-                q, k, dout, gamma, beta, U, Wk2, TPin, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv,
-                saved ? 0 : 1, rows);
+                mq, mk, mo, k, gamma, U, Wk2, TPin, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv,
+                saved ? 0 : 1, rows, opt_wait_limit_ns());
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {
@@ -2342,6 +2407,19 @@ cudaError_t launch_bwd(const void *q, const void *k, const void *v, const float 
         (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, g, beta, d,
         init, (const __nv_bfloat16 *)dout, dfinal, (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk_out,
         (__nv_bfloat16 *)dv_out, dg, dbeta, dinit, BH, T, dk, dv, C, w, e, s, saved);
+}
+
+// Reads and clears the error word of this file's kernels (synchronous).
+cudaError_t take_bwd_error_word(unsigned *value) {
+    unsigned word = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&word, g_bwd_error_word, sizeof(word));
+    if (e != cudaSuccess) return e;
+    *value = word;
+    if (word != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_bwd_error_word, &zero, sizeof(zero));
+    }
+    return e;
 }
 
 }  // namespace gdr

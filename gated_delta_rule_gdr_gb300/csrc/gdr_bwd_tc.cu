@@ -716,4 +716,6 @@ cudaError_t launch_bwd_chunk_tc(const void *q, const void *k, const void *v, con
 
 cudaError_t take_bwd_tc_error_word(unsigned *value) { return take_error_word(value); }
 
+bool make_rows_map(CUtensorMap *m, const void *ptr, int BH, int T) { return make_map(m, ptr, BH, T); }
+
 }  // namespace gdr

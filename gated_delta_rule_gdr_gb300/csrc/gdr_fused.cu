@@ -640,7 +640,9 @@ cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned *value) {
     unsigned m = 0, t = 0;
     if (e == cudaSuccess) e = take_mla_error_word(&m);
     if (e == cudaSuccess) e = take_bwd_tc_error_word(&t);
-    *value = a | b | c | d | f | m | t;
+    unsigned r = 0;
+    if (e == cudaSuccess) e = take_bwd_error_word(&r);
+    *value = a | b | c | d | f | m | t | r;
     return e;
 }
 

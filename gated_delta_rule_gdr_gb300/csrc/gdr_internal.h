@@ -3,6 +3,7 @@
 // include/gdr.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -159,6 +160,9 @@ inline float *segment_states(float *seg_ws, int BH, int S) {
 cudaError_t take_segment_error_word(unsigned *value);
 // Read and clear the device error words of the two kernels (synchronous).
 cudaError_t take_prep_error_word(unsigned *value);
+cudaError_t take_bwd_error_word(unsigned *value);
+// TMA map of a bf16 [BH][T][128] tensor: 64 x 64 boxes, 128-byte swizzle, zero fill past T
+bool make_rows_map(CUtensorMap *m, const void *ptr, int BH, int T);
 cudaError_t take_chain_error_word(unsigned *value);
 
 // ---- one decode step of gated multi-head latent attention (gdr_mla.cu) ----

@@ -20,8 +20,8 @@
 // prepares the current one.
 //
 // For training (tpb, tsc given) it also writes what the backward's tiles and
-// decay kernels would recompute: T as a plain bf16 [64][64] tile, P as the tile's
-// 128-byte-swizzled half, and the chunk's row scalars gamma, 1/gamma, beta,
+// decay kernels would recompute: T and P as bf16 [64][64] tiles with the 128-byte
+// swizzle (P is the tile's half as it is), and the chunk's row scalars gamma, 1/gamma, beta,
 // d log(alpha)/dg (rows past the chunk's end 1, 1, 0, 0).
 //
 // CTA: 128 threads, three per SM.  Thread 0 issues the TMA loads, the
@@ -300,8 +300,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
         }
         if (kTrain) {
-            // training: T (the unit lower triangle) as plain bf16 rows, each warp store
-            // covering four whole rows
+            // training: T (the unit lower triangle) as bf16 rows with the tile's 128-byte
+            // swizzle, each warp store covering four whole rows
             __nv_bfloat16 *tdst = tpb + ((int64_t)bh * nslot + n) * 2 * C * C;
 #pragma unroll 1
             for (int x = tid; x < C * 8; x += NT) {
@@ -312,7 +312,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 float m[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m[e] = (8 * c8 + e <= r) ? tv[e] : 0.f;
-                *reinterpret_cast<uint4 *>(tdst + r * C + 8 * c8) =
+                *reinterpret_cast<uint4 *>(tdst + r * C + ((c8 ^ (r & 7)) << 3)) =
                     make_uint4(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]), pack_bf16x2(m[4], m[5]),
                                pack_bf16x2(m[6], m[7]));
             }

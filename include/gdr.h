@@ -434,7 +434,7 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
  *   transposed (bf16 [128 value rows][128 key columns]); the tiles W_n
  *   transposed (bf16 [128 value rows][64 chunk positions], zero past T); T_n and
  *   P_n (bf16 [64][64] each, T first; past T the rows of T are the identity's and
- *   those of P zero; P's 128-byte rows hold their 16-byte chunks swizzled, chunk c
+ *   those of P zero; their 128-byte rows hold the 16-byte chunks swizzled, chunk c
  *   of row r at byte 128 r + 16 (c XOR (r mod 8))); the row scalars (fp32 [4][64]: gamma_r, 1 / gamma_r, beta_r,
  *   d log(alpha_r) / d g_r; 1, 1, 0, 0 past T).  0 for unsupported arguments or
  *   empty work.  Host-only.

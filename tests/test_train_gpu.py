@@ -50,13 +50,14 @@ def saved_views(saved, B, H, T):
     flat = raw[: 2 * (n_st + n_w + n_tp)].view(torch.bfloat16)
     st = flat[:n_st].view(BH, NC, 128, 128)                        # [j][i] = M[i][j]
     wt = flat[n_st:n_st + n_w].view(BH, NC, 128, 64)               # [j][s] = W[s][j]
-    tp = flat[n_st + n_w:].view(BH, NC, 2, 64, 64).float()
-    # P's 16-byte chunks are swizzled by row: plain chunk c of row r is stored chunk c ^ (r % 8)
+    tp = flat[n_st + n_w:].view(BH, NC, 2, 64, 8, 8).float()
+    # T and P have their 16-byte chunks swizzled by row: plain chunk c of row r is stored
+    # chunk c ^ (r % 8)
     r = torch.arange(64, device=saved.device)[:, None]
     c = torch.arange(8, device=saved.device)[None, :]
-    pt = tp[:, :, 1].reshape(BH, NC, 64, 8, 8)[:, :, r, c ^ (r % 8), :].reshape(BH, NC, 64, 64)
+    tp = tp[:, :, :, r, c ^ (r % 8), :].reshape(BH, NC, 2, 64, 64)
     sc = raw[2 * (n_st + n_w + n_tp):].view(torch.float32).view(BH, NC, 4, 64)
-    return st.transpose(-1, -2).float(), wt.transpose(-1, -2).float(), tp[:, :, 0], pt, sc
+    return st.transpose(-1, -2).float(), wt.transpose(-1, -2).float(), tp[:, :, 0], tp[:, :, 1], sc
 
 
 def train_fwd(x, w, bound=None, decay="affine", init=True):
