@@ -2007,22 +2007,30 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
     const int jw = j0 + 16 * warp;
     auto bar = [&](int s) { return sm100::smem_u32(&r_bar[s]); };
     int issued[2] = {0, 0};   // thread 0: loads issued per stage
-    auto issue = [&](int s, int n) {   // stage s takes chunk n (n < 0: nothing); thread 0
-        if (n < 0) return;
+    // Stage s takes chunk n (n < 0: nothing): lane 0 of each warp issues a share of the
+    // copies (thread 0 first arms the barrier with all the bytes; a copy that lands
+    // before that only leaves the phase waiting for the arrival).
+    auto issue = [&](int s, int n) {
+        if (n < 0 || lane != 0) return;
         const uint32_t st = sb + (uint32_t)s * R_STAGE, b = bar(s);
         const __nv_bfloat16 *tp = TPb + ((int64_t)bh * NC + n) * 2 * C * C;
         const float *blk = rows + ((int64_t)bh * NC + n) * 4 * C;
-        sm100::mbar_arrive_expect_tx(b, R_TX);
-        sm100::tma_load_3d(st + R_K, tm_k, b, 0, n * C, bh);
-        sm100::tma_load_3d(st + R_K + 8192, tm_k, b, 64, n * C, bh);
-        sm100::tma_load_3d(st + R_Q, tm_q, b, 0, n * C, bh);
-        sm100::tma_load_3d(st + R_Q + 8192, tm_q, b, 64, n * C, bh);
-        sm100::tma_load_3d(st + R_O, tm_o, b, j0, n * C, bh);
-        sm100::bulk_load(st + R_T, tp, 8192, b);
-        sm100::bulk_load(st + R_P, tp + C * C, 8192, b);
-        sm100::bulk_load(st + R_G, blk, C * 4, b);
-        sm100::bulk_load(st + R_B, blk + 2 * C, C * 4, b);
-        ++issued[s];
+        if (warp == 0) {
+            sm100::mbar_arrive_expect_tx(b, R_TX);
+            sm100::tma_load_3d(st + R_K, tm_k, b, 0, n * C, bh);
+            sm100::tma_load_3d(st + R_K + 8192, tm_k, b, 64, n * C, bh);
+            ++issued[s];
+        } else if (warp == 1) {
+            sm100::tma_load_3d(st + R_Q, tm_q, b, 0, n * C, bh);
+            sm100::tma_load_3d(st + R_Q + 8192, tm_q, b, 64, n * C, bh);
+        } else if (warp == 2) {
+            sm100::tma_load_3d(st + R_O, tm_o, b, j0, n * C, bh);
+            sm100::bulk_load(st + R_T, tp, 8192, b);
+        } else {
+            sm100::bulk_load(st + R_P, tp + C * C, 8192, b);
+            sm100::bulk_load(st + R_G, blk, C * 4, b);
+            sm100::bulk_load(st + R_B, blk + 2 * C, C * 4, b);
+        }
     };
     float dm[16][4];   // dM'^T: rows jw + gq (+ 8), key columns 8 nt + 2 t4 (+ 1)
 #pragma unroll
@@ -2036,10 +2044,13 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
         sm100::mbar_init(bar(0), 1);
         sm100::mbar_init(bar(1), 1);
         sm100::fence_mbar_init();
-        issue(0, NC - 1);
-        issue(1, NC - 2);
+        sm100::tma_prefetch_desc(tm_q);
+        sm100::tma_prefetch_desc(tm_k);
+        sm100::tma_prefetch_desc(tm_o);
     }
     sm100::named_sync(bar_id, NT);   // the barriers are initialised
+    issue(0, NC - 1);
+    issue(1, NC - 2);
     bool ok = true;
     for (int it = 0; it < NC; ++it) {
         const int n = NC - 1 - it, s = it & 1;
@@ -2163,11 +2174,12 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
             }
         }
         sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
-        if (tid == 0) issue(s, n - 2);
+        issue(s, n - 2);
     }
     if (!ok && tid == 0) {
-        // a wait ran out: the latest copies of each stage (its phases complete in order)
-        // land before the CTA leaves
+        // a wait ran out: the latest copies of each stage (its phases complete in order;
+        // the other warps' copies of a phase complete it together with thread 0's) land
+        // before the CTA leaves
         for (int x = 0; x < 2; ++x)
             if (issued[x] > 0) sm100::mbar_wait(bar(x), (uint32_t)(issued[x] - 1) & 1u, 2000000000ull);
     }
