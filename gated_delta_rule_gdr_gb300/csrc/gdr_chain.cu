@@ -293,12 +293,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (NC == 0 && fin_view) store_state();   // an empty sequence: final = initial
         if (NC > 0) publish(0);
 
+        bool ready = false;   // chunk n's barriers were found complete during chunk n - 1
         for (int n = 0; n < NC; ++n) {
             const int wb = n & 1;
             const uint32_t st_a = stage(n);
             // ---- K, Q, v, [Lb | P] and the scalars of chunk n are in place, and the
             // Wt and MS buffers this chunk writes are free
-            if (!chunk_wait(n)) break;
+            if (!ready && !chunk_wait(n)) break;
             const Scal S = scal(n);
 
             // ---- X^T = S_J K^T (16 x 64, K = 128): A = bf16(S_J), B = K[s][i] rows
@@ -466,6 +467,16 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         mma16816(s[8 * slab + 2 * ip + 1], ef[ks], bq[qq % 3][ip][2], bq[qq % 3][ip][3]);
                     }
                 }
+            }
+            // while the state update's MMAs run: are chunk n + 1's barriers already
+            // complete (then its start needs no wait)?  Lanes 0 and 1 test one each.
+            {
+                bool t = n + 1 < NC;
+                if (t && lane == 0)
+                    t = mbar_test_wait(bar(B_FULL0 + (n + 1) % NST), (uint32_t)((n + 1) / NST) & 1u);
+                else if (t && lane == 1)
+                    t = mbar_test_wait(bar(B_SAFE0 + ((n + 1) & 1)), (uint32_t)(n >> 1) & 1u);
+                ready = __all_sync(0xffffffffu, t);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_FREE0 + n % NST));   // this warp is done with stage n
