@@ -347,8 +347,10 @@ def prefill_leg_line(gdr, w, ms, pk, pk_kind, world, max_over_ranks):
 
 
 CSRC = "gated_delta_rule_gdr_gb300/csrc/"
-# the four launches of one backward step on the bf16, d = 128, chunk 64 shape
-BWD_KERNELS = ("backward: decay_kernel + bwd_tiles_mma_kernel + bwd_passes_vc_kernel + "
+# the four launches of one backward step on the bf16, d = 128, chunk 64 shape: the training
+# forward into the workspace (its chain keeps the states and W tiles), then the saved-state
+# backward
+BWD_KERNELS = ("backward: chunk_prep_kernel<true> + chain_kernel<64> + bwd_passes_vc_kernel + "
                "bwd_chunk_tc_kernel")
 # one training step: the forward with saves (two-kernel path) and the saved-state backward
 # (the forward's prep kernel also writes T, P and the row scalars, so the backward runs
@@ -786,7 +788,9 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": BWD_KERNELS, "achieved": round(bgbs, 1),
                          "peak": pk["hbm_gbs"], "peak_kind": pk_kind, "unit": "GB/s",
                          "frac": round(bgbs / pk["hbm_gbs"], 4),
-                         "traffic": committed_traffic(BWD_KERNELS, BWD_SRCS + _COMMON, main_w.name),
+                         "traffic": committed_traffic(BWD_KERNELS, BWD_SRCS + _COMMON + [CSRC + "gdr_prep.cu",
+                                                                                       CSRC + "gdr_chain.cu"],
+                                                      main_w.name),
                          "algorithmic_bytes": bby},
             "workspace_bytes": bws, "gpu_launches": 4 * len(bms),
         }

@@ -560,6 +560,28 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
             (reinterpret_cast<uintptr_t>(workspace) & 15))
             return GDR_ERR_INVALID_ARG;
     }
+    // bf16, d = 128, chunk 64 (the default per-chunk kernel): the forward's intermediates come
+    // from the training forward, run into the part of the workspace the saved-state backward
+    // leaves free (its chain keeps every chunk's state and W tile, its preparation T, P and
+    // the row scalars), then the saved-state backward.  The forward's chain recomputes the
+    // states faster than the tiles kernel and the forward-state pass of the other path.
+    if (T > 0 && gdr::opt_bwd_variant() == 0 && range_ok(d, kTile) &&
+        gdr::bwd_saved_shape(dk, dv, chunk, elem_of(dtype), d_q, d_k, d_v)) {
+        size_t off = 0, room = 0;
+        gdr::bwd_free_region((int)BH, T, dk, dv, chunk, &off, &room);
+        auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+        const size_t sv = up(gdr::saved_bytes(BH, T)), ob = up((size_t)BH * T * dv * 2);
+        const size_t fw = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype);
+        if (fw > 0 && sv + ob + fw <= room) {
+            uint8_t *base = static_cast<uint8_t *>(workspace) + off;
+            const gdr_status_t st = two_kernel_fwd(q, k, v, g, beta, d, init_state, base + sv, nullptr,
+                                                   (int)BH, T, base + sv + ob, base, s);
+            if (st != GDR_OK) return st;
+            return from_cuda(gdr::launch_bwd(q, k, v, g, beta, d, init_state, d_out, d_final, d_q, d_k,
+                                             d_v, d_g, d_beta, d_init, (int)BH, T, dk, dv, chunk,
+                                             workspace, elem_of(dtype), s, base));
+        }
+    }
     return from_cuda(gdr::launch_bwd(q, k, v, g, beta, d, init_state, d_out, d_final, d_q, d_k,
                                      d_v, d_g, d_beta, d_init, (int)BH, T, dk, dv, chunk,
                                      workspace, elem_of(dtype), s));

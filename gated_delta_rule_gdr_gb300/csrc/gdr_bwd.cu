@@ -2388,6 +2388,13 @@ size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C) {
                             3 * round4((size_t)BH * NC * C * C));
 }
 
+void bwd_free_region(int BH, int T, int dk, int dv, int C, size_t *offset, size_t *bytes) {
+    const int NC = (T + C - 1) / C;
+    const size_t tok = (size_t)BH * T, st = (size_t)BH * NC * dk * dv;
+    *offset = sizeof(float) * round4(tok);   // after gamma: U, Wk, W, the states
+    *bytes = sizeof(float) * (round4(tok * dv) + round4(tok * dk) + round4((size_t)BH * NC * C * dv) + round4(st));
+}
+
 bool bwd_saved_shape(int dk, int dv, int C, Elem e, const void *dq, const void *dk_out,
                      const void *dv_out) {
     return e == Elem::BF16 && dk == 128 && dv == 128 && C == 64 &&

@@ -64,6 +64,9 @@ int opt_bwd_variant();
 // ---- backward of the chunked form (gdr_bwd.cu) ----
 bool bwd_supported(int dk, int dv, int C);
 size_t bwd_workspace_bytes(int BH, int T, int dk, int dv, int C);
+// The part of that workspace the saved-state backward (launch_bwd with `saved`) leaves
+// untouched: [offset, offset + bytes), 16-byte aligned.
+void bwd_free_region(int BH, int T, int dk, int dv, int C, size_t *offset, size_t *bytes);
 // saved != nullptr: the states and W^T saved by the forward (launch_chain's saved
 // buffer); the forward-state recomputation is skipped.  Only the bf16 d = 128 chunk-64
 // shape with 16-byte aligned d_q, d_k, d_v (bwd_saved_shape).

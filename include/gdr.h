@@ -383,11 +383,14 @@ gdr_status_t gdr_decode_step_ex(const void *q, const void *k, const void *v, con
  * reverse pass over the chunks carries dL/dM, and one fully parallel pass
  * forms every chunk's gradients.  fp32 arithmetic throughout, except for bf16
  * with dk = dv = 128, chunk 64 and 16-byte aligned d_q, d_k, d_v: there the
- * products run on tensor cores with bf16 operands and fp32 accumulation (the
- * recomputed states and W keep near-fp32 accuracy through split-bf16 operands;
- * the gradients measure ~3e-3 relative L2 against an fp64 reference, d_init
- * ~2e-3), in four launches instead of five; other shapes and fp32 stay on the
- * fp32 kernels (~3e-7).
+ * products run on tensor cores with bf16 operands and fp32 accumulation, and
+ * the intermediates come from gdr_chunk_fwd_train's kernels run into the
+ * workspace, followed by gdr_chunk_bwd_saved's (four launches; six with the
+ * sequence segments of few heads); the gradients measure ~3e-3 relative L2
+ * against an fp64 reference.  GDR_OPT_BWD_VARIANT 1 or 2 recompute them with
+ * the backward's own tiles kernel and forward-state pass instead (near-fp32
+ * states through split-bf16 operands, d_init ~2e-3; five launches).  Other
+ * shapes and fp32 stay on the fp32 kernels (~3e-7).
  *
  * q, k, v, g, beta, (decay, bound), init_state: as gdr_chunk_fwd_ex (the
  *          forward whose gradients are taken; init_state may be NULL = zeros).
@@ -522,9 +525,11 @@ gdr_status_t gdr_mla_decode(const void *q_abs, const void *ckv, const int *seqle
  *                          path: 0 chosen by head count (default), 1 or 2.
  *   GDR_OPT_SEGMENTS       sequence segments of the two-kernel path: 0 chosen by
  *                          head count (default), else that many (at most 4096).
- *   GDR_OPT_BWD_VARIANT    the per-chunk gradient kernel of the bf16 d = 128
- *                          chunk-64 backward: 0 default (tensor cores), 1 warp-level
- *                          MMAs, 2 tensor cores.
+ *   GDR_OPT_BWD_VARIANT    the bf16 d = 128 chunk-64 backward: 0 default (the
+ *                          training forward's kernels recompute the intermediates,
+ *                          per-chunk gradients on tensor cores), 1 the backward's own
+ *                          recomputation with the warp-level-MMA per-chunk kernel,
+ *                          2 the same with the tensor-core per-chunk kernel.
  * gdr_set_option returns GDR_ERR_INVALID_ARG for an unknown option or a value
  * out of its range; gdr_get_option returns the current value (-1 if unknown).
  * The library reads no environment variable.

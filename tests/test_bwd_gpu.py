@@ -92,9 +92,10 @@ def test_bwd_bf16_prefill_shape_optional_state_terms(init, final):
 @pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 300])
 def test_bwd_bf16_per_chunk_kernels(variant, T):
-    """Both per-chunk gradient kernels of the prefill shape: 1 warp-level MMAs, 2 the
-    tensor cores (the default), with ragged and single-chunk sequences, several heads
-    (the persistent grid walks several tasks per CTA at B = 3, H = 64, T = 300)."""
+    """Both per-chunk gradient kernels of the prefill shape after the backward's own
+    recomputation: 1 warp-level MMAs, 2 the tensor cores (the default's per-chunk
+    kernel), with ragged and single-chunk sequences, several heads (the persistent grid
+    walks several tasks per CTA at B = 3, H = 64, T = 300)."""
     w = I.PREFILL.with_(B=1, H=2, T=T) if T != 300 else I.PREFILL.with_(B=3, H=64, T=300)
     with gdr.option(bwd_variant=variant):
         got, ref = run(w)

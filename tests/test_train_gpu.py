@@ -206,12 +206,27 @@ def test_bwd_saved_tracks_the_recomputing_backward():
     fp32 values straddle a rounding boundary."""
     w = I.PREFILL.with_(B=2, H=4, T=1000)
     x, ct, init_state, d_final, got = bwd_pair(w)
-    rec = gdr.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, init_state,
-                        ct["d_out"], d_final)
+    with gdr.option(bwd_variant=2):   # the backward's own recomputation
+        rec = gdr.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, init_state,
+                            ct["d_out"], d_final)
     torch.cuda.synchronize()
     errs = {n: oracle.rel_l2(a, b) for n, a, b in zip(NAMES, got, rec)}
     print(" ".join(f"{n} {e:.2e}" for n, e in errs.items()))
     assert all(e <= TOL for e in errs.values()), errs
+
+
+def test_default_backward_is_the_saved_state_pair():
+    """gdr_chunk_bwd's default for this shape runs the training forward's kernels into
+    its workspace and then the saved-state backward: bit-identical to the pair called
+    by hand (the same kernels on the same inputs, deterministic reductions)."""
+    w = I.PREFILL.with_(B=2, H=4, T=1000)
+    x, ct, init_state, d_final, got = bwd_pair(w)
+    with gdr.option(segments=1):   # as bwd_pair's forward
+        dflt = gdr.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], w.a_min, init_state,
+                             ct["d_out"], d_final)
+    torch.cuda.synchronize()
+    for n, a, b in zip(NAMES, got, dflt):
+        assert torch.equal(a, b), n
 
 
 def test_train_pair_empty_sequence():
