@@ -302,7 +302,7 @@ namespace {
 gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float a_min, const float *init_state, void *out,
                             float *final_state, int BH, int T, void *workspace, void *saved,
-                            cudaStream_t s);
+                            cudaStream_t s, bool states_only = false);
 
 gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, const float *g,
                                const float *beta, float a_min, const float *init_state, void *out,
@@ -334,7 +334,7 @@ gdr_status_t chunk_fwd_ws_impl(const void *q, const void *k, const void *v, cons
 gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float a_min, const float *init_state, void *out,
                             float *final_state, int BH, int T, void *workspace, void *saved,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool states_only) {
     if (!q || !k || !v || !g || !beta || !out) return GDR_ERR_INVALID_ARG;
     const int S = gdr::segment_count(BH, T);
     // training: the preparation also leaves T, P and the row scalars in the saved buffer
@@ -346,7 +346,7 @@ gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const f
     if (S <= 1) {
         if (e == cudaSuccess)
             e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace,
-                                  BH, T, nullptr, 0, 0, s, 1, nullptr, saved);
+                                  BH, T, nullptr, 0, 0, s, 1, nullptr, saved, states_only);
         return from_cuda(e);
     }
     // sequence segments: their maps and the scan, then every segment's chain at once
@@ -357,7 +357,8 @@ gdr_status_t two_kernel_fwd(const void *q, const void *k, const void *v, const f
                                        S, s);
     if (e == cudaSuccess)
         e = gdr::launch_chain(q, k, v, g, beta, a_min, init_state, out, final_state, workspace, BH,
-                              T, nullptr, 0, 0, s, S, gdr::segment_states(seg_ws, BH, S), saved);
+                              T, nullptr, 0, 0, s, S, gdr::segment_states(seg_ws, BH, S), saved,
+                              states_only);
     return from_cuda(e);
 }
 
@@ -561,9 +562,9 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
             return GDR_ERR_INVALID_ARG;
     }
     // bf16, d = 128, chunk 64 (the default per-chunk kernel): the forward's intermediates come
-    // from the training forward, run into the part of the workspace the saved-state backward
-    // leaves free (its chain keeps every chunk's state and W tile, its preparation T, P and
-    // the row scalars), then the saved-state backward.  The forward's chain recomputes the
+    // from the training forward's kernels, run into the part of the workspace the saved-state
+    // backward leaves free (its chain, without the output products, keeps every chunk's state
+    // and W tile, its preparation T, P and the row scalars), then the saved-state backward.  The forward's chain recomputes the
     // states faster than the tiles kernel and the forward-state pass of the other path.
     if (T > 0 && gdr::opt_bwd_variant() == 0 && range_ok(d, kTile) &&
         gdr::bwd_saved_shape(dk, dv, chunk, elem_of(dtype), d_q, d_k, d_v)) {
@@ -574,8 +575,9 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const fl
         const size_t fw = gdr_chunk_fwd_workspace_size(B, H, T, dk, dv, chunk, dtype);
         if (fw > 0 && sv + ob + fw <= room) {
             uint8_t *base = static_cast<uint8_t *>(workspace) + off;
+            // (the forward's chain without its output products: only the states and W tiles)
             const gdr_status_t st = two_kernel_fwd(q, k, v, g, beta, d, init_state, base + sv, nullptr,
-                                                   (int)BH, T, base + sv + ob, base, s);
+                                                   (int)BH, T, base + sv + ob, base, s, true);
             if (st != GDR_OK) return st;
             return from_cuda(gdr::launch_bwd(q, k, v, g, beta, d, init_state, d_out, d_final, d_q, d_k,
                                              d_v, d_g, d_beta, d_init, (int)BH, T, dk, dv, chunk,

@@ -154,7 +154,10 @@ __device__ __noinline__ void stage_rows(uint32_t x, uint32_t y, int r, const flo
     }
 }
 
-template <int DVH>
+// SO (states only, with saving): the chain without the output products -- the
+// backward's recomputation of the states and W tiles, which needs no output; the
+// output thread only stores the published tiles, the copy warp loads no Q or P.
+template <int DVH, bool SO>
 __global__ void __launch_bounds__(ChainCfg<DVH>::NT, 1)
 chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -190,7 +193,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int i = 0; i < NUM_BARS; ++i) {
             uint32_t count = 1;
             if (i >= B_FULL0 && i < B_FULL0 + 3) count = 2;
-            if (i >= B_FREE0 && i < B_FREE0 + 3) count = NCH + 1;
+            if (i >= B_FREE0 && i < B_FREE0 + 3) count = SO ? NCH : NCH + 1;   // + the output warps
             if (i == B_MSREADY0 || i == B_MSREADY0 + 1) count = NCH;
             mbar_init(bar(i), count);
         }
@@ -198,8 +201,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         fence_mbar_init();
     }
     if (warp == NCH) {
-        tmem_alloc(smem_u32(&s_tmem), Cfg::TM_COLS);
-        tmem_relinquish();
+        if (!SO) {
+            tmem_alloc(smem_u32(&s_tmem), Cfg::TM_COLS);
+            tmem_relinquish();
+        }
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -210,7 +215,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = s_tmem;
+    const uint32_t tmem = SO ? 0u : s_tmem;
 
     if (warp < NCH) {
         // ================================================================ chain
@@ -485,6 +490,32 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             publish(n + 1);   // MS_{n+1} (if any) and W_n
             if (n + 1 == NC && fin_view) store_state();
         }
+    } else if (SO && warp == NCH + 1) {
+        // ================================================================ saves only
+        // Iteration m: once MS_m and W_{m-1} are published, their tiles leave by tensor
+        // stores; once the stores have read them, the chain may overwrite the buffers.
+        if (lane == 0) {
+            const int64_t x0 = (int64_t)sv.z * ((a.T + C - 1) / C) + sv.tz / C;
+            for (int m = 0; m <= NC && NC > 0; ++m) {
+                if (!role_wait(bar(B_MSREADY0 + (m & 1)), (uint32_t)(m >> 1) & 1u, a.limit_ns, &s_abort)) break;
+                if (m < NC) {
+                    const uint32_t ms = sbase + Cfg::OFF_MS + (uint32_t)(m % Cfg::MSB) * 2 * Cfg::MS_SLAB;
+                    tma_store_3d(&tm_sm, ms, 0, j0, (int)(x0 + m));
+                    tma_store_3d(&tm_sm, ms + Cfg::MS_SLAB, 64, j0, (int)(x0 + m));
+                }
+                if (m > 0)
+                    tma_store_3d(&tm_sw, sbase + Cfg::OFF_WT + (uint32_t)((m - 1) & 1) * Cfg::WT_BYTES, 0, j0,
+                                 (int)(x0 + m - 1));
+                bulk_commit();
+                bulk_wait_read_all();
+                if (m < NC) {
+                    mbar_arrive(bar(B_QMS));
+                    if (m + 1 < NC) mbar_arrive(bar(B_SAFE0 + ((m + 1) & 1)));
+                }
+            }
+            bulk_wait_all();   // the saved tiles are written before the CTA leaves
+        }
+        __syncwarp();
     } else if (warp == NCH + 1) {
         // ================================================================ output products
         if (lane == 0) {
@@ -558,6 +589,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (a.save) bulk_wait_all();   // the saved tiles are written before the CTA leaves
         }
         __syncwarp();
+    } else if (SO && warp >= NCH + 2) {
+        // no outputs
     } else if (warp >= NCH + 2) {
         // ================================================================ output rows
         // thread r: accumulator row 64 + r (TMEM lane 64 + r) = output row r of a chunk
@@ -605,7 +638,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // [Lb | P] tile by a bulk copy, and the chunk's decay scalars; two arrivals
         // (the expect_tx and the decay) and the bytes complete it.
         uint32_t issued[3] = {0, 0, 0};
-        constexpr uint32_t STAGE_TX = 32768 + DVH * 128 + TILE_BYTES;
+        // without outputs the chain reads K, v and Lb only
+        constexpr uint32_t STAGE_TX = SO ? 16384 + DVH * 128 + TILE_BYTES / 2 : 32768 + DVH * 128 + TILE_BYTES;
         auto issue = [&](int n) {     // lane 0 only
             const int st = n % NST;
             const uint32_t b = bar(B_FULL0 + st);
@@ -613,13 +647,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int row = sv.tz + n * C;
             mbar_arrive_expect_tx(b, STAGE_TX);
             tma_load_3d(kq + Cfg::ST_K, &tm_k, b, 0, row, sv.z);
-            tma_load_3d(kq + Cfg::ST_Q, &tm_q, b, 0, row, sv.z);
+            if (!SO) tma_load_3d(kq + Cfg::ST_Q, &tm_q, b, 0, row, sv.z);
             tma_load_3d(kq + Cfg::ST_K + 16384, &tm_k, b, 64, row, sv.z);
-            tma_load_3d(kq + Cfg::ST_Q + 16384, &tm_q, b, 64, row, sv.z);
+            if (!SO) tma_load_3d(kq + Cfg::ST_Q + 16384, &tm_q, b, 64, row, sv.z);
 #pragma unroll
             for (int vs = 0; vs < DVH / 64; ++vs)
                 tma_load_3d(kq + Cfg::ST_V + vs * 8192, &tm_v, b, j0 + 64 * vs, row, sv.z);
-            bulk_load(kq + Cfg::ST_LP, tiles + (int64_t)n * TILE_BYTES, TILE_BYTES, b);
+            bulk_load(kq + Cfg::ST_LP, tiles + (int64_t)n * TILE_BYTES, SO ? TILE_BYTES / 2 : TILE_BYTES, b);
             ++issued[st];
         };
         // Pull the inputs of chunk n into L2 ahead of their shared-memory loads.
@@ -628,8 +662,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int row = sv.tz + n * C;
             tma_prefetch_3d(&tm_k, 0, row, sv.z);
             tma_prefetch_3d(&tm_k, 64, row, sv.z);
-            tma_prefetch_3d(&tm_q, 0, row, sv.z);
-            tma_prefetch_3d(&tm_q, 64, row, sv.z);
+            if (!SO) {
+                tma_prefetch_3d(&tm_q, 0, row, sv.z);
+                tma_prefetch_3d(&tm_q, 64, row, sv.z);
+            }
 #pragma unroll
             for (int vs = 0; vs < DVH / 64; ++vs) tma_prefetch_3d(&tm_v, j0 + 64 * vs, row, sv.z);
         };
@@ -679,18 +715,18 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == NCH) {
+    if (!SO && warp == NCH) {
         __syncwarp();
         tmem_dealloc(tmem, Cfg::TM_COLS);
     }
 }
 
-template <int DVH>
+template <int DVH, bool SO>
 cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mo, const CUtensorMap &msm, const CUtensorMap &msw,
                            const FusedArgs &a, const void *ws, int64_t nslot, int BH, cudaStream_t s) {
     using Cfg = ChainCfg<DVH>;
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DVH, SO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent of the preparation kernel before it: the CTAs
@@ -706,7 +742,7 @@ cudaError_t launch_chain_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chain_kernel<DVH>, mq, mk, mv, mo, msm, msw, a,
+    return cudaLaunchKernelEx(&cfg, chain_kernel<DVH, SO>, mq, mk, mv, mo, msm, msw, a,
                               static_cast<const uint8_t *>(ws), nslot);
 }
 
@@ -744,7 +780,7 @@ bool make_map_saved(CUtensorMap *m, void *ptr, int inner, int n, int64_t rows, i
 cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
                          int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
-                         int nseg, const float *seg_init, void *saved) {
+                         int nseg, const float *seg_init, void *saved, bool states_only) {
     if (BH == 0 || (cu_seqlens ? total_T : T) == 0) return cudaSuccess;   // callers copy the state
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
          reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(ws)) & 15)
@@ -778,8 +814,11 @@ cudaError_t launch_chain(const void *q, const void *k, const void *v, const floa
             return cudaErrorInvalidValue;
         a.save = 1;
     }
-    return split == 2 ? launch_chain_t<64>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s)
-                      : launch_chain_t<128>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s);
+    if (states_only && saved)   // the states and W tiles only, no outputs
+        return split == 2 ? launch_chain_t<64, true>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s)
+                          : launch_chain_t<128, true>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s);
+    return split == 2 ? launch_chain_t<64, false>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s)
+                      : launch_chain_t<128, false>(mq, mk, mv, mo, msm, msw, a, ws, nslot, views, s);
 }
 
 cudaError_t take_chain_error_word(unsigned *value) { return take_error_word(value); }

@@ -125,11 +125,13 @@ cudaError_t launch_prep(const void *q, const void *k, const float *g, const floa
 // nseg > 1 (dense only): the chain of every segment of every head at once, each
 // from its state in seg_init ([BH][nseg][dk][dv], from launch_segment_states).
 // saved != nullptr (dense only): every chunk's state M_n^T ([BH][NC][128 j][128 i]) and
-// W_n^T ([BH][NC][128 j][64 s]) as value-major bf16 tiles, for gdr_chunk_bwd_saved.
+// W_n^T ([BH][NC][128 j][64 s]) as value-major bf16 tiles, for gdr_chunk_bwd_saved;
+// states_only (with saved): those only, without the output products (out is not written).
 cudaError_t launch_chain(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float a_min, const float *init, void *out, float *final_state, const void *ws,
                          int BH, int T, const int *cu_seqlens, int H, int total_T, cudaStream_t s,
-                         int nseg = 1, const float *seg_init = nullptr, void *saved = nullptr);
+                         int nseg = 1, const float *seg_init = nullptr, void *saved = nullptr,
+                         bool states_only = false);
 // The saved buffer, per (head, chunk) tile x of X = BH ceil(T / 64), in four parts: the
 // states M_x^T (bf16 [128][128]), then W_x^T (bf16 [128][64]), then T_x and P_x (bf16
 // [2][64][64]), then the row scalars (fp32 [4][64]).  Offsets of the parts and the size.
