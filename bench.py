@@ -348,9 +348,9 @@ def prefill_leg_line(gdr, w, ms, pk, pk_kind, world, max_over_ranks):
 
 CSRC = "gated_delta_rule_gdr_gb300/csrc/"
 # the four launches of one backward step on the bf16, d = 128, chunk 64 shape: the training
-# forward into the workspace (its chain keeps the states and W tiles), then the saved-state
-# backward
-BWD_KERNELS = ("backward: chunk_prep_kernel<true> + chain_kernel<64> + bwd_passes_vc_kernel + "
+# forward's kernels into the workspace (its chain, without output products, keeps the states
+# and W tiles), then the saved-state backward
+BWD_KERNELS = ("backward: chunk_prep_kernel<true> + chain_kernel<64> (states only) + bwd_passes_vc_kernel + "
                "bwd_chunk_tc_kernel")
 # one training step: the forward with saves (two-kernel path) and the saved-state backward
 # (the forward's prep kernel also writes T, P and the row scalars, so the backward runs

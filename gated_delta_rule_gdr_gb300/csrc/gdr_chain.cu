@@ -474,8 +474,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
             }
             // while the state update's MMAs run: are chunk n + 1's barriers already
-            // complete (then its start needs no wait)?  Lanes 0 and 1 test one each.
-            {
+            // complete (then its start needs no wait)?  Lanes 0 and 1 test one each.  Only
+            // with four chain warps: with eight (two per SM sub-partition) the tests cost
+            // more issue slots than the waits they save (measured: 2.010 -> 2.091 ms on the
+            // long workload, against 0.1686 -> 0.1645 ms on the prefill with four).
+            if constexpr (DVH == 64) {
                 bool t = n + 1 < NC;
                 if (t && lane == 0)
                     t = mbar_test_wait(bar(B_FULL0 + (n + 1) % NST), (uint32_t)((n + 1) / NST) & 1u);
