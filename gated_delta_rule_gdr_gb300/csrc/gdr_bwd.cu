@@ -1994,7 +1994,8 @@ __device__ __forceinline__ void
 chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
            const CUtensorMap *tm_o, const float *dfinal, const __nv_bfloat16 *__restrict__ TPb,
            float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv,
-           const float *__restrict__ rows, uint64_t limit_ns) {
+           const float *__restrict__ rows, uint64_t limit_ns, uint8_t *stg, const CUtensorMap *tm_dr,
+           const CUtensorMap *tm_ds) {
     using namespace vc;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
@@ -2059,7 +2060,32 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
         const uint32_t st = sb + (uint32_t)s * R_STAGE;
         const float *gs = reinterpret_cast<const float *>(smb + s * R_STAGE + R_G);
         const float *bs = reinterpret_cast<const float *>(smb + s * R_STAGE + R_B);
-        {   // dM' of this chunk, value-major bf16
+        if (stg) {
+            // dM' of this chunk through this warp's staging tile (16 value rows, two
+            // 64-column slabs, 128-byte swizzle) and a tensor store; the staging is free
+            // once the previous chunk's stores have read it
+            if (lane == 0) sm100::bulk_wait_read_all();
+            __syncwarp();
+            const uint32_t ds = sm100::smem_u32(stg) + (uint32_t)warp * 8192u + 4096u;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t jl = (uint32_t)(gq + 8 * h);
+                    const uint32_t addr = ds + (uint32_t)(nt >> 3) * 2048u + jl * 128u +
+                                          ((((uint32_t)nt & 7u) ^ (jl & 7u)) << 4) + (uint32_t)t4 * 4u;
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pack_bf2(dm[nt][2 * h], dm[nt][2 * h + 1]))
+                                 : "memory");
+                }
+            sm100::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int x = bh * NC + n;
+                sm100::tma_store_3d(tm_ds, ds, 0, jw, x);
+                sm100::tma_store_3d(tm_ds, ds + 2048u, 64, jw, x);
+                sm100::bulk_commit();
+            }
+        } else {   // dM' of this chunk, value-major bf16
             __nv_bfloat16 *dst = dSb + ((int64_t)bh * NC + n) * DK * dv;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt)
@@ -2146,14 +2172,32 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
             }
         }
         // dR out; -gamma beta dR as the A operand of the state update
+        if (stg) {   // through this warp's staging tile ([64 rows][16 columns] fp32) and a tensor store
+            const uint32_t dr = sm100::smem_u32(stg) + (uint32_t)warp * 8192u;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
-                if (r < c) dR[(row0 + r) * dv + j] = a2[nt][e];
-                a2[nt][e] *= gb[nt][e & 1];
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t r = (uint32_t)(8 * nt + 2 * t4 + (e & 1)), jl = (uint32_t)(gq + 8 * (e >> 1));
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(dr + r * 64u + jl * 4u), "f"(a2[nt][e]) : "memory");
+                    a2[nt][e] *= gb[nt][e & 1];
+                }
+            sm100::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {   // rows past the sequence's end are clipped
+                sm100::tma_store_3d(tm_dr, dr, jw, n * C, bh);
+                sm100::bulk_commit();
             }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
+                    if (r < c) dR[(row0 + r) * dv + j] = a2[nt][e];
+                    a2[nt][e] *= gb[nt][e & 1];
+                }
+        }
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
@@ -2176,6 +2220,7 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
         sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
         issue(s, n - 2);
     }
+    if (stg && lane == 0) sm100::bulk_wait_all();   // this warp's tensor stores are complete
     if (!ok && tid == 0) {
         // a wait ran out: the latest copies of each stage (its phases complete in order;
         // the other warps' copies of a phase complete it together with thread 0's) land
@@ -2206,7 +2251,8 @@ bwd_passes_vc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const float *init, const float *dfinal, __nv_bfloat16 *__restrict__ Wt,
                      __nv_bfloat16 *__restrict__ Sb, float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb,
                      float *dinit, int T, int dv, int fwd_role, const float *__restrict__ rows,
-                     uint64_t limit_ns) {
+                     uint64_t limit_ns, const __grid_constant__ CUtensorMap tm_dr,
+                     const __grid_constant__ CUtensorMap tm_ds) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (the reverse chain's swizzled tiles), derived from the
     // __shared__ array so that accesses through it stay shared-memory accesses
@@ -2217,7 +2263,9 @@ bwd_passes_vc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (tid < vc::NT) {
         if (fwd_role) fwd_state_pass(smb + 2 * vc::R_STAGE, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
     } else
-        chain_pass(smb, tid - vc::NT, 2, &tm_q, &tm_k, &tm_o, dfinal, TPb, dR, dSb, dinit, T, dv, rows, limit_ns);
+        // without the forward-state role its stages hold the reverse chain's store staging
+        chain_pass(smb, tid - vc::NT, 2, &tm_q, &tm_k, &tm_o, dfinal, TPb, dR, dSb, dinit, T, dv, rows, limit_ns,
+                   fwd_role ? nullptr : smb + 2 * vc::R_STAGE, &tm_dr, &tm_ds);
 }
 
 template <typename K>
@@ -2294,14 +2342,15 @@ cudaError_t launch_bwd_t(const TE *q, const TE *k, const TE *v, const float *g, 
                 if ((err = cudaGetLastError()) != cudaSuccess) return err;
                 rows = Pt;
             }
-            CUtensorMap mq, mk, mo;
-            if (!make_rows_map(&mq, q, BH, T) || !make_rows_map(&mk, k, BH, T) || !make_rows_map(&mo, dout, BH, T))
+            CUtensorMap mq, mk, mo, mdr, mds;
+            if (!make_rows_map(&mq, q, BH, T) || !make_rows_map(&mk, k, BH, T) || !make_rows_map(&mo, dout, BH, T) ||
+                !make_dr_store_map(&mdr, dR, BH, T) || !make_ds_store_map(&mds, dSbb, (int64_t)BH * NC))
                 return cudaErrorInvalidValue;
             const size_t sp = 2 * (size_t)vc::F_STAGE + 2 * (size_t)vc::R_STAGE + 1024;
             if ((err = bwd_set_smem(bwd_passes_vc_kernel, sp)) != cudaSuccess) return err;
             bwd_passes_vc_kernel<<<dim3(dv / vc::DSC, BH), 2 * vc::NT, sp, s>>>(
                 mq, mk, mo, k, gamma, U, Wk2, TPin, init, dfinal, Wtb, Sbb, dR, dSbb, dinit, T, dv,
-                saved ? 0 : 1, rows, opt_wait_limit_ns());
+                saved ? 0 : 1, rows, opt_wait_limit_ns(), mdr, mds);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else {

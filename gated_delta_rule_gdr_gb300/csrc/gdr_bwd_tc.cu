@@ -718,4 +718,30 @@ cudaError_t take_bwd_tc_error_word(unsigned *value) { return take_error_word(val
 
 bool make_rows_map(CUtensorMap *m, const void *ptr, int BH, int T) { return make_map(m, ptr, BH, T); }
 
+// The reverse chain's tensor stores: dR (fp32 [BH][T][128]) in boxes of 16 columns x 64
+// rows, no swizzle, clipped at T; dM' (bf16 [X][128 j][128 i]) in boxes of 64 i x 16 j with
+// the 128-byte swizzle.
+bool make_dr_store_map(CUtensorMap *m, void *ptr, int BH, int T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)T * D * 4};
+    cuuint32_t box[3] = {16, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_ds_store_map(CUtensorMap *m, void *ptr, int64_t X) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)X};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * D * 2};
+    cuuint32_t box[3] = {64, 16, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gdr

@@ -168,6 +168,10 @@ cudaError_t take_prep_error_word(unsigned *value);
 cudaError_t take_bwd_error_word(unsigned *value);
 // TMA map of a bf16 [BH][T][128] tensor: 64 x 64 boxes, 128-byte swizzle, zero fill past T
 bool make_rows_map(CUtensorMap *m, const void *ptr, int BH, int T);
+// Store maps of the backward's reverse chain: dR fp32 [BH][T][128] (16 x 64 boxes) and the
+// per-chunk dM' tiles bf16 [X][128][128] (64 x 16 boxes, 128-byte swizzle)
+bool make_dr_store_map(CUtensorMap *m, void *ptr, int BH, int T);
+bool make_ds_store_map(CUtensorMap *m, void *ptr, int64_t X);
 cudaError_t take_chain_error_word(unsigned *value);
 
 // ---- one decode step of gated multi-head latent attention (gdr_mla.cu) ----
