@@ -1831,6 +1831,20 @@ __device__ __forceinline__ uint32_t bt_sw(uint32_t base, uint32_t slab, int N, i
 
 // Sticky error word of this file's kernels (the reverse chain's bounded waits)
 __device__ unsigned g_bwd_error_word = 0;
+// Bounded wait that also gives up once *abort is raised (by another warp of the CTA);
+// raises it itself (and the error word) when its own limit passes.
+__device__ __noinline__ bool pass_wait_ab(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort) {
+    if (sm100::mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = sm100::global_timer_ns();
+    while (limit_ns > 0) {
+        if (sm100::mbar_try_wait_hint(bar, parity, 20000)) return true;
+        if (*abort) return false;
+        if (sm100::global_timer_ns() - t0 > limit_ns) break;
+    }
+    *abort = 1;
+    atomicOr(&g_bwd_error_word, kDevErrTimeout);
+    return false;
+}
 // Bounded wait of one thread on an mbarrier phase: false (and the error word raised)
 // once limit_ns pass; limit_ns = 0 gives up at once unless the phase is complete.
 __device__ __noinline__ bool pass_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -1995,18 +2009,21 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
            const CUtensorMap *tm_o, const float *dfinal, const __nv_bfloat16 *__restrict__ TPb,
            float *__restrict__ dR, __nv_bfloat16 *__restrict__ dSb, float *dinit, int T, int dv,
            const float *__restrict__ rows, uint64_t limit_ns, uint8_t *stg, const CUtensorMap *tm_dr,
-           const CUtensorMap *tm_ds) {
+           const CUtensorMap *tm_ds, uint64_t *r_bar, volatile int *r_abort) {
     using namespace vc;
     using sm100::ldsm_x4;
     using sm100::ldsm_x4_t;
     using sm100::mma16816;
-    __shared__ __align__(8) uint64_t r_bar[2];
+    // ext: another warp (reverse_loader) fills the stages, and this pass's warps hand
+    // each stage back through its EMPTY barrier instead of meeting at named barriers
+    const bool ext = stg != nullptr;
     const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
     const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t4 = lane & 3;
     const uint32_t sb = sm100::smem_u32(smb);
     const int NC = (T + C - 1) / C;
     const int jw = j0 + 16 * warp;
-    auto bar = [&](int s) { return sm100::smem_u32(&r_bar[s]); };
+    auto bar = [&](int s) { return sm100::smem_u32(&r_bar[s]); };        // FULL of stage s
+    auto ebar = [&](int s) { return sm100::smem_u32(&r_bar[2 + s]); };   // EMPTY of stage s
     int issued[2] = {0, 0};   // thread 0: loads issued per stage
     // Stage s takes chunk n (n < 0: nothing): lane 0 of each warp issues a share of the
     // copies (thread 0 first arms the barrier with all the bytes; a copy that lands
@@ -2041,17 +2058,15 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
             const int i = 8 * nt + 2 * t4 + (e & 1), j = jw + gq + 8 * (e >> 1);
             dm[nt][e] = dfinal ? dfinal[((int64_t)bh * DK + i) * dv + j] : 0.f;
         }
-    if (tid == 0) {
-        sm100::mbar_init(bar(0), 1);
-        sm100::mbar_init(bar(1), 1);
-        sm100::fence_mbar_init();
-        sm100::tma_prefetch_desc(tm_q);
-        sm100::tma_prefetch_desc(tm_k);
-        sm100::tma_prefetch_desc(tm_o);
+    if (!ext) {
+        if (tid == 0) {
+            sm100::tma_prefetch_desc(tm_q);
+            sm100::tma_prefetch_desc(tm_k);
+            sm100::tma_prefetch_desc(tm_o);
+        }
+        issue(0, NC - 1);
+        issue(1, NC - 2);
     }
-    sm100::named_sync(bar_id, NT);   // the barriers are initialised
-    issue(0, NC - 1);
-    issue(1, NC - 2);
     bool ok = true;
     for (int it = 0; it < NC; ++it) {
         const int n = NC - 1 - it, s = it & 1;
@@ -2096,10 +2111,18 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
         }
         // the stage has landed (each warp's lane 0 waits); all warps leave together otherwise
         bool landed = true;
-        if (lane == 0) landed = pass_wait(bar(s), (uint32_t)(it >> 1) & 1u, limit_ns);
-        if (!sm100::named_and(bar_id, NT, landed)) {
-            ok = false;
-            break;
+        if (ext) {   // each warp on its own; a wait that runs out raises the CTA's abort flag
+            if (lane == 0) landed = pass_wait_ab(bar(s), (uint32_t)(it >> 1) & 1u, limit_ns, r_abort);
+            if (!__shfl_sync(0xffffffffu, landed ? 1 : 0, 0)) {
+                ok = false;
+                break;
+            }
+        } else {
+            if (lane == 0) landed = pass_wait(bar(s), (uint32_t)(it >> 1) & 1u, limit_ns);
+            if (!sm100::named_and(bar_id, NT, landed)) {
+                ok = false;
+                break;
+            }
         }
         const float gC = gs[c - 1];
         // dO^T fragments (k = token) and their gamma-scaled copies
@@ -2217,11 +2240,16 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
                 mma16816(dm[2 * np + 1], ar, bk[2], bk[3]);
             }
         }
-        sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
-        issue(s, n - 2);
+        if (ext) {   // this warp is done with the stage
+            __syncwarp();
+            if (lane == 0) sm100::mbar_arrive(ebar(s));
+        } else {
+            sm100::named_sync(bar_id, NT);   // every warp of the pass is done with this stage
+            issue(s, n - 2);
+        }
     }
     if (stg && lane == 0) sm100::bulk_wait_all();   // this warp's tensor stores are complete
-    if (!ok && tid == 0) {
+    if (!ok && !ext && tid == 0) {
         // a wait ran out: the latest copies of each stage (its phases complete in order;
         // the other warps' copies of a phase complete it together with thread 0's) land
         // before the CTA leaves
@@ -2237,6 +2265,50 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
                 dinit[((int64_t)bh * DK + i) * dv + j] = dm[nt][e];
             }
     }
+}
+
+// The reverse chain's loader when the forward-state role is idle (one thread): stage s =
+// it % 2 takes chunk NC - 1 - it once the four chain warps have handed the stage back;
+// the copies as in chain_pass's own issue.  On a timed-out wait (or the chain's abort) it
+// stops; either way it lets its copies in flight land before it leaves.
+__device__ void reverse_loader(uint8_t *smb, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                               const CUtensorMap *tm_o, const __nv_bfloat16 *__restrict__ TPb,
+                               const float *__restrict__ rows, int T, uint64_t limit_ns, uint64_t *r_bar,
+                               volatile int *r_abort) {
+    using namespace vc;
+    const int j0 = blockIdx.x * DSC, bh = blockIdx.y;
+    const int NC = (T + C - 1) / C;
+    const uint32_t sb = sm100::smem_u32(smb);
+    sm100::tma_prefetch_desc(tm_q);
+    sm100::tma_prefetch_desc(tm_k);
+    sm100::tma_prefetch_desc(tm_o);
+    int issued[2] = {0, 0};
+    for (int it = 0; it < NC; ++it) {
+        const int s = it & 1, n = NC - 1 - it;
+        if (it >= 2 && !pass_wait_ab(sm100::smem_u32(&r_bar[2 + s]), (uint32_t)((it - 2) >> 1) & 1u, limit_ns,
+                                     r_abort))
+            break;
+        const uint32_t st = sb + (uint32_t)s * R_STAGE, b = sm100::smem_u32(&r_bar[s]);
+        const __nv_bfloat16 *tp = TPb + ((int64_t)bh * NC + n) * 2 * C * C;
+        const float *blk = rows + ((int64_t)bh * NC + n) * 4 * C;
+        sm100::mbar_arrive_expect_tx(b, R_TX);
+        sm100::tma_load_3d(st + R_K, tm_k, b, 0, n * C, bh);
+        sm100::tma_load_3d(st + R_K + 8192, tm_k, b, 64, n * C, bh);
+        sm100::tma_load_3d(st + R_Q, tm_q, b, 0, n * C, bh);
+        sm100::tma_load_3d(st + R_Q + 8192, tm_q, b, 64, n * C, bh);
+        sm100::tma_load_3d(st + R_O, tm_o, b, j0, n * C, bh);
+        sm100::bulk_load(st + R_T, tp, 8192, b);
+        sm100::bulk_load(st + R_P, tp + C * C, 8192, b);
+        sm100::bulk_load(st + R_G, blk, C * 4, b);
+        sm100::bulk_load(st + R_B, blk + 2 * C, C * 4, b);
+        ++issued[s];
+    }
+    // the latest copies of each stage (its phases complete in order) land before this
+    // thread leaves, so the CTA cannot leave with copies in flight even if the chain warps
+    // left early
+    for (int x = 0; x < 2; ++x)
+        if (issued[x] > 0)
+            sm100::mbar_wait(sm100::smem_u32(&r_bar[x]), (uint32_t)(issued[x] - 1) & 1u, 2000000000ull);
 }
 
 // The two sequential passes in one launch: they are independent (both need only the
@@ -2257,15 +2329,29 @@ bwd_passes_vc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // 1024-byte aligned base (the reverse chain's swizzled tiles), derived from the
     // __shared__ array so that accesses through it stay shared-memory accesses
     uint8_t *smb = smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ __align__(8) uint64_t r_bar[4];   // the reverse chain's FULL (2) and EMPTY (2) barriers
+    __shared__ volatile int r_abort;
     const int tid = threadIdx.x;
-    // fwd_role = 0: the forward saved W^T and the states; only the reverse chain runs (the
-    // two roles share no barrier, so the first four warps simply leave)
+    if (tid == 0) {
+        sm100::mbar_init(sm100::smem_u32(&r_bar[0]), 1);
+        sm100::mbar_init(sm100::smem_u32(&r_bar[1]), 1);
+        sm100::mbar_init(sm100::smem_u32(&r_bar[2]), vc::NW);
+        sm100::mbar_init(sm100::smem_u32(&r_bar[3]), vc::NW);
+        r_abort = 0;
+        sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    // fwd_role = 0: the forward saved W^T and the states; only the reverse chain runs, its
+    // stages filled by the first warp (thread 0) and the store staging in the idle
+    // forward-state stages (the two roles share no barrier, so the other warps leave)
     if (tid < vc::NT) {
-        if (fwd_role) fwd_state_pass(smb + 2 * vc::R_STAGE, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
+        if (fwd_role)
+            fwd_state_pass(smb + 2 * vc::R_STAGE, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
+        else if (tid == 0)
+            reverse_loader(smb, &tm_q, &tm_k, &tm_o, TPb, rows, T, limit_ns, r_bar, &r_abort);
     } else
-        // without the forward-state role its stages hold the reverse chain's store staging
         chain_pass(smb, tid - vc::NT, 2, &tm_q, &tm_k, &tm_o, dfinal, TPb, dR, dSb, dinit, T, dv, rows, limit_ns,
-                   fwd_role ? nullptr : smb + 2 * vc::R_STAGE, &tm_dr, &tm_ds);
+                   fwd_role ? nullptr : smb + 2 * vc::R_STAGE, &tm_dr, &tm_ds, r_bar, &r_abort);
 }
 
 template <typename K>
