@@ -2125,6 +2125,18 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
             }
         }
         const float gC = gs[c - 1];
+        // the row scales of the combine and the state update (this lane's rows r = 8 nt +
+        // 2 t4 + e, e < 2), formed before the products so that their loads and divisions
+        // overlap the MMAs
+        float sc[8][2], gb[8][2];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 8 * nt + 2 * t4 + e;
+                sc[nt][e] = r < c ? __fdividef(gC, gs[r]) : 0.f;
+                gb[nt][e] = -gs[r] * bs[r];
+            }
         // dO^T fragments (k = token) and their gamma-scaled copies
         uint32_t ao[4][4], ag[4][4];
 #pragma unroll
@@ -2164,15 +2176,6 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
                 mma16816(a2[2 * np + 1], a, b[2], b[3]);
             }
         }
-        float sc[8][2], gb[8][2];   // this lane's rows r = 8 nt + 2 t4 + e, e < 2
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int r = 8 * nt + 2 * t4 + e;
-                sc[nt][e] = r < c ? __fdividef(gC, gs[r]) : 0.f;
-                gb[nt][e] = -gs[r] * bs[r];
-            }
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
