@@ -1808,6 +1808,9 @@ constexpr uint32_t R_K = 0, R_Q = 16384, R_P = 32768, R_T = 40960, R_O = 49152, 
                    R_STAGE = 58368;
 constexpr uint32_t R_TX = 2 * 16384 + 3 * 8192 + 2 * C * 4;   // bytes landing per stage
 static_assert(F_STAGE % 16 == 0 && R_STAGE % 1024 == 0 && R_B + C * 4 <= R_STAGE, "stage layout");
+// from saves, the idle forward-state stages hold a third reverse-chain stage and the four
+// warps' store staging (8 KB each)
+static_assert(R_STAGE + NW * 8192 <= 2 * F_STAGE, "third stage and staging");
 }  // namespace vc
 
 // Byte offset of element (row, col) (col a multiple of 8) of a tile of 64-column slabs
@@ -2022,8 +2025,10 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
     const uint32_t sb = sm100::smem_u32(smb);
     const int NC = (T + C - 1) / C;
     const int jw = j0 + 16 * warp;
+    // stages: three with the loader (the third in the idle forward-state area), else two
+    const int NS = ext ? 3 : 2;
     auto bar = [&](int s) { return sm100::smem_u32(&r_bar[s]); };        // FULL of stage s
-    auto ebar = [&](int s) { return sm100::smem_u32(&r_bar[2 + s]); };   // EMPTY of stage s
+    auto ebar = [&](int s) { return sm100::smem_u32(&r_bar[3 + s]); };   // EMPTY of stage s
     int issued[2] = {0, 0};   // thread 0: loads issued per stage
     // Stage s takes chunk n (n < 0: nothing): lane 0 of each warp issues a share of the
     // copies (thread 0 first arms the barrier with all the bytes; a copy that lands
@@ -2069,7 +2074,8 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
     }
     bool ok = true;
     for (int it = 0; it < NC; ++it) {
-        const int n = NC - 1 - it, s = it & 1;
+        const int n = NC - 1 - it, s = it % NS;
+        const uint32_t ph = (uint32_t)(it / NS) & 1u;   // the stage's phase of this chunk
         const int c = min(C, T - n * C);
         const int64_t row0 = (int64_t)bh * T + (int64_t)n * C;
         const uint32_t st = sb + (uint32_t)s * R_STAGE;
@@ -2112,13 +2118,13 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
         // the stage has landed (each warp's lane 0 waits); all warps leave together otherwise
         bool landed = true;
         if (ext) {   // each warp on its own; a wait that runs out raises the CTA's abort flag
-            if (lane == 0) landed = pass_wait_ab(bar(s), (uint32_t)(it >> 1) & 1u, limit_ns, r_abort);
+            if (lane == 0) landed = pass_wait_ab(bar(s), ph, limit_ns, r_abort);
             if (!__shfl_sync(0xffffffffu, landed ? 1 : 0, 0)) {
                 ok = false;
                 break;
             }
         } else {
-            if (lane == 0) landed = pass_wait(bar(s), (uint32_t)(it >> 1) & 1u, limit_ns);
+            if (lane == 0) landed = pass_wait(bar(s), ph, limit_ns);
             if (!sm100::named_and(bar_id, NT, landed)) {
                 ok = false;
                 break;
@@ -2271,7 +2277,7 @@ chain_pass(uint8_t *smb, int tid, uint32_t bar_id, const CUtensorMap *tm_q, cons
 }
 
 // The reverse chain's loader when the forward-state role is idle (one thread): stage s =
-// it % 2 takes chunk NC - 1 - it once the four chain warps have handed the stage back;
+// it % 3 takes chunk NC - 1 - it once the four chain warps have handed the stage back;
 // the copies as in chain_pass's own issue.  On a timed-out wait (or the chain's abort) it
 // stops; either way it lets its copies in flight land before it leaves.
 __device__ void reverse_loader(uint8_t *smb, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
@@ -2285,10 +2291,10 @@ __device__ void reverse_loader(uint8_t *smb, const CUtensorMap *tm_q, const CUte
     sm100::tma_prefetch_desc(tm_q);
     sm100::tma_prefetch_desc(tm_k);
     sm100::tma_prefetch_desc(tm_o);
-    int issued[2] = {0, 0};
+    int issued[3] = {0, 0, 0};
     for (int it = 0; it < NC; ++it) {
-        const int s = it & 1, n = NC - 1 - it;
-        if (it >= 2 && !pass_wait_ab(sm100::smem_u32(&r_bar[2 + s]), (uint32_t)((it - 2) >> 1) & 1u, limit_ns,
+        const int s = it % 3, n = NC - 1 - it;
+        if (it >= 3 && !pass_wait_ab(sm100::smem_u32(&r_bar[3 + s]), (uint32_t)((it - 3) / 3) & 1u, limit_ns,
                                      r_abort))
             break;
         const uint32_t st = sb + (uint32_t)s * R_STAGE, b = sm100::smem_u32(&r_bar[s]);
@@ -2309,7 +2315,7 @@ __device__ void reverse_loader(uint8_t *smb, const CUtensorMap *tm_q, const CUte
     // the latest copies of each stage (its phases complete in order) land before this
     // thread leaves, so the CTA cannot leave with copies in flight even if the chain warps
     // left early
-    for (int x = 0; x < 2; ++x)
+    for (int x = 0; x < 3; ++x)
         if (issued[x] > 0)
             sm100::mbar_wait(sm100::smem_u32(&r_bar[x]), (uint32_t)(issued[x] - 1) & 1u, 2000000000ull);
 }
@@ -2332,21 +2338,22 @@ bwd_passes_vc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // 1024-byte aligned base (the reverse chain's swizzled tiles), derived from the
     // __shared__ array so that accesses through it stay shared-memory accesses
     uint8_t *smb = smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ __align__(8) uint64_t r_bar[4];   // the reverse chain's FULL (2) and EMPTY (2) barriers
+    __shared__ __align__(8) uint64_t r_bar[6];   // the reverse chain's FULL (3) and EMPTY (3) barriers
     __shared__ volatile int r_abort;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        sm100::mbar_init(sm100::smem_u32(&r_bar[0]), 1);
-        sm100::mbar_init(sm100::smem_u32(&r_bar[1]), 1);
-        sm100::mbar_init(sm100::smem_u32(&r_bar[2]), vc::NW);
-        sm100::mbar_init(sm100::smem_u32(&r_bar[3]), vc::NW);
+        for (int x = 0; x < 3; ++x) {
+            sm100::mbar_init(sm100::smem_u32(&r_bar[x]), 1);
+            sm100::mbar_init(sm100::smem_u32(&r_bar[3 + x]), vc::NW);
+        }
         r_abort = 0;
         sm100::fence_mbar_init();
     }
     __syncthreads();
     // fwd_role = 0: the forward saved W^T and the states; only the reverse chain runs, its
-    // stages filled by the first warp (thread 0) and the store staging in the idle
-    // forward-state stages (the two roles share no barrier, so the other warps leave)
+    // stages filled by the first warp (thread 0), a third stage and the store staging in
+    // the idle forward-state stages (the two roles share no barrier, so the other warps
+    // leave)
     if (tid < vc::NT) {
         if (fwd_role)
             fwd_state_pass(smb + 2 * vc::R_STAGE, tid, 1, k, gamma, U, Wk2, init, Wt, Sb, T, dv);
@@ -2354,7 +2361,7 @@ bwd_passes_vc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             reverse_loader(smb, &tm_q, &tm_k, &tm_o, TPb, rows, T, limit_ns, r_bar, &r_abort);
     } else
         chain_pass(smb, tid - vc::NT, 2, &tm_q, &tm_k, &tm_o, dfinal, TPb, dR, dSb, dinit, T, dv, rows, limit_ns,
-                   fwd_role ? nullptr : smb + 2 * vc::R_STAGE, &tm_dr, &tm_ds, r_bar, &r_abort);
+                   fwd_role ? nullptr : smb + 3 * vc::R_STAGE, &tm_dr, &tm_ds, r_bar, &r_abort);
 }
 
 template <typename K>
