@@ -35,6 +35,8 @@
 
 #include "gdr_fused_common.cuh"
 
+#include <algorithm>
+
 namespace gdr {
 namespace {
 
@@ -421,18 +423,43 @@ int segment_count(int BH, int T) {
     if (BH <= 0 || NC <= 0) return 1;
     int S = opt_segments();
     if (S <= 0) {
-        // Automatic: as many segments as keep every pass-1 CTA (2 S - 3 per head) and
-        // every chain CTA (S per head, one each) on an SM of its own, when that is at
-        // least 3 (fewer segments cost more than they save) and every segment keeps
-        // at least 8 chunks.
+        // Automatic: the count (3 or more, every segment keeping at least 8 chunks) that
+        // minimises a wave-quantised cost of the two sequential kernels, each running
+        // ceil(CTAs / SMs) waves of L = ceil(NC / S) dependent chunks plus a fixed ramp of
+        // ~9 chunk times per wave: pass 1 with 2 S - 3 CTAs per head at ~0.65 of a
+        // one-CTA-per-view chain chunk's time, the chain with S views per head at 1 (one
+        // CTA per view) or 0.6 (two); no segments unless that saves 10 % against one
+        // chain per head.  The weights are fitted to measured counts: long prefill B1 H32
+        // T65536 takes 2.05, 2.12, 2.09, 1.95, 2.17, 2.10, 2.19 ms with 3, 4, 6, 8, 10, 12,
+        // 16 segments (this picks 8); million-token B1 H16 15.85, 16.37, 14.87, 18.45,
+        // 18.39, 16.39, 14.32 ms with 6, 8, 9, 10, 12, 16, 19 (this picks 19).
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return 1;
         }
-        S = (sms / BH + 3) / 2;
-        if (S > NC / 8) S = NC / 8;
+        if (sms <= 0) return 1;
+        constexpr double kRamp = 9.0, kPass1 = 0.65, kSplit2 = 0.6;
+        auto waves = [&](int64_t ctas) { return (double)((ctas + sms - 1) / sms); };
+        auto chain = [&](int views, int L) {
+            const int sp = chain_split(views);
+            const double w = waves((int64_t)views * sp);
+            return w * (L * (sp == 2 ? kSplit2 : 1.0) + kRamp);
+        };
+        const double base = chain(BH, NC);
+        const int top = (int)std::min<int64_t>((int64_t)NC / 8, 4LL * sms / BH);
+        double best = 0.9 * base;
+        S = 1;
+        for (int s = 3; s <= top; ++s) {
+            const int L = (NC + s - 1) / s;
+            const double w1 = waves((int64_t)BH * (2 * s - 3));
+            const double c = w1 * (L * kPass1 + kRamp) + chain(BH * s, L);
+            if (c < best) {
+                best = c;
+                S = s;
+            }
+        }
         if (S < 3) return 1;
     }
     if (S > NC) S = NC;

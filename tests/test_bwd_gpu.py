@@ -81,6 +81,16 @@ def test_bwd_bf16_prefill_shape(T):
     check(*run(w), TOL["bf16"])
 
 
+@pytest.mark.parametrize("segments", [3, 4])
+def test_bwd_bf16_default_with_sequence_segments(segments):
+    """The default backward recomputes through the training forward's kernels, which cut
+    few heads' long sequences into segments (forced here on 2 heads of 32 chunks): the
+    saved states then come from the segment chains."""
+    w = I.PREFILL.with_(B=1, H=2, T=2048)
+    with gdr.option(segments=segments):
+        check(*run(w), TOL["bf16"])
+
+
 @pytest.mark.parametrize("init,final", [(False, False), (True, False), (False, True)])
 def test_bwd_bf16_prefill_shape_optional_state_terms(init, final):
     """The tensor-core kernels of the prefill shape without an initial state and / or a
