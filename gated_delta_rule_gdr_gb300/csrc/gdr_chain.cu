@@ -396,7 +396,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             __syncwarp();
 
-            // ---- W^T = X^T + E^T Lb^T: A = E^T (this warp's rows), B = Lb[r][s] rows
+            // ---- W^T = X^T + E^T Lb^T: A = E^T (this warp's rows), B = Lb[r][s] rows.
+            // Lb is strictly lower triangular (exact zeros for s >= r), so the 16 x 16
+            // blocks with s-block ks above r-block rp add nothing and are skipped: 20 of the
+            // 32 products remain.
             float2 sca[8];   // gamma_C / gamma at r = 8p + 2t4 (+1), loaded during the products
             {
                 const uint32_t lb_a = st_a + Cfg::ST_LP;
@@ -405,7 +408,8 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         ldsm_x4(af, smem_u32(wt) + swz((uint32_t)jw + bt_r, (uint32_t)(2 * ks) + bt_c));
 #pragma unroll
                     for (int rp = 0; rp < 4; ++rp)
-                        ldsm_x4(bf[rp], lb_a + swz((uint32_t)(16 * rp) + bn_r, (uint32_t)(2 * ks) + bn_c));
+                        if (rp >= ks)
+                            ldsm_x4(bf[rp], lb_a + swz((uint32_t)(16 * rp) + bn_r, (uint32_t)(2 * ks) + bn_c));
                 };
                 uint32_t aq[2][4], bq[2][4][4];
                 load_l(aq[0], bq[0], 0);
@@ -418,7 +422,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     }
                     const uint32_t (&af)[4] = Cfg::E_REGS ? ea[ks] : aq[ks & 1];
 #pragma unroll
-                    for (int rp = 0; rp < 4; ++rp) {   // r = 16 rp .. 16 rp + 15
+                    for (int rp = ks; rp < 4; ++rp) {   // r = 16 rp .. 16 rp + 15
                         mma16816(x[2 * rp], af, bq[ks & 1][rp][0], bq[ks & 1][rp][1]);
                         mma16816(x[2 * rp + 1], af, bq[ks & 1][rp][2], bq[ks & 1][rp][3]);
                     }

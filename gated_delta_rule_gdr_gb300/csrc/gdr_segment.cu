@@ -228,14 +228,16 @@ seg_pass1_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
             }
 
-            // ---- W^T = X^T + E^T Lb^T: B = Lb[r][s] rows
+            // ---- W^T = X^T + E^T Lb^T: B = Lb[r][s] rows (strictly lower triangular: the
+            // blocks with ks > rp are zero and skipped)
             float2 sca[8];
             {
                 const uint32_t lb_a = st_a + ST_LB;
                 auto load_l = [&](uint32_t (&bf)[4][4], int ks) {
 #pragma unroll
                     for (int rp = 0; rp < 4; ++rp)
-                        ldsm_x4(bf[rp], lb_a + swz((uint32_t)(16 * rp) + bn_r, (uint32_t)(2 * ks) + bn_c));
+                        if (rp >= ks)
+                            ldsm_x4(bf[rp], lb_a + swz((uint32_t)(16 * rp) + bn_r, (uint32_t)(2 * ks) + bn_c));
                 };
                 uint32_t bq[2][4][4];
                 load_l(bq[0], 0);
@@ -247,7 +249,7 @@ seg_pass1_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                         for (int p = 0; p < 8; ++p) sca[p] = *reinterpret_cast<const float2 *>(&S.sc[8 * p + 2 * t4]);
                     }
 #pragma unroll
-                    for (int rp = 0; rp < 4; ++rp) {
+                    for (int rp = ks; rp < 4; ++rp) {
                         mma16816(x[2 * rp], ea[ks], bq[ks & 1][rp][0], bq[ks & 1][rp][1]);
                         mma16816(x[2 * rp + 1], ea[ks], bq[ks & 1][rp][2], bq[ks & 1][rp][3]);
                     }
