@@ -272,7 +272,9 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  * gdr_chunk_fwd_workspace_size: bytes of workspace gdr_chunk_fwd_ws uses for
  *   these arguments, or 0 for empty work or unsupported arguments.  Host-only.
  *   bf16 with dk = dv = 128 and chunk = 64: the two-kernel path (B * H *
- *   ceil(T / 64) tiles of 16 KB).  fp32 and the other shapes: the four staged
+ *   ceil(T / 64) tiles of 16 KB; with S > 1 sequence segments also
+ *   B * H * (3 S - 2) fp32 128 x 128 maps: each segment's offset and
+ *   transition, and its first state).  fp32 and the other shapes: the four staged
  *   kernels (gdr_chunk_decay .. gdr_chunk_output) with their intermediates in
  *   the workspace, 4 * (B*H*T*(1 + dk + 2*dv) + B*H*ceil(T/chunk)*dk*dv) bytes;
  *   their WY/UT and output steps run every chunk in parallel, so they beat the
@@ -283,8 +285,8 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  *   and exit are scratch.  With a null workspace, one that is too small, or
  *   arguments the two-kernel path does not take, the call is exactly
  *   gdr_chunk_fwd (the single-launch fused or staged path, with its chunk
- *   range rule).  Two launches, asynchronous on `stream`; errors as
- *   gdr_chunk_fwd.
+ *   range rule).  Two launches (four with sequence segments), asynchronous on
+ *   `stream`; errors as gdr_chunk_fwd.
  * gdr_chunk_fwd_varlen_workspace_size / gdr_chunk_fwd_varlen_ws: the same for
  *   packed sequences; the workspace holds H * (total_T / 64 + S + 1) tiles
  *   (sequence s starts at tile total offset cu_seqlens[s] / 64 + s of its head);
@@ -293,9 +295,12 @@ int gdr_chunk_fwd_path(int B, int H, int T, int dk, int dv, int chunk, float a_m
  * gdr_chunk_fwd_ws_path: the path gdr_chunk_fwd_ws takes given a large enough
  *   workspace: 1 the staged kernels, 4 two kernels with two CTAs per head in
  *   the chain kernel (value columns split), 5 two kernels with one CTA per
- *   head, else the value of gdr_chunk_fwd_path.  The split is two CTAs per
- *   head while every CTA has an SM of its own; the GDR_OPT_CHAIN_SPLIT option
- *   forces one.  Launches nothing.
+ *   head, 7 the two kernels over sequence segments (few heads, long
+ *   sequences: every segment's state map and offset in parallel, a scan over
+ *   the segments, then the chain over every (head, segment) at once; exact,
+ *   the maps compose), else the value of gdr_chunk_fwd_path.  The split is
+ *   two CTAs per head while every CTA has an SM of its own; the
+ *   GDR_OPT_CHAIN_SPLIT option forces one.  Launches nothing.
  */
 size_t gdr_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
                                     gdr_dtype_t dtype);
@@ -524,7 +529,8 @@ gdr_status_t gdr_mla_decode(const void *q_abs, const void *ckv, const int *seqle
  *   GDR_OPT_CHAIN_SPLIT    CTAs per head in the chain kernel of the two-kernel
  *                          path: 0 chosen by head count (default), 1 or 2.
  *   GDR_OPT_SEGMENTS       sequence segments of the two-kernel path: 0 chosen by
- *                          head count (default), else that many (at most 4096).
+ *                          a cost model of the heads, the sequence length and the
+ *                          SM count (default), else that many (at most 4096).
  *   GDR_OPT_BWD_VARIANT    the bf16 d = 128 chunk-64 backward: 0 default (the
  *                          training forward's kernels recompute the intermediates,
  *                          per-chunk gradients on tensor cores), 1 the backward's own
